@@ -1,0 +1,251 @@
+"""Python binding of the fp64 CPU oracle (``rdot_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg, never by the ``group_gemm_gb300`` package. Arguments are numpy
+arrays (or torch CPU tensors, converted without copying when contiguous); results are float64
+numpy arrays.
+
+Functions and the passages they follow (page titles and sections):
+
+* :func:`offsets` -- "Group-GEMM in XLA", Part 3 "Non-Contracting" (prefix sums).
+* :func:`group_of_row` -- same section, Table 2 (group lookup).
+* :func:`forward` / :func:`forward_rows` -- Part 1 "The Ragged-Dot Operation", Part 3.
+* :func:`grad_weight` / :func:`grad_weight_rows` -- Part 3 "Contracting", Part 4 Table 7.
+* :func:`forward_mxfp8_rows` -- AITER PR #5658 (E4M3 + E8M0 per 32 K elements).
+* :func:`tile_map` -- the library's scheduler order (not on the pages), by brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rdot_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "librdot_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16, F64 = 0, 1, 3
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler (plain C, OpenMP, no fast-math, no FMA
+    contraction so results agree between x86-64 and aarch64 hosts)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-ffp-contract=off", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        vp = ctypes.c_void_p
+        dp = ctypes.POINTER(ctypes.c_double)
+        i64 = ctypes.c_int64
+        lib.orc_offsets.argtypes = [i32p, ctypes.c_int, i64, i64p]
+        lib.orc_offsets.restype = ctypes.c_int
+        lib.orc_group_of_row.argtypes = [i64p, ctypes.c_int, i64]
+        lib.orc_group_of_row.restype = ctypes.c_int
+        lib.orc_forward_rows.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i32p, i64, i64, i64,
+                                         ctypes.c_int, i64p, i64, dp]
+        lib.orc_forward_rows.restype = ctypes.c_int
+        lib.orc_grad_weight_rows.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i32p, i64, i64,
+                                             i64, ctypes.c_int, i32p, i64p, i64, dp]
+        lib.orc_grad_weight_rows.restype = ctypes.c_int
+        lib.orc_forward_mxfp8_rows.argtypes = [vp, vp, vp, vp, i32p, i64, i64, i64, ctypes.c_int,
+                                               i64p, i64, dp]
+        lib.orc_forward_mxfp8_rows.restype = ctypes.c_int
+        lib.orc_tile_map.argtypes = [i32p, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, i32p, i32p, i64]
+        lib.orc_tile_map.restype = ctypes.c_int64
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_decode.restype = ctypes.c_double
+        lib.orc_e8m0_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e8m0_decode.restype = ctypes.c_double
+        lib.orc_set_threads.argtypes = [ctypes.c_int]
+        lib.orc_set_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+# ----------------------------------------------------------------------------------------------
+def _as_np(x):
+    """numpy view of a CPU array/tensor; bf16 tensors become their raw uint16 patterns."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            if x.is_cuda:
+                raise ValueError("oracle inputs must live on the host")
+            if x.dtype == torch.bfloat16:
+                return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy().view(np.uint16)), BF16
+            if x.dtype == torch.float8_e4m3fn:
+                return np.ascontiguousarray(x.contiguous().view(torch.uint8).numpy()), None
+            x = x.contiguous().numpy()
+    except ImportError:
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, F32
+    if x.dtype == np.float64:
+        return x, F64
+    if x.dtype == np.uint16:
+        return x, BF16          # raw bf16 patterns
+    return x, None
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _gs(group_sizes):
+    gs, _ = _as_np(group_sizes)
+    return np.ascontiguousarray(gs, dtype=np.int32)
+
+
+def set_threads(n: int) -> int:
+    """Set the OpenMP thread count (n <= 0 leaves it); returns the count in effect."""
+    return _load().orc_set_threads(int(n))
+
+
+def offsets(group_sizes, m: int):
+    """Returns ``(offsets int64[G+1], flags)``."""
+    gs = _gs(group_sizes)
+    off = np.zeros((gs.size + 1,), dtype=np.int64)
+    flags = _load().orc_offsets(_ptr(gs, ctypes.c_int32), gs.size, int(m), _ptr(off, ctypes.c_int64))
+    return off, flags
+
+
+def group_of_row(group_sizes, m: int, row: int) -> int:
+    off, _ = offsets(group_sizes, m)
+    return _load().orc_group_of_row(_ptr(off, ctypes.c_int64), off.size - 1, int(row))
+
+
+def forward_rows(lhs, rhs, group_sizes, rows):
+    """Rows ``rows`` of the ragged-dot forward, as float64 ``[len(rows), N]``."""
+    a, adt = _as_np(lhs)
+    b, bdt = _as_np(rhs)
+    if adt is None or bdt is None:
+        raise TypeError("lhs/rhs must be f32, f64 or bf16")
+    m, k = a.shape
+    g, k2, n = b.shape
+    if k2 != k:
+        raise ValueError("lhs/rhs contraction sizes differ")
+    gs = _gs(group_sizes)
+    if gs.size != g:
+        raise ValueError("group_sizes length must equal rhs.shape[0]")
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((r.size, n), dtype=np.float64)
+    flags = _load().orc_forward_rows(a.ctypes.data, adt, b.ctypes.data, bdt, _ptr(gs, ctypes.c_int32),
+                                     m, k, n, g, _ptr(r, ctypes.c_int64), r.size,
+                                     _ptr(out, ctypes.c_double))
+    if flags < 0:
+        raise MemoryError("oracle allocation failed")
+    return out
+
+
+def forward(lhs, rhs, group_sizes):
+    """Full ragged-dot forward ``[M, N]`` in float64."""
+    m = _as_np(lhs)[0].shape[0]
+    return forward_rows(lhs, rhs, group_sizes, np.arange(m, dtype=np.int64))
+
+
+def grad_weight_rows(lhs, dy, group_sizes, gsel, asel):
+    """Entries ``dW[gsel[e], asel[e], :]`` of the weight gradient, float64 ``[len, N]``."""
+    a, adt = _as_np(lhs)
+    d, ddt = _as_np(dy)
+    if adt is None or ddt is None:
+        raise TypeError("lhs/dy must be f32, f64 or bf16")
+    m, k = a.shape
+    m2, n = d.shape
+    if m2 != m:
+        raise ValueError("lhs/dy row counts differ")
+    gs = _gs(group_sizes)
+    gsel = np.ascontiguousarray(gsel, dtype=np.int32)
+    asel = np.ascontiguousarray(asel, dtype=np.int64)
+    out = np.empty((gsel.size, n), dtype=np.float64)
+    flags = _load().orc_grad_weight_rows(a.ctypes.data, adt, d.ctypes.data, ddt,
+                                         _ptr(gs, ctypes.c_int32), m, k, n, gs.size,
+                                         _ptr(gsel, ctypes.c_int32), _ptr(asel, ctypes.c_int64),
+                                         gsel.size, _ptr(out, ctypes.c_double))
+    if flags < 0:
+        raise MemoryError("oracle allocation failed")
+    return out
+
+
+def grad_weight(lhs, dy, group_sizes):
+    """Full weight gradient ``dW [G, K, N]`` in float64."""
+    k = _as_np(lhs)[0].shape[1]
+    n = _as_np(dy)[0].shape[1]
+    g = _gs(group_sizes).size
+    gsel = np.repeat(np.arange(g, dtype=np.int32), k)
+    asel = np.tile(np.arange(k, dtype=np.int64), g)
+    return grad_weight_rows(lhs, dy, group_sizes, gsel, asel).reshape(g, k, n)
+
+
+def forward_mxfp8_rows(lhs_q, lhs_s, rhs_q, rhs_s, group_sizes, rows):
+    """Rows of the MXFP8 forward (codes and scales as uint8 arrays), float64 ``[len, N]``."""
+    aq = np.ascontiguousarray(_as_np(lhs_q)[0]).view(np.uint8)
+    as_ = np.ascontiguousarray(_as_np(lhs_s)[0]).view(np.uint8)
+    bq = np.ascontiguousarray(_as_np(rhs_q)[0]).view(np.uint8)
+    bs = np.ascontiguousarray(_as_np(rhs_s)[0]).view(np.uint8)
+    m, k = aq.shape
+    g, k2, n = bq.shape
+    if k2 != k or k % 32:
+        raise ValueError("bad MXFP8 shapes")
+    if as_.shape != (m, k // 32) or bs.shape != (g, k // 32, n):
+        raise ValueError("bad MXFP8 scale shapes")
+    gs = _gs(group_sizes)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((r.size, n), dtype=np.float64)
+    flags = _load().orc_forward_mxfp8_rows(aq.ctypes.data, as_.ctypes.data, bq.ctypes.data,
+                                           bs.ctypes.data, _ptr(gs, ctypes.c_int32), m, k, n,
+                                           g, _ptr(r, ctypes.c_int64), r.size,
+                                           _ptr(out, ctypes.c_double))
+    if flags < 0:
+        raise MemoryError("oracle allocation failed")
+    return out
+
+
+def forward_mxfp8(lhs_q, lhs_s, rhs_q, rhs_s, group_sizes):
+    m = np.asarray(_as_np(lhs_q)[0]).shape[0]
+    return forward_mxfp8_rows(lhs_q, lhs_s, rhs_q, rhs_s, group_sizes, np.arange(m))
+
+
+def e4m3_decode(code: int) -> float:
+    return _load().orc_e4m3_decode(int(code))
+
+
+def e8m0_decode(code: int) -> float:
+    return _load().orc_e8m0_decode(int(code))
+
+
+def tile_map(group_sizes, m: int, n: int, bm: int, bn: int, m_inner: bool):
+    """Returns ``(tile_prefix int32[G+1], tiles int32[W, 3])`` of (group, row tile, col tile)."""
+    gs = _gs(group_sizes)
+    lib = _load()
+    pref = np.zeros((gs.size + 1,), dtype=np.int32)
+    total = lib.orc_tile_map(_ptr(gs, ctypes.c_int32), gs.size, int(m), int(n), int(bm), int(bn),
+                             int(bool(m_inner)), _ptr(pref, ctypes.c_int32),
+                             _ptr(np.zeros((1, 3), np.int32), ctypes.c_int32), 0)
+    tiles = np.zeros((max(total, 1), 3), dtype=np.int32)
+    lib.orc_tile_map(_ptr(gs, ctypes.c_int32), gs.size, int(m), int(n), int(bm), int(bn),
+                     int(bool(m_inner)), _ptr(pref, ctypes.c_int32), _ptr(tiles, ctypes.c_int32),
+                     total)
+    return pref, tiles[:total]

@@ -1,0 +1,332 @@
+"""Pins of the fp64 CPU oracle against things other than itself (no GPU needed).
+
+* the pages' worked example and Table 2 (golden fixtures, cited in the files);
+* brute force against per-expert numpy matmuls (a library routine);
+* invariants: padded batched matmul restricted to valid rows, G = 1 is a plain GEMM,
+  zero-size groups and trailing rows, linearity, expert permutation;
+* weight gradient: per-group ``lhs_g^T dy_g``, the sum over groups, empty groups;
+* MXFP8: the E4M3 decoder against torch's float8_e4m3fn on all 256 codes, E8M0 special
+  values, the scale-hoist identity, all-unit scales, power-of-two scale shifts;
+* tile map: closed form of the prefix, brute-force decode, the static tile-count bound.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rdot_inputs as ri
+from tests import _golden
+
+TOL = 1e-12
+
+
+def _rel(a, b):
+    return float(np.max(np.abs(np.asarray(a) - np.asarray(b)) / (np.abs(np.asarray(b)) + 1.0))) if np.size(b) else 0.0
+
+
+def _np_forward(lhs, rhs, gs):
+    """Independent route: per-expert numpy matmul on row slices, rows past the sum are zero."""
+    m = lhs.shape[0]
+    out = np.zeros((m, rhs.shape[2]))
+    start = 0
+    for g, s in enumerate(gs):
+        out[start:start + s] = lhs[start:start + s].astype(np.float64) @ rhs[g].astype(np.float64)
+        start += s
+    return out
+
+
+# ------------------------------------------------------------------------------------ golden
+def test_worked_example():
+    d = _golden.read("worked_example.txt")
+    gs = d["group_sizes"].astype(np.int32)
+    out = oracle.forward(d["lhs"], d["rhs"], gs)
+    assert out.shape == d["out"].shape
+    assert np.max(np.abs(out - d["out"])) < 1e-14
+
+
+def test_table2_group_lookup():
+    d = _golden.read("table2_group_lookup.txt")
+    gs = d["group_sizes"].astype(np.int32)
+    m = int(gs.sum())
+    off, flags = oracle.offsets(gs, m)
+    assert flags == 0
+    assert list(off[:-1]) == list(d["prefix_exclusive"].astype(int))
+    assert list(off[1:]) == list(d["prefix_inclusive"].astype(int))
+    bm = int(d["block_m"][0])
+    for pid_m, row_start, g, start in d["lookup"].astype(int):
+        assert row_start == pid_m * bm
+        assert oracle.group_of_row(gs, m, row_start) == g
+        assert off[g] == start
+
+
+def test_balanced_seeding_generators():
+    for m, g, conv, *sizes in _golden.read("balanced_seeding.txt")["_rows"]:
+        got = ri.balanced_group_sizes(int(m), int(g), conv)
+        assert list(got) == [int(s) for s in sizes]
+        assert int(got.sum()) == int(m)
+
+
+# ------------------------------------------------------------------------------- brute force
+@pytest.mark.parametrize("seed", range(6))
+def test_forward_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    g = int(rng.integers(1, 7))
+    k = int(rng.integers(1, 9))
+    n = int(rng.integers(1, 7))
+    gs = rng.integers(0, 5, size=g).astype(np.int32)
+    if seed % 2:
+        gs[rng.integers(0, g)] = 0
+    m = int(gs.sum()) + int(rng.integers(0, 4))      # sometimes rows past the sum
+    lhs = rng.standard_normal((m, k))
+    rhs = rng.standard_normal((g, k, n))
+    assert _rel(oracle.forward(lhs, rhs, gs), _np_forward(lhs, rhs, gs)) < TOL
+
+
+def test_forward_rows_subset_matches_full():
+    rng = np.random.default_rng(7)
+    gs = np.array([5, 0, 3, 9], np.int32)
+    lhs = rng.standard_normal((20, 6))
+    rhs = rng.standard_normal((4, 6, 5))
+    full = oracle.forward(lhs, rhs, gs)
+    rows = np.array([19, 0, 4, 5, 16, 17, 8])
+    assert np.array_equal(oracle.forward_rows(lhs, rhs, gs, rows), full[rows])
+
+
+def test_forward_f32_and_bf16_inputs_are_decoded_exactly():
+    rng = np.random.default_rng(3)
+    gs = np.array([2, 3], np.int32)
+    lhs32 = rng.standard_normal((6, 8)).astype(np.float32)
+    rhs32 = rng.standard_normal((2, 8, 4)).astype(np.float32)
+    ref = _np_forward(lhs32.astype(np.float64), rhs32.astype(np.float64), gs)
+    assert _rel(oracle.forward(lhs32, rhs32, gs), ref) < TOL
+    lb = torch.from_numpy(lhs32).to(torch.bfloat16)
+    rb = torch.from_numpy(rhs32).to(torch.bfloat16)
+    refb = _np_forward(lb.double().numpy(), rb.double().numpy(), gs)
+    assert _rel(oracle.forward(lb, rb, gs), refb) < TOL
+
+
+# -------------------------------------------------------------------------------- invariants
+def test_equals_padded_batched_matmul_on_valid_rows():
+    # the padded-dot baseline: pad each group to capacity C, run E x [C,k] x [k,n]
+    # ("Group-GEMM in XLA", Part 1 "The Naive Support, and Why It Hurts: Padded-Dot")
+    rng = np.random.default_rng(11)
+    gs = np.array([4, 0, 7, 2, 5], np.int32)
+    m, k, n = int(gs.sum()) + 3, 9, 6
+    lhs = rng.standard_normal((m, k))
+    rhs = rng.standard_normal((5, k, n))
+    cap = int(gs.max())
+    pad = np.zeros((5, cap, k))
+    start = 0
+    for g, s in enumerate(gs):
+        pad[g, :s] = lhs[start:start + s]
+        start += s
+    outp = np.einsum("gck,gkn->gcn", pad, rhs)
+    out = oracle.forward(lhs, rhs, gs)
+    start = 0
+    for g, s in enumerate(gs):
+        assert _rel(out[start:start + s], outp[g, :s]) < TOL
+        start += s
+    assert np.all(out[start:] == 0.0)
+
+
+def test_single_group_is_plain_gemm():
+    rng = np.random.default_rng(12)
+    lhs = rng.standard_normal((13, 10))
+    rhs = rng.standard_normal((1, 10, 7))
+    out = oracle.forward(lhs, rhs, np.array([13], np.int32))
+    assert _rel(out, lhs @ rhs[0]) < TOL
+
+
+def test_zero_groups_contribute_nothing_and_tail_is_zero():
+    rng = np.random.default_rng(13)
+    k, n = 5, 4
+    gs = np.array([0, 3, 0, 0, 2, 0], np.int32)
+    lhs = rng.standard_normal((8, k))
+    lhs[5:] = np.nan                       # rows past the sum are never read
+    rhs = rng.standard_normal((6, k, n))
+    rhs[[0, 2, 3, 5]] = np.nan             # weights of empty groups are never read
+    out = oracle.forward(lhs, rhs, gs)
+    ref = oracle.forward(lhs[:5], rhs[[1, 4]], np.array([3, 2], np.int32))
+    assert np.array_equal(out[:5], ref)
+    assert np.all(out[5:] == 0.0)
+
+
+def test_linearity_in_lhs():
+    rng = np.random.default_rng(14)
+    gs = np.array([3, 4, 1], np.int32)
+    x = rng.standard_normal((9, 6))
+    y = rng.standard_normal((9, 6))
+    rhs = rng.standard_normal((3, 6, 5))
+    lhs = oracle.forward(2.5 * x - 0.75 * y, rhs, gs)
+    rhs_side = 2.5 * oracle.forward(x, rhs, gs) - 0.75 * oracle.forward(y, rhs, gs)
+    assert _rel(lhs, rhs_side) < 1e-12
+
+
+def test_expert_permutation_permutes_row_blocks():
+    rng = np.random.default_rng(15)
+    gs = np.array([2, 5, 3, 1], np.int32)
+    k, n = 7, 3
+    lhs = rng.standard_normal((11, k))
+    rhs = rng.standard_normal((4, k, n))
+    perm = np.array([2, 0, 3, 1])
+    starts = np.concatenate([[0], np.cumsum(gs)])
+    lhs_p = np.concatenate([lhs[starts[p]:starts[p + 1]] for p in perm])
+    out = oracle.forward(lhs, rhs, gs)
+    out_p = oracle.forward(lhs_p, rhs[perm], gs[perm])
+    ref_p = np.concatenate([out[starts[p]:starts[p + 1]] for p in perm])
+    assert np.array_equal(out_p, ref_p)
+
+
+def test_group_size_clamping_reading():
+    # negative sizes count as 0, the running end is clamped to M, and the flag is raised
+    off, flags = oracle.offsets(np.array([3, -2, 4, 10], np.int32), 9)
+    assert list(off) == [0, 3, 3, 7, 9] and flags == 1
+    off, flags = oracle.offsets(np.array([3, 2, 4], np.int32), 9)
+    assert list(off) == [0, 3, 5, 9] and flags == 0
+    rng = np.random.default_rng(16)
+    lhs = rng.standard_normal((9, 4))
+    rhs = rng.standard_normal((4, 4, 2))
+    gs = np.array([3, -2, 4, 10], np.int32)
+    ref = _np_forward(lhs, rhs, np.array([3, 0, 4, 2]))
+    assert _rel(oracle.forward(lhs, rhs, gs), ref) < TOL
+
+
+# ---------------------------------------------------------------------------- weight gradient
+def test_grad_weight_brute_force_and_sum_invariant():
+    rng = np.random.default_rng(21)
+    gs = np.array([4, 0, 6, 1, 3], np.int32)
+    m, k, n = int(gs.sum()) + 2, 7, 5
+    lhs = rng.standard_normal((m, k))
+    dy = rng.standard_normal((m, n))
+    lhs[-2:] = np.nan                     # rows past the sum are ignored
+    dy[-2:] = np.nan
+    dw = oracle.grad_weight(lhs, dy, gs)
+    start = 0
+    for g, s in enumerate(gs):
+        ref = lhs[start:start + s].T @ dy[start:start + s]
+        if s == 0:
+            assert np.all(dw[g] == 0.0)
+        assert _rel(dw[g], ref) < TOL
+        start += s
+    total = lhs[:start].T @ dy[:start]
+    assert _rel(dw.sum(axis=0), total) < 1e-11
+
+
+def test_grad_weight_entries_match_full():
+    rng = np.random.default_rng(22)
+    gs = np.array([3, 5], np.int32)
+    lhs = rng.standard_normal((8, 4))
+    dy = rng.standard_normal((8, 6))
+    full = oracle.grad_weight(lhs, dy, gs)
+    gsel = np.array([1, 0, 1])
+    asel = np.array([3, 0, 1])
+    assert np.array_equal(oracle.grad_weight_rows(lhs, dy, gs, gsel, asel), full[gsel, asel])
+
+
+# ------------------------------------------------------------------------------------- MXFP8
+def test_e4m3_decoder_matches_torch_on_all_codes():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        got = oracle.e4m3_decode(c)
+        if math.isnan(ref[c]):
+            assert math.isnan(got), c
+        else:
+            assert got == ref[c], (c, got, ref[c])
+    # format facts: largest normal 448, smallest subnormal 2^-9
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_e8m0_special_values():
+    assert oracle.e8m0_decode(127) == 1.0
+    assert oracle.e8m0_decode(128) == 2.0
+    assert oracle.e8m0_decode(126) == 0.5
+    assert oracle.e8m0_decode(0) == 2.0 ** -127
+    assert oracle.e8m0_decode(254) == 2.0 ** 127
+    assert math.isnan(oracle.e8m0_decode(255))
+
+
+def _mx_case(seed, m=12, k=96, n=10, g=3, gs=(5, 0, 6)):
+    x = torch.from_numpy(ri.host_normal((m, k), seed))
+    w = torch.from_numpy(ri.host_normal((g, k, n), seed + 1, 0.02))
+    aq, as_ = ri.quantize_mx_e4m3(x, axis=1)
+    bq, bs = ri.quantize_mx_e4m3(w, axis=1)
+    return aq, as_, bq, bs, np.array(gs, np.int32)
+
+
+def _dequant_torch(q, s, axis):
+    v = q.view(torch.float8_e4m3fn).to(torch.float64)
+    sc = torch.pow(2.0, s.to(torch.float64) - 127.0).repeat_interleave(32, dim=axis)
+    return (v * sc).numpy()
+
+
+def test_mxfp8_brute_force_against_torch_dequant():
+    aq, as_, bq, bs, gs = _mx_case(31)
+    # make the scales vary along every axis so a transposed or misbroadcast scale fails
+    as_ = (as_.to(torch.int32) + torch.randint(-3, 4, as_.shape, generator=torch.Generator().manual_seed(1))).clamp(1, 254).to(torch.uint8)
+    bs = (bs.to(torch.int32) + torch.randint(-3, 4, bs.shape, generator=torch.Generator().manual_seed(2))).clamp(1, 254).to(torch.uint8)
+    a = _dequant_torch(aq, as_, 1)
+    b = _dequant_torch(bq, bs, 1)
+    ref = _np_forward(a, b, gs)
+    got = oracle.forward_mxfp8(aq, as_, bq, bs, gs)
+    assert _rel(got, ref) < TOL
+
+
+def test_mxfp8_scale_hoist_identity():
+    # with one scale per operand per 32-wide K step, scaling the partial product of each step
+    # equals scaling the operands (AITER follow-up #5832)
+    aq, as_, bq, bs, gs = _mx_case(41)
+    va = aq.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    vb = bq.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    sa = np.power(2.0, as_.numpy().astype(np.float64) - 127)
+    sb = np.power(2.0, bs.numpy().astype(np.float64) - 127)
+    m, k = va.shape
+    ref = np.zeros((m, vb.shape[2]))
+    start = 0
+    for g, s in enumerate(gs):
+        for kb in range(k // 32):
+            sl = slice(32 * kb, 32 * kb + 32)
+            part = va[start:start + s, sl] @ vb[g, sl, :]
+            ref[start:start + s] += part * sa[start:start + s, kb:kb + 1] * sb[g, kb:kb + 1, :]
+        start += s
+    assert _rel(oracle.forward_mxfp8(aq, as_, bq, bs, gs), ref) < TOL
+
+
+def test_mxfp8_unit_scales_and_power_of_two_shift():
+    aq, as_, bq, bs, gs = _mx_case(51)
+    ones_a = torch.full_like(as_, 127)
+    ones_b = torch.full_like(bs, 127)
+    va = aq.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    vb = bq.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    base = oracle.forward_mxfp8(aq, ones_a, bq, ones_b, gs)
+    assert _rel(base, _np_forward(va, vb, gs)) < TOL
+    shifted = oracle.forward_mxfp8(aq, torch.full_like(as_, 130), bq, ones_b, gs)
+    assert np.array_equal(shifted, base * 8.0)
+
+
+# ------------------------------------------------------------------------------------ tile map
+@pytest.mark.parametrize("m_inner", [True, False])
+def test_tile_map_closed_form_and_decode(m_inner):
+    rng = np.random.default_rng(61)
+    gs = rng.integers(0, 300, size=9).astype(np.int32)
+    gs[[2, 5]] = 0
+    m, n, bm, bn = int(gs.sum()) + 17, 700, 128, 256
+    pref, tiles = oracle.tile_map(gs, m, n, bm, bn, m_inner)
+    nt = -(-n // bn)
+    mt = -(-gs.astype(np.int64) // bm)
+    assert list(pref) == list(np.concatenate([[0], np.cumsum(mt * nt)]))
+    # decode rule: w -> (g, local) with g the largest group with pref[g] <= w and tiles
+    for w, (g, r, c) in enumerate(tiles):
+        gg = int(np.searchsorted(pref, w, side="right") - 1)
+        while mt[gg] == 0:
+            gg -= 1
+        assert gg == g
+        loc = w - pref[g]
+        if m_inner:
+            assert (r, c) == (loc % mt[g], loc // mt[g])
+        else:
+            assert (r, c) == (loc // nt, loc % nt)
+    # static bound: sum ceil(m_g / bm) <= ceil(M / bm) + G
+    assert mt.sum() <= -(-m // bm) + gs.size
