@@ -1,0 +1,432 @@
+"""Benchmark of the ragged-dot hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one ragged-dot forward over one batch of the workload (default: the Mixtral-like bf16
+forward, 16384 rows x K=4096 x N=14336, G=8). Inputs are seeded synthetic data resident in HBM;
+the timed region covers exactly K steps bracketed by a barrier and a device synchronisation,
+timed with CUDA events on the launching stream. The JSON line reports useful TFLOP/s
+(F_useful = 2 * sum(group_sizes) * K * N, the padded-work model's useful FLOPs in "How to Scale
+Your Model on AMD", ch. 6 "Grouped GEMM kernels for MoE"), its fraction of the measured dense
+bf16 peak, the roofline of the dominant kernel, an end-to-end number through the public API
+with host buffers, the oracle timed on the host cores, and the other workloads of the suite.
+
+Multi-GPU: one process per GPU (torchrun); the path shards by independent problems, so every
+rank runs its own replica with no collective in the data path ("scaling": "weak").
+
+``--impl reference`` times the fp64 CPU oracle instead (the reference arm of this suite) on the
+host cores, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import rdot_inputs as ri  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+
+
+# ----------------------------------------------------------------------------------- helpers
+def useful_flops(gs, k, n) -> float:
+    return 2.0 * float(np.sum(np.maximum(gs, 0))) * k * n
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+FWD_TC_SOURCES = ["group_gemm_gb300/csrc/fwd_tc.cu", "group_gemm_gb300/csrc/ptx.cuh",
+                  "group_gemm_gb300/csrc/sched.cuh"]
+
+
+def ncu_traffic(kernel: str, workload: str, sources):
+    """Per-launch DRAM bytes from the committed ncu summary, or None when absent or when the
+    kernel's sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}:{workload}")
+    if not e or e.get("source_hash") != kernel_source_hash(sources):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0:   # wait for the first sample
+            time.sleep(0.01)
+        self.lines.clear()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in list(self.lines):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ workloads
+def make_forward_inputs(name, device, seed=0):
+    import torch
+    cfg = ri.CONFIGS[name]
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    gs = ri.config_group_sizes(name, seed)
+    dt = torch.bfloat16 if cfg["in_dtype"] == "bf16" else torch.float32
+    lhs = ri.device_normal((m, k), 1000 + seed, cfg["lhs"][1], device, dt)
+    rhs = ri.device_normal((g, k, n), 2000 + seed, cfg["rhs"][1], device, dt)
+    return cfg, gs, lhs, rhs
+
+
+def time_region(fn, steps, stream, barrier):
+    import torch
+    barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end) / 1e3   # seconds
+
+
+def cpu_oracle_sample(name, gs, lhs_host, rhs_host, budget_s, batch=16):
+    """Times the fp64 oracle on successive batches of rows until ~budget_s seconds; returns
+    (useful FLOP/s, cores, description)."""
+    import oracle
+    cfg = ri.CONFIGS[name]
+    k, n = cfg["k"], cfg["n"]
+    oracle.build()
+    cores = oracle.set_threads(0)
+    off = np.concatenate([[0], np.cumsum(gs)])
+    valid = np.arange(int(off[-1]))
+    rng = np.random.default_rng(7)
+    order = rng.permutation(valid)
+    done, t_total, i = 0, 0.0, 0
+    while t_total < budget_s and i < order.size:
+        rows = np.sort(order[i:i + batch])
+        i += batch
+        t0 = time.perf_counter()
+        oracle.forward_rows(lhs_host, rhs_host, gs, rows)
+        t_total += time.perf_counter() - t0
+        done += rows.size
+    flops = 2.0 * done * k * n
+    return flops / t_total, cores, f"{done} random valid rows of {name} (x full N), fp64, {t_total:.1f} s"
+
+
+# ---------------------------------------------------------------------------- our arm
+def bench_ours(args, rank, world, barrier):
+    import torch
+    import group_gemm_gb300 as gg
+
+    gg.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    name = args.workload
+    cfg, gs, lhs, rhs = make_forward_inputs(name, dev)
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    flops = useful_flops(gs, k, n)
+    plan = gg.Plan(m, k, n, g, "forward", cfg["in_dtype"], cfg["out_dtype"], device=dev.index)
+    gs_d = torch.from_numpy(gs).to(dev)
+    out_dt = torch.bfloat16 if cfg["out_dtype"] == "bf16" else torch.float32
+    out = torch.empty((m, n), dtype=out_dt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    t = time_region(step, args.steps, stream, barrier)
+    clk = clocks.stop()
+    status = plan.status()
+    if status:
+        raise RuntimeError(f"device status bits {status:#x} after the timed region")
+    t_max = t
+    if world > 1:
+        tt = torch.tensor([t], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(tt.item())
+    per_step = t_max / args.steps
+    value = flops * world / per_step / 1e12
+    launch_s = t / args.steps
+    achieved = flops / launch_s / 1e12
+
+    # end to end through the public API: pinned host lhs + group_sizes in, output back to host
+    lhs_h = torch.empty(lhs.shape, dtype=lhs.dtype, pin_memory=True)
+    lhs_h.copy_(lhs)
+    gs_h = torch.from_numpy(gs.copy()).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    lhs_d2 = torch.empty_like(lhs)
+    gs_d2 = torch.empty_like(gs_d)
+
+    def e2e_step():
+        lhs_d2.copy_(lhs_h, non_blocking=True)
+        gs_d2.copy_(gs_h, non_blocking=True)
+        gg.rdot_forward(plan.handle, lhs_d2, rhs, gs_d2, out, plan.workspace, stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 50))
+    t_e2e = time_region(e2e_step, e2e_steps, stream, barrier)
+    if world > 1:
+        tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    e2e = {"value": round(flops * world / (t_e2e / e2e_steps) / 1e12, 3), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": int(lhs.numel() * lhs.element_size() + gs_d.numel() * 4),
+           "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+           "note": "weights resident; activations and group_sizes copied in, output copied out each step"}
+    result = {
+        "metric": "ragged-dot useful TFLOP/s (fraction of GB300 dense bf16 peak; speedup vs padded in per_config)",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg["in_dtype"], "data": "synthetic (seeded)",
+        "config": {"workload": f"{name}: M={m} K={k} N={n} G={g}, {cfg['in_dtype']} in / {cfg['out_dtype']} out",
+                   "group_sizes": f"sum={int(gs.sum())} min={int(gs.min())} max={int(gs.max())}",
+                   "l2": "inputs larger than L2 (no flush)" if (lhs.numel() * lhs.element_size() + rhs.numel()
+                                                               * rhs.element_size()) > L2_BYTES else "warm L2",
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": ncu_traffic("fwd_tc", name, FWD_TC_SOURCES),
+                     "kernel": "fwd_tc_kernel", "peak_kind": f"{peaks['source']} bf16 burst"},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "device_status": status,
+    }
+    del lhs, rhs, out, lhs_h, out_h, lhs_d2
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_extras:
+        result["per_config"] = extra_configs(args, dev, peaks, name)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_leg(name, args.cpu_seconds)
+    return result
+
+
+def extra_configs(args, dev, peaks, main_name):
+    """The other bf16 forward workloads, measured the same way with fewer steps."""
+    import torch
+    import group_gemm_gb300 as gg
+    res = {}
+    for name in ("mixtral_bf16", "deepseek_bf16"):
+        if name == main_name:
+            continue
+        cfg, gs, lhs, rhs = make_forward_inputs(name, dev)
+        m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+        plan = gg.Plan(m, k, n, g, "forward", cfg["in_dtype"], cfg["out_dtype"], device=dev.index)
+        gs_d = torch.from_numpy(gs).to(dev)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        stream = torch.cuda.current_stream(dev)
+
+        def step():
+            gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream)
+
+        for _ in range(3):
+            step()
+        steps = max(5, min(args.steps, 30))
+        t = time_region(step, steps, stream, lambda: None) / steps
+        fl = useful_flops(gs, k, n)
+        nz = int(np.count_nonzero(gs))
+        min_bytes = (nz * k * n + int(gs.sum()) * k + m * n) * 2
+        res[name] = {"tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
+                     "frac_of_bf16_peak": round(fl / t / 1e12 / peaks["bf16_tflops"], 4),
+                     "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1),
+                     "frac_of_hbm": round(min_bytes / t / 1e9 / peaks["hbm_gbs"], 4),
+                     "status": plan.status()}
+        del lhs, rhs, out
+        torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline_leg(name, seconds):
+    import torch
+    cfg = ri.CONFIGS[name]
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    if dev is not None:
+        _, gs, lhs, rhs = make_forward_inputs(name, dev)
+        lhs_h, rhs_h = lhs.cpu(), rhs.cpu()
+        del lhs, rhs
+        torch.cuda.empty_cache()
+    else:
+        gs = ri.config_group_sizes(name)
+        lhs_h = torch.from_numpy(ri.host_normal((cfg["m"], cfg["k"]), 1000, cfg["lhs"][1])).to(torch.bfloat16)
+        rhs_h = torch.from_numpy(ri.host_normal((cfg["g"], cfg["k"], cfg["n"]), 2000, cfg["rhs"][1])).to(torch.bfloat16)
+    v, cores, sample = cpu_oracle_sample(name, gs, lhs_h, rhs_h, seconds)
+    return {"value": round(v / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+
+# ------------------------------------------------------------------------- reference arm
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import torch
+    name = args.workload
+    cfg = ri.CONFIGS[name]
+    k, n = cfg["k"], cfg["n"]
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    if dev is not None:
+        _, gs, lhs, rhs = make_forward_inputs(name, dev)
+        lhs_h, rhs_h = lhs.cpu(), rhs.cpu()
+        del lhs, rhs
+        torch.cuda.empty_cache()
+    else:
+        gs = ri.config_group_sizes(name)
+        lhs_h = torch.from_numpy(ri.host_normal((cfg["m"], cfg["k"]), 1000, cfg["lhs"][1])).to(torch.bfloat16)
+        rhs_h = torch.from_numpy(ri.host_normal((cfg["g"], k, n), 2000, cfg["rhs"][1])).to(torch.bfloat16)
+    import oracle
+    oracle.build()
+    cores = oracle.set_threads(0)
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows_per_step = None
+    for _ in range(args.warmup):
+        v, _, _ = cpu_oracle_sample(name, gs, lhs_h, rhs_h, per_step)
+        rows_per_step = rows_per_step or max(16, int(v * per_step / (2.0 * k * n)))
+    rows_per_step = rows_per_step or 64
+    off = int(np.sum(gs))
+    rng = np.random.default_rng(11)
+    t_total, fl_total = 0.0, 0.0
+    for _ in range(args.steps):
+        rows = np.sort(rng.choice(off, size=min(rows_per_step, off), replace=False))
+        t0 = time.perf_counter()
+        oracle.forward_rows(lhs_h, rhs_h, gs, rows)
+        t_total += time.perf_counter() - t0
+        fl_total += 2.0 * rows.size * k * n
+    value = fl_total / t_total / 1e12
+    sample = f"{rows_per_step} random valid rows of {name} (x full N) per step, fp64 oracle"
+    return {
+        "impl": "reference", "metric": "ragged-dot useful TFLOP/s (fraction of GB300 dense bf16 peak; speedup vs "
+                                       "padded in per_config)",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_total / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": f"{name}: M={cfg['m']} K={k} N={n} G={cfg['g']}", "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral_bf16", choices=["mixtral_bf16", "deepseek_bf16"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    barrier = lambda: None  # noqa: E731
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group(backend=backend)
+        barrier = dist.barrier
+
+    if args.impl == "reference":
+        res = bench_reference(args, rank, world)
+    else:
+        res = bench_ours(args, rank, world, barrier)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,390 @@
+// api.cu -- the C ABI of librdot (declared in include/rdot.h).
+//
+// Host side only: argument checks, plan state, TMA tensor-map encoding (through the driver
+// entry point the runtime hands out, so the library links against libcudart alone) and kernel
+// launches on the caller's stream. No call here synchronises the host with the GPU except
+// rdot_read_status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "kernels.h"
+#include "rdot.h"
+
+using namespace rdot;
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s of device time per wait
+constexpr size_t kWorkspaceBytes = 256;
+
+thread_local std::string g_last_cuda_error;
+
+rdot_status cuda_fail(cudaError_t e, const char* what) {
+    char buf[256];
+    std::snprintf(buf, sizeof buf, "%s: %s (%d)", what, cudaGetErrorString(e), static_cast<int>(e));
+    g_last_cuda_error = buf;
+    return RDOT_ERR_CUDA;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+
+// Saves and restores the caller's current device around a call.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            ok = false;
+            return;
+        }
+        if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+struct rdot_plan_s {
+    rdot_problem p{};
+    int device = 0;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int kind = 0;          // 0: SIMT fp32, 1: tcgen05 bf16 forward
+    int tile_m = 0, tile_n = 0;
+    int m_inner = 1;
+    int grid = 1;
+    uint64_t timeout_ns = kDefaultTimeoutNs;
+    // tensor maps cached by operand pointers (re-encoded when a pointer changes)
+    const void* map_lhs_ptr = nullptr;
+    const void* map_rhs_ptr = nullptr;
+    CUtensorMap map_a{}, map_b{};
+};
+
+namespace {
+
+rdot_status encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled entry point unavailable";
+        return RDOT_ERR_CUDA;
+    }
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled (2d) failed: " + std::to_string(static_cast<int>(r));
+        return RDOT_ERR_CUDA;
+    }
+    return RDOT_OK;
+}
+
+rdot_status encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1,
+                      uint64_t d2, uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled entry point unavailable";
+        return RDOT_ERR_CUDA;
+    }
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+    cuuint32_t box[3] = {b0, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error = "cuTensorMapEncodeTiled (3d) failed: " + std::to_string(static_cast<int>(r));
+        return RDOT_ERR_CUDA;
+    }
+    return RDOT_OK;
+}
+
+rdot_status check_problem(const rdot_problem* p) {
+    if (!p) return RDOT_ERR_INVALID_ARG;
+    if (p->m < 0 || p->k < 1 || p->n < 1 || p->groups < 1 || p->groups > RDOT_MAX_GROUPS)
+        return RDOT_ERR_INVALID_ARG;
+    if (p->m > 0x7fffffffLL || p->k > 0x7fffffffLL || p->n > 0x7fffffffLL) return RDOT_ERR_UNSUPPORTED;
+    if (p->flags & ~3) return RDOT_ERR_INVALID_ARG;
+    if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256) return RDOT_ERR_UNSUPPORTED;
+    switch (p->mode) {
+        case RDOT_MODE_FORWARD:
+            if (p->in_dtype == RDOT_F32) {
+                if (p->out_dtype != RDOT_F32 && p->out_dtype != RDOT_BF16) return RDOT_ERR_UNSUPPORTED;
+                if (p->out_dtype == RDOT_BF16 && (p->n % 8)) return RDOT_ERR_UNSUPPORTED;
+                return RDOT_OK;
+            }
+            if (p->in_dtype == RDOT_BF16) {
+                if (p->out_dtype != RDOT_F32 && p->out_dtype != RDOT_BF16) return RDOT_ERR_UNSUPPORTED;
+                if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;   // 16-byte TMA row pitch
+                return RDOT_OK;
+            }
+            return RDOT_ERR_UNSUPPORTED;
+        case RDOT_MODE_GRAD_WEIGHT:
+        case RDOT_MODE_FORWARD_MXFP8:
+            return RDOT_ERR_UNSUPPORTED;
+        default:
+            return RDOT_ERR_INVALID_ARG;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan_out) {
+    if (!plan_out) return RDOT_ERR_INVALID_ARG;
+    *plan_out = nullptr;
+    rdot_status st = check_problem(problem);
+    if (st != RDOT_OK) return st;
+    int ndev = 0;
+    cudaError_t e = cudaGetDeviceCount(&ndev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+    if (device < 0 || device >= ndev) return RDOT_ERR_INVALID_ARG;
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+
+    rdot_plan_s* pl = new (std::nothrow) rdot_plan_s();
+    if (!pl) return RDOT_ERR_INVALID_ARG;
+    pl->p = *problem;
+    pl->device = device;
+    pl->sm_count = prop.multiProcessorCount;
+    pl->cc_major = prop.major;
+    pl->cc_minor = prop.minor;
+    const rdot_problem& p = pl->p;
+    // row tiles fastest inside a group when the group's average lhs slice is smaller than its
+    // weights (the ragged M/N-swap decision on M_avg = M / G)
+    const long long m_avg = p.m / p.groups;
+    pl->m_inner = (m_avg <= p.n) ? 1 : 0;
+    if (p.flags & 1) pl->m_inner = 1;
+    if (p.flags & 2) pl->m_inner = 0;
+
+    if (p.mode == RDOT_MODE_FORWARD && p.in_dtype == RDOT_F32) {
+        pl->kind = 0;
+        pl->tile_m = SIMT_BM;
+        pl->tile_n = SIMT_BN;
+        const int nt = static_cast<int>((p.n + SIMT_BN - 1) / SIMT_BN);
+        const long long bound = forward_tile_bound(p.m, p.groups, SIMT_BM, nt);
+        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, 4LL * pl->sm_count)));
+    } else if (p.mode == RDOT_MODE_FORWARD && p.in_dtype == RDOT_BF16) {
+        if (prop.major != 10) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;   // tcgen05 kernels are built for sm_103a only
+        }
+        pl->kind = 1;
+        pl->tile_m = TC_BM;
+        pl->tile_n = p.tile_n ? p.tile_n : (p.n <= 128 ? 128 : 256);
+        const int nt = static_cast<int>((p.n + pl->tile_n - 1) / pl->tile_n);
+        const long long bound = forward_tile_bound(p.m, p.groups, TC_BM, nt);
+        if (bound > 0x7fffffffLL) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
+    } else {
+        delete pl;
+        return RDOT_ERR_UNSUPPORTED;
+    }
+    *plan_out = pl;
+    return RDOT_OK;
+}
+
+rdot_status rdot_plan_destroy(rdot_plan_t plan) {
+    delete plan;
+    return RDOT_OK;
+}
+
+rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes) {
+    if (!plan || !bytes) return RDOT_ERR_INVALID_ARG;
+    *bytes = kWorkspaceBytes;
+    return RDOT_OK;
+}
+
+rdot_status rdot_plan_info(rdot_plan_t plan, int32_t* tile_m, int32_t* tile_n, int32_t* m_inner,
+                           int32_t* grid_ctas) {
+    if (!plan) return RDOT_ERR_INVALID_ARG;
+    if (tile_m) *tile_m = plan->tile_m;
+    if (tile_n) *tile_n = plan->tile_n;
+    if (m_inner) *m_inner = plan->m_inner;
+    if (grid_ctas) *grid_ctas = plan->grid;
+    return RDOT_OK;
+}
+
+rdot_status rdot_set_wait_timeout(rdot_plan_t plan, uint64_t timeout_ns) {
+    if (!plan) return RDOT_ERR_INVALID_ARG;
+    plan->timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+    return RDOT_OK;
+}
+
+rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, const int32_t* group_sizes, void* out,
+                         void* workspace, void* stream) {
+    if (!plan || !group_sizes || !workspace) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.mode != RDOT_MODE_FORWARD) return RDOT_ERR_INVALID_ARG;
+    if (p.m == 0) return RDOT_OK;
+    if (!lhs || !rhs || !out) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    FwdArgs a{};
+    a.group_sizes = group_sizes;
+    a.out = out;
+    a.M = static_cast<int>(p.m);
+    a.K = static_cast<int>(p.k);
+    a.N = static_cast<int>(p.n);
+    a.G = p.groups;
+    a.NT = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
+    a.m_inner = plan->m_inner;
+    a.status = static_cast<int32_t*>(workspace);
+    a.timeout_ns = plan->timeout_ns;
+    cudaError_t e;
+    if (plan->kind == 0) {
+        e = launch_fwd_simt(static_cast<const float*>(lhs), static_cast<const float*>(rhs), a,
+                            p.out_dtype == RDOT_BF16, plan->grid, s);
+        if (e != cudaSuccess) return cuda_fail(e, "fwd_simt launch");
+        return RDOT_OK;
+    }
+    if (plan->map_lhs_ptr != lhs) {
+        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs, p.k, p.m, p.k * 2, TC_BK,
+                                   TC_BM);
+        if (st != RDOT_OK) return st;
+        plan->map_lhs_ptr = lhs;
+    }
+    if (plan->map_rhs_ptr != rhs) {
+        rdot_status st = encode_3d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rhs, p.n, p.k, p.groups, p.n * 2,
+                                   p.k * p.n * 2, 64, TC_BK, 1);
+        if (st != RDOT_OK) return st;
+        plan->map_rhs_ptr = rhs;
+    }
+    e = launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fwd_tc launch");
+    return RDOT_OK;
+}
+
+rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t* lhs_scale, const void* rhs,
+                               const uint8_t* rhs_scale, const int32_t* group_sizes, void* out, void* workspace,
+                               void* stream) {
+    (void)lhs; (void)lhs_scale; (void)rhs; (void)rhs_scale; (void)group_sizes; (void)out; (void)workspace;
+    (void)stream;
+    if (!plan) return RDOT_ERR_INVALID_ARG;
+    return RDOT_ERR_UNSUPPORTED;
+}
+
+rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, const int32_t* group_sizes,
+                             float* dw, void* workspace, void* stream) {
+    (void)lhs; (void)dy; (void)group_sizes; (void)dw; (void)workspace; (void)stream;
+    if (!plan) return RDOT_ERR_INVALID_ARG;
+    return RDOT_ERR_UNSUPPORTED;
+}
+
+rdot_status rdot_padded_workspace_size(rdot_plan_t plan, int64_t capacity, size_t* bytes) {
+    (void)capacity;
+    if (!plan || !bytes) return RDOT_ERR_INVALID_ARG;
+    return RDOT_ERR_UNSUPPORTED;
+}
+
+rdot_status rdot_padded_forward(rdot_plan_t plan, const void* lhs, const void* rhs, const int32_t* group_sizes,
+                                void* out, int64_t capacity, void* pad_workspace, void* workspace, void* stream) {
+    (void)lhs; (void)rhs; (void)group_sizes; (void)out; (void)capacity; (void)pad_workspace; (void)workspace;
+    (void)stream;
+    if (!plan) return RDOT_ERR_INVALID_ARG;
+    return RDOT_ERR_UNSUPPORTED;
+}
+
+rdot_status rdot_read_status(rdot_plan_t plan, const void* workspace, int32_t* flags, void* stream) {
+    if (!plan || !workspace || !flags) return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "rdot_read_status");
+    *flags = v;
+    if (v & RDOT_STATUS_BIT_TIMEOUT) return RDOT_ERR_DEVICE_TIMEOUT;
+    if (v & RDOT_STATUS_BIT_GROUP_SIZES) return RDOT_WARN_GROUP_SIZES;
+    return RDOT_OK;
+}
+
+rdot_status rdot_clear_status(rdot_plan_t plan, void* workspace, void* stream) {
+    if (!plan || !workspace) return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "rdot_clear_status");
+    return RDOT_OK;
+}
+
+rdot_status rdot_debug_offsets_tilemap(rdot_plan_t plan, const int32_t* group_sizes, int32_t* offsets,
+                                       int32_t* tile_prefix, int32_t* tiles, int64_t max_tiles, void* workspace,
+                                       void* stream) {
+    if (!plan || !group_sizes || !workspace) return RDOT_ERR_INVALID_ARG;
+    if (tiles && max_tiles < 0) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    DeviceGuard dg(plan->device);
+    const int nt = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
+    cudaError_t e = launch_scan_export(group_sizes, p.groups, static_cast<int>(p.m), plan->tile_m, nt, plan->m_inner,
+                                       offsets, tile_prefix, tiles, tiles ? max_tiles : 0,
+                                       static_cast<int32_t*>(workspace), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "scan export launch");
+    return RDOT_OK;
+}
+
+rdot_status rdot_debug_wait_timeout(rdot_plan_t plan, uint64_t timeout_ns, void* workspace, void* stream) {
+    if (!plan || !workspace || timeout_ns == 0 || timeout_ns > 10000000000ull) return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    cudaError_t e = launch_wait_probe(timeout_ns, static_cast<int32_t*>(workspace), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
+    return RDOT_OK;
+}
+
+const char* rdot_status_string(rdot_status status) {
+    switch (status) {
+        case RDOT_OK: return "RDOT_OK";
+        case RDOT_ERR_INVALID_ARG: return "RDOT_ERR_INVALID_ARG";
+        case RDOT_ERR_UNSUPPORTED: return "RDOT_ERR_UNSUPPORTED";
+        case RDOT_ERR_CUDA: return "RDOT_ERR_CUDA";
+        case RDOT_ERR_DEVICE_TIMEOUT: return "RDOT_ERR_DEVICE_TIMEOUT";
+        case RDOT_WARN_GROUP_SIZES: return "RDOT_WARN_GROUP_SIZES";
+        default: return "RDOT_STATUS_UNKNOWN";
+    }
+}
+
+const char* rdot_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+int rdot_version(void) { return 100; }
+
+}  // extern "C"

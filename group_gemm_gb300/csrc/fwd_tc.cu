@@ -1,0 +1,291 @@
+// fwd_tc.cu -- bf16 ragged-dot forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes ("Group-GEMM in XLA", Part 3 "Non-Contracting (the MoE Case)"): for every
+// group g, out[rows of g, :] = lhs[rows of g, :] @ rhs[g]; rows past the last end offset are
+// written as zeros. Each group is a genuine dense GEMM of shape [m_g, K] x [K, N], so it runs on
+// the 5th-generation tensor cores; only the group boundaries are ragged.
+//
+// Design (one persistent CTA per SM, 192 threads, warp-specialised):
+//   warp 0      TMA producer: lhs tile [128 rows x 64 K] (K-major) and rhs tile [64 K x BN]
+//               (N-contiguous, so the B operand is MN-major), both 128-byte swizzled, into an
+//               S-stage shared-memory ring guarded by full/empty mbarriers.
+//   warp 1      allocates 2*BN TMEM columns (two fp32 accumulators of 128 lanes x BN) and issues
+//               tcgen05.mma kind::f16 (M=128, N=BN, K=16) from one thread; tcgen05.commit frees
+//               each smem stage and, after the last K block, signals "accumulator full".
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, fp32 -> bf16 (round to nearest
+//               even) or fp32, 16-byte stores of the rows that belong to the group; then mark
+//               the accumulator empty so the MMA warp can start the tile after next.
+// The two accumulators let the epilogue of tile i overlap the mainloop of tile i+1.
+//
+// Ragged rows: a tile starts at a group's start row + 128*mt and its TMA box may run into the
+// next group's rows. Those rows only feed accumulator rows that the epilogue never stores (each
+// accumulator row depends on its own lhs row), so the loads need no masking; rows past M and K
+// or N columns past the tensor come back zero-filled from TMA.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace rdot {
+
+namespace {
+
+constexpr int THREADS = 192;
+
+template <int BN, int STAGES>
+struct TcLayout {
+    static constexpr int A_BYTES = TC_BM * TC_BK * 2;             // 16 KB
+    static constexpr int B_CHUNK_BYTES = 64 * TC_BK * 2;          // 64 N x 64 K = 8 KB
+    static constexpr int B_BYTES = (BN / 64) * B_CHUNK_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;          // full, empty, tfull[2], tempty[2], drain
+    static constexpr int MISC_BYTES = 16;                          // tmem base, abort flag
+    static constexpr int TMEM_COLS = 2 * BN;
+    static size_t smem_bytes(int G) {
+        return 1024 + RING_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+    }
+};
+
+template <int BN, int STAGES, bool OUT_F32>
+__global__ void __launch_bounds__(THREADS, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                  FwdArgs a) {
+    using L = TcLayout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + L::RING_BYTES + L::BAR_BYTES + L::MISC_BYTES);
+    int32_t* tprefix = off + a.G + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 2) {
+        const int bad = group_scan_warp(a.group_sizes, a.G, a.M, TC_BM, a.NT, off, tprefix);
+        if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *tmem_holder;
+    const int W = tprefix[a.G];
+    const int KB = (a.K + TC_BK - 1) / TC_BK;
+    const bool m_inner = a.m_inner != 0;
+    const WaitGuard guard{abort_flag, a.status, a.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;   // stages with a load in flight, and its phase
+            bool ok = true;
+            for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
+                const Tile t = decode_tile(w, tprefix, off, a.G, TC_BM, a.NT, m_inner);
+                const int n0 = t.nt * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * L::STAGE_BYTES;
+                    uint8_t* sb = sa + L::A_BYTES;
+                    // 64-wide column chunks entirely past N are not loaded: they only feed
+                    // accumulator columns the epilogue never stores
+                    const int nchunks = min(BN / 64, (a.N - n0 + 63) / 64);
+                    mbar_arrive_expect_tx(&full[stage], L::A_BYTES + nchunks * L::B_CHUNK_BYTES);
+                    tma_load_2d(sa, &tmap_a, &full[stage], kb * TC_BK, t.row0);
+                    for (int j = 0; j < nchunks; ++j)
+                        tma_load_3d(sb + j * L::B_CHUNK_BYTES, &tmap_b, &full[stage], n0 + 64 * j, kb * TC_BK, t.g);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // stopping early: let every load still in flight land before the CTA exits
+                WaitGuard drain_guard{guard.abort, nullptr, guard.timeout_ns};
+                int dummy = 0;
+                drain_guard.abort = &dummy;
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(TC_BM, BN, true, true, false, true);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, guard)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, guard)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * L::STAGE_BYTES);
+                    const uint32_t sb = sa + L::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < TC_BK / 16; ++kk) {
+                        // A: K-major, +32 bytes per 16-element K step inside the 128-byte row
+                        const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+                        // B: MN-major, +2 groups of 8 K rows (2 x 1024 bytes) per K step
+                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, L::B_CHUNK_BYTES, 1024);
+                        mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            // all MMAs issued by this thread complete before teardown frees TMEM
+            mma_commit(drain);
+            WaitGuard drain_guard = guard;
+            int dummy = 0;
+            drain_guard.abort = &dummy;
+            (void)mbar_wait(drain, 0, drain_guard);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;            // accumulator row = TMEM lane
+        uint32_t acc = 0, acc_phase = 0;
+        for (int w = blockIdx.x; w < W; w += gridDim.x) {
+            const Tile t = decode_tile(w, tprefix, off, a.G, TC_BM, a.NT, m_inner);
+            const int n0 = t.nt * BN;
+            // the warp leaves together: tcgen05.ld below must be executed by all 32 lanes
+            const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            const bool row_ok = r < t.rows;
+            const long long orow = static_cast<long long>(t.row0 + r) * a.N;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, v);
+                tmem_ld_wait();
+                const int col = n0 + c * 32;
+                if (row_ok && col < a.N) {
+                    if (OUT_F32) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + col);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (col + 4 * j < a.N)
+                                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + col);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (col + 8 * j < a.N) {
+                                uint4 p;
+                                p.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                                p.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                                p.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                                p.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                                dst[j] = p;
+                            }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+        // zero rows [off[G], M): one contiguous range, split over CTAs and the 128 epilogue threads
+        {
+            const int esz = OUT_F32 ? 4 : 2;
+            const long long b0 = static_cast<long long>(off[a.G]) * a.N * esz;
+            const long long b1 = static_cast<long long>(a.M) * a.N * esz;   // both multiples of 16
+            const long long nv = (b1 - b0) / 16;
+            if (nv > 0) {
+                uint4* base = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + b0);
+                const long long per = (nv + gridDim.x - 1) / gridDim.x;
+                const long long s = per * blockIdx.x;
+                const long long e = min(nv, s + per);
+                for (long long i = s + (threadIdx.x - 64); i < e; i += 128) base[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+template <int BN, int STAGES, bool OUT_F32>
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const FwdArgs& a, int grid,
+                       cudaStream_t stream) {
+    using L = TcLayout<BN, STAGES>;
+    const size_t shm = L::smem_bytes(a.G);
+    auto kern = fwd_tc_kernel<BN, STAGES, OUT_F32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, THREADS, shm, stream>>>(ta, tb, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, int bn,
+                          bool out_f32, int grid, cudaStream_t stream) {
+    if (bn == 256) {
+        return out_f32 ? launch_one<256, 4, true>(tmap_a, tmap_b, a, grid, stream)
+                       : launch_one<256, 4, false>(tmap_a, tmap_b, a, grid, stream);
+    }
+    if (bn == 128) {
+        return out_f32 ? launch_one<128, 6, true>(tmap_a, tmap_b, a, grid, stream)
+                       : launch_one<128, 6, false>(tmap_a, tmap_b, a, grid, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rdot

@@ -1,0 +1,47 @@
+// kernels.h -- host-side launch interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rdot {
+
+// Arguments shared by the forward kernels (passed by value).
+struct FwdArgs {
+    const int32_t* group_sizes;  // device [G]
+    void* out;                   // device [M, N]
+    int M, K, N, G;
+    int NT;                      // column tiles per group
+    int m_inner;                 // 1: row tiles fastest inside a group
+    int32_t* status;             // device status word (may be null)
+    uint64_t timeout_ns;         // bounded-wait limit
+};
+
+// Static upper bound on the work items of a forward: sum_g ceil(m_g/BM) <= ceil(M/BM) + G.
+inline long long forward_tile_bound(long long M, int G, int BM, int NT) {
+    return ((M + BM - 1) / BM + G) * static_cast<long long>(NT);
+}
+
+// fp32 inputs, CUDA-core FMA (fwd_simt.cu). out_bf16 selects the output type.
+cudaError_t launch_fwd_simt(const float* lhs, const float* rhs, const FwdArgs& a, bool out_bf16, int grid,
+                            cudaStream_t stream);
+constexpr int SIMT_BM = 64;
+constexpr int SIMT_BN = 64;
+
+// bf16 inputs, tcgen05 tensor cores (fwd_tc.cu). tmap_a: lhs [M,K] box (64,128);
+// tmap_b: rhs [G,K,N] box (64,64,1); both 128-byte swizzled.
+cudaError_t launch_fwd_tc(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, int bn,
+                          bool out_f32, int grid, cudaStream_t stream);
+constexpr int TC_BM = 128;
+constexpr int TC_BK = 64;
+
+// Debug export of the scan and the tile decode (fwd_simt.cu).
+cudaError_t launch_scan_export(const int32_t* group_sizes, int G, int M, int BM, int NT, int m_inner,
+                               int32_t* offsets, int32_t* tile_prefix, int32_t* tiles, long long max_tiles,
+                               int32_t* status, cudaStream_t stream);
+
+// Bounded-wait probe: one CTA waits on a barrier nothing completes (fwd_simt.cu).
+cudaError_t launch_wait_probe(uint64_t timeout_ns, int32_t* status, cudaStream_t stream);
+
+}  // namespace rdot

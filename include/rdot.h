@@ -1,0 +1,201 @@
+/*
+ * rdot.h -- C ABI of librdot: ragged-dot / Group-GEMM for Mixture-of-Experts on GB300 (sm_103a).
+ *
+ * The operation ("Group-GEMM in XLA", Part 1 "The Ragged-Dot Operation"; Part 3
+ * "Non-Contracting (the MoE Case)"): lhs [M, K] holds the tokens stacked in group order,
+ * rhs [G, K, N] one weight matrix per expert, group_sizes [G] the number of rows of each
+ * group. Row i of the output is lhs[i, :] @ rhs[g(i)], where g(i) is the group whose
+ * [start, end) interval of the prefix sums of group_sizes contains i. K, N and G are fixed when
+ * a plan is made; the sizes themselves are runtime data that stay on the device.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" point to device memory of the plan's device; nothing is copied
+ *     to or from the host and the host never waits on the GPU (except rdot_read_status).
+ *   - All tensors are dense, row-major (C order) and contiguous. Every base pointer must be
+ *     16-byte aligned (TMA and vector stores).
+ *   - The caller owns every buffer, including the workspace. A plan owns host state only.
+ *   - Calls are asynchronous on the given stream (0 = legacy default stream) and make no host
+ *     synchronisation, so they can be captured in a CUDA graph after the first call on a
+ *     pointer set (the first call encodes tensor maps on the host).
+ *   - Argument errors are returned synchronously and launch nothing. Problems only visible on
+ *     the device (a negative group size, sizes summing past M, a pipeline wait that ran out)
+ *     set bits in the status word at the start of the workspace; the bits are sticky until the
+ *     caller clears them (rdot_clear_status) and are read with rdot_read_status.
+ *   - Reading of group_sizes: a negative size counts as 0 and each running end offset is
+ *     clamped to M (RDOT_STATUS_BIT_GROUP_SIZES is then set). Output rows at or past the last
+ *     end offset are written with zeros.
+ *   - A plan is not thread-safe: one host thread at a time may call into a given plan.
+ */
+#ifndef RDOT_H_
+#define RDOT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RDOT_API __attribute__((visibility("default")))
+#else
+#define RDOT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    RDOT_OK = 0,
+    RDOT_ERR_INVALID_ARG = 1,   /* a null pointer, a bad size, a misaligned pointer */
+    RDOT_ERR_UNSUPPORTED = 2,   /* a dtype/mode combination or size the library does not build */
+    RDOT_ERR_CUDA = 3,          /* a CUDA runtime or driver call failed (see rdot_last_cuda_error) */
+    RDOT_ERR_DEVICE_TIMEOUT = 4,/* rdot_read_status: a device-side wait ran out */
+    RDOT_WARN_GROUP_SIZES = 5   /* rdot_read_status: group_sizes were clamped on the device */
+} rdot_status;
+
+typedef enum { RDOT_F32 = 0, RDOT_BF16 = 1, RDOT_E4M3 = 2 } rdot_dtype;
+
+typedef enum {
+    RDOT_MODE_FORWARD = 0,       /* out[M,N] = lhs[M,K] @ rhs[g(i),K,N] (non-contracting ragged M) */
+    RDOT_MODE_GRAD_WEIGHT = 1,   /* dw[G,K,N] = lhs_g^T dy_g (ragged contraction over the rows) */
+    RDOT_MODE_FORWARD_MXFP8 = 2  /* forward with E4M3 operands and E8M0 scales per 32 K elements */
+} rdot_mode;
+
+/* Bits of the device status word (int32 at offset 0 of the workspace). */
+#define RDOT_STATUS_BIT_GROUP_SIZES 0x1  /* a size was negative or the sizes summed past M */
+#define RDOT_STATUS_BIT_TIMEOUT 0x2      /* a pipeline wait ran out; the kernel stopped early */
+
+/* rdot_problem.flags: force the order of work inside a group. By default row tiles run fastest
+ * when the average group's lhs slice (M/G rows) is no taller than the weights are wide (N), so
+ * consecutive CTAs share one weight slab in L2 ("Group-GEMM in XLA", Part 3 "The Compilation
+ * Pipeline": the M/N swap decided on M_avg = M_total / G). */
+#define RDOT_FLAG_ROW_TILES_INNER 0x1
+#define RDOT_FLAG_COL_TILES_INNER 0x2
+
+/* Largest number of groups a plan accepts (the group table lives in shared memory). */
+#define RDOT_MAX_GROUPS 1024
+
+typedef struct {
+    int64_t m;          /* rows of lhs (forward) or of lhs and dy (grad-weight): the static
+                           upper bound on sum(group_sizes) */
+    int64_t k;          /* lhs width (contraction of the forward) */
+    int64_t n;          /* output width: rhs.shape[2] (forward) or dy width (grad-weight) */
+    int32_t groups;     /* G, 1 .. RDOT_MAX_GROUPS */
+    int32_t mode;       /* rdot_mode */
+    int32_t in_dtype;   /* rdot_dtype of lhs/rhs (forward, grad-weight); RDOT_E4M3 for MXFP8 */
+    int32_t out_dtype;  /* RDOT_F32 or RDOT_BF16 (forward); RDOT_F32 (grad-weight) */
+    int32_t tile_n;     /* 0 = choose; otherwise the N tile width of the tensor-core kernels */
+    int32_t flags;      /* RDOT_FLAG_* bits; 0 lets the plan choose */
+} rdot_problem;
+
+typedef struct rdot_plan_s* rdot_plan_t;
+
+/* Creates a plan for one problem shape on one device. Checks the problem (sizes, dtype and
+ * mode combination, alignment rules: k and n multiples of 8 for 16-bit inputs, of 16 for
+ * E4M3, k a multiple of 32 for MXFP8) and picks the kernel and its tile configuration. The
+ * plan-versus-runtime split follows "Group-GEMM in XLA", Part 2 "The Compile-Time vs. Runtime
+ * Problem": the shape is fixed here, the group sizes arrive at run time on the device.
+ * Returns RDOT_ERR_INVALID_ARG / RDOT_ERR_UNSUPPORTED without creating a plan on error. */
+RDOT_API rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan_out);
+
+/* Destroys a plan (host memory only; no device work). Null is accepted. */
+RDOT_API rdot_status rdot_plan_destroy(rdot_plan_t plan);
+
+/* Bytes of device workspace the plan's calls need (at least 256, 256-byte aligned by the
+ * caller). The workspace holds the status word followed by the group table exported by
+ * rdot_debug_offsets_tilemap. It must be zeroed once before first use. */
+RDOT_API rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes);
+
+/* Forward ragged-dot, non-contracting ragged dimension ("Group-GEMM in XLA", Part 3
+ * "Non-Contracting (the MoE Case)").
+ *   lhs          device [M, K], the plan's in_dtype (RDOT_F32 or RDOT_BF16)
+ *   rhs          device [G, K, N], same dtype
+ *   group_sizes  device int32 [G]
+ *   out          device [M, N], the plan's out_dtype; every row is written (zeros past the sum)
+ *   workspace    device, rdot_workspace_size bytes
+ * fp32 inputs run on CUDA-core fp32 FMA; bf16 inputs on the tcgen05 tensor cores with fp32
+ * accumulation in tensor memory. */
+RDOT_API rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs,
+                         const int32_t* group_sizes, void* out, void* workspace, void* stream);
+
+/* MXFP8 forward (AITER PR #5658 "Merge MoE MXFP8 GEMM into _moe_gemm_a8w8": OCP E4M3 operands,
+ * one E8M0 scale per 32 consecutive K elements, quant_block_size == 32, K % 32 == 0).
+ *   lhs        device uint8 [M, K]   E4M3 codes
+ *   lhs_scale  device uint8 [M, K/32] E8M0 scales (value = 2^(s-127))
+ *   rhs        device uint8 [G, K, N] E4M3 codes
+ *   rhs_scale  device uint8 [G, K/32, N] E8M0 scales
+ *   out        device bf16 [M, N]
+ * Element value = decode(code) * 2^(scale - 127); products accumulate in fp32. */
+RDOT_API rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t* lhs_scale,
+                               const void* rhs, const uint8_t* rhs_scale,
+                               const int32_t* group_sizes, void* out, void* workspace,
+                               void* stream);
+
+/* Weight gradient: the ragged dimension is the contraction ("Group-GEMM in XLA", Part 3
+ * "Contracting"; Part 4 Table 7, class wgrad_wi).
+ *   lhs  device bf16 [M, K]
+ *   dy   device bf16 [M, N]
+ *   dw   device fp32 [G, K, N]: dw[g] = sum over rows i of group g of lhs[i,:]^T dy[i,:];
+ *        every group's slab is written (zeros for an empty group). Rows at or past the last
+ *        end offset are never read into the result. */
+RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy,
+                             const int32_t* group_sizes, float* dw, void* workspace,
+                             void* stream);
+
+/* Bytes of the padded baseline's scratch for a capacity of `capacity` rows per group
+ * (the padded lhs [G, capacity, K] plus the padded output [G, capacity, N] plus a small table). */
+RDOT_API rdot_status rdot_padded_workspace_size(rdot_plan_t plan, int64_t capacity, size_t* bytes);
+
+/* Padded-dense baseline ("Group-GEMM in XLA", Part 1 "The Naive Support, and Why It Hurts:
+ * Padded-Dot"): every group is padded (or cut) to `capacity` rows, one uniform batched GEMM
+ * G x [capacity, K] x [K, N] runs on the same tensor-core mainloop, and the rows are gathered
+ * back. Rows of a group beyond `capacity` are dropped (written as zeros), as in a fixed-capacity
+ * MoE. Same argument rules as rdot_forward (bf16 only); pad_workspace holds
+ * rdot_padded_workspace_size bytes. capacity must be a positive multiple of 128. */
+RDOT_API rdot_status rdot_padded_forward(rdot_plan_t plan, const void* lhs, const void* rhs,
+                                const int32_t* group_sizes, void* out, int64_t capacity,
+                                void* pad_workspace, void* workspace, void* stream);
+
+/* Copies the device status word into *flags (RDOT_STATUS_BIT_*). Synchronises the stream.
+ * Returns RDOT_ERR_DEVICE_TIMEOUT if the timeout bit is set, RDOT_WARN_GROUP_SIZES if only the
+ * group-size bit is set, RDOT_OK otherwise. */
+RDOT_API rdot_status rdot_read_status(rdot_plan_t plan, const void* workspace, int32_t* flags, void* stream);
+
+/* Clears the status word (an asynchronous memset on the stream). */
+RDOT_API rdot_status rdot_clear_status(rdot_plan_t plan, void* workspace, void* stream);
+
+/* Debug export of the device group scan and the persistent scheduler's table, computed by the
+ * same device code the kernels use: offsets int32 [G+1] (prefix sums with the clamping
+ * reading, "Group-GEMM in XLA" Part 3 and Table 2) and tile_prefix int32 [G+1] (number of work
+ * tiles before each group for the plan's tile shape). Both device pointers; either may be null.
+ * tiles, if not null, receives int32 [max_tiles, 3] = (group, row tile, column tile) for the
+ * first max_tiles work items in scheduler order. */
+RDOT_API rdot_status rdot_debug_offsets_tilemap(rdot_plan_t plan, const int32_t* group_sizes,
+                                       int32_t* offsets, int32_t* tile_prefix, int32_t* tiles,
+                                       int64_t max_tiles, void* workspace, void* stream);
+
+/* The tile shape and scheduling order the plan chose (for tests and reports). */
+RDOT_API rdot_status rdot_plan_info(rdot_plan_t plan, int32_t* tile_m, int32_t* tile_n, int32_t* m_inner,
+                           int32_t* grid_ctas);
+
+/* Test hook for the bounded device waits: launches one CTA that waits on a barrier nothing
+ * completes, for at most timeout_ns of device time, then sets RDOT_STATUS_BIT_TIMEOUT in the
+ * workspace status word and returns. The context stays usable. */
+RDOT_API rdot_status rdot_debug_wait_timeout(rdot_plan_t plan, uint64_t timeout_ns, void* workspace,
+                                    void* stream);
+
+/* Overrides the device-side wait limit (ns) of the plan's kernels; 0 restores the default. */
+RDOT_API rdot_status rdot_set_wait_timeout(rdot_plan_t plan, uint64_t timeout_ns);
+
+/* Human-readable status name. */
+RDOT_API const char* rdot_status_string(rdot_status status);
+
+/* Text of the last CUDA error seen by this library on the calling host thread ("" if none). */
+RDOT_API const char* rdot_last_cuda_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+RDOT_API int rdot_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RDOT_H_ */

@@ -1,0 +1,66 @@
+"""The C-ABI library builds, loads and exports every function include/rdot.h declares; host-side
+argument checks answer without a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import group_gemm_gb300 as gg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gg.build()
+    return gg.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^RDOT_API\s+[\w\s\*]+?\b(rdot_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert declared, "no declarations found"
+    assert declared == set(gg.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert gg.rdot_status_string(0) == "RDOT_OK"
+    assert gg.rdot_status_string(4) == "RDOT_ERR_DEVICE_TIMEOUT"
+    assert gg.rdot_status_string(99) == "RDOT_STATUS_UNKNOWN"
+    assert gg.rdot_version() >= 100
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(m=16, k=0, n=8, groups=1), gg.RDOT_ERR_INVALID_ARG),
+    (dict(m=16, k=8, n=8, groups=0), gg.RDOT_ERR_INVALID_ARG),
+    (dict(m=16, k=8, n=8, groups=gg.RDOT_MAX_GROUPS + 1), gg.RDOT_ERR_INVALID_ARG),
+    (dict(m=-1, k=8, n=8, groups=1), gg.RDOT_ERR_INVALID_ARG),
+    (dict(m=16, k=12, n=8, groups=1, in_dtype=gg.RDOT_BF16), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=8, n=8, groups=1, flags=4), gg.RDOT_ERR_INVALID_ARG),
+    (dict(m=16, k=8, n=8, groups=1, tile_n=96), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=8, n=8, groups=1, mode=7), gg.RDOT_ERR_INVALID_ARG),
+])
+def test_plan_argument_checks_without_gpu(lib, kw, status):
+    base = dict(m=16, k=8, n=8, groups=1, mode=0, in_dtype=gg.RDOT_BF16, out_dtype=gg.RDOT_BF16, tile_n=0, flags=0)
+    base.update(kw)
+    h = ctypes.c_void_p()
+    assert lib.rdot_plan(ctypes.byref(gg.Problem(**base)), 0, ctypes.byref(h)) == status
+    assert not h.value
+
+
+def test_null_arguments_are_rejected(lib):
+    assert lib.rdot_plan(None, 0, None) == gg.RDOT_ERR_INVALID_ARG
+    assert lib.rdot_forward(None, None, None, None, None, None, None) == gg.RDOT_ERR_INVALID_ARG
+    assert lib.rdot_workspace_size(None, None) == gg.RDOT_ERR_INVALID_ARG
+    assert lib.rdot_plan_destroy(None) == gg.RDOT_OK
