@@ -78,7 +78,7 @@ struct rdot_plan_s {
     int device = 0;
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
-    int kind = 0;          // 0: SIMT fp32, 1: tcgen05 bf16 forward
+    int kind = 0;          // 0: SIMT fp32 forward, 1: tcgen05 bf16 forward, 2: tcgen05 grad-weight
     int tile_m = 0, tile_n = 0;
     int m_inner = 1;
     int grid = 1;
@@ -87,6 +87,10 @@ struct rdot_plan_s {
     const void* map_lhs_ptr = nullptr;
     const void* map_rhs_ptr = nullptr;
     CUtensorMap map_a{}, map_b{};
+    // the padded baseline's own lhs map (over the padded buffer)
+    const void* pad_map_ptr = nullptr;
+    int64_t pad_map_rows = 0;
+    CUtensorMap pad_map_a{};
 };
 
 namespace {
@@ -152,6 +156,9 @@ rdot_status check_problem(const rdot_problem* p) {
             }
             return RDOT_ERR_UNSUPPORTED;
         case RDOT_MODE_GRAD_WEIGHT:
+            if (p->in_dtype != RDOT_BF16 || p->out_dtype != RDOT_F32) return RDOT_ERR_UNSUPPORTED;
+            if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;
+            return RDOT_OK;
         case RDOT_MODE_FORWARD_MXFP8:
             return RDOT_ERR_UNSUPPORTED;
         default:
@@ -213,6 +220,21 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             return RDOT_ERR_UNSUPPORTED;
         }
         pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
+    } else if (p.mode == RDOT_MODE_GRAD_WEIGHT) {
+        if (prop.major != 10) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->kind = 2;
+        pl->tile_m = TC_BM;   // rows of dw (the K axis) per tile
+        pl->tile_n = p.tile_n ? p.tile_n : (p.n <= 128 ? 128 : 256);
+        const long long kt = (p.k + TC_BM - 1) / TC_BM, nt = (p.n + pl->tile_n - 1) / pl->tile_n;
+        const long long work = kt * nt * p.groups;
+        if (work > 0x7fffffffLL) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(work, pl->sm_count)));
     } else {
         delete pl;
         return RDOT_ERR_UNSUPPORTED;
@@ -307,23 +329,137 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
 
 rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, const int32_t* group_sizes,
                              float* dw, void* workspace, void* stream) {
-    (void)lhs; (void)dy; (void)group_sizes; (void)dw; (void)workspace; (void)stream;
-    if (!plan) return RDOT_ERR_INVALID_ARG;
-    return RDOT_ERR_UNSUPPORTED;
+    if (!plan || !group_sizes || !workspace || !dw) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.mode != RDOT_MODE_GRAD_WEIGHT || plan->kind != 2) return RDOT_ERR_INVALID_ARG;
+    if (p.m > 0 && (!lhs || !dy)) return RDOT_ERR_INVALID_ARG;
+    if ((lhs && !aligned16(lhs)) || (dy && !aligned16(dy)) || !aligned16(dw) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.m == 0) {
+        // no rows at all: every slab is zero
+        cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * p.groups * p.k * p.n, s);
+        return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (plan->map_lhs_ptr != lhs) {
+        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs, p.k, p.m, p.k * 2, 64, 64);
+        if (st != RDOT_OK) return st;
+        plan->map_lhs_ptr = lhs;
+    }
+    if (plan->map_rhs_ptr != dy) {
+        rdot_status st = encode_2d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, p.n, p.m, p.n * 2, 64, 64);
+        if (st != RDOT_OK) return st;
+        plan->map_rhs_ptr = dy;
+    }
+    WgradArgs a{};
+    a.group_sizes = group_sizes;
+    a.dw = dw;
+    a.M = static_cast<int>(p.m);
+    a.K = static_cast<int>(p.k);
+    a.N = static_cast<int>(p.n);
+    a.G = p.groups;
+    a.KT = static_cast<int>((p.k + TC_BM - 1) / TC_BM);
+    a.NT = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
+    a.status = static_cast<int32_t*>(workspace);
+    a.timeout_ns = plan->timeout_ns;
+    cudaError_t e = launch_wgrad_tc(plan->map_a, plan->map_b, a, plan->tile_n, plan->grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "wgrad_tc launch");
+    return RDOT_OK;
 }
 
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct PadLayout {
+    size_t lhs_off, out_off, gs_off, total;
+};
+
+PadLayout pad_layout(const rdot_problem& p, int64_t capacity) {
+    PadLayout l{};
+    const size_t rows = static_cast<size_t>(p.groups) * static_cast<size_t>(capacity);
+    const size_t out_esz = p.out_dtype == RDOT_F32 ? 4 : 2;
+    l.lhs_off = 0;
+    l.out_off = align256(rows * static_cast<size_t>(p.k) * 2);
+    l.gs_off = l.out_off + align256(rows * static_cast<size_t>(p.n) * out_esz);
+    l.total = l.gs_off + align256(sizeof(int32_t) * static_cast<size_t>(p.groups));
+    return l;
+}
+
+bool padded_ok(const rdot_plan_s* plan, int64_t capacity) {
+    return plan->kind == 1 && capacity > 0 && capacity % TC_BM == 0 &&
+           static_cast<long long>(plan->p.groups) * capacity <= 0x7fffffffLL;
+}
+}  // namespace
+
 rdot_status rdot_padded_workspace_size(rdot_plan_t plan, int64_t capacity, size_t* bytes) {
-    (void)capacity;
     if (!plan || !bytes) return RDOT_ERR_INVALID_ARG;
-    return RDOT_ERR_UNSUPPORTED;
+    if (plan->kind != 1) return RDOT_ERR_UNSUPPORTED;
+    if (!padded_ok(plan, capacity)) return RDOT_ERR_INVALID_ARG;
+    *bytes = pad_layout(plan->p, capacity).total;
+    return RDOT_OK;
 }
 
 rdot_status rdot_padded_forward(rdot_plan_t plan, const void* lhs, const void* rhs, const int32_t* group_sizes,
                                 void* out, int64_t capacity, void* pad_workspace, void* workspace, void* stream) {
-    (void)lhs; (void)rhs; (void)group_sizes; (void)out; (void)capacity; (void)pad_workspace; (void)workspace;
-    (void)stream;
-    if (!plan) return RDOT_ERR_INVALID_ARG;
-    return RDOT_ERR_UNSUPPORTED;
+    if (!plan || !group_sizes || !workspace || !pad_workspace) return RDOT_ERR_INVALID_ARG;
+    if (plan->kind != 1) return RDOT_ERR_UNSUPPORTED;
+    if (!padded_ok(plan, capacity)) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.m == 0) return RDOT_OK;
+    if (!lhs || !rhs || !out) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(pad_workspace) & 255u) || (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const PadLayout l = pad_layout(p, capacity);
+    uint8_t* base = static_cast<uint8_t*>(pad_workspace);
+    void* lhs_pad = base + l.lhs_off;
+    void* out_pad = base + l.out_off;
+    int32_t* ugs = reinterpret_cast<int32_t*>(base + l.gs_off);
+    const int C = static_cast<int>(capacity);
+    const int rows_pad = p.groups * C;
+    int32_t* status = static_cast<int32_t*>(workspace);
+    const int esz_out = p.out_dtype == RDOT_F32 ? 4 : 2;
+    cudaError_t e = launch_pad_scatter(lhs, group_sizes, lhs_pad, ugs, static_cast<int>(p.m), p.groups, C, p.k * 2,
+                                       4 * plan->sm_count, status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pad scatter launch");
+    if (plan->pad_map_ptr != lhs_pad || plan->pad_map_rows != rows_pad) {
+        rdot_status st = encode_2d(&plan->pad_map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs_pad, p.k, rows_pad, p.k * 2,
+                                   TC_BK, TC_BM);
+        if (st != RDOT_OK) return st;
+        plan->pad_map_ptr = lhs_pad;
+        plan->pad_map_rows = rows_pad;
+    }
+    if (plan->map_rhs_ptr != rhs) {
+        rdot_status st = encode_3d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rhs, p.n, p.k, p.groups, p.n * 2,
+                                   p.k * p.n * 2, 64, TC_BK, 1);
+        if (st != RDOT_OK) return st;
+        plan->map_rhs_ptr = rhs;
+    }
+    FwdArgs a{};
+    a.group_sizes = ugs;
+    a.out = out_pad;
+    a.M = rows_pad;
+    a.K = static_cast<int>(p.k);
+    a.N = static_cast<int>(p.n);
+    a.G = p.groups;
+    a.NT = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
+    a.m_inner = C <= p.n ? 1 : 0;
+    a.status = status;
+    a.timeout_ns = plan->timeout_ns;
+    const long long bound = forward_tile_bound(rows_pad, p.groups, TC_BM, a.NT);
+    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, plan->sm_count)));
+    e = launch_fwd_tc(plan->pad_map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "padded GEMM launch");
+    e = launch_pad_gather(out_pad, group_sizes, out, static_cast<int>(p.m), p.groups, C, p.n * esz_out,
+                          4 * plan->sm_count, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pad gather launch");
+    return RDOT_OK;
 }
 
 rdot_status rdot_read_status(rdot_plan_t plan, const void* workspace, int32_t* flags, void* stream) {

@@ -36,6 +36,27 @@ cudaError_t launch_fwd_tc(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, 
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;
 
+// Arguments of the weight-gradient kernel (passed by value).
+struct WgradArgs {
+    const int32_t* group_sizes;  // device [G]
+    float* dw;                   // device [G, K, N]
+    int M, K, N, G;
+    int KT, NT;                  // 128-row tiles of K, BN-wide tiles of N
+    int32_t* status;
+    uint64_t timeout_ns;
+};
+
+// bf16 lhs [M,K] and dy [M,N], fp32 dw [G,K,N], tcgen05 (wgrad_tc.cu). Both maps 2-D with a
+// (64, 64) box, 128-byte swizzled.
+cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int bn,
+                            int grid, cudaStream_t stream);
+
+// Padded-dense baseline data movement (padded.cu).
+cudaError_t launch_pad_scatter(const void* lhs, const int32_t* gs, void* lhs_pad, int32_t* uniform_gs, int M, int G,
+                               int C, long long row_bytes, int grid, int32_t* status, cudaStream_t stream);
+cudaError_t launch_pad_gather(const void* out_pad, const int32_t* gs, void* out, int M, int G, int C,
+                              long long row_bytes, int grid, cudaStream_t stream);
+
 // Debug export of the scan and the tile decode (fwd_simt.cu).
 cudaError_t launch_scan_export(const int32_t* group_sizes, int G, int M, int BM, int NT, int m_inner,
                                int32_t* offsets, int32_t* tile_prefix, int32_t* tiles, long long max_tiles,

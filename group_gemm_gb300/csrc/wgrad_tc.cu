@@ -1,0 +1,295 @@
+// wgrad_tc.cu -- weight gradient of ragged-dot on the sm_103a tensor cores: the ragged
+// dimension is the contraction ("Group-GEMM in XLA", Part 3 "Contracting": each group reduces
+// only over its own slice of the contracted axis and owns its own output matrix; Part 4 Table 7,
+// class wgrad_wi: [M,K] x [M,N] -> [E,K,N]).
+//
+//   dw[g, a, b] = sum over rows i in [off[g], off[g+1]) of lhs[i, a] * dy[i, b]     (fp32 out)
+//
+// Work items are (g, K tile of 128, N tile of BN), all groups included (an empty group's slab
+// is written as zeros without touching the tensor cores). The contraction runs over the group's
+// rows in chunks of 64: TMA brings lhs[rows, 128 K columns] and dy[rows, BN columns]; both are
+// MN-major operands (the MMA's M = K columns and N = dy columns are the contiguous axes), 128-byte
+// swizzled. The last chunk of a group usually runs into the next group's rows: those rows are
+// zeroed in shared memory (both operands, so NaN/Inf there cannot leak through 0 * x) before the
+// MMA reads them. Roles: warp 0 TMA, warp 1 MMA (+ tail zeroing), warps 2..5 epilogue; two TMEM
+// accumulators let the epilogue of one tile overlap the next tile's mainloop.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace rdot {
+
+namespace {
+
+constexpr int THREADS = 192;
+constexpr int ROWS = 64;   // contraction rows per stage
+
+template <int BN, int STAGES>
+struct WgLayout {
+    static constexpr int CHUNK_BYTES = 64 * ROWS * 2;           // 64 MN x 64 rows of bf16 = 8 KB
+    static constexpr int A_CHUNKS = TC_BM / 64;                 // 2
+    static constexpr int B_CHUNKS = BN / 64;
+    static constexpr int A_BYTES = A_CHUNKS * CHUNK_BYTES;
+    static constexpr int B_BYTES = B_CHUNKS * CHUNK_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
+    static constexpr int MISC_BYTES = 16;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static size_t smem_bytes(int G) {
+        return 1024 + RING_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+    }
+};
+
+struct WgTile {
+    int g, kt, nt, row0, rows;
+};
+
+__device__ __forceinline__ WgTile wg_decode(int w, int KT, int NT, const int32_t* off) {
+    WgTile t;
+    t.g = w / (KT * NT);
+    const int rem = w - t.g * KT * NT;
+    t.kt = rem / NT;
+    t.nt = rem - t.kt * NT;
+    t.row0 = off[t.g];
+    t.rows = off[t.g + 1] - off[t.g];
+    return t;
+}
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(THREADS, 1)
+    wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_dy,
+                    WgradArgs a) {
+    using L = WgLayout<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + L::RING_BYTES + L::BAR_BYTES + L::MISC_BYTES);
+    int32_t* unused = off + a.G + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_x);
+        tma_prefetch_desc(&tmap_dy);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 2) {
+        const int bad = group_scan_warp(a.group_sizes, a.G, a.M, 1, 1, off, unused);
+        if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *tmem_holder;
+    const int W = a.G * a.KT * a.NT;
+    const WaitGuard guard{abort_flag, a.status, a.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
+                const WgTile t = wg_decode(w, a.KT, a.NT, off);
+                const int nchunks_rows = (t.rows + ROWS - 1) / ROWS;
+                const int k0 = t.kt * TC_BM, n0 = t.nt * BN;
+                const int a_chunks = min(L::A_CHUNKS, (a.K - k0 + 63) / 64);
+                const int b_chunks = min(L::B_CHUNKS, (a.N - n0 + 63) / 64);
+                for (int c = 0; c < nchunks_rows; ++c) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * L::STAGE_BYTES;
+                    uint8_t* sb = sa + L::A_BYTES;
+                    const int r0 = t.row0 + c * ROWS;
+                    mbar_arrive_expect_tx(&full[stage], (a_chunks + b_chunks) * L::CHUNK_BYTES);
+                    for (int j = 0; j < a_chunks; ++j)
+                        tma_load_2d(sa + j * L::CHUNK_BYTES, &tmap_x, &full[stage], k0 + 64 * j, r0);
+                    for (int j = 0; j < b_chunks; ++j)
+                        tma_load_2d(sb + j * L::CHUNK_BYTES, &tmap_dy, &full[stage], n0 + 64 * j, r0);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                WaitGuard drain_guard = guard;
+                int dummy = 0;
+                drain_guard.abort = &dummy;
+                drain_guard.status = nullptr;
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer (+ tail zeroing)
+        constexpr uint32_t idesc = idesc_f16(TC_BM, BN, true, true, true, true);
+        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
+            const WgTile t = wg_decode(w, a.KT, a.NT, off);
+            const int nchunks_rows = (t.rows + ROWS - 1) / ROWS;
+            if (nchunks_rows == 0) continue;                 // empty group: the epilogue writes zeros
+            const bool free_acc = mbar_wait(&tempty[acc], acc_phase ^ 1, guard);
+            if (!__all_sync(0xffffffffu, free_acc)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int c = 0; c < nchunks_rows; ++c) {
+                const bool landed = mbar_wait(&full[stage], phase, guard);
+                if (!__all_sync(0xffffffffu, landed)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sa = smem + stage * L::STAGE_BYTES;
+                const int valid = min(ROWS, t.rows - c * ROWS);
+                if (valid < ROWS) {
+                    // rows [valid, 64) of this chunk belong to the next group (or lie past M):
+                    // zero them in every 64-wide chunk of both operands. A row is 128 contiguous
+                    // bytes of its chunk whatever the swizzle, which only permutes 16-byte units
+                    // inside the row.
+                    constexpr int CHUNKS = L::A_CHUNKS + L::B_CHUNKS;
+                    const int nstore = (ROWS - valid) * 8 * CHUNKS;
+                    for (int i = lane; i < nstore; i += 32) {
+                        const int chunk = i / ((ROWS - valid) * 8);
+                        const int rem = i - chunk * (ROWS - valid) * 8;
+                        const int row = valid + rem / 8;
+                        const int u = rem % 8;
+                        *reinterpret_cast<uint4*>(sa + chunk * L::CHUNK_BYTES + row * 128 + u * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sa);
+                    const uint32_t b_addr = a_addr + L::A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < ROWS / 16; ++kk) {
+                        // both operands MN-major: +2 groups of 8 contraction rows per K=16 step
+                        const uint64_t adesc = smem_desc_sw128(a_addr + kk * 2048, L::CHUNK_BYTES, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 2048, L::CHUNK_BYTES, 1024);
+                        mma_f16(d_tmem, adesc, bdesc, idesc, (c | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(&tfull[acc]);
+            __syncwarp();
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+        if (lane == 0) {
+            mma_commit(drain);
+            WaitGuard drain_guard = guard;
+            int dummy = 0;
+            drain_guard.abort = &dummy;
+            (void)mbar_wait(drain, 0, drain_guard);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int w = blockIdx.x; w < W; w += gridDim.x) {
+            const WgTile t = wg_decode(w, a.KT, a.NT, off);
+            const int k0 = t.kt * TC_BM, n0 = t.nt * BN;
+            const bool row_ok = k0 + r < a.K;
+            float* drow = a.dw + (static_cast<long long>(t.g) * a.K + k0 + r) * a.N;
+            if (t.rows <= 0) {
+                if (row_ok)
+                    for (int col = n0; col < min(a.N, n0 + BN); col += 4)
+                        *reinterpret_cast<float4*>(drow + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+                continue;
+            }
+            const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, v);
+                tmem_ld_wait();
+                const int col = n0 + c * 32;
+                if (row_ok && col < a.N) {
+                    float4* dst = reinterpret_cast<float4*>(drow + col);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (col + 4 * j < a.N)
+                            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_wg(const CUtensorMap& tx, const CUtensorMap& tdy, const WgradArgs& a, int grid,
+                      cudaStream_t stream) {
+    using L = WgLayout<BN, STAGES>;
+    const size_t shm = L::smem_bytes(a.G);
+    auto kern = wgrad_tc_kernel<BN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, THREADS, shm, stream>>>(tx, tdy, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int bn,
+                            int grid, cudaStream_t stream) {
+    if (bn == 256) return launch_wg<256, 4>(tmap_x, tmap_dy, a, grid, stream);
+    if (bn == 128) return launch_wg<128, 6>(tmap_x, tmap_dy, a, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rdot
