@@ -1,0 +1,104 @@
+"""Runs one librdot kernel on a reduced copy of a workload, for profilers.
+
+    python -m group_gemm_gb300.profile_case --kernel fwd --workload mixtral_bf16 --tokens 2048 --iters 3
+
+The group sizes follow the workload's routing recipe with ``--tokens`` tokens instead of the
+full batch; K, N and G are the workload's. One warm-up launch precedes ``--iters`` launches.
+Prints the mean launch time (CUDA events) so a plain run doubles as a quick timing.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    import torch
+
+    import group_gemm_gb300 as gg
+    import rdot_inputs as ri
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--kernel", choices=["fwd", "wgrad", "padded", "mxfp8"], default="fwd")
+    ap.add_argument("--workload", default="mixtral_bf16")
+    ap.add_argument("--tokens", type=int, default=2048)
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args()
+
+    gg.build()
+    dev = torch.device("cuda", 0)
+    cfg = ri.CONFIGS[args.workload]
+    k, n, g = cfg["k"], cfg["n"], cfg["g"]
+    topk = cfg["m"] // {"mixtral_bf16": 8192, "deepseek_bf16": 4096, "wgrad_bf16": 16384, "mxfp8": 8192}.get(
+        args.workload, cfg["m"])
+    if args.workload == "deepseek_bf16":
+        gs = ri.zipf_routed_group_sizes(args.tokens, g, topk, 1.1, seed=0, n_zero=8)
+    elif args.workload == "mxfp8":
+        gs = ri.zipf_routed_group_sizes(args.tokens, g, topk, 1.0, seed=0)
+    else:
+        sigma = 1.5 if args.workload == "wgrad_bf16" else 1.0
+        gs = ri.routed_group_sizes(args.tokens, g, topk, sigma, seed=0)
+    m = int(gs.sum())
+    gs_d = torch.from_numpy(gs).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    if args.kernel in ("fwd", "padded"):
+        lhs = ri.device_normal((m, k), 1, 1.0, dev, torch.bfloat16)
+        rhs = ri.device_normal((g, k, n), 2, 0.02, dev, torch.bfloat16)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        plan = gg.Plan(m, k, n, g, "forward", "bf16", "bf16")
+        if args.kernel == "fwd":
+            def run():
+                gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream)
+        else:
+            cap = -(-int(gs.max()) // 128) * 128
+            pad = torch.empty(gg.rdot_padded_workspace_size(plan.handle, cap), dtype=torch.uint8, device=dev)
+
+            def run():
+                gg.rdot_padded_forward(plan.handle, lhs, rhs, gs_d, out, cap, pad, plan.workspace, stream)
+        flops = 2.0 * m * k * n
+    elif args.kernel == "wgrad":
+        lhs = ri.device_normal((m, k), 1, 1.0, dev, torch.bfloat16)
+        dy = ri.device_normal((m, n), 2, 1.0, dev, torch.bfloat16)
+        dw = torch.empty((g, k, n), dtype=torch.float32, device=dev)
+        plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32")
+
+        def run():
+            gg.rdot_grad_weight(plan.handle, lhs, dy, gs_d, dw, plan.workspace, stream)
+        flops = 2.0 * m * k * n
+    else:
+        x = ri.device_normal((m, k), 1, 1.0, dev, torch.float32)
+        w = ri.device_normal((g, k, n), 2, 0.02, dev, torch.float32)
+        aq, as_ = ri.quantize_mx_e4m3(x, axis=1)
+        bq, bs = ri.quantize_mx_e4m3(w, axis=1)
+        del x, w
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16")
+
+        def run():
+            gg.rdot_forward_mxfp8(plan.handle, aq, as_, bq, bs, gs_d, out, plan.workspace, stream)
+        flops = 2.0 * m * k * n
+    run()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(args.iters):
+        run()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.iters
+    st = plan.status()
+    print(f"{args.kernel} {args.workload} tokens={args.tokens} M={m} K={k} N={n} G={g}: {ms:.4f} ms/launch, "
+          f"{flops / ms / 1e9:.1f} TFLOP/s, status={st}")
+    if st:
+        sys.exit(3)
+
+
+if __name__ == "__main__":
+    main()
