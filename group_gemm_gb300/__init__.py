@@ -22,7 +22,7 @@ __all__ = [
     "rdot_grad_weight", "rdot_padded_workspace_size", "rdot_padded_forward", "rdot_read_status",
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
-    "ragged_dot", "grad_weight", "ragged_dot_mxfp8", "padded_ragged_dot",
+    "rdot_forward_no_alloc", "ragged_dot", "grad_weight", "ragged_dot_mxfp8", "padded_ragged_dot",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "rdot_grad_weight", "rdot_padded_workspace_size", "rdot_padded_forward", "rdot_read_status",
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
+    "rdot_forward_no_alloc",
 )
 
 _DTYPE_CODES = {"f32": RDOT_F32, "bf16": RDOT_BF16, "e4m3": RDOT_E4M3}
@@ -100,6 +101,7 @@ def load():
             "rdot_status_string": ([st], ctypes.c_char_p),
             "rdot_last_cuda_error": ([], ctypes.c_char_p),
             "rdot_version": ([], ctypes.c_int),
+            "rdot_forward_no_alloc": ([vp, vp, vp, vp, vp, vp], st),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -204,6 +206,12 @@ def rdot_debug_wait_timeout(plan, timeout_ns: int, workspace, stream=None) -> No
 
 def rdot_set_wait_timeout(plan, timeout_ns: int) -> None:
     _check(load().rdot_set_wait_timeout(plan, int(timeout_ns)), "rdot_set_wait_timeout")
+
+
+def rdot_forward_no_alloc(plan, lhs, rhs, group_sizes, out, stream=None) -> None:
+    """Forward with the library's static device scratch instead of a caller workspace."""
+    _check(load().rdot_forward_no_alloc(plan, _ptr(lhs), _ptr(rhs), _ptr(group_sizes), _ptr(out),
+                                        _stream(stream, out.device)), "rdot_forward_no_alloc")
 
 
 def rdot_status_string(status: int) -> str:

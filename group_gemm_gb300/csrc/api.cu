@@ -73,6 +73,8 @@ struct DeviceGuard {
 
 }  // namespace
 
+void rdot::set_last_error(const std::string& text) { g_last_cuda_error = text; }
+
 struct rdot_plan_s {
     rdot_problem p{};
     int device = 0;
@@ -92,6 +94,8 @@ struct rdot_plan_s {
     int64_t pad_map_rows = 0;
     CUtensorMap pad_map_a{};
 };
+
+int rdot::plan_device(rdot_plan_t plan) { return plan->device; }
 
 namespace {
 

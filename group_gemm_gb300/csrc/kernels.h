@@ -5,7 +5,15 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
+#include "rdot.h"
+
 namespace rdot {
+
+// Host-side helpers shared by the C-ABI files (api.cu).
+void set_last_error(const std::string& text);   // text returned by rdot_last_cuda_error
+int plan_device(rdot_plan_t plan);              // the device a plan was made for
 
 // Arguments shared by the forward kernels (passed by value).
 struct FwdArgs {

@@ -185,6 +185,26 @@ RDOT_API rdot_status rdot_debug_wait_timeout(rdot_plan_t plan, uint64_t timeout_
 /* Overrides the device-side wait limit (ns) of the plan's kernels; 0 restores the default. */
 RDOT_API rdot_status rdot_set_wait_timeout(rdot_plan_t plan, uint64_t timeout_ns);
 
+/* Size of the static device scratch used by rdot_forward_no_alloc. */
+#define RDOT_NO_ALLOC_SCRATCH_BYTES 256
+
+/* Forward ragged-dot for callers that cannot allocate device memory. The pages have no
+ * counterpart: this entry point exists for callers such as plugins inside a framework whose
+ * memory manager owns the whole device heap, latency-critical code that cannot afford
+ * cudaMalloc's implicit synchronisation, or systems that must not allocate after start-up.
+ * Same arguments and results as rdot_forward, minus the workspace: the workspace lives in a
+ * RDOT_NO_ALLOC_SCRATCH_BYTES-byte static __device__ array that the library holds on every GPU
+ * where it is loaded, until the process exits. Plans needing a larger workspace are rejected
+ * with RDOT_ERR_UNSUPPORTED (the reason is in rdot_last_cuda_error). Nothing is allocated:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make this first call before any stream capture.
+ *   - Every call shares the one array. Each call first clears it on `stream`, so the device
+ *     status bits of earlier calls are not kept. Calls that overlap on the GPU (different
+ *     streams, or different host threads) race on the array. */
+RDOT_API rdot_status rdot_forward_no_alloc(rdot_plan_t plan, const void* lhs, const void* rhs,
+                                           const int32_t* group_sizes, void* out, void* stream);
+
 /* Human-readable status name. */
 RDOT_API const char* rdot_status_string(rdot_status status);
 
