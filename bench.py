@@ -281,44 +281,104 @@ def bench_ours(args, rank, world, barrier):
     del lhs, rhs, out, lhs_h, out_h, lhs_d2
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_extras:
-        result["per_config"] = extra_configs(args, dev, peaks, name)
+        try:
+            result["per_config"] = extra_configs(args, dev, peaks, name)
+        except Exception as e:  # a failing extra must not hide the main line
+            result["per_config"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_leg(name, args.cpu_seconds)
     return result
 
 
+def _time_steps(fn, steps, stream):
+    for _ in range(3):
+        fn()
+    return time_region(fn, steps, stream, lambda: None) / steps
+
+
 def extra_configs(args, dev, peaks, main_name):
-    """The other bf16 forward workloads, measured the same way with fewer steps."""
+    """The other workloads of the suite, measured the same way with fewer steps: the bf16
+    forwards (with the padded-dense baseline beside them), the weight gradient and MXFP8."""
     import torch
     import group_gemm_gb300 as gg
     res = {}
+    stream = torch.cuda.current_stream(dev)
+    steps = max(5, min(args.steps, 30))
     for name in ("mixtral_bf16", "deepseek_bf16"):
-        if name == main_name:
-            continue
         cfg, gs, lhs, rhs = make_forward_inputs(name, dev)
         m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
         plan = gg.Plan(m, k, n, g, "forward", cfg["in_dtype"], cfg["out_dtype"], device=dev.index)
         gs_d = torch.from_numpy(gs).to(dev)
         out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        stream = torch.cuda.current_stream(dev)
-
-        def step():
-            gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream)
-
-        for _ in range(3):
-            step()
-        steps = max(5, min(args.steps, 30))
-        t = time_region(step, steps, stream, lambda: None) / steps
         fl = useful_flops(gs, k, n)
-        nz = int(np.count_nonzero(gs))
-        min_bytes = (nz * k * n + int(gs.sum()) * k + m * n) * 2
-        res[name] = {"tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
-                     "frac_of_bf16_peak": round(fl / t / 1e12 / peaks["bf16_tflops"], 4),
-                     "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1),
-                     "frac_of_hbm": round(min_bytes / t / 1e9 / peaks["hbm_gbs"], 4),
-                     "status": plan.status()}
-        del lhs, rhs, out
+        entry = {}
+        if name != main_name:
+            t = _time_steps(lambda: gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream),
+                            steps, stream)
+            nz = int(np.count_nonzero(gs))
+            min_bytes = (nz * k * n + int(gs.sum()) * k + m * n) * 2
+            entry.update({"tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
+                          "frac_of_bf16_peak": round(fl / t / 1e12 / peaks["bf16_tflops"], 4),
+                          "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1),
+                          "frac_of_hbm": round(min_bytes / t / 1e9 / peaks["hbm_gbs"], 4)})
+        else:
+            t = None
+        # padded-dense baseline: every group padded to the largest group (rounded up to 128 rows)
+        cap = -(-int(gs.max()) // 128) * 128
+        pad = torch.empty(gg.rdot_padded_workspace_size(plan.handle, cap), dtype=torch.uint8, device=dev)
+        tp = _time_steps(lambda: gg.rdot_padded_forward(plan.handle, lhs, rhs, gs_d, out, cap, pad, plan.workspace,
+                                                        stream), max(3, steps // 5), stream)
+        entry.update({"padded_ms": round(tp * 1e3, 3), "padded_tflops_useful": round(fl / tp / 1e12, 3),
+                      "padded_capacity": cap, "padded_flops_ratio": round(g * cap / float(gs.sum()), 3)})
+        if t is not None:
+            entry["speedup_vs_padded"] = round(tp / t, 3)
+        entry["status"] = plan.status()
+        res[name] = entry
+        del lhs, rhs, out, pad
         torch.cuda.empty_cache()
+    # weight gradient
+    cfg = ri.CONFIGS["wgrad_bf16"]
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    gs = ri.config_group_sizes("wgrad_bf16")
+    lhs = ri.device_normal((m, k), 1000, 1.0, dev, torch.bfloat16)
+    dy = ri.device_normal((m, n), 2000, 1.0, dev, torch.bfloat16)
+    dw = torch.empty((g, k, n), dtype=torch.float32, device=dev)
+    plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", device=dev.index)
+    gs_d = torch.from_numpy(gs).to(dev)
+    t = _time_steps(lambda: gg.rdot_grad_weight(plan.handle, lhs, dy, gs_d, dw, plan.workspace, stream), steps,
+                    stream)
+    fl = useful_flops(gs, k, n)
+    min_bytes = 2 * m * (k + n) + 4 * g * k * n
+    res["wgrad_bf16"] = {"tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
+                         "frac_of_bf16_peak": round(fl / t / 1e12 / peaks["bf16_tflops"], 4),
+                         "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1), "status": plan.status()}
+    del lhs, dy, dw
+    torch.cuda.empty_cache()
+    # MXFP8 forward
+    cfg = ri.CONFIGS["mxfp8"]
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    gs = ri.config_group_sizes("mxfp8")
+    x = ri.device_normal((m, k), 1000, 1.0, dev, torch.float32)
+    aq, as_ = ri.quantize_mx_e4m3(x, axis=1)
+    del x
+    w = ri.device_normal((g, k, n), 2000, 0.02, dev, torch.float32)
+    bq, bs = ri.quantize_mx_e4m3(w, axis=1)
+    del w
+    torch.cuda.empty_cache()
+    plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16", device=dev.index)
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    gs_d = torch.from_numpy(gs).to(dev)
+    t = _time_steps(lambda: gg.rdot_forward_mxfp8(plan.handle, aq, as_, bq, bs, gs_d, out, plan.workspace, stream),
+                    steps, stream)
+    fl = useful_flops(gs, k, n)
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    min_bytes = m * k + g * k * n + (m * k + g * k * n) // 32 + 2 * m * n
+    res["mxfp8"] = {"tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
+                    "frac_of_fp8_peak_assumed_2x_bf16": round(fl / t / 1e12 / fp8_peak, 4),
+                    "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1), "status": plan.status(),
+                    "note": "FP8 peak not measured on this pool; taken as 2x the measured bf16 burst peak"}
+    del aq, as_, bq, bs, out
+    torch.cuda.empty_cache()
     return res
 
 

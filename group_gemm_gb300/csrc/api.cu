@@ -80,7 +80,7 @@ struct rdot_plan_s {
     int device = 0;
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
-    int kind = 0;          // 0: SIMT fp32 forward, 1: tcgen05 bf16 forward, 2: tcgen05 grad-weight
+    int kind = 0;          // 0: SIMT fp32 forward, 1: tcgen05 bf16 forward, 2: tcgen05 grad-weight, 3: MXFP8
     int tile_m = 0, tile_n = 0;
     int m_inner = 1;
     int grid = 1;
@@ -164,7 +164,9 @@ rdot_status check_problem(const rdot_problem* p) {
             if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;
             return RDOT_OK;
         case RDOT_MODE_FORWARD_MXFP8:
-            return RDOT_ERR_UNSUPPORTED;
+            if (p->in_dtype != RDOT_E4M3 || p->out_dtype != RDOT_BF16) return RDOT_ERR_UNSUPPORTED;
+            if (p->k % 32 || p->n % 16) return RDOT_ERR_UNSUPPORTED;   // MX block 32; 16-byte row pitch
+            return RDOT_OK;
         default:
             return RDOT_ERR_INVALID_ARG;
     }
@@ -224,6 +226,21 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             return RDOT_ERR_UNSUPPORTED;
         }
         pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
+    } else if (p.mode == RDOT_MODE_FORWARD_MXFP8) {
+        if (prop.major != 10) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->kind = 3;
+        pl->tile_m = TC_BM;
+        pl->tile_n = MX_BN;
+        const int nt = static_cast<int>((p.n + MX_BN - 1) / MX_BN);
+        const long long bound = forward_tile_bound(p.m, p.groups, TC_BM, nt);
+        if (bound > 0x7fffffffLL) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
     } else if (p.mode == RDOT_MODE_GRAD_WEIGHT) {
         if (prop.major != 10) {
             delete pl;
@@ -252,9 +269,28 @@ rdot_status rdot_plan_destroy(rdot_plan_t plan) {
     return RDOT_OK;
 }
 
+namespace {
+// MXFP8 workspace: status word, then the reordered scale blocks.
+struct MxLayout {
+    size_t sfa_off, sfb_off, total;
+    int ks, nt;
+};
+
+MxLayout mx_layout(const rdot_problem& p) {
+    MxLayout l{};
+    l.ks = static_cast<int>((p.k + 127) / 128);
+    l.nt = static_cast<int>((p.n + MX_BN - 1) / MX_BN);
+    const size_t mtiles = static_cast<size_t>((p.m + TC_BM - 1) / TC_BM) + static_cast<size_t>(p.groups);
+    l.sfa_off = kWorkspaceBytes;
+    l.sfb_off = l.sfa_off + mtiles * l.ks * MX_SFA_BLOCK_BYTES;
+    l.total = l.sfb_off + static_cast<size_t>(p.groups) * l.nt * l.ks * MX_SFB_BLOCK_BYTES;
+    return l;
+}
+}  // namespace
+
 rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes) {
     if (!plan || !bytes) return RDOT_ERR_INVALID_ARG;
-    *bytes = kWorkspaceBytes;
+    *bytes = plan->kind == 3 ? mx_layout(plan->p).total : kWorkspaceBytes;
     return RDOT_OK;
 }
 
@@ -325,10 +361,47 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
 rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t* lhs_scale, const void* rhs,
                                const uint8_t* rhs_scale, const int32_t* group_sizes, void* out, void* workspace,
                                void* stream) {
-    (void)lhs; (void)lhs_scale; (void)rhs; (void)rhs_scale; (void)group_sizes; (void)out; (void)workspace;
-    (void)stream;
-    if (!plan) return RDOT_ERR_INVALID_ARG;
-    return RDOT_ERR_UNSUPPORTED;
+    if (!plan || !group_sizes || !workspace) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.mode != RDOT_MODE_FORWARD_MXFP8 || plan->kind != 3) return RDOT_ERR_INVALID_ARG;
+    if (p.m == 0) return RDOT_OK;
+    if (!lhs || !rhs || !out || !lhs_scale || !rhs_scale) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+        (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan->map_lhs_ptr != lhs) {
+        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, lhs, p.k, p.m, p.k, 128, 128);
+        if (st != RDOT_OK) return st;
+        plan->map_lhs_ptr = lhs;
+    }
+    if (plan->map_rhs_ptr != rhs) {
+        rdot_status st = encode_3d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, rhs, p.n, p.k, p.groups, p.n,
+                                   p.k * p.n, 128, 128, 1);
+        if (st != RDOT_OK) return st;
+        plan->map_rhs_ptr = rhs;
+    }
+    const MxLayout l = mx_layout(p);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    MxArgs a{};
+    a.out = out;
+    a.M = static_cast<int>(p.m);
+    a.K = static_cast<int>(p.k);
+    a.N = static_cast<int>(p.n);
+    a.G = p.groups;
+    a.NT = l.nt;
+    a.KS = l.ks;
+    a.m_inner = plan->m_inner;
+    a.sfa = ws + l.sfa_off;
+    a.sfb = ws + l.sfb_off;
+    a.status = static_cast<int32_t*>(workspace);
+    a.timeout_ns = plan->timeout_ns;
+    cudaError_t e = launch_mxfp8(plan->map_a, plan->map_b, lhs_scale, rhs_scale, group_sizes, a, plan->grid,
+                                 4 * plan->sm_count, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mxfp8 launch");
+    return RDOT_OK;
 }
 
 rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, const int32_t* group_sizes,

@@ -59,6 +59,28 @@ struct WgradArgs {
 cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int bn,
                             int grid, cudaStream_t stream);
 
+// MXFP8 forward (mxfp8_tc.cu): 128x128 tiles, K stages of 128 E4M3 bytes (4 scale blocks).
+constexpr int MX_BN = 128;
+constexpr int MX_SFA_BLOCK_BYTES = 2048;   // 128 rows x 16 bytes per (m-tile, K stage)
+constexpr int MX_SFB_BLOCK_BYTES = 512;    // 128 columns x 4 scales per (group, n-tile, K stage)
+
+struct MxArgs {
+    void* out;                   // device bf16 [M, N]
+    int M, K, N, G;
+    int NT, KS;                  // column tiles, K stages of 128
+    int m_inner;
+    uint8_t* sfa;                // workspace: reordered lhs scales, [m-tiles, KS] blocks
+    uint8_t* sfb;                // workspace: reordered rhs scales, [G, NT, KS] blocks
+    int32_t* status;
+    uint64_t timeout_ns;
+};
+
+// tmap_a: lhs codes [M, K] uint8, box (128, 128); tmap_b: rhs codes [G, K, N] uint8 as (N, K, G),
+// box (128, 128, 1); both 128-byte swizzled. Launches the scale reorder, then the GEMM.
+cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const uint8_t* lhs_scale,
+                         const uint8_t* rhs_scale, const int32_t* group_sizes, const MxArgs& a, int grid,
+                         int prep_grid, cudaStream_t stream);
+
 // Padded-dense baseline data movement (padded.cu).
 cudaError_t launch_pad_scatter(const void* lhs, const int32_t* gs, void* lhs_pad, int32_t* uniform_gs, int M, int G,
                                int C, long long row_bytes, int grid, int32_t* status, cudaStream_t stream);

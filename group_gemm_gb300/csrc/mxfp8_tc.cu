@@ -1,0 +1,339 @@
+// mxfp8_tc.cu -- MXFP8 ragged-dot forward on the sm_103a block-scaled tensor cores.
+//
+// What it computes (AITER PR #5658 "Merge MoE MXFP8 GEMM into existing _moe_gemm_a8w8 kernel",
+// with follow-ups #5831/#5832): lhs and rhs hold OCP E4M3 codes; every 32 consecutive elements
+// along K share one E8M0 scale (value 2^(s-127)); the element value is decode(code) * scale, and
+// out[rows of g, :] = A[rows of g, :] @ B[g] with fp32 accumulation and bf16 output. Rows past the
+// last group end are zero, as in the bf16 forward.
+//
+// On sm_103a the scale is applied inside the MMA (tcgen05.mma kind::mxf8f6f4.block_scale,
+// scale_vec::1X), so the operands stay FP8 in shared memory: one MMA covers K = 32 = one scale
+// block, and the scale-factor ids of the instruction descriptor pick the block's byte out of the
+// 32-bit scale column in tensor memory.
+//
+// Two kernels per call:
+//   mx_prep_kernel   reorders the caller's scales ([M, K/32] and [G, K/32, N]) into one small
+//                    block per (tile, K stage of 128) in the workspace, in the order the
+//                    tensor-memory copies want: A blocks are 128 rows x 16 bytes with the row's 4
+//                    scales repeated in each 4-byte column; B blocks are 128 columns x 4 scales as
+//                    32 rows x 16 bytes (byte 16*(n%32) + 4*(n/32) + kblock).
+//   mxfp8_tc_kernel  persistent, warp-specialised like the bf16 forward: warp 0 brings the codes by
+//                    TMA (lhs [128 x 128 B] K-major, rhs [128 K x 128 N] MN-major, 128-byte
+//                    swizzle) and the scale blocks by bulk copy; warp 1 copies the scale blocks to
+//                    tensor memory (tcgen05.cp) and issues four M=128 N=128 K=32 MMAs per stage;
+//                    warps 2..5 run the ragged bf16 epilogue.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace rdot {
+
+namespace {
+
+constexpr int THREADS = 192;
+constexpr int BM = 128;
+constexpr int BN = MX_BN;
+constexpr int BKB = 128;            // K bytes (= elements) per stage: 4 scale blocks
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BKB;   // 16 KB
+constexpr int B_BYTES = BKB * BN;   // 16 KB
+constexpr int SFA_BYTES = MX_SFA_BLOCK_BYTES;   // 2 KB
+constexpr int SFB_BYTES = MX_SFB_BLOCK_BYTES;   // 512 B
+constexpr int STAGE_BYTES = 35840;              // A + B + SFA + SFB rounded up to 1 KB
+static_assert(A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES <= STAGE_BYTES, "stage layout");
+constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
+constexpr int MISC_BYTES = 16;
+constexpr int TMEM_COLS = 512;      // 2 accumulators of 128 columns + 8 scale columns per stage
+constexpr int TMEM_SF_BASE = 2 * BN;
+
+size_t smem_bytes(int G) { return 1024 + RING_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1); }
+
+__device__ __forceinline__ uint32_t scale_word(const uint8_t* p, int avail) {
+    // four consecutive E8M0 bytes; blocks past K read as 127 (2^0): their codes are zero-filled
+    uint32_t w = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w |= static_cast<uint32_t>(j < avail ? __ldg(p + j) : 127u) << (8 * j);
+    return w;
+}
+
+__global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict__ lhs_scale,
+                                                      const uint8_t* __restrict__ rhs_scale,
+                                                      const int32_t* __restrict__ gs, MxArgs a) {
+    extern __shared__ int32_t table[];
+    int32_t* off = table;
+    int32_t* mt_prefix = table + a.G + 1;
+    if (threadIdx.x < 32) (void)group_scan_warp(gs, a.G, a.M, BM, 1, off, mt_prefix);
+    __syncthreads();
+    const int KB32 = a.K / 32;
+    const long long Tm = mt_prefix[a.G];
+    const long long sfa_blocks = Tm * a.KS;
+    const long long sfb_blocks = static_cast<long long>(a.G) * a.NT * a.KS;
+    const int lane = threadIdx.x & 31;
+    const long long warp0 = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+    for (long long b = warp0; b < sfa_blocks + sfb_blocks; b += nwarps) {
+        if (b < sfa_blocks) {
+            const int T = static_cast<int>(b / a.KS);
+            const int ks = static_cast<int>(b - static_cast<long long>(T) * a.KS);
+            int lo = 0, hi = a.G - 1;   // group of m-tile T: largest g with mt_prefix[g] <= T
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (mt_prefix[mid] <= T) lo = mid;
+                else hi = mid - 1;
+            }
+            const int row0 = off[lo] + (T - mt_prefix[lo]) * BM;
+            const int rows = min(BM, off[lo + 1] - row0);
+            const int avail = min(4, KB32 - 4 * ks);
+            uint4* dst = reinterpret_cast<uint4*>(a.sfa + b * SFA_BYTES);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = lane + 32 * i;
+                uint32_t w = 0x7f7f7f7fu;
+                if (r < rows) w = scale_word(lhs_scale + static_cast<long long>(row0 + r) * KB32 + 4 * ks, avail);
+                dst[r] = make_uint4(w, w, w, w);
+            }
+        } else {
+            const long long bb = b - sfa_blocks;
+            const int ks = static_cast<int>(bb % a.KS);
+            const long long gn = bb / a.KS;
+            const int nt = static_cast<int>(gn % a.NT);
+            const int g = static_cast<int>(gn / a.NT);
+            const int avail = min(4, KB32 - 4 * ks);
+            uint32_t* dst = reinterpret_cast<uint32_t*>(a.sfb + bb * SFB_BYTES);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int nl = lane + 32 * j;
+                const int n = nt * BN + nl;
+                uint32_t w = 0x7f7f7f7fu;
+                if (n < a.N) {
+                    w = 0;
+                    const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + n;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        w |= static_cast<uint32_t>(q < avail ? __ldg(src + static_cast<long long>(q) * a.N) : 127u)
+                             << (8 * q);
+                }
+                dst[4 * lane + j] = w;   // byte 16*(n%32) + 4*(n/32) + kblock
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    mxfp8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const int32_t* __restrict__ group_sizes, MxArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + BAR_BYTES + MISC_BYTES);
+    int32_t* tprefix = off + a.G + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 128);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 2) {
+        const int bad = group_scan_warp(group_sizes, a.G, a.M, BM, a.NT, off, tprefix);
+        if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *tmem_holder;
+    const int W = tprefix[a.G];
+    const bool m_inner = a.m_inner != 0;
+    const WaitGuard guard{abort_flag, a.status, a.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
+                const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
+                const long long mtile = tprefix[t.g] / a.NT + t.mt;
+                const uint8_t* sfa_src = a.sfa + mtile * a.KS * SFA_BYTES;
+                const uint8_t* sfb_src = a.sfb + (static_cast<long long>(t.g) * a.NT + t.nt) * a.KS * SFB_BYTES;
+                for (int ks = 0; ks < a.KS; ++ks) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
+                    tma_load_2d(st, &tmap_a, &full[stage], ks * BKB, t.row0);
+                    tma_load_3d(st + A_BYTES, &tmap_b, &full[stage], t.nt * BN, ks * BKB, t.g);
+                    bulk_load(st + A_BYTES + B_BYTES, sfa_src + static_cast<long long>(ks) * SFA_BYTES, SFA_BYTES,
+                              &full[stage]);
+                    bulk_load(st + A_BYTES + B_BYTES + SFA_BYTES, sfb_src + static_cast<long long>(ks) * SFB_BYTES,
+                              SFB_BYTES, &full[stage]);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                WaitGuard drain_guard = guard;
+                int dummy = 0;
+                drain_guard.abort = &dummy;
+                drain_guard.status = nullptr;
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, guard)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int ks = 0; ks < a.KS; ++ks) {
+                    if (!mbar_wait(&full[stage], phase, guard)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t sfa_t = tmem_base + TMEM_SF_BASE + 8 * stage;
+                    const uint32_t sfb_t = sfa_t + 4;
+                    tmem_cp_128x128b(sfa_t, smem_desc_rows16(sb + B_BYTES));
+                    tmem_cp_32x128b_warpx4(sfb_t, smem_desc_rows16(sb + B_BYTES + SFA_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < BKB / 32; ++kk) {
+                        // A K-major: +32 bytes per 32-element K step; B MN-major: +32 K rows of 128 B
+                        const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 4096, B_BYTES, 1024);
+                        mma_mxf8(d_tmem, adesc, bdesc, idesc_mxf8(BM, BN, false, true, kk, kk), sfa_t, sfb_t,
+                                 (ks | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            mma_commit(drain);
+            WaitGuard drain_guard = guard;
+            int dummy = 0;
+            drain_guard.abort = &dummy;
+            (void)mbar_wait(drain, 0, drain_guard);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int w = blockIdx.x; w < W; w += gridDim.x) {
+            const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
+            const int n0 = t.nt * BN;
+            const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            const bool row_ok = r < t.rows;
+            const long long orow = static_cast<long long>(t.row0 + r) * a.N;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, v);
+                tmem_ld_wait();
+                const int col = n0 + c * 32;
+                if (row_ok && col < a.N) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + col);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (col + 8 * j < a.N) {
+                            uint4 p;
+                            p.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                            p.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                            p.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                            p.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                            dst[j] = p;
+                        }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+        {
+            const long long b0 = static_cast<long long>(off[a.G]) * a.N * 2;
+            const long long b1 = static_cast<long long>(a.M) * a.N * 2;
+            const long long nv = (b1 - b0) / 16;
+            if (nv > 0) {
+                uint4* base = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + b0);
+                const long long per = (nv + gridDim.x - 1) / gridDim.x;
+                const long long s = per * blockIdx.x;
+                const long long e = min(nv, s + per);
+                for (long long i = s + (threadIdx.x - 64); i < e; i += 128) base[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const uint8_t* lhs_scale,
+                         const uint8_t* rhs_scale, const int32_t* group_sizes, const MxArgs& a, int grid,
+                         int prep_grid, cudaStream_t stream) {
+    const size_t prep_shm = sizeof(int32_t) * 2 * (a.G + 1);
+    mx_prep_kernel<<<prep_grid, 256, prep_shm, stream>>>(lhs_scale, rhs_scale, group_sizes, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t shm = smem_bytes(a.G);
+    e = cudaFuncSetAttribute(mxfp8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
+    if (e != cudaSuccess) return e;
+    mxfp8_tc_kernel<<<grid, THREADS, shm, stream>>>(tmap_a, tmap_b, group_sizes, a);
+    return cudaGetLastError();
+}
+
+}  // namespace rdot

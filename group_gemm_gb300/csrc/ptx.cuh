@@ -152,6 +152,50 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
+// D (tmem, fp32) (+)= (A * scale_A) (B * scale_B), kind::mxf8f6f4 with one E8M0 scale per 32 K
+// elements (scale_vec::1X). sfa/sfb are TMEM addresses of the scale columns; the byte inside each
+// 32-bit column is chosen by the scale-factor ids in the instruction descriptor.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Shared memory -> tensor memory copies (issued by one thread; ordered with later tcgen05.mma of
+// the same thread). 128x128b: 128 rows of 16 bytes to lanes 0..127, 4 columns. 32x128b.warpx4:
+// 32 rows of 16 bytes to lanes 0..31 of each of the four lane quarters, 4 columns.
+__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Non-swizzled shared-memory descriptor: rows of 16 bytes, 8-row core matrices contiguous
+// (SBO = 128 bytes between consecutive core matrices).
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+    d |= static_cast<uint64_t>((2048u >> 4) & 0x3FFF) << 16;
+    d |= static_cast<uint64_t>((128u >> 4) & 0x3FFF) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` on the mbarrier. Both addresses 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // 32 lanes x 32 columns of 32-bit words: thread t of the warp receives TMEM lane
 // (lane base + t), columns [col, col + 32).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -202,6 +246,17 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool a_bf16, bool
     return (1u << 4) | ((a_bf16 ? 1u : 0u) << 7) | ((b_bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
            ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
            (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scaling (32 bits):
+//   [4,6) B scale-factor id (byte of the 32-bit scale column), [7,10) A format (0 = E4M3),
+//   [10,13) B format, [15] A major, [16] B major, [17,23) N >> 3, [23] scale type (1 = UE8M0),
+//   [24,29) M >> 4, [29,31) A scale-factor id. D is always fp32.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int m, int n, bool a_mn_major, bool b_mn_major, uint32_t sfa_id,
+                                                  uint32_t sfb_id) {
+    return ((sfb_id & 3u) << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24) |
+           ((sfa_id & 3u) << 29);
 }
 
 // ------------------------------------------------------------------------------ packing

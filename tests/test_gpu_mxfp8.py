@@ -1,0 +1,89 @@
+"""GPU parity of the MXFP8 forward (E4M3 codes, E8M0 scale per 32 K elements, bf16 out) through
+the C ABI against the fp64 oracle on the same bytes: max |d| / (|ref| + 1) <= 1e-2.
+
+The cases separate the parts that can go wrong: unit scales exercise the FP8 codes alone; then
+only the lhs scales vary; then only the rhs scales; then both, on ragged shapes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import group_gemm_gb300 as gg
+import oracle
+import rdot_inputs as ri
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gg.build()
+    gg.load()
+
+
+def rel_err(got, ref):
+    got = got.detach().to("cpu", torch.float64).numpy()
+    return float(np.max(np.abs(got - ref) / (np.abs(ref) + 1.0))) if ref.size else 0.0
+
+
+def make_case(m, k, n, gs, seed, vary=("a", "b")):
+    x = torch.from_numpy(ri.host_normal((m, k), seed))
+    w = torch.from_numpy(ri.host_normal((len(gs), k, n), seed + 1, 0.02))
+    aq, as_ = ri.quantize_mx_e4m3(x, axis=1)
+    bq, bs = ri.quantize_mx_e4m3(w, axis=1)
+    gen = torch.Generator().manual_seed(seed + 2)
+    if "a" in vary:
+        as_ = (as_.to(torch.int32) + torch.randint(-4, 5, as_.shape, generator=gen)).clamp(100, 150).to(torch.uint8)
+    else:
+        as_ = torch.full_like(as_, 127)
+    if "b" in vary:
+        bs = (bs.to(torch.int32) + torch.randint(-4, 5, bs.shape, generator=gen)).clamp(100, 150).to(torch.uint8)
+    else:
+        bs = torch.full_like(bs, 127)
+    return aq, as_, bq, bs, np.asarray(gs, np.int32)
+
+
+def run(aq, as_, bq, bs, gs):
+    m, k = aq.shape
+    g, _, n = bq.shape
+    plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16")
+    ws = torch.zeros(gg.rdot_workspace_size(plan.handle), dtype=torch.uint8, device=DEV)
+    out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gg.rdot_forward_mxfp8(plan.handle, aq.to(DEV), as_.to(DEV), bq.to(DEV), bs.to(DEV),
+                          torch.from_numpy(gs).to(DEV), out, ws)
+    status = gg.rdot_read_status(plan.handle, ws)
+    return out, status
+
+
+@pytest.mark.parametrize("vary", [(), ("a",), ("b",), ("a", "b")])
+def test_mxfp8_scale_axes(vary):
+    aq, as_, bq, bs, gs = make_case(256, 256, 256, [128, 128], 5, vary)
+    out, status = run(aq, as_, bq, bs, gs)
+    ref = oracle.forward_mxfp8(aq, as_, bq, bs, gs)
+    assert status == 0
+    assert rel_err(out, ref) <= TOL
+
+
+@pytest.mark.parametrize("m,k,n,gs", [
+    (300, 128, 128, [300]),                       # G = 1, ragged tail
+    (420, 96, 144, [130, 0, 77, 200, 5]),         # K = 96 (3 of 4 scale blocks), N = 144, empty group
+    (512, 32, 256, [0, 256, 256, 0]),             # K = 32 (one scale block)
+    (1000, 512, 384, [0, 313, 1, 0, 257, 300, 129]),
+])
+def test_mxfp8_ragged_parity(m, k, n, gs):
+    aq, as_, bq, bs, gs = make_case(m, k, n, gs, 17)
+    total = int(gs.sum())
+    aq[total:] = 0x7F                             # E4M3 NaN codes past the sum must never leak
+    out, status = run(aq, as_, bq, bs, gs)
+    ref = oracle.forward_mxfp8(aq, as_, bq, bs, gs)
+    assert status == 0
+    assert rel_err(out, ref) <= TOL
+    assert torch.all(out[total:] == 0)
+
+
+def test_mxfp8_workspace_is_reported():
+    plan = gg.Plan(65536, 4096, 1536, 128, "forward_mxfp8", "e4m3", "bf16")
+    ws = gg.rdot_workspace_size(plan.handle)
+    assert ws > 256   # scale blocks live in the workspace
