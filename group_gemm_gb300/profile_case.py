@@ -30,16 +30,17 @@ def main():
     ap.add_argument("--workload", default="mixtral_bf16")
     ap.add_argument("--tokens", type=int, default=2048)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--groups", type=int, default=0, help="override the workload's expert count")
     args = ap.parse_args()
 
     gg.build()
     dev = torch.device("cuda", 0)
     cfg = ri.CONFIGS[args.workload]
-    k, n, g = cfg["k"], cfg["n"], cfg["g"]
+    k, n, g = cfg["k"], cfg["n"], (args.groups or cfg["g"])
     topk = cfg["m"] // {"mixtral_bf16": 8192, "deepseek_bf16": 4096, "wgrad_bf16": 16384, "mxfp8": 8192}.get(
         args.workload, cfg["m"])
     if args.workload == "deepseek_bf16":
-        gs = ri.zipf_routed_group_sizes(args.tokens, g, topk, 1.1, seed=0, n_zero=8)
+        gs = ri.zipf_routed_group_sizes(args.tokens, g, topk, 1.1, seed=0, n_zero=min(8, g - topk))
     elif args.workload == "mxfp8":
         gs = ri.zipf_routed_group_sizes(args.tokens, g, topk, 1.0, seed=0)
     else:
