@@ -396,6 +396,8 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
     a.m_inner = plan->m_inner;
     a.sfa = ws + l.sfa_off;
     a.sfb = ws + l.sfb_off;
+    a.sfb_vec = (p.n % 4 == 0 && (reinterpret_cast<uintptr_t>(rhs_scale) & 3u) == 0) ? 1 : 0;
+    a.sfa_vec = (p.k % 128 == 0 && (reinterpret_cast<uintptr_t>(lhs_scale) & 3u) == 0) ? 1 : 0;
     a.status = static_cast<int32_t*>(workspace);
     a.timeout_ns = plan->timeout_ns;
     cudaError_t e = launch_mxfp8(plan->map_a, plan->map_b, lhs_scale, rhs_scale, group_sizes, a, plan->grid,

@@ -1,0 +1,69 @@
+// epilogue.cuh -- coalesced stores of accumulator blocks read from tensor memory.
+//
+// tcgen05.ld with the 32x32b shape hands each lane one accumulator row (32 consecutive columns).
+// Storing straight from there makes every warp store touch 32 different rows, writing half
+// sectors. Instead each warp transposes its 32 x 32 block through a private shared-memory tile
+// (padded rows, conflict-free) and stores it with lanes running along the rows: fp32 blocks go
+// out as 4 rows x 128 bytes per instruction, bf16 blocks as 8 rows x 64 bytes, so DRAM sees whole
+// sectors and full lines.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace rdot {
+
+// shared-memory words each epilogue warp needs for one 32 x 32 block
+template <bool F32>
+struct EpiStage {
+    static constexpr int ROW_WORDS = F32 ? 33 : 17;   // 32 fp32 or 16 bf16x2 words + 1 pad
+    static constexpr int WORDS = 32 * ROW_WORDS;
+    static constexpr int BYTES = WORDS * 4;
+};
+
+// v[j] = accumulator element (row = lane, column j) of a 32 x 32 block whose first element is
+// out[0] (row pitch ld elements). Rows >= rows_valid and columns >= cols_valid are not stored
+// (cols_valid is a multiple of 8). Must be called by all 32 lanes of the warp.
+template <bool F32>
+__device__ __forceinline__ void store_block_32x32(const uint32_t (&v)[32], uint32_t* stage, void* out, long long ld,
+                                                  int rows_valid, int cols_valid) {
+    using S = EpiStage<F32>;
+    const int lane = threadIdx.x & 31;
+    if (F32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) stage[lane * S::ROW_WORDS + j] = v[j];
+        __syncwarp();
+        const int rr = lane >> 3, c4 = (lane & 7) * 4;
+        float* o = static_cast<float*>(out);
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int row = it * 4 + rr;
+            if (row < rows_valid && c4 < cols_valid) {
+                const uint32_t* s = stage + row * S::ROW_WORDS + c4;
+                *reinterpret_cast<float4*>(o + row * ld + c4) =
+                    make_float4(__uint_as_float(s[0]), __uint_as_float(s[1]), __uint_as_float(s[2]),
+                                __uint_as_float(s[3]));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            stage[lane * S::ROW_WORDS + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        __syncwarp();
+        const int rr = lane >> 2, w4 = (lane & 3) * 4;
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int row = it * 8 + rr;
+            if (row < rows_valid && 2 * w4 < cols_valid) {
+                const uint32_t* s = stage + row * S::ROW_WORDS + w4;
+                *reinterpret_cast<uint4*>(o + row * ld + 2 * w4) = make_uint4(s[0], s[1], s[2], s[3]);
+            }
+        }
+    }
+    __syncwarp();
+}
+
+}  // namespace rdot

@@ -13,8 +13,9 @@
 //               tcgen05.mma kind::f16 (M=128, N=BN, K=16) from one thread; tcgen05.commit frees
 //               each smem stage and, after the last K block, signals "accumulator full".
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, fp32 -> bf16 (round to nearest
-//               even) or fp32, 16-byte stores of the rows that belong to the group; then mark
-//               the accumulator empty so the MMA warp can start the tile after next.
+//               even) or fp32, transposed through shared memory and stored as whole lines, only
+//               the rows that belong to the group; then mark the accumulator empty so the MMA
+//               warp can start the tile after next.
 // The two accumulators let the epilogue of tile i overlap the mainloop of tile i+1.
 //
 // Ragged rows: a tile starts at a group's start row + 128*mt and its TMA box may run into the
@@ -23,6 +24,7 @@
 // or N columns past the tensor come back zero-filled from TMA.
 #include <cuda_bf16.h>
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -33,18 +35,19 @@ namespace {
 
 constexpr int THREADS = 192;
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool OUT_F32>
 struct TcLayout {
     static constexpr int A_BYTES = TC_BM * TC_BK * 2;             // 16 KB
     static constexpr int B_CHUNK_BYTES = 64 * TC_BK * 2;          // 64 N x 64 K = 8 KB
     static constexpr int B_BYTES = (BN / 64) * B_CHUNK_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int EPI_BYTES = 4 * EpiStage<OUT_F32>::BYTES;   // one transpose tile per epilogue warp
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;          // full, empty, tfull[2], tempty[2], drain
     static constexpr int MISC_BYTES = 16;                          // tmem base, abort flag
     static constexpr int TMEM_COLS = 2 * BN;
     static size_t smem_bytes(int G) {
-        return 1024 + RING_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+        return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
     }
 };
 
@@ -52,17 +55,18 @@ template <int BN, int STAGES, bool OUT_F32>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                   FwdArgs a) {
-    using L = TcLayout<BN, STAGES>;
+    using L = TcLayout<BN, STAGES, OUT_F32>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);
+    uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + L::RING_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES + L::EPI_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-    int32_t* off = reinterpret_cast<int32_t*>(smem + L::RING_BYTES + L::BAR_BYTES + L::MISC_BYTES);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + L::RING_BYTES + L::EPI_BYTES + L::BAR_BYTES + L::MISC_BYTES);
     int32_t* tprefix = off + a.G + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -190,7 +194,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else {
         // ------------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
-        const int r = q * 32 + lane;            // accumulator row = TMEM lane
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < W; w += gridDim.x) {
             const Tile t = decode_tile(w, tprefix, off, a.G, TC_BM, a.NT, m_inner);
@@ -200,36 +203,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            const bool row_ok = r < t.rows;
-            const long long orow = static_cast<long long>(t.row0 + r) * a.N;
+            // this warp's 32 rows of the tile, stored 32 columns at a time
+            const int rows_valid = t.rows - q * 32;
+            uint8_t* out_rows = static_cast<uint8_t*>(a.out) +
+                                (static_cast<long long>(t.row0) + q * 32) * a.N * (OUT_F32 ? 4 : 2);
+            uint32_t* stage = epi_stage + (warp - 2) * EpiStage<OUT_F32>::WORDS;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tbase + c * 32, v);
                 tmem_ld_wait();
                 const int col = n0 + c * 32;
-                if (row_ok && col < a.N) {
-                    if (OUT_F32) {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + col);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (col + 4 * j < a.N)
-                                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                    } else {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + col);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (col + 8 * j < a.N) {
-                                uint4 p;
-                                p.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-                                p.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-                                p.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-                                p.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-                                dst[j] = p;
-                            }
-                    }
-                }
+                if (rows_valid > 0 && col < a.N)
+                    store_block_32x32<OUT_F32>(v, stage, out_rows + static_cast<long long>(col) * (OUT_F32 ? 4 : 2),
+                                               a.N, rows_valid, a.N - col);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -264,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int BN, int STAGES, bool OUT_F32>
 cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const FwdArgs& a, int grid,
                        cudaStream_t stream) {
-    using L = TcLayout<BN, STAGES>;
+    using L = TcLayout<BN, STAGES, OUT_F32>;
     const size_t shm = L::smem_bytes(a.G);
     auto kern = fwd_tc_kernel<BN, STAGES, OUT_F32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));

@@ -61,7 +61,7 @@ cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_d
 
 // MXFP8 forward (mxfp8_tc.cu): 128x128 tiles, K stages of 128 E4M3 bytes (4 scale blocks).
 constexpr int MX_BN = 128;
-constexpr int MX_SFA_BLOCK_BYTES = 2048;   // 128 rows x 16 bytes per (m-tile, K stage)
+constexpr int MX_SFA_BLOCK_BYTES = 512;    // 128 rows x 4 scales per (m-tile, K stage)
 constexpr int MX_SFB_BLOCK_BYTES = 512;    // 128 columns x 4 scales per (group, n-tile, K stage)
 
 struct MxArgs {
@@ -71,6 +71,8 @@ struct MxArgs {
     int m_inner;
     uint8_t* sfa;                // workspace: reordered lhs scales, [m-tiles, KS] blocks
     uint8_t* sfb;                // workspace: reordered rhs scales, [G, NT, KS] blocks
+    int sfb_vec;                 // rhs_scale rows can be read as 32-bit words (N % 4 == 0, aligned)
+    int sfa_vec;                 // lhs_scale rows can be read as 32-bit words (K % 128 == 0, aligned)
     int32_t* status;
     uint64_t timeout_ns;
 };

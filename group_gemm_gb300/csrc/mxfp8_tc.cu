@@ -12,11 +12,13 @@
 // 32-bit scale column in tensor memory.
 //
 // Two kernels per call:
-//   mx_prep_kernel   reorders the caller's scales ([M, K/32] and [G, K/32, N]) into one small
+//   mx_prep_kernel   reorders the caller's scales ([M, K/32] and [G, K/32, N]) into one 512-byte
 //                    block per (tile, K stage of 128) in the workspace, in the order the
-//                    tensor-memory copies want: A blocks are 128 rows x 16 bytes with the row's 4
-//                    scales repeated in each 4-byte column; B blocks are 128 columns x 4 scales as
-//                    32 rows x 16 bytes (byte 16*(n%32) + 4*(n/32) + kblock).
+//                    tensor-memory copy (tcgen05.cp 32x128b.warpx4) wants: 128 rows (or columns)
+//                    x 4 scales as 32 rows x 16 bytes, byte 16*(r%32) + 4*(r/32) + kblock. The copy
+//                    replicates the 32 lanes into all four lane quarters, and the MMA reads the
+//                    scales of accumulator rows 32q..32q+31 from column q of quarter q, so every
+//                    row finds its own scales.
 //   mxfp8_tc_kernel  persistent, warp-specialised like the bf16 forward: warp 0 brings the codes by
 //                    TMA (lhs [128 x 128 B] K-major, rhs [128 K x 128 N] MN-major, 128-byte
 //                    swizzle) and the scale blocks by bulk copy; warp 1 copies the scale blocks to
@@ -24,6 +26,7 @@
 //                    warps 2..5 run the ragged bf16 epilogue.
 #include <cuda_bf16.h>
 
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -39,17 +42,20 @@ constexpr int BKB = 128;            // K bytes (= elements) per stage: 4 scale b
 constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BKB;   // 16 KB
 constexpr int B_BYTES = BKB * BN;   // 16 KB
-constexpr int SFA_BYTES = MX_SFA_BLOCK_BYTES;   // 2 KB
+constexpr int SFA_BYTES = MX_SFA_BLOCK_BYTES;   // 512 B
 constexpr int SFB_BYTES = MX_SFB_BLOCK_BYTES;   // 512 B
-constexpr int STAGE_BYTES = 35840;              // A + B + SFA + SFB rounded up to 1 KB
+constexpr int STAGE_BYTES = 33792;              // A + B + SFA + SFB (33 KB, keeps 1 KB alignment)
 static_assert(A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES <= STAGE_BYTES, "stage layout");
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+constexpr int EPI_BYTES = 4 * EpiStage<false>::BYTES;
 constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
 constexpr int MISC_BYTES = 16;
 constexpr int TMEM_COLS = 512;      // 2 accumulators of 128 columns + 8 scale columns per stage
 constexpr int TMEM_SF_BASE = 2 * BN;
 
-size_t smem_bytes(int G) { return 1024 + RING_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1); }
+size_t smem_bytes(int G) {
+    return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+}
 
 __device__ __forceinline__ uint32_t scale_word(const uint8_t* p, int avail) {
     // four consecutive E8M0 bytes; blocks past K read as 127 (2^0): their codes are zero-filled
@@ -87,14 +93,17 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
             const int row0 = off[lo] + (T - mt_prefix[lo]) * BM;
             const int rows = min(BM, off[lo + 1] - row0);
             const int avail = min(4, KB32 - 4 * ks);
-            uint4* dst = reinterpret_cast<uint4*>(a.sfa + b * SFA_BYTES);
+            // lane l gathers rows l, l+32, l+64, l+96: bytes 16*l .. 16*l+15 of the block
+            uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = lane + 32 * i;
-                uint32_t w = 0x7f7f7f7fu;
-                if (r < rows) w = scale_word(lhs_scale + static_cast<long long>(row0 + r) * KB32 + 4 * ks, avail);
-                dst[r] = make_uint4(w, w, w, w);
+                const uint8_t* src = lhs_scale + static_cast<long long>(row0 + r) * KB32 + 4 * ks;
+                w[i] = 0x7f7f7f7fu;
+                if (r < rows) w[i] = (a.sfa_vec && avail == 4) ? __ldg(reinterpret_cast<const uint32_t*>(src))
+                                                               : scale_word(src, avail);
             }
+            reinterpret_cast<uint4*>(a.sfa + b * SFA_BYTES)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
         } else {
             const long long bb = b - sfa_blocks;
             const int ks = static_cast<int>(bb % a.KS);
@@ -103,20 +112,41 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
             const int g = static_cast<int>(gn / a.NT);
             const int avail = min(4, KB32 - 4 * ks);
             uint32_t* dst = reinterpret_cast<uint32_t*>(a.sfb + bb * SFB_BYTES);
+            const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + nt * BN;
+            const int n4 = nt * BN + 4 * lane;          // this lane's 4 consecutive columns
+            if (a.sfb_vec && n4 + 3 < a.N) {
+                // rows kb 0..3 of the block: one coalesced 128-byte load each, then a 4 x 4 byte
+                // transpose so that word i holds the 4 scales of column n4 + i
+                uint32_t r[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int nl = lane + 32 * j;
-                const int n = nt * BN + nl;
-                uint32_t w = 0x7f7f7f7fu;
-                if (n < a.N) {
-                    w = 0;
-                    const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + n;
+                for (int q = 0; q < 4; ++q)
+                    r[q] = q < avail ? __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<long long>(q) * a.N) +
+                                             lane)
+                                     : 0x7f7f7f7fu;
+                const uint32_t lo01 = __byte_perm(r[0], r[1], 0x5140), hi01 = __byte_perm(r[0], r[1], 0x7362);
+                const uint32_t lo23 = __byte_perm(r[2], r[3], 0x5140), hi23 = __byte_perm(r[2], r[3], 0x7362);
+                const uint32_t w[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                                       __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        w |= static_cast<uint32_t>(q < avail ? __ldg(src + static_cast<long long>(q) * a.N) : 127u)
-                             << (8 * q);
+                for (int i = 0; i < 4; ++i) {
+                    const int nl = 4 * lane + i;      // byte 16*(nl%32) + 4*(nl/32) + kblock
+                    dst[4 * (nl & 31) + (nl >> 5)] = w[i];
                 }
-                dst[4 * lane + j] = w;   // byte 16*(n%32) + 4*(n/32) + kblock
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int nl = 4 * lane + i;
+                    uint32_t w = 0x7f7f7f7fu;
+                    if (nt * BN + nl < a.N) {
+                        w = 0;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            w |= static_cast<uint32_t>(q < avail ? __ldg(src + static_cast<long long>(q) * a.N + nl)
+                                                                 : 127u)
+                                 << (8 * q);
+                    }
+                    dst[4 * (nl & 31) + (nl >> 5)] = w;
+                }
             }
         }
     }
@@ -127,14 +157,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int32_t* __restrict__ group_sizes, MxArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+    uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + RING_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + EPI_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + BAR_BYTES + MISC_BYTES);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
     int32_t* tprefix = off + a.G + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -231,7 +262,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sb = sa + A_BYTES;
                     const uint32_t sfa_t = tmem_base + TMEM_SF_BASE + 8 * stage;
                     const uint32_t sfb_t = sfa_t + 4;
-                    tmem_cp_128x128b(sfa_t, smem_desc_rows16(sb + B_BYTES));
+                    tmem_cp_32x128b_warpx4(sfa_t, smem_desc_rows16(sb + B_BYTES));
                     tmem_cp_32x128b_warpx4(sfb_t, smem_desc_rows16(sb + B_BYTES + SFA_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < BKB / 32; ++kk) {
@@ -262,7 +293,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else {
         // ------------------------------------------------------------------ epilogue
         const int q = warp & 3;
-        const int r = q * 32 + lane;
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < W; w += gridDim.x) {
             const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
@@ -271,27 +301,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-            const bool row_ok = r < t.rows;
-            const long long orow = static_cast<long long>(t.row0 + r) * a.N;
+            const int rows_valid = t.rows - q * 32;
+            __nv_bfloat16* out_rows =
+                static_cast<__nv_bfloat16*>(a.out) + (static_cast<long long>(t.row0) + q * 32) * a.N;
+            uint32_t* stage = epi_stage + (warp - 2) * EpiStage<false>::WORDS;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tbase + c * 32, v);
                 tmem_ld_wait();
                 const int col = n0 + c * 32;
-                if (row_ok && col < a.N) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + col);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        if (col + 8 * j < a.N) {
-                            uint4 p;
-                            p.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
-                            p.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-                            p.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-                            p.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-                            dst[j] = p;
-                        }
-                }
+                if (rows_valid > 0 && col < a.N)
+                    store_block_32x32<false>(v, stage, out_rows + col, a.N, rows_valid, a.N - col);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);

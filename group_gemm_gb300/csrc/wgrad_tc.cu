@@ -13,6 +13,7 @@
 // zeroed in shared memory (both operands, so NaN/Inf there cannot leak through 0 * x) before the
 // MMA reads them. Roles: warp 0 TMA, warp 1 MMA (+ tail zeroing), warps 2..5 epilogue; two TMEM
 // accumulators let the epilogue of one tile overlap the next tile's mainloop.
+#include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -33,11 +34,12 @@ struct WgLayout {
     static constexpr int B_BYTES = B_CHUNKS * CHUNK_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int EPI_BYTES = 4 * EpiStage<true>::BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
     static constexpr int MISC_BYTES = 16;
     static constexpr int TMEM_COLS = 2 * BN;
     static size_t smem_bytes(int G) {
-        return 1024 + RING_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+        return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
     }
 };
 
@@ -63,14 +65,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     using L = WgLayout<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES);
+    uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + L::RING_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES + L::EPI_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-    int32_t* off = reinterpret_cast<int32_t*>(smem + L::RING_BYTES + L::BAR_BYTES + L::MISC_BYTES);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + L::RING_BYTES + L::EPI_BYTES + L::BAR_BYTES + L::MISC_BYTES);
     int32_t* unused = off + a.G + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -224,17 +227,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else {
         // ------------------------------------------------------------------ epilogue
         const int q = warp & 3;
-        const int r = q * 32 + lane;
+        uint32_t* stage = epi_stage + (warp - 2) * EpiStage<true>::WORDS;
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < W; w += gridDim.x) {
             const WgTile t = wg_decode(w, a.KT, a.NT, off);
             const int k0 = t.kt * TC_BM, n0 = t.nt * BN;
-            const bool row_ok = k0 + r < a.K;
-            float* drow = a.dw + (static_cast<long long>(t.g) * a.K + k0 + r) * a.N;
+            // this warp's 32 rows of dw[g] (rows k0 + 32q ..), stored 32 columns at a time
+            const int rows_valid = a.K - (k0 + q * 32);
+            float* drows = a.dw + (static_cast<long long>(t.g) * a.K + k0 + q * 32) * a.N;
             if (t.rows <= 0) {
-                if (row_ok)
-                    for (int col = n0; col < min(a.N, n0 + BN); col += 4)
-                        *reinterpret_cast<float4*>(drow + col) = make_float4(0.f, 0.f, 0.f, 0.f);
+                // empty group: its slab is zero, the tensor cores never ran for it
+                uint32_t z[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) z[j] = 0u;
+                for (int col = n0; col < min(a.N, n0 + BN); col += 32)
+                    if (rows_valid > 0) store_block_32x32<true>(z, stage, drows + col, a.N, rows_valid, a.N - col);
                 continue;
             }
             const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
@@ -247,14 +254,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld_32x32b_x32(tbase + c * 32, v);
                 tmem_ld_wait();
                 const int col = n0 + c * 32;
-                if (row_ok && col < a.N) {
-                    float4* dst = reinterpret_cast<float4*>(drow + col);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (col + 4 * j < a.N)
-                            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                }
+                if (rows_valid > 0 && col < a.N)
+                    store_block_32x32<true>(v, stage, drows + col, a.N, rows_valid, a.N - col);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
