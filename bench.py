@@ -63,8 +63,12 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-FWD_TC_SOURCES = ["group_gemm_gb300/csrc/fwd_tc.cu", "group_gemm_gb300/csrc/ptx.cuh",
-                  "group_gemm_gb300/csrc/sched.cuh"]
+KERNEL_SOURCES = {
+    "fwd_tc_kernel": ["group_gemm_gb300/csrc/fwd_tc.cu", "group_gemm_gb300/csrc/ptx.cuh",
+                      "group_gemm_gb300/csrc/sched.cuh", "group_gemm_gb300/csrc/epilogue.cuh"],
+    "fwd_tc2_kernel": ["group_gemm_gb300/csrc/fwd_tc2.cu", "group_gemm_gb300/csrc/ptx.cuh",
+                       "group_gemm_gb300/csrc/sched.cuh", "group_gemm_gb300/csrc/epilogue.cuh"],
+}
 
 
 def ncu_traffic(kernel: str, workload: str, sources):
@@ -204,6 +208,7 @@ def bench_ours(args, rank, world, barrier):
     m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
     flops = useful_flops(gs, k, n)
     plan = gg.Plan(m, k, n, g, "forward", cfg["in_dtype"], cfg["out_dtype"], device=dev.index)
+    kernel = "fwd_tc2_kernel" if plan.info["tile_m"] == 256 else "fwd_tc_kernel"
     gs_d = torch.from_numpy(gs).to(dev)
     out_dt = torch.bfloat16 if cfg["out_dtype"] == "bf16" else torch.float32
     out = torch.empty((m, n), dtype=out_dt, device=dev)
@@ -271,8 +276,9 @@ def bench_ours(args, rank, world, barrier):
         "frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": ncu_traffic("fwd_tc", name, FWD_TC_SOURCES),
-                     "kernel": "fwd_tc_kernel", "peak_kind": f"{peaks['source']} bf16 burst"},
+                     "traffic": ncu_traffic(kernel, name, KERNEL_SOURCES[kernel]),
+                     "kernel": kernel, "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}",
+                     "peak_kind": f"{peaks['source']} bf16 burst"},
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clk,
@@ -282,7 +288,7 @@ def bench_ours(args, rank, world, barrier):
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_extras:
         try:
-            result["per_config"] = extra_configs(args, dev, peaks, name)
+            result["per_config"] = extra_configs(args, dev, peaks, name, launch_s)
         except Exception as e:  # a failing extra must not hide the main line
             result["per_config"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0 and not args.no_cpu_baseline:
@@ -296,7 +302,7 @@ def _time_steps(fn, steps, stream):
     return time_region(fn, steps, stream, lambda: None) / steps
 
 
-def extra_configs(args, dev, peaks, main_name):
+def extra_configs(args, dev, peaks, main_name, main_step_s):
     """The other workloads of the suite, measured the same way with fewer steps: the bf16
     forwards (with the padded-dense baseline beside them), the weight gradient and MXFP8."""
     import torch
@@ -312,17 +318,24 @@ def extra_configs(args, dev, peaks, main_name):
         out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
         fl = useful_flops(gs, k, n)
         entry = {}
+        if name == main_name:
+            t = main_step_s
         if name != main_name:
             t = _time_steps(lambda: gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream),
                             steps, stream)
+            entry["tile"] = f"{plan.info['tile_m']}x{plan.info['tile_n']}"
+            other = gg.Plan(m, k, n, g, "forward", cfg["in_dtype"], cfg["out_dtype"], device=dev.index,
+                            flags=gg.RDOT_FLAG_NO_CTA_PAIR if plan.info["tile_m"] == 256 else gg.RDOT_FLAG_CTA_PAIR)
+            t2 = _time_steps(lambda: gg.rdot_forward(other.handle, lhs, rhs, gs_d, out, other.workspace, stream),
+                             steps, stream)
+            entry["other_tile"] = {"tile": f"{other.info['tile_m']}x{other.info['tile_n']}",
+                                   "tflops": round(fl / t2 / 1e12, 3), "ms": round(t2 * 1e3, 4)}
             nz = int(np.count_nonzero(gs))
             min_bytes = (nz * k * n + int(gs.sum()) * k + m * n) * 2
             entry.update({"tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
                           "frac_of_bf16_peak": round(fl / t / 1e12 / peaks["bf16_tflops"], 4),
                           "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1),
                           "frac_of_hbm": round(min_bytes / t / 1e9 / peaks["hbm_gbs"], 4)})
-        else:
-            t = None
         # padded-dense baseline: every group padded to the largest group (rounded up to 128 rows)
         cap = -(-int(gs.max()) // 128) * 128
         pad = torch.empty(gg.rdot_padded_workspace_size(plan.handle, cap), dtype=torch.uint8, device=dev)
@@ -330,8 +343,7 @@ def extra_configs(args, dev, peaks, main_name):
                                                         stream), max(3, steps // 5), stream)
         entry.update({"padded_ms": round(tp * 1e3, 3), "padded_tflops_useful": round(fl / tp / 1e12, 3),
                       "padded_capacity": cap, "padded_flops_ratio": round(g * cap / float(gs.sum()), 3)})
-        if t is not None:
-            entry["speedup_vs_padded"] = round(tp / t, 3)
+        entry["speedup_vs_padded"] = round(tp / t, 3)
         entry["status"] = plan.status()
         res[name] = entry
         del lhs, rhs, out, pad

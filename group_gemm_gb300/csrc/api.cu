@@ -84,6 +84,7 @@ struct rdot_plan_s {
     int tile_m = 0, tile_n = 0;
     int m_inner = 1;
     int grid = 1;
+    bool pair = false;     // bf16 forward on CTA pairs (256 x 256 tiles)
     uint64_t timeout_ns = kDefaultTimeoutNs;
     // tensor maps cached by operand pointers (re-encoded when a pointer changes)
     const void* map_lhs_ptr = nullptr;
@@ -144,7 +145,8 @@ rdot_status check_problem(const rdot_problem* p) {
     if (p->m < 0 || p->k < 1 || p->n < 1 || p->groups < 1 || p->groups > RDOT_MAX_GROUPS)
         return RDOT_ERR_INVALID_ARG;
     if (p->m > 0x7fffffffLL || p->k > 0x7fffffffLL || p->n > 0x7fffffffLL) return RDOT_ERR_UNSUPPORTED;
-    if (p->flags & ~3) return RDOT_ERR_INVALID_ARG;
+    if (p->flags & ~0xF) return RDOT_ERR_INVALID_ARG;
+    if ((p->flags & RDOT_FLAG_CTA_PAIR) && (p->flags & RDOT_FLAG_NO_CTA_PAIR)) return RDOT_ERR_INVALID_ARG;
     if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256) return RDOT_ERR_UNSUPPORTED;
     switch (p->mode) {
         case RDOT_MODE_FORWARD:
@@ -217,15 +219,33 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             return RDOT_ERR_UNSUPPORTED;   // tcgen05 kernels are built for sm_103a only
         }
         pl->kind = 1;
-        pl->tile_m = TC_BM;
-        pl->tile_n = p.tile_n ? p.tile_n : (p.n <= 128 ? 128 : 256);
+        const bool want_pair = (p.flags & RDOT_FLAG_CTA_PAIR) ||
+                               (!(p.flags & RDOT_FLAG_NO_CTA_PAIR) && m_avg >= TC2_BM && p.n >= 256);
+        if (want_pair && p.tile_n == 128) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        int clusters = 0;
+        if (want_pair) {
+            clusters = fwd_tc2_max_clusters(p.out_dtype == RDOT_F32, p.groups);
+            if (clusters <= 0) {
+                delete pl;
+                return cuda_fail(cudaGetLastError(), "cudaOccupancyMaxActiveClusters");
+            }
+        }
+        pl->pair = want_pair;
+        pl->tile_m = want_pair ? TC2_BM : TC_BM;
+        pl->tile_n = want_pair ? 256 : (p.tile_n ? p.tile_n : (p.n <= 128 ? 128 : 256));
         const int nt = static_cast<int>((p.n + pl->tile_n - 1) / pl->tile_n);
-        const long long bound = forward_tile_bound(p.m, p.groups, TC_BM, nt);
+        const long long bound = forward_tile_bound(p.m, p.groups, pl->tile_m, nt);
         if (bound > 0x7fffffffLL) {
             delete pl;
             return RDOT_ERR_UNSUPPORTED;
         }
-        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
+        if (want_pair)
+            pl->grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(bound, clusters)));
+        else
+            pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
     } else if (p.mode == RDOT_MODE_FORWARD_MXFP8) {
         if (prop.major != 10) {
             delete pl;
@@ -353,7 +373,10 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = rhs;
     }
-    e = launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
+    if (plan->pair)
+        e = launch_fwd_tc2(plan->map_a, plan->map_b, a, p.out_dtype == RDOT_F32, plan->grid, s);
+    else
+        e = launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "fwd_tc launch");
     return RDOT_OK;
 }
@@ -531,9 +554,14 @@ rdot_status rdot_padded_forward(rdot_plan_t plan, const void* lhs, const void* r
     a.m_inner = C <= p.n ? 1 : 0;
     a.status = status;
     a.timeout_ns = plan->timeout_ns;
-    const long long bound = forward_tile_bound(rows_pad, p.groups, TC_BM, a.NT);
-    const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, plan->sm_count)));
-    e = launch_fwd_tc(plan->pad_map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, grid, s);
+    const long long bound = forward_tile_bound(rows_pad, p.groups, plan->tile_m, a.NT);
+    if (plan->pair) {
+        const int grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(bound, plan->grid / 2)));
+        e = launch_fwd_tc2(plan->pad_map_a, plan->map_b, a, p.out_dtype == RDOT_F32, grid, s);
+    } else {
+        const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, plan->sm_count)));
+        e = launch_fwd_tc(plan->pad_map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, grid, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "padded GEMM launch");
     e = launch_pad_gather(out_pad, group_sizes, out, static_cast<int>(p.m), p.groups, C, p.n * esz_out,
                           4 * plan->sm_count, s);

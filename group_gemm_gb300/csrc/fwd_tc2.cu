@@ -1,0 +1,306 @@
+// fwd_tc2.cu -- bf16 ragged-dot forward on CTA pairs (tcgen05 cta_group::2), 256 x 256 tiles.
+//
+// Same operation and ragged semantics as fwd_tc.cu ("Group-GEMM in XLA", Part 3
+// "Non-Contracting (the MoE Case)"); only the tile shape and the hardware mapping differ.
+//
+// A cluster of two CTAs (two SMs) computes one 256-row x 256-column tile of one group:
+//   - CTA r (r = cluster rank) loads rows [row0 + 128 r, +128) of lhs and columns
+//     [n0 + 128 r, +128) of rhs[g] into its own shared memory, 64 K at a time (32 KB per stage,
+//     six stages). Both CTAs' TMA loads complete on the even CTA's "full" barrier.
+//   - The even CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): the tensor cores of
+//     the pair read A from each CTA's own rows and the two halves of B from both CTAs, and write
+//     accumulator rows 128 r .. 128 r + 127 into CTA r's tensor memory. Commits multicast to both
+//     CTAs ("stage free" and "accumulator full").
+//   - Each CTA's four epilogue warps drain its 128 accumulator rows exactly as in fwd_tc.cu and
+//     arrive on the even CTA's "accumulator empty" barrier (one arrival per warp, 8 in all).
+// Per SM, a stage carries 32 KB for 128 x 256 x 64 multiply-adds instead of 48 KB with one-CTA
+// tiles: the ring covers half again as much MMA time and L2 serves a third fewer bytes.
+#include <cuda_bf16.h>
+
+#include "epilogue.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace rdot {
+
+namespace {
+
+constexpr int THREADS = 192;
+constexpr int BM = 256;               // rows per cluster tile (128 per CTA)
+constexpr int BN = 256;               // columns per tile (128 per CTA's B half)
+constexpr int STAGES = 6;
+constexpr int A_BYTES = 128 * TC_BK * 2;     // 16 KB
+constexpr int B_CHUNK_BYTES = 64 * TC_BK * 2;  // 8 KB
+constexpr int B_BYTES = 2 * B_CHUNK_BYTES;   // this CTA's 128 columns
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
+constexpr int MISC_BYTES = 16;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr uint32_t EMPTY_ARRIVALS = 8;       // 4 epilogue warps x 2 CTAs
+
+template <bool OUT_F32>
+size_t smem_bytes(int G) {
+    return 1024 + RING_BYTES + 4 * EpiStage<OUT_F32>::BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+}
+
+template <bool OUT_F32>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                   FwdArgs a) {
+    constexpr int EPI_BYTES = 4 * EpiStage<OUT_F32>::BYTES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + RING_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + EPI_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    int32_t* tprefix = off + a.G + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = static_cast<int>(cluster_id_x());
+    const int nclusters = static_cast<int>(cluster_count_x());
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], EMPTY_ARRIVALS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, TMEM_COLS);   // collectively, one warp in each CTA of the pair
+        tmem_relinquish_pair();
+    }
+    if (warp == 2) {
+        const int bad = group_scan_warp(a.group_sizes, a.G, a.M, BM, a.NT, off, tprefix);
+        if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers of both CTAs initialised, TMEM allocated in both
+    tc_fence_after();
+
+    const uint32_t tmem_base = *tmem_holder;
+    const int W = tprefix[a.G];
+    const int KB = (a.K + TC_BK - 1) / TC_BK;
+    const bool m_inner = a.m_inner != 0;
+    const WaitGuard guard{abort_flag, a.status, a.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int w = cluster; w < W && ok; w += nclusters) {
+                const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
+                const int n0 = t.nt * BN;
+                // bytes each CTA brings in: its A half unless it lies wholly past M, and the
+                // 64-column chunks of its B half that are not wholly past N
+                const int a0 = A_BYTES, a1 = (t.row0 + 128 < a.M) ? A_BYTES : 0;
+                const int c0 = max(0, min(2, (a.N - n0 + 63) / 64));
+                const int c1 = max(0, min(2, (a.N - n0 - 128 + 63) / 64));
+                const int my_a = rank ? a1 : a0;
+                const int my_c = rank ? c1 : c0;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    if (leader) mbar_arrive_expect_tx(&full[stage], a0 + a1 + (c0 + c1) * B_CHUNK_BYTES);
+                    const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+                    if (my_a) tma_load_2d_pair(sa, &tmap_a, fb, kb * TC_BK, t.row0 + 128 * static_cast<int>(rank));
+                    for (int j = 0; j < my_c; ++j)
+                        tma_load_3d_pair(sb + j * B_CHUNK_BYTES, &tmap_b, fb, n0 + 128 * static_cast<int>(rank) + 64 * j,
+                                         kb * TC_BK, t.g);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                // stopping early: let the loads in flight land before the CTA can exit. The even
+                // CTA sees both CTAs' bytes on its barriers; the odd CTA cannot, so it waits a
+                // fixed 100 us, far longer than a TMA transfer.
+                WaitGuard drain_guard = guard;
+                int dummy = 0;
+                drain_guard.abort = &dummy;
+                drain_guard.status = nullptr;
+                if (leader) {
+                    for (int s = 0; s < STAGES; ++s)
+                        if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
+                } else {
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 100000ull) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_f16(BM, BN, true, true, false, true);
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int w = cluster; w < W && ok; w += nclusters) {
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1, guard)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, guard)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < TC_BK / 16; ++kk) {
+                        const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, B_CHUNK_BYTES, 1024);
+                        mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit_pair_multicast(&empty[stage], 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair_multicast(&tfull[acc], 0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1;
+            }
+            mma_commit_pair(drain);
+            WaitGuard drain_guard = guard;
+            int dummy = 0;
+            drain_guard.abort = &dummy;
+            (void)mbar_wait(drain, 0, drain_guard);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        uint32_t* stage_buf = epi_stage + (warp - 2) * EpiStage<OUT_F32>::WORDS;
+        uint32_t acc = 0, acc_phase = 0;
+        for (int w = cluster; w < W; w += nclusters) {
+            const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
+            const int n0 = t.nt * BN;
+            const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
+            if (!__all_sync(0xffffffffu, ready)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            const int first = 128 * static_cast<int>(rank) + q * 32;    // first tile row of this warp
+            const int rows_valid = t.rows - first;
+            uint8_t* out_rows =
+                static_cast<uint8_t*>(a.out) + (static_cast<long long>(t.row0) + first) * a.N * (OUT_F32 ? 4 : 2);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, v);
+                tmem_ld_wait();
+                const int col = n0 + c * 32;
+                if (rows_valid > 0 && col < a.N)
+                    store_block_32x32<OUT_F32>(v, stage_buf,
+                                               out_rows + static_cast<long long>(col) * (OUT_F32 ? 4 : 2), a.N,
+                                               rows_valid, a.N - col);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+        }
+        {
+            const int esz = OUT_F32 ? 4 : 2;
+            const long long b0 = static_cast<long long>(off[a.G]) * a.N * esz;
+            const long long b1 = static_cast<long long>(a.M) * a.N * esz;
+            const long long nv = (b1 - b0) / 16;
+            if (nv > 0) {
+                uint4* base = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.out) + b0);
+                const long long per = (nv + gridDim.x - 1) / gridDim.x;
+                const long long s = per * blockIdx.x;
+                const long long e = min(nv, s + per);
+                for (long long i = s + (threadIdx.x - 64); i < e; i += 128) base[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------------- teardown
+    tc_fence_before();
+    cluster_sync();   // neither CTA leaves while the pair's MMAs, copies or arrivals may touch it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+template <bool OUT_F32>
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const FwdArgs& a, int grid,
+                       cudaStream_t stream) {
+    const size_t shm = smem_bytes<OUT_F32>(a.G);
+    auto kern = fwd_tc2_kernel<OUT_F32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, THREADS, shm, stream>>>(ta, tb, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc2(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, bool out_f32,
+                           int grid, cudaStream_t stream) {
+    if (grid % 2) return cudaErrorInvalidValue;
+    return out_f32 ? launch_one<true>(tmap_a, tmap_b, a, grid, stream)
+                   : launch_one<false>(tmap_a, tmap_b, a, grid, stream);
+}
+
+int fwd_tc2_max_clusters(bool out_f32, int G) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = out_f32 ? smem_bytes<true>(G) : smem_bytes<false>(G);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cudaError_t e;
+    if (out_f32) {
+        e = cudaFuncSetAttribute(fwd_tc2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(cfg.dynamicSmemBytes));
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, fwd_tc2_kernel<true>, &cfg);
+    } else {
+        e = cudaFuncSetAttribute(fwd_tc2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(cfg.dynamicSmemBytes));
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, fwd_tc2_kernel<false>, &cfg);
+    }
+    return e == cudaSuccess ? n : 0;
+}
+
+}  // namespace rdot

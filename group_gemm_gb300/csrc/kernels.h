@@ -44,6 +44,13 @@ cudaError_t launch_fwd_tc(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, 
 constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;
 
+// bf16 inputs on CTA pairs (fwd_tc2.cu): clusters of 2 CTAs, 256 x 256 tiles, same maps as
+// launch_fwd_tc. grid must be even (2 CTAs per cluster).
+cudaError_t launch_fwd_tc2(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, bool out_f32,
+                           int grid, cudaStream_t stream);
+int fwd_tc2_max_clusters(bool out_f32, int G);   // co-resident clusters of that kernel (0 on error)
+constexpr int TC2_BM = 256;
+
 // Arguments of the weight-gradient kernel (passed by value).
 struct WgradArgs {
     const int32_t* group_sizes;  // device [G]

@@ -140,6 +140,25 @@ def test_bf16_forward_parity(m, k, n, gs, out_dtype):
     assert torch.all(out[total:] == 0)
 
 
+@pytest.mark.parametrize("m,k,n,gs", BF16_CASES + [(1700, 320, 640, [700, 0, 129, 1, 512, 300]),
+                                              (2000, 256, 512, [257, 255, 256, 1, 1000, 0, 231])])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_bf16_forward_parity_cta_pairs(m, k, n, gs, out_dtype):
+    """The 256 x 256 CTA-pair kernel (tcgen05 cta_group::2) on the same ragged cases, including
+    tiles whose odd-CTA half lies wholly past the group or past M, and B halves past N."""
+    gs = np.asarray(gs, np.int32)
+    lhs = torch.from_numpy(ri.host_normal((m, k), 13)).to(torch.bfloat16)
+    rhs = torch.from_numpy(ri.host_normal((gs.size, k, n), 14, 0.05)).to(torch.bfloat16)
+    total = int(gs.sum())
+    lhs[total:] = float("nan")
+    out, status, plan = run_forward(lhs, rhs, gs, out_dtype=out_dtype, flags=gg.RDOT_FLAG_CTA_PAIR)
+    assert plan.info["tile_m"] == 256 and plan.info["grid_ctas"] % 2 == 0
+    ref = oracle.forward(lhs, rhs, gs)
+    assert status == 0
+    assert rel_err(out, ref) <= TOL_BF16
+    assert torch.all(out[total:] == 0)
+
+
 @pytest.mark.parametrize("flags", [gg.RDOT_FLAG_ROW_TILES_INNER, gg.RDOT_FLAG_COL_TILES_INNER])
 @pytest.mark.parametrize("tile_n", [128, 256])
 def test_bf16_orders_and_tiles(flags, tile_n):
@@ -147,7 +166,7 @@ def test_bf16_orders_and_tiles(flags, tile_n):
     m, k, n = 1700, 320, 640
     lhs = torch.from_numpy(ri.host_normal((m, k), 21)).to(torch.bfloat16)
     rhs = torch.from_numpy(ri.host_normal((gs.size, k, n), 22, 0.05)).to(torch.bfloat16)
-    out, _, plan = run_forward(lhs, rhs, gs, flags=flags, tile_n=tile_n)
+    out, _, plan = run_forward(lhs, rhs, gs, flags=flags | gg.RDOT_FLAG_NO_CTA_PAIR, tile_n=tile_n)
     assert plan.info["tile_n"] == tile_n
     assert rel_err(out, oracle.forward(lhs, rhs, gs)) <= TOL_BF16
 

@@ -54,14 +54,16 @@ def oracle_rows_on_subset(lhs_d, rhs_d, gs, rows, groups_of_rows):
     return oracle.forward(lhs_h, rhs_h, counts.astype(np.int32))
 
 
-@pytest.mark.parametrize("name", ["mixtral_bf16", "deepseek_bf16"])
-def test_full_size_bf16_forward_sampled_rows(name):
+@pytest.mark.parametrize("name, flags", [("mixtral_bf16", 0), ("deepseek_bf16", 0),
+                                         ("mixtral_bf16", 8), ("deepseek_bf16", 4)])
+def test_full_size_bf16_forward_sampled_rows(name, flags):
+    """flags 0 = the plan's own choice (what bench.py times); 8 / 4 force the other tile shape."""
     cfg = ri.CONFIGS[name]
     m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
     gs = ri.config_group_sizes(name)
     lhs = ri.device_normal((m, k), 1000, cfg["lhs"][1], DEV, torch.bfloat16)
     rhs = ri.device_normal((g, k, n), 2000, cfg["rhs"][1], DEV, torch.bfloat16)
-    plan = gg.Plan(m, k, n, g, "forward", "bf16", "bf16")
+    plan = gg.Plan(m, k, n, g, "forward", "bf16", "bf16", flags=flags)
     out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
     gs_d = torch.from_numpy(gs).to(DEV)
     gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace)
