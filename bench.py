@@ -363,7 +363,14 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
     min_bytes = 2 * m * (k + n) + 4 * g * k * n
     res["wgrad_bf16"] = {"tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
                          "frac_of_bf16_peak": round(fl / t / 1e12 / peaks["bf16_tflops"], 4),
-                         "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1), "status": plan.status()}
+                         "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1), "status": plan.status(),
+                         "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}"}
+    other = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", device=dev.index,
+                    flags=gg.RDOT_FLAG_NO_CTA_PAIR if plan.info["tile_m"] == 256 else gg.RDOT_FLAG_CTA_PAIR)
+    t2 = _time_steps(lambda: gg.rdot_grad_weight(other.handle, lhs, dy, gs_d, dw, other.workspace, stream), steps,
+                     stream)
+    res["wgrad_bf16"]["other_tile"] = {"tile": f"{other.info['tile_m']}x{other.info['tile_n']}",
+                                       "tflops": round(fl / t2 / 1e12, 3), "ms": round(t2 * 1e3, 4)}
     del lhs, dy, dw
     torch.cuda.empty_cache()
     # MXFP8 forward
@@ -388,7 +395,14 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
     res["mxfp8"] = {"tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
                     "frac_of_fp8_peak_assumed_2x_bf16": round(fl / t / 1e12 / fp8_peak, 4),
                     "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1), "status": plan.status(),
+                    "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}",
                     "note": "FP8 peak not measured on this pool; taken as 2x the measured bf16 burst peak"}
+    other = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16", device=dev.index,
+                    tile_n=128 if plan.info["tile_n"] == 256 else 256)
+    t2 = _time_steps(lambda: gg.rdot_forward_mxfp8(other.handle, aq, as_, bq, bs, gs_d, out, other.workspace, stream),
+                     steps, stream)
+    res["mxfp8"]["other_tile"] = {"tile": f"{other.info['tile_m']}x{other.info['tile_n']}",
+                                  "tflops": round(fl / t2 / 1e12, 3), "ms": round(t2 * 1e3, 4)}
     del aq, as_, bq, bs, out
     torch.cuda.empty_cache()
     return res

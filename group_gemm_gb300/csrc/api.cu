@@ -253,8 +253,8 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         }
         pl->kind = 3;
         pl->tile_m = TC_BM;
-        pl->tile_n = MX_BN;
-        const int nt = static_cast<int>((p.n + MX_BN - 1) / MX_BN);
+        pl->tile_n = p.tile_n ? p.tile_n : (p.n >= 256 ? 256 : 128);
+        const int nt = static_cast<int>((p.n + pl->tile_n - 1) / pl->tile_n);
         const long long bound = forward_tile_bound(p.m, p.groups, TC_BM, nt);
         if (bound > 0x7fffffffLL) {
             delete pl;
@@ -267,15 +267,33 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             return RDOT_ERR_UNSUPPORTED;
         }
         pl->kind = 2;
-        pl->tile_m = TC_BM;   // rows of dw (the K axis) per tile
-        pl->tile_n = p.tile_n ? p.tile_n : (p.n <= 128 ? 128 : 256);
-        const long long kt = (p.k + TC_BM - 1) / TC_BM, nt = (p.n + pl->tile_n - 1) / pl->tile_n;
+        // single-CTA tiles measure faster for the weight gradient on GB300; pairs on request
+        const bool want_pair = (p.flags & RDOT_FLAG_CTA_PAIR) != 0;
+        if (want_pair && p.tile_n == 128) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        int clusters = 0;
+        if (want_pair) {
+            clusters = wgrad_tc2_max_clusters(p.groups);
+            if (clusters <= 0) {
+                delete pl;
+                return cuda_fail(cudaGetLastError(), "cudaOccupancyMaxActiveClusters");
+            }
+        }
+        pl->pair = want_pair;
+        pl->tile_m = want_pair ? 256 : TC_BM;   // rows of dw (the K axis) per tile
+        pl->tile_n = want_pair ? 256 : (p.tile_n ? p.tile_n : (p.n <= 128 ? 128 : 256));
+        const long long kt = (p.k + pl->tile_m - 1) / pl->tile_m, nt = (p.n + pl->tile_n - 1) / pl->tile_n;
         const long long work = kt * nt * p.groups;
         if (work > 0x7fffffffLL) {
             delete pl;
             return RDOT_ERR_UNSUPPORTED;
         }
-        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(work, pl->sm_count)));
+        if (want_pair)
+            pl->grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(work, clusters)));
+        else
+            pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(work, pl->sm_count)));
     } else {
         delete pl;
         return RDOT_ERR_UNSUPPORTED;
@@ -296,21 +314,21 @@ struct MxLayout {
     int ks, nt;
 };
 
-MxLayout mx_layout(const rdot_problem& p) {
+MxLayout mx_layout(const rdot_problem& p, int bn) {
     MxLayout l{};
     l.ks = static_cast<int>((p.k + 127) / 128);
-    l.nt = static_cast<int>((p.n + MX_BN - 1) / MX_BN);
+    l.nt = static_cast<int>((p.n + bn - 1) / bn);
     const size_t mtiles = static_cast<size_t>((p.m + TC_BM - 1) / TC_BM) + static_cast<size_t>(p.groups);
     l.sfa_off = kWorkspaceBytes;
     l.sfb_off = l.sfa_off + mtiles * l.ks * MX_SFA_BLOCK_BYTES;
-    l.total = l.sfb_off + static_cast<size_t>(p.groups) * l.nt * l.ks * MX_SFB_BLOCK_BYTES;
+    l.total = l.sfb_off + static_cast<size_t>(p.groups) * l.nt * l.ks * (bn / 128) * MX_SFB_ATOM_BYTES;
     return l;
 }
 }  // namespace
 
 rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes) {
     if (!plan || !bytes) return RDOT_ERR_INVALID_ARG;
-    *bytes = plan->kind == 3 ? mx_layout(plan->p).total : kWorkspaceBytes;
+    *bytes = plan->kind == 3 ? mx_layout(plan->p, plan->tile_n).total : kWorkspaceBytes;
     return RDOT_OK;
 }
 
@@ -406,7 +424,7 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = rhs;
     }
-    const MxLayout l = mx_layout(p);
+    const MxLayout l = mx_layout(p, plan->tile_n);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     MxArgs a{};
     a.out = out;
@@ -414,8 +432,10 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
     a.K = static_cast<int>(p.k);
     a.N = static_cast<int>(p.n);
     a.G = p.groups;
+    a.BN = plan->tile_n;
     a.NT = l.nt;
     a.KS = l.ks;
+    a.NT128 = static_cast<int>((p.n + 127) / 128);
     a.m_inner = plan->m_inner;
     a.sfa = ws + l.sfa_off;
     a.sfb = ws + l.sfb_off;
@@ -463,11 +483,12 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
     a.K = static_cast<int>(p.k);
     a.N = static_cast<int>(p.n);
     a.G = p.groups;
-    a.KT = static_cast<int>((p.k + TC_BM - 1) / TC_BM);
+    a.KT = static_cast<int>((p.k + plan->tile_m - 1) / plan->tile_m);
     a.NT = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
     a.status = static_cast<int32_t*>(workspace);
     a.timeout_ns = plan->timeout_ns;
-    cudaError_t e = launch_wgrad_tc(plan->map_a, plan->map_b, a, plan->tile_n, plan->grid, s);
+    cudaError_t e = plan->pair ? launch_wgrad_tc2(plan->map_a, plan->map_b, a, plan->grid, s)
+                               : launch_wgrad_tc(plan->map_a, plan->map_b, a, plan->tile_n, plan->grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "wgrad_tc launch");
     return RDOT_OK;
 }

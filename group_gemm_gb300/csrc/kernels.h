@@ -66,18 +66,20 @@ struct WgradArgs {
 cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int bn,
                             int grid, cudaStream_t stream);
 
-// MXFP8 forward (mxfp8_tc.cu): 128x128 tiles, K stages of 128 E4M3 bytes (4 scale blocks).
-constexpr int MX_BN = 128;
+// MXFP8 forward (mxfp8_tc.cu): 128 x BN tiles (BN = 128 or 256), K stages of 128 E4M3 bytes
+// (4 scale blocks).
 constexpr int MX_SFA_BLOCK_BYTES = 512;    // 128 rows x 4 scales per (m-tile, K stage)
-constexpr int MX_SFB_BLOCK_BYTES = 512;    // 128 columns x 4 scales per (group, n-tile, K stage)
+constexpr int MX_SFB_ATOM_BYTES = 512;     // 128 columns x 4 scales per (group, 128 columns, K stage)
 
 struct MxArgs {
     void* out;                   // device bf16 [M, N]
     int M, K, N, G;
-    int NT, KS;                  // column tiles, K stages of 128
+    int BN;                      // tile width: 128 or 256
+    int NT, KS;                  // BN-wide column tiles, K stages of 128
+    int NT128;                   // 128-column scale atoms across N
     int m_inner;
     uint8_t* sfa;                // workspace: reordered lhs scales, [m-tiles, KS] blocks
-    uint8_t* sfb;                // workspace: reordered rhs scales, [G, NT, KS] blocks
+    uint8_t* sfb;                // workspace: reordered rhs scales, [G, NT, KS] blocks of BN/128 atoms
     int sfb_vec;                 // rhs_scale rows can be read as 32-bit words (N % 4 == 0, aligned)
     int sfa_vec;                 // lhs_scale rows can be read as 32-bit words (K % 128 == 0, aligned)
     int32_t* status;
@@ -89,6 +91,11 @@ struct MxArgs {
 cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const uint8_t* lhs_scale,
                          const uint8_t* rhs_scale, const int32_t* group_sizes, const MxArgs& a, int grid,
                          int prep_grid, cudaStream_t stream);
+
+// CTA-pair grad-weight (wgrad_tc2.cu): 256 x 256 tiles of dw[g]; a.KT counts 256-wide K tiles.
+cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int grid,
+                             cudaStream_t stream);
+int wgrad_tc2_max_clusters(int G);
 
 // Padded-dense baseline data movement (padded.cu).
 cudaError_t launch_pad_scatter(const void* lhs, const int32_t* gs, void* lhs_pad, int32_t* uniform_gs, int M, int G,

@@ -37,25 +37,34 @@ namespace {
 
 constexpr int THREADS = 192;
 constexpr int BM = 128;
-constexpr int BN = MX_BN;
 constexpr int BKB = 128;            // K bytes (= elements) per stage: 4 scale blocks
-constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BKB;   // 16 KB
-constexpr int B_BYTES = BKB * BN;   // 16 KB
 constexpr int SFA_BYTES = MX_SFA_BLOCK_BYTES;   // 512 B
-constexpr int SFB_BYTES = MX_SFB_BLOCK_BYTES;   // 512 B
-constexpr int STAGE_BYTES = 33792;              // A + B + SFA + SFB (33 KB, keeps 1 KB alignment)
-static_assert(A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES <= STAGE_BYTES, "stage layout");
-constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-constexpr int EPI_BYTES = 4 * EpiStage<false>::BYTES;
-constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
-constexpr int MISC_BYTES = 16;
-constexpr int TMEM_COLS = 512;      // 2 accumulators of 128 columns + 8 scale columns per stage
-constexpr int TMEM_SF_BASE = 2 * BN;
+constexpr int SF_ATOM_BYTES = MX_SFB_ATOM_BYTES;   // scales of 128 columns x one K stage
 
-size_t smem_bytes(int G) {
-    return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
-}
+// BN = 128: two accumulators (the epilogue overlaps the next tile), six stages.
+// BN = 256: one accumulator (256 columns plus the scale columns fill tensor memory), four
+//           stages; per MMA the tensor cores read 96 instead of 128 bytes of shared memory per
+//           clock.
+template <int BN>
+struct MxLayout {
+    static constexpr int NACC = BN == 128 ? 2 : 1;
+    static constexpr int STAGES = BN == 128 ? 6 : 4;
+    static constexpr int B_BYTES = BKB * BN;
+    static constexpr int SFB_BYTES = (BN / 128) * SF_ATOM_BYTES;
+    static constexpr int STAGE_BYTES = ((A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + 1023) / 1024) * 1024;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int EPI_BYTES = 4 * EpiStage<false>::BYTES;
+    static constexpr int BAR_BYTES = (2 * STAGES + 2 * NACC + 1) * 8;
+    static constexpr int MISC_BYTES = 16;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int TMEM_SF_BASE = NACC * BN;    // then per stage: 4 scale columns of A, BN/32 of B
+    static constexpr int SF_COLS = 4 + BN / 32;
+    static_assert(TMEM_SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
+    static size_t smem_bytes(int G) {
+        return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+    }
+};
 
 __device__ __forceinline__ uint32_t scale_word(const uint8_t* p, int avail) {
     // four consecutive E8M0 bytes; blocks past K read as 127 (2^0): their codes are zero-filled
@@ -76,7 +85,7 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
     const int KB32 = a.K / 32;
     const long long Tm = mt_prefix[a.G];
     const long long sfa_blocks = Tm * a.KS;
-    const long long sfb_blocks = static_cast<long long>(a.G) * a.NT * a.KS;
+    const long long sfb_blocks = static_cast<long long>(a.G) * a.NT128 * a.KS;
     const int lane = threadIdx.x & 31;
     const long long warp0 = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
     const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
@@ -105,15 +114,19 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
             }
             reinterpret_cast<uint4*>(a.sfa + b * SFA_BYTES)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
         } else {
+            // one 128-column atom: (group g, 128-column block nt, K stage ks)
             const long long bb = b - sfa_blocks;
             const int ks = static_cast<int>(bb % a.KS);
             const long long gn = bb / a.KS;
-            const int nt = static_cast<int>(gn % a.NT);
-            const int g = static_cast<int>(gn / a.NT);
+            const int nt = static_cast<int>(gn % a.NT128);
+            const int g = static_cast<int>(gn / a.NT128);
             const int avail = min(4, KB32 - 4 * ks);
-            uint32_t* dst = reinterpret_cast<uint32_t*>(a.sfb + bb * SFB_BYTES);
-            const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + nt * BN;
-            const int n4 = nt * BN + 4 * lane;          // this lane's 4 consecutive columns
+            const int atoms = a.BN / 128;   // atoms per tile; a tile's block holds its atoms in order
+            const long long blk = (static_cast<long long>(g) * a.NT + nt / atoms) * a.KS + ks;
+            uint32_t* dst = reinterpret_cast<uint32_t*>(a.sfb + blk * (atoms * SF_ATOM_BYTES) +
+                                                        (nt % atoms) * SF_ATOM_BYTES);
+            const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + nt * 128;
+            const int n4 = nt * 128 + 4 * lane;         // this lane's 4 consecutive columns
             if (a.sfb_vec && n4 + 3 < a.N) {
                 // rows kb 0..3 of the block: one coalesced 128-byte load each, then a 4 x 4 byte
                 // transpose so that word i holds the 4 scales of column n4 + i
@@ -137,7 +150,7 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
                 for (int i = 0; i < 4; ++i) {
                     const int nl = 4 * lane + i;
                     uint32_t w = 0x7f7f7f7fu;
-                    if (nt * BN + nl < a.N) {
+                    if (nt * 128 + nl < a.N) {
                         w = 0;
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
@@ -152,17 +165,28 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
     }
 }
 
+template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     mxfp8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const int32_t* __restrict__ group_sizes, MxArgs a) {
+    using L = MxLayout<BN>;
+    constexpr int STAGES = L::STAGES;
+    constexpr int NACC = L::NACC;
+    constexpr int STAGE_BYTES = L::STAGE_BYTES;
+    constexpr int RING_BYTES = L::RING_BYTES;
+    constexpr int EPI_BYTES = L::EPI_BYTES;
+    constexpr int BAR_BYTES = L::BAR_BYTES;
+    constexpr int MISC_BYTES = L::MISC_BYTES;
+    constexpr int B_BYTES = L::B_BYTES;
+    constexpr int SFB_BYTES = L::SFB_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + RING_BYTES);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + EPI_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
+    uint64_t* tempty = tfull + NACC;
+    uint64_t* drain = tempty + NACC;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
@@ -175,7 +199,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NACC; ++i) {
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], 128);
         }
@@ -186,7 +210,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tmap_b);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, TMEM_COLS);
+        tmem_alloc(tmem_holder, L::TMEM_COLS);
         tmem_relinquish();
     }
     if (warp == 2) {
@@ -218,9 +242,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     uint8_t* st = smem + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
+                    // 128-column boxes wholly past N are not loaded (they only feed unstored columns)
+                    const int nb = min(BN / 128, (a.N - t.nt * BN + 127) / 128);
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + nb * (BKB * 128) + SFA_BYTES + SFB_BYTES);
                     tma_load_2d(st, &tmap_a, &full[stage], ks * BKB, t.row0);
-                    tma_load_3d(st + A_BYTES, &tmap_b, &full[stage], t.nt * BN, ks * BKB, t.g);
+                    for (int j = 0; j < nb; ++j)
+                        tma_load_3d(st + A_BYTES + j * (BKB * 128), &tmap_b, &full[stage], t.nt * BN + 128 * j,
+                                    ks * BKB, t.g);
                     bulk_load(st + A_BYTES + B_BYTES, sfa_src + static_cast<long long>(ks) * SFA_BYTES, SFA_BYTES,
                               &full[stage]);
                     bulk_load(st + A_BYTES + B_BYTES + SFA_BYTES, sfb_src + static_cast<long long>(ks) * SFB_BYTES,
@@ -260,15 +288,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
-                    const uint32_t sfa_t = tmem_base + TMEM_SF_BASE + 8 * stage;
+                    const uint32_t sfa_t = tmem_base + L::TMEM_SF_BASE + L::SF_COLS * stage;
                     const uint32_t sfb_t = sfa_t + 4;
                     tmem_cp_32x128b_warpx4(sfa_t, smem_desc_rows16(sb + B_BYTES));
-                    tmem_cp_32x128b_warpx4(sfb_t, smem_desc_rows16(sb + B_BYTES + SFA_BYTES));
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j)
+                        tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
+                                               smem_desc_rows16(sb + B_BYTES + SFA_BYTES + j * SF_ATOM_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < BKB / 32; ++kk) {
                         // A K-major: +32 bytes per 32-element K step; B MN-major: +32 K rows of 128 B
                         const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 4096, B_BYTES, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 4096, BKB * 128, 1024);
                         mma_mxf8(d_tmem, adesc, bdesc, idesc_mxf8(BM, BN, false, true, kk, kk), sfa_t, sfb_t,
                                  (ks | kk) != 0 ? 1u : 0u);
                     }
@@ -280,8 +311,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1;
+                if (++acc == NACC) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
             }
             mma_commit(drain);
             WaitGuard drain_guard = guard;
@@ -316,8 +349,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1;
+            if (++acc == NACC) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
         }
         {
             const long long b0 = static_cast<long long>(off[a.G]) * a.N * 2;
@@ -337,8 +372,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc(tmem_base, L::TMEM_COLS);
     }
+}
+
+template <int BN>
+cudaError_t launch_main(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const int32_t* group_sizes,
+                        const MxArgs& a, int grid, cudaStream_t stream) {
+    const size_t shm = MxLayout<BN>::smem_bytes(a.G);
+    auto kern = mxfp8_tc_kernel<BN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
+    if (e != cudaSuccess) return e;
+    kern<<<grid, THREADS, shm, stream>>>(tmap_a, tmap_b, group_sizes, a);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -350,11 +396,9 @@ cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, c
     mx_prep_kernel<<<prep_grid, 256, prep_shm, stream>>>(lhs_scale, rhs_scale, group_sizes, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t shm = smem_bytes(a.G);
-    e = cudaFuncSetAttribute(mxfp8_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
-    if (e != cudaSuccess) return e;
-    mxfp8_tc_kernel<<<grid, THREADS, shm, stream>>>(tmap_a, tmap_b, group_sizes, a);
-    return cudaGetLastError();
+    if (a.BN == 256) return launch_main<256>(tmap_a, tmap_b, group_sizes, a, grid, stream);
+    if (a.BN == 128) return launch_main<128>(tmap_a, tmap_b, group_sizes, a, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace rdot

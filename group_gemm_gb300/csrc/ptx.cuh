@@ -357,6 +357,17 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// 16-byte store to shared memory anywhere in the cluster (`cluster_addr` from mapa_shared).
+__device__ __forceinline__ void st_shared_cluster_zero16(uint32_t cluster_addr) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(cluster_addr), "r"(0u) : "memory");
+}
+
+// Orders this thread's generic-proxy writes to shared memory of any CTA in the cluster before its
+// later async-proxy operations (tensor-core reads of operands).
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------ packing
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     // round to nearest even, NaN preserved (cvt.rn.bf16x2.f32 packs the first operand high)

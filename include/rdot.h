@@ -69,9 +69,10 @@ typedef enum {
  * Pipeline": the M/N swap decided on M_avg = M_total / G). */
 #define RDOT_FLAG_ROW_TILES_INNER 0x1
 #define RDOT_FLAG_COL_TILES_INNER 0x2
-/* bf16 forward only: run 256 x 256 tiles on pairs of CTAs (tcgen05 cta_group::2), or force
- * 128 x BN tiles on single CTAs. By default pairs are used when the average group has at least
- * 256 rows and N >= 256. */
+/* bf16 forward and grad-weight: run 256 x 256 tiles on pairs of CTAs (tcgen05 cta_group::2), or
+ * force 128 x BN tiles on single CTAs. By default the forward uses pairs when the average group
+ * has at least 256 rows and N >= 256; the grad-weight uses single CTAs unless pairs are asked
+ * for. */
 #define RDOT_FLAG_CTA_PAIR 0x4
 #define RDOT_FLAG_NO_CTA_PAIR 0x8
 

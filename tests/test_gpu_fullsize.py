@@ -86,13 +86,15 @@ def test_full_size_bf16_forward_sampled_rows(name, flags):
     assert rel_err(got, ref) <= TOL
 
 
-def test_full_size_grad_weight_sampled_rows():
+@pytest.mark.parametrize("flags", [0, 4])
+def test_full_size_grad_weight_sampled_rows(flags):
+    """flags 0 = the plan's own choice (single-CTA tiles); 4 forces CTA pairs."""
     cfg = ri.CONFIGS["wgrad_bf16"]
     m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
     gs = ri.config_group_sizes("wgrad_bf16")
     lhs = ri.device_normal((m, k), 1000, 1.0, DEV, torch.bfloat16)
     dy = ri.device_normal((m, n), 2000, 1.0, DEV, torch.bfloat16)
-    plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32")
+    plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", flags=flags)
     dw = torch.full((g, k, n), float("nan"), dtype=torch.float32, device=DEV)
     gg.rdot_grad_weight(plan.handle, lhs, dy, torch.from_numpy(gs).to(DEV), dw, plan.workspace)
     assert plan.status() == 0

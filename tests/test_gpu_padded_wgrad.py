@@ -65,15 +65,16 @@ WG_CASES = [
 ]
 
 
+@pytest.mark.parametrize("flags", [gg.RDOT_FLAG_NO_CTA_PAIR, gg.RDOT_FLAG_CTA_PAIR])
 @pytest.mark.parametrize("m,k,n,gs", WG_CASES)
-def test_grad_weight_matches_oracle(m, k, n, gs):
+def test_grad_weight_matches_oracle(m, k, n, gs, flags):
     gs = np.asarray(gs, np.int32)
     lhs = torch.from_numpy(ri.host_normal((m, k), 81)).to(torch.bfloat16)
     dy = torch.from_numpy(ri.host_normal((m, n), 82)).to(torch.bfloat16)
     total = int(gs.sum())
     lhs[total:] = float("nan")                       # rows past the sum must never be read
     dy[total:] = float("inf")
-    plan = gg.Plan(m, k, n, gs.size, "grad_weight", "bf16", "f32")
+    plan = gg.Plan(m, k, n, gs.size, "grad_weight", "bf16", "f32", flags=flags)
     dw = torch.full((gs.size, k, n), float("nan"), dtype=torch.float32, device=DEV)
     gg.rdot_grad_weight(plan.handle, lhs.to(DEV), dy.to(DEV), torch.from_numpy(gs).to(DEV), dw, plan.workspace)
     assert plan.status() == 0
@@ -83,14 +84,17 @@ def test_grad_weight_matches_oracle(m, k, n, gs):
         assert torch.all(dw[g] == 0)
 
 
-def test_grad_weight_next_group_nan_does_not_leak():
+@pytest.mark.parametrize("flags", [gg.RDOT_FLAG_NO_CTA_PAIR, gg.RDOT_FLAG_CTA_PAIR])
+def test_grad_weight_next_group_nan_does_not_leak(flags):
     # the group after a ragged tail holds NaN rows: the tail chunk must zero them before the MMA
     gs = np.array([70, 58], np.int32)
     m, k, n = 128, 128, 128
     lhs = torch.from_numpy(ri.host_normal((m, k), 83)).to(torch.bfloat16)
     dy = torch.from_numpy(ri.host_normal((m, n), 84)).to(torch.bfloat16)
     lhs[70:] = float("nan")
-    dw = gg.grad_weight(lhs.to(DEV), dy.to(DEV), torch.from_numpy(gs).to(DEV))
+    plan = gg.Plan(m, k, n, 2, "grad_weight", "bf16", "f32", flags=flags)
+    dw = torch.empty((2, k, n), dtype=torch.float32, device=DEV)
+    gg.rdot_grad_weight(plan.handle, lhs.to(DEV), dy.to(DEV), torch.from_numpy(gs).to(DEV), dw, plan.workspace)
     assert torch.isfinite(dw[0]).all()
     ref = oracle.grad_weight(lhs, dy, gs)
     assert rel_err(dw[0], ref[0]) <= TOL
