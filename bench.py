@@ -156,6 +156,23 @@ def make_forward_inputs(name, device, seed=0):
     return cfg, gs, lhs, rhs
 
 
+def aggregate_over_ranks(t_local: float, units_local: float, world: int, device=None):
+    """Whole-job numbers from one rank's timing: the max of the ranks' elapsed times and the sum
+    of the units they processed (replicas: every rank processes units_local). Returns
+    (t_max, total_units / t_max). Uses the process group's backend (NCCL on GPUs, gloo on CPU)."""
+    if world <= 1:
+        return t_local, units_local / t_local
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([t_local, units_local], dtype=torch.float64, device=device)
+    t_max = tt[:1].clone()
+    dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    units = tt[1:].clone()
+    dist.all_reduce(units, op=dist.ReduceOp.SUM)
+    t_max = float(t_max.item())
+    return t_max, float(units.item()) / t_max
+
+
 def time_region(fn, steps, stream, barrier):
     import torch
     barrier()
@@ -227,13 +244,9 @@ def bench_ours(args, rank, world, barrier):
     status = plan.status()
     if status:
         raise RuntimeError(f"device status bits {status:#x} after the timed region")
-    t_max = t
-    if world > 1:
-        tt = torch.tensor([t], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max, rate = aggregate_over_ranks(t, flops * args.steps, world, dev)
     per_step = t_max / args.steps
-    value = flops * world / per_step / 1e12
+    value = rate / 1e12
     launch_s = t / args.steps
     achieved = flops / launch_s / 1e12
 
@@ -255,11 +268,8 @@ def bench_ours(args, rank, world, barrier):
         e2e_step()
     e2e_steps = max(3, min(args.steps, 50))
     t_e2e = time_region(e2e_step, e2e_steps, stream, barrier)
-    if world > 1:
-        tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_e2e = float(tt.item())
-    e2e = {"value": round(flops * world / (t_e2e / e2e_steps) / 1e12, 3), "unit": "TFLOP/s",
+    t_e2e, e2e_rate = aggregate_over_ranks(t_e2e, flops * e2e_steps, world, dev)
+    e2e = {"value": round(e2e_rate / 1e12, 3), "unit": "TFLOP/s",
            "h2d_bytes_per_step": int(lhs.numel() * lhs.element_size() + gs_d.numel() * 4),
            "d2h_bytes_per_step": int(out.numel() * out.element_size()),
            "note": "weights resident; activations and group_sizes copied in, output copied out each step"}
