@@ -35,7 +35,8 @@ namespace rdot {
 
 namespace {
 
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter, each draining half the columns
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int BM = 128;
 constexpr int BKB = 128;            // K bytes (= elements) per stage: 4 scale blocks
 constexpr int A_BYTES = BM * BKB;   // 16 KB
@@ -54,7 +55,7 @@ struct MxLayout {
     static constexpr int SFB_BYTES = (BN / 128) * SF_ATOM_BYTES;
     static constexpr int STAGE_BYTES = ((A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + 1023) / 1024) * 1024;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int EPI_BYTES = 4 * EpiStage<false>::BYTES;
+    static constexpr int EPI_BYTES = EPI_WARPS * EpiStage<false>::BYTES;
     static constexpr int BAR_BYTES = (2 * STAGES + 2 * NACC + 1) * 8;
     static constexpr int MISC_BYTES = 16;
     static constexpr int TMEM_COLS = 512;
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int i = 0; i < NACC; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 128);
+            mbar_init(&tempty[i], 32 * EPI_WARPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -325,21 +326,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ epilogue
+        // warp w drains TMEM lane quarter w % 4 and one half of the tile's columns
         const int q = warp & 3;
+        const int half = (warp - 2) / 4;
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < W; w += gridDim.x) {
             const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
-            const int n0 = t.nt * BN;
+            const int n0 = t.nt * BN + half * (BN / 2);
             const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
             if (!__all_sync(0xffffffffu, ready)) break;
             tc_fence_after();
-            const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            const uint32_t tbase =
+                tmem_base + acc * BN + half * (BN / 2) + (static_cast<uint32_t>(q * 32) << 16);
             const int rows_valid = t.rows - q * 32;
             __nv_bfloat16* out_rows =
                 static_cast<__nv_bfloat16*>(a.out) + (static_cast<long long>(t.row0) + q * 32) * a.N;
             uint32_t* stage = epi_stage + (warp - 2) * EpiStage<false>::WORDS;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = 0; c < BN / 64; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tbase + c * 32, v);
                 tmem_ld_wait();
@@ -363,7 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const long long per = (nv + gridDim.x - 1) / gridDim.x;
                 const long long s = per * blockIdx.x;
                 const long long e = min(nv, s + per);
-                for (long long i = s + (threadIdx.x - 64); i < e; i += 128) base[i] = make_uint4(0, 0, 0, 0);
+                for (long long i = s + (threadIdx.x - 64); i < e; i += 32 * EPI_WARPS) base[i] = make_uint4(0, 0, 0, 0);
             }
         }
     }
