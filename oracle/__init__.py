@@ -73,7 +73,7 @@ def _load():
                                                i64p, i64, dp]
         lib.orc_forward_mxfp8_rows.restype = ctypes.c_int
         lib.orc_tile_map.argtypes = [i32p, ctypes.c_int, i64, i64, ctypes.c_int, ctypes.c_int,
-                                     ctypes.c_int, i32p, i32p, i64]
+                                     ctypes.c_int, ctypes.c_int, i32p, i32p, i64]
         lib.orc_tile_map.restype = ctypes.c_int64
         lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.orc_e4m3_decode.restype = ctypes.c_double
@@ -236,16 +236,17 @@ def e8m0_decode(code: int) -> float:
     return _load().orc_e8m0_decode(int(code))
 
 
-def tile_map(group_sizes, m: int, n: int, bm: int, bn: int, m_inner: bool):
-    """Returns ``(tile_prefix int32[G+1], tiles int32[W, 3])`` of (group, row tile, col tile)."""
+def tile_map(group_sizes, m: int, n: int, bm: int, bn: int, m_inner: bool, big_mt: int = 0):
+    """Returns ``(tile_prefix int32[G+1], tiles int32[W, 3])`` of (group, row tile, col tile);
+    ``big_mt > 0`` gives the interleaved order of groups with >= big_mt row tiles."""
     gs = _gs(group_sizes)
     lib = _load()
     pref = np.zeros((gs.size + 1,), dtype=np.int32)
     total = lib.orc_tile_map(_ptr(gs, ctypes.c_int32), gs.size, int(m), int(n), int(bm), int(bn),
-                             int(bool(m_inner)), _ptr(pref, ctypes.c_int32),
+                             int(bool(m_inner)), int(big_mt), _ptr(pref, ctypes.c_int32),
                              _ptr(np.zeros((1, 3), np.int32), ctypes.c_int32), 0)
     tiles = np.zeros((max(total, 1), 3), dtype=np.int32)
     lib.orc_tile_map(_ptr(gs, ctypes.c_int32), gs.size, int(m), int(n), int(bm), int(bn),
-                     int(bool(m_inner)), _ptr(pref, ctypes.c_int32), _ptr(tiles, ctypes.c_int32),
+                     int(bool(m_inner)), int(big_mt), _ptr(pref, ctypes.c_int32), _ptr(tiles, ctypes.c_int32),
                      total)
     return pref, tiles[:total]

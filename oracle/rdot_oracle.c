@@ -189,33 +189,67 @@ int orc_forward_mxfp8_rows(const uint8_t* lhs_q, const uint8_t* lhs_s, const uin
  * Group g has ceil(m_g / bm) row tiles and ceil(n / bn) column tiles. Groups are visited in
  * index order; inside a group, m_inner = 1 visits row tiles fastest (column tile outer), and
  * m_inner = 0 visits column tiles fastest. tile_prefix[g] is the number of tiles before group g
- * (tile_prefix[G] = total). tiles [max_tiles, 3] receives (g, row tile, column tile) per work
- * item. Returns the total number of tiles (entries beyond max_tiles are not written). */
+ * in that plain order (tile_prefix[G] = total).
+ * big_mt > 0 selects the interleaved order: the plain sequence is split into the tiles of groups
+ * with at least big_mt row tiles ("big") and the rest ("small"), each keeping its order, and
+ * the two are merged so that among the first w items exactly floor(w * nb / W) are big
+ * (nb = number of big tiles, W = all tiles).
+ * tiles [max_tiles, 3] receives (g, row tile, column tile) per work item. Returns the total
+ * number of tiles (entries beyond max_tiles are not written). */
 int64_t orc_tile_map(const int32_t* group_sizes, int g_count, int64_t m, int64_t n, int bm,
-                     int bn, int m_inner, int32_t* tile_prefix, int32_t* tiles,
+                     int bn, int m_inner, int big_mt, int32_t* tile_prefix, int32_t* tiles,
                      int64_t max_tiles) {
     int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(g_count + 1));
     if (!off) return -1;
     orc_offsets(group_sizes, g_count, m, off);
     int64_t nt = (n + bn - 1) / bn;
-    int64_t w = 0;
+    int64_t total = 0;
     for (int g = 0; g < g_count; ++g) {
-        tile_prefix[g] = (int32_t)w;
-        int64_t rows = off[g + 1] - off[g];
-        int64_t mt = (rows + bm - 1) / bm;
+        tile_prefix[g] = (int32_t)total;
+        total += ((off[g + 1] - off[g] + bm - 1) / bm) * nt;
+    }
+    tile_prefix[g_count] = (int32_t)total;
+    /* the plain sequence, and for each entry whether its group is big */
+    int32_t* seq = (int32_t*)malloc(sizeof(int32_t) * 3 * (size_t)(total > 0 ? total : 1));
+    char* is_big = (char*)malloc((size_t)(total > 0 ? total : 1));
+    if (!seq || !is_big) {
+        free(off);
+        free(seq);
+        free(is_big);
+        return -1;
+    }
+    int64_t w = 0, nb = 0;
+    for (int g = 0; g < g_count; ++g) {
+        int64_t mt = (off[g + 1] - off[g] + bm - 1) / bm;
+        int big = big_mt > 0 && mt >= big_mt;
         for (int64_t outer = 0; outer < (m_inner ? nt : mt); ++outer)
             for (int64_t inner = 0; inner < (m_inner ? mt : nt); ++inner) {
-                if (w < max_tiles) {
-                    tiles[3 * w + 0] = g;
-                    tiles[3 * w + 1] = (int32_t)(m_inner ? inner : outer);
-                    tiles[3 * w + 2] = (int32_t)(m_inner ? outer : inner);
-                }
+                seq[3 * w + 0] = g;
+                seq[3 * w + 1] = (int32_t)(m_inner ? inner : outer);
+                seq[3 * w + 2] = (int32_t)(m_inner ? outer : inner);
+                is_big[w] = (char)big;
+                nb += big;
                 ++w;
             }
     }
-    tile_prefix[g_count] = (int32_t)w;
+    /* merge: walk the big and the small entries of the plain sequence with two cursors */
+    int64_t cb = 0, cs = 0, taken_big = 0;
+    for (int64_t k = 0; k < total; ++k) {
+        int pick_big = big_mt > 0 && (k + 1) * nb / total > taken_big;
+        int64_t* cur = pick_big ? &cb : &cs;
+        while (is_big[*cur] != (char)pick_big) ++*cur;
+        if (k < max_tiles) {
+            tiles[3 * k + 0] = seq[3 * *cur + 0];
+            tiles[3 * k + 1] = seq[3 * *cur + 1];
+            tiles[3 * k + 2] = seq[3 * *cur + 2];
+        }
+        ++*cur;
+        taken_big += pick_big;
+    }
+    free(seq);
+    free(is_big);
     free(off);
-    return w;
+    return total;
 }
 
 int orc_set_threads(int n) {

@@ -330,3 +330,26 @@ def test_tile_map_closed_form_and_decode(m_inner):
             assert (r, c) == (loc // nt, loc % nt)
     # static bound: sum ceil(m_g / bm) <= ceil(M / bm) + G
     assert mt.sum() <= -(-m // bm) + gs.size
+
+
+def test_tile_map_interleaved_order_properties():
+    # interleaved order: a merge of the big-group and small-group subsequences of the plain
+    # order that keeps each subsequence's order and puts floor(w * nb / W) big items among the
+    # first w; those three properties determine the sequence
+    gs = ri.zipf_routed_group_sizes(512, 32, 4, 1.1, seed=9, n_zero=3)
+    m, n, bm, bn, big_mt = int(gs.sum()), 512, 32, 256, 4
+    _, plain = oracle.tile_map(gs, m, n, bm, bn, True)
+    _, inter = oracle.tile_map(gs, m, n, bm, bn, True, big_mt)
+    mt = -(-gs.astype(np.int64) // bm)
+    assert sorted(map(tuple, plain)) == sorted(map(tuple, inter))
+    big = np.array([mt[g] >= big_mt for g, _, _ in inter])
+    W, nb = len(inter), int(big.sum())
+    assert 0 < nb < W
+    pb = [tuple(t) for t in plain if mt[t[0]] >= big_mt]
+    ps = [tuple(t) for t in plain if mt[t[0]] < big_mt]
+    assert [tuple(t) for t, b in zip(inter, big) if b] == pb
+    assert [tuple(t) for t, b in zip(inter, big) if not b] == ps
+    assert all(int(big[:w].sum()) == (w * nb) // W for w in range(W + 1))
+    # no big groups (threshold above every group): the plain order
+    _, same = oracle.tile_map(gs, m, n, bm, bn, True, 10 ** 6)
+    assert np.array_equal(same, plain)
