@@ -32,7 +32,7 @@ RDOT_F32, RDOT_BF16, RDOT_E4M3 = 0, 1, 2
 RDOT_MODE_FORWARD, RDOT_MODE_GRAD_WEIGHT, RDOT_MODE_FORWARD_MXFP8 = 0, 1, 2
 RDOT_STATUS_BIT_GROUP_SIZES, RDOT_STATUS_BIT_TIMEOUT = 0x1, 0x2
 RDOT_FLAG_ROW_TILES_INNER, RDOT_FLAG_COL_TILES_INNER = 0x1, 0x2
-RDOT_FLAG_CTA_PAIR, RDOT_FLAG_NO_CTA_PAIR = 0x4, 0x8
+RDOT_FLAG_CTA_PAIR, RDOT_FLAG_NO_CTA_PAIR, RDOT_FLAG_NATURAL_ORDER = 0x4, 0x8, 0x10
 RDOT_MAX_GROUPS = 1024
 
 # every function include/rdot.h declares

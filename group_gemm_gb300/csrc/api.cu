@@ -85,6 +85,7 @@ struct rdot_plan_s {
     int m_inner = 1;
     int grid = 1;
     bool pair = false;     // bf16 forward on CTA pairs (256 x 256 tiles)
+    int big_mt = 0;        // > 0: interleaved work order (groups with >= big_mt row tiles vs the rest)
     uint64_t timeout_ns = kDefaultTimeoutNs;
     // tensor maps cached by operand pointers (re-encoded when a pointer changes)
     const void* map_lhs_ptr = nullptr;
@@ -145,7 +146,7 @@ rdot_status check_problem(const rdot_problem* p) {
     if (p->m < 0 || p->k < 1 || p->n < 1 || p->groups < 1 || p->groups > RDOT_MAX_GROUPS)
         return RDOT_ERR_INVALID_ARG;
     if (p->m > 0x7fffffffLL || p->k > 0x7fffffffLL || p->n > 0x7fffffffLL) return RDOT_ERR_UNSUPPORTED;
-    if (p->flags & ~0xF) return RDOT_ERR_INVALID_ARG;
+    if (p->flags & ~0x1F) return RDOT_ERR_INVALID_ARG;
     if ((p->flags & RDOT_FLAG_CTA_PAIR) && (p->flags & RDOT_FLAG_NO_CTA_PAIR)) return RDOT_ERR_INVALID_ARG;
     if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256) return RDOT_ERR_UNSUPPORTED;
     switch (p->mode) {
@@ -246,6 +247,9 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             pl->grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(bound, clusters)));
         else
             pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
+        // small average groups: interleave the tiles of large groups (4+ row tiles) with the
+        // others so every wave mixes tensor-core-bound and weight-streaming work
+        pl->big_mt = (!want_pair && !(p.flags & RDOT_FLAG_NATURAL_ORDER)) ? 4 : 0;
     } else if (p.mode == RDOT_MODE_FORWARD_MXFP8) {
         if (prop.major != 10) {
             delete pl;
@@ -370,6 +374,7 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
     a.G = p.groups;
     a.NT = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
     a.m_inner = plan->m_inner;
+    a.big_mt = plan->big_mt;
     a.status = static_cast<int32_t*>(workspace);
     a.timeout_ns = plan->timeout_ns;
     cudaError_t e;
@@ -621,7 +626,7 @@ rdot_status rdot_debug_offsets_tilemap(rdot_plan_t plan, const int32_t* group_si
     DeviceGuard dg(plan->device);
     const int nt = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
     cudaError_t e = launch_scan_export(group_sizes, p.groups, static_cast<int>(p.m), plan->tile_m, nt, plan->m_inner,
-                                       offsets, tile_prefix, tiles, tiles ? max_tiles : 0,
+                                       plan->big_mt, offsets, tile_prefix, tiles, tiles ? max_tiles : 0,
                                        static_cast<int32_t*>(workspace), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "scan export launch");
     return RDOT_OK;

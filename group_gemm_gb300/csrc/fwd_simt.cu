@@ -124,14 +124,17 @@ __global__ void __launch_bounds__(THREADS) fwd_simt_kernel(const float* __restri
 }
 
 __global__ void scan_export_kernel(const int32_t* __restrict__ gs, int G, int M, int BM, int NT, int m_inner,
-                                   int32_t* offsets, int32_t* tile_prefix, int32_t* tiles, long long max_tiles,
-                                   int32_t* status) {
+                                   int big_mt, int32_t* offsets, int32_t* tile_prefix, int32_t* tiles,
+                                   long long max_tiles, int32_t* status) {
     extern __shared__ int32_t table[];
     int32_t* off = table;
     int32_t* tprefix = table + G + 1;
+    int32_t* psmall = table + 2 * (G + 1);
+    int32_t* pbig = table + 3 * (G + 1);
     if (threadIdx.x < 32) {
         const int bad = group_scan_warp(gs, G, M, BM, NT, off, tprefix);
         if (bad && threadIdx.x == 0 && status) atomicOr(status, bad);
+        if (big_mt > 0) split_prefix_warp(off, G, BM, NT, big_mt, pbig, psmall);
     }
     __syncthreads();
     for (int i = threadIdx.x; i <= G; i += blockDim.x) {
@@ -141,7 +144,9 @@ __global__ void scan_export_kernel(const int32_t* __restrict__ gs, int G, int M,
     if (tiles) {
         const long long W = min(static_cast<long long>(tprefix[G]), max_tiles);
         for (long long w = threadIdx.x; w < W; w += blockDim.x) {
-            const Tile t = decode_tile(static_cast<int>(w), tprefix, off, G, BM, NT, m_inner != 0);
+            const Tile t = big_mt > 0
+                               ? decode_tile_split(static_cast<int>(w), pbig, psmall, off, G, BM, NT, m_inner != 0)
+                               : decode_tile(static_cast<int>(w), tprefix, off, G, BM, NT, m_inner != 0);
             tiles[3 * w + 0] = t.g;
             tiles[3 * w + 1] = t.mt;
             tiles[3 * w + 2] = t.nt;
@@ -178,12 +183,12 @@ cudaError_t launch_fwd_simt(const float* lhs, const float* rhs, const FwdArgs& a
     return cudaGetLastError();
 }
 
-cudaError_t launch_scan_export(const int32_t* group_sizes, int G, int M, int BM, int NT, int m_inner,
+cudaError_t launch_scan_export(const int32_t* group_sizes, int G, int M, int BM, int NT, int m_inner, int big_mt,
                                int32_t* offsets, int32_t* tile_prefix, int32_t* tiles, long long max_tiles,
                                int32_t* status, cudaStream_t stream) {
-    const size_t shm = sizeof(int32_t) * 2 * (G + 1);
-    scan_export_kernel<<<1, 256, shm, stream>>>(group_sizes, G, M, BM, NT, m_inner, offsets, tile_prefix, tiles,
-                                                max_tiles, status);
+    const size_t shm = sizeof(int32_t) * 4 * (G + 1);
+    scan_export_kernel<<<1, 256, shm, stream>>>(group_sizes, G, M, BM, NT, m_inner, big_mt, offsets, tile_prefix,
+                                                tiles, max_tiles, status);
     return cudaGetLastError();
 }
 

@@ -47,7 +47,7 @@ struct TcLayout {
     static constexpr int MISC_BYTES = 16;                          // tmem base, abort flag
     static constexpr int TMEM_COLS = 2 * BN;
     static size_t smem_bytes(int G) {
-        return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+        return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 3 * (G + 1);
     }
 };
 
@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
     int32_t* off = reinterpret_cast<int32_t*>(smem + L::RING_BYTES + L::EPI_BYTES + L::BAR_BYTES + L::MISC_BYTES);
-    int32_t* tprefix = off + a.G + 1;
+    int32_t* tprefix = off + a.G + 1;       // natural order; the small list in interleaved order
+    int32_t* pbig = off + 2 * (a.G + 1);    // interleaved order: the big list
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -94,13 +95,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 2) {
         const int bad = group_scan_warp(a.group_sizes, a.G, a.M, TC_BM, a.NT, off, tprefix);
         if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
+        if (a.big_mt > 0) split_prefix_warp(off, a.G, TC_BM, a.NT, a.big_mt, pbig, tprefix);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem_base = *tmem_holder;
-    const int W = tprefix[a.G];
+    const int W = tprefix[a.G] + (a.big_mt > 0 ? pbig[a.G] : 0);
+    auto decode = [&](int w) {
+        return a.big_mt > 0 ? decode_tile_split(w, pbig, tprefix, off, a.G, TC_BM, a.NT, a.m_inner != 0)
+                            : decode_tile(w, tprefix, off, a.G, TC_BM, a.NT, a.m_inner != 0);
+    };
     const int KB = (a.K + TC_BK - 1) / TC_BK;
     const bool m_inner = a.m_inner != 0;
     const WaitGuard guard{abort_flag, a.status, a.timeout_ns};
@@ -112,7 +118,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t issued_mask = 0, issued_phase = 0;   // stages with a load in flight, and its phase
             bool ok = true;
             for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
-                const Tile t = decode_tile(w, tprefix, off, a.G, TC_BM, a.NT, m_inner);
+                const Tile t = decode(w);
                 const int n0 = t.nt * BN;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
@@ -196,7 +202,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < W; w += gridDim.x) {
-            const Tile t = decode_tile(w, tprefix, off, a.G, TC_BM, a.NT, m_inner);
+            const Tile t = decode(w);
             const int n0 = t.nt * BN;
             // the warp leaves together: tcgen05.ld below must be executed by all 32 lanes
             const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);

@@ -22,6 +22,7 @@ struct FwdArgs {
     int M, K, N, G;
     int NT;                      // column tiles per group
     int m_inner;                 // 1: row tiles fastest inside a group
+    int big_mt;                  // > 0: interleave groups with >= big_mt row tiles with the others
     int32_t* status;             // device status word (may be null)
     uint64_t timeout_ns;         // bounded-wait limit
 };
@@ -104,7 +105,7 @@ cudaError_t launch_pad_gather(const void* out_pad, const int32_t* gs, void* out,
                               long long row_bytes, int grid, cudaStream_t stream);
 
 // Debug export of the scan and the tile decode (fwd_simt.cu).
-cudaError_t launch_scan_export(const int32_t* group_sizes, int G, int M, int BM, int NT, int m_inner,
+cudaError_t launch_scan_export(const int32_t* group_sizes, int G, int M, int BM, int NT, int m_inner, int big_mt,
                                int32_t* offsets, int32_t* tile_prefix, int32_t* tiles, long long max_tiles,
                                int32_t* status, cudaStream_t stream);
 

@@ -84,6 +84,49 @@ __device__ __forceinline__ int group_scan_warp(const int32_t* __restrict__ group
     return bad ? 0x1 : 0;
 }
 
+// Interleaved order. Groups with at least `big_mt` row tiles form the "big" list, the others the
+// "small" list; each list keeps the group-local order above. Work item w goes to the big list iff
+// floor((w+1) nb / W) > floor(w nb / W) (nb = tiles of the big list, W = all tiles), so every
+// wave of persistent CTAs mixes tiles of large, compute-heavy groups with tiles of small groups
+// whose cost is streaming their weights, instead of alternating between the two.
+// Fills pref_big[g] / pref_small[g] (tiles of the list before group g; index G holds the totals).
+__device__ __forceinline__ void split_prefix_warp(const int32_t* off, int G, int BM, int NT, int big_mt,
+                                                  int32_t* pref_big, int32_t* pref_small) {
+    __syncwarp();   // offsets were written by all lanes of this warp
+    const int lane = threadIdx.x & 31;
+    const int chunk = (G + 31) / 32;
+    const int g0 = min(lane * chunk, G);
+    const int g1 = min(g0 + chunk, G);
+    long long mb = 0, ms = 0;
+    for (int g = g0; g < g1; ++g) {
+        const long long t = (off[g + 1] - off[g] + BM - 1) / BM;
+        if (t >= big_mt) mb += t * NT;
+        else ms += t * NT;
+    }
+    long long ib = mb, is = ms;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const long long vb = __shfl_up_sync(0xffffffffu, ib, d);
+        const long long vs = __shfl_up_sync(0xffffffffu, is, d);
+        if (lane >= d) {
+            ib += vb;
+            is += vs;
+        }
+    }
+    long long rb = ib - mb, rs = is - ms;
+    for (int g = g0; g < g1; ++g) {
+        pref_big[g] = static_cast<int32_t>(rb);
+        pref_small[g] = static_cast<int32_t>(rs);
+        const long long t = (off[g + 1] - off[g] + BM - 1) / BM;
+        if (t >= big_mt) rb += t * NT;
+        else rs += t * NT;
+    }
+    if (lane == 31) {
+        pref_big[G] = static_cast<int32_t>(ib);
+        pref_small[G] = static_cast<int32_t>(is);
+    }
+}
+
 struct Tile {
     int g;      // group
     int mt;     // row tile inside the group
@@ -92,8 +135,8 @@ struct Tile {
     int rows;   // valid rows of the tile (<= BM)
 };
 
-__device__ __forceinline__ Tile decode_tile(int w, const int32_t* tile_prefix, const int32_t* off, int G, int BM,
-                                            int NT, bool m_inner) {
+__device__ __forceinline__ Tile decode_in_list(int w, const int32_t* tile_prefix, const int32_t* off, int G, int BM,
+                                               int NT, bool m_inner) {
     int lo = 0, hi = G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -115,6 +158,23 @@ __device__ __forceinline__ Tile decode_tile(int w, const int32_t* tile_prefix, c
     t.row0 = off[lo] + t.mt * BM;
     t.rows = min(BM, off[lo + 1] - t.row0);
     return t;
+}
+
+// Natural order: groups in index order.
+__device__ __forceinline__ Tile decode_tile(int w, const int32_t* tile_prefix, const int32_t* off, int G, int BM,
+                                            int NT, bool m_inner) {
+    return decode_in_list(w, tile_prefix, off, G, BM, NT, m_inner);
+}
+
+// Interleaved order (see split_prefix_warp).
+__device__ __forceinline__ Tile decode_tile_split(int w, const int32_t* pref_big, const int32_t* pref_small,
+                                                  const int32_t* off, int G, int BM, int NT, bool m_inner) {
+    const long long nb = pref_big[G];
+    const long long W = nb + pref_small[G];
+    const long long before = (static_cast<long long>(w) * nb) / W;        // big items among the first w
+    const bool big = (static_cast<long long>(w + 1) * nb) / W > before;
+    return big ? decode_in_list(static_cast<int>(before), pref_big, off, G, BM, NT, m_inner)
+               : decode_in_list(static_cast<int>(w - before), pref_small, off, G, BM, NT, m_inner);
 }
 
 }  // namespace rdot

@@ -47,7 +47,7 @@ def test_status_strings_and_version(lib):
     (dict(m=16, k=8, n=8, groups=gg.RDOT_MAX_GROUPS + 1), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=-1, k=8, n=8, groups=1), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=16, k=12, n=8, groups=1, in_dtype=gg.RDOT_BF16), gg.RDOT_ERR_UNSUPPORTED),
-    (dict(m=16, k=8, n=8, groups=1, flags=0x10), gg.RDOT_ERR_INVALID_ARG),
+    (dict(m=16, k=8, n=8, groups=1, flags=0x20), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=16, k=8, n=8, groups=1, flags=gg.RDOT_FLAG_CTA_PAIR | gg.RDOT_FLAG_NO_CTA_PAIR), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=16, k=8, n=8, groups=1, tile_n=96), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=8, n=8, groups=1, mode=7), gg.RDOT_ERR_INVALID_ARG),
