@@ -239,3 +239,20 @@ def test_misaligned_pointer_is_rejected_before_launch():
                                 ctypes.c_void_p(gs.data_ptr()), ctypes.c_void_p(out.data_ptr()),
                                 ctypes.c_void_p(plan.workspace.data_ptr()), None)
     assert st == gg.RDOT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("mode", ["f32", "bf16_single", "bf16_pair"])
+def test_max_groups_forward(mode):
+    """G = RDOT_MAX_GROUPS (the largest shared-memory group table) with mostly tiny groups."""
+    rng = np.random.default_rng(71)
+    g = gg.RDOT_MAX_GROUPS
+    gs = rng.integers(0, 5, size=g).astype(np.int32)
+    gs[[3, 500]] = [300, 257]
+    m, k, n = int(gs.sum()) + 40, 64, 256
+    dt = torch.float32 if mode == "f32" else torch.bfloat16
+    lhs = torch.from_numpy(ri.host_normal((m, k), 72)).to(dt)
+    rhs = torch.from_numpy(ri.host_normal((g, k, n), 73, 0.05)).to(dt)
+    flags = {"f32": 0, "bf16_single": gg.RDOT_FLAG_NO_CTA_PAIR, "bf16_pair": gg.RDOT_FLAG_CTA_PAIR}[mode]
+    out, status, _ = run_forward(lhs, rhs, gs, flags=flags)
+    assert status == 0
+    assert rel_err(out, oracle.forward(lhs, rhs, gs)) <= (TOL_F32 if mode == "f32" else TOL_BF16)

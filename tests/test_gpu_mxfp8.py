@@ -91,3 +91,14 @@ def test_mxfp8_workspace_is_reported():
     plan = gg.Plan(65536, 4096, 1536, 128, "forward_mxfp8", "e4m3", "bf16")
     ws = gg.rdot_workspace_size(plan.handle)
     assert ws > 256   # scale blocks live in the workspace
+
+
+def test_mxfp8_max_groups():
+    rng = np.random.default_rng(93)
+    g = 1024
+    gs = rng.integers(0, 4, size=g).astype(np.int32)
+    gs[11] = 300
+    aq, as_, bq, bs, gs = make_case(int(gs.sum()), 128, 256, gs, 94)
+    out, status = run(aq, as_, bq, bs, gs)
+    assert status == 0
+    assert rel_err(out, oracle.forward_mxfp8(aq, as_, bq, bs, gs)) <= TOL

@@ -98,3 +98,22 @@ def test_grad_weight_next_group_nan_does_not_leak(flags):
     assert torch.isfinite(dw[0]).all()
     ref = oracle.grad_weight(lhs, dy, gs)
     assert rel_err(dw[0], ref[0]) <= TOL
+
+
+@pytest.mark.parametrize("flags", [gg.RDOT_FLAG_NO_CTA_PAIR, gg.RDOT_FLAG_CTA_PAIR])
+def test_grad_weight_max_groups(flags):
+    rng = np.random.default_rng(85)
+    g = gg.RDOT_MAX_GROUPS
+    gs = rng.integers(0, 3, size=g).astype(np.int32)
+    gs[7] = 200
+    m, k, n = int(gs.sum()), 256, 256
+    lhs = torch.from_numpy(ri.host_normal((m, k), 86)).to(torch.bfloat16)
+    dy = torch.from_numpy(ri.host_normal((m, n), 87)).to(torch.bfloat16)
+    plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", flags=flags)
+    dw = torch.full((g, k, n), float("nan"), dtype=torch.float32, device=DEV)
+    gg.rdot_grad_weight(plan.handle, lhs.to(DEV), dy.to(DEV), torch.from_numpy(gs).to(DEV), dw, plan.workspace)
+    assert plan.status() == 0
+    sel = np.array([0, 7, 8, g - 1] + list(np.nonzero(gs)[0][:6]))
+    ref = oracle.grad_weight_rows(lhs, dy, gs, np.repeat(sel, k), np.tile(np.arange(k), sel.size))
+    got = dw[torch.from_numpy(sel).to(DEV)].reshape(-1, n)
+    assert rel_err(got, ref) <= TOL

@@ -66,3 +66,13 @@ def test_no_alloc_forward_fp32_path():
         torch.cuda.synchronize()
         assert _rel(got, ref) <= 1e-5
     assert np.all(got[240:].cpu().numpy() == 0)
+
+
+def test_no_alloc_rejects_plans_needing_more_scratch():
+    gg.build()
+    lib = gg.load()
+    plan = gg.Plan(4096, 256, 256, 8, "forward_mxfp8", "e4m3", "bf16")   # scale blocks need more than 256 B
+    assert gg.rdot_workspace_size(plan.handle) > 256
+    st = lib.rdot_forward_no_alloc(plan.handle, None, None, None, None, None)
+    assert st == gg.RDOT_ERR_UNSUPPORTED
+    assert "static scratch" in gg.rdot_last_cuda_error()
