@@ -247,9 +247,9 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             pl->grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(bound, clusters)));
         else
             pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
-        // small average groups: interleave the tiles of large groups (4+ row tiles) with the
+        // small average groups: interleave the tiles of groups with 2+ row tiles with the
         // others so every wave mixes tensor-core-bound and weight-streaming work
-        pl->big_mt = (!want_pair && !(p.flags & RDOT_FLAG_NATURAL_ORDER)) ? 4 : 0;
+        pl->big_mt = (!want_pair && !(p.flags & RDOT_FLAG_NATURAL_ORDER)) ? 2 : 0;
     } else if (p.mode == RDOT_MODE_FORWARD_MXFP8) {
         if (prop.major != 10) {
             delete pl;

@@ -108,7 +108,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                             : decode_tile(w, tprefix, off, a.G, TC_BM, a.NT, a.m_inner != 0);
     };
     const int KB = (a.K + TC_BK - 1) / TC_BK;
-    const bool m_inner = a.m_inner != 0;
     const WaitGuard guard{abort_flag, a.status, a.timeout_ns};
 
     if (warp == 0) {
@@ -205,8 +204,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const Tile t = decode(w);
             const int n0 = t.nt * BN;
             // the warp leaves together: tcgen05.ld below must be executed by all 32 lanes
-            const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
-            if (!__all_sync(0xffffffffu, ready)) break;
+            const bool ready = mbar_wait_warp(&tfull[acc], acc_phase, guard);
+            if (!ready) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
             // this warp's 32 rows of the tile, stored 32 columns at a time

@@ -208,8 +208,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         for (int w = cluster; w < W; w += nclusters) {
             const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
             const int n0 = t.nt * BN;
-            const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
-            if (!__all_sync(0xffffffffu, ready)) break;
+            const bool ready = mbar_wait_warp(&tfull[acc], acc_phase, guard);
+            if (!ready) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
             const int first = 128 * static_cast<int>(rank) + q * 32;    // first tile row of this warp

@@ -333,8 +333,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int w = blockIdx.x; w < W; w += gridDim.x) {
             const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
             const int n0 = t.nt * BN + half * (BN / 2);
-            const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
-            if (!__all_sync(0xffffffffu, ready)) break;
+            const bool ready = mbar_wait_warp(&tfull[acc], acc_phase, guard);
+            if (!ready) break;
             tc_fence_after();
             const uint32_t tbase =
                 tmem_base + acc * BN + half * (BN / 2) + (static_cast<uint32_t>(q * 32) << 16);

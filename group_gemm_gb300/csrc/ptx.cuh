@@ -90,6 +90,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// Warp-wide wait: lane 0 alone waits on the barrier and the result is broadcast. A wait by all
+// 32 lanes costs the wake-up of the slowest suspended lane on every call; a shuffle only costs a
+// warp synchronisation. The lanes leave converged, as .sync.aligned tcgen05 instructions need.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitGuard& g) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, g) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // --------------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -161,13 +161,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             const WgTile t = wg_decode(w, a.KT, a.NT, off);
             const int nchunks_rows = (t.rows + ROWS - 1) / ROWS;
             if (nchunks_rows == 0) continue;                 // empty group: the epilogue writes zeros
-            const bool free_acc = mbar_wait(&tempty[acc], acc_phase ^ 1, guard);
-            if (!__all_sync(0xffffffffu, free_acc)) break;
+            const bool free_acc = mbar_wait_warp(&tempty[acc], acc_phase ^ 1, guard);
+            if (!free_acc) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * BN;
             for (int c = 0; c < nchunks_rows; ++c) {
-                const bool landed = mbar_wait(&full[stage], phase, guard);
-                if (!__all_sync(0xffffffffu, landed)) {
+                const bool landed = mbar_wait_warp(&full[stage], phase, guard);
+                if (!landed) {
                     ok = false;
                     break;
                 }
@@ -244,8 +244,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (rows_valid > 0) store_block_32x32<true>(z, stage, drows + col, a.N, rows_valid, a.N - col);
                 continue;
             }
-            const bool ready = mbar_wait(&tfull[acc], acc_phase, guard);
-            if (!__all_sync(0xffffffffu, ready)) break;
+            const bool ready = mbar_wait_warp(&tfull[acc], acc_phase, guard);
+            if (!ready) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1

@@ -75,8 +75,8 @@ typedef enum {
  * for. */
 #define RDOT_FLAG_CTA_PAIR 0x4
 #define RDOT_FLAG_NO_CTA_PAIR 0x8
-/* bf16 forward on single CTAs: by default work items of groups with 4 or more row tiles are
- * interleaved in proportion with those of smaller groups, so that every wave mixes
+/* bf16 forward on single CTAs: by default work items of groups with 2 or more row tiles are
+ * interleaved in proportion with those of single-tile groups, so that every wave mixes
  * tensor-core-bound and weight-streaming tiles; this flag keeps plain group order. The order is
  * visible through rdot_debug_offsets_tilemap. */
 #define RDOT_FLAG_NATURAL_ORDER 0x10

@@ -65,8 +65,8 @@ def test_scan_and_tile_map_bit_exact(gs, m, in_dtype, n, flags):
     gs = np.asarray(gs, np.int32)
     plan = gg.Plan(m, 64, n, gs.size, "forward", in_dtype, in_dtype, flags=flags)
     info = plan.info
-    # single-CTA bf16 plans interleave groups of 4+ row tiles with the rest unless told not to
-    big_mt = 4 if (in_dtype == "bf16" and info["tile_m"] == 128 and not flags & gg.RDOT_FLAG_NATURAL_ORDER) else 0
+    # single-CTA bf16 plans interleave groups of 2+ row tiles with the rest unless told not to
+    big_mt = 2 if (in_dtype == "bf16" and info["tile_m"] == 128 and not flags & gg.RDOT_FLAG_NATURAL_ORDER) else 0
     off_ref, flags_ref = oracle.offsets(gs, m)
     pref_ref, tiles_ref = oracle.tile_map(gs, m, n, info["tile_m"], info["tile_n"], bool(info["m_inner"]), big_mt)
     gs_d = torch.from_numpy(gs).to(DEV)
