@@ -452,6 +452,13 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                      steps, stream)
     res["mxfp8"]["other_tile"] = {"tile": f"{other.info['tile_m']}x{other.info['tile_n']}",
                                   "tflops": round(fl / t2 / 1e12, 3), "ms": round(t2 * 1e3, 4)}
+    pair = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16", device=dev.index,
+                   flags=gg.RDOT_FLAG_NO_CTA_PAIR if plan.info["tile_m"] == 256 else gg.RDOT_FLAG_CTA_PAIR)
+    t3 = _time_steps(lambda: gg.rdot_forward_mxfp8(pair.handle, aq, as_, bq, bs, gs_d, out, pair.workspace, stream),
+                     steps, stream)
+    res["mxfp8"]["other_pairing"] = {"tile": f"{pair.info['tile_m']}x{pair.info['tile_n']}",
+                                     "tflops": round(fl / t3 / 1e12, 3), "ms": round(t3 * 1e3, 4),
+                                     "status": pair.status()}
     del aq, as_, bq, bs, out
     torch.cuda.empty_cache()
     return res

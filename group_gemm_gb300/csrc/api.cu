@@ -91,6 +91,9 @@ struct rdot_plan_s {
     const void* map_lhs_ptr = nullptr;
     const void* map_rhs_ptr = nullptr;
     CUtensorMap map_a{}, map_b{};
+    // MXFP8 on CTA pairs: the scale blocks in the workspace, cached by workspace pointer
+    const void* map_ws_ptr = nullptr;
+    CUtensorMap map_sfa{}, map_sfb{};
     // the padded baseline's own lhs map (over the padded buffer)
     const void* pad_map_ptr = nullptr;
     int64_t pad_map_rows = 0;
@@ -102,7 +105,8 @@ int rdot::plan_device(rdot_plan_t plan) { return plan->device; }
 namespace {
 
 rdot_status encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) {
         g_last_cuda_error = "cuTensorMapEncodeTiled entry point unavailable";
@@ -113,7 +117,7 @@ rdot_status encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         g_last_cuda_error = "cuTensorMapEncodeTiled (2d) failed: " + std::to_string(static_cast<int>(r));
         return RDOT_ERR_CUDA;
@@ -256,15 +260,32 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             return RDOT_ERR_UNSUPPORTED;
         }
         pl->kind = 3;
-        pl->tile_m = TC_BM;
-        pl->tile_n = p.tile_n ? p.tile_n : (p.n >= 256 ? 256 : 128);
+        const bool want_pair = (p.flags & RDOT_FLAG_CTA_PAIR) != 0;
+        if (want_pair && p.tile_n == 128) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        int clusters = 0;
+        if (want_pair) {
+            clusters = mxfp8_pair_max_clusters(p.groups);
+            if (clusters <= 0) {
+                delete pl;
+                return cuda_fail(cudaGetLastError(), "cudaOccupancyMaxActiveClusters");
+            }
+        }
+        pl->pair = want_pair;
+        pl->tile_m = want_pair ? TC2_BM : TC_BM;
+        pl->tile_n = want_pair ? 256 : (p.tile_n ? p.tile_n : (p.n >= 256 ? 256 : 128));
         const int nt = static_cast<int>((p.n + pl->tile_n - 1) / pl->tile_n);
-        const long long bound = forward_tile_bound(p.m, p.groups, TC_BM, nt);
+        const long long bound = forward_tile_bound(p.m, p.groups, pl->tile_m, nt);
         if (bound > 0x7fffffffLL) {
             delete pl;
             return RDOT_ERR_UNSUPPORTED;
         }
-        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
+        if (want_pair)
+            pl->grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(bound, clusters)));
+        else
+            pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
     } else if (p.mode == RDOT_MODE_GRAD_WEIGHT) {
         if (prop.major != 10) {
             delete pl;
@@ -312,27 +333,31 @@ rdot_status rdot_plan_destroy(rdot_plan_t plan) {
 }
 
 namespace {
-// MXFP8 workspace: status word, then the reordered scale blocks.
+// MXFP8 workspace: status word, then the reordered scale blocks. A row tile of the pair kernel
+// (256 rows) holds two 128-row scale blocks per K stage.
 struct MxLayout {
     size_t sfa_off, sfb_off, total;
+    size_t sfa_blocks, sfb_blocks;
     int ks, nt;
 };
 
-MxLayout mx_layout(const rdot_problem& p, int bn) {
+MxLayout mx_layout(const rdot_problem& p, int bm, int bn) {
     MxLayout l{};
     l.ks = static_cast<int>((p.k + 127) / 128);
     l.nt = static_cast<int>((p.n + bn - 1) / bn);
-    const size_t mtiles = static_cast<size_t>((p.m + TC_BM - 1) / TC_BM) + static_cast<size_t>(p.groups);
+    const size_t mtiles = static_cast<size_t>((p.m + bm - 1) / bm) + static_cast<size_t>(p.groups);
+    l.sfa_blocks = mtiles * l.ks * (bm / TC_BM);
+    l.sfb_blocks = static_cast<size_t>(p.groups) * l.nt * l.ks;
     l.sfa_off = kWorkspaceBytes;
-    l.sfb_off = l.sfa_off + mtiles * l.ks * MX_SFA_BLOCK_BYTES;
-    l.total = l.sfb_off + static_cast<size_t>(p.groups) * l.nt * l.ks * (bn / 128) * MX_SFB_ATOM_BYTES;
+    l.sfb_off = l.sfa_off + l.sfa_blocks * MX_SFA_BLOCK_BYTES;
+    l.total = l.sfb_off + l.sfb_blocks * (bn / 128) * MX_SFB_ATOM_BYTES;
     return l;
 }
 }  // namespace
 
 rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes) {
     if (!plan || !bytes) return RDOT_ERR_INVALID_ARG;
-    *bytes = plan->kind == 3 ? mx_layout(plan->p, plan->tile_n).total : kWorkspaceBytes;
+    *bytes = plan->kind == 3 ? mx_layout(plan->p, plan->tile_m, plan->tile_n).total : kWorkspaceBytes;
     return RDOT_OK;
 }
 
@@ -429,7 +454,7 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = rhs;
     }
-    const MxLayout l = mx_layout(p, plan->tile_n);
+    const MxLayout l = mx_layout(p, plan->tile_m, plan->tile_n);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     MxArgs a{};
     a.out = out;
@@ -448,8 +473,28 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
     a.sfa_vec = (p.k % 128 == 0 && (reinterpret_cast<uintptr_t>(lhs_scale) & 3u) == 0) ? 1 : 0;
     a.status = static_cast<int32_t*>(workspace);
     a.timeout_ns = plan->timeout_ns;
-    cudaError_t e = launch_mxfp8(plan->map_a, plan->map_b, lhs_scale, rhs_scale, group_sizes, a, plan->grid,
-                                 4 * plan->sm_count, s);
+    a.pair = plan->pair ? 1 : 0;
+    cudaError_t e;
+    if (plan->pair) {
+        // the pair kernel fetches the scale blocks by TMA (each CTA's copy completes on the even
+        // CTA's barrier): 32-bit views of 512-byte (lhs) and 1 KB (rhs) blocks, one block a box
+        if (plan->map_ws_ptr != workspace) {
+            rdot_status st = encode_2d(&plan->map_sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.sfa, MX_SFA_BLOCK_BYTES / 4,
+                                       l.sfa_blocks, MX_SFA_BLOCK_BYTES, MX_SFA_BLOCK_BYTES / 4, 1,
+                                       CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (st != RDOT_OK) return st;
+            st = encode_2d(&plan->map_sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.sfb, 2 * MX_SFB_ATOM_BYTES / 4,
+                           l.sfb_blocks, 2 * MX_SFB_ATOM_BYTES, 2 * MX_SFB_ATOM_BYTES / 4, 1,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (st != RDOT_OK) return st;
+            plan->map_ws_ptr = workspace;
+        }
+        e = launch_mxfp8_pair(plan->map_a, plan->map_b, plan->map_sfa, plan->map_sfb, lhs_scale, rhs_scale,
+                              group_sizes, a, plan->grid, 4 * plan->sm_count, s);
+    } else {
+        e = launch_mxfp8(plan->map_a, plan->map_b, lhs_scale, rhs_scale, group_sizes, a, plan->grid,
+                         4 * plan->sm_count, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "mxfp8 launch");
     return RDOT_OK;
 }

@@ -66,4 +66,26 @@ __device__ __forceinline__ void store_block_32x32(const uint32_t (&v)[32], uint3
     __syncwarp();
 }
 
+// The bf16 store of store_block_32x32 for a block already packed: p[j] holds columns 2j, 2j+1 of
+// row `lane` as bf16x2. Lets an epilogue release tensor memory before its global stores.
+__device__ __forceinline__ void store_packed_bf16_32x32(const uint32_t (&p)[16], uint32_t* stage, void* out,
+                                                        long long ld, int rows_valid, int cols_valid) {
+    using S = EpiStage<false>;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) stage[lane * S::ROW_WORDS + j] = p[j];
+    __syncwarp();
+    const int rr = lane >> 2, w4 = (lane & 3) * 4;
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int row = it * 8 + rr;
+        if (row < rows_valid && 2 * w4 < cols_valid) {
+            const uint32_t* s = stage + row * S::ROW_WORDS + w4;
+            *reinterpret_cast<uint4*>(o + row * ld + 2 * w4) = make_uint4(s[0], s[1], s[2], s[3]);
+        }
+    }
+    __syncwarp();
+}
+
 }  // namespace rdot

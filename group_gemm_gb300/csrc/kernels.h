@@ -83,6 +83,7 @@ struct MxArgs {
     uint8_t* sfb;                // workspace: reordered rhs scales, [G, NT, KS] blocks of BN/128 atoms
     int sfb_vec;                 // rhs_scale rows can be read as 32-bit words (N % 4 == 0, aligned)
     int sfa_vec;                 // lhs_scale rows can be read as 32-bit words (K % 128 == 0, aligned)
+    int pair;                    // 1: 256-row tiles on CTA pairs (sfa blocks per 128-row half)
     int32_t* status;
     uint64_t timeout_ns;
 };
@@ -97,6 +98,17 @@ cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, c
 cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int grid,
                              cudaStream_t stream);
 int wgrad_tc2_max_clusters(int G);
+
+// The scale reorder alone (mxfp8_tc.cu), and the CTA-pair MXFP8 GEMM (mxfp8_tc2.cu): 256 x 256
+// tiles; tmap_sfa / tmap_sfb view the reordered scale blocks as rows of 32-bit words (box of one
+// block). Launches the reorder, then the GEMM.
+cudaError_t launch_mx_prep(const uint8_t* lhs_scale, const uint8_t* rhs_scale, const int32_t* group_sizes,
+                           const MxArgs& a, int prep_grid, cudaStream_t stream);
+cudaError_t launch_mxfp8_pair(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const CUtensorMap& tmap_sfa,
+                              const CUtensorMap& tmap_sfb, const uint8_t* lhs_scale, const uint8_t* rhs_scale,
+                              const int32_t* group_sizes, const MxArgs& a, int grid, int prep_grid,
+                              cudaStream_t stream);
+int mxfp8_pair_max_clusters(int G);
 
 // Padded-dense baseline data movement (padded.cu).
 cudaError_t launch_pad_scatter(const void* lhs, const int32_t* gs, void* lhs_pad, int32_t* uniform_gs, int M, int G,

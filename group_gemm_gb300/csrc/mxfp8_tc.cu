@@ -81,27 +81,33 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
     extern __shared__ int32_t table[];
     int32_t* off = table;
     int32_t* mt_prefix = table + a.G + 1;
-    if (threadIdx.x < 32) (void)group_scan_warp(gs, a.G, a.M, BM, 1, off, mt_prefix);
+    // row tiles of the GEMM: 128 rows, or 256 rows on CTA pairs (two 128-row halves per tile)
+    const int SBM = a.pair ? 256 : BM;
+    const int halves = a.pair ? 2 : 1;
+    if (threadIdx.x < 32) (void)group_scan_warp(gs, a.G, a.M, SBM, 1, off, mt_prefix);
     __syncthreads();
     const int KB32 = a.K / 32;
     const long long Tm = mt_prefix[a.G];
-    const long long sfa_blocks = Tm * a.KS;
+    const long long sfa_blocks = Tm * a.KS * halves;
     const long long sfb_blocks = static_cast<long long>(a.G) * a.NT128 * a.KS;
     const int lane = threadIdx.x & 31;
     const long long warp0 = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
     const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
     for (long long b = warp0; b < sfa_blocks + sfb_blocks; b += nwarps) {
         if (b < sfa_blocks) {
-            const int T = static_cast<int>(b / a.KS);
-            const int ks = static_cast<int>(b - static_cast<long long>(T) * a.KS);
+            // block (row tile T, K stage ks, half hh): rows [row0 + 128 hh, +128) of the tile
+            const int T = static_cast<int>(b / (a.KS * halves));
+            const int rem = static_cast<int>(b - static_cast<long long>(T) * a.KS * halves);
+            const int ks = rem / halves;
+            const int hh = rem - ks * halves;
             int lo = 0, hi = a.G - 1;   // group of m-tile T: largest g with mt_prefix[g] <= T
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
                 if (mt_prefix[mid] <= T) lo = mid;
                 else hi = mid - 1;
             }
-            const int row0 = off[lo] + (T - mt_prefix[lo]) * BM;
-            const int rows = min(BM, off[lo + 1] - row0);
+            const int row0 = off[lo] + (T - mt_prefix[lo]) * SBM + 128 * hh;
+            const int rows = min(BM, off[lo + 1] - row0);   // <= 0 for an empty half
             const int avail = min(4, KB32 - 4 * ks);
             // lane l gathers rows l, l+32, l+64, l+96: bytes 16*l .. 16*l+15 of the block
             uint32_t w[4];
@@ -342,17 +348,40 @@ __global__ void __launch_bounds__(THREADS, 1)
             __nv_bfloat16* out_rows =
                 static_cast<__nv_bfloat16*>(a.out) + (static_cast<long long>(t.row0) + q * 32) * a.N;
             uint32_t* stage = epi_stage + (warp - 2) * EpiStage<false>::WORDS;
+            if constexpr (NACC == 1) {
+                // one accumulator: read this warp's 32 x (BN/2) block out as bf16, hand tensor
+                // memory back to the MMA warp, then store while the next tile's MMAs run
+                uint32_t pk[BN / 64][16];
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        pk[c][j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c) {
+                    const int col = n0 + c * 32;
+                    if (rows_valid > 0 && col < a.N)
+                        store_packed_bf16_32x32(pk[c], stage, out_rows + col, a.N, rows_valid, a.N - col);
+                }
+            } else {
 #pragma unroll 1
-            for (int c = 0; c < BN / 64; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, v);
-                tmem_ld_wait();
-                const int col = n0 + c * 32;
-                if (rows_valid > 0 && col < a.N)
-                    store_block_32x32<false>(v, stage, out_rows + col, a.N, rows_valid, a.N - col);
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    const int col = n0 + c * 32;
+                    if (rows_valid > 0 && col < a.N)
+                        store_block_32x32<false>(v, stage, out_rows + col, a.N, rows_valid, a.N - col);
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty[acc]);
             }
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
             if (++acc == NACC) {
                 acc = 0;
                 acc_phase ^= 1;
@@ -393,12 +422,17 @@ cudaError_t launch_main(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, co
 
 }  // namespace
 
+cudaError_t launch_mx_prep(const uint8_t* lhs_scale, const uint8_t* rhs_scale, const int32_t* group_sizes,
+                           const MxArgs& a, int prep_grid, cudaStream_t stream) {
+    const size_t prep_shm = sizeof(int32_t) * 2 * (a.G + 1);
+    mx_prep_kernel<<<prep_grid, 256, prep_shm, stream>>>(lhs_scale, rhs_scale, group_sizes, a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const uint8_t* lhs_scale,
                          const uint8_t* rhs_scale, const int32_t* group_sizes, const MxArgs& a, int grid,
                          int prep_grid, cudaStream_t stream) {
-    const size_t prep_shm = sizeof(int32_t) * 2 * (a.G + 1);
-    mx_prep_kernel<<<prep_grid, 256, prep_shm, stream>>>(lhs_scale, rhs_scale, group_sizes, a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_mx_prep(lhs_scale, rhs_scale, group_sizes, a, prep_grid, stream);
     if (e != cudaSuccess) return e;
     if (a.BN == 256) return launch_main<256>(tmap_a, tmap_b, group_sizes, a, grid, stream);
     if (a.BN == 128) return launch_main<128>(tmap_a, tmap_b, group_sizes, a, grid, stream);

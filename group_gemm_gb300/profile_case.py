@@ -31,6 +31,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=2048)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--groups", type=int, default=0, help="override the workload's expert count")
+    ap.add_argument("--flags", type=lambda v: int(v, 0), default=0, help="rdot_problem.flags of the plan")
     args = ap.parse_args()
 
     gg.build()
@@ -53,7 +54,7 @@ def main():
         lhs = ri.device_normal((m, k), 1, 1.0, dev, torch.bfloat16)
         rhs = ri.device_normal((g, k, n), 2, 0.02, dev, torch.bfloat16)
         out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        plan = gg.Plan(m, k, n, g, "forward", "bf16", "bf16")
+        plan = gg.Plan(m, k, n, g, "forward", "bf16", "bf16", flags=args.flags)
         if args.kernel == "fwd":
             def run():
                 gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream)
@@ -68,7 +69,7 @@ def main():
         lhs = ri.device_normal((m, k), 1, 1.0, dev, torch.bfloat16)
         dy = ri.device_normal((m, n), 2, 1.0, dev, torch.bfloat16)
         dw = torch.empty((g, k, n), dtype=torch.float32, device=dev)
-        plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32")
+        plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", flags=args.flags)
 
         def run():
             gg.rdot_grad_weight(plan.handle, lhs, dy, gs_d, dw, plan.workspace, stream)
@@ -80,7 +81,7 @@ def main():
         bq, bs = ri.quantize_mx_e4m3(w, axis=1)
         del x, w
         out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16")
+        plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16", flags=args.flags)
 
         def run():
             gg.rdot_forward_mxfp8(plan.handle, aq, as_, bq, bs, gs_d, out, plan.workspace, stream)

@@ -69,10 +69,11 @@ typedef enum {
  * Pipeline": the M/N swap decided on M_avg = M_total / G). */
 #define RDOT_FLAG_ROW_TILES_INNER 0x1
 #define RDOT_FLAG_COL_TILES_INNER 0x2
-/* bf16 forward and grad-weight: run 256 x 256 tiles on pairs of CTAs (tcgen05 cta_group::2), or
- * force 128 x BN tiles on single CTAs. By default the forward uses pairs when the average group
- * has at least 256 rows and N >= 256; the grad-weight uses single CTAs unless pairs are asked
- * for. */
+/* bf16 forward, grad-weight and MXFP8 forward: run 256 x 256 tiles on pairs of CTAs (tcgen05
+ * cta_group::2), or force 128 x BN tiles on single CTAs. By default the bf16 forward uses pairs
+ * when the average group has at least 256 rows and N >= 256; the grad-weight and the MXFP8
+ * forward use single CTAs unless pairs are asked for. A pair plan with tile_n = 128 is
+ * RDOT_ERR_UNSUPPORTED. */
 #define RDOT_FLAG_CTA_PAIR 0x4
 #define RDOT_FLAG_NO_CTA_PAIR 0x8
 /* bf16 forward on single CTAs: by default work items of groups with 2 or more row tiles are

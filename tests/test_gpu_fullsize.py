@@ -107,7 +107,8 @@ def test_full_size_grad_weight_sampled_rows(flags):
     assert rel_err(got, ref) <= TOL
 
 
-def test_full_size_mxfp8_sampled_rows():
+@pytest.mark.parametrize("flags", [0, gg.RDOT_FLAG_CTA_PAIR])
+def test_full_size_mxfp8_sampled_rows(flags):
     cfg = ri.CONFIGS["mxfp8"]
     m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
     gs = ri.config_group_sizes("mxfp8")
@@ -118,7 +119,7 @@ def test_full_size_mxfp8_sampled_rows():
     bq, bs = ri.quantize_mx_e4m3(w, axis=1)
     del w
     torch.cuda.empty_cache()
-    plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16")
+    plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16", flags=flags)
     out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
     gg.rdot_forward_mxfp8(plan.handle, aq, as_, bq, bs, torch.from_numpy(gs).to(DEV), out, plan.workspace)
     assert plan.status() == 0

@@ -45,12 +45,19 @@ def make_case(m, k, n, gs, seed, vary=("a", "b")):
     return aq, as_, bq, bs, np.asarray(gs, np.int32)
 
 
-def run(aq, as_, bq, bs, gs, tile_n=0):
+# kernel variants: single CTA with 128- or 256-column tiles, and 256 x 256 tiles on CTA pairs
+VARIANTS = {"t128": (128, 0), "t256": (256, 0), "pair": (0, gg.RDOT_FLAG_CTA_PAIR)}
+
+
+def run(aq, as_, bq, bs, gs, variant="t256"):
     m, k = aq.shape
     g, _, n = bq.shape
-    plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16", tile_n=tile_n)
+    tile_n, flags = VARIANTS[variant]
+    plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16", tile_n=tile_n, flags=flags)
     if tile_n:
         assert plan.info["tile_n"] == tile_n
+    if flags:
+        assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 256
     ws = torch.zeros(gg.rdot_workspace_size(plan.handle), dtype=torch.uint8, device=DEV)
     out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
     gg.rdot_forward_mxfp8(plan.handle, aq.to(DEV), as_.to(DEV), bq.to(DEV), bs.to(DEV),
@@ -59,28 +66,28 @@ def run(aq, as_, bq, bs, gs, tile_n=0):
     return out, status
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("vary", [(), ("a",), ("b",), ("a", "b")])
-def test_mxfp8_scale_axes(vary, tile_n):
-    aq, as_, bq, bs, gs = make_case(256, 256, 512, [128, 128], 5, vary)
-    out, status = run(aq, as_, bq, bs, gs, tile_n)
+def test_mxfp8_scale_axes(vary, variant):
+    aq, as_, bq, bs, gs = make_case(512, 256, 512, [256, 256], 5, vary)
+    out, status = run(aq, as_, bq, bs, gs, variant)
     ref = oracle.forward_mxfp8(aq, as_, bq, bs, gs)
     assert status == 0
     assert rel_err(out, ref) <= TOL
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("variant", list(VARIANTS))
 @pytest.mark.parametrize("m,k,n,gs", [
     (300, 128, 128, [300]),                       # G = 1, ragged tail
     (420, 96, 144, [130, 0, 77, 200, 5]),         # K = 96 (3 of 4 scale blocks), N = 144, empty group
     (512, 32, 256, [0, 256, 256, 0]),             # K = 32 (one scale block)
     (1000, 512, 384, [0, 313, 1, 0, 257, 300, 129]),   # N = 384: 1.5 tiles of 256
 ])
-def test_mxfp8_ragged_parity(m, k, n, gs, tile_n):
+def test_mxfp8_ragged_parity(m, k, n, gs, variant):
     aq, as_, bq, bs, gs = make_case(m, k, n, gs, 17)
     total = int(gs.sum())
     aq[total:] = 0x7F                             # E4M3 NaN codes past the sum must never leak
-    out, status = run(aq, as_, bq, bs, gs, tile_n)
+    out, status = run(aq, as_, bq, bs, gs, variant)
     ref = oracle.forward_mxfp8(aq, as_, bq, bs, gs)
     assert status == 0
     assert rel_err(out, ref) <= TOL
@@ -93,12 +100,13 @@ def test_mxfp8_workspace_is_reported():
     assert ws > 256   # scale blocks live in the workspace
 
 
-def test_mxfp8_max_groups():
+@pytest.mark.parametrize("variant", ["t256", "pair"])
+def test_mxfp8_max_groups(variant):
     rng = np.random.default_rng(93)
     g = 1024
     gs = rng.integers(0, 4, size=g).astype(np.int32)
     gs[11] = 300
     aq, as_, bq, bs, gs = make_case(int(gs.sum()), 128, 256, gs, 94)
-    out, status = run(aq, as_, bq, bs, gs)
+    out, status = run(aq, as_, bq, bs, gs, variant)
     assert status == 0
     assert rel_err(out, oracle.forward_mxfp8(aq, as_, bq, bs, gs)) <= TOL
