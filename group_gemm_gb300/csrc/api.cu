@@ -292,8 +292,10 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             return RDOT_ERR_UNSUPPORTED;
         }
         pl->kind = 2;
-        // single-CTA tiles measure faster for the weight gradient on GB300; pairs on request
-        const bool want_pair = (p.flags & RDOT_FLAG_CTA_PAIR) != 0;
+        // pairs halve each SM's operand traffic but couple two SMs per contraction step: they
+        // measure faster on GB300 once a group holds about 1024 rows (16 chunks per tile)
+        const bool want_pair = (p.flags & RDOT_FLAG_CTA_PAIR) ||
+                               (!(p.flags & RDOT_FLAG_NO_CTA_PAIR) && m_avg >= 1024 && p.k >= 256 && p.n >= 256);
         if (want_pair && p.tile_n == 128) {
             delete pl;
             return RDOT_ERR_UNSUPPORTED;

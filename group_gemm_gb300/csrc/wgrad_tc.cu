@@ -172,22 +172,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 uint8_t* sa = smem + stage * L::STAGE_BYTES;
+                // the chunk's rows [valid, 64) belong to the next group (or lie past M). Only
+                // the K=16 steps holding group rows are issued; the rows [valid, 16 * ksteps) of
+                // the last one are zeroed in every 64-wide chunk of both operands (so NaN/Inf
+                // there cannot leak through 0 * x). A row is 128 contiguous bytes of its chunk
+                // whatever the swizzle, which only permutes 16-byte units inside the row. The
+                // loop has no division: this warp stalls the tensor pipe while it runs.
                 const int valid = min(ROWS, t.rows - c * ROWS);
-                if (valid < ROWS) {
-                    // rows [valid, 64) of this chunk belong to the next group (or lie past M):
-                    // zero them in every 64-wide chunk of both operands. A row is 128 contiguous
-                    // bytes of its chunk whatever the swizzle, which only permutes 16-byte units
-                    // inside the row.
-                    constexpr int CHUNKS = L::A_CHUNKS + L::B_CHUNKS;
-                    const int nstore = (ROWS - valid) * 8 * CHUNKS;
-                    for (int i = lane; i < nstore; i += 32) {
-                        const int chunk = i / ((ROWS - valid) * 8);
-                        const int rem = i - chunk * (ROWS - valid) * 8;
-                        const int row = valid + rem / 8;
-                        const int u = rem % 8;
-                        *reinterpret_cast<uint4*>(sa + chunk * L::CHUNK_BYTES + row * 128 + u * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    }
+                const int ksteps = (valid + 15) / 16;
+                const int zunits = (ksteps * 16 - valid) * 8;     // 16-byte units per chunk
+                if (zunits > 0) {
+                    uint8_t* zbase = sa + valid * 128;
+#pragma unroll
+                    for (int chunk = 0; chunk < L::A_CHUNKS + L::B_CHUNKS; ++chunk)
+                        for (int i = lane; i < zunits; i += 32)
+                            *reinterpret_cast<uint4*>(zbase + chunk * L::CHUNK_BYTES + i * 16) = make_uint4(0, 0, 0, 0);
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
@@ -197,6 +196,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t b_addr = a_addr + L::A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < ROWS / 16; ++kk) {
+                        if (kk >= ksteps) break;
                         // both operands MN-major: +2 groups of 8 contraction rows per K=16 step
                         const uint64_t adesc = smem_desc_sw128(a_addr + kk * 2048, L::CHUNK_BYTES, 1024);
                         const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 2048, L::CHUNK_BYTES, 1024);

@@ -182,23 +182,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         break;
                     }
                     uint8_t* sa = smem + stage * STAGE_BYTES;
+                    // only the K=16 steps holding group rows are issued; rows [valid, 16 * ksteps)
+                    // of the last one are zeroed in the four 64-wide chunks of the stage, in both
+                    // CTAs (a row is 128 contiguous bytes of its chunk whatever the swizzle)
                     const int valid = min(ROWS, t.rows - c * ROWS);
-                    if (valid < ROWS) {
-                        // rows [valid, 64) of the four 64-wide chunks of the stage, in both CTAs;
-                        // a row is 128 contiguous bytes of its chunk whatever the swizzle
-                        const uint32_t own = smem_u32(sa);
-                        const uint32_t peer = mapa_shared(own, 1);
-                        const int per_cta = (ROWS - valid) * 8 * 4;
-                        for (int i = lane; i < 2 * per_cta; i += 32) {
-                            const int j = i < per_cta ? i : i - per_cta;
-                            const int chunk = j / ((ROWS - valid) * 8);
-                            const int rem = j - chunk * (ROWS - valid) * 8;
-                            const uint32_t off_b = chunk * CHUNK_BYTES + (valid + rem / 8) * 128 + (rem % 8) * 16;
-                            if (i < per_cta)
-                                *reinterpret_cast<uint4*>(sa + off_b) = make_uint4(0, 0, 0, 0);
-                            else
+                    const int ksteps = (valid + 15) / 16;
+                    const int zunits = (ksteps * 16 - valid) * 8;     // 16-byte units per chunk
+                    if (zunits > 0) {
+                        const uint32_t peer = mapa_shared(smem_u32(sa) + valid * 128, 1);
+#pragma unroll
+                        for (int chunk = 0; chunk < 4; ++chunk)
+                            for (int i = lane; i < zunits; i += 32) {
+                                const uint32_t off_b = chunk * CHUNK_BYTES + i * 16;
+                                *reinterpret_cast<uint4*>(sa + valid * 128 + off_b) = make_uint4(0, 0, 0, 0);
                                 st_shared_cluster_zero16(peer + off_b);
-                        }
+                            }
                         fence_proxy_async_cluster();
                     }
                     __syncwarp();
@@ -208,6 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
                         for (int kk = 0; kk < ROWS / 16; ++kk) {
+                            if (kk >= ksteps) break;
                             const uint64_t adesc = smem_desc_sw128(a_addr + kk * 2048, CHUNK_BYTES, 1024);
                             const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 2048, CHUNK_BYTES, 1024);
                             mma_f16_pair(d_tmem, adesc, bdesc, idesc, (c | kk) != 0 ? 1u : 0u);
