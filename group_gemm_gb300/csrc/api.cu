@@ -91,6 +91,9 @@ struct rdot_plan_s {
     const void* map_lhs_ptr = nullptr;
     const void* map_rhs_ptr = nullptr;
     CUtensorMap map_a{}, map_b{};
+    // grad-weight output map (the epilogue's TMA stores), cached by dw pointer
+    const void* map_out_ptr = nullptr;
+    CUtensorMap map_out{};
     // MXFP8 on CTA pairs: the scale blocks in the workspace, cached by workspace pointer
     const void* map_ws_ptr = nullptr;
     CUtensorMap map_sfa{}, map_sfb{};
@@ -528,6 +531,12 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = dy;
     }
+    if (plan->map_out_ptr != dw) {
+        rdot_status st = encode_3d(&plan->map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dw, p.n, p.k, p.groups, p.n * 4,
+                                   p.k * p.n * 4, 32, 32, 1);
+        if (st != RDOT_OK) return st;
+        plan->map_out_ptr = dw;
+    }
     WgradArgs a{};
     a.group_sizes = group_sizes;
     a.dw = dw;
@@ -539,8 +548,9 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
     a.NT = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
     a.status = static_cast<int32_t*>(workspace);
     a.timeout_ns = plan->timeout_ns;
-    cudaError_t e = plan->pair ? launch_wgrad_tc2(plan->map_a, plan->map_b, a, plan->grid, s)
-                               : launch_wgrad_tc(plan->map_a, plan->map_b, a, plan->tile_n, plan->grid, s);
+    cudaError_t e = plan->pair ? launch_wgrad_tc2(plan->map_a, plan->map_b, plan->map_out, a, plan->grid, s)
+                               : launch_wgrad_tc(plan->map_a, plan->map_b, plan->map_out, a, plan->tile_n,
+                                                 plan->grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "wgrad_tc launch");
     return RDOT_OK;
 }

@@ -88,4 +88,36 @@ __device__ __forceinline__ void store_packed_bf16_32x32(const uint32_t (&p)[16],
     __syncwarp();
 }
 
+// TMA-store epilogue for fp32 blocks. A warp writes its 32 x 32 block (row = lane, v[j] = column
+// j) into a 4 KB staging tile in the layout a {32, 32} box with 128-byte swizzle has in shared
+// memory (16-byte unit u of row r at unit u ^ (r % 8); the tile must be 1024-byte aligned), then
+// one lane stores the tile with a single TMA instruction: whole 128-byte lines, no per-lane
+// address arithmetic, rows and columns past the tensor's end clipped by the copy engine.
+constexpr int EPI_TMA_F32_BYTES = 32 * 128;
+
+__device__ __forceinline__ void stage_f32_32x32_sw128(const uint32_t (&v)[32], uint8_t* tile) {
+    const int lane = threadIdx.x & 31;
+    uint8_t* row = tile + lane * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(row + ((u ^ (lane & 7)) << 4)) =
+            make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+}
+
+// Stages v and stores it at (c0, c1, c2) of `map`. Called by all 32 lanes; the previous store
+// from `tile` (issued by lane 0) must have read it, which this waits for first.
+__device__ __forceinline__ void tma_store_block_f32(const uint32_t (&v)[32], uint8_t* tile, const CUtensorMap* map,
+                                                    int c0, int c1, int c2) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
+    stage_f32_32x32_sw128(v, tile);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(map, tile, c0, c1, c2);
+        bulk_commit_group();
+    }
+}
+
 }  // namespace rdot

@@ -62,10 +62,11 @@ struct WgradArgs {
     uint64_t timeout_ns;
 };
 
-// bf16 lhs [M,K] and dy [M,N], fp32 dw [G,K,N], tcgen05 (wgrad_tc.cu). Both maps 2-D with a
-// (64, 64) box, 128-byte swizzled.
-cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int bn,
-                            int grid, cudaStream_t stream);
+// bf16 lhs [M,K] and dy [M,N], fp32 dw [G,K,N], tcgen05 (wgrad_tc.cu). Both operand maps 2-D
+// with a (64, 64) box, 128-byte swizzled; the dw map 3-D (N, K, G) fp32 with a (32, 32, 1) box,
+// 128-byte swizzled (the epilogue stores through it).
+cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
+                            const WgradArgs& a, int bn, int grid, cudaStream_t stream);
 
 // MXFP8 forward (mxfp8_tc.cu): 128 x BN tiles (BN = 128 or 256), K stages of 128 E4M3 bytes
 // (4 scale blocks).
@@ -95,7 +96,8 @@ cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, c
                          int prep_grid, cudaStream_t stream);
 
 // CTA-pair grad-weight (wgrad_tc2.cu): 256 x 256 tiles of dw[g]; a.KT counts 256-wide K tiles.
-cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int grid,
+cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
+                             const WgradArgs& a, int grid,
                              cudaStream_t stream);
 int wgrad_tc2_max_clusters(int G);
 

@@ -34,7 +34,7 @@ struct WgLayout {
     static constexpr int B_BYTES = B_CHUNKS * CHUNK_BYTES;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int EPI_BYTES = 4 * EpiStage<true>::BYTES;
+    static constexpr int EPI_BYTES = 4 * EPI_TMA_F32_BYTES;   // one staging tile per epilogue warp
     static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
     static constexpr int MISC_BYTES = 16;
     static constexpr int TMEM_COLS = 2 * BN;
@@ -61,11 +61,11 @@ __device__ __forceinline__ WgTile wg_decode(int w, int KT, int NT, const int32_t
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(THREADS, 1)
     wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_dy,
-                    WgradArgs a) {
+                    const __grid_constant__ CUtensorMap tmap_dw, WgradArgs a) {
     using L = WgLayout<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + L::RING_BYTES);
+    uint8_t* epi_stage = smem + L::RING_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::RING_BYTES + L::EPI_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmap_x);
         tma_prefetch_desc(&tmap_dy);
+        tma_prefetch_desc(&tmap_dw);
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, L::TMEM_COLS);
@@ -226,22 +227,32 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ epilogue
+        // warp w drains TMEM lane quarter w % 4 (32 rows of the dw tile) through its own staging
+        // tile and TMA stores; the copy engine clips rows past K and columns past N
         const int q = warp & 3;
-        uint32_t* stage = epi_stage + (warp - 2) * EpiStage<true>::WORDS;
+        uint8_t* tile = epi_stage + (warp - 2) * EPI_TMA_F32_BYTES;
         uint32_t acc = 0, acc_phase = 0;
         for (int w = blockIdx.x; w < W; w += gridDim.x) {
             const WgTile t = wg_decode(w, a.KT, a.NT, off);
-            const int k0 = t.kt * TC_BM, n0 = t.nt * BN;
-            // this warp's 32 rows of dw[g] (rows k0 + 32q ..), stored 32 columns at a time
-            const int rows_valid = a.K - (k0 + q * 32);
-            float* drows = a.dw + (static_cast<long long>(t.g) * a.K + k0 + q * 32) * a.N;
+            const int k0 = t.kt * TC_BM + q * 32, n0 = t.nt * BN;
+            if (k0 >= a.K) {
+                // no dw rows for this warp; keep the accumulator hand-shake
+                if (t.rows > 0) {
+                    if (!mbar_wait_warp(&tfull[acc], acc_phase, guard)) break;
+                    tc_fence_before();
+                    mbar_arrive(&tempty[acc]);
+                    acc ^= 1;
+                    if (acc == 0) acc_phase ^= 1;
+                }
+                continue;
+            }
             if (t.rows <= 0) {
                 // empty group: its slab is zero, the tensor cores never ran for it
                 uint32_t z[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) z[j] = 0u;
                 for (int col = n0; col < min(a.N, n0 + BN); col += 32)
-                    if (rows_valid > 0) store_block_32x32<true>(z, stage, drows + col, a.N, rows_valid, a.N - col);
+                    tma_store_block_f32(z, tile, &tmap_dw, col, k0, t.g);
                 continue;
             }
             const bool ready = mbar_wait_warp(&tfull[acc], acc_phase, guard);
@@ -250,18 +261,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
+                const int col = n0 + c * 32;
+                if (col >= a.N) break;
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tbase + c * 32, v);
                 tmem_ld_wait();
-                const int col = n0 + c * 32;
-                if (rows_valid > 0 && col < a.N)
-                    store_block_32x32<true>(v, stage, drows + col, a.N, rows_valid, a.N - col);
+                tma_store_block_f32(v, tile, &tmap_dw, col, k0, t.g);
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        // the staging tile must stay valid until the copy engine has read it, and the stores
+        // must be complete before the kernel ends
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -273,23 +288,23 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int BN, int STAGES>
-cudaError_t launch_wg(const CUtensorMap& tx, const CUtensorMap& tdy, const WgradArgs& a, int grid,
-                      cudaStream_t stream) {
+cudaError_t launch_wg(const CUtensorMap& tx, const CUtensorMap& tdy, const CUtensorMap& tdw, const WgradArgs& a,
+                      int grid, cudaStream_t stream) {
     using L = WgLayout<BN, STAGES>;
     const size_t shm = L::smem_bytes(a.G);
     auto kern = wgrad_tc_kernel<BN, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, shm, stream>>>(tx, tdy, a);
+    kern<<<grid, THREADS, shm, stream>>>(tx, tdy, tdw, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int bn,
-                            int grid, cudaStream_t stream) {
-    if (bn == 256) return launch_wg<256, 4>(tmap_x, tmap_dy, a, grid, stream);
-    if (bn == 128) return launch_wg<128, 6>(tmap_x, tmap_dy, a, grid, stream);
+cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
+                            const WgradArgs& a, int bn, int grid, cudaStream_t stream) {
+    if (bn == 256) return launch_wg<256, 4>(tmap_x, tmap_dy, tmap_dw, a, grid, stream);
+    if (bn == 128) return launch_wg<128, 6>(tmap_x, tmap_dy, tmap_dw, a, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -33,7 +33,7 @@ constexpr int A_BYTES = 2 * CHUNK_BYTES;       // this CTA's 128 K columns
 constexpr int B_BYTES = 2 * CHUNK_BYTES;       // this CTA's 128 N columns
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-constexpr int EPI_BYTES = 4 * EpiStage<true>::BYTES;
+constexpr int EPI_BYTES = 4 * EPI_TMA_F32_BYTES;   // one staging tile per epilogue warp
 constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;   // full, empty, tfull[2], tempty[2], drain
 constexpr int MISC_BYTES = 16;
 constexpr int TMEM_COLS = 2 * BN;
@@ -59,10 +59,11 @@ __device__ __forceinline__ PairTile decode(int w, int KT, int NT, const int32_t*
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     wgrad_tc2_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_dy,
+                     const __grid_constant__ CUtensorMap tmap_dw,
                      WgradArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint32_t* epi_stage = reinterpret_cast<uint32_t*>(smem + RING_BYTES);
+    uint8_t* epi_stage = smem + RING_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + EPI_BYTES);
     uint64_t* empty = full + STAGES;
     uint64_t* tfull = empty + STAGES;
@@ -94,6 +95,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmap_x);
         tma_prefetch_desc(&tmap_dy);
+        tma_prefetch_desc(&tmap_dw);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_holder, TMEM_COLS);
@@ -236,35 +238,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ epilogue (both CTAs)
+        // warp w drains TMEM lane quarter w % 4 of this CTA's 128 dw rows through its own staging
+        // tile and TMA stores (rows past K and columns past N clipped by the copy engine)
         const int q = warp & 3;
-        uint32_t* stage_buf = epi_stage + (warp - 2) * EpiStage<true>::WORDS;
+        uint8_t* tile = epi_stage + (warp - 2) * EPI_TMA_F32_BYTES;
         uint32_t acc = 0, acc_phase = 0;
         for (int w = cluster; w < W; w += nclusters) {
             const PairTile t = decode(w, a.KT, a.NT, off);
             const int k0 = t.kt * BM + 128 * static_cast<int>(rank) + q * 32;   // first dw row of this warp
             const int n0 = t.nt * BN;
-            const int rows_valid = a.K - k0;
-            float* drows = a.dw + (static_cast<long long>(t.g) * a.K + k0) * a.N;
             if (t.rows <= 0) {
-                uint32_t z[32];
+                if (k0 < a.K) {
+                    uint32_t z[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) z[j] = 0u;
-                for (int col = n0; col < min(a.N, n0 + BN); col += 32)
-                    if (rows_valid > 0) store_block_32x32<true>(z, stage_buf, drows + col, a.N, rows_valid, a.N - col);
+                    for (int j = 0; j < 32; ++j) z[j] = 0u;
+                    for (int col = n0; col < min(a.N, n0 + BN); col += 32)
+                        tma_store_block_f32(z, tile, &tmap_dw, col, k0, t.g);
+                }
                 continue;
             }
             const bool ready_acc = mbar_wait_warp(&tfull[acc], acc_phase, guard);
             if (!ready_acc) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            if (k0 < a.K) {
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, v);
-                tmem_ld_wait();
-                const int col = n0 + c * 32;
-                if (rows_valid > 0 && col < a.N)
-                    store_block_32x32<true>(v, stage_buf, drows + col, a.N, rows_valid, a.N - col);
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int col = n0 + c * 32;
+                    if (col >= a.N) break;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    tma_store_block_f32(v, tile, &tmap_dw, col, k0, t.g);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -272,6 +278,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -284,14 +292,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a, int grid,
+cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
+                             const WgradArgs& a, int grid,
                              cudaStream_t stream) {
     if (grid % 2) return cudaErrorInvalidValue;
     const size_t shm = smem_bytes(a.G);
     cudaError_t e =
         cudaFuncSetAttribute(wgrad_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    wgrad_tc2_kernel<<<grid, THREADS, shm, stream>>>(tmap_x, tmap_dy, a);
+    wgrad_tc2_kernel<<<grid, THREADS, shm, stream>>>(tmap_x, tmap_dy, tmap_dw, a);
     return cudaGetLastError();
 }
 
