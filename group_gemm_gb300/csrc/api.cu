@@ -362,7 +362,12 @@ MxLayout mx_layout(const rdot_problem& p, int bm, int bn) {
 
 rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes) {
     if (!plan || !bytes) return RDOT_ERR_INVALID_ARG;
-    *bytes = plan->kind == 3 ? mx_layout(plan->p, plan->tile_m, plan->tile_n).total : kWorkspaceBytes;
+    if (plan->kind == 3)
+        *bytes = mx_layout(plan->p, plan->tile_m, plan->tile_n).total;
+    else if (plan->kind == 2)
+        *bytes = kWorkspaceBytes + static_cast<size_t>(2 * WG_MAP_BYTES) * plan->p.groups;   // group tensor maps
+    else
+        *bytes = kWorkspaceBytes;
     return RDOT_OK;
 }
 
@@ -510,7 +515,8 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
     const rdot_problem& p = plan->p;
     if (p.mode != RDOT_MODE_GRAD_WEIGHT || plan->kind != 2) return RDOT_ERR_INVALID_ARG;
     if (p.m > 0 && (!lhs || !dy)) return RDOT_ERR_INVALID_ARG;
-    if ((lhs && !aligned16(lhs)) || (dy && !aligned16(dy)) || !aligned16(dw) || !aligned16(workspace) ||
+    if ((lhs && !aligned16(lhs)) || (dy && !aligned16(dy)) || !aligned16(dw) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 127u) ||
         (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
         return RDOT_ERR_INVALID_ARG;
     DeviceGuard dg(plan->device);
@@ -540,6 +546,7 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
     WgradArgs a{};
     a.group_sizes = group_sizes;
     a.dw = dw;
+    a.maps = static_cast<uint8_t*>(workspace) + kWorkspaceBytes;
     a.M = static_cast<int>(p.m);
     a.K = static_cast<int>(p.k);
     a.N = static_cast<int>(p.n);
@@ -548,7 +555,9 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
     a.NT = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
     a.status = static_cast<int32_t*>(workspace);
     a.timeout_ns = plan->timeout_ns;
-    cudaError_t e = plan->pair ? launch_wgrad_tc2(plan->map_a, plan->map_b, plan->map_out, a, plan->grid, s)
+    cudaError_t e = launch_wg_maps(plan->map_a, plan->map_b, a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "wgrad group maps launch");
+    e = plan->pair ? launch_wgrad_tc2(plan->map_a, plan->map_b, plan->map_out, a, plan->grid, s)
                                : launch_wgrad_tc(plan->map_a, plan->map_b, plan->map_out, a, plan->tile_n,
                                                  plan->grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "wgrad_tc launch");

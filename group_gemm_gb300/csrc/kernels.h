@@ -56,6 +56,8 @@ constexpr int TC2_BM = 256;
 struct WgradArgs {
     const int32_t* group_sizes;  // device [G]
     float* dw;                   // device [G, K, N]
+    uint8_t* maps;               // device workspace: per group, the lhs then the dy tensor map
+                                 // with the row extent cut at the group's end (128 B each)
     int M, K, N, G;
     int KT, NT;                  // 128-row tiles of K, BN-wide tiles of N
     int32_t* status;
@@ -65,6 +67,13 @@ struct WgradArgs {
 // bf16 lhs [M,K] and dy [M,N], fp32 dw [G,K,N], tcgen05 (wgrad_tc.cu). Both operand maps 2-D
 // with a (64, 64) box, 128-byte swizzled; the dw map 3-D (N, K, G) fp32 with a (32, 32, 1) box,
 // 128-byte swizzled (the epilogue stores through it).
+// Writes a.maps: for each group g, copies of tmap_x and tmap_dy whose row extent is the group's
+// end offset, so that a box reaching past the group reads zeros (wgrad_tc.cu). Runs before either
+// grad-weight kernel on the same stream.
+cudaError_t launch_wg_maps(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a,
+                           cudaStream_t stream);
+constexpr int WG_MAP_BYTES = 128;
+
 cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
                             const WgradArgs& a, int bn, int grid, cudaStream_t stream);
 

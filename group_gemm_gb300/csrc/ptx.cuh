@@ -119,6 +119,25 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// Tensor maps edited on the device. A thread copies a host-encoded map into global memory,
+// changes the extent of one dimension with tensormap.replace (a generic-proxy write of the
+// 128-byte object) and releases it to the tensor-map proxy; a TMA issuer acquires it before use.
+__device__ __forceinline__ void tensormap_set_rows_global(void* map, int rows) {
+    asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(rows)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tensormap_release_gpu() {
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ void tensormap_acquire_gpu(const void* map) {
+    asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map))
+                 : "memory");
+}
+
 // TMA store of a box from this CTA's shared memory (bulk-group completion). Elements outside the
 // tensor are not written. Coordinates must not be negative.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {

@@ -9,10 +9,12 @@
 // is written as zeros without touching the tensor cores). The contraction runs over the group's
 // rows in chunks of 64: TMA brings lhs[rows, 128 K columns] and dy[rows, BN columns]; both are
 // MN-major operands (the MMA's M = K columns and N = dy columns are the contiguous axes), 128-byte
-// swizzled. The last chunk of a group usually runs into the next group's rows: those rows are
-// zeroed in shared memory (both operands, so NaN/Inf there cannot leak through 0 * x) before the
-// MMA reads them. Roles: warp 0 TMA, warp 1 MMA (+ tail zeroing), warps 2..5 epilogue; two TMEM
-// accumulators let the epilogue of one tile overlap the next tile's mainloop.
+// swizzled. The last chunk of a group usually runs into the next group's rows. It is loaded
+// through per-group copies of the two tensor maps whose row extent ends at the group's end
+// (written by wg_maps_kernel before the GEMM), so the copy engine fills those rows with zeros in
+// both operands and NaN/Inf there cannot leak through 0 * x; only the K=16 steps that hold group
+// rows are issued. Roles: warp 0 TMA, warp 1 MMA, warps 2..5 epilogue; two TMEM accumulators let
+// the epilogue of one tile overlap the next tile's mainloop.
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -56,6 +58,30 @@ __device__ __forceinline__ WgTile wg_decode(int w, int KT, int NT, const int32_t
     t.row0 = off[t.g];
     t.rows = off[t.g + 1] - off[t.g];
     return t;
+}
+
+// One block: offsets by a warp scan, then per group g two map copies with rows = off[g+1].
+__global__ void __launch_bounds__(1024) wg_maps_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                                                       const __grid_constant__ CUtensorMap tmap_dy, WgradArgs a) {
+    extern __shared__ int32_t wg_table[];
+    int32_t* off = wg_table;
+    if (threadIdx.x < 32) (void)group_scan_warp(a.group_sizes, a.G, a.M, 1, 1, off, wg_table + a.G + 1);
+    __syncthreads();
+    const uint4* src_x = reinterpret_cast<const uint4*>(&tmap_x);
+    const uint4* src_dy = reinterpret_cast<const uint4*>(&tmap_dy);
+    for (int g = threadIdx.x; g < a.G; g += blockDim.x) {
+        uint4* dx = reinterpret_cast<uint4*>(a.maps + (2 * g) * WG_MAP_BYTES);
+        uint4* ddy = reinterpret_cast<uint4*>(a.maps + (2 * g + 1) * WG_MAP_BYTES);
+#pragma unroll
+        for (int i = 0; i < WG_MAP_BYTES / 16; ++i) {
+            dx[i] = src_x[i];
+            ddy[i] = src_dy[i];
+        }
+        const int rows = max(1, off[g + 1]);   // an empty leading group is never loaded
+        tensormap_set_rows_global(dx, rows);
+        tensormap_set_rows_global(ddy, rows);
+    }
+    tensormap_release_gpu();
 }
 
 template <int BN, int STAGES>
@@ -122,6 +148,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int k0 = t.kt * TC_BM, n0 = t.nt * BN;
                 const int a_chunks = min(L::A_CHUNKS, (a.K - k0 + 63) / 64);
                 const int b_chunks = min(L::B_CHUNKS, (a.N - n0 + 63) / 64);
+                // the group's maps, for a last chunk that runs past the group's end
+                const CUtensorMap* gmap_x = reinterpret_cast<const CUtensorMap*>(a.maps + (2 * t.g) * WG_MAP_BYTES);
+                const CUtensorMap* gmap_dy = reinterpret_cast<const CUtensorMap*>(a.maps + (2 * t.g + 1) * WG_MAP_BYTES);
+                const bool ragged = (t.rows % ROWS) != 0;
+                if (ragged) {
+                    tensormap_acquire_gpu(gmap_x);
+                    tensormap_acquire_gpu(gmap_dy);
+                    tma_prefetch_desc(gmap_x);
+                    tma_prefetch_desc(gmap_dy);
+                }
                 for (int c = 0; c < nchunks_rows; ++c) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
                         ok = false;
@@ -130,11 +166,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint8_t* sa = smem + stage * L::STAGE_BYTES;
                     uint8_t* sb = sa + L::A_BYTES;
                     const int r0 = t.row0 + c * ROWS;
+                    const bool tail = ragged && c == nchunks_rows - 1;
+                    const CUtensorMap* mx = tail ? gmap_x : &tmap_x;
+                    const CUtensorMap* mdy = tail ? gmap_dy : &tmap_dy;
                     mbar_arrive_expect_tx(&full[stage], (a_chunks + b_chunks) * L::CHUNK_BYTES);
                     for (int j = 0; j < a_chunks; ++j)
-                        tma_load_2d(sa + j * L::CHUNK_BYTES, &tmap_x, &full[stage], k0 + 64 * j, r0);
+                        tma_load_2d(sa + j * L::CHUNK_BYTES, mx, &full[stage], k0 + 64 * j, r0);
                     for (int j = 0; j < b_chunks; ++j)
-                        tma_load_2d(sb + j * L::CHUNK_BYTES, &tmap_dy, &full[stage], n0 + 64 * j, r0);
+                        tma_load_2d(sb + j * L::CHUNK_BYTES, mdy, &full[stage], n0 + 64 * j, r0);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -154,7 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer (+ tail zeroing)
+        // ------------------------------------------------------------------ MMA issuer
         constexpr uint32_t idesc = idesc_f16(TC_BM, BN, true, true, true, true);
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true;
@@ -173,23 +212,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 uint8_t* sa = smem + stage * L::STAGE_BYTES;
-                // the chunk's rows [valid, 64) belong to the next group (or lie past M). Only
-                // the K=16 steps holding group rows are issued; the rows [valid, 16 * ksteps) of
-                // the last one are zeroed in every 64-wide chunk of both operands (so NaN/Inf
-                // there cannot leak through 0 * x). A row is 128 contiguous bytes of its chunk
-                // whatever the swizzle, which only permutes 16-byte units inside the row. The
-                // loop has no division: this warp stalls the tensor pipe while it runs.
+                // rows [valid, 64) of a group's last chunk arrive as zeros (group maps); the K=16
+                // steps past the group's rows are not issued
                 const int valid = min(ROWS, t.rows - c * ROWS);
                 const int ksteps = (valid + 15) / 16;
-                const int zunits = (ksteps * 16 - valid) * 8;     // 16-byte units per chunk
-                if (zunits > 0) {
-                    uint8_t* zbase = sa + valid * 128;
-#pragma unroll
-                    for (int chunk = 0; chunk < L::A_CHUNKS + L::B_CHUNKS; ++chunk)
-                        for (int i = lane; i < zunits; i += 32)
-                            *reinterpret_cast<uint4*>(zbase + chunk * L::CHUNK_BYTES + i * 16) = make_uint4(0, 0, 0, 0);
-                    fence_proxy_async_smem();
-                }
                 __syncwarp();
                 if (lane == 0) {
                     tc_fence_after();
@@ -300,6 +326,13 @@ cudaError_t launch_wg(const CUtensorMap& tx, const CUtensorMap& tdy, const CUten
 }
 
 }  // namespace
+
+cudaError_t launch_wg_maps(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a,
+                           cudaStream_t stream) {
+    const size_t shm = sizeof(int32_t) * 2 * (a.G + 1);
+    wg_maps_kernel<<<1, 1024, shm, stream>>>(tmap_x, tmap_dy, a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
                             const WgradArgs& a, int bn, int grid, cudaStream_t stream) {

@@ -8,9 +8,8 @@
 //     MMA's M) and dy columns [n0 + 128 r, +128) (its half of B): 32 KB per stage, six stages. Both
 //     operands are MN-major, 128-byte swizzled.
 //   - Both CTAs' TMA loads complete on the even CTA's "full" barrier. The last chunk of a group
-//     runs into the next group's rows: once a stage is full, the even CTA's MMA warp zeroes those
-//     rows in both CTAs' shared memory (its own directly, the odd CTA's through distributed shared
-//     memory) and fences them for the tensor cores before issuing the MMAs.
+//     runs into the next group's rows: both CTAs load it through the group's tensor maps (row
+//     extent cut at the group's end, written by wg_maps_kernel), so those rows arrive as zeros.
 //   - The even CTA issues M=256 N=256 K=16 MMAs; commits multicast "stage free" and
 //     "accumulator full" to both CTAs; each CTA's epilogue stores its 128 rows of dw[g] and arrives
 //     on the even CTA's "accumulator empty" barrier.
@@ -127,6 +126,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const int bc0 = max(0, min(2, (a.N - nb0 + 63) / 64)), bc1 = max(0, min(2, (a.N - nb0 - 128 + 63) / 64));
                 const int k0 = kb0 + 128 * static_cast<int>(rank), n0 = nb0 + 128 * static_cast<int>(rank);
                 const int ac = rank ? ac1 : ac0, bc = rank ? bc1 : bc0;
+                // a last chunk that runs past the group's end loads through the group's maps,
+                // whose row extent ends there: the copy engine fills those rows with zeros
+                const CUtensorMap* gmap_x = reinterpret_cast<const CUtensorMap*>(a.maps + (2 * t.g) * WG_MAP_BYTES);
+                const CUtensorMap* gmap_dy = reinterpret_cast<const CUtensorMap*>(a.maps + (2 * t.g + 1) * WG_MAP_BYTES);
+                const bool ragged = (t.rows % ROWS) != 0;
+                if (ragged) {
+                    tensormap_acquire_gpu(gmap_x);
+                    tensormap_acquire_gpu(gmap_dy);
+                    tma_prefetch_desc(gmap_x);
+                    tma_prefetch_desc(gmap_dy);
+                }
                 for (int c = 0; c < nchunks; ++c) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
                         ok = false;
@@ -137,8 +147,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     const int r0 = t.row0 + c * ROWS;
                     if (leader) mbar_arrive_expect_tx(&full[stage], (ac0 + ac1 + bc0 + bc1) * CHUNK_BYTES);
                     const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-                    for (int j = 0; j < ac; ++j) tma_load_2d_pair(sa + j * CHUNK_BYTES, &tmap_x, fb, k0 + 64 * j, r0);
-                    for (int j = 0; j < bc; ++j) tma_load_2d_pair(sb + j * CHUNK_BYTES, &tmap_dy, fb, n0 + 64 * j, r0);
+                    const bool tail = ragged && c == nchunks - 1;
+                    const CUtensorMap* mx = tail ? gmap_x : &tmap_x;
+                    const CUtensorMap* mdy = tail ? gmap_dy : &tmap_dy;
+                    for (int j = 0; j < ac; ++j) tma_load_2d_pair(sa + j * CHUNK_BYTES, mx, fb, k0 + 64 * j, r0);
+                    for (int j = 0; j < bc; ++j) tma_load_2d_pair(sb + j * CHUNK_BYTES, mdy, fb, n0 + 64 * j, r0);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -164,7 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ---------------------------------------------- MMA issue and tail zeroing (even CTA only)
+        // ------------------------------------------------------------- MMA issue (even CTA only)
         if (leader) {
             constexpr uint32_t idesc = idesc_f16(BM, BN, true, true, true, true);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -184,23 +197,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         break;
                     }
                     uint8_t* sa = smem + stage * STAGE_BYTES;
-                    // only the K=16 steps holding group rows are issued; rows [valid, 16 * ksteps)
-                    // of the last one are zeroed in the four 64-wide chunks of the stage, in both
-                    // CTAs (a row is 128 contiguous bytes of its chunk whatever the swizzle)
+                    // rows [valid, 64) of a group's last chunk arrive as zeros in both CTAs (group
+                    // maps); the K=16 steps past the group's rows are not issued
                     const int valid = min(ROWS, t.rows - c * ROWS);
                     const int ksteps = (valid + 15) / 16;
-                    const int zunits = (ksteps * 16 - valid) * 8;     // 16-byte units per chunk
-                    if (zunits > 0) {
-                        const uint32_t peer = mapa_shared(smem_u32(sa) + valid * 128, 1);
-#pragma unroll
-                        for (int chunk = 0; chunk < 4; ++chunk)
-                            for (int i = lane; i < zunits; i += 32) {
-                                const uint32_t off_b = chunk * CHUNK_BYTES + i * 16;
-                                *reinterpret_cast<uint4*>(sa + valid * 128 + off_b) = make_uint4(0, 0, 0, 0);
-                                st_shared_cluster_zero16(peer + off_b);
-                            }
-                        fence_proxy_async_cluster();
-                    }
                     __syncwarp();
                     if (lane == 0) {
                         tc_fence_after();
