@@ -114,7 +114,9 @@ RDOT_API rdot_status rdot_plan_destroy(rdot_plan_t plan);
 
 /* Bytes of device workspace the plan's calls need (at least 256, 256-byte aligned by the
  * caller). The workspace holds the status word followed by the group table exported by
- * rdot_debug_offsets_tilemap. It must be zeroed once before first use. */
+ * rdot_debug_offsets_tilemap; an MXFP8 plan adds the reordered scale blocks, a grad-weight plan
+ * two 128-byte tensor maps per group (rewritten on the device by every call). It must be zeroed
+ * once before first use. Calls that share a workspace must not overlap on the GPU. */
 RDOT_API rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes);
 
 /* Forward ragged-dot, non-contracting ragged dimension ("Group-GEMM in XLA", Part 3
