@@ -296,9 +296,9 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         }
         pl->kind = 2;
         // pairs halve each SM's operand traffic but couple two SMs per contraction step: they
-        // measure faster on GB300 once a group holds about 1024 rows (16 chunks per tile)
+        // measure faster on GB300 once a group holds about 512 rows (8 chunks per tile)
         const bool want_pair = (p.flags & RDOT_FLAG_CTA_PAIR) ||
-                               (!(p.flags & RDOT_FLAG_NO_CTA_PAIR) && m_avg >= 1024 && p.k >= 256 && p.n >= 256);
+                               (!(p.flags & RDOT_FLAG_NO_CTA_PAIR) && m_avg >= 512 && p.k >= 256 && p.n >= 256);
         if (want_pair && p.tile_n == 128) {
             delete pl;
             return RDOT_ERR_UNSUPPORTED;

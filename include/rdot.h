@@ -72,7 +72,7 @@ typedef enum {
 /* bf16 forward, grad-weight and MXFP8 forward: run 256 x 256 tiles on pairs of CTAs (tcgen05
  * cta_group::2), or force 128 x BN tiles on single CTAs. By default the bf16 forward uses pairs
  * when the average group has at least 256 rows and N >= 256, the grad-weight when it has at
- * least 1024 rows and K, N >= 256; the MXFP8 forward uses single CTAs unless pairs are asked
+ * least 512 rows and K, N >= 256; the MXFP8 forward uses single CTAs unless pairs are asked
  * for. A pair plan with tile_n = 128 is
  * RDOT_ERR_UNSUPPORTED. */
 #define RDOT_FLAG_CTA_PAIR 0x4
