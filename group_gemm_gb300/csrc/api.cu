@@ -84,7 +84,8 @@ struct rdot_plan_s {
     int tile_m = 0, tile_n = 0;
     int m_inner = 1;
     int grid = 1;
-    bool pair = false;     // bf16 forward on CTA pairs (256 x 256 tiles)
+    bool pair = false;     // CTA pairs (256-row tiles)
+    bool wide = false;     // bf16 forward on CTA pairs with 256 x 512 tiles
     int big_mt = 0;        // > 0: interleaved work order (groups with >= big_mt row tiles vs the rest)
     uint64_t timeout_ns = kDefaultTimeoutNs;
     // tensor maps cached by operand pointers (re-encoded when a pointer changes)
@@ -155,7 +156,11 @@ rdot_status check_problem(const rdot_problem* p) {
     if (p->m > 0x7fffffffLL || p->k > 0x7fffffffLL || p->n > 0x7fffffffLL) return RDOT_ERR_UNSUPPORTED;
     if (p->flags & ~0x1F) return RDOT_ERR_INVALID_ARG;
     if ((p->flags & RDOT_FLAG_CTA_PAIR) && (p->flags & RDOT_FLAG_NO_CTA_PAIR)) return RDOT_ERR_INVALID_ARG;
-    if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256) return RDOT_ERR_UNSUPPORTED;
+    if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256 && p->tile_n != 512) return RDOT_ERR_UNSUPPORTED;
+    // 512-column tiles: the bf16-out forward on CTA pairs only
+    if (p->tile_n == 512 && (p->mode != RDOT_MODE_FORWARD || p->in_dtype != RDOT_BF16 || p->out_dtype != RDOT_BF16 ||
+                             (p->flags & RDOT_FLAG_NO_CTA_PAIR)))
+        return RDOT_ERR_UNSUPPORTED;
     switch (p->mode) {
         case RDOT_MODE_FORWARD:
             if (p->in_dtype == RDOT_F32) {
@@ -227,7 +232,8 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             return RDOT_ERR_UNSUPPORTED;   // tcgen05 kernels are built for sm_103a only
         }
         pl->kind = 1;
-        const bool want_pair = (p.flags & RDOT_FLAG_CTA_PAIR) ||
+        const bool wide = p.tile_n == 512;
+        const bool want_pair = wide || (p.flags & RDOT_FLAG_CTA_PAIR) ||
                                (!(p.flags & RDOT_FLAG_NO_CTA_PAIR) && m_avg >= TC2_BM && p.n >= 256);
         if (want_pair && p.tile_n == 128) {
             delete pl;
@@ -235,15 +241,16 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         }
         int clusters = 0;
         if (want_pair) {
-            clusters = fwd_tc2_max_clusters(p.out_dtype == RDOT_F32, p.groups);
+            clusters = wide ? fwd_tc2w_max_clusters(p.groups) : fwd_tc2_max_clusters(p.out_dtype == RDOT_F32, p.groups);
             if (clusters <= 0) {
                 delete pl;
                 return cuda_fail(cudaGetLastError(), "cudaOccupancyMaxActiveClusters");
             }
         }
         pl->pair = want_pair;
+        pl->wide = wide;
         pl->tile_m = want_pair ? TC2_BM : TC_BM;
-        pl->tile_n = want_pair ? 256 : (p.tile_n ? p.tile_n : (p.n <= 128 ? 128 : 256));
+        pl->tile_n = wide ? 512 : want_pair ? 256 : (p.tile_n ? p.tile_n : (p.n <= 128 ? 128 : 256));
         const int nt = static_cast<int>((p.n + pl->tile_n - 1) / pl->tile_n);
         const long long bound = forward_tile_bound(p.m, p.groups, pl->tile_m, nt);
         if (bound > 0x7fffffffLL) {
@@ -431,7 +438,9 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = rhs;
     }
-    if (plan->pair)
+    if (plan->wide)
+        e = launch_fwd_tc2w(plan->map_a, plan->map_b, a, plan->grid, s);
+    else if (plan->pair)
         e = launch_fwd_tc2(plan->map_a, plan->map_b, a, p.out_dtype == RDOT_F32, plan->grid, s);
     else
         e = launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
@@ -649,7 +658,8 @@ rdot_status rdot_padded_forward(rdot_plan_t plan, const void* lhs, const void* r
     const long long bound = forward_tile_bound(rows_pad, p.groups, plan->tile_m, a.NT);
     if (plan->pair) {
         const int grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(bound, plan->grid / 2)));
-        e = launch_fwd_tc2(plan->pad_map_a, plan->map_b, a, p.out_dtype == RDOT_F32, grid, s);
+        e = plan->wide ? launch_fwd_tc2w(plan->pad_map_a, plan->map_b, a, grid, s)
+                       : launch_fwd_tc2(plan->pad_map_a, plan->map_b, a, p.out_dtype == RDOT_F32, grid, s);
     } else {
         const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, plan->sm_count)));
         e = launch_fwd_tc(plan->pad_map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, grid, s);

@@ -49,6 +49,10 @@ constexpr int TC_BK = 64;
 // launch_fwd_tc. grid must be even (2 CTAs per cluster).
 cudaError_t launch_fwd_tc2(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, bool out_f32,
                            int grid, cudaStream_t stream);
+// CTA-pair bf16 forward with 256 x 512 tiles, bf16 out (fwd_tc2w.cu); a.NT counts 512-wide tiles.
+cudaError_t launch_fwd_tc2w(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, int grid,
+                            cudaStream_t stream);
+int fwd_tc2w_max_clusters(int G);
 int fwd_tc2_max_clusters(bool out_f32, int G);   // co-resident clusters of that kernel (0 on error)
 constexpr int TC2_BM = 256;
 

@@ -32,6 +32,7 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--groups", type=int, default=0, help="override the workload's expert count")
     ap.add_argument("--flags", type=lambda v: int(v, 0), default=0, help="rdot_problem.flags of the plan")
+    ap.add_argument("--tile-n", type=int, default=0, help="rdot_problem.tile_n of the plan (0: the plan's choice)")
     args = ap.parse_args()
 
     gg.build()
@@ -54,7 +55,7 @@ def main():
         lhs = ri.device_normal((m, k), 1, 1.0, dev, torch.bfloat16)
         rhs = ri.device_normal((g, k, n), 2, 0.02, dev, torch.bfloat16)
         out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-        plan = gg.Plan(m, k, n, g, "forward", "bf16", "bf16", flags=args.flags)
+        plan = gg.Plan(m, k, n, g, "forward", "bf16", "bf16", flags=args.flags, tile_n=args.tile_n)
         if args.kernel == "fwd":
             def run():
                 gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream)

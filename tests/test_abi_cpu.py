@@ -50,6 +50,10 @@ def test_status_strings_and_version(lib):
     (dict(m=16, k=8, n=8, groups=1, flags=0x20), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=16, k=8, n=8, groups=1, flags=gg.RDOT_FLAG_CTA_PAIR | gg.RDOT_FLAG_NO_CTA_PAIR), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=16, k=8, n=8, groups=1, tile_n=96), gg.RDOT_ERR_UNSUPPORTED),
+    # 512-column tiles exist for the bf16-out forward on CTA pairs only
+    (dict(m=16, k=8, n=8, groups=1, tile_n=512, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=8, n=8, groups=1, tile_n=512, flags=gg.RDOT_FLAG_NO_CTA_PAIR), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=8, n=8, groups=1, tile_n=512, mode=1, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=8, n=8, groups=1, mode=7), gg.RDOT_ERR_INVALID_ARG),
 ])
 def test_plan_argument_checks_without_gpu(lib, kw, status):

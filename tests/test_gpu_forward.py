@@ -80,6 +80,23 @@ def test_scan_and_tile_map_bit_exact(gs, m, in_dtype, n, flags):
     assert (plan.status() & gg.RDOT_STATUS_BIT_GROUP_SIZES) == (gg.RDOT_STATUS_BIT_GROUP_SIZES if flags_ref else 0)
 
 
+@pytest.mark.parametrize("gs, m", SCAN_CASES)
+def test_tile_map_wide_pair_tiles(gs, m):
+    """256 x 512 tiles: the device's work list equals the oracle's enumeration bit for bit."""
+    gs = np.asarray(gs, np.int32)
+    plan = gg.Plan(m, 64, 1536, gs.size, "forward", "bf16", "bf16", tile_n=512)
+    info = plan.info
+    assert (info["tile_m"], info["tile_n"]) == (256, 512)
+    pref_ref, tiles_ref = oracle.tile_map(gs, m, 1536, 256, 512, bool(info["m_inner"]), 0)
+    gs_d = torch.from_numpy(gs).to(DEV)
+    off = torch.full((gs.size + 1,), -7, dtype=torch.int32, device=DEV)
+    pref = torch.full((gs.size + 1,), -7, dtype=torch.int32, device=DEV)
+    tiles = torch.full((max(len(tiles_ref), 1), 3), -7, dtype=torch.int32, device=DEV)
+    gg.rdot_debug_offsets_tilemap(plan.handle, gs_d, off, pref, tiles, plan.workspace)
+    assert np.array_equal(pref.cpu().numpy(), pref_ref)
+    assert np.array_equal(tiles.cpu().numpy()[:len(tiles_ref)], tiles_ref)
+
+
 # ------------------------------------------------------------------------------ fp32 SIMT
 def test_tiny_f32_workload():
     cfg = ri.CONFIGS["tiny_f32"]
@@ -159,6 +176,35 @@ def test_bf16_forward_parity_cta_pairs(m, k, n, gs, out_dtype):
     assert status == 0
     assert rel_err(out, ref) <= TOL_BF16
     assert torch.all(out[total:] == 0)
+
+
+@pytest.mark.parametrize("m,k,n,gs", BF16_CASES + [(1700, 320, 640, [700, 0, 129, 1, 512, 300]),
+                                              (2000, 256, 1024, [257, 255, 256, 1, 1000, 0, 231]),
+                                              (900, 128, 1536, [450, 450]),
+                                              (700, 64, 520, [0, 699, 1])])
+@pytest.mark.parametrize("flags", [0, gg.RDOT_FLAG_COL_TILES_INNER])
+def test_bf16_forward_parity_wide_pair_tiles(m, k, n, gs, flags):
+    """The 256 x 512 CTA-pair kernel (two N=256 cta_group::2 MMAs per K step, one 512-column
+    accumulator handed over per half): ragged groups, halves of either CTA past the group or M,
+    column halves and 64-column chunks past N (N = 64, 200, 384, 520), both tile orders."""
+    gs = np.asarray(gs, np.int32)
+    lhs = torch.from_numpy(ri.host_normal((m, k), 15)).to(torch.bfloat16)
+    rhs = torch.from_numpy(ri.host_normal((gs.size, k, n), 16, 0.05)).to(torch.bfloat16)
+    total = int(gs.sum())
+    lhs[total:] = float("nan")
+    out, status, plan = run_forward(lhs, rhs, gs, tile_n=512, flags=flags)
+    assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 512 and plan.info["grid_ctas"] % 2 == 0
+    ref = oracle.forward(lhs, rhs, gs)
+    assert status == 0
+    assert rel_err(out, ref) <= TOL_BF16
+    assert torch.all(out[total:] == 0)
+
+
+def test_wide_pair_tiles_need_bf16_out_and_pairs():
+    for kw in (dict(out_dtype="f32"), dict(flags=gg.RDOT_FLAG_NO_CTA_PAIR)):
+        with pytest.raises(RuntimeError):
+            gg.Plan(512, 64, 512, 2, "forward", "bf16", kw.get("out_dtype", "bf16"), tile_n=512,
+                    flags=kw.get("flags", 0))
 
 
 @pytest.mark.parametrize("flags", [gg.RDOT_FLAG_ROW_TILES_INNER, gg.RDOT_FLAG_COL_TILES_INNER])
@@ -241,7 +287,7 @@ def test_misaligned_pointer_is_rejected_before_launch():
     assert st == gg.RDOT_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("mode", ["f32", "bf16_single", "bf16_pair"])
+@pytest.mark.parametrize("mode", ["f32", "bf16_single", "bf16_pair", "bf16_wide"])
 def test_max_groups_forward(mode):
     """G = RDOT_MAX_GROUPS (the largest shared-memory group table) with mostly tiny groups."""
     rng = np.random.default_rng(71)
@@ -252,7 +298,8 @@ def test_max_groups_forward(mode):
     dt = torch.float32 if mode == "f32" else torch.bfloat16
     lhs = torch.from_numpy(ri.host_normal((m, k), 72)).to(dt)
     rhs = torch.from_numpy(ri.host_normal((g, k, n), 73, 0.05)).to(dt)
-    flags = {"f32": 0, "bf16_single": gg.RDOT_FLAG_NO_CTA_PAIR, "bf16_pair": gg.RDOT_FLAG_CTA_PAIR}[mode]
-    out, status, _ = run_forward(lhs, rhs, gs, flags=flags)
+    flags = {"f32": 0, "bf16_single": gg.RDOT_FLAG_NO_CTA_PAIR, "bf16_pair": gg.RDOT_FLAG_CTA_PAIR,
+             "bf16_wide": 0}[mode]
+    out, status, _ = run_forward(lhs, rhs, gs, flags=flags, tile_n=512 if mode == "bf16_wide" else 0)
     assert status == 0
     assert rel_err(out, oracle.forward(lhs, rhs, gs)) <= (TOL_F32 if mode == "f32" else TOL_BF16)

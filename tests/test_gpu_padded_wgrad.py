@@ -44,6 +44,26 @@ def test_padded_matches_oracle(m, k, n, gs):
     assert rel_err(out, ref) <= TOL
 
 
+@pytest.mark.parametrize("tile_n, flags", [(0, gg.RDOT_FLAG_CTA_PAIR), (512, 0)])
+def test_padded_on_cta_pair_plans(tile_n, flags):
+    """The padded baseline runs its uniform GEMM with the plan's kernel: 256 x 256 and
+    256 x 512 CTA-pair tiles (N = 1000: a ragged last column tile)."""
+    gs = np.array([0, 313, 1, 0, 257, 300, 129], np.int32)
+    m, k, n = 1000, 256, 1000
+    lhs = torch.from_numpy(ri.host_normal((m, k), 75)).to(torch.bfloat16)
+    rhs = torch.from_numpy(ri.host_normal((gs.size, k, n), 76, 0.05)).to(torch.bfloat16)
+    plan = gg.Plan(m, k, n, gs.size, "forward", "bf16", "bf16", tile_n=tile_n, flags=flags)
+    assert plan.info["tile_m"] == 256
+    cap = _round_up(gs.max(), 256)
+    need = gg.rdot_padded_workspace_size(plan.handle, cap)
+    pad = torch.empty(need, dtype=torch.uint8, device=DEV)
+    out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gg.rdot_padded_forward(plan.handle, lhs.to(DEV), rhs.to(DEV), torch.from_numpy(gs).to(DEV), out, cap, pad,
+                           plan.workspace)
+    assert plan.status() == 0
+    assert rel_err(out, oracle.forward(lhs, rhs, gs)) <= TOL
+
+
 def test_padded_drops_rows_beyond_capacity():
     gs = np.array([300, 20, 100], np.int32)
     m, k, n = 450, 128, 256
