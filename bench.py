@@ -312,6 +312,13 @@ def bench_ours(args, rank, world, barrier):
            "steps": e2e_steps,
            "note": "weights resident; each step copies its activations and group sizes in and its output "
                    "out, pipelined over three streams (copy-in, compute, copy-out)"}
+    # a timed region of back-to-back launches lasting a quarter second or more runs at the
+    # power-capped clock, like the driver's sustained GEMM loop; a shorter one compares with the
+    # burst figure
+    if per_step * args.steps >= 0.25:
+        peak, peak_kind = peaks["bf16_tflops_sustained"], f"{peaks['source']} bf16 sustained (timed region {per_step * args.steps:.2f} s)"
+    else:
+        peak, peak_kind = peaks["bf16_tflops"], f"{peaks['source']} bf16 burst (timed region {per_step * args.steps:.3f} s)"
     result = {
         "metric": "ragged-dot useful TFLOP/s (fraction of GB300 dense bf16 peak; speedup vs padded in per_config)",
         "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -323,11 +330,12 @@ def bench_ours(args, rank, world, barrier):
                                                                * rhs.element_size()) > L2_BYTES else "warm L2",
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": round(value / world / peaks["bf16_tflops"], 4),
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": ncu_traffic(kernel, name, KERNEL_SOURCES[kernel]),
                      "kernel": kernel, "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}",
-                     "peak_kind": f"{peaks['source']} bf16 burst"},
+                     "peak_kind": peak_kind,
+                     "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4)},
         "e2e": e2e,
         "gpu_launches": args.steps,   # one librdot launch per timed step
         "clocks": clk,
