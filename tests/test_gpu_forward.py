@@ -15,6 +15,7 @@ import torch
 import group_gemm_gb300 as gg
 import oracle
 import rdot_inputs as ri
+from tests._metrics import COSINE_MIN, cosine_to_rounded
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -156,6 +157,7 @@ def test_bf16_forward_parity(m, k, n, gs, out_dtype):
     ref = oracle.forward(lhs, rhs, gs)
     assert status == 0
     assert rel_err(out, ref) <= TOL_BF16
+    assert cosine_to_rounded(out, ref, out_dtype) >= COSINE_MIN
     assert torch.all(out[total:] == 0)
 
 

@@ -13,6 +13,7 @@ import torch
 import group_gemm_gb300 as gg
 import oracle
 import rdot_inputs as ri
+from tests._metrics import COSINE_MIN, cosine_to_rounded
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -84,6 +85,7 @@ def test_full_size_bf16_forward_sampled_rows(name, flags):
     ref = oracle_rows_on_subset(lhs, rhs, gs, rows, gor)
     got = out[torch.from_numpy(rows).to(DEV)].double().cpu().numpy()
     assert rel_err(got, ref) <= TOL
+    assert cosine_to_rounded(got, ref) >= COSINE_MIN
 
 
 @pytest.mark.parametrize("flags", [0, 4])
@@ -136,3 +138,4 @@ def test_full_size_mxfp8_sampled_rows(flags):
                                counts.astype(np.int32))
     got = out[ridx].double().cpu().numpy()
     assert rel_err(got, ref) <= TOL
+    assert cosine_to_rounded(got, ref) >= COSINE_MIN

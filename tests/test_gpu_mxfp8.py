@@ -11,6 +11,7 @@ import torch
 import group_gemm_gb300 as gg
 import oracle
 import rdot_inputs as ri
+from tests._metrics import COSINE_MIN, cosine_to_rounded
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -91,6 +92,7 @@ def test_mxfp8_ragged_parity(m, k, n, gs, variant):
     ref = oracle.forward_mxfp8(aq, as_, bq, bs, gs)
     assert status == 0
     assert rel_err(out, ref) <= TOL
+    assert cosine_to_rounded(out, ref) >= COSINE_MIN
     assert torch.all(out[total:] == 0)
 
 
