@@ -432,6 +432,18 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
         entry.update({"padded_ms": round(tp * 1e3, 3), "padded_tflops_useful": round(fl / tp / 1e12, 3),
                       "padded_capacity": cap, "padded_flops_ratio": round(g * cap / float(gs.sum()), 3)})
         entry["speedup_vs_padded"] = round(tp / t, 3)
+        # the padded baseline's GEMM alone: the same kernel family on the padded buffers that the
+        # call above left in its scratch (every group exactly `cap` rows), scatter/gather excluded
+        rows = g * cap
+        out_off = -(-rows * k * 2 // 256) * 256
+        lhs_pad = pad[: rows * k * 2].view(torch.bfloat16).view(rows, k)
+        out_pad = pad[out_off: out_off + rows * n * 2].view(torch.bfloat16).view(rows, n)
+        uni = gg.Plan(rows, k, n, g, "forward", "bf16", "bf16", device=dev.index,
+                      flags=gg.RDOT_FLAG_CTA_PAIR if plan.info["tile_m"] == 256 else gg.RDOT_FLAG_NO_CTA_PAIR)
+        gs_u = torch.full((g,), cap, dtype=torch.int32, device=dev)
+        tg = _time_steps(lambda: gg.rdot_forward(uni.handle, lhs_pad, rhs, gs_u, out_pad, uni.workspace, stream),
+                         max(3, steps // 5), stream)
+        entry.update({"padded_gemm_only_ms": round(tg * 1e3, 3), "speedup_vs_padded_gemm_only": round(tg / t, 3)})
         entry["status"] = plan.status()
         res[name] = entry
         del lhs, rhs, out, pad

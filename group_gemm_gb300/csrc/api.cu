@@ -536,13 +536,16 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
         cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * p.groups * p.k * p.n, s);
         return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "cudaMemsetAsync");
     }
+    // boxes of 64 columns x the kernel's contraction rows per stage
+    const uint32_t box_rows = plan->pair ? WG2_ROWS : WG_ROWS;
     if (plan->map_lhs_ptr != lhs) {
-        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs, p.k, p.m, p.k * 2, 64, 64);
+        rdot_status st =
+            encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs, p.k, p.m, p.k * 2, 64, box_rows);
         if (st != RDOT_OK) return st;
         plan->map_lhs_ptr = lhs;
     }
     if (plan->map_rhs_ptr != dy) {
-        rdot_status st = encode_2d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, p.n, p.m, p.n * 2, 64, 64);
+        rdot_status st = encode_2d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, p.n, p.m, p.n * 2, 64, box_rows);
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = dy;
     }

@@ -66,6 +66,25 @@ __device__ __forceinline__ void store_block_32x32(const uint32_t (&v)[32], uint3
     __syncwarp();
 }
 
+// Reads a warp's 32 rows x 128 columns of fp32 accumulator (TMEM columns taddr .. taddr+127 of
+// its lane quarter) as packed bf16: pk[c][j] holds columns 32c + 2j, 32c + 2j + 1 of row `lane`.
+// Two 32-column loads are in flight per wait, which halves the serialised load latency of an
+// epilogue that holds the MMA warp while it runs.
+__device__ __forceinline__ void tmem_read_bf16_32x128(uint32_t taddr, uint32_t (&pk)[4][16]) {
+#pragma unroll
+    for (int c = 0; c < 4; c += 2) {
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, v0);
+        tmem_ld_32x32b_x32(taddr + (c + 1) * 32, v1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            pk[c][j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+            pk[c + 1][j] = pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
+        }
+    }
+}
+
 // The bf16 store of store_block_32x32 for a block already packed: p[j] holds columns 2j, 2j+1 of
 // row `lane` as bf16x2. Lets an epilogue release tensor memory before its global stores.
 __device__ __forceinline__ void store_packed_bf16_32x32(const uint32_t (&p)[16], uint32_t* stage, void* out,

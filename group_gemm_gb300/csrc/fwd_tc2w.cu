@@ -238,15 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const uint32_t tbase = tmem_base + h * HALF + 128 * sub + (static_cast<uint32_t>(q * 32) << 16);
                 uint32_t pk[4][16];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        pk[c][j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                }
+                tmem_read_bf16_32x128(tbase, pk);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[h]), 0));

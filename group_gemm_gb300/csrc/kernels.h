@@ -77,6 +77,9 @@ struct WgradArgs {
 cudaError_t launch_wg_maps(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a,
                            cudaStream_t stream);
 constexpr int WG_MAP_BYTES = 128;
+// contraction rows per stage (and per TMA box) of the grad-weight kernels
+constexpr int WG_ROWS = 64;        // wgrad_tc.cu
+constexpr int WG2_ROWS = 128;      // wgrad_tc2.cu
 
 cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
                             const WgradArgs& a, int bn, int grid, cudaStream_t stream);

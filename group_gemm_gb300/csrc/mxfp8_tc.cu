@@ -351,20 +351,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             if constexpr (NACC == 1) {
                 // one accumulator: read this warp's 32 x (BN/2) block out as bf16, hand tensor
                 // memory back to the MMA warp, then store while the next tile's MMAs run
-                uint32_t pk[BN / 64][16];
-#pragma unroll
-                for (int c = 0; c < BN / 64; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        pk[c][j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                }
+                static_assert(BN == 256, "one accumulator only with 256-column tiles");
+                uint32_t pk[4][16];
+                tmem_read_bf16_32x128(tbase, pk);
                 tc_fence_before();
                 mbar_arrive(&tempty[acc]);
 #pragma unroll
-                for (int c = 0; c < BN / 64; ++c) {
+                for (int c = 0; c < 4; ++c) {
                     const int col = n0 + c * 32;
                     if (rows_valid > 0 && col < a.N)
                         store_packed_bf16_32x32(pk[c], stage, out_rows + col, a.N, rows_valid, a.N - col);

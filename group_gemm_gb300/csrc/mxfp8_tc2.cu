@@ -234,21 +234,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 static_cast<__nv_bfloat16*>(a.out) + (static_cast<long long>(t.row0) + first) * a.N;
             // read this warp's 32 x 128 block out as bf16, hand the accumulator back, then store
             // while the pair's next tile runs
-            uint32_t pk[BN / 64][16];
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    pk[c][j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-            }
+            uint32_t pk[4][16];
+            tmem_read_bf16_32x128(tbase, pk);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(tempty), 0));
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 const int col = n0 + c * 32;
                 if (rows_valid > 0 && col < a.N)
                     store_packed_bf16_32x32(pk[c], stage_buf, out_rows + col, a.N, rows_valid, a.N - col);

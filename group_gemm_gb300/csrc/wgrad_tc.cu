@@ -25,7 +25,7 @@ namespace rdot {
 namespace {
 
 constexpr int THREADS = 192;
-constexpr int ROWS = 64;   // contraction rows per stage
+constexpr int ROWS = WG_ROWS;   // contraction rows per stage
 
 template <int BN, int STAGES>
 struct WgLayout {
