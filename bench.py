@@ -249,6 +249,16 @@ def bench_ours(args, rank, world, barrier):
     value = rate / 1e12
     launch_s = t / args.steps
     achieved = flops / launch_s / 1e12
+    # the median launch, from a separate pass with events around every launch (the mean above is
+    # the reported value; this pass is not part of it)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(min(args.steps, 50))]
+    for e0, e1 in ev:
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    median_ms = float(np.median([e0.elapsed_time(e1) for e0, e1 in ev]))
 
     # end to end through the public API: every step copies its activations and group sizes in
     # from pinned host memory and its output back out. The copies are pipelined the way a
@@ -322,7 +332,8 @@ def bench_ours(args, rank, world, barrier):
     result = {
         "metric": "ragged-dot useful TFLOP/s (fraction of GB300 dense bf16 peak; speedup vs padded in per_config)",
         "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 4), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 4),
+        "ms_per_step_median": round(median_ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg["in_dtype"], "data": "synthetic (seeded)",
         "config": {"workload": f"{name}: M={m} K={k} N={n} G={g}, {cfg['in_dtype']} in / {cfg['out_dtype']} out",
                    "group_sizes": f"sum={int(gs.sum())} min={int(gs.min())} max={int(gs.max())}",
