@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            const uint64_t a_policy = l2_policy_evict_last();
             uint32_t stage = 0, phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;   // stages with a load in flight, and its phase
             bool ok = true;
@@ -130,7 +131,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // accumulator columns the epilogue never stores
                     const int nchunks = min(BN / 64, (a.N - n0 + 63) / 64);
                     mbar_arrive_expect_tx(&full[stage], L::A_BYTES + nchunks * L::B_CHUNK_BYTES);
-                    tma_load_2d(sa, &tmap_a, &full[stage], kb * TC_BK, t.row0);
+                    // a row tile of lhs is re-read by every column tile of its group while the
+                    // weights of other groups stream through L2: keep it (DeepSeek-like: -1 %)
+                    tma_load_2d_hint(sa, &tmap_a, &full[stage], kb * TC_BK, t.row0, a_policy);
                     for (int j = 0; j < nchunks; ++j)
                         tma_load_3d(sb + j * L::B_CHUNK_BYTES, &tmap_b, &full[stage], n0 + 64 * j, kb * TC_BK, t.g);
                     issued_mask |= 1u << stage;
