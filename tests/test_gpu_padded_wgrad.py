@@ -82,6 +82,7 @@ WG_CASES = [
     (700, 256, 384, [0, 333, 0, 250]),               # trailing rows past the sum, empty ends
     (256, 64, 64, [256]),                            # G = 1
     (130, 512, 1408, [40, 90]),                      # wgrad widths of the suite
+    (1200, 256, 256, [129, 255, 256, 257, 191, 100]),  # tails of 128-row stages (pair kernel)
 ]
 
 
@@ -137,3 +138,30 @@ def test_grad_weight_max_groups(flags):
     ref = oracle.grad_weight_rows(lhs, dy, gs, np.repeat(sel, k), np.tile(np.arange(k), sel.size))
     got = dw[torch.from_numpy(sel).to(DEV)].reshape(-1, n)
     assert rel_err(got, ref) <= TOL
+
+
+@pytest.mark.parametrize("flags", [gg.RDOT_FLAG_NO_CTA_PAIR, gg.RDOT_FLAG_CTA_PAIR])
+def test_grad_weight_cuda_graph_replay_with_new_sizes(flags):
+    """A call is two launches (the per-group tensor maps, then the GEMM); both live on the device
+    side, so a captured graph replays correctly when only the group sizes change."""
+    m, k, n, g = 900, 256, 384, 4
+    lhs = torch.from_numpy(ri.host_normal((m, k), 95)).to(torch.bfloat16).to(DEV)
+    dy = torch.from_numpy(ri.host_normal((m, n), 96)).to(torch.bfloat16).to(DEV)
+    plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", flags=flags)
+    gs_d = torch.tensor([300, 200, 0, 300], dtype=torch.int32, device=DEV)
+    dw = torch.empty((g, k, n), dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        gg.rdot_grad_weight(plan.handle, lhs, dy, gs_d, dw, plan.workspace, s)   # encodes tensor maps
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        gg.rdot_grad_weight(plan.handle, lhs, dy, gs_d, dw, plan.workspace, s)
+    for sizes in ([900, 0, 0, 0], [1, 129, 64, 700], [0, 0, 0, 0], [257, 255, 128, 3]):
+        gs_d.copy_(torch.tensor(sizes, dtype=torch.int32))
+        dw.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert plan.status() == 0
+        ref = oracle.grad_weight(lhs.cpu(), dy.cpu(), np.array(sizes, np.int32))
+        assert rel_err(dw, ref) <= TOL
