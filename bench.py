@@ -173,17 +173,28 @@ def aggregate_over_ranks(t_local: float, units_local: float, world: int, device=
     return t_max, float(units.item()) / t_max
 
 
-def time_region(fn, steps, stream, barrier):
+def time_region(fn, steps, stream, barrier, per_step_ms=None):
+    """Seconds for `steps` calls of fn between a barrier + synchronize on both sides, by CUDA
+    events on `stream`. With a list for per_step_ms, an event after every call also yields each
+    step's duration (events are recorded between launches; the GPU work is unchanged)."""
     import torch
     barrier()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if per_step_ms is not None else None
     start.record(stream)
-    for _ in range(steps):
+    for i in range(steps):
         fn()
+        if marks is not None:
+            marks[i].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
+    if marks is not None:
+        prev = start
+        for m in marks:
+            per_step_ms.append(prev.elapsed_time(m))
+            prev = m
     return start.elapsed_time(end) / 1e3   # seconds
 
 
@@ -239,7 +250,8 @@ def bench_ours(args, rank, world, barrier):
     torch.cuda.synchronize()
     clocks = ClockSampler(dev.index)
     clocks.start()
-    t = time_region(step, args.steps, stream, barrier)
+    step_ms = []
+    t = time_region(step, args.steps, stream, barrier, step_ms)
     clk = clocks.stop()
     status = plan.status()
     if status:
@@ -249,16 +261,7 @@ def bench_ours(args, rank, world, barrier):
     value = rate / 1e12
     launch_s = t / args.steps
     achieved = flops / launch_s / 1e12
-    # the median launch, from a separate pass with events around every launch (the mean above is
-    # the reported value; this pass is not part of it)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(min(args.steps, 50))]
-    for e0, e1 in ev:
-        e0.record(stream)
-        step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    median_ms = float(np.median([e0.elapsed_time(e1) for e0, e1 in ev]))
+    median_ms = float(np.median(step_ms))   # of the same timed region, step by step
 
     # end to end through the public API: every step copies its activations and group sizes in
     # from pinned host memory and its output back out. The copies are pipelined the way a
