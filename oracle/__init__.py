@@ -11,6 +11,8 @@ Functions and the passages they follow (page titles and sections):
 * :func:`group_of_row` -- same section, Table 2 (group lookup).
 * :func:`forward` / :func:`forward_rows` -- Part 1 "The Ragged-Dot Operation", Part 3.
 * :func:`grad_weight` / :func:`grad_weight_rows` -- Part 3 "Contracting", Part 4 Table 7.
+* :func:`grad_input` / :func:`grad_input_rows` -- Part 4 Table 7 (dgrad_wi: dy[M,N] x rhs[E,K,N]
+  -> [M,K], contracting rhs's dimension 2).
 * :func:`forward_mxfp8_rows` -- AITER PR #5658 (E4M3 + E8M0 per 32 K elements).
 * :func:`tile_map` -- the library's scheduler order (not on the pages), by brute force.
 """
@@ -69,6 +71,9 @@ def _load():
         lib.orc_grad_weight_rows.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i32p, i64, i64,
                                              i64, ctypes.c_int, i32p, i64p, i64, dp]
         lib.orc_grad_weight_rows.restype = ctypes.c_int
+        lib.orc_grad_input_rows.argtypes = [vp, ctypes.c_int, vp, ctypes.c_int, i32p, i64, i64, i64,
+                                            ctypes.c_int, i64p, i64, dp]
+        lib.orc_grad_input_rows.restype = ctypes.c_int
         lib.orc_forward_mxfp8_rows.argtypes = [vp, vp, vp, vp, i32p, i64, i64, i64, ctypes.c_int,
                                                i64p, i64, dp]
         lib.orc_forward_mxfp8_rows.restype = ctypes.c_int
@@ -164,6 +169,35 @@ def forward(lhs, rhs, group_sizes):
     """Full ragged-dot forward ``[M, N]`` in float64."""
     m = _as_np(lhs)[0].shape[0]
     return forward_rows(lhs, rhs, group_sizes, np.arange(m, dtype=np.int64))
+
+
+def grad_input_rows(dy, rhs, group_sizes, rows):
+    """Rows ``rows`` of the data gradient ``dlhs = dy @ rhs[g]^T`` (dgrad_wi), float64
+    ``[len(rows), K]``; dy is ``[M, N]``, rhs ``[G, K, N]``."""
+    d, ddt = _as_np(dy)
+    b, bdt = _as_np(rhs)
+    if ddt is None or bdt is None:
+        raise TypeError("dy/rhs must be f32, f64 or bf16")
+    m, n = d.shape
+    g, k, n2 = b.shape
+    if n2 != n:
+        raise ValueError("dy/rhs contraction sizes differ")
+    gs = _gs(group_sizes)
+    if gs.size != g:
+        raise ValueError("group_sizes length must equal rhs.shape[0]")
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((r.size, k), dtype=np.float64)
+    flags = _load().orc_grad_input_rows(d.ctypes.data, ddt, b.ctypes.data, bdt, _ptr(gs, ctypes.c_int32),
+                                        m, k, n, g, _ptr(r, ctypes.c_int64), r.size, _ptr(out, ctypes.c_double))
+    if flags < 0:
+        raise MemoryError("oracle allocation failed")
+    return out
+
+
+def grad_input(dy, rhs, group_sizes):
+    """Full data gradient ``dlhs [M, K]`` in float64."""
+    m = _as_np(dy)[0].shape[0]
+    return grad_input_rows(dy, rhs, group_sizes, np.arange(m, dtype=np.int64))
 
 
 def grad_weight_rows(lhs, dy, group_sizes, gsel, asel):

@@ -18,6 +18,9 @@
  *                pull request #5831 item 1 zero-fills them).
  *   grad_weight  Part 3 "Contracting" and Part 4 Table 7 (wgrad_wi):
  *                dW[g] = lhs_g^T . dy_g, the contraction running over group g's rows only.
+ *   grad_input   Part 4 Table 7 (dgrad_wi): dlhs[M,K] from dy[M,N] and rhs[E,K,N], contracting
+ *                dy's dimension 1 with rhs's dimension 2 (the weight's output features):
+ *                dlhs[i, :] = dy[i, :] @ rhs[g(i)]^T; rows past sum(group_sizes) are zero.
  *   mxfp8        AITER PR #5658: E4M3 operands with one E8M0 scale per 32 elements of K;
  *                the element value is decode(code) * 2^(scale - 127).
  *   tile_map     not on the pages: the enumeration order of the library's per-group tiles,
@@ -147,6 +150,33 @@ int orc_grad_weight_rows(const void* lhs, int lhs_dtype, const void* dy, int dy_
         for (int64_t i = off[g]; i < off[g + 1]; ++i) {
             double x = orc_load(lhs, lhs_dtype, i * k + a);
             for (int64_t b = 0; b < n; ++b) o[b] += x * orc_load(dy, dy_dtype, i * n + b);
+        }
+    }
+    free(off);
+    return flags;
+}
+
+/* Data gradient (dgrad_wi: the weight's output-feature axis is contracted) for a list of rows.
+ * dy [m, n], rhs [g, k, n], out [nrows, k] (row r of out is row rows[r] of the full dlhs).
+ * Each element is sum_{j ascending} dy[i, j] * rhs[g(i), kk, j] in double. */
+int orc_grad_input_rows(const void* dy, int dy_dtype, const void* rhs, int rhs_dtype,
+                        const int32_t* group_sizes, int64_t m, int64_t k, int64_t n, int g_count,
+                        const int64_t* rows, int64_t nrows, double* out) {
+    int64_t* off = (int64_t*)malloc(sizeof(int64_t) * (size_t)(g_count + 1));
+    if (!off) return -1;
+    int flags = orc_offsets(group_sizes, g_count, m, off);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows[r];
+        double* o = out + r * k;
+        for (int64_t kk = 0; kk < k; ++kk) o[kk] = 0.0;
+        int g = (i >= 0 && i < m) ? orc_group_of_row(off, g_count, i) : -1;
+        if (g < 0) continue;
+        for (int64_t kk = 0; kk < k; ++kk) {
+            int64_t b0 = ((int64_t)g * k + kk) * n;
+            double acc = 0.0;
+            for (int64_t j = 0; j < n; ++j) acc += orc_load(dy, dy_dtype, i * n + j) * orc_load(rhs, rhs_dtype, b0 + j);
+            o[kk] = acc;
         }
     }
     free(off);

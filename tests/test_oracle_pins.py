@@ -225,6 +225,57 @@ def test_grad_weight_entries_match_full():
     assert np.array_equal(oracle.grad_weight_rows(lhs, dy, gs, gsel, asel), full[gsel, asel])
 
 
+# ----------------------------------------------------------------------------- data gradient
+@pytest.mark.parametrize("seed", [31, 32, 33])
+def test_grad_input_brute_force(seed):
+    """dgrad_wi ("Group-GEMM in XLA", Part 4 Table 7): dlhs[M,K] = dy[M,N] . rhs[g]^T, contracting
+    dy's dimension 1 with rhs's dimension 2, by numpy per group; rows past the sum are zero."""
+    rng = np.random.default_rng(seed)
+    g = int(rng.integers(1, 6))
+    gs = rng.integers(0, 7, size=g).astype(np.int32)
+    gs[rng.integers(0, g)] = 0
+    m, k, n = int(gs.sum()) + 3, int(rng.integers(1, 9)), int(rng.integers(1, 9))
+    dy = rng.standard_normal((m, n))
+    rhs = rng.standard_normal((g, k, n))
+    dy[int(gs.sum()):] = np.nan                        # rows past the sum never contribute
+    got = oracle.grad_input(dy, rhs, gs)
+    ref = np.zeros((m, k))
+    start = 0
+    for e, sz in enumerate(gs):
+        ref[start:start + sz] = dy[start:start + sz] @ rhs[e].T
+        start += sz
+    assert got.shape == (m, k)
+    assert _rel(got, ref) < TOL
+    assert np.all(got[start:] == 0.0)
+
+
+def test_grad_input_is_the_adjoint_of_the_forward():
+    """For every x, <forward(x, W), dy> = <x, grad_input(dy, W)> over the rows inside the groups:
+    the data gradient is the transpose of the forward map (a transposed operand, a wrong
+    contraction axis or a wrong group fails it)."""
+    rng = np.random.default_rng(34)
+    gs = np.array([5, 0, 3, 7, 1], np.int32)
+    m, k, n = int(gs.sum()) + 4, 6, 9
+    x = rng.standard_normal((m, k))
+    dy = rng.standard_normal((m, n))
+    w = rng.standard_normal((gs.size, k, n))
+    lhs_side = float(np.sum(oracle.forward(x, w, gs) * dy))
+    rhs_side = float(np.sum(x * oracle.grad_input(dy, w, gs)))
+    assert abs(lhs_side - rhs_side) <= 1e-10 * (abs(lhs_side) + 1.0)
+
+
+def test_grad_input_rows_subset_and_transposed_forward():
+    rng = np.random.default_rng(35)
+    gs = np.array([2, 4, 0, 3], np.int32)
+    dy = rng.standard_normal((10, 5))
+    w = rng.standard_normal((4, 3, 5))
+    full = oracle.grad_input(dy, w, gs)
+    rows = np.array([9, 0, 5, 2])
+    assert np.array_equal(oracle.grad_input_rows(dy, w, gs, rows), full[rows])
+    # the same numbers as a forward whose weights are the transposed slabs [G, N, K]
+    assert _rel(full, oracle.forward(dy, np.ascontiguousarray(w.transpose(0, 2, 1)), gs)) < TOL
+
+
 # ------------------------------------------------------------------------------------- MXFP8
 def test_e4m3_decoder_matches_torch_on_all_codes():
     codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
