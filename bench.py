@@ -462,6 +462,24 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
         res[name] = entry
         del lhs, rhs, out, pad
         torch.cuda.empty_cache()
+    # data gradient of the Mixtral-like forward: dlhs [M, K] = dy [M, N] . rhs[g]^T
+    cfg = ri.CONFIGS["mixtral_bf16"]
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    gs = ri.config_group_sizes("mixtral_bf16")
+    dy = ri.device_normal((m, n), 3000, 1.0, dev, torch.bfloat16)
+    rhs = ri.device_normal((g, k, n), 2000, 0.02, dev, torch.bfloat16)
+    dlhs = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
+    gs_d = torch.from_numpy(gs).to(dev)
+    plan = gg.Plan(m, k, n, g, "grad_input", "bf16", "bf16", device=dev.index)
+    t = _time_steps(lambda: gg.rdot_grad_input(plan.handle, dy, rhs, gs_d, dlhs, plan.workspace, stream), steps,
+                    stream)
+    fl = useful_flops(gs, k, n)
+    res["dgrad_bf16"] = {"workload": f"data gradient of mixtral_bf16: dy [{m}, {n}] x rhs [{g}, {k}, {n}] -> [{m}, {k}]",
+                         "tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
+                         "frac_of_bf16_peak": round(fl / t / 1e12 / peaks["bf16_tflops"], 4), "status": plan.status(),
+                         "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}"}
+    del dy, rhs, dlhs
+    torch.cuda.empty_cache()
     # weight gradient
     cfg = ri.CONFIGS["wgrad_bf16"]
     m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]

@@ -22,14 +22,14 @@ __all__ = [
     "rdot_grad_weight", "rdot_padded_workspace_size", "rdot_padded_forward", "rdot_read_status",
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
-    "rdot_forward_no_alloc", "ragged_dot", "grad_weight", "ragged_dot_mxfp8", "padded_ragged_dot",
-    "EXPORTED_SYMBOLS",
+    "rdot_forward_no_alloc", "rdot_grad_input", "ragged_dot", "grad_weight", "grad_input",
+    "ragged_dot_mxfp8", "padded_ragged_dot", "EXPORTED_SYMBOLS",
 ]
 
 RDOT_OK, RDOT_ERR_INVALID_ARG, RDOT_ERR_UNSUPPORTED, RDOT_ERR_CUDA = 0, 1, 2, 3
 RDOT_ERR_DEVICE_TIMEOUT, RDOT_WARN_GROUP_SIZES = 4, 5
 RDOT_F32, RDOT_BF16, RDOT_E4M3 = 0, 1, 2
-RDOT_MODE_FORWARD, RDOT_MODE_GRAD_WEIGHT, RDOT_MODE_FORWARD_MXFP8 = 0, 1, 2
+RDOT_MODE_FORWARD, RDOT_MODE_GRAD_WEIGHT, RDOT_MODE_FORWARD_MXFP8, RDOT_MODE_GRAD_INPUT = 0, 1, 2, 3
 RDOT_STATUS_BIT_GROUP_SIZES, RDOT_STATUS_BIT_TIMEOUT = 0x1, 0x2
 RDOT_FLAG_ROW_TILES_INNER, RDOT_FLAG_COL_TILES_INNER = 0x1, 0x2
 RDOT_FLAG_CTA_PAIR, RDOT_FLAG_NO_CTA_PAIR, RDOT_FLAG_NATURAL_ORDER = 0x4, 0x8, 0x10
@@ -41,12 +41,12 @@ EXPORTED_SYMBOLS = (
     "rdot_grad_weight", "rdot_padded_workspace_size", "rdot_padded_forward", "rdot_read_status",
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
-    "rdot_forward_no_alloc",
+    "rdot_forward_no_alloc", "rdot_grad_input",
 )
 
 _DTYPE_CODES = {"f32": RDOT_F32, "bf16": RDOT_BF16, "e4m3": RDOT_E4M3}
 _MODE_CODES = {"forward": RDOT_MODE_FORWARD, "grad_weight": RDOT_MODE_GRAD_WEIGHT,
-               "forward_mxfp8": RDOT_MODE_FORWARD_MXFP8}
+               "forward_mxfp8": RDOT_MODE_FORWARD_MXFP8, "grad_input": RDOT_MODE_GRAD_INPUT}
 
 
 class RdotError(RuntimeError):
@@ -91,6 +91,7 @@ def load():
             "rdot_forward": ([vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_forward_mxfp8": ([vp, vp, vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_grad_weight": ([vp, vp, vp, vp, vp, vp, vp], st),
+            "rdot_grad_input": ([vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_padded_workspace_size": ([vp, i64, ctypes.POINTER(ctypes.c_size_t)], st),
             "rdot_padded_forward": ([vp, vp, vp, vp, vp, i64, vp, vp, vp], st),
             "rdot_read_status": ([vp, vp, i32p, vp], st),
@@ -159,6 +160,11 @@ def rdot_forward_mxfp8(plan, lhs, lhs_scale, rhs, rhs_scale, group_sizes, out, w
 def rdot_grad_weight(plan, lhs, dy, group_sizes, dw, workspace, stream=None) -> None:
     _check(load().rdot_grad_weight(plan, _ptr(lhs), _ptr(dy), _ptr(group_sizes), _ptr(dw), _ptr(workspace),
                                    _stream(stream, dw.device)), "rdot_grad_weight")
+
+
+def rdot_grad_input(plan, dy, rhs, group_sizes, dlhs, workspace, stream=None) -> None:
+    _check(load().rdot_grad_input(plan, _ptr(dy), _ptr(rhs), _ptr(group_sizes), _ptr(dlhs), _ptr(workspace),
+                                  _stream(stream, dlhs.device)), "rdot_grad_input")
 
 
 def rdot_padded_workspace_size(plan, capacity: int) -> int:
@@ -307,6 +313,24 @@ def grad_weight(lhs, dy, group_sizes, dw=None, stream=None):
     rdot_grad_weight(plan.handle, lhs.contiguous(), dy.contiguous(), group_sizes.to(torch.int32).contiguous(), dw,
                      plan.workspace, stream)
     return dw
+
+
+def grad_input(dy, rhs, group_sizes, out_dtype=None, dlhs=None, stream=None):
+    """``dlhs[i] = dy[i] @ rhs[g(i)]^T`` ([M, K]) for bf16 dy [M, N] and rhs [G, K, N]: the
+    data gradient of :func:`ragged_dot` (zeros past the sum)."""
+    import torch
+    m, n = dy.shape
+    g, k, _ = rhs.shape
+    out_dtype = out_dtype or dy.dtype
+    names = {torch.bfloat16: "bf16", torch.float32: "f32"}
+    key = ("dgrad", m, k, n, g, out_dtype, dy.device)
+    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="grad_input", in_dtype="bf16",
+                        out_dtype=names[out_dtype], device=dy.device)
+    if dlhs is None:
+        dlhs = torch.empty((m, k), dtype=out_dtype, device=dy.device)
+    rdot_grad_input(plan.handle, dy.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(), dlhs,
+                    plan.workspace, stream)
+    return dlhs
 
 
 def ragged_dot_mxfp8(lhs_q, lhs_scale, rhs_q, rhs_scale, group_sizes, out=None, stream=None):

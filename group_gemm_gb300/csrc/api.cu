@@ -80,7 +80,8 @@ struct rdot_plan_s {
     int device = 0;
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
-    int kind = 0;          // 0: SIMT fp32 forward, 1: tcgen05 bf16 forward, 2: tcgen05 grad-weight, 3: MXFP8
+    int kind = 0;          // 0: SIMT fp32 forward, 1: tcgen05 bf16 forward, 2: tcgen05 grad-weight, 3: MXFP8,
+                           // 4: tcgen05 data gradient (the forward kernels, K-major B)
     int tile_m = 0, tile_n = 0;
     int m_inner = 1;
     int grid = 1;
@@ -178,6 +179,11 @@ rdot_status check_problem(const rdot_problem* p) {
             if (p->in_dtype != RDOT_BF16 || p->out_dtype != RDOT_F32) return RDOT_ERR_UNSUPPORTED;
             if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;
             return RDOT_OK;
+        case RDOT_MODE_GRAD_INPUT:
+            if (p->in_dtype != RDOT_BF16) return RDOT_ERR_UNSUPPORTED;
+            if (p->out_dtype != RDOT_F32 && p->out_dtype != RDOT_BF16) return RDOT_ERR_UNSUPPORTED;
+            if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;   // 16-byte TMA rows
+            return RDOT_OK;
         case RDOT_MODE_FORWARD_MXFP8:
             if (p->in_dtype != RDOT_E4M3 || p->out_dtype != RDOT_BF16) return RDOT_ERR_UNSUPPORTED;
             if (p->k % 32 || p->n % 16) return RDOT_ERR_UNSUPPORTED;   // MX block 32; 16-byte row pitch
@@ -263,6 +269,44 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
         // small average groups: interleave the tiles of groups with 2+ row tiles with the
         // others so every wave mixes tensor-core-bound and weight-streaming work
+        pl->big_mt = (!want_pair && !(p.flags & RDOT_FLAG_NATURAL_ORDER)) ? 2 : 0;
+    } else if (p.mode == RDOT_MODE_GRAD_INPUT) {
+        if (prop.major != 10) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->kind = 4;
+        // the forward's tiling with the output width K in place of N: dlhs[M,K] = dy[M,N] rhs^T
+        pl->m_inner = (m_avg <= p.k) ? 1 : 0;
+        if (p.flags & 1) pl->m_inner = 1;
+        if (p.flags & 2) pl->m_inner = 0;
+        const bool want_pair = (p.flags & RDOT_FLAG_CTA_PAIR) ||
+                               (!(p.flags & RDOT_FLAG_NO_CTA_PAIR) && m_avg >= TC2_BM && p.k >= 256);
+        if (want_pair && p.tile_n == 128) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        int clusters = 0;
+        if (want_pair) {
+            clusters = fwd_tc2_max_clusters(p.out_dtype == RDOT_F32, p.groups);
+            if (clusters <= 0) {
+                delete pl;
+                return cuda_fail(cudaGetLastError(), "cudaOccupancyMaxActiveClusters");
+            }
+        }
+        pl->pair = want_pair;
+        pl->tile_m = want_pair ? TC2_BM : TC_BM;
+        pl->tile_n = want_pair ? 256 : (p.tile_n ? p.tile_n : (p.k <= 128 ? 128 : 256));
+        const int nt = static_cast<int>((p.k + pl->tile_n - 1) / pl->tile_n);
+        const long long bound = forward_tile_bound(p.m, p.groups, pl->tile_m, nt);
+        if (bound > 0x7fffffffLL) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        if (want_pair)
+            pl->grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(bound, clusters)));
+        else
+            pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
         pl->big_mt = (!want_pair && !(p.flags & RDOT_FLAG_NATURAL_ORDER)) ? 2 : 0;
     } else if (p.mode == RDOT_MODE_FORWARD_MXFP8) {
         if (prop.major != 10) {
@@ -445,6 +489,54 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
     else
         e = launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "fwd_tc launch");
+    return RDOT_OK;
+}
+
+rdot_status rdot_grad_input(rdot_plan_t plan, const void* dy, const void* rhs, const int32_t* group_sizes,
+                            void* dlhs, void* workspace, void* stream) {
+    if (!plan || !group_sizes || !workspace) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.mode != RDOT_MODE_GRAD_INPUT || plan->kind != 4) return RDOT_ERR_INVALID_ARG;
+    if (p.m == 0) return RDOT_OK;
+    if (!dy || !rhs || !dlhs) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(dy) || !aligned16(rhs) || !aligned16(dlhs) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // A = dy [M, N], K-major with the contraction N contiguous; B = rhs[g] viewed as
+    // [K rows (output columns), N (contraction)]: K-major, one box of 64 N x (output columns)
+    if (plan->map_lhs_ptr != dy) {
+        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, p.n, p.m, p.n * 2, TC_BK,
+                                   TC_BM);
+        if (st != RDOT_OK) return st;
+        plan->map_lhs_ptr = dy;
+    }
+    if (plan->map_rhs_ptr != rhs) {
+        const uint32_t box_rows = plan->pair ? 128 : static_cast<uint32_t>(plan->tile_n);
+        rdot_status st = encode_3d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rhs, p.n, p.k, p.groups, p.n * 2,
+                                   p.k * p.n * 2, TC_BK, box_rows, 1);
+        if (st != RDOT_OK) return st;
+        plan->map_rhs_ptr = rhs;
+    }
+    FwdArgs a{};
+    a.group_sizes = group_sizes;
+    a.out = dlhs;
+    a.M = static_cast<int>(p.m);
+    a.K = static_cast<int>(p.n);   // the contraction
+    a.N = static_cast<int>(p.k);   // the output width
+    a.G = p.groups;
+    a.NT = static_cast<int>((p.k + plan->tile_n - 1) / plan->tile_n);
+    a.m_inner = plan->m_inner;
+    a.big_mt = plan->big_mt;
+    a.b_kmajor = 1;
+    a.status = static_cast<int32_t*>(workspace);
+    a.timeout_ns = plan->timeout_ns;
+    cudaError_t e = plan->pair
+                        ? launch_fwd_tc2(plan->map_a, plan->map_b, a, p.out_dtype == RDOT_F32, plan->grid, s)
+                        : launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "grad_input launch");
     return RDOT_OK;
 }
 
@@ -703,7 +795,8 @@ rdot_status rdot_debug_offsets_tilemap(rdot_plan_t plan, const int32_t* group_si
     if (tiles && max_tiles < 0) return RDOT_ERR_INVALID_ARG;
     const rdot_problem& p = plan->p;
     DeviceGuard dg(plan->device);
-    const int nt = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
+    const int64_t out_width = plan->kind == 4 ? p.k : p.n;   // the data gradient's output is [M, K]
+    const int nt = static_cast<int>((out_width + plan->tile_n - 1) / plan->tile_n);
     cudaError_t e = launch_scan_export(group_sizes, p.groups, static_cast<int>(p.m), plan->tile_m, nt, plan->m_inner,
                                        plan->big_mt, offsets, tile_prefix, tiles, tiles ? max_tiles : 0,
                                        static_cast<int32_t*>(workspace), static_cast<cudaStream_t>(stream));
@@ -733,6 +826,6 @@ const char* rdot_status_string(rdot_status status) {
 
 const char* rdot_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
-int rdot_version(void) { return 100; }
+int rdot_version(void) { return 101; }
 
 }  // extern "C"

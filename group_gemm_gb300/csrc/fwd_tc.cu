@@ -8,7 +8,9 @@
 // Design (one persistent CTA per SM, 192 threads, warp-specialised):
 //   warp 0      TMA producer: lhs tile [128 rows x 64 K] (K-major) and rhs tile [64 K x BN]
 //               (N-contiguous, so the B operand is MN-major), both 128-byte swizzled, into an
-//               S-stage shared-memory ring guarded by full/empty mbarriers.
+//               S-stage shared-memory ring guarded by full/empty mbarriers. The data gradient
+//               (dgrad_wi of Part 4 Table 7) runs the same kernel with a K-major B: its rhs slab
+//               [N out, K contraction] has the contraction contiguous, one [BN x 64] box a stage.
 //   warp 1      allocates 2*BN TMEM columns (two fp32 accumulators of 128 lanes x BN) and issues
 //               tcgen05.mma kind::f16 (M=128, N=BN, K=16) from one thread; tcgen05.commit frees
 //               each smem stage and, after the last K block, signals "accumulator full".
@@ -127,15 +129,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     uint8_t* sa = smem + stage * L::STAGE_BYTES;
                     uint8_t* sb = sa + L::A_BYTES;
-                    // 64-wide column chunks entirely past N are not loaded: they only feed
-                    // accumulator columns the epilogue never stores
+                    // MN-major B: 64-wide column chunks entirely past N are not loaded (they only
+                    // feed accumulator columns the epilogue never stores). K-major B: one box of
+                    // BN rows x 64 K, rows past N zero-filled.
                     const int nchunks = min(BN / 64, (a.N - n0 + 63) / 64);
-                    mbar_arrive_expect_tx(&full[stage], L::A_BYTES + nchunks * L::B_CHUNK_BYTES);
+                    mbar_arrive_expect_tx(&full[stage],
+                                          L::A_BYTES + (a.b_kmajor ? L::B_BYTES : nchunks * L::B_CHUNK_BYTES));
                     // a row tile of lhs is re-read by every column tile of its group while the
                     // weights of other groups stream through L2: keep it (DeepSeek-like: -1 %)
                     tma_load_2d_hint(sa, &tmap_a, &full[stage], kb * TC_BK, t.row0, a_policy);
-                    for (int j = 0; j < nchunks; ++j)
-                        tma_load_3d(sb + j * L::B_CHUNK_BYTES, &tmap_b, &full[stage], n0 + 64 * j, kb * TC_BK, t.g);
+                    if (a.b_kmajor)
+                        tma_load_3d(sb, &tmap_b, &full[stage], kb * TC_BK, n0, t.g);
+                    else
+                        for (int j = 0; j < nchunks; ++j)
+                            tma_load_3d(sb + j * L::B_CHUNK_BYTES, &tmap_b, &full[stage], n0 + 64 * j, kb * TC_BK,
+                                        t.g);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -157,7 +165,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(TC_BM, BN, true, true, false, true);
+            const bool kmaj = a.b_kmajor != 0;
+            const uint32_t idesc = kmaj ? idesc_f16(TC_BM, BN, true, true, false, false)
+                                        : idesc_f16(TC_BM, BN, true, true, false, true);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
@@ -176,8 +186,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int kk = 0; kk < TC_BK / 16; ++kk) {
                         // A: K-major, +32 bytes per 16-element K step inside the 128-byte row
                         const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
-                        // B: MN-major, +2 groups of 8 K rows (2 x 1024 bytes) per K step
-                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, L::B_CHUNK_BYTES, 1024);
+                        // B: MN-major, +2 groups of 8 K rows (2 x 1024 bytes) per K step; or
+                        // K-major like A (BN rows of 128 bytes), +32 bytes per K step
+                        const uint64_t bdesc = kmaj ? smem_desc_sw128(sb + kk * 32, 16, 1024)
+                                                    : smem_desc_sw128(sb + kk * 2048, L::B_CHUNK_BYTES, 1024);
                         mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit(&empty[stage]);

@@ -114,8 +114,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 // bytes each CTA brings in: its A half unless it lies wholly past M, and the
                 // 64-column chunks of its B half that are not wholly past N
                 const int a0 = A_BYTES, a1 = (t.row0 + 128 < a.M) ? A_BYTES : 0;
-                const int c0 = max(0, min(2, (a.N - n0 + 63) / 64));
-                const int c1 = max(0, min(2, (a.N - n0 - 128 + 63) / 64));
+                // (K-major B, the data gradient: one 128-row box per CTA, or none past N)
+                const bool kmaj = a.b_kmajor != 0;
+                const int c0 = kmaj ? 2 : max(0, min(2, (a.N - n0 + 63) / 64));
+                const int c1 = kmaj ? (n0 + 128 < a.N ? 2 : 0) : max(0, min(2, (a.N - n0 - 128 + 63) / 64));
                 const int my_a = rank ? a1 : a0;
                 const int my_c = rank ? c1 : c0;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -128,9 +130,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     if (leader) mbar_arrive_expect_tx(&full[stage], a0 + a1 + (c0 + c1) * B_CHUNK_BYTES);
                     const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
                     if (my_a) tma_load_2d_pair(sa, &tmap_a, fb, kb * TC_BK, t.row0 + 128 * static_cast<int>(rank));
-                    for (int j = 0; j < my_c; ++j)
-                        tma_load_3d_pair(sb + j * B_CHUNK_BYTES, &tmap_b, fb, n0 + 128 * static_cast<int>(rank) + 64 * j,
-                                         kb * TC_BK, t.g);
+                    if (kmaj) {
+                        if (my_c) tma_load_3d_pair(sb, &tmap_b, fb, kb * TC_BK, n0 + 128 * static_cast<int>(rank), t.g);
+                    } else {
+                        for (int j = 0; j < my_c; ++j)
+                            tma_load_3d_pair(sb + j * B_CHUNK_BYTES, &tmap_b, fb,
+                                             n0 + 128 * static_cast<int>(rank) + 64 * j, kb * TC_BK, t.g);
+                    }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -161,7 +167,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && leader) {
-            constexpr uint32_t idesc = idesc_f16(BM, BN, true, true, false, true);
+            const bool kmaj = a.b_kmajor != 0;
+            const uint32_t idesc = kmaj ? idesc_f16(BM, BN, true, true, false, false)
+                                        : idesc_f16(BM, BN, true, true, false, true);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int w = cluster; w < W && ok; w += nclusters) {
@@ -179,7 +187,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int kk = 0; kk < TC_BK / 16; ++kk) {
                         const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 2048, B_CHUNK_BYTES, 1024);
+                        const uint64_t bdesc = kmaj ? smem_desc_sw128(sb + kk * 32, 16, 1024)
+                                                    : smem_desc_sw128(sb + kk * 2048, B_CHUNK_BYTES, 1024);
                         mma_f16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit_pair_multicast(&empty[stage], 0x3);

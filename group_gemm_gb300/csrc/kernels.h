@@ -23,6 +23,8 @@ struct FwdArgs {
     int NT;                      // column tiles per group
     int m_inner;                 // 1: row tiles fastest inside a group
     int big_mt;                  // > 0: interleave groups with >= big_mt row tiles with the others
+    int b_kmajor;                // 1: the B operand is K-major (rhs [G, N, K] with K contiguous; the
+                                 // data gradient), 0: MN-major (rhs [G, K, N], the forward)
     int32_t* status;             // device status word (may be null)
     uint64_t timeout_ns;         // bounded-wait limit
 };

@@ -26,7 +26,7 @@ def main():
     import rdot_inputs as ri
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwd", "wgrad", "padded", "mxfp8"], default="fwd")
+    ap.add_argument("--kernel", choices=["fwd", "dgrad", "wgrad", "padded", "mxfp8"], default="fwd")
     ap.add_argument("--workload", default="mixtral_bf16")
     ap.add_argument("--tokens", type=int, default=2048)
     ap.add_argument("--iters", type=int, default=3)
@@ -65,6 +65,15 @@ def main():
 
             def run():
                 gg.rdot_padded_forward(plan.handle, lhs, rhs, gs_d, out, cap, pad, plan.workspace, stream)
+        flops = 2.0 * m * k * n
+    elif args.kernel == "dgrad":
+        dy = ri.device_normal((m, n), 1, 1.0, dev, torch.bfloat16)
+        rhs = ri.device_normal((g, k, n), 2, 0.02, dev, torch.bfloat16)
+        dlhs = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
+        plan = gg.Plan(m, k, n, g, "grad_input", "bf16", "bf16", flags=args.flags, tile_n=args.tile_n)
+
+        def run():
+            gg.rdot_grad_input(plan.handle, dy, rhs, gs_d, dlhs, plan.workspace, stream)
         flops = 2.0 * m * k * n
     elif args.kernel == "wgrad":
         lhs = ri.device_normal((m, k), 1, 1.0, dev, torch.bfloat16)

@@ -56,7 +56,8 @@ typedef enum { RDOT_F32 = 0, RDOT_BF16 = 1, RDOT_E4M3 = 2 } rdot_dtype;
 typedef enum {
     RDOT_MODE_FORWARD = 0,       /* out[M,N] = lhs[M,K] @ rhs[g(i),K,N] (non-contracting ragged M) */
     RDOT_MODE_GRAD_WEIGHT = 1,   /* dw[G,K,N] = lhs_g^T dy_g (ragged contraction over the rows) */
-    RDOT_MODE_FORWARD_MXFP8 = 2  /* forward with E4M3 operands and E8M0 scales per 32 K elements */
+    RDOT_MODE_FORWARD_MXFP8 = 2, /* forward with E4M3 operands and E8M0 scales per 32 K elements */
+    RDOT_MODE_GRAD_INPUT = 3     /* dlhs[M,K] = dy[M,N] @ rhs[g(i),K,N]^T (contracts rhs's N axis) */
 } rdot_mode;
 
 /* Bits of the device status word (int32 at offset 0 of the workspace). */
@@ -154,6 +155,18 @@ RDOT_API rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const
 RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy,
                              const int32_t* group_sizes, float* dw, void* workspace,
                              void* stream);
+
+/* Data gradient of the forward ("Group-GEMM in XLA", Part 4 Table 7, class dgrad_wi: lhs [M,N],
+ * rhs [E,K,N], out [M,K], contracting lhs dimension 1 with rhs dimension 2).
+ *   dy    device bf16 [M, N]      (the forward's output gradient)
+ *   rhs   device bf16 [G, K, N]   (the forward's weights, as laid out for rdot_forward)
+ *   dlhs  device [M, K], the plan's out_dtype (bf16 or fp32): dlhs[i,:] = dy[i,:] @ rhs[g(i)]^T;
+ *         every row is written (zeros past the sum)
+ * The plan's problem describes the forward (m, k, n, groups) with mode RDOT_MODE_GRAD_INPUT,
+ * in_dtype RDOT_BF16; K and N must be multiples of 8 (16-byte TMA rows). Same workspace, status
+ * and stream rules as rdot_forward; the kernels are the forward's with a K-major B operand. */
+RDOT_API rdot_status rdot_grad_input(rdot_plan_t plan, const void* dy, const void* rhs,
+                            const int32_t* group_sizes, void* dlhs, void* workspace, void* stream);
 
 /* Bytes of the padded baseline's scratch for a capacity of `capacity` rows per group
  * (the padded lhs [G, capacity, K] plus the padded output [G, capacity, N] plus a small table). */
