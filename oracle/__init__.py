@@ -15,6 +15,12 @@ Functions and the passages they follow (page titles and sections):
   -> [M,K], contracting rhs's dimension 2).
 * :func:`forward_mxfp8_rows` -- AITER PR #5658 (E4M3 + E8M0 per 32 K elements).
 * :func:`tile_map` -- the library's scheduler order (not on the pages), by brute force.
+* :func:`moe_permute` / :func:`moe_unpermute` -- "Group-GEMM in XLA", Part 4 "The Three MoE
+  Compute Paths in MaxText", Path 1 (sparse / ragged-dot): the pre-processing sorts the token
+  copies by destination expert (a stable argsort of the flattened top-k indices), gathers the
+  replicated inputs in that order and bincounts group_sizes; the post-processing scatters the
+  rows back and sums each token's k outputs weighted by the router (Part 5 "Next steps";
+  "How to Scale Your Model", the MaxText MoE steps 2 and 5).
 """
 from __future__ import annotations
 
@@ -284,3 +290,47 @@ def tile_map(group_sizes, m: int, n: int, bm: int, bn: int, m_inner: bool, big_m
                      int(bool(m_inner)), int(big_mt), _ptr(pref, ctypes.c_int32), _ptr(tiles, ctypes.c_int32),
                      total)
     return pref, tiles[:total]
+
+
+# ------------------------------------------------------------------------ MoE permute / combine
+def moe_permute(topk_ids, x, n_experts: int):
+    """The sparse path's pre-processing, in plain numpy.
+
+    topk_ids [T, k] int: each token's k destination experts; x [T, K]: the token rows.
+    Returns ``(group_sizes int32[E], order int64[V], inv int64[T*k], x_sorted [T*k, K] float64)``:
+    ``order`` lists the flat indices t*k + j of the valid entries (0 <= id < E) by expert, ties in
+    flat order (a stable argsort); ``inv[t*k + j]`` is the sorted row of that copy (-1 for an
+    entry outside [0, E), which is dropped); ``x_sorted[p] = x[order[p] // k]`` for p < V and 0
+    past it. ``group_sizes`` is the bincount of the valid ids."""
+    ids = np.asarray(topk_ids).astype(np.int64)
+    t, k = ids.shape
+    flat = ids.reshape(-1)
+    valid = (flat >= 0) & (flat < n_experts)
+    key = np.where(valid, flat, n_experts)            # dropped entries sort after every expert
+    order_all = np.argsort(key, kind="stable")
+    v = int(valid.sum())
+    order = order_all[:v]
+    inv = np.full(t * k, -1, dtype=np.int64)
+    inv[order] = np.arange(v)
+    gs = np.bincount(flat[valid], minlength=n_experts).astype(np.int32)
+    xs = np.asarray(x, dtype=np.float64) if not hasattr(x, "float") else x.double().numpy()
+    x_sorted = np.zeros((t * k, xs.shape[1]))
+    x_sorted[:v] = xs[order // k]
+    return gs, order, inv, x_sorted
+
+
+def moe_unpermute(y_sorted, inv, topk_weights):
+    """The sparse path's post-processing: ``out[t] = sum_j w[t, j] * y_sorted[inv[t*k + j]]``
+    over the copies that were not dropped, in float64. y_sorted [T*k, N]; inv int[T*k];
+    topk_weights [T, k]."""
+    y = np.asarray(y_sorted, dtype=np.float64) if not hasattr(y_sorted, "float") else y_sorted.double().numpy()
+    w = np.asarray(topk_weights, dtype=np.float64) if not hasattr(topk_weights, "float") else \
+        topk_weights.double().numpy()
+    t, k = w.shape
+    inv = np.asarray(inv).reshape(t, k)
+    out = np.zeros((t, y.shape[1]))
+    for tt in range(t):
+        for j in range(k):
+            if inv[tt, j] >= 0:
+                out[tt] += w[tt, j] * y[inv[tt, j]]
+    return out

@@ -276,6 +276,62 @@ def test_grad_input_rows_subset_and_transposed_forward():
     assert _rel(full, oracle.forward(dy, np.ascontiguousarray(w.transpose(0, 2, 1)), gs)) < TOL
 
 
+# --------------------------------------------------------------------- MoE permute / combine
+def test_moe_route_worked_example():
+    d = _golden.read("moe_route_example.txt")
+    ids = d["topk_ids"].astype(np.int64)
+    x = np.arange(3 * 4, dtype=np.float64).reshape(3, 4)
+    gs, order, inv, xs = oracle.moe_permute(ids, x, int(d["n_experts"][0]))
+    assert np.array_equal(gs, d["group_sizes"].astype(np.int32))
+    assert np.array_equal(order, d["order"].astype(np.int64))
+    assert np.array_equal(order // 2, d["sorted_token"].astype(np.int64))
+    assert np.array_equal(inv, d["inv"].astype(np.int64))
+    assert np.array_equal(xs, x[d["sorted_token"].astype(np.int64)])
+    y = np.stack([np.arange(6.0), 10 * np.arange(6.0)], axis=1)
+    assert np.array_equal(oracle.moe_unpermute(y, inv, d["weights"]), d["out"])
+
+
+@pytest.mark.parametrize("seed", [51, 52])
+def test_moe_permute_is_a_stable_sort_with_bincount_sizes(seed):
+    rng = np.random.default_rng(seed)
+    t, k, e = 37, 3, 6
+    ids = rng.integers(-1, e + 1, size=(t, k))          # -1 and e are outside [0, E): dropped
+    x = rng.standard_normal((t, 5))
+    gs, order, inv, xs = oracle.moe_permute(ids, x, e)
+    flat = ids.reshape(-1)
+    valid = np.nonzero((flat >= 0) & (flat < e))[0]
+    assert np.array_equal(np.sort(order), valid)                          # a permutation of the valid copies
+    ex = flat[order]
+    assert np.all(np.diff(ex) >= 0)                                       # grouped by expert
+    same = np.diff(ex) == 0
+    assert np.all(np.diff(order)[same] > 0)                               # ties keep flat order
+    assert np.array_equal(gs, np.array([np.sum(flat == g) for g in range(e)], np.int32))
+    assert np.array_equal(inv[order], np.arange(order.size))
+    assert np.all(inv[np.setdiff1d(np.arange(t * k), valid)] == -1)
+    assert np.array_equal(xs[:order.size], x[order // k]) and np.all(xs[order.size:] == 0)
+
+
+def test_moe_unpermute_equals_a_dense_scatter_matmul_and_inverts_permute():
+    rng = np.random.default_rng(53)
+    t, k, e, n = 29, 2, 5, 7
+    ids = rng.integers(0, e, size=(t, k))
+    ids[3, 1] = -1                                       # one dropped copy
+    w = rng.random((t, k))
+    x = rng.standard_normal((t, n))
+    gs, order, inv, xs = oracle.moe_permute(ids, x, e)
+    y = rng.standard_normal((t * k, n))
+    # independent route: the scatter matrix S[t, inv[t*k+j]] = w[t, j], then one matmul
+    s_mat = np.zeros((t, t * k))
+    for tt in range(t):
+        for j in range(k):
+            if inv[tt * k + j] >= 0:
+                s_mat[tt, inv[tt * k + j]] += w[tt, j]
+    assert _rel(oracle.moe_unpermute(y, inv, w), s_mat @ y) < TOL
+    # combining the permuted copies of x gives each token times the sum of its kept weights
+    kept = w * (inv.reshape(t, k) >= 0)
+    assert _rel(oracle.moe_unpermute(xs, inv, w), x * kept.sum(axis=1, keepdims=True)) < TOL
+
+
 # ------------------------------------------------------------------------------------- MXFP8
 def test_e4m3_decoder_matches_torch_on_all_codes():
     codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
