@@ -22,7 +22,8 @@ __all__ = [
     "rdot_grad_weight", "rdot_padded_workspace_size", "rdot_padded_forward", "rdot_read_status",
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
-    "rdot_forward_no_alloc", "rdot_grad_input", "ragged_dot", "grad_weight", "grad_input",
+    "rdot_forward_no_alloc", "rdot_grad_input", "rdot_moe_route_workspace_size", "rdot_moe_permute",
+    "rdot_moe_unpermute", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight", "grad_input",
     "ragged_dot_mxfp8", "padded_ragged_dot", "EXPORTED_SYMBOLS",
 ]
 
@@ -41,7 +42,8 @@ EXPORTED_SYMBOLS = (
     "rdot_grad_weight", "rdot_padded_workspace_size", "rdot_padded_forward", "rdot_read_status",
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
-    "rdot_forward_no_alloc", "rdot_grad_input",
+    "rdot_forward_no_alloc", "rdot_grad_input", "rdot_moe_route_workspace_size", "rdot_moe_permute",
+    "rdot_moe_unpermute",
 )
 
 _DTYPE_CODES = {"f32": RDOT_F32, "bf16": RDOT_BF16, "e4m3": RDOT_E4M3}
@@ -92,6 +94,10 @@ def load():
             "rdot_forward_mxfp8": ([vp, vp, vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_grad_weight": ([vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_grad_input": ([vp, vp, vp, vp, vp, vp, vp], st),
+            "rdot_moe_route_workspace_size": ([i64, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
+                                              st),
+            "rdot_moe_permute": ([vp, i64, ctypes.c_int32, ctypes.c_int32, vp, i64, vp, vp, vp, vp, vp, vp], st),
+            "rdot_moe_unpermute": ([vp, vp, vp, i64, ctypes.c_int32, i64, vp, vp], st),
             "rdot_padded_workspace_size": ([vp, i64, ctypes.POINTER(ctypes.c_size_t)], st),
             "rdot_padded_forward": ([vp, vp, vp, vp, vp, i64, vp, vp, vp], st),
             "rdot_read_status": ([vp, vp, i32p, vp], st),
@@ -165,6 +171,27 @@ def rdot_grad_weight(plan, lhs, dy, group_sizes, dw, workspace, stream=None) -> 
 def rdot_grad_input(plan, dy, rhs, group_sizes, dlhs, workspace, stream=None) -> None:
     _check(load().rdot_grad_input(plan, _ptr(dy), _ptr(rhs), _ptr(group_sizes), _ptr(dlhs), _ptr(workspace),
                                   _stream(stream, dlhs.device)), "rdot_grad_input")
+
+
+def rdot_moe_route_workspace_size(tokens: int, topk: int, n_experts: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().rdot_moe_route_workspace_size(int(tokens), int(topk), int(n_experts), ctypes.byref(n)),
+           "rdot_moe_route_workspace_size")
+    return n.value
+
+
+def rdot_moe_permute(topk_ids, x, n_experts, group_sizes, order, inv, x_sorted, workspace, stream=None) -> None:
+    t, k = topk_ids.shape
+    _check(load().rdot_moe_permute(_ptr(topk_ids), int(t), int(k), int(n_experts), _ptr(x),
+                                   int(x.shape[1] * x.element_size()), _ptr(group_sizes), _ptr(order), _ptr(inv),
+                                   _ptr(x_sorted), _ptr(workspace), _stream(stream, x.device)), "rdot_moe_permute")
+
+
+def rdot_moe_unpermute(y_sorted, inv, topk_weights, out, stream=None) -> None:
+    t, k = topk_weights.shape
+    _check(load().rdot_moe_unpermute(_ptr(y_sorted), _ptr(inv), _ptr(topk_weights), int(t), int(k),
+                                     int(y_sorted.shape[1]), _ptr(out), _stream(stream, out.device)),
+           "rdot_moe_unpermute")
 
 
 def rdot_padded_workspace_size(plan, capacity: int) -> int:
@@ -331,6 +358,32 @@ def grad_input(dy, rhs, group_sizes, out_dtype=None, dlhs=None, stream=None):
     rdot_grad_input(plan.handle, dy.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(), dlhs,
                     plan.workspace, stream)
     return dlhs
+
+
+def moe_permute(topk_ids, x, n_experts, stream=None):
+    """Sorts the token copies by expert: returns ``(x_sorted [T*k, K], group_sizes [E], order,
+    inv)`` for int32 topk_ids [T, k] and x [T, K] (any dtype with 16-byte rows)."""
+    import torch
+    t, k = topk_ids.shape
+    dev = x.device
+    ids = topk_ids.to(device=dev, dtype=torch.int32).contiguous()
+    gs = torch.empty(n_experts, dtype=torch.int32, device=dev)
+    order = torch.empty(t * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(t * k, dtype=torch.int32, device=dev)
+    xs = torch.empty((t * k, x.shape[1]), dtype=x.dtype, device=dev)
+    ws = torch.empty(rdot_moe_route_workspace_size(t, k, n_experts), dtype=torch.uint8, device=dev)
+    rdot_moe_permute(ids, x.contiguous(), n_experts, gs, order, inv, xs, ws, stream)
+    return xs, gs, order, inv
+
+
+def moe_unpermute(y_sorted, inv, topk_weights, out=None, stream=None):
+    """``out[t] = sum_j w[t, j] * y_sorted[inv[t*k + j]]`` (bf16 [T, N])."""
+    import torch
+    t, _ = topk_weights.shape
+    if out is None:
+        out = torch.empty((t, y_sorted.shape[1]), dtype=torch.bfloat16, device=y_sorted.device)
+    rdot_moe_unpermute(y_sorted.contiguous(), inv, topk_weights.to(torch.float32).contiguous(), out, stream)
+    return out
 
 
 def ragged_dot_mxfp8(lhs_q, lhs_scale, rhs_q, rhs_scale, group_sizes, out=None, stream=None):

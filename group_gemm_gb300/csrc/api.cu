@@ -812,6 +812,61 @@ rdot_status rdot_debug_wait_timeout(rdot_plan_t plan, uint64_t timeout_ns, void*
     return RDOT_OK;
 }
 
+rdot_status rdot_moe_route_workspace_size(int64_t tokens, int32_t topk, int32_t n_experts, size_t* bytes) {
+    if (!bytes || tokens < 0 || topk < 1 || n_experts < 1 || n_experts > RDOT_MAX_GROUPS) return RDOT_ERR_INVALID_ARG;
+    if (tokens * static_cast<int64_t>(topk) > 0x7fffffffLL) return RDOT_ERR_UNSUPPORTED;
+    *bytes = moe_route_workspace_bytes(tokens * topk, n_experts);
+    return RDOT_OK;
+}
+
+namespace {
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int current_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+}  // namespace
+
+rdot_status rdot_moe_permute(const int32_t* topk_ids, int64_t tokens, int32_t topk, int32_t n_experts, const void* x,
+                             int64_t row_bytes, int32_t* group_sizes, int32_t* order, int32_t* inv, void* x_sorted,
+                             void* workspace, void* stream) {
+    if (tokens < 0 || topk < 1 || n_experts < 1 || n_experts > RDOT_MAX_GROUPS || !group_sizes)
+        return RDOT_ERR_INVALID_ARG;
+    if (tokens * static_cast<int64_t>(topk) > 0x7fffffffLL) return RDOT_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (tokens == 0) {
+        cudaError_t e = cudaMemsetAsync(group_sizes, 0, sizeof(int32_t) * n_experts, s);
+        return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (!topk_ids || !x || !order || !inv || !x_sorted || !workspace) return RDOT_ERR_INVALID_ARG;
+    if (row_bytes <= 0 || row_bytes % 16 || row_bytes / 16 > 0x7fffffffLL) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(x_sorted) || !aligned4(topk_ids) || !aligned4(group_sizes) || !aligned4(order) ||
+        !aligned4(inv) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return RDOT_ERR_INVALID_ARG;
+    const int sms = current_sm_count();
+    if (sms <= 0) return cuda_fail(cudaGetLastError(), "cudaDeviceGetAttribute");
+    cudaError_t e = launch_moe_permute(topk_ids, tokens, topk, n_experts, x, row_bytes, group_sizes, order, inv,
+                                       x_sorted, workspace, sms, s);
+    return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "moe permute launch");
+}
+
+rdot_status rdot_moe_unpermute(const void* y_sorted, const int32_t* inv, const float* topk_weights, int64_t tokens,
+                               int32_t topk, int64_t n, void* out, void* stream) {
+    if (tokens < 0 || topk < 1 || n < 1) return RDOT_ERR_INVALID_ARG;
+    if (n % 8 || tokens * static_cast<int64_t>(topk) > 0x7fffffffLL) return RDOT_ERR_UNSUPPORTED;
+    if (tokens == 0) return RDOT_OK;
+    if (!y_sorted || !inv || !topk_weights || !out) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(y_sorted) || !aligned16(out) || !aligned4(inv) || !aligned4(topk_weights)) return RDOT_ERR_INVALID_ARG;
+    const int sms = current_sm_count();
+    if (sms <= 0) return cuda_fail(cudaGetLastError(), "cudaDeviceGetAttribute");
+    cudaError_t e = launch_moe_combine(y_sorted, inv, topk_weights, tokens, topk, n, out, sms,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "moe un-permute launch");
+}
+
 const char* rdot_status_string(rdot_status status) {
     switch (status) {
         case RDOT_OK: return "RDOT_OK";

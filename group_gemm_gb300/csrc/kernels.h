@@ -130,6 +130,15 @@ cudaError_t launch_mxfp8_pair(const CUtensorMap& tmap_a, const CUtensorMap& tmap
                               cudaStream_t stream);
 int mxfp8_pair_max_clusters(int G);
 
+// MoE permute / un-permute around the ragged dot (route.cu). The permute needs
+// moe_route_workspace_bytes(T*k, E) bytes of 256-byte-aligned workspace; E <= 1024, T*k < 2^31.
+size_t moe_route_workspace_bytes(long long total, int E);
+cudaError_t launch_moe_permute(const int32_t* ids, long long tokens, int k, int E, const void* x, long long row_bytes,
+                               int32_t* group_sizes, int32_t* order, int32_t* inv, void* x_sorted, void* workspace,
+                               int sm_count, cudaStream_t stream);
+cudaError_t launch_moe_combine(const void* y_sorted, const int32_t* inv, const float* weights, long long tokens, int k,
+                               long long n, void* out, int sm_count, cudaStream_t stream);
+
 // Padded-dense baseline data movement (padded.cu).
 cudaError_t launch_pad_scatter(const void* lhs, const int32_t* gs, void* lhs_pad, int32_t* uniform_gs, int M, int G,
                                int C, long long row_bytes, int grid, int32_t* status, cudaStream_t stream);

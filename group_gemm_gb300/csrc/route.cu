@@ -1,0 +1,225 @@
+// route.cu -- the MoE pre- and post-processing around the ragged dot on the device.
+//
+// What it computes ("Group-GEMM in XLA", Part 4 "The Three MoE Compute Paths in MaxText", Path 1
+// (sparse / ragged-dot); Part 5 "Next steps"): the permute sorts the T*k token copies by
+// destination expert -- a stable sort of the flattened top-k indices, so copies of one expert keep
+// their flat order t*k + j -- bincounts group_sizes and gathers each copy's token row into that
+// order; the un-permute sums each token's k expert outputs, weighted by the router. Copies whose
+// expert id lies outside [0, E) are dropped (no sorted row, inv = -1, no contribution).
+//
+// The sort is a counting sort in three passes over chunks of 1024 copies (one warp per chunk):
+//   moe_count_kernel  per-chunk histogram of the expert ids (shared-memory counters)
+//   moe_scan_kernel   per-expert exclusive scan over the chunks (chunk bases), totals ->
+//                     group_sizes, exclusive scan over the experts (expert bases)
+//   moe_place_kernel  each chunk again, 32 copies at a time: __match_any_sync groups the lanes of
+//                     one expert, a lane's rank is the number of lower lanes in its group, and
+//                     the group's last lane advances the expert's running position -- the order
+//                     of equal keys is the flat order, as the stable sort defines it.
+// The gather and the combine are HBM-bound row copies: one warp per row, 16-byte vectors.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace rdot {
+
+namespace {
+
+constexpr int CHUNK = 1024;   // copies per counting-sort chunk (one warp)
+
+__global__ void __launch_bounds__(32) moe_count_kernel(const int32_t* __restrict__ ids, long long total, int E,
+                                                       int32_t* __restrict__ chunk_hist) {
+    extern __shared__ int32_t cnt[];
+    const int lane = threadIdx.x;
+    for (int e = lane; e < E; e += 32) cnt[e] = 0;
+    __syncwarp();
+    const long long base = static_cast<long long>(blockIdx.x) * CHUNK;
+    for (int i = lane; i < CHUNK; i += 32) {
+        const long long f = base + i;
+        if (f < total) {
+            const int e = __ldg(ids + f);
+            if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        }
+    }
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) chunk_hist[static_cast<long long>(blockIdx.x) * E + e] = cnt[e];
+}
+
+__global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E,
+                                                        int32_t* __restrict__ group_sizes,
+                                                        int32_t* __restrict__ expert_base, int32_t* __restrict__ valid) {
+    __shared__ int32_t tot[1024];
+    __shared__ int32_t warp_sum[32];
+    const int e = threadIdx.x;
+    int32_t run = 0;
+    if (e < E) {
+        // coalesced across the experts for each chunk; eight chunks' loads in flight at a time
+        for (int c0 = 0; c0 < nchunks; c0 += 8) {
+            int32_t v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = c0 + j < nchunks ? chunk_hist[static_cast<long long>(c0 + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (c0 + j < nchunks) chunk_hist[static_cast<long long>(c0 + j) * E + e] = run;
+                run += v[j];
+            }
+        }
+        group_sizes[e] = run;
+    }
+    tot[e] = e < E ? run : 0;
+    __syncthreads();
+    // exclusive scan of the totals over the experts (warp scans, then over the warps)
+    const int lane = e & 31, w = e >> 5;
+    int32_t x = tot[e];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) warp_sum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int32_t s = warp_sum[lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, s, d);
+            if (lane >= d) s += y;
+        }
+        warp_sum[lane] = s;   // inclusive over the warps
+    }
+    __syncthreads();
+    const int32_t incl = x + (w > 0 ? warp_sum[w - 1] : 0);
+    if (e < E) expert_base[e] = incl - tot[e];
+    if (e == 1023) *valid = incl;
+}
+
+__global__ void __launch_bounds__(32) moe_place_kernel(const int32_t* __restrict__ ids, long long total, int E,
+                                                       const int32_t* __restrict__ chunk_base,
+                                                       const int32_t* __restrict__ expert_base,
+                                                       int32_t* __restrict__ order, int32_t* __restrict__ inv) {
+    extern __shared__ int32_t pos[];
+    const int lane = threadIdx.x;
+    for (int e = lane; e < E; e += 32)
+        pos[e] = expert_base[e] + chunk_base[static_cast<long long>(blockIdx.x) * E + e];
+    __syncwarp();
+    const long long base = static_cast<long long>(blockIdx.x) * CHUNK;
+    const uint32_t lower = (1u << lane) - 1u;
+    for (int i = 0; i < CHUNK; i += 32) {
+        const long long f = base + i + lane;
+        const bool in = f < total;
+        int e = in ? __ldg(ids + f) : -1;
+        const bool valid = in && e >= 0 && e < E;
+        if (!valid) e = -1 - (in ? 0 : 1);   // -1: dropped copy, -2: past the end (both unmatched to experts)
+        const uint32_t same = __match_any_sync(0xffffffffu, e);
+        if (valid) {
+            const int32_t p = pos[e] + __popc(same & lower);
+            order[p] = static_cast<int32_t>(f);
+            inv[f] = p;
+        } else if (in) {
+            inv[f] = -1;
+        }
+        __syncwarp();
+        // the group's last lane moves the expert's running position past this step's copies
+        if (valid && (same >> lane) == 1u) pos[e] += __popc(same);
+        __syncwarp();
+    }
+}
+
+// x_sorted[p] = x[order[p] / k] for p < valid; past it the row is zero and order[p] = -1.
+// One warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict__ x, int32_t* __restrict__ order,
+                                                         const int32_t* __restrict__ valid, long long rows, int k,
+                                                         int vec_per_row, uint4* __restrict__ x_sorted) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    const int32_t v = *valid;
+    for (long long p = warp; p < rows; p += nwarps) {
+        uint4* dst = x_sorted + p * vec_per_row;
+        if (p < v) {
+            const uint4* src = x + static_cast<long long>(order[p] / k) * vec_per_row;
+            for (int i = lane; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
+        } else {
+            for (int i = lane; i < vec_per_row; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+            if (lane == 0) order[p] = -1;
+        }
+    }
+}
+
+__device__ __forceinline__ void acc_bf16x8(float (&a)[8], uint4 u, float w) {
+    const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        a[2 * i] += w * __uint_as_float(q[i] << 16);
+        a[2 * i + 1] += w * __uint_as_float(q[i] & 0xffff0000u);
+    }
+}
+
+// out[t] = sum_j w[t, j] * y[inv[t*k + j]] in fp32, stored as bf16 (round to nearest even).
+__global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ inv,
+                                                          const float* __restrict__ w, long long tokens, int k,
+                                                          int vec_per_row, uint4* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    for (long long t = warp; t < tokens; t += nwarps) {
+        for (int i = lane; i < vec_per_row; i += 32) {
+            float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < k; ++j) {
+                const int32_t p = __ldg(inv + t * k + j);
+                if (p < 0) continue;
+                acc_bf16x8(a, __ldg(y + static_cast<long long>(p) * vec_per_row + i), __ldg(w + t * k + j));
+            }
+            uint4 o;
+            o.x = pack_bf16x2(a[0], a[1]);
+            o.y = pack_bf16x2(a[2], a[3]);
+            o.z = pack_bf16x2(a[4], a[5]);
+            o.w = pack_bf16x2(a[6], a[7]);
+            out[t * vec_per_row + i] = o;
+        }
+    }
+}
+
+}  // namespace
+
+size_t moe_route_workspace_bytes(long long total, int E) {
+    const long long nchunks = (total + CHUNK - 1) / CHUNK;
+    const size_t hist = static_cast<size_t>(nchunks) * static_cast<size_t>(E) * sizeof(int32_t);
+    return ((hist + 255) / 256) * 256 + 256 + ((static_cast<size_t>(E) * sizeof(int32_t) + 255) / 256) * 256;
+}
+
+cudaError_t launch_moe_permute(const int32_t* ids, long long tokens, int k, int E, const void* x, long long row_bytes,
+                               int32_t* group_sizes, int32_t* order, int32_t* inv, void* x_sorted, void* workspace,
+                               int sm_count, cudaStream_t stream) {
+    const long long total = tokens * k;
+    const long long nchunks = (total + CHUNK - 1) / CHUNK;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t hist_bytes = ((static_cast<size_t>(nchunks) * E * sizeof(int32_t) + 255) / 256) * 256;
+    int32_t* chunk_hist = reinterpret_cast<int32_t*>(ws);
+    int32_t* valid = reinterpret_cast<int32_t*>(ws + hist_bytes);
+    int32_t* expert_base = reinterpret_cast<int32_t*>(ws + hist_bytes + 256);
+    const size_t cnt_shm = sizeof(int32_t) * E;
+    moe_count_kernel<<<static_cast<unsigned>(nchunks), 32, cnt_shm, stream>>>(ids, total, E, chunk_hist);
+    moe_scan_kernel<<<1, 1024, 0, stream>>>(chunk_hist, static_cast<int>(nchunks), E, group_sizes, expert_base, valid);
+    moe_place_kernel<<<static_cast<unsigned>(nchunks), 32, cnt_shm, stream>>>(ids, total, E, chunk_hist, expert_base,
+                                                                             order, inv);
+    const int vec = static_cast<int>(row_bytes / 16);
+    const long long want = (total + 7) / 8;
+    const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
+    moe_gather_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), order, valid, total, k, vec,
+                                                static_cast<uint4*>(x_sorted));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_moe_combine(const void* y_sorted, const int32_t* inv, const float* weights, long long tokens, int k,
+                               long long n, void* out, int sm_count, cudaStream_t stream) {
+    const int vec = static_cast<int>(n / 8);
+    const long long want = (tokens + 7) / 8;
+    const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
+    moe_combine_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(y_sorted), inv, weights, tokens, k, vec,
+                                                 static_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace rdot

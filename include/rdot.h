@@ -168,6 +168,39 @@ RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const v
 RDOT_API rdot_status rdot_grad_input(rdot_plan_t plan, const void* dy, const void* rhs,
                             const int32_t* group_sizes, void* dlhs, void* workspace, void* stream);
 
+/* MoE pre- and post-processing around the ragged dot ("Group-GEMM in XLA", Part 4 "The Three MoE
+ * Compute Paths in MaxText", Path 1 (sparse / ragged-dot), and Part 5 "Next steps": permute before
+ * the Group-GEMM, un-permute after it). They run on the calling thread's current device and never
+ * synchronise the host.
+ *
+ * rdot_moe_permute sorts the T*k token copies by destination expert -- a stable sort of the
+ * flattened top-k indices (copies of one expert keep their flat order t*k + j) -- and gathers
+ * each copy's token row into that order:
+ *   topk_ids     device int32 [T, k]: each token's k destination experts; an id outside
+ *                [0, n_experts) drops that copy (no sorted row, no contribution)
+ *   x            device [T, row_bytes]: the token rows (any element type; row_bytes % 16 == 0)
+ *   group_sizes  device int32 [n_experts] out: copies per expert (the bincount)
+ *   order        device int32 [T*k] out: flat index of each sorted row; -1 past sum(group_sizes)
+ *   inv          device int32 [T*k] out: sorted row of each copy t*k + j, or -1 if dropped
+ *   x_sorted     device [T*k, row_bytes] out: x_sorted[p] = x[order[p] / k]; zero rows past
+ *                sum(group_sizes) -- the lhs of rdot_forward with these group_sizes
+ *   workspace    device, rdot_moe_route_workspace_size bytes, 256-byte aligned, no initial state
+ * n_experts <= RDOT_MAX_GROUPS, T*k < 2^31. 16-byte alignment for x and x_sorted, 4 for the rest. */
+RDOT_API rdot_status rdot_moe_route_workspace_size(int64_t tokens, int32_t topk, int32_t n_experts, size_t* bytes);
+RDOT_API rdot_status rdot_moe_permute(const int32_t* topk_ids, int64_t tokens, int32_t topk, int32_t n_experts,
+                             const void* x, int64_t row_bytes, int32_t* group_sizes, int32_t* order,
+                             int32_t* inv, void* x_sorted, void* workspace, void* stream);
+
+/* rdot_moe_unpermute combines each token's k expert outputs, weighted by the router:
+ *   out[t, :] = sum_j topk_weights[t, j] * y_sorted[inv[t*k + j], :] over the copies kept,
+ * accumulated in fp32 and stored as bf16 (round to nearest even).
+ *   y_sorted      device bf16 [T*k, n] (rows in rdot_moe_permute's order)
+ *   inv           device int32 [T*k] (from rdot_moe_permute)
+ *   topk_weights  device fp32 [T, k]
+ *   out           device bf16 [T, n]; n % 8 == 0; 16-byte alignment for y_sorted and out. */
+RDOT_API rdot_status rdot_moe_unpermute(const void* y_sorted, const int32_t* inv, const float* topk_weights,
+                               int64_t tokens, int32_t topk, int64_t n, void* out, void* stream);
+
 /* Bytes of the padded baseline's scratch for a capacity of `capacity` rows per group
  * (the padded lhs [G, capacity, K] plus the padded output [G, capacity, N] plus a small table). */
 RDOT_API rdot_status rdot_padded_workspace_size(rdot_plan_t plan, int64_t capacity, size_t* bytes);

@@ -73,3 +73,15 @@ def test_null_arguments_are_rejected(lib):
     assert lib.rdot_forward(None, None, None, None, None, None, None) == gg.RDOT_ERR_INVALID_ARG
     assert lib.rdot_workspace_size(None, None) == gg.RDOT_ERR_INVALID_ARG
     assert lib.rdot_plan_destroy(None) == gg.RDOT_OK
+
+
+def test_moe_route_argument_checks_without_gpu(lib):
+    n = ctypes.c_size_t()
+    assert lib.rdot_moe_route_workspace_size(100, 0, 8, ctypes.byref(n)) == gg.RDOT_ERR_INVALID_ARG
+    assert lib.rdot_moe_route_workspace_size(100, 2, gg.RDOT_MAX_GROUPS + 1, ctypes.byref(n)) == gg.RDOT_ERR_INVALID_ARG
+    assert lib.rdot_moe_route_workspace_size(2 ** 31, 2, 8, ctypes.byref(n)) == gg.RDOT_ERR_UNSUPPORTED
+    assert lib.rdot_moe_route_workspace_size(8192, 2, 8, ctypes.byref(n)) == gg.RDOT_OK and n.value >= 256
+    gs = ctypes.c_void_p(16)   # never dereferenced: the checks fail first
+    assert lib.rdot_moe_permute(gs, 10, 2, 8, gs, 24, gs, gs, gs, gs, gs, None) == gg.RDOT_ERR_INVALID_ARG   # row_bytes % 16
+    assert lib.rdot_moe_unpermute(gs, gs, gs, 10, 2, 12, gs, None) == gg.RDOT_ERR_UNSUPPORTED                 # n % 8
+    assert lib.rdot_moe_unpermute(gs, gs, gs, -1, 2, 16, gs, None) == gg.RDOT_ERR_INVALID_ARG

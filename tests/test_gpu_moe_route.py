@@ -1,0 +1,125 @@
+"""GPU parity of the MoE permute / un-permute (the sparse path's pre- and post-processing around
+the ragged dot) through the C ABI against the oracle: the sort, the sizes and the gathered rows
+bit for bit; the weighted combine within the bf16 tolerance; and a whole MoE expert layer
+(permute -> ragged dot -> un-permute) against the dense definition."""
+import numpy as np
+import pytest
+import torch
+
+import group_gemm_gb300 as gg
+import oracle
+import rdot_inputs as ri
+from tests._metrics import COSINE_MIN, cosine_to_rounded
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gg.build()
+    gg.load()
+
+
+def rel_err(got, ref):
+    got = got.detach().to("cpu", torch.float64).numpy() if isinstance(got, torch.Tensor) else got
+    return float(np.max(np.abs(got - ref) / (np.abs(ref) + 1.0))) if ref.size else 0.0
+
+
+def routed_ids(t, k, e, seed, drop=0.0):
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((t, e)) + np.linspace(0, 2, e)       # skewed expert popularity
+    ids = np.argsort(-logits, axis=1)[:, :k].astype(np.int32)
+    if drop:
+        mask = rng.random((t, k)) < drop
+        ids[mask] = np.where(rng.random(mask.sum()) < 0.5, -1, e)        # outside [0, E): dropped
+    return ids
+
+
+@pytest.mark.parametrize("t,k,e,width,drop", [
+    (1000, 2, 8, 64, 0.0),
+    (3, 2, 3, 16, 0.0),
+    (5000, 8, 256, 128, 0.05),      # DeepSeek-like top-8 of 256, some copies dropped
+    (777, 1, 1, 32, 0.0),           # one expert
+    (2049, 4, 1024, 64, 0.1),       # the largest expert count, chunk boundary + 1
+])
+def test_permute_matches_oracle_bit_for_bit(t, k, e, width, drop):
+    ids = routed_ids(t, k, e, 61 + t, drop)
+    x = torch.from_numpy(ri.host_normal((t, width), 62)).to(torch.bfloat16)
+    xs, gs, order, inv = gg.moe_permute(torch.from_numpy(ids).to(DEV), x.to(DEV), e)
+    torch.cuda.synchronize()
+    gs_ref, order_ref, inv_ref, _ = oracle.moe_permute(ids, x.double().numpy(), e)
+    v = order_ref.size
+    assert np.array_equal(gs.cpu().numpy(), gs_ref)
+    assert np.array_equal(order.cpu().numpy()[:v].astype(np.int64), order_ref)
+    assert np.all(order.cpu().numpy()[v:] == -1)
+    assert np.array_equal(inv.cpu().numpy().astype(np.int64), inv_ref)
+    xs_h = xs.cpu()
+    assert torch.equal(xs_h[:v], x[torch.from_numpy(order_ref // k)])           # exact bytes
+    assert torch.all(xs_h[v:] == 0)
+
+
+@pytest.mark.parametrize("t,k,n", [(1000, 2, 64), (513, 8, 256), (7, 3, 8)])
+def test_unpermute_matches_oracle(t, k, n):
+    rng = np.random.default_rng(63)
+    ids = routed_ids(t, k, 16, 64, 0.05)
+    _, _, inv_ref, _ = oracle.moe_permute(ids, np.zeros((t, 8)), 16)
+    y = torch.from_numpy(ri.host_normal((t * k, n), 65)).to(torch.bfloat16)
+    w = torch.from_numpy(rng.random((t, k)).astype(np.float32))
+    out = gg.moe_unpermute(y.to(DEV), torch.from_numpy(inv_ref.astype(np.int32)).to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.moe_unpermute(y.double().numpy(), inv_ref, w.double().numpy())
+    assert rel_err(out, ref) <= TOL
+    assert cosine_to_rounded(out, ref) >= COSINE_MIN
+
+
+def test_moe_expert_layer_end_to_end():
+    """permute -> ragged dot (the library's forward) -> un-permute equals the dense definition
+    out[t] = sum_j w[t, j] * x[t] @ W[e_tj] over the kept copies."""
+    t, k, e, kk, n = 700, 2, 8, 128, 256
+    ids = routed_ids(t, k, e, 66, 0.02)
+    rng = np.random.default_rng(67)
+    w_route = rng.random((t, k)).astype(np.float32)
+    x = torch.from_numpy(ri.host_normal((t, kk), 68)).to(torch.bfloat16)
+    wts = torch.from_numpy(ri.host_normal((e, kk, n), 69, 0.05)).to(torch.bfloat16)
+    xs, gs, order, inv = gg.moe_permute(torch.from_numpy(ids).to(DEV), x.to(DEV), e)
+    ys = gg.ragged_dot(xs, wts.to(DEV), gs)
+    out = gg.moe_unpermute(ys, inv, torch.from_numpy(w_route).to(DEV))
+    torch.cuda.synchronize()
+    xd, wd = x.double().numpy(), wts.double().numpy()
+    ref = np.zeros((t, n))
+    for tt in range(t):
+        for j in range(k):
+            if 0 <= ids[tt, j] < e:
+                ref[tt] += w_route[tt, j] * (xd[tt] @ wd[ids[tt, j]])
+    assert rel_err(out, ref) <= TOL
+
+
+def test_mixtral_like_routing_full_size():
+    """8192 tokens, top-2 of 8, width 4096: the sorted order and the gathered rows exactly."""
+    t, k, e, width = 8192, 2, 8, 4096
+    ids = routed_ids(t, k, e, 70)
+    x = ri.device_normal((t, width), 71, 1.0, DEV, torch.bfloat16)
+    xs, gs, order, inv = gg.moe_permute(torch.from_numpy(ids).to(DEV), x, e)
+    gs_ref, order_ref, inv_ref, _ = oracle.moe_permute(ids, np.zeros((t, 1)), e)
+    assert np.array_equal(gs.cpu().numpy(), gs_ref)
+    assert np.array_equal(order.cpu().numpy().astype(np.int64), order_ref)
+    assert np.array_equal(inv.cpu().numpy().astype(np.int64), inv_ref)
+    assert torch.equal(xs, x[torch.from_numpy(order_ref // k).to(DEV)])
+
+
+def test_no_tokens_and_all_dropped():
+    gs = torch.full((4,), 7, dtype=torch.int32, device=DEV)
+    st = gg.load().rdot_moe_permute(None, 0, 2, 4, None, 16, gs.data_ptr(), None, None, None, None, None)
+    torch.cuda.synchronize()
+    assert st == gg.RDOT_OK and torch.all(gs == 0)
+    ids = np.full((5, 2), -1, np.int32)
+    x = torch.ones((5, 8), dtype=torch.bfloat16, device=DEV)
+    xs, gs, order, inv = gg.moe_permute(torch.from_numpy(ids).to(DEV), x, 4)
+    torch.cuda.synchronize()
+    assert torch.all(gs == 0) and torch.all(order == -1) and torch.all(inv == -1) and torch.all(xs == 0)
+    out = gg.moe_unpermute(torch.ones((10, 8), dtype=torch.bfloat16, device=DEV), inv,
+                           torch.ones((5, 2), device=DEV))
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
