@@ -480,6 +480,30 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                          "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}"}
     del dy, rhs, dlhs
     torch.cuda.empty_cache()
+    # MoE permute / un-permute around the Mixtral-like layer: 8192 tokens, top-2 of 8, width 4096
+    t, k, e, width = m // 2, 2, g, cfg["k"]
+    rng = np.random.default_rng(0)
+    logits = rng.standard_normal((t, e))
+    ids = torch.from_numpy(np.argsort(-logits, axis=1)[:, :k].astype(np.int32)).to(dev)
+    x = ri.device_normal((t, width), 4000, 1.0, dev, torch.bfloat16)
+    xs = torch.empty((t * k, width), dtype=torch.bfloat16, device=dev)
+    gsz = torch.empty(e, dtype=torch.int32, device=dev)
+    order = torch.empty(t * k, dtype=torch.int32, device=dev)
+    inv = torch.empty(t * k, dtype=torch.int32, device=dev)
+    ws = torch.empty(gg.rdot_moe_route_workspace_size(t, k, e), dtype=torch.uint8, device=dev)
+    tp = _time_steps(lambda: gg.rdot_moe_permute(ids, x, e, gsz, order, inv, xs, ws, stream), steps, stream)
+    wr = torch.rand((t, k), device=dev)
+    outc = torch.empty((t, width), dtype=torch.bfloat16, device=dev)
+    tc = _time_steps(lambda: gg.rdot_moe_unpermute(xs, inv, wr, outc, stream), steps, stream)
+    perm_bytes = t * width * 2 + t * k * width * 2 + t * k * 4 * 3 + e * 4      # x once, x_sorted, ids/order/inv
+    comb_bytes = t * k * width * 2 + t * width * 2 + t * k * 8                  # y_sorted, out, inv + weights
+    res["moe_route"] = {"workload": f"{t} tokens, top-{k} of {e} experts, rows of {width} bf16",
+                        "permute_ms": round(tp * 1e3, 4), "permute_gbs_algorithmic": round(perm_bytes / tp / 1e9, 1),
+                        "permute_frac_of_hbm": round(perm_bytes / tp / 1e9 / peaks["hbm_gbs"], 4),
+                        "unpermute_ms": round(tc * 1e3, 4), "unpermute_gbs_algorithmic": round(comb_bytes / tc / 1e9, 1),
+                        "unpermute_frac_of_hbm": round(comb_bytes / tc / 1e9 / peaks["hbm_gbs"], 4)}
+    del x, xs, outc, ws
+    torch.cuda.empty_cache()
     # weight gradient
     cfg = ri.CONFIGS["wgrad_bf16"]
     m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]

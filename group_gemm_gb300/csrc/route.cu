@@ -7,7 +7,7 @@
 // order; the un-permute sums each token's k expert outputs, weighted by the router. Copies whose
 // expert id lies outside [0, E) are dropped (no sorted row, inv = -1, no contribution).
 //
-// The sort is a counting sort in three passes over chunks of 1024 copies (one warp per chunk):
+// The sort is a counting sort in three passes over chunks of 512 copies (one warp per chunk):
 //   moe_count_kernel  per-chunk histogram of the expert ids (shared-memory counters)
 //   moe_scan_kernel   per-expert exclusive scan over the chunks (chunk bases), totals ->
 //                     group_sizes, exclusive scan over the experts (expert bases)
@@ -25,7 +25,7 @@ namespace rdot {
 
 namespace {
 
-constexpr int CHUNK = 1024;   // copies per counting-sort chunk (one warp)
+constexpr int CHUNK = 512;   // copies per counting-sort chunk (one warp)
 
 __global__ void __launch_bounds__(32) moe_count_kernel(const int32_t* __restrict__ ids, long long total, int E,
                                                        int32_t* __restrict__ chunk_hist) {
@@ -34,13 +34,15 @@ __global__ void __launch_bounds__(32) moe_count_kernel(const int32_t* __restrict
     for (int e = lane; e < E; e += 32) cnt[e] = 0;
     __syncwarp();
     const long long base = static_cast<long long>(blockIdx.x) * CHUNK;
-    for (int i = lane; i < CHUNK; i += 32) {
-        const long long f = base + i;
-        if (f < total) {
-            const int e = __ldg(ids + f);
-            if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-        }
+    int id[CHUNK / 32];   // all loads of the chunk in flight before any counting
+#pragma unroll
+    for (int i = 0; i < CHUNK / 32; ++i) {
+        const long long f = base + i * 32 + lane;
+        id[i] = f < total ? __ldg(ids + f) : -1;
     }
+#pragma unroll
+    for (int i = 0; i < CHUNK / 32; ++i)
+        if (id[i] >= 0 && id[i] < E) atomicAdd(&cnt[id[i]], 1);
     __syncwarp();
     for (int e = lane; e < E; e += 32) chunk_hist[static_cast<long long>(blockIdx.x) * E + e] = cnt[e];
 }
@@ -105,10 +107,17 @@ __global__ void __launch_bounds__(32) moe_place_kernel(const int32_t* __restrict
     __syncwarp();
     const long long base = static_cast<long long>(blockIdx.x) * CHUNK;
     const uint32_t lower = (1u << lane) - 1u;
-    for (int i = 0; i < CHUNK; i += 32) {
-        const long long f = base + i + lane;
+    int id[CHUNK / 32];   // all loads of the chunk in flight before the ordered placement
+#pragma unroll
+    for (int i = 0; i < CHUNK / 32; ++i) {
+        const long long f = base + i * 32 + lane;
+        id[i] = f < total ? __ldg(ids + f) : -1;
+    }
+#pragma unroll
+    for (int i = 0; i < CHUNK / 32; ++i) {
+        const long long f = base + i * 32 + lane;
         const bool in = f < total;
-        int e = in ? __ldg(ids + f) : -1;
+        int e = id[i];
         const bool valid = in && e >= 0 && e < E;
         if (!valid) e = -1 - (in ? 0 : 1);   // -1: dropped copy, -2: past the end (both unmatched to experts)
         const uint32_t same = __match_any_sync(0xffffffffu, e);
@@ -139,6 +148,7 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict
         uint4* dst = x_sorted + p * vec_per_row;
         if (p < v) {
             const uint4* src = x + static_cast<long long>(order[p] / k) * vec_per_row;
+#pragma unroll 4
             for (int i = lane; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
         } else {
             for (int i = lane; i < vec_per_row; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
@@ -164,6 +174,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restric
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     for (long long t = warp; t < tokens; t += nwarps) {
+#pragma unroll 4
         for (int i = lane; i < vec_per_row; i += 32) {
             float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             for (int j = 0; j < k; ++j) {
