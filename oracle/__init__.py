@@ -15,6 +15,9 @@ Functions and the passages they follow (page titles and sections):
   -> [M,K], contracting rhs's dimension 2).
 * :func:`forward_mxfp8_rows` -- AITER PR #5658 (E4M3 + E8M0 per 32 K elements).
 * :func:`tile_map` -- the library's scheduler order (not on the pages), by brute force.
+* :func:`gated_forward` -- "Group-GEMM in XLA", Part 4 "The Three MoE Compute Paths in MaxText":
+  the up projection's two ragged dots feed ``activation(layer_w0) * layer_w1``; the activation is
+  read as SiLU, z * sigmoid(z), the gated unit of the evaluated MoE models.
 * :func:`moe_permute` / :func:`moe_unpermute` -- "Group-GEMM in XLA", Part 4 "The Three MoE
   Compute Paths in MaxText", Path 1 (sparse / ragged-dot): the pre-processing sorts the token
   copies by destination expert (a stable argsort of the flattened top-k indices), gathers the
@@ -334,3 +337,13 @@ def moe_unpermute(y_sorted, inv, topk_weights):
             if inv[tt, j] >= 0:
                 out[tt] += w[tt, j] * y[inv[tt, j]]
     return out
+
+
+def gated_forward(lhs, w0, w1, group_sizes):
+    """``silu(lhs @ w0[g]) * (lhs @ w1[g])`` per row of group g (zeros past the sum), float64;
+    silu(z) = z / (1 + exp(-z)). Both ragged dots are the oracle's forward."""
+    a = forward(lhs, w0, group_sizes)
+    b = forward(lhs, w1, group_sizes)
+    with np.errstate(over="ignore"):
+        silu = a / (1.0 + np.exp(-a))
+    return silu * b

@@ -276,6 +276,29 @@ def test_grad_input_rows_subset_and_transposed_forward():
     assert _rel(full, oracle.forward(dy, np.ascontiguousarray(w.transpose(0, 2, 1)), gs)) < TOL
 
 
+# ------------------------------------------------------------------------- gated up projection
+def test_gated_forward_brute_force_and_silu_identity():
+    """activation(x w0) * (x w1) with SiLU: numpy per group; and the closed form
+    silu(z) - silu(-z) = z, so out(w0) - out(-w0) = (x w0) * (x w1) exactly up to rounding."""
+    rng = np.random.default_rng(41)
+    gs = np.array([4, 0, 5, 2], np.int32)
+    m, k, f = int(gs.sum()) + 2, 6, 5
+    x = rng.standard_normal((m, k))
+    w0 = rng.standard_normal((gs.size, k, f))
+    w1 = rng.standard_normal((gs.size, k, f))
+    got = oracle.gated_forward(x, w0, w1, gs)
+    ref = np.zeros((m, f))
+    start = 0
+    for g, sz in enumerate(gs):
+        z = x[start:start + sz] @ w0[g]
+        ref[start:start + sz] = z / (1.0 + np.exp(-z)) * (x[start:start + sz] @ w1[g])
+        start += sz
+    assert _rel(got, ref) < TOL and np.all(got[start:] == 0.0)
+    diff = got - oracle.gated_forward(x, -w0, w1, gs)
+    assert _rel(diff, _np_forward(x, w0, gs) * _np_forward(x, w1, gs)) < 1e-12
+    assert np.all(oracle.gated_forward(x, np.zeros_like(w0), w1, gs) == 0.0)     # silu(0) = 0
+
+
 # --------------------------------------------------------------------- MoE permute / combine
 def test_moe_route_worked_example():
     d = _golden.read("moe_route_example.txt")
