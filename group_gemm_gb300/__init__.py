@@ -23,7 +23,8 @@ __all__ = [
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_grad_input", "rdot_moe_route_workspace_size", "rdot_moe_permute",
-    "rdot_moe_unpermute", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight", "grad_input",
+    "rdot_moe_unpermute", "rdot_forward_gated", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
+    "grad_input", "ragged_dot_gated",
     "ragged_dot_mxfp8", "padded_ragged_dot", "EXPORTED_SYMBOLS",
 ]
 
@@ -31,6 +32,7 @@ RDOT_OK, RDOT_ERR_INVALID_ARG, RDOT_ERR_UNSUPPORTED, RDOT_ERR_CUDA = 0, 1, 2, 3
 RDOT_ERR_DEVICE_TIMEOUT, RDOT_WARN_GROUP_SIZES = 4, 5
 RDOT_F32, RDOT_BF16, RDOT_E4M3 = 0, 1, 2
 RDOT_MODE_FORWARD, RDOT_MODE_GRAD_WEIGHT, RDOT_MODE_FORWARD_MXFP8, RDOT_MODE_GRAD_INPUT = 0, 1, 2, 3
+RDOT_MODE_FORWARD_GATED = 4
 RDOT_STATUS_BIT_GROUP_SIZES, RDOT_STATUS_BIT_TIMEOUT = 0x1, 0x2
 RDOT_FLAG_ROW_TILES_INNER, RDOT_FLAG_COL_TILES_INNER = 0x1, 0x2
 RDOT_FLAG_CTA_PAIR, RDOT_FLAG_NO_CTA_PAIR, RDOT_FLAG_NATURAL_ORDER = 0x4, 0x8, 0x10
@@ -43,12 +45,13 @@ EXPORTED_SYMBOLS = (
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_grad_input", "rdot_moe_route_workspace_size", "rdot_moe_permute",
-    "rdot_moe_unpermute",
+    "rdot_moe_unpermute", "rdot_forward_gated",
 )
 
 _DTYPE_CODES = {"f32": RDOT_F32, "bf16": RDOT_BF16, "e4m3": RDOT_E4M3}
 _MODE_CODES = {"forward": RDOT_MODE_FORWARD, "grad_weight": RDOT_MODE_GRAD_WEIGHT,
-               "forward_mxfp8": RDOT_MODE_FORWARD_MXFP8, "grad_input": RDOT_MODE_GRAD_INPUT}
+               "forward_mxfp8": RDOT_MODE_FORWARD_MXFP8, "grad_input": RDOT_MODE_GRAD_INPUT,
+               "forward_gated": RDOT_MODE_FORWARD_GATED}
 
 
 class RdotError(RuntimeError):
@@ -94,6 +97,7 @@ def load():
             "rdot_forward_mxfp8": ([vp, vp, vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_grad_weight": ([vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_grad_input": ([vp, vp, vp, vp, vp, vp, vp], st),
+            "rdot_forward_gated": ([vp, vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_moe_route_workspace_size": ([i64, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
                                               st),
             "rdot_moe_permute": ([vp, i64, ctypes.c_int32, ctypes.c_int32, vp, i64, vp, vp, vp, vp, vp, vp], st),
@@ -171,6 +175,11 @@ def rdot_grad_weight(plan, lhs, dy, group_sizes, dw, workspace, stream=None) -> 
 def rdot_grad_input(plan, dy, rhs, group_sizes, dlhs, workspace, stream=None) -> None:
     _check(load().rdot_grad_input(plan, _ptr(dy), _ptr(rhs), _ptr(group_sizes), _ptr(dlhs), _ptr(workspace),
                                   _stream(stream, dlhs.device)), "rdot_grad_input")
+
+
+def rdot_forward_gated(plan, lhs, w0, w1, group_sizes, out, workspace, stream=None) -> None:
+    _check(load().rdot_forward_gated(plan, _ptr(lhs), _ptr(w0), _ptr(w1), _ptr(group_sizes), _ptr(out),
+                                     _ptr(workspace), _stream(stream, out.device)), "rdot_forward_gated")
 
 
 def rdot_moe_route_workspace_size(tokens: int, topk: int, n_experts: int) -> int:
@@ -358,6 +367,24 @@ def grad_input(dy, rhs, group_sizes, out_dtype=None, dlhs=None, stream=None):
     rdot_grad_input(plan.handle, dy.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(), dlhs,
                     plan.workspace, stream)
     return dlhs
+
+
+def ragged_dot_gated(lhs, w0, w1, group_sizes, out_dtype=None, out=None, stream=None):
+    """``silu(lhs @ w0[g]) * (lhs @ w1[g])`` for bf16 lhs [M, K], w0/w1 [G, K, N]: the fused gated
+    up projection of an expert layer (zeros past the sum)."""
+    import torch
+    m, k = lhs.shape
+    g, _, n = w0.shape
+    out_dtype = out_dtype or lhs.dtype
+    names = {torch.bfloat16: "bf16", torch.float32: "f32"}
+    key = ("gated", m, k, n, g, out_dtype, lhs.device)
+    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="forward_gated", in_dtype="bf16",
+                        out_dtype=names[out_dtype], device=lhs.device)
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
+    rdot_forward_gated(plan.handle, lhs.contiguous(), w0.contiguous(), w1.contiguous(),
+                       group_sizes.to(torch.int32).contiguous(), out, plan.workspace, stream)
+    return out
 
 
 def moe_permute(topk_ids, x, n_experts, stream=None):

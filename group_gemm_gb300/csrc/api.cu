@@ -81,7 +81,8 @@ struct rdot_plan_s {
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
     int kind = 0;          // 0: SIMT fp32 forward, 1: tcgen05 bf16 forward, 2: tcgen05 grad-weight, 3: MXFP8,
-                           // 4: tcgen05 data gradient (the forward kernels, K-major B)
+                           // 4: tcgen05 data gradient (the forward kernels, K-major B),
+                           // 5: gated up projection (CTA pairs)
     int tile_m = 0, tile_n = 0;
     int m_inner = 1;
     int grid = 1;
@@ -96,6 +97,9 @@ struct rdot_plan_s {
     // grad-weight output map (the epilogue's TMA stores), cached by dw pointer
     const void* map_out_ptr = nullptr;
     CUtensorMap map_out{};
+    // gated up projection: the second weight tensor's map, cached by pointer
+    const void* map_b1_ptr = nullptr;
+    CUtensorMap map_b1{};
     // MXFP8 on CTA pairs: the scale blocks in the workspace, cached by workspace pointer
     const void* map_ws_ptr = nullptr;
     CUtensorMap map_sfa{}, map_sfb{};
@@ -177,6 +181,12 @@ rdot_status check_problem(const rdot_problem* p) {
             return RDOT_ERR_UNSUPPORTED;
         case RDOT_MODE_GRAD_WEIGHT:
             if (p->in_dtype != RDOT_BF16 || p->out_dtype != RDOT_F32) return RDOT_ERR_UNSUPPORTED;
+            if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;
+            return RDOT_OK;
+        case RDOT_MODE_FORWARD_GATED:
+            if (p->in_dtype != RDOT_BF16 || p->tile_n != 0 || (p->flags & RDOT_FLAG_NO_CTA_PAIR))
+                return RDOT_ERR_UNSUPPORTED;
+            if (p->out_dtype != RDOT_F32 && p->out_dtype != RDOT_BF16) return RDOT_ERR_UNSUPPORTED;
             if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;
             return RDOT_OK;
         case RDOT_MODE_GRAD_INPUT:
@@ -270,6 +280,31 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         // small average groups: interleave the tiles of groups with 2+ row tiles with the
         // others so every wave mixes tensor-core-bound and weight-streaming work
         pl->big_mt = (!want_pair && !(p.flags & RDOT_FLAG_NATURAL_ORDER)) ? 2 : 0;
+    } else if (p.mode == RDOT_MODE_FORWARD_GATED) {
+        if (prop.major != 10) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->kind = 5;
+        // the group's weights are 2 x K x N: row tiles inner while a group's lhs slice is smaller
+        pl->m_inner = (m_avg <= 2 * p.n) ? 1 : 0;
+        if (p.flags & 1) pl->m_inner = 1;
+        if (p.flags & 2) pl->m_inner = 0;
+        const int clusters = fwd_tc2_max_clusters(p.out_dtype == RDOT_F32, p.groups);
+        if (clusters <= 0) {
+            delete pl;
+            return cuda_fail(cudaGetLastError(), "cudaOccupancyMaxActiveClusters");
+        }
+        pl->pair = true;
+        pl->tile_m = TC2_BM;
+        pl->tile_n = 128;   // output columns per tile (256 accumulator columns: w0's and w1's)
+        const int nt = static_cast<int>((p.n + 127) / 128);
+        const long long bound = forward_tile_bound(p.m, p.groups, TC2_BM, nt);
+        if (bound > 0x7fffffffLL) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(bound, clusters)));
     } else if (p.mode == RDOT_MODE_GRAD_INPUT) {
         if (prop.major != 10) {
             delete pl;
@@ -489,6 +524,54 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
     else
         e = launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "fwd_tc launch");
+    return RDOT_OK;
+}
+
+rdot_status rdot_forward_gated(rdot_plan_t plan, const void* lhs, const void* w0, const void* w1,
+                               const int32_t* group_sizes, void* out, void* workspace, void* stream) {
+    if (!plan || !group_sizes || !workspace) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.mode != RDOT_MODE_FORWARD_GATED || plan->kind != 5) return RDOT_ERR_INVALID_ARG;
+    if (p.m == 0) return RDOT_OK;
+    if (!lhs || !w0 || !w1 || !out) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(lhs) || !aligned16(w0) || !aligned16(w1) || !aligned16(out) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan->map_lhs_ptr != lhs) {
+        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs, p.k, p.m, p.k * 2, TC_BK,
+                                   TC_BM);
+        if (st != RDOT_OK) return st;
+        plan->map_lhs_ptr = lhs;
+    }
+    if (plan->map_rhs_ptr != w0) {
+        rdot_status st = encode_3d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w0, p.n, p.k, p.groups, p.n * 2,
+                                   p.k * p.n * 2, 64, TC_BK, 1);
+        if (st != RDOT_OK) return st;
+        plan->map_rhs_ptr = w0;
+    }
+    if (plan->map_b1_ptr != w1) {
+        rdot_status st = encode_3d(&plan->map_b1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w1, p.n, p.k, p.groups, p.n * 2,
+                                   p.k * p.n * 2, 64, TC_BK, 1);
+        if (st != RDOT_OK) return st;
+        plan->map_b1_ptr = w1;
+    }
+    FwdArgs a{};
+    a.group_sizes = group_sizes;
+    a.out = out;
+    a.M = static_cast<int>(p.m);
+    a.K = static_cast<int>(p.k);
+    a.N = static_cast<int>(p.n);
+    a.G = p.groups;
+    a.NT = static_cast<int>((p.n + 127) / 128);
+    a.m_inner = plan->m_inner;
+    a.gated = 1;
+    a.status = static_cast<int32_t*>(workspace);
+    a.timeout_ns = plan->timeout_ns;
+    cudaError_t e = launch_fwd_tc2(plan->map_a, plan->map_b, a, p.out_dtype == RDOT_F32, plan->grid, s, &plan->map_b1);
+    if (e != cudaSuccess) return cuda_fail(e, "gated forward launch");
     return RDOT_OK;
 }
 
@@ -881,6 +964,6 @@ const char* rdot_status_string(rdot_status status) {
 
 const char* rdot_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
-int rdot_version(void) { return 101; }
+int rdot_version(void) { return 102; }
 
 }  // extern "C"

@@ -48,7 +48,7 @@ size_t smem_bytes(int G) {
 template <bool OUT_F32>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                   FwdArgs a) {
+                   const __grid_constant__ CUtensorMap tmap_b1, FwdArgs a) {
     constexpr int EPI_BYTES = 4 * EpiStage<OUT_F32>::BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -110,14 +110,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             bool ok = true;
             for (int w = cluster; w < W && ok; w += nclusters) {
                 const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
-                const int n0 = t.nt * BN;
+                const bool gated = a.gated != 0;
+                const int n0 = t.nt * (gated ? BN / 2 : BN);
                 // bytes each CTA brings in: its A half unless it lies wholly past M, and the
                 // 64-column chunks of its B half that are not wholly past N
                 const int a0 = A_BYTES, a1 = (t.row0 + 128 < a.M) ? A_BYTES : 0;
-                // (K-major B, the data gradient: one 128-row box per CTA, or none past N)
+                // (K-major B, the data gradient: one 128-row box per CTA, or none past N; gated:
+                // both CTAs load the same 128 columns, of w0 and of w1)
                 const bool kmaj = a.b_kmajor != 0;
                 const int c0 = kmaj ? 2 : max(0, min(2, (a.N - n0 + 63) / 64));
-                const int c1 = kmaj ? (n0 + 128 < a.N ? 2 : 0) : max(0, min(2, (a.N - n0 - 128 + 63) / 64));
+                const int c1 = kmaj ? (n0 + 128 < a.N ? 2 : 0)
+                                    : gated ? c0 : max(0, min(2, (a.N - n0 - 128 + 63) / 64));
+                const CUtensorMap* map_b = (gated && rank) ? &tmap_b1 : &tmap_b;
+                const int b_col = gated ? n0 : n0 + 128 * static_cast<int>(rank);
                 const int my_a = rank ? a1 : a0;
                 const int my_c = rank ? c1 : c0;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -131,11 +136,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
                     if (my_a) tma_load_2d_pair(sa, &tmap_a, fb, kb * TC_BK, t.row0 + 128 * static_cast<int>(rank));
                     if (kmaj) {
-                        if (my_c) tma_load_3d_pair(sb, &tmap_b, fb, kb * TC_BK, n0 + 128 * static_cast<int>(rank), t.g);
+                        if (my_c) tma_load_3d_pair(sb, map_b, fb, kb * TC_BK, b_col, t.g);
                     } else {
                         for (int j = 0; j < my_c; ++j)
-                            tma_load_3d_pair(sb + j * B_CHUNK_BYTES, &tmap_b, fb,
-                                             n0 + 128 * static_cast<int>(rank) + 64 * j, kb * TC_BK, t.g);
+                            tma_load_3d_pair(sb + j * B_CHUNK_BYTES, map_b, fb, b_col + 64 * j, kb * TC_BK, t.g);
                     }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -216,7 +220,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t acc = 0, acc_phase = 0;
         for (int w = cluster; w < W; w += nclusters) {
             const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
-            const int n0 = t.nt * BN;
+            const bool gated = a.gated != 0;
+            const int n0 = t.nt * (gated ? BN / 2 : BN);
             const bool ready = mbar_wait_warp(&tfull[acc], acc_phase, guard);
             if (!ready) break;
             tc_fence_after();
@@ -225,16 +230,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const int rows_valid = t.rows - first;
             uint8_t* out_rows =
                 static_cast<uint8_t*>(a.out) + (static_cast<long long>(t.row0) + first) * a.N * (OUT_F32 ? 4 : 2);
+            if (gated) {
+                // accumulator columns [0, 128) hold lhs . w0, [128, 256) lhs . w1 for the same
+                // 128 output columns: out = silu(z0) * z1, silu(z) = z / (1 + e^-z)
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, v);
-                tmem_ld_wait();
-                const int col = n0 + c * 32;
-                if (rows_valid > 0 && col < a.N)
-                    store_block_32x32<OUT_F32>(v, stage_buf,
-                                               out_rows + static_cast<long long>(col) * (OUT_F32 ? 4 : 2), a.N,
-                                               rows_valid, a.N - col);
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t z0[32], z1[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, z0);
+                    tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, z1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float z = __uint_as_float(z0[j]);
+                        z0[j] = __float_as_uint(z / (1.0f + __expf(-z)) * __uint_as_float(z1[j]));
+                    }
+                    const int col = n0 + c * 32;
+                    if (rows_valid > 0 && col < a.N)
+                        store_block_32x32<OUT_F32>(z0, stage_buf,
+                                                   out_rows + static_cast<long long>(col) * (OUT_F32 ? 4 : 2), a.N,
+                                                   rows_valid, a.N - col);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    const int col = n0 + c * 32;
+                    if (rows_valid > 0 && col < a.N)
+                        store_block_32x32<OUT_F32>(v, stage_buf,
+                                                   out_rows + static_cast<long long>(col) * (OUT_F32 ? 4 : 2), a.N,
+                                                   rows_valid, a.N - col);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -267,23 +294,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 template <bool OUT_F32>
-cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const FwdArgs& a, int grid,
-                       cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb1, const FwdArgs& a,
+                       int grid, cudaStream_t stream) {
     const size_t shm = smem_bytes<OUT_F32>(a.G);
     auto kern = fwd_tc2_kernel<OUT_F32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, shm, stream>>>(ta, tb, a);
+    kern<<<grid, THREADS, shm, stream>>>(ta, tb, tb1, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc2(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, bool out_f32,
-                           int grid, cudaStream_t stream) {
-    if (grid % 2) return cudaErrorInvalidValue;
-    return out_f32 ? launch_one<true>(tmap_a, tmap_b, a, grid, stream)
-                   : launch_one<false>(tmap_a, tmap_b, a, grid, stream);
+                           int grid, cudaStream_t stream, const CUtensorMap* tmap_b1) {
+    if (grid % 2 || (a.gated && (!tmap_b1 || a.b_kmajor))) return cudaErrorInvalidValue;
+    const CUtensorMap& tb1 = tmap_b1 ? *tmap_b1 : tmap_b;
+    return out_f32 ? launch_one<true>(tmap_a, tmap_b, tb1, a, grid, stream)
+                   : launch_one<false>(tmap_a, tmap_b, tb1, a, grid, stream);
 }
 
 int fwd_tc2_max_clusters(bool out_f32, int G) {

@@ -57,7 +57,8 @@ typedef enum {
     RDOT_MODE_FORWARD = 0,       /* out[M,N] = lhs[M,K] @ rhs[g(i),K,N] (non-contracting ragged M) */
     RDOT_MODE_GRAD_WEIGHT = 1,   /* dw[G,K,N] = lhs_g^T dy_g (ragged contraction over the rows) */
     RDOT_MODE_FORWARD_MXFP8 = 2, /* forward with E4M3 operands and E8M0 scales per 32 K elements */
-    RDOT_MODE_GRAD_INPUT = 3     /* dlhs[M,K] = dy[M,N] @ rhs[g(i),K,N]^T (contracts rhs's N axis) */
+    RDOT_MODE_GRAD_INPUT = 3,    /* dlhs[M,K] = dy[M,N] @ rhs[g(i),K,N]^T (contracts rhs's N axis) */
+    RDOT_MODE_FORWARD_GATED = 4  /* out[M,N] = silu(lhs @ w0[g(i)]) * (lhs @ w1[g(i)]) (gated up projection) */
 } rdot_mode;
 
 /* Bits of the device status word (int32 at offset 0 of the workspace). */
@@ -167,6 +168,20 @@ RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const v
  * and stream rules as rdot_forward; the kernels are the forward's with a K-major B operand. */
 RDOT_API rdot_status rdot_grad_input(rdot_plan_t plan, const void* dy, const void* rhs,
                             const int32_t* group_sizes, void* dlhs, void* workspace, void* stream);
+
+/* Gated up projection of an MoE expert layer, fused ("Group-GEMM in XLA", Part 4 "The Three MoE
+ * Compute Paths in MaxText": the two ragged dots of the up projection feed
+ * activation(layer_w0) * layer_w1; the activation is SiLU, silu(z) = z / (1 + e^-z)):
+ *   out[i, :] = silu(lhs[i, :] @ w0[g(i)]) * (lhs[i, :] @ w1[g(i)])
+ *   lhs     device bf16 [M, K];  w0, w1  device bf16 [G, K, N] each (N = the layer's hidden width)
+ *   out     device [M, N], the plan's out_dtype (bf16 or fp32); zeros past the sum
+ * Both products accumulate in fp32 in tensor memory of the same 256-row CTA-pair tile (one CTA
+ * stages w0's columns, the other w1's) and only the activated result is stored. The plan's
+ * problem: mode RDOT_MODE_FORWARD_GATED, in_dtype RDOT_BF16, tile_n 0, K and N multiples of 8;
+ * RDOT_FLAG_NO_CTA_PAIR is RDOT_ERR_UNSUPPORTED. Same workspace, status and stream rules as
+ * rdot_forward. */
+RDOT_API rdot_status rdot_forward_gated(rdot_plan_t plan, const void* lhs, const void* w0, const void* w1,
+                               const int32_t* group_sizes, void* out, void* workspace, void* stream);
 
 /* MoE pre- and post-processing around the ragged dot ("Group-GEMM in XLA", Part 4 "The Three MoE
  * Compute Paths in MaxText", Path 1 (sparse / ragged-dot), and Part 5 "Next steps": permute before

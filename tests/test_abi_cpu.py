@@ -55,6 +55,10 @@ def test_status_strings_and_version(lib):
     (dict(m=16, k=8, n=8, groups=1, tile_n=512, flags=gg.RDOT_FLAG_NO_CTA_PAIR), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=8, n=8, groups=1, tile_n=512, mode=1, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=8, n=8, groups=1, mode=7), gg.RDOT_ERR_INVALID_ARG),
+    # the gated up projection: bf16, CTA pairs, no tile override
+    (dict(m=16, k=8, n=8, groups=1, mode=4, tile_n=128), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=8, n=8, groups=1, mode=4, flags=gg.RDOT_FLAG_NO_CTA_PAIR), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=8, n=8, groups=1, mode=4, in_dtype=gg.RDOT_F32, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
     # the data gradient: bf16 inputs, 16-byte rows on both widths
     (dict(m=16, k=8, n=8, groups=1, mode=3, in_dtype=gg.RDOT_F32, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=12, n=8, groups=1, mode=3), gg.RDOT_ERR_UNSUPPORTED),
