@@ -53,7 +53,9 @@ struct TcLayout {
     }
 };
 
-template <int BN, int STAGES, bool OUT_F32>
+// KMAJ: the data gradient's K-major B operand, a compile-time choice (a runtime branch costs
+// the forward a few per cent).
+template <int BN, int STAGES, bool OUT_F32, bool KMAJ>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                   FwdArgs a) {
@@ -134,11 +136,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // BN rows x 64 K, rows past N zero-filled.
                     const int nchunks = min(BN / 64, (a.N - n0 + 63) / 64);
                     mbar_arrive_expect_tx(&full[stage],
-                                          L::A_BYTES + (a.b_kmajor ? L::B_BYTES : nchunks * L::B_CHUNK_BYTES));
+                                          L::A_BYTES + (KMAJ ? L::B_BYTES : nchunks * L::B_CHUNK_BYTES));
                     // a row tile of lhs is re-read by every column tile of its group while the
                     // weights of other groups stream through L2: keep it (DeepSeek-like: -1 %)
                     tma_load_2d_hint(sa, &tmap_a, &full[stage], kb * TC_BK, t.row0, a_policy);
-                    if (a.b_kmajor)
+                    if (KMAJ)
                         tma_load_3d(sb, &tmap_b, &full[stage], kb * TC_BK, n0, t.g);
                     else
                         for (int j = 0; j < nchunks; ++j)
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const bool kmaj = a.b_kmajor != 0;
+            constexpr bool kmaj = KMAJ;
             const uint32_t idesc = kmaj ? idesc_f16(TC_BM, BN, true, true, false, false)
                                         : idesc_f16(TC_BM, BN, true, true, false, true);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -273,7 +275,7 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const FwdAr
                        cudaStream_t stream) {
     using L = TcLayout<BN, STAGES, OUT_F32>;
     const size_t shm = L::smem_bytes(a.G);
-    auto kern = fwd_tc_kernel<BN, STAGES, OUT_F32>;
+    auto kern = a.b_kmajor ? fwd_tc_kernel<BN, STAGES, OUT_F32, true> : fwd_tc_kernel<BN, STAGES, OUT_F32, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
     kern<<<grid, THREADS, shm, stream>>>(ta, tb, a);
