@@ -480,6 +480,21 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                          "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}"}
     del dy, rhs, dlhs
     torch.cuda.empty_cache()
+    # fused gated up projection at the Mixtral-like size: silu(x w0) * (x w1), two ragged dots
+    x = ri.device_normal((m, k), 1000, 1.0, dev, torch.bfloat16)
+    rhs1 = ri.device_normal((g, k, n), 2001, 0.02, dev, torch.bfloat16)
+    rhs0 = ri.device_normal((g, k, n), 2000, 0.02, dev, torch.bfloat16)
+    hout = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    plan = gg.Plan(m, k, n, g, "forward_gated", "bf16", "bf16", device=dev.index)
+    t = _time_steps(lambda: gg.rdot_forward_gated(plan.handle, x, rhs0, rhs1, gs_d, hout, plan.workspace, stream),
+                    steps, stream)
+    fl = 2.0 * useful_flops(gs, k, n)
+    res["gated_up_bf16"] = {"workload": f"silu(x w0) * (x w1): x [{m}, {k}], w0/w1 [{g}, {k}, {n}]",
+                            "tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
+                            "frac_of_bf16_peak": round(fl / t / 1e12 / peaks["bf16_tflops"], 4),
+                            "status": plan.status(), "tile": "256x128 (x2 accumulators: w0, w1)"}
+    del x, rhs0, rhs1, hout
+    torch.cuda.empty_cache()
     # MoE permute / un-permute around the Mixtral-like layer: 8192 tokens, top-2 of 8, width 4096
     t, k, e, width = m // 2, 2, g, cfg["k"]
     rng = np.random.default_rng(0)
