@@ -462,6 +462,28 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
         res[name] = entry
         del lhs, rhs, out, pad
         torch.cuda.empty_cache()
+    # decode-sized forwards: a few dozen tokens, so every routed expert's weights stream once
+    # (HBM-bound whatever the tile shape); reported against the HBM copy peak
+    for name, tokens, topk, sigma in (("mixtral_bf16", 64, 2, None), ("deepseek_bf16", 64, 8, 1.1)):
+        cfg = ri.CONFIGS[name]
+        k, n, g = cfg["k"], cfg["n"], cfg["g"]
+        gs = (ri.routed_group_sizes(tokens, g, topk, 1.0, seed=0) if sigma is None else
+              ri.zipf_routed_group_sizes(tokens, g, topk, sigma, seed=0, n_zero=8))
+        m = int(gs.sum())
+        lhs = ri.device_normal((m, k), 1, 1.0, dev, torch.bfloat16)
+        rhs = ri.device_normal((g, k, n), 2, 0.02, dev, torch.bfloat16)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        gs_d = torch.from_numpy(gs).to(dev)
+        plan = gg.Plan(m, k, n, g, "forward", "bf16", "bf16", device=dev.index)
+        t = _time_steps(lambda: gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream), 20, stream)
+        wbytes = int(np.count_nonzero(gs)) * k * n * 2 + m * (k + n) * 2
+        res[f"decode_{name}"] = {"workload": f"{tokens} tokens top-{topk}: M={m}, {int(np.count_nonzero(gs))} of {g} "
+                                             f"experts routed", "ms": round(t * 1e3, 4),
+                                 "hbm_gbs_algorithmic": round(wbytes / t / 1e9, 1),
+                                 "frac_of_hbm": round(wbytes / t / 1e9 / peaks["hbm_gbs"], 4), "status": plan.status(),
+                                 "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}"}
+        del lhs, rhs, out
+        torch.cuda.empty_cache()
     # data gradient of the Mixtral-like forward: dlhs [M, K] = dy [M, N] . rhs[g]^T
     cfg = ri.CONFIGS["mixtral_bf16"]
     m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
