@@ -421,7 +421,11 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
         fl = useful_flops(gs, k, n)
         entry = {}
         if name == main_name:
-            t = main_step_s
+            # the same kernel timed like the baselines below (a short burst), so that the
+            # speedups compare like with like; the long timed region's figure is the bench value
+            t = _time_steps(lambda: gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream),
+                            steps, stream)
+            entry["ms_burst"] = round(t * 1e3, 4)
         if name != main_name:
             t = _time_steps(lambda: gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream),
                             steps, stream)
