@@ -15,7 +15,8 @@
 //                     one expert, a lane's rank is the number of lower lanes in its group, and
 //                     the group's last lane advances the expert's running position -- the order
 //                     of equal keys is the flat order, as the stable sort defines it.
-// The gather and the combine are HBM-bound row copies: one warp per row, 16-byte vectors.
+// The gather (one warp per token: its row read once, its k copies written) and the combine (one
+// warp per token: its k copies read, one row written) are HBM-bound, in 16-byte vectors.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -135,25 +136,32 @@ __global__ void __launch_bounds__(32) moe_place_kernel(const int32_t* __restrict
     }
 }
 
-// x_sorted[p] = x[order[p] / k] for p < valid; past it the row is zero and order[p] = -1.
-// One warp per row, 16-byte vectors.
-__global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict__ x, int32_t* __restrict__ order,
-                                                         const int32_t* __restrict__ valid, long long rows, int k,
-                                                         int vec_per_row, uint4* __restrict__ x_sorted) {
+// x_sorted[inv[t*k + j]] = x[t] for every kept copy: one warp per token reads its row once and
+// writes its k copies (a gather by sorted row would read each token row k times). Then the rows
+// past the kept copies (dropped ids) are zeroed and their order entries set to -1.
+__global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv,
+                                                         int32_t* __restrict__ order, const int32_t* __restrict__ valid,
+                                                         long long tokens, int k, int vec_per_row,
+                                                         uint4* __restrict__ x_sorted) {
     const int lane = threadIdx.x & 31;
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-    const int32_t v = *valid;
-    for (long long p = warp; p < rows; p += nwarps) {
-        uint4* dst = x_sorted + p * vec_per_row;
-        if (p < v) {
-            const uint4* src = x + static_cast<long long>(order[p] / k) * vec_per_row;
-#pragma unroll 4
-            for (int i = lane; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
-        } else {
-            for (int i = lane; i < vec_per_row; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
-            if (lane == 0) order[p] = -1;
+    for (long long t = warp; t < tokens; t += nwarps) {
+        const uint4* src = x + t * vec_per_row;
+        for (int i = lane; i < vec_per_row; i += 32) {
+            const uint4 v = __ldg(src + i);
+            for (int j = 0; j < k; ++j) {
+                const int32_t p = __ldg(inv + t * k + j);
+                if (p >= 0) x_sorted[static_cast<long long>(p) * vec_per_row + i] = v;
+            }
         }
+    }
+    const long long total = tokens * k;
+    const int32_t v = *valid;
+    for (long long p = v + warp; p < total; p += nwarps) {
+        uint4* dst = x_sorted + p * vec_per_row;
+        for (int i = lane; i < vec_per_row; i += 32) dst[i] = make_uint4(0, 0, 0, 0);
+        if (lane == 0) order[p] = -1;
     }
 }
 
@@ -216,9 +224,9 @@ cudaError_t launch_moe_permute(const int32_t* ids, long long tokens, int k, int 
     moe_place_kernel<<<static_cast<unsigned>(nchunks), 32, cnt_shm, stream>>>(ids, total, E, chunk_hist, expert_base,
                                                                              order, inv);
     const int vec = static_cast<int>(row_bytes / 16);
-    const long long want = (total + 7) / 8;
+    const long long want = (tokens + 7) / 8;
     const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
-    moe_gather_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), order, valid, total, k, vec,
+    moe_gather_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), inv, order, valid, tokens, k, vec,
                                                 static_cast<uint4*>(x_sorted));
     return cudaGetLastError();
 }
