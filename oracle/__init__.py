@@ -15,6 +15,9 @@ Functions and the passages they follow (page titles and sections):
   -> [M,K], contracting rhs's dimension 2).
 * :func:`forward_mxfp8_rows` -- AITER PR #5658 (E4M3 + E8M0 per 32 K elements).
 * :func:`tile_map` -- the library's scheduler order (not on the pages), by brute force.
+* :func:`grad_input_mxfp8` -- the data gradient (Part 4 Table 7, dgrad_wi) on MXFP8 operands
+  (AITER PR #5658 number format): dy and the weights carry one E8M0 scale per 32 elements of the
+  contracted axis N; the elements are dequantised one by one and the fp64 data gradient applies.
 * :func:`gated_forward` -- "Group-GEMM in XLA", Part 4 "The Three MoE Compute Paths in MaxText":
   the up projection's two ragged dots feed ``activation(layer_w0) * layer_w1``; the activation is
   read as SiLU, z * sigmoid(z), the gated unit of the evaluated MoE models.
@@ -347,3 +350,19 @@ def gated_forward(lhs, w0, w1, group_sizes):
     with np.errstate(over="ignore"):
         silu = a / (1.0 + np.exp(-a))
     return silu * b
+
+
+def mx_dequant(codes, scales, axis: int):
+    """Element values of OCP-MX E4M3 codes with one E8M0 scale per 32 elements along ``axis``:
+    decode(code) * 2^(scale - 127), float64, from this file's decoders."""
+    c = np.ascontiguousarray(_as_np(codes)[0]).view(np.uint8)
+    sc = np.ascontiguousarray(_as_np(scales)[0]).view(np.uint8)
+    lut_c = np.array([e4m3_decode(i) for i in range(256)])
+    lut_s = np.array([e8m0_decode(i) for i in range(256)])
+    return lut_c[c] * np.repeat(lut_s[sc], 32, axis=axis)
+
+
+def grad_input_mxfp8(dy_q, dy_s, w_q, w_s, group_sizes):
+    """Data gradient on MXFP8 operands, float64 ``[M, K]``: dy_q [M, N] with dy_s [M, N/32] and
+    w_q [G, K, N] with w_s [G, K, N/32] (scales along the contracted N)."""
+    return grad_input(mx_dequant(dy_q, dy_s, 1), mx_dequant(w_q, w_s, 2), group_sizes)

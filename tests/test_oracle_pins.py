@@ -276,6 +276,41 @@ def test_grad_input_rows_subset_and_transposed_forward():
     assert _rel(full, oracle.forward(dy, np.ascontiguousarray(w.transpose(0, 2, 1)), gs)) < TOL
 
 
+def _mx_dgrad_case(seed, m, k, n, g):
+    rng = np.random.default_rng(seed)
+    dy = torch.from_numpy(rng.standard_normal((m, n)))
+    w = torch.from_numpy(rng.standard_normal((g, k, n)) * 0.1)
+    dq, ds = ri.quantize_mx_e4m3(dy.float(), axis=1)
+    wq, ws = ri.quantize_mx_e4m3(w.float(), axis=2)
+    return dq, ds, wq, ws
+
+
+def test_grad_input_mxfp8_unit_scales_shift_and_adjoint():
+    """Unit scales: the data gradient of the E4M3 values (decoded by torch's float8 cast, not by
+    the oracle); +3 on every dy scale: exactly 8x; and the adjoint identity with the fp64 forward
+    on the dequantised weights."""
+    gs = np.array([5, 0, 9, 2], np.int32)
+    m, k, n = int(gs.sum()) + 3, 8, 64
+    dq, ds, wq, ws = _mx_dgrad_case(42, m, k, n, gs.size)
+    one_d, one_w = torch.full_like(ds, 127), torch.full_like(ws, 127)
+    dec_d = dq.view(torch.float8_e4m3fn).double().numpy()
+    dec_w = wq.view(torch.float8_e4m3fn).double().numpy()
+    ref = np.zeros((m, k))
+    start = 0
+    for e, sz in enumerate(gs):
+        ref[start:start + sz] = dec_d[start:start + sz] @ dec_w[e].T
+        start += sz
+    assert _rel(oracle.grad_input_mxfp8(dq, one_d, wq, one_w, gs), ref) < TOL
+    base = oracle.grad_input_mxfp8(dq, ds, wq, ws, gs)
+    shifted = oracle.grad_input_mxfp8(dq, (ds.int() + 3).to(torch.uint8), wq, ws, gs)
+    assert np.array_equal(shifted, base * 8.0)
+    x = np.random.default_rng(43).standard_normal((m, k))
+    wd = oracle.mx_dequant(wq, ws, 2)
+    lhs_side = float(np.sum(oracle.forward(x, wd, gs) * oracle.mx_dequant(dq, ds, 1)))
+    rhs_side = float(np.sum(x * base))
+    assert abs(lhs_side - rhs_side) <= 1e-10 * (abs(lhs_side) + 1.0)
+
+
 # ------------------------------------------------------------------------- gated up projection
 def test_gated_forward_brute_force_and_silu_identity():
     """activation(x w0) * (x w1) with SiLU: numpy per group; and the closed form
