@@ -23,7 +23,7 @@ __all__ = [
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_grad_input", "rdot_moe_route_workspace_size", "rdot_moe_permute",
-    "rdot_moe_unpermute", "rdot_forward_gated", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
+    "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
     "grad_input", "ragged_dot_gated",
     "ragged_dot_mxfp8", "padded_ragged_dot", "EXPORTED_SYMBOLS",
 ]
@@ -32,7 +32,7 @@ RDOT_OK, RDOT_ERR_INVALID_ARG, RDOT_ERR_UNSUPPORTED, RDOT_ERR_CUDA = 0, 1, 2, 3
 RDOT_ERR_DEVICE_TIMEOUT, RDOT_WARN_GROUP_SIZES = 4, 5
 RDOT_F32, RDOT_BF16, RDOT_E4M3 = 0, 1, 2
 RDOT_MODE_FORWARD, RDOT_MODE_GRAD_WEIGHT, RDOT_MODE_FORWARD_MXFP8, RDOT_MODE_GRAD_INPUT = 0, 1, 2, 3
-RDOT_MODE_FORWARD_GATED = 4
+RDOT_MODE_FORWARD_GATED, RDOT_MODE_GRAD_INPUT_MXFP8 = 4, 5
 RDOT_STATUS_BIT_GROUP_SIZES, RDOT_STATUS_BIT_TIMEOUT = 0x1, 0x2
 RDOT_FLAG_ROW_TILES_INNER, RDOT_FLAG_COL_TILES_INNER = 0x1, 0x2
 RDOT_FLAG_CTA_PAIR, RDOT_FLAG_NO_CTA_PAIR, RDOT_FLAG_NATURAL_ORDER = 0x4, 0x8, 0x10
@@ -45,13 +45,13 @@ EXPORTED_SYMBOLS = (
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_grad_input", "rdot_moe_route_workspace_size", "rdot_moe_permute",
-    "rdot_moe_unpermute", "rdot_forward_gated",
+    "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8",
 )
 
 _DTYPE_CODES = {"f32": RDOT_F32, "bf16": RDOT_BF16, "e4m3": RDOT_E4M3}
 _MODE_CODES = {"forward": RDOT_MODE_FORWARD, "grad_weight": RDOT_MODE_GRAD_WEIGHT,
                "forward_mxfp8": RDOT_MODE_FORWARD_MXFP8, "grad_input": RDOT_MODE_GRAD_INPUT,
-               "forward_gated": RDOT_MODE_FORWARD_GATED}
+               "forward_gated": RDOT_MODE_FORWARD_GATED, "grad_input_mxfp8": RDOT_MODE_GRAD_INPUT_MXFP8}
 
 
 class RdotError(RuntimeError):
@@ -98,6 +98,7 @@ def load():
             "rdot_grad_weight": ([vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_grad_input": ([vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_forward_gated": ([vp, vp, vp, vp, vp, vp, vp, vp], st),
+            "rdot_grad_input_mxfp8": ([vp, vp, vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_moe_route_workspace_size": ([i64, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
                                               st),
             "rdot_moe_permute": ([vp, i64, ctypes.c_int32, ctypes.c_int32, vp, i64, vp, vp, vp, vp, vp, vp], st),
@@ -175,6 +176,12 @@ def rdot_grad_weight(plan, lhs, dy, group_sizes, dw, workspace, stream=None) -> 
 def rdot_grad_input(plan, dy, rhs, group_sizes, dlhs, workspace, stream=None) -> None:
     _check(load().rdot_grad_input(plan, _ptr(dy), _ptr(rhs), _ptr(group_sizes), _ptr(dlhs), _ptr(workspace),
                                   _stream(stream, dlhs.device)), "rdot_grad_input")
+
+
+def rdot_grad_input_mxfp8(plan, dy_q, dy_scale, w_q, w_scale, group_sizes, dlhs, workspace, stream=None) -> None:
+    _check(load().rdot_grad_input_mxfp8(plan, _ptr(dy_q), _ptr(dy_scale), _ptr(w_q), _ptr(w_scale),
+                                        _ptr(group_sizes), _ptr(dlhs), _ptr(workspace),
+                                        _stream(stream, dlhs.device)), "rdot_grad_input_mxfp8")
 
 
 def rdot_forward_gated(plan, lhs, w0, w1, group_sizes, out, workspace, stream=None) -> None:

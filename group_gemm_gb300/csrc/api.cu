@@ -82,7 +82,7 @@ struct rdot_plan_s {
     int cc_major = 0, cc_minor = 0;
     int kind = 0;          // 0: SIMT fp32 forward, 1: tcgen05 bf16 forward, 2: tcgen05 grad-weight, 3: MXFP8,
                            // 4: tcgen05 data gradient (the forward kernels, K-major B),
-                           // 5: gated up projection (CTA pairs)
+                           // 5: gated up projection (CTA pairs), 6: MXFP8 data gradient
     int tile_m = 0, tile_n = 0;
     int m_inner = 1;
     int grid = 1;
@@ -183,6 +183,11 @@ rdot_status check_problem(const rdot_problem* p) {
             if (p->in_dtype != RDOT_BF16 || p->out_dtype != RDOT_F32) return RDOT_ERR_UNSUPPORTED;
             if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;
             return RDOT_OK;
+        case RDOT_MODE_GRAD_INPUT_MXFP8:
+            if (p->in_dtype != RDOT_E4M3 || p->out_dtype != RDOT_BF16) return RDOT_ERR_UNSUPPORTED;
+            if (p->n % 32 || p->k % 8 || (p->flags & RDOT_FLAG_CTA_PAIR) || p->tile_n == 512)
+                return RDOT_ERR_UNSUPPORTED;
+            return RDOT_OK;
         case RDOT_MODE_FORWARD_GATED:
             if (p->in_dtype != RDOT_BF16 || p->tile_n != 0 || (p->flags & RDOT_FLAG_NO_CTA_PAIR))
                 return RDOT_ERR_UNSUPPORTED;
@@ -280,6 +285,24 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         // small average groups: interleave the tiles of groups with 2+ row tiles with the
         // others so every wave mixes tensor-core-bound and weight-streaming work
         pl->big_mt = (!want_pair && !(p.flags & RDOT_FLAG_NATURAL_ORDER)) ? 2 : 0;
+    } else if (p.mode == RDOT_MODE_GRAD_INPUT_MXFP8) {
+        if (prop.major != 10) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->kind = 6;
+        pl->m_inner = (m_avg <= p.k) ? 1 : 0;   // the output width is K
+        if (p.flags & 1) pl->m_inner = 1;
+        if (p.flags & 2) pl->m_inner = 0;
+        pl->tile_m = TC_BM;
+        pl->tile_n = p.tile_n ? p.tile_n : (p.k >= 256 ? 256 : 128);
+        const int nt = static_cast<int>((p.k + pl->tile_n - 1) / pl->tile_n);
+        const long long bound = forward_tile_bound(p.m, p.groups, TC_BM, nt);
+        if (bound > 0x7fffffffLL) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
     } else if (p.mode == RDOT_MODE_FORWARD_GATED) {
         if (prop.major != 10) {
             delete pl;
@@ -432,6 +455,14 @@ struct MxLayout {
     int ks, nt;
 };
 
+// The data gradient's GEMM in the forward's terms: contraction = the problem's n, output = k.
+rdot_problem swapped_kn(const rdot_problem& p) {
+    rdot_problem q = p;
+    q.k = p.n;
+    q.n = p.k;
+    return q;
+}
+
 MxLayout mx_layout(const rdot_problem& p, int bm, int bn) {
     MxLayout l{};
     l.ks = static_cast<int>((p.k + 127) / 128);
@@ -450,6 +481,8 @@ rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes) {
     if (!plan || !bytes) return RDOT_ERR_INVALID_ARG;
     if (plan->kind == 3)
         *bytes = mx_layout(plan->p, plan->tile_m, plan->tile_n).total;
+    else if (plan->kind == 6)
+        *bytes = mx_layout(swapped_kn(plan->p), plan->tile_m, plan->tile_n).total;
     else if (plan->kind == 2)
         *bytes = kWorkspaceBytes + static_cast<size_t>(2 * WG_MAP_BYTES) * plan->p.groups;   // group tensor maps
     else
@@ -524,6 +557,60 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
     else
         e = launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "fwd_tc launch");
+    return RDOT_OK;
+}
+
+rdot_status rdot_grad_input_mxfp8(rdot_plan_t plan, const void* dy_q, const uint8_t* dy_scale, const void* w_q,
+                                  const uint8_t* w_scale, const int32_t* group_sizes, void* dlhs, void* workspace,
+                                  void* stream) {
+    if (!plan || !group_sizes || !workspace) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.mode != RDOT_MODE_GRAD_INPUT_MXFP8 || plan->kind != 6) return RDOT_ERR_INVALID_ARG;
+    if (p.m == 0) return RDOT_OK;
+    if (!dy_q || !dy_scale || !w_q || !w_scale || !dlhs) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(dy_q) || !aligned16(w_q) || !aligned16(dlhs) || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+        (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // A = dy codes [M, N] (K-major, the contraction N contiguous); B = w codes viewed as
+    // [K output rows, N contraction] (K-major): boxes of 128 rows x 128 bytes
+    if (plan->map_lhs_ptr != dy_q) {
+        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, dy_q, p.n, p.m, p.n, 128, 128);
+        if (st != RDOT_OK) return st;
+        plan->map_lhs_ptr = dy_q;
+    }
+    if (plan->map_rhs_ptr != w_q) {
+        rdot_status st = encode_3d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_q, p.n, p.k, p.groups, p.n,
+                                   p.k * p.n, 128, 128, 1);
+        if (st != RDOT_OK) return st;
+        plan->map_rhs_ptr = w_q;
+    }
+    const rdot_problem q = swapped_kn(p);
+    const MxLayout l = mx_layout(q, plan->tile_m, plan->tile_n);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    MxArgs a{};
+    a.out = dlhs;
+    a.M = static_cast<int>(p.m);
+    a.K = static_cast<int>(p.n);   // the contraction
+    a.N = static_cast<int>(p.k);   // the output width
+    a.G = p.groups;
+    a.BN = plan->tile_n;
+    a.NT = l.nt;
+    a.KS = l.ks;
+    a.NT128 = static_cast<int>((p.k + 127) / 128);
+    a.m_inner = plan->m_inner;
+    a.sfa = ws + l.sfa_off;
+    a.sfb = ws + l.sfb_off;
+    a.sfb_vec = 0;
+    a.sfa_vec = (p.n % 128 == 0 && (reinterpret_cast<uintptr_t>(dy_scale) & 3u) == 0) ? 1 : 0;
+    a.b_kmajor = 1;
+    a.status = static_cast<int32_t*>(workspace);
+    a.timeout_ns = plan->timeout_ns;
+    cudaError_t e = launch_mxfp8(plan->map_a, plan->map_b, dy_scale, w_scale, group_sizes, a, plan->grid,
+                                 4 * plan->sm_count, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mxfp8 grad_input launch");
     return RDOT_OK;
 }
 
@@ -964,6 +1051,6 @@ const char* rdot_status_string(rdot_status status) {
 
 const char* rdot_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
 
-int rdot_version(void) { return 102; }
+int rdot_version(void) { return 103; }
 
 }  // extern "C"

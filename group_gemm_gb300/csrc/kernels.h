@@ -106,6 +106,8 @@ struct MxArgs {
     int sfb_vec;                 // rhs_scale rows can be read as 32-bit words (N % 4 == 0, aligned)
     int sfa_vec;                 // lhs_scale rows can be read as 32-bit words (K % 128 == 0, aligned)
     int pair;                    // 1: 256-row tiles on CTA pairs (sfa blocks per 128-row half)
+    int b_kmajor;                // 1: the data gradient -- B codes [G, N out, K] with K contiguous and
+                                 // rhs_scale [G, N, K/32] (scales along K); 0: the forward
     int32_t* status;
     uint64_t timeout_ns;
 };

@@ -132,6 +132,21 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
             const long long blk = (static_cast<long long>(g) * a.NT + nt / atoms) * a.KS + ks;
             uint32_t* dst = reinterpret_cast<uint32_t*>(a.sfb + blk * (atoms * SF_ATOM_BYTES) +
                                                         (nt % atoms) * SF_ATOM_BYTES);
+            if (a.b_kmajor) {
+                // scales along K: rhs_scale [G, N, K/32]; the atom's 128 B rows are read like the
+                // lhs rows (lane l gathers rows l, l+32, l+64, l+96)
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = lane + 32 * i;
+                    const int nrow = nt * 128 + r;
+                    w[i] = 0x7f7f7f7fu;
+                    if (nrow < a.N)
+                        w[i] = scale_word(rhs_scale + (static_cast<long long>(g) * a.N + nrow) * KB32 + 4 * ks, avail);
+                }
+                reinterpret_cast<uint4*>(dst)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+                continue;
+            }
             const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + nt * 128;
             const int n4 = nt * 128 + 4 * lane;         // this lane's 4 consecutive columns
             if (a.sfb_vec && n4 + 3 < a.N) {
@@ -172,7 +187,8 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
     }
 }
 
-template <int BN>
+// KMAJ: the data gradient's K-major B (codes [G, N out, K]); a compile-time choice.
+template <int BN, bool KMAJ>
 __global__ void __launch_bounds__(THREADS, 1)
     mxfp8_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const int32_t* __restrict__ group_sizes, MxArgs a) {
@@ -253,9 +269,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int nb = min(BN / 128, (a.N - t.nt * BN + 127) / 128);
                     mbar_arrive_expect_tx(&full[stage], A_BYTES + nb * (BKB * 128) + SFA_BYTES + SFB_BYTES);
                     tma_load_2d(st, &tmap_a, &full[stage], ks * BKB, t.row0);
-                    for (int j = 0; j < nb; ++j)
-                        tma_load_3d(st + A_BYTES + j * (BKB * 128), &tmap_b, &full[stage], t.nt * BN + 128 * j,
-                                    ks * BKB, t.g);
+                    for (int j = 0; j < nb; ++j) {
+                        if (KMAJ)   // 128 output rows x 128 K bytes, rows past N zero-filled
+                            tma_load_3d(st + A_BYTES + j * (BKB * 128), &tmap_b, &full[stage], ks * BKB,
+                                        t.nt * BN + 128 * j, t.g);
+                        else
+                            tma_load_3d(st + A_BYTES + j * (BKB * 128), &tmap_b, &full[stage], t.nt * BN + 128 * j,
+                                        ks * BKB, t.g);
+                    }
                     bulk_load(st + A_BYTES + B_BYTES, sfa_src + static_cast<long long>(ks) * SFA_BYTES, SFA_BYTES,
                               &full[stage]);
                     bulk_load(st + A_BYTES + B_BYTES + SFA_BYTES, sfb_src + static_cast<long long>(ks) * SFB_BYTES,
@@ -304,10 +325,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                smem_desc_rows16(sb + B_BYTES + SFA_BYTES + j * SF_ATOM_BYTES));
 #pragma unroll
                     for (int kk = 0; kk < BKB / 32; ++kk) {
-                        // A K-major: +32 bytes per 32-element K step; B MN-major: +32 K rows of 128 B
+                        // A K-major: +32 bytes per 32-element K step; B MN-major: +32 K rows of
+                        // 128 B, or K-major like A (BN rows of 128 B)
                         const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
-                        const uint64_t bdesc = smem_desc_sw128(sb + kk * 4096, BKB * 128, 1024);
-                        mma_mxf8(d_tmem, adesc, bdesc, idesc_mxf8(BM, BN, false, true, kk, kk), sfa_t, sfb_t,
+                        const uint64_t bdesc = KMAJ ? smem_desc_sw128(sb + kk * 32, 16, 1024)
+                                                    : smem_desc_sw128(sb + kk * 4096, BKB * 128, 1024);
+                        mma_mxf8(d_tmem, adesc, bdesc, idesc_mxf8(BM, BN, false, !KMAJ, kk, kk), sfa_t, sfb_t,
                                  (ks | kk) != 0 ? 1u : 0u);
                     }
                     mma_commit(&empty[stage]);
@@ -406,7 +429,7 @@ template <int BN>
 cudaError_t launch_main(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const int32_t* group_sizes,
                         const MxArgs& a, int grid, cudaStream_t stream) {
     const size_t shm = MxLayout<BN>::smem_bytes(a.G);
-    auto kern = mxfp8_tc_kernel<BN>;
+    auto kern = a.b_kmajor ? mxfp8_tc_kernel<BN, true> : mxfp8_tc_kernel<BN, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
     kern<<<grid, THREADS, shm, stream>>>(tmap_a, tmap_b, group_sizes, a);

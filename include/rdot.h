@@ -58,7 +58,8 @@ typedef enum {
     RDOT_MODE_GRAD_WEIGHT = 1,   /* dw[G,K,N] = lhs_g^T dy_g (ragged contraction over the rows) */
     RDOT_MODE_FORWARD_MXFP8 = 2, /* forward with E4M3 operands and E8M0 scales per 32 K elements */
     RDOT_MODE_GRAD_INPUT = 3,    /* dlhs[M,K] = dy[M,N] @ rhs[g(i),K,N]^T (contracts rhs's N axis) */
-    RDOT_MODE_FORWARD_GATED = 4  /* out[M,N] = silu(lhs @ w0[g(i)]) * (lhs @ w1[g(i)]) (gated up projection) */
+    RDOT_MODE_FORWARD_GATED = 4, /* out[M,N] = silu(lhs @ w0[g(i)]) * (lhs @ w1[g(i)]) (gated up projection) */
+    RDOT_MODE_GRAD_INPUT_MXFP8 = 5  /* the data gradient on MXFP8 operands (scales along N) */
 } rdot_mode;
 
 /* Bits of the device status word (int32 at offset 0 of the workspace). */
@@ -168,6 +169,19 @@ RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const v
  * and stream rules as rdot_forward; the kernels are the forward's with a K-major B operand. */
 RDOT_API rdot_status rdot_grad_input(rdot_plan_t plan, const void* dy, const void* rhs,
                             const int32_t* group_sizes, void* dlhs, void* workspace, void* stream);
+
+/* Data gradient on MXFP8 operands (Part 4 Table 7 dgrad_wi with the number format of AITER PR
+ * #5658): dlhs[i,:] = dequant(dy)[i,:] @ dequant(w)[g(i)]^T, fp32 accumulation, bf16 out.
+ *   dy_q      device uint8 [M, N]       E4M3 codes;  dy_scale  device uint8 [M, N/32]    E8M0
+ *   w_q       device uint8 [G, K, N]    E4M3 codes;  w_scale   device uint8 [G, K, N/32] E8M0
+ *   dlhs      device bf16 [M, K]; zeros past the sum
+ * The scales run along the contracted N on both operands (the backward's quantisation; the
+ * forward's weight scales run along K). Plan: mode RDOT_MODE_GRAD_INPUT_MXFP8, in_dtype
+ * RDOT_E4M3, out_dtype RDOT_BF16, N % 32 == 0, K % 8 == 0; workspace rdot_workspace_size bytes,
+ * 256-byte aligned (the reordered scale blocks). */
+RDOT_API rdot_status rdot_grad_input_mxfp8(rdot_plan_t plan, const void* dy_q, const uint8_t* dy_scale,
+                                  const void* w_q, const uint8_t* w_scale, const int32_t* group_sizes,
+                                  void* dlhs, void* workspace, void* stream);
 
 /* Gated up projection of an MoE expert layer, fused ("Group-GEMM in XLA", Part 4 "The Three MoE
  * Compute Paths in MaxText": the two ragged dots of the up projection feed

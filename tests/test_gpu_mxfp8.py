@@ -112,3 +112,70 @@ def test_mxfp8_max_groups(variant):
     out, status = run(aq, as_, bq, bs, gs, variant)
     assert status == 0
     assert rel_err(out, oracle.forward_mxfp8(aq, as_, bq, bs, gs)) <= TOL
+
+
+# ------------------------------------------------------------------ data gradient on MXFP8 operands
+def make_dgrad_case(m, k, n, gs, seed, vary=("a", "b")):
+    dy = torch.from_numpy(ri.host_normal((m, n), seed))
+    w = torch.from_numpy(ri.host_normal((len(gs), k, n), seed + 1, 0.02))
+    dq, ds = ri.quantize_mx_e4m3(dy, axis=1)
+    wq, ws = ri.quantize_mx_e4m3(w, axis=2)          # the backward's scales run along N
+    gen = torch.Generator().manual_seed(seed + 2)
+    ds = (ds.to(torch.int32) + torch.randint(-4, 5, ds.shape, generator=gen)).clamp(100, 150).to(torch.uint8) \
+        if "a" in vary else torch.full_like(ds, 127)
+    ws = (ws.to(torch.int32) + torch.randint(-4, 5, ws.shape, generator=gen)).clamp(100, 150).to(torch.uint8) \
+        if "b" in vary else torch.full_like(ws, 127)
+    return dq, ds, wq, ws, np.asarray(gs, np.int32)
+
+
+def run_dgrad(dq, ds, wq, ws, gs, tile_n=0):
+    m, n = dq.shape
+    g, k, _ = wq.shape
+    plan = gg.Plan(m, k, n, g, "grad_input_mxfp8", "e4m3", "bf16", tile_n=tile_n)
+    if tile_n:
+        assert plan.info["tile_n"] == tile_n
+    wsp = torch.zeros(gg.rdot_workspace_size(plan.handle), dtype=torch.uint8, device=DEV)
+    out = torch.full((m, k), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gg.rdot_grad_input_mxfp8(plan.handle, dq.to(DEV), ds.to(DEV), wq.to(DEV), ws.to(DEV),
+                             torch.from_numpy(gs).to(DEV), out, wsp)
+    return out, gg.rdot_read_status(plan.handle, wsp)
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("vary", [(), ("a",), ("b",), ("a", "b")])
+def test_mxfp8_dgrad_scale_axes(vary, tile_n):
+    dq, ds, wq, ws, gs = make_dgrad_case(512, 512, 256, [256, 256], 7, vary)
+    out, status = run_dgrad(dq, ds, wq, ws, gs, tile_n)
+    ref = oracle.grad_input_mxfp8(dq, ds, wq, ws, gs)
+    assert status == 0
+    assert rel_err(out, ref) <= TOL
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("m,k,n,gs", [
+    (300, 128, 128, [300]),
+    (420, 144, 96, [130, 0, 77, 200, 5]),          # contraction 96 (3 scale blocks), output 144
+    (512, 256, 32, [0, 256, 256, 0]),              # contraction 32
+    (1000, 384, 512, [0, 313, 1, 0, 257, 300, 129]),
+])
+def test_mxfp8_dgrad_ragged_parity(m, k, n, gs, tile_n):
+    dq, ds, wq, ws, gs = make_dgrad_case(m, k, n, gs, 19)
+    total = int(gs.sum())
+    dq[total:] = 0x7F                              # E4M3 NaN codes past the sum must never leak
+    out, status = run_dgrad(dq, ds, wq, ws, gs, tile_n)
+    ref = oracle.grad_input_mxfp8(dq, ds, wq, ws, gs)
+    assert status == 0
+    assert rel_err(out, ref) <= TOL
+    assert cosine_to_rounded(out, ref) >= COSINE_MIN
+    assert torch.all(out[total:] == 0)
+
+
+def test_mxfp8_dgrad_max_groups():
+    rng = np.random.default_rng(95)
+    g = 1024
+    gs = rng.integers(0, 4, size=g).astype(np.int32)
+    gs[11] = 300
+    dq, ds, wq, ws, gs = make_dgrad_case(int(gs.sum()), 256, 128, gs, 96)
+    out, status = run_dgrad(dq, ds, wq, ws, gs)
+    assert status == 0
+    assert rel_err(out, oracle.grad_input_mxfp8(dq, ds, wq, ws, gs)) <= TOL
