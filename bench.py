@@ -607,6 +607,25 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                    flags=gg.RDOT_FLAG_NO_CTA_PAIR if plan.info["tile_m"] == 256 else gg.RDOT_FLAG_CTA_PAIR)
     t3 = _time_steps(lambda: gg.rdot_forward_mxfp8(pair.handle, aq, as_, bq, bs, gs_d, out, pair.workspace, stream),
                      steps, stream)
+    # the data gradient on MXFP8 operands at the same size: dy [M, N] x w [G, K, N] -> [M, K]
+    dyf = ri.device_normal((m, n), 3000, 1.0, dev, torch.float32)
+    dq, dsc = ri.quantize_mx_e4m3(dyf, axis=1)
+    del dyf
+    wf = ri.device_normal((g, k, n), 2000, 0.02, dev, torch.float32)
+    wq, wsc = ri.quantize_mx_e4m3(wf, axis=2)
+    del wf
+    torch.cuda.empty_cache()
+    dplan = gg.Plan(m, k, n, g, "grad_input_mxfp8", "e4m3", "bf16", device=dev.index)
+    dws = torch.zeros(gg.rdot_workspace_size(dplan.handle), dtype=torch.uint8, device=dev)
+    dout = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
+    t4 = _time_steps(lambda: gg.rdot_grad_input_mxfp8(dplan.handle, dq, dsc, wq, wsc, gs_d, dout, dws, stream),
+                     steps, stream)
+    res["mxfp8_dgrad"] = {"workload": f"dy [{m}, {n}] x w [{g}, {k}, {n}] -> [{m}, {k}], scales along {n}",
+                          "tflops": round(fl / t4 / 1e12, 3), "ms": round(t4 * 1e3, 4),
+                          "frac_of_fp8_peak": round(fl / t4 / 1e12 / fp8_peak, 4),
+                          "status": gg.rdot_read_status(dplan.handle, dws),
+                          "tile": f"{dplan.info['tile_m']}x{dplan.info['tile_n']}"}
+    del dq, dsc, wq, wsc, dout, dws
     res["mxfp8"]["other_pairing"] = {"tile": f"{pair.info['tile_m']}x{pair.info['tile_n']}",
                                      "tflops": round(fl / t3 / 1e12, 3), "ms": round(t3 * 1e3, 4),
                                      "status": pair.status()}
