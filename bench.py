@@ -521,6 +521,30 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                             "status": plan.status(), "tile": "256x128 (x2 accumulators: w0, w1)"}
     del x, rhs0, rhs1, hout
     torch.cuda.empty_cache()
+    # a whole Mixtral-like expert layer on the library: permute -> gated up projection -> down
+    # projection -> weighted un-permute (8192 tokens, top-2 of 8, 4096 -> 14336 -> 4096)
+    t_l, k_l = m // 2, 2
+    rng = np.random.default_rng(1)
+    ids_l = torch.from_numpy(np.argsort(-rng.standard_normal((t_l, g)), axis=1)[:, :k_l].astype(np.int32)).to(dev)
+    wr_l = torch.rand((t_l, k_l), device=dev)
+    x_l = ri.device_normal((t_l, k), 5000, 1.0, dev, torch.bfloat16)
+    w0_l = ri.device_normal((g, k, n), 5001, 0.02, dev, torch.bfloat16)
+    w1_l = ri.device_normal((g, k, n), 5002, 0.02, dev, torch.bfloat16)
+    wo_l = ri.device_normal((g, n, k), 5003, 0.02, dev, torch.bfloat16)
+
+    def layer():
+        xs_l, gs_l, _, inv_l = gg.moe_permute(ids_l, x_l, g, stream)
+        h_l = gg.ragged_dot_gated(xs_l, w0_l, w1_l, gs_l, stream=stream)
+        y_l = gg.ragged_dot(h_l, wo_l, gs_l, stream=stream)
+        return gg.moe_unpermute(y_l, inv_l, wr_l, stream=stream)
+    tl = _time_steps(layer, max(5, steps // 3), stream)
+    fl_l = 3.0 * 2.0 * t_l * k_l * k * n
+    res["moe_layer"] = {"workload": f"{t_l} tokens top-{k_l} of {g}: permute, gated up {k}->{n}, down {n}->{k}, "
+                                    "un-permute", "ms": round(tl * 1e3, 4), "tflops": round(fl_l / tl / 1e12, 3),
+                        "frac_of_bf16_peak": round(fl_l / tl / 1e12 / peaks["bf16_tflops"], 4),
+                        "launches_per_layer": 4 + 1 + 1 + 1}
+    del x_l, w0_l, w1_l, wo_l
+    torch.cuda.empty_cache()
     # MoE permute / un-permute around the Mixtral-like layer: 8192 tokens, top-2 of 8, width 4096
     t, k, e, width = m // 2, 2, g, cfg["k"]
     rng = np.random.default_rng(0)

@@ -123,3 +123,71 @@ def test_no_tokens_and_all_dropped():
                            torch.ones((5, 2), device=DEV))
     torch.cuda.synchronize()
     assert torch.all(out == 0)
+
+
+def _layer(x, ids, w_route, w0, w1, wo, e, stream=None):
+    """One MoE expert layer on the library: permute -> gated up projection -> down projection ->
+    weighted un-permute."""
+    xs, gs, order, inv = gg.moe_permute(ids, x, e, stream)
+    h = gg.ragged_dot_gated(xs, w0, w1, gs, stream=stream)
+    y = gg.ragged_dot(h, wo, gs, stream=stream)
+    return gg.moe_unpermute(y, inv, w_route, stream=stream)
+
+
+def _layer_ref(x, ids, w_route, w0, w1, wo, e):
+    xd, w0d, w1d, wod = (t.double().cpu().numpy() for t in (x, w0, w1, wo))
+    t, k = ids.shape
+    out = np.zeros((t, wod.shape[2]))
+    for tt in range(t):
+        for j in range(k):
+            g = ids[tt, j]
+            if 0 <= g < e:
+                z0, z1 = xd[tt] @ w0d[g], xd[tt] @ w1d[g]
+                h = torch.from_numpy(z0 / (1.0 + np.exp(-z0)) * z1).to(torch.bfloat16).double().numpy()
+                y = torch.from_numpy(h @ wod[g]).to(torch.bfloat16).double().numpy()
+                out[tt] += w_route[tt, j] * y
+    return out
+
+
+def test_moe_layer_with_gated_up_and_down_projection():
+    """The whole expert layer against the dense definition. The layer keeps its intermediates in
+    bf16 (the activated hidden rows and the down projection's rows), so the reference rounds
+    them the same way (round to nearest even) before the next step."""
+    t, k, e, d, f = 300, 2, 4, 128, 256
+    ids = routed_ids(t, k, e, 72, 0.02)
+    w_route = np.random.default_rng(73).random((t, k)).astype(np.float32)
+    x = torch.from_numpy(ri.host_normal((t, d), 74)).to(torch.bfloat16)
+    w0 = torch.from_numpy(ri.host_normal((e, d, f), 75, 0.1)).to(torch.bfloat16)
+    w1 = torch.from_numpy(ri.host_normal((e, d, f), 76, 0.1)).to(torch.bfloat16)
+    wo = torch.from_numpy(ri.host_normal((e, f, d), 77, 0.1)).to(torch.bfloat16)
+    out = _layer(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(w_route).to(DEV), w0.to(DEV),
+                 w1.to(DEV), wo.to(DEV), e)
+    torch.cuda.synchronize()
+    assert rel_err(out, _layer_ref(x, ids, w_route, w0, w1, wo, e)) <= TOL
+
+
+def test_moe_layer_cuda_graph_replay_with_new_routing():
+    """Every step of the layer runs on the device with no host synchronisation, so a captured
+    graph replays correctly when only the routing (ids and weights) changes."""
+    t, k, e, d, f = 256, 2, 4, 128, 128
+    w0 = torch.from_numpy(ri.host_normal((e, d, f), 78, 0.1)).to(torch.bfloat16).to(DEV)
+    w1 = torch.from_numpy(ri.host_normal((e, d, f), 79, 0.1)).to(torch.bfloat16).to(DEV)
+    wo = torch.from_numpy(ri.host_normal((e, f, d), 80, 0.1)).to(torch.bfloat16).to(DEV)
+    x = torch.from_numpy(ri.host_normal((t, d), 81)).to(torch.bfloat16).to(DEV)
+    ids_d = torch.from_numpy(routed_ids(t, k, e, 82)).to(DEV)
+    wr_d = torch.rand((t, k), device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        _layer(x, ids_d, wr_d, w0, w1, wo, e, s)            # plans and tensor maps made outside capture
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        out = _layer(x, ids_d, wr_d, w0, w1, wo, e, s)
+    for seed in (83, 84):
+        ids = routed_ids(t, k, e, seed, 0.05)
+        w_route = np.random.default_rng(seed).random((t, k)).astype(np.float32)
+        ids_d.copy_(torch.from_numpy(ids))
+        wr_d.copy_(torch.from_numpy(w_route))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert rel_err(out, _layer_ref(x.cpu(), ids, w_route, w0.cpu(), w1.cpu(), wo.cpu(), e)) <= TOL
