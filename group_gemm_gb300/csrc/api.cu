@@ -603,7 +603,8 @@ rdot_status rdot_grad_input_mxfp8(rdot_plan_t plan, const void* dy_q, const uint
     a.m_inner = plan->m_inner;
     a.sfa = ws + l.sfa_off;
     a.sfb = ws + l.sfb_off;
-    a.sfb_vec = 0;
+    // the weight scales are read as 32-bit words along N when every row of them is word-aligned
+    a.sfb_vec = (p.n % 128 == 0 && (reinterpret_cast<uintptr_t>(w_scale) & 3u) == 0) ? 1 : 0;
     a.sfa_vec = (p.n % 128 == 0 && (reinterpret_cast<uintptr_t>(dy_scale) & 3u) == 0) ? 1 : 0;
     a.b_kmajor = 1;
     a.status = static_cast<int32_t*>(workspace);

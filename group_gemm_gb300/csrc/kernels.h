@@ -103,7 +103,8 @@ struct MxArgs {
     int m_inner;
     uint8_t* sfa;                // workspace: reordered lhs scales, [m-tiles, KS] blocks
     uint8_t* sfb;                // workspace: reordered rhs scales, [G, NT, KS] blocks of BN/128 atoms
-    int sfb_vec;                 // rhs_scale rows can be read as 32-bit words (N % 4 == 0, aligned)
+    int sfb_vec;                 // rhs_scale can be read as 32-bit words (forward: N % 4 == 0; data
+                                 // gradient: K % 128 == 0; aligned)
     int sfa_vec;                 // lhs_scale rows can be read as 32-bit words (K % 128 == 0, aligned)
     int pair;                    // 1: 256-row tiles on CTA pairs (sfa blocks per 128-row half)
     int b_kmajor;                // 1: the data gradient -- B codes [G, N out, K] with K contiguous and

@@ -141,8 +141,11 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
                     const int r = lane + 32 * i;
                     const int nrow = nt * 128 + r;
                     w[i] = 0x7f7f7f7fu;
-                    if (nrow < a.N)
-                        w[i] = scale_word(rhs_scale + (static_cast<long long>(g) * a.N + nrow) * KB32 + 4 * ks, avail);
+                    if (nrow < a.N) {
+                        const uint8_t* src = rhs_scale + (static_cast<long long>(g) * a.N + nrow) * KB32 + 4 * ks;
+                        w[i] = (a.sfb_vec && avail == 4) ? __ldg(reinterpret_cast<const uint32_t*>(src))
+                                                         : scale_word(src, avail);
+                    }
                 }
                 reinterpret_cast<uint4*>(dst)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
                 continue;
