@@ -373,6 +373,33 @@ def _time_steps(fn, steps, stream):
     return time_region(fn, steps, stream, lambda: None) / steps
 
 
+def _time_graph(fn, dev, calls=20, replays=5):
+    """Device time of one call of fn(stream): `calls` calls captured in a CUDA graph on a side
+    stream, replayed `replays` times between CUDA events (no host launch cost in the region)."""
+    import torch
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(calls):
+            fn(side)
+    cur = torch.cuda.current_stream(dev)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(cur)
+    for _ in range(replays):
+        g.replay()
+    b.record(cur)
+    torch.cuda.synchronize(dev)
+    del g
+    return a.elapsed_time(b) / 1e3 / (calls * replays)
+
+
 def measure_fp8_peak(dev, n=8192, reps=10):
     """Dense FP8 tensor-core throughput on this GPU: cuBLAS E4M3 x E4M3 -> bf16 GEMM (n^3, unit
     tensorwise scales) through torch._scaled_mm, best of `reps` after warm-up. The block-scaled
@@ -556,17 +583,23 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
     order = torch.empty(t * k, dtype=torch.int32, device=dev)
     inv = torch.empty(t * k, dtype=torch.int32, device=dev)
     ws = torch.empty(gg.rdot_moe_route_workspace_size(t, k, e), dtype=torch.uint8, device=dev)
-    tp = _time_steps(lambda: gg.rdot_moe_permute(ids, x, e, gsz, order, inv, xs, ws, stream), steps, stream)
+    tp_loop = _time_steps(lambda: gg.rdot_moe_permute(ids, x, e, gsz, order, inv, xs, ws, stream), steps, stream)
+    tp = _time_graph(lambda st: gg.rdot_moe_permute(ids, x, e, gsz, order, inv, xs, ws, st), dev)
     wr = torch.rand((t, k), device=dev)
     outc = torch.empty((t, width), dtype=torch.bfloat16, device=dev)
-    tc = _time_steps(lambda: gg.rdot_moe_unpermute(xs, inv, wr, outc, stream), steps, stream)
+    tc_loop = _time_steps(lambda: gg.rdot_moe_unpermute(xs, inv, wr, outc, stream), steps, stream)
+    tc = _time_graph(lambda st: gg.rdot_moe_unpermute(xs, inv, wr, outc, st), dev)
     perm_bytes = t * width * 2 + t * k * width * 2 + t * k * 4 * 3 + e * 4      # x once, x_sorted, ids/order/inv
     comb_bytes = t * k * width * 2 + t * width * 2 + t * k * 8                  # y_sorted, out, inv + weights
     res["moe_route"] = {"workload": f"{t} tokens, top-{k} of {e} experts, rows of {width} bf16",
+                        "timing": "device time per call from CUDA-graph replays of 20 calls; *_python_loop: "
+                                  "one Python call per step, host launch cost included",
                         "permute_ms": round(tp * 1e3, 4), "permute_gbs_algorithmic": round(perm_bytes / tp / 1e9, 1),
                         "permute_frac_of_hbm": round(perm_bytes / tp / 1e9 / peaks["hbm_gbs"], 4),
+                        "permute_ms_python_loop": round(tp_loop * 1e3, 4),
                         "unpermute_ms": round(tc * 1e3, 4), "unpermute_gbs_algorithmic": round(comb_bytes / tc / 1e9, 1),
-                        "unpermute_frac_of_hbm": round(comb_bytes / tc / 1e9 / peaks["hbm_gbs"], 4)}
+                        "unpermute_frac_of_hbm": round(comb_bytes / tc / 1e9 / peaks["hbm_gbs"], 4),
+                        "unpermute_ms_python_loop": round(tc_loop * 1e3, 4)}
     del x, xs, outc, ws
     torch.cuda.empty_cache()
     # weight gradient

@@ -16,7 +16,8 @@
 //                     the group's last lane advances the expert's running position -- the order
 //                     of equal keys is the flat order, as the stable sort defines it.
 // The gather (one warp per token: its row read once, its k copies written) and the combine (one
-// warp per token: its k copies read, one row written) are HBM-bound, in 16-byte vectors.
+// warp per token: its k copies read, one row written) are HBM-bound, in 16-byte vectors with
+// four loads in flight per lane.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -27,6 +28,7 @@ namespace rdot {
 namespace {
 
 constexpr int CHUNK = 512;   // copies per counting-sort chunk (one warp)
+constexpr int VEC_UNROLL = 4;   // 16-byte loads in flight per lane (gather, combine)
 
 __global__ void __launch_bounds__(32) moe_count_kernel(const int32_t* __restrict__ ids, long long total, int E,
                                                        int32_t* __restrict__ chunk_hist) {
@@ -148,11 +150,18 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     for (long long t = warp; t < tokens; t += nwarps) {
         const uint4* src = x + t * vec_per_row;
-        for (int i = lane; i < vec_per_row; i += 32) {
-            const uint4 v = __ldg(src + i);
+        for (int i0 = lane; i0 < vec_per_row; i0 += 32 * VEC_UNROLL) {
+            uint4 v[VEC_UNROLL];
+#pragma unroll
+            for (int u = 0; u < VEC_UNROLL; ++u)
+                if (i0 + 32 * u < vec_per_row) v[u] = __ldg(src + i0 + 32 * u);
             for (int j = 0; j < k; ++j) {
                 const int32_t p = __ldg(inv + t * k + j);
-                if (p >= 0) x_sorted[static_cast<long long>(p) * vec_per_row + i] = v;
+                if (p < 0) continue;
+                uint4* dst = x_sorted + static_cast<long long>(p) * vec_per_row + i0;
+#pragma unroll
+                for (int u = 0; u < VEC_UNROLL; ++u)
+                    if (i0 + 32 * u < vec_per_row) dst[32 * u] = v[u];
             }
         }
     }
@@ -182,20 +191,35 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restric
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
     for (long long t = warp; t < tokens; t += nwarps) {
-#pragma unroll 4
-        for (int i = lane; i < vec_per_row; i += 32) {
-            float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int i0 = lane; i0 < vec_per_row; i0 += 32 * VEC_UNROLL) {
+            float a[VEC_UNROLL][8];
+#pragma unroll
+            for (int u = 0; u < VEC_UNROLL; ++u)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) a[u][c] = 0.f;
             for (int j = 0; j < k; ++j) {
                 const int32_t p = __ldg(inv + t * k + j);
                 if (p < 0) continue;
-                acc_bf16x8(a, __ldg(y + static_cast<long long>(p) * vec_per_row + i), __ldg(w + t * k + j));
+                const float wj = __ldg(w + t * k + j);
+                const uint4* src = y + static_cast<long long>(p) * vec_per_row + i0;
+                uint4 v[VEC_UNROLL];
+#pragma unroll
+                for (int u = 0; u < VEC_UNROLL; ++u)
+                    if (i0 + 32 * u < vec_per_row) v[u] = __ldg(src + 32 * u);
+#pragma unroll
+                for (int u = 0; u < VEC_UNROLL; ++u)
+                    if (i0 + 32 * u < vec_per_row) acc_bf16x8(a[u], v[u], wj);
             }
-            uint4 o;
-            o.x = pack_bf16x2(a[0], a[1]);
-            o.y = pack_bf16x2(a[2], a[3]);
-            o.z = pack_bf16x2(a[4], a[5]);
-            o.w = pack_bf16x2(a[6], a[7]);
-            out[t * vec_per_row + i] = o;
+#pragma unroll
+            for (int u = 0; u < VEC_UNROLL; ++u) {
+                if (i0 + 32 * u >= vec_per_row) continue;
+                uint4 o;
+                o.x = pack_bf16x2(a[u][0], a[u][1]);
+                o.y = pack_bf16x2(a[u][2], a[u][3]);
+                o.z = pack_bf16x2(a[u][4], a[u][5]);
+                o.w = pack_bf16x2(a[u][6], a[u][7]);
+                out[t * vec_per_row + i0 + 32 * u] = o;
+            }
         }
     }
 }

@@ -43,6 +43,9 @@ def routed_ids(t, k, e, seed, drop=0.0):
     (5000, 8, 256, 128, 0.05),      # DeepSeek-like top-8 of 256, some copies dropped
     (777, 1, 1, 32, 0.0),           # one expert
     (2049, 4, 1024, 64, 0.1),       # the largest expert count, chunk boundary + 1
+    (301, 2, 8, 1600, 0.0),         # 200 vectors a row: the last of four in-flight loads ragged
+    (40000, 4, 64, 16, 0.02),       # 313 chunks of 512 copies, the last one partial
+    (33000, 8, 1024, 24, 0.05),     # 516 chunks with the largest expert count
 ])
 def test_permute_matches_oracle_bit_for_bit(t, k, e, width, drop):
     ids = routed_ids(t, k, e, 61 + t, drop)
@@ -60,7 +63,7 @@ def test_permute_matches_oracle_bit_for_bit(t, k, e, width, drop):
     assert torch.all(xs_h[v:] == 0)
 
 
-@pytest.mark.parametrize("t,k,n", [(1000, 2, 64), (513, 8, 256), (7, 3, 8)])
+@pytest.mark.parametrize("t,k,n", [(1000, 2, 64), (513, 8, 256), (7, 3, 8), (300, 2, 1600)])
 def test_unpermute_matches_oracle(t, k, n):
     rng = np.random.default_rng(63)
     ids = routed_ids(t, k, 16, 64, 0.05)
