@@ -401,34 +401,46 @@ def _time_graph(fn, dev, calls=20, replays=5):
 
 
 def measure_fp8_peak(dev, n=8192, reps=10):
-    """Dense FP8 tensor-core throughput on this GPU: cuBLAS E4M3 x E4M3 -> bf16 GEMM (n^3, unit
-    tensorwise scales) through torch._scaled_mm, best of `reps` after warm-up. The block-scaled
-    MMA of the MXFP8 path issues at the same rate as plain FP8, so this is its peak. Returns
-    TFLOP/s, or None where torch or cuBLAS does not offer the call."""
+    """Dense FP8 tensor-core throughput on this GPU through torch._scaled_mm (E4M3 x E4M3 -> bf16,
+    n^3, best of `reps` after warm-up): cuBLAS's MXFP8 GEMM (E8M0 scales, one per 32 elements of
+    K: the block-scaled MMA the MXFP8 path issues) where torch offers it, else the GEMM with
+    unit tensorwise scales. Returns (TFLOP/s, kind), or (None, None) where neither call works."""
     import torch
     try:
         a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
         b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()      # column-major operand
-        one = torch.ones((), device=dev, dtype=torch.float32)
-
-        def run():
-            return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
-        for _ in range(3):
-            run()
-        torch.cuda.synchronize(dev)
-        best = float("inf")
-        for _ in range(reps):
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record()
-            run()
-            e.record()
-            e.synchronize()
-            best = min(best, s.elapsed_time(e) / 1e3)
-        del a, b
-        torch.cuda.empty_cache()
-        return 2.0 * n ** 3 / best / 1e12
     except Exception:
-        return None
+        return None, None
+    one = torch.ones((), device=dev, dtype=torch.float32)
+    forms = []
+    e8m0 = getattr(torch, "float8_e8m0fnu", None)
+    if e8m0 is not None:
+        sc = torch.full((n * (n // 32),), 127, dtype=torch.uint8, device=dev).view(e8m0)   # 2^0 everywhere
+        forms.append(("cuBLAS MXFP8 GEMM (E8M0 block scales)", sc, sc))
+    forms.append(("cuBLAS E4M3 GEMM (tensorwise scales)", one, one))
+    result = (None, None)
+    for kind, sa, sb in forms:
+        try:
+            def run():
+                return torch._scaled_mm(a, b, scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+            for _ in range(3):
+                run()
+            torch.cuda.synchronize(dev)
+            best = float("inf")
+            for _ in range(reps):
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record()
+                run()
+                e.record()
+                e.synchronize()
+                best = min(best, s.elapsed_time(e) / 1e3)
+            result = (2.0 * n ** 3 / best / 1e12, f"measured here: {kind} {n}^3, best of {reps}")
+            break
+        except Exception:
+            continue
+    del a, b
+    torch.cuda.empty_cache()
+    return result
 
 
 def extra_configs(args, dev, peaks, main_name, main_step_s):
@@ -644,13 +656,13 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
     t = _time_steps(lambda: gg.rdot_forward_mxfp8(plan.handle, aq, as_, bq, bs, gs_d, out, plan.workspace, stream),
                     steps, stream)
     fl = useful_flops(gs, k, n)
-    fp8_measured = measure_fp8_peak(dev)
+    fp8_measured, fp8_kind = measure_fp8_peak(dev)
     fp8_peak = fp8_measured if fp8_measured else 2.0 * peaks["bf16_tflops"]
     min_bytes = m * k + g * k * n + (m * k + g * k * n) // 32 + 2 * m * n
     res["mxfp8"] = {"tflops": round(fl / t / 1e12, 3), "ms": round(t * 1e3, 4),
                     "frac_of_fp8_peak": round(fl / t / 1e12 / fp8_peak, 4),
                     "fp8_peak_tflops": round(fp8_peak, 1),
-                    "fp8_peak_kind": ("measured here: cuBLAS E4M3 GEMM 8192^3, best of 10" if fp8_measured
+                    "fp8_peak_kind": (fp8_kind if fp8_measured
                                       else "not measurable here; taken as 2x the measured bf16 burst peak"),
                     "hbm_gbs_algorithmic": round(min_bytes / t / 1e9, 1), "status": plan.status(),
                     "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}"}
