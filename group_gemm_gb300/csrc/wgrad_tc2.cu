@@ -13,6 +13,9 @@
 //   - The even CTA issues M=256 N=256 K=16 MMAs; commits multicast "stage free" and
 //     "accumulator full" to both CTAs; each CTA's epilogue stores its 128 rows of dw[g] and arrives
 //     on the even CTA's "accumulator empty" barrier.
+//   - A last column tile with at most 128 columns left before N runs N=128 MMAs: CTA r stages
+//     dy columns [n0 + 64 r, +64), so no MMA work goes to columns past N (the 1408-wide dy of the
+//     suite ends in such a tile). Accumulator column c is dw column n0 + c in both widths.
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -124,9 +127,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const int nchunks = (t.rows + ROWS - 1) / ROWS;
                 // 64-wide chunks of each CTA's halves that are not wholly past K or N
                 const int kb0 = t.kt * BM, nb0 = t.nt * BN;
+                const bool narrow = a.N - nb0 <= BN / 2;   // N=128 MMAs: 64 columns per CTA
                 const int ac0 = max(0, min(2, (a.K - kb0 + 63) / 64)), ac1 = max(0, min(2, (a.K - kb0 - 128 + 63) / 64));
-                const int bc0 = max(0, min(2, (a.N - nb0 + 63) / 64)), bc1 = max(0, min(2, (a.N - nb0 - 128 + 63) / 64));
-                const int k0 = kb0 + 128 * static_cast<int>(rank), n0 = nb0 + 128 * static_cast<int>(rank);
+                const int bc0 = narrow ? 1 : max(0, min(2, (a.N - nb0 + 63) / 64));
+                const int bc1 = narrow ? (nb0 + 64 < a.N ? 1 : 0) : max(0, min(2, (a.N - nb0 - 128 + 63) / 64));
+                const int k0 = kb0 + 128 * static_cast<int>(rank);
+                const int n0 = nb0 + (narrow ? 64 : 128) * static_cast<int>(rank);
                 const int ac = rank ? ac1 : ac0, bc = rank ? bc1 : bc0;
                 // a last chunk that runs past the group's end loads through the group's maps,
                 // whose row extent ends there: the copy engine fills those rows with zeros
@@ -181,7 +187,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issue (even CTA only)
         if (leader) {
-            constexpr uint32_t idesc = idesc_f16(BM, BN, true, true, true, true);
+            constexpr uint32_t idesc_wide = idesc_f16(BM, BN, true, true, true, true);
+            constexpr uint32_t idesc_narrow = idesc_f16(BM, BN / 2, true, true, true, true);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int w = cluster; w < W && ok; w += nclusters) {
@@ -192,6 +199,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (!free_acc) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
+                const uint32_t idesc = a.N - t.nt * BN <= BN / 2 ? idesc_narrow : idesc_wide;
                 for (int c = 0; c < nchunks; ++c) {
                     const bool landed = mbar_wait_warp(&full[stage], phase, guard);
                     if (!landed) {

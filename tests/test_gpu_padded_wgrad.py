@@ -83,6 +83,9 @@ WG_CASES = [
     (256, 64, 64, [256]),                            # G = 1
     (130, 512, 1408, [40, 90]),                      # wgrad widths of the suite
     (1200, 256, 256, [129, 255, 256, 257, 191, 100]),  # tails of 128-row stages (pair kernel)
+    (400, 96, 360, [150, 0, 250]),                   # a 104-column last tile: N=128 pair MMAs, the odd
+                                                     # CTA's 64 columns cut at N
+    (300, 128, 296, [120, 180]),                     # a 40-column last tile: the odd CTA stages nothing
 ]
 
 
