@@ -13,6 +13,12 @@
 //     CTAs ("stage free" and "accumulator full").
 //   - Each CTA's four epilogue warps drain its 128 accumulator rows exactly as in fwd_tc.cu and
 //     arrive on the even CTA's "accumulator empty" barrier (one arrival per warp, 8 in all).
+//   - Half tiles: a tile with at most 128 rows of its group left (a group's last tile) runs
+//     M = 128 MMAs at half the cost of M = 256 ones. CTA r then stages rows [row0 + 64 r, +64) at
+//     the top of its A buffer, and its tensor memory holds those 64 rows twice over in 128 columns:
+//     lanes [0, 64) with output columns [n0, n0 + 128), lanes [64, 128) with [n0 + 128, n0 + 256).
+//     The forward and the data gradient use them; the gated projection, whose epilogue pairs column
+//     c with column c + 128 of the same row, keeps 256-row tiles.
 // Per SM, a stage carries 32 KB for 128 x 256 x 64 multiply-adds instead of 48 KB with one-CTA
 // tiles: the ring covers half again as much MMA time and L2 serves a third fewer bytes.
 #include <cuda_bf16.h>
@@ -114,9 +120,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
                 constexpr bool gated = VAR == 2;
                 const int n0 = t.nt * (gated ? BN / 2 : BN);
+                const int a_rows = (!gated && t.rows <= 128) ? 64 : 128;   // A rows per CTA (half tile: 64)
                 // bytes each CTA brings in: its A half unless it lies wholly past M, and the
                 // 64-column chunks of its B half that are not wholly past N
-                const int a0 = A_BYTES, a1 = (t.row0 + 128 < a.M) ? A_BYTES : 0;
+                const int a0 = A_BYTES, a1 = (t.row0 + a_rows < a.M) ? A_BYTES : 0;
                 // (K-major B, the data gradient: one 128-row box per CTA, or none past N; gated:
                 // both CTAs load the same 128 columns, of w0 and of w1)
                 constexpr bool kmaj = VAR == 1;
@@ -136,7 +143,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     uint8_t* sb = sa + A_BYTES;
                     if (leader) mbar_arrive_expect_tx(&full[stage], a0 + a1 + (c0 + c1) * B_CHUNK_BYTES);
                     const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-                    if (my_a) tma_load_2d_pair(sa, &tmap_a, fb, kb * TC_BK, t.row0 + 128 * static_cast<int>(rank));
+                    if (my_a) tma_load_2d_pair(sa, &tmap_a, fb, kb * TC_BK, t.row0 + a_rows * static_cast<int>(rank));
                     if (kmaj) {
                         if (my_c) tma_load_3d_pair(sb, map_b, fb, kb * TC_BK, b_col, t.g);
                     } else {
@@ -174,11 +181,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && leader) {
             constexpr bool kmaj = VAR == 1;
-            const uint32_t idesc = kmaj ? idesc_f16(BM, BN, true, true, false, false)
-                                        : idesc_f16(BM, BN, true, true, false, true);
+            constexpr uint32_t idesc_full = idesc_f16(BM, BN, true, true, false, !kmaj);
+            constexpr uint32_t idesc_half = idesc_f16(BM / 2, BN, true, true, false, !kmaj);
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int w = cluster; w < W && ok; w += nclusters) {
+                const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
+                const uint32_t idesc = (VAR != 2 && t.rows <= 128) ? idesc_half : idesc_full;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1, guard)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * BN;
@@ -251,6 +260,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         store_block_32x32<OUT_F32>(z0, stage_buf,
                                                    out_rows + static_cast<long long>(col) * (OUT_F32 ? 4 : 2), a.N,
                                                    rows_valid, a.N - col);
+                }
+            } else if (t.rows <= 128) {
+                // half tile: lane quarter q holds rows 64 r + 32 (q & 1) + lane of the tile and
+                // output columns n0 + 128 (q >> 1) + [0, 128) in tensor-memory columns [0, 128)
+                const int hfirst = 64 * static_cast<int>(rank) + 32 * (q & 1);
+                const int hrows = min(32, t.rows - hfirst);
+                const int hcol0 = n0 + 128 * (q >> 1);
+                uint8_t* hout = static_cast<uint8_t*>(a.out) +
+                                (static_cast<long long>(t.row0) + hfirst) * a.N * (OUT_F32 ? 4 : 2);
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    const int col = hcol0 + c * 32;
+                    if (hrows > 0 && col < a.N)
+                        store_block_32x32<OUT_F32>(v, stage_buf,
+                                                   hout + static_cast<long long>(col) * (OUT_F32 ? 4 : 2), a.N,
+                                                   hrows, a.N - col);
                 }
             } else {
 #pragma unroll 1

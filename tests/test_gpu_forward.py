@@ -162,7 +162,11 @@ def test_bf16_forward_parity(m, k, n, gs, out_dtype):
 
 
 @pytest.mark.parametrize("m,k,n,gs", BF16_CASES + [(1700, 320, 640, [700, 0, 129, 1, 512, 300]),
-                                              (2000, 256, 512, [257, 255, 256, 1, 1000, 0, 231])])
+                                              (2000, 256, 512, [257, 255, 256, 1, 1000, 0, 231]),
+                                              # last tiles of 64, 65, 127, 128 rows (M = 128 half
+                                              # tiles), 384 = 256 + 128, 320 = 256 + 64 (the odd
+                                              # CTA's rows all past the group), a 40-row tail at M
+                                              (1300, 192, 320, [64, 65, 127, 128, 384, 320, 172, 40])])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_bf16_forward_parity_cta_pairs(m, k, n, gs, out_dtype):
     """The 256 x 256 CTA-pair kernel (tcgen05 cta_group::2) on the same ragged cases, including

@@ -48,6 +48,7 @@ CASES = [
     (256, 64, 96, [17, 200, 39]),                  # output width 64 -> 128-wide tiles
     (1000, 768, 520, [0, 313, 1, 0, 257, 300, 129]),
     (2000, 512, 256, [257, 255, 256, 1, 1000, 0, 231]),
+    (1300, 320, 192, [64, 65, 127, 128, 384, 320, 172, 40]),   # 128-row pair tiles at every group end
 ]
 
 
