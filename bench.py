@@ -736,12 +736,15 @@ def bench_reference(args, rank, world):
         torch.cuda.empty_cache()
     else:
         gs = ri.config_group_sizes(name)
-        lhs_h = torch.from_numpy(ri.host_normal((cfg["m"], cfg["k"]), 1000, cfg["lhs"][1])).to(torch.bfloat16)
-        rhs_h = torch.from_numpy(ri.host_normal((cfg["g"], k, n), 2000, cfg["rhs"][1])).to(torch.bfloat16)
+        std_l = cfg["lhs"][1] if cfg["lhs"][0] == "normal" else 1.0
+        std_r = cfg["rhs"][1] if cfg["rhs"][0] == "normal" else 1.0
+        lhs_h = torch.from_numpy(ri.host_normal((cfg["m"], cfg["k"]), 1000, std_l)).to(torch.bfloat16)
+        rhs_h = torch.from_numpy(ri.host_normal((cfg["g"], k, n), 2000, std_r)).to(torch.bfloat16)
     import oracle
     oracle.build()
     cores = oracle.set_threads(0)
-    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    # seconds of oracle work per step: the whole run stays near 150 s (a test may ask for less)
+    per_step = getattr(args, "ref_step_seconds", None) or max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     rows_per_step = None
     for _ in range(args.warmup):
         v, _, _ = cpu_oracle_sample(name, gs, lhs_h, rhs_h, per_step)
