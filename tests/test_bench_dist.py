@@ -38,7 +38,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks_aggregate_max_time_and_total_units():
     world = 2
     port = _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()   # no fork: other tests may have started threads
     out = manager.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     for rank in range(world):
