@@ -1027,7 +1027,8 @@ rdot_status rdot_moe_permute(const int32_t* topk_ids, int64_t tokens, int32_t to
 rdot_status rdot_moe_unpermute(const void* y_sorted, const int32_t* inv, const float* topk_weights, int64_t tokens,
                                int32_t topk, int64_t n, void* out, void* stream) {
     if (tokens < 0 || topk < 1 || n < 1) return RDOT_ERR_INVALID_ARG;
-    if (n % 8 || tokens * static_cast<int64_t>(topk) > 0x7fffffffLL) return RDOT_ERR_UNSUPPORTED;
+    if (n % 8 || n / 8 > 0x7fffffffLL || tokens * static_cast<int64_t>(topk) > 0x7fffffffLL)
+        return RDOT_ERR_UNSUPPORTED;
     if (tokens == 0) return RDOT_OK;
     if (!y_sorted || !inv || !topk_weights || !out) return RDOT_ERR_INVALID_ARG;
     if (!aligned16(y_sorted) || !aligned16(out) || !aligned4(inv) || !aligned4(topk_weights)) return RDOT_ERR_INVALID_ARG;

@@ -226,7 +226,8 @@ RDOT_API rdot_status rdot_moe_permute(const int32_t* topk_ids, int64_t tokens, i
  *   y_sorted      device bf16 [T*k, n] (rows in rdot_moe_permute's order)
  *   inv           device int32 [T*k] (from rdot_moe_permute)
  *   topk_weights  device fp32 [T, k]
- *   out           device bf16 [T, n]; n % 8 == 0; 16-byte alignment for y_sorted and out. */
+ *   out           device bf16 [T, n]; n % 8 == 0, n / 8 < 2^31; 16-byte alignment for y_sorted and out.
+ * A width outside these bounds, or T*k >= 2^31, is RDOT_ERR_UNSUPPORTED. */
 RDOT_API rdot_status rdot_moe_unpermute(const void* y_sorted, const int32_t* inv, const float* topk_weights,
                                int64_t tokens, int32_t topk, int64_t n, void* out, void* stream);
 

@@ -88,4 +88,5 @@ def test_moe_route_argument_checks_without_gpu(lib):
     gs = ctypes.c_void_p(16)   # never dereferenced: the checks fail first
     assert lib.rdot_moe_permute(gs, 10, 2, 8, gs, 24, gs, gs, gs, gs, gs, None) == gg.RDOT_ERR_INVALID_ARG   # row_bytes % 16
     assert lib.rdot_moe_unpermute(gs, gs, gs, 10, 2, 12, gs, None) == gg.RDOT_ERR_UNSUPPORTED                 # n % 8
+    assert lib.rdot_moe_unpermute(gs, gs, gs, 10, 2, 1 << 40, gs, None) == gg.RDOT_ERR_UNSUPPORTED            # n / 8 >= 2^31
     assert lib.rdot_moe_unpermute(gs, gs, gs, -1, 2, 16, gs, None) == gg.RDOT_ERR_INVALID_ARG
