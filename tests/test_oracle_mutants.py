@@ -1,0 +1,233 @@
+"""Sensitivity of the oracle's pins (CPU only).
+
+Each group of pins is written here as a function of the implementation it checks and returns the
+pins that fail. The oracle passes all of them. Every planted mistake -- a plausible bug, built on
+the CPU around the oracle's own routines or restated with the bug in numpy -- fails at least one.
+A pin set that let one of these through would not pin that part of the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import _golden
+from tests.test_oracle_pins import _np_forward, _rel
+
+TOL = 1e-12
+
+
+def _check(name, predicate, fails):
+    try:
+        ok = bool(predicate())
+    except Exception:          # a shape error or a crash is a failed pin too
+        ok = False
+    if not ok:
+        fails.append(name)
+
+
+def _offsets(gs):
+    return np.concatenate([[0], np.cumsum(gs)]).astype(np.int64)
+
+
+# ----------------------------------------------------------------------------------- forward
+def forward_pin_failures(fwd):
+    fails = []
+    d = _golden.read("worked_example.txt")
+    gs_ex = d["group_sizes"].astype(np.int32)
+    _check("worked example", lambda: np.max(np.abs(fwd(d["lhs"], d["rhs"], gs_ex) - d["out"])) < 1e-14, fails)
+    rng = np.random.default_rng(71)
+    gs = np.array([3, 0, 4, 2], np.int32)
+    m, k = 12, 5                                   # three rows past the sum, an empty group, K == N
+    lhs, rhs = rng.standard_normal((m, k)), rng.standard_normal((4, k, k))
+    _check("brute force", lambda: _rel(fwd(lhs, rhs, gs), _np_forward(lhs, rhs, gs)) < TOL, fails)
+    _check("rows past the sum are zero", lambda: np.all(fwd(lhs, rhs, gs)[int(gs.sum()):] == 0), fails)
+    one = np.array([m], np.int32)
+    _check("G = 1 is a plain GEMM", lambda: _rel(fwd(lhs, rhs[:1], one), lhs @ rhs[0]) < TOL, fails)
+    return fails
+
+
+def _fwd_boundary_one_row_late(lhs, rhs, gs):
+    # the first row of each group is given to the group before it (searchsorted on the wrong side)
+    lhs, rhs = np.asarray(lhs, np.float64), np.asarray(rhs, np.float64)
+    ends = _offsets(gs)[1:]
+    out = np.zeros((lhs.shape[0], rhs.shape[2]))
+    for r in range(int(ends[-1])):
+        g = min(int(np.searchsorted(ends, r, side="left")), len(gs) - 1)
+        out[r] = lhs[r] @ rhs[g]
+    return out
+
+
+def _fwd_fp32_accumulation(lhs, rhs, gs):
+    lhs, rhs = np.asarray(lhs, np.float32), np.asarray(rhs, np.float32)
+    off = _offsets(gs)
+    out = np.zeros((lhs.shape[0], rhs.shape[2]), np.float32)
+    for g in range(len(gs)):
+        out[off[g]:off[g + 1]] = lhs[off[g]:off[g + 1]] @ rhs[g]
+    return out.astype(np.float64)
+
+
+FORWARD_MUTANTS = {
+    "the last K term dropped": lambda l, r, g: oracle.forward(np.asarray(l)[:, :-1], np.asarray(r)[:, :-1, :], g),
+    "sign flipped": lambda l, r, g: -oracle.forward(l, r, g),
+    "weights transposed": lambda l, r, g: oracle.forward(l, np.ascontiguousarray(np.asarray(r).transpose(0, 2, 1)), g),
+    "the next expert's weights": lambda l, r, g: oracle.forward(l, np.roll(np.asarray(r), -1, axis=0), g),
+    "group boundary one row late": _fwd_boundary_one_row_late,
+    "rows past the sum given to the last group":
+        lambda l, r, g: oracle.forward(l, r, np.append(g[:-1], g[-1] + np.asarray(l).shape[0] - g.sum()).astype(np.int32)),
+    "empty groups skipped when indexing experts":
+        lambda l, r, g: oracle.forward(l, np.asarray(r)[:int(np.count_nonzero(g))], g[g > 0].astype(np.int32)),
+    "fp32 accumulation": _fwd_fp32_accumulation,
+}
+
+
+def test_forward_pins_pass_on_the_oracle():
+    assert forward_pin_failures(oracle.forward) == []
+
+
+@pytest.mark.parametrize("name", list(FORWARD_MUTANTS))
+def test_forward_pins_catch_a_planted_mistake(name):
+    assert forward_pin_failures(FORWARD_MUTANTS[name]) != [], name
+
+
+# ------------------------------------------------------------------------------ grad-weight
+def grad_weight_pin_failures(gw):
+    fails = []
+    rng = np.random.default_rng(72)
+    gs = np.array([4, 0, 3, 5], np.int32)
+    m, k = 14, 4                                   # two rows past the sum, an empty group, K == N
+    lhs, dy = rng.standard_normal((m, k)), rng.standard_normal((m, k))
+    off = _offsets(gs)
+    ref = np.stack([lhs[off[g]:off[g + 1]].T @ dy[off[g]:off[g + 1]] for g in range(gs.size)])
+    _check("brute force", lambda: _rel(gw(lhs, dy, gs), ref) < TOL, fails)
+    _check("sum over the groups", lambda: _rel(gw(lhs, dy, gs).sum(0), lhs[:off[-1]].T @ dy[:off[-1]]) < TOL, fails)
+    _check("empty group is zero", lambda: np.all(gw(lhs, dy, gs)[1] == 0), fails)
+    return fails
+
+
+def _gw_one_row_past_the_end(lhs, dy, gs):
+    lhs, dy = np.asarray(lhs, np.float64), np.asarray(dy, np.float64)
+    off = _offsets(gs)
+    out = np.zeros((len(gs), lhs.shape[1], dy.shape[1]))
+    for g in range(len(gs)):
+        if gs[g] > 0:
+            e = min(int(off[g + 1]) + 1, lhs.shape[0])
+            out[g] = lhs[off[g]:e].T @ dy[off[g]:e]
+    return out
+
+
+GRAD_WEIGHT_MUTANTS = {
+    "dW transposed": lambda l, d, g: oracle.grad_weight(l, d, g).transpose(0, 2, 1),
+    "the next group's rows": lambda l, d, g: np.roll(oracle.grad_weight(l, d, g), -1, axis=0),
+    "one row past the group's end": _gw_one_row_past_the_end,
+}
+
+
+def test_grad_weight_pins_pass_on_the_oracle():
+    assert grad_weight_pin_failures(oracle.grad_weight) == []
+
+
+@pytest.mark.parametrize("name", list(GRAD_WEIGHT_MUTANTS))
+def test_grad_weight_pins_catch_a_planted_mistake(name):
+    assert grad_weight_pin_failures(GRAD_WEIGHT_MUTANTS[name]) != [], name
+
+
+# ----------------------------------------------------------------------------------- MXFP8
+def _torch_dequant(codes, scales, axis):
+    """E4M3 codes decoded by torch's float8_e4m3fn cast, times 2^(scale - 127) per 32 along axis."""
+    vals = torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+    return vals * np.repeat(np.exp2(np.asarray(scales, np.float64) - 127.0), 32, axis=axis)
+
+
+def mxfp8_pin_failures(fm):
+    fails = []
+    rng = np.random.default_rng(73)
+    gs = np.array([3, 0, 2], np.int32)
+    m, k, n = 6, 64, 3                              # two scale blocks along K, a row past the sum
+
+    def codes(shape):                               # any E4M3 code but the two NaNs
+        c = rng.integers(0, 0x7F, size=shape).astype(np.uint8)
+        return c | (rng.integers(0, 2, size=shape).astype(np.uint8) << 7)
+    lq, rq = codes((m, k)), codes((gs.size, k, n))
+    ls = rng.integers(118, 136, size=(m, k // 32)).astype(np.uint8)
+    rs = rng.integers(118, 136, size=(gs.size, k // 32, n)).astype(np.uint8)
+    ref = _np_forward(_torch_dequant(lq, ls, 1), _torch_dequant(rq, rs, 1), gs)
+    _check("brute force against torch's dequantisation", lambda: _rel(fm(lq, ls, rq, rs, gs), ref) < TOL, fails)
+    ones_l, ones_r = np.full_like(ls, 127), np.full_like(rs, 127)
+    plain = _np_forward(_torch_dequant(lq, ones_l, 1), _torch_dequant(rq, ones_r, 1), gs)
+    _check("unit scales = the plain FP8 product", lambda: _rel(fm(lq, ones_l, rq, ones_r, gs), plain) < TOL, fails)
+    return fails
+
+
+MXFP8_MUTANTS = {
+    "scales ignored": lambda lq, ls, rq, rs, g: oracle.forward_mxfp8(lq, np.full_like(ls, 127), rq,
+                                                                      np.full_like(rs, 127), g),
+    "scale blocks swapped along K": lambda lq, ls, rq, rs, g: oracle.forward_mxfp8(lq, np.roll(ls, 1, axis=1), rq,
+                                                                                    rs, g),
+    "E8M0 bias 126": lambda lq, ls, rq, rs, g: 2.0 * oracle.forward_mxfp8(lq, ls, rq, rs, g),
+}
+
+
+def test_mxfp8_pins_pass_on_the_oracle():
+    assert mxfp8_pin_failures(oracle.forward_mxfp8) == []
+
+
+@pytest.mark.parametrize("name", list(MXFP8_MUTANTS))
+def test_mxfp8_pins_catch_a_planted_mistake(name):
+    assert mxfp8_pin_failures(MXFP8_MUTANTS[name]) != [], name
+
+
+# ------------------------------------------------------------------------------ MoE permute
+def permute_pin_failures(perm):
+    fails = []
+    d = _golden.read("moe_route_example.txt")
+    x = np.arange(12, dtype=np.float64).reshape(3, 4)
+    ids = d["topk_ids"].astype(np.int64)
+
+    def golden():
+        gs, order, inv, _ = perm(ids, x, int(d["n_experts"][0]))
+        return (np.array_equal(gs, d["group_sizes"].astype(np.int32)) and
+                np.array_equal(order, d["order"].astype(np.int64)) and np.array_equal(inv, d["inv"].astype(np.int64)))
+    _check("worked example", golden, fails)
+    rng = np.random.default_rng(74)
+    t, k, e = 31, 3, 5
+    ids_r = rng.integers(-1, e + 1, size=(t, k))
+
+    def sort_invariants():
+        gs, order, inv, _ = perm(ids_r, np.zeros((t, 2)), e)
+        flat = ids_r.reshape(-1)
+        ex = flat[order]
+        same = np.diff(ex) == 0
+        return (np.array_equal(np.sort(order), np.nonzero((flat >= 0) & (flat < e))[0]) and np.all(np.diff(ex) >= 0)
+                and np.all(np.diff(order)[same] > 0)
+                and np.array_equal(gs, np.array([np.sum(flat == g) for g in range(e)], np.int32)))
+    _check("stable sort with bincount sizes", sort_invariants, fails)
+    return fails
+
+
+def _perm_ties_reversed(ids, x, e):
+    gs, order, inv, xs = oracle.moe_permute(ids, x, e)
+    flat = np.asarray(ids).reshape(-1)
+    key = flat[order]
+    order = order[np.lexsort((-order, key))]          # equal experts in reverse flat order
+    inv = np.full(flat.size, -1, np.int64)
+    inv[order] = np.arange(order.size)
+    return gs, order, inv, xs
+
+
+def _perm_counts_dropped(ids, x, e):
+    gs, order, inv, xs = oracle.moe_permute(ids, x, e)
+    flat = np.asarray(ids).reshape(-1)
+    return np.bincount(np.clip(flat, 0, e - 1), minlength=e).astype(np.int32), order, inv, xs
+
+
+PERMUTE_MUTANTS = {"ties in reverse flat order": _perm_ties_reversed,
+                   "dropped copies counted in the sizes": _perm_counts_dropped}
+
+
+def test_permute_pins_pass_on_the_oracle():
+    assert permute_pin_failures(oracle.moe_permute) == []
+
+
+@pytest.mark.parametrize("name", list(PERMUTE_MUTANTS))
+def test_permute_pins_catch_a_planted_mistake(name):
+    assert permute_pin_failures(PERMUTE_MUTANTS[name]) != [], name
