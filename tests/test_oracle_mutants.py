@@ -231,3 +231,163 @@ def test_permute_pins_pass_on_the_oracle():
 @pytest.mark.parametrize("name", list(PERMUTE_MUTANTS))
 def test_permute_pins_catch_a_planted_mistake(name):
     assert permute_pin_failures(PERMUTE_MUTANTS[name]) != [], name
+
+
+# ---------------------------------------------------------------------------- data gradient
+def grad_input_pin_failures(gi):
+    fails = []
+    rng = np.random.default_rng(75)
+    gs = np.array([3, 0, 4, 2], np.int32)
+    m, k = 11, 5                                   # two rows past the sum, an empty group, K == N
+    dy, w = rng.standard_normal((m, k)), rng.standard_normal((gs.size, k, k))
+    off = _offsets(gs)
+    ref = np.zeros((m, k))
+    for e in range(gs.size):
+        ref[off[e]:off[e + 1]] = dy[off[e]:off[e + 1]] @ w[e].T
+    _check("brute force", lambda: _rel(gi(dy, w, gs), ref) < TOL, fails)
+    x = rng.standard_normal((m, k))
+
+    def adjoint():
+        a = float(np.sum(oracle.forward(x, w, gs) * dy))
+        b = float(np.sum(x * gi(dy, w, gs)))
+        return abs(a - b) <= 1e-10 * (abs(a) + 1.0)
+    _check("adjoint of the forward", adjoint, fails)
+    return fails
+
+
+GRAD_INPUT_MUTANTS = {
+    "the forward instead of its transpose": lambda d, w, g: oracle.forward(d, w, g),
+    "the next expert's weights": lambda d, w, g: oracle.grad_input(d, np.roll(np.asarray(w), -1, axis=0), g),
+    "rows past the sum given to the last group":
+        lambda d, w, g: oracle.grad_input(d, w, np.append(g[:-1], g[-1] + np.asarray(d).shape[0] - g.sum()).astype(np.int32)),
+}
+
+
+def test_grad_input_pins_pass_on_the_oracle():
+    assert grad_input_pin_failures(oracle.grad_input) == []
+
+
+@pytest.mark.parametrize("name", list(GRAD_INPUT_MUTANTS))
+def test_grad_input_pins_catch_a_planted_mistake(name):
+    assert grad_input_pin_failures(GRAD_INPUT_MUTANTS[name]) != [], name
+
+
+# ----------------------------------------------------------------------- gated up projection
+def gated_pin_failures(gf):
+    fails = []
+    rng = np.random.default_rng(76)
+    gs = np.array([4, 0, 3], np.int32)
+    m, k, f = 9, 5, 4
+    x = rng.standard_normal((m, k))
+    w0, w1 = rng.standard_normal((gs.size, k, f)), rng.standard_normal((gs.size, k, f))
+    a, b = _np_forward(x, w0, gs), _np_forward(x, w1, gs)
+    _check("numpy per group", lambda: _rel(gf(x, w0, w1, gs), a / (1.0 + np.exp(-a)) * b) < TOL, fails)
+    _check("silu(z) - silu(-z) = z", lambda: _rel(gf(x, w0, w1, gs) - gf(x, -w0, w1, gs), a * b) < 1e-12, fails)
+    return fails
+
+
+def _gated_sigmoid(x, w0, w1, gs):
+    a, b = _np_forward(x, w0, gs), _np_forward(x, w1, gs)
+    return b / (1.0 + np.exp(-a)) * (np.arange(a.shape[0]) < gs.sum())[:, None]
+
+
+GATED_MUTANTS = {
+    "w0 and w1 swapped": lambda x, w0, w1, g: oracle.gated_forward(x, w1, w0, g),
+    "sigmoid gate instead of SiLU": _gated_sigmoid,
+}
+
+
+def test_gated_pins_pass_on_the_oracle():
+    assert gated_pin_failures(oracle.gated_forward) == []
+
+
+@pytest.mark.parametrize("name", list(GATED_MUTANTS))
+def test_gated_pins_catch_a_planted_mistake(name):
+    assert gated_pin_failures(GATED_MUTANTS[name]) != [], name
+
+
+# ---------------------------------------------------------------------------- MoE combine
+def unpermute_pin_failures(up):
+    fails = []
+    rng = np.random.default_rng(77)
+    t, k, e, n = 13, 2, 4, 3
+    ids = rng.integers(0, e, size=(t, k))
+    ids[2, 1] = -1                                  # one dropped copy
+    w = rng.random((t, k))
+    x = rng.standard_normal((t, n))
+    _, _, inv, xs = oracle.moe_permute(ids, x, e)
+    y = rng.standard_normal((t * k, n))
+    s_mat = np.zeros((t, t * k))
+    for tt in range(t):
+        for j in range(k):
+            if inv[tt * k + j] >= 0:
+                s_mat[tt, inv[tt * k + j]] += w[tt, j]
+    _check("dense scatter matmul", lambda: _rel(up(y, inv, w), s_mat @ y) < TOL, fails)
+    kept = w * (inv.reshape(t, k) >= 0)
+    _check("round trip of x", lambda: _rel(up(xs, inv, w), x * kept.sum(axis=1, keepdims=True)) < TOL, fails)
+    return fails
+
+
+def _unpermute_unmasked(y, inv, w):
+    # a dropped copy (inv = -1) indexes the last sorted row instead of contributing nothing
+    y, w = np.asarray(y, np.float64), np.asarray(w, np.float64)
+    t, k = w.shape
+    idx = np.asarray(inv).reshape(t, k)
+    return sum(w[:, j, None] * y[idx[:, j]] for j in range(k))
+
+
+UNPERMUTE_MUTANTS = {
+    "each copy weighted by the other copy's weight": lambda y, inv, w: oracle.moe_unpermute(y, inv, np.asarray(w)[:, ::-1]),
+    "dropped copies read the last row": _unpermute_unmasked,
+}
+
+
+def test_unpermute_pins_pass_on_the_oracle():
+    assert unpermute_pin_failures(oracle.moe_unpermute) == []
+
+
+@pytest.mark.parametrize("name", list(UNPERMUTE_MUTANTS))
+def test_unpermute_pins_catch_a_planted_mistake(name):
+    assert unpermute_pin_failures(UNPERMUTE_MUTANTS[name]) != [], name
+
+
+# ---------------------------------------------------------------------------------- tile map
+def tile_map_pin_failures(tm):
+    fails = []
+    rng = np.random.default_rng(78)
+    gs = rng.integers(0, 300, size=7).astype(np.int32)
+    gs[3] = 0
+    m, n, bm, bn = int(gs.sum()) + 9, 700, 128, 256
+    nt = -(-n // bn)
+    mt = -(-gs.astype(np.int64) // bm)
+
+    def prefix():
+        pref, _ = tm(gs, m, n, bm, bn, True)
+        return list(pref) == list(np.concatenate([[0], np.cumsum(mt * nt)]))
+
+    def decode():
+        pref, tiles = tm(gs, m, n, bm, bn, True)
+        for w_, (g, r, c) in enumerate(tiles):
+            loc = w_ - pref[g]
+            if not (pref[g] <= w_ < pref[g + 1] and (r, c) == (loc % mt[g], loc // mt[g])):
+                return False
+        return len(tiles) == pref[-1]
+    _check("closed-form prefix", prefix, fails)
+    _check("decode rule (row tiles inner)", decode, fails)
+    return fails
+
+
+TILE_MAP_MUTANTS = {
+    "the two orders swapped": lambda gs, m, n, bm, bn, inner, big=0: oracle.tile_map(gs, m, n, bm, bn, not inner, big),
+    "column tiles from N rounded down": lambda gs, m, n, bm, bn, inner, big=0: oracle.tile_map(gs, m, n - n % bn, bm, bn,
+                                                                                                inner, big),
+}
+
+
+def test_tile_map_pins_pass_on_the_oracle():
+    assert tile_map_pin_failures(oracle.tile_map) == []
+
+
+@pytest.mark.parametrize("name", list(TILE_MAP_MUTANTS))
+def test_tile_map_pins_catch_a_planted_mistake(name):
+    assert tile_map_pin_failures(TILE_MAP_MUTANTS[name]) != [], name
