@@ -94,6 +94,7 @@ struct rdot_plan_s {
     const void* map_lhs_ptr = nullptr;
     const void* map_rhs_ptr = nullptr;
     CUtensorMap map_a{}, map_b{};
+    CUtensorMap map_a64{};   // CTA-pair forwards: lhs with 64-row boxes (group-end half tiles)
     // grad-weight output map (the epilogue's TMA stores), cached by dw pointer
     const void* map_out_ptr = nullptr;
     CUtensorMap map_out{};
@@ -541,6 +542,8 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
     if (plan->map_lhs_ptr != lhs) {
         rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs, p.k, p.m, p.k * 2, TC_BK,
                                    TC_BM);
+        if (st == RDOT_OK && plan->pair)
+            st = encode_2d(&plan->map_a64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs, p.k, p.m, p.k * 2, TC_BK, 64);
         if (st != RDOT_OK) return st;
         plan->map_lhs_ptr = lhs;
     }
@@ -550,12 +553,15 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = rhs;
     }
-    if (plan->wide)
+    if (plan->wide) {
         e = launch_fwd_tc2w(plan->map_a, plan->map_b, a, plan->grid, s);
-    else if (plan->pair)
-        e = launch_fwd_tc2(plan->map_a, plan->map_b, a, p.out_dtype == RDOT_F32, plan->grid, s);
-    else
+    } else if (plan->pair) {
+        a.a64 = 1;
+        e = launch_fwd_tc2(plan->map_a, plan->map_b, a, p.out_dtype == RDOT_F32, plan->grid, s, nullptr,
+                           &plan->map_a64);
+    } else {
         e = launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "fwd_tc launch");
     return RDOT_OK;
 }
@@ -681,6 +687,8 @@ rdot_status rdot_grad_input(rdot_plan_t plan, const void* dy, const void* rhs, c
     if (plan->map_lhs_ptr != dy) {
         rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, p.n, p.m, p.n * 2, TC_BK,
                                    TC_BM);
+        if (st == RDOT_OK && plan->pair)
+            st = encode_2d(&plan->map_a64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, p.n, p.m, p.n * 2, TC_BK, 64);
         if (st != RDOT_OK) return st;
         plan->map_lhs_ptr = dy;
     }
@@ -702,10 +710,12 @@ rdot_status rdot_grad_input(rdot_plan_t plan, const void* dy, const void* rhs, c
     a.m_inner = plan->m_inner;
     a.big_mt = plan->big_mt;
     a.b_kmajor = 1;
+    a.a64 = plan->pair ? 1 : 0;
     a.status = static_cast<int32_t*>(workspace);
     a.timeout_ns = plan->timeout_ns;
     cudaError_t e = plan->pair
-                        ? launch_fwd_tc2(plan->map_a, plan->map_b, a, p.out_dtype == RDOT_F32, plan->grid, s)
+                        ? launch_fwd_tc2(plan->map_a, plan->map_b, a, p.out_dtype == RDOT_F32, plan->grid, s, nullptr,
+                                         &plan->map_a64)
                         : launch_fwd_tc(plan->map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, plan->grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "grad_input launch");
     return RDOT_OK;

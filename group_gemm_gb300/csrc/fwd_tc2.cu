@@ -15,7 +15,9 @@
 //     arrive on the even CTA's "accumulator empty" barrier (one arrival per warp, 8 in all).
 //   - Half tiles: a tile with at most 128 rows of its group left (a group's last tile) runs
 //     M = 128 MMAs at half the cost of M = 256 ones. CTA r then stages rows [row0 + 64 r, +64) at
-//     the top of its A buffer, and its tensor memory holds those 64 rows twice over in 128 columns:
+//     the top of its A buffer (through a map with 64-row boxes where the caller passes one: the
+//     first 8 KB of the 128-row swizzled layout, so the descriptors do not change), and its
+//     tensor memory holds those 64 rows twice over in 128 columns:
 //     lanes [0, 64) with output columns [n0, n0 + 128), lanes [64, 128) with [n0 + 128, n0 + 256).
 //     The forward and the data gradient use them; the gated projection, whose epilogue pairs column
 //     c with column c + 128 of the same row, keeps 256-row tiles.
@@ -56,7 +58,8 @@ size_t smem_bytes(int G) {
 template <bool OUT_F32, int VAR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                   const __grid_constant__ CUtensorMap tmap_b1, FwdArgs a) {
+                   const __grid_constant__ CUtensorMap tmap_b1, const __grid_constant__ CUtensorMap tmap_a64,
+                   FwdArgs a) {
     constexpr int EPI_BYTES = 4 * EpiStage<OUT_F32>::BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -92,6 +95,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmap_a);
         tma_prefetch_desc(&tmap_b);
+        if (a.a64) tma_prefetch_desc(&tmap_a64);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_holder, TMEM_COLS);   // collectively, one warp in each CTA of the pair
@@ -120,10 +124,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
                 constexpr bool gated = VAR == 2;
                 const int n0 = t.nt * (gated ? BN / 2 : BN);
-                const int a_rows = (!gated && t.rows <= 128) ? 64 : 128;   // A rows per CTA (half tile: 64)
+                const bool half = !gated && t.rows <= 128;
+                const int a_rows = half ? 64 : 128;                         // A rows per CTA
+                const bool a_small = half && a.a64;                         // 64-row boxes
+                const CUtensorMap* map_a = a_small ? &tmap_a64 : &tmap_a;
+                const int a_bytes = a_small ? A_BYTES / 2 : A_BYTES;
                 // bytes each CTA brings in: its A half unless it lies wholly past M, and the
                 // 64-column chunks of its B half that are not wholly past N
-                const int a0 = A_BYTES, a1 = (t.row0 + a_rows < a.M) ? A_BYTES : 0;
+                const int a0 = a_bytes, a1 = (t.row0 + a_rows < a.M) ? a_bytes : 0;
                 // (K-major B, the data gradient: one 128-row box per CTA, or none past N; gated:
                 // both CTAs load the same 128 columns, of w0 and of w1)
                 constexpr bool kmaj = VAR == 1;
@@ -143,7 +151,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     uint8_t* sb = sa + A_BYTES;
                     if (leader) mbar_arrive_expect_tx(&full[stage], a0 + a1 + (c0 + c1) * B_CHUNK_BYTES);
                     const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
-                    if (my_a) tma_load_2d_pair(sa, &tmap_a, fb, kb * TC_BK, t.row0 + a_rows * static_cast<int>(rank));
+                    if (my_a) tma_load_2d_pair(sa, map_a, fb, kb * TC_BK, t.row0 + a_rows * static_cast<int>(rank));
                     if (kmaj) {
                         if (my_c) tma_load_3d_pair(sb, map_b, fb, kb * TC_BK, b_col, t.g);
                     } else {
@@ -324,30 +332,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 template <bool OUT_F32, int VAR>
-cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb1, const FwdArgs& a,
-                       int grid, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tb1, const CUtensorMap& ta64,
+                       const FwdArgs& a, int grid, cudaStream_t stream) {
     const size_t shm = smem_bytes<OUT_F32>(a.G);
     auto kern = fwd_tc2_kernel<OUT_F32, VAR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, shm, stream>>>(ta, tb, tb1, a);
+    kern<<<grid, THREADS, shm, stream>>>(ta, tb, tb1, ta64, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc2(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, bool out_f32,
-                           int grid, cudaStream_t stream, const CUtensorMap* tmap_b1) {
-    if (grid % 2 || (a.gated && (!tmap_b1 || a.b_kmajor))) return cudaErrorInvalidValue;
+                           int grid, cudaStream_t stream, const CUtensorMap* tmap_b1, const CUtensorMap* tmap_a64) {
+    if (grid % 2 || (a.gated && (!tmap_b1 || a.b_kmajor)) || (a.a64 && !tmap_a64)) return cudaErrorInvalidValue;
     const CUtensorMap& tb1 = tmap_b1 ? *tmap_b1 : tmap_b;
+    const CUtensorMap& ta64 = tmap_a64 ? *tmap_a64 : tmap_a;
     if (a.gated)
-        return out_f32 ? launch_one<true, 2>(tmap_a, tmap_b, tb1, a, grid, stream)
-                       : launch_one<false, 2>(tmap_a, tmap_b, tb1, a, grid, stream);
+        return out_f32 ? launch_one<true, 2>(tmap_a, tmap_b, tb1, ta64, a, grid, stream)
+                       : launch_one<false, 2>(tmap_a, tmap_b, tb1, ta64, a, grid, stream);
     if (a.b_kmajor)
-        return out_f32 ? launch_one<true, 1>(tmap_a, tmap_b, tb1, a, grid, stream)
-                       : launch_one<false, 1>(tmap_a, tmap_b, tb1, a, grid, stream);
-    return out_f32 ? launch_one<true, 0>(tmap_a, tmap_b, tb1, a, grid, stream)
-                   : launch_one<false, 0>(tmap_a, tmap_b, tb1, a, grid, stream);
+        return out_f32 ? launch_one<true, 1>(tmap_a, tmap_b, tb1, ta64, a, grid, stream)
+                       : launch_one<false, 1>(tmap_a, tmap_b, tb1, ta64, a, grid, stream);
+    return out_f32 ? launch_one<true, 0>(tmap_a, tmap_b, tb1, ta64, a, grid, stream)
+                   : launch_one<false, 0>(tmap_a, tmap_b, tb1, ta64, a, grid, stream);
 }
 
 int fwd_tc2_max_clusters(bool out_f32, int G) {

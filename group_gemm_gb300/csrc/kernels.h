@@ -25,6 +25,8 @@ struct FwdArgs {
     int big_mt;                  // > 0: interleave groups with >= big_mt row tiles with the others
     int b_kmajor;                // 1: the B operand is K-major (rhs [G, N, K] with K contiguous; the
                                  // data gradient), 0: MN-major (rhs [G, K, N], the forward)
+    int a64;                     // CTA pairs: 1 = a second lhs map with 64-row boxes is passed (the
+                                 // group-end half tiles load 64 rows per CTA through it)
     int gated;                   // CTA pairs only: 1 = out = silu(lhs w0) * (lhs w1), the even CTA's B
                                  // from w0 and the odd CTA's from w1 (second map), 128 output columns
                                  // per tile (N = the width of w0, w1 and out)
@@ -52,8 +54,10 @@ constexpr int TC_BK = 64;
 
 // bf16 inputs on CTA pairs (fwd_tc2.cu): clusters of 2 CTAs, 256 x 256 tiles, same maps as
 // launch_fwd_tc. grid must be even (2 CTAs per cluster).
+// tmap_a64: the lhs map with a (64, 64) box, used when a.a64 is set.
 cudaError_t launch_fwd_tc2(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, bool out_f32,
-                           int grid, cudaStream_t stream, const CUtensorMap* tmap_b1 = nullptr);
+                           int grid, cudaStream_t stream, const CUtensorMap* tmap_b1 = nullptr,
+                           const CUtensorMap* tmap_a64 = nullptr);
 // CTA-pair bf16 forward with 256 x 512 tiles, bf16 out (fwd_tc2w.cu); a.NT counts 512-wide tiles.
 cudaError_t launch_fwd_tc2w(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, int grid,
                             cudaStream_t stream);
