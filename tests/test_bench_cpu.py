@@ -25,3 +25,26 @@ def test_reference_arm_line_has_the_contract_keys():
                            "d2h_bytes_per_step": 0}
     # rank > 0 of a multi-rank reference run does no work
     assert bench.bench_reference(args, 1, 2) is None
+
+
+def test_traffic_figure_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
+    """The roofline's DRAM traffic comes from a committed ncu capture keyed by a hash of the
+    kernel's sources: it is reported while they are unchanged and null once any of them changes."""
+    sys.path.insert(0, ROOT)
+    import bench
+    srcs = bench.KERNEL_SOURCES["fwd_tc2_kernel"]
+    got = bench.ncu_traffic("fwd_tc2_kernel", "mixtral_bf16", srcs)
+    assert got is not None and got > 0                      # the committed capture is of these sources
+    assert bench.ncu_traffic("fwd_tc2_kernel", "deepseek_bf16", srcs) is None   # no capture of that workload
+    # a changed source file: copy the sources into a scratch root, edit one, hash again
+    for f in srcs:
+        dst = tmp_path / f
+        dst.parent.mkdir(parents=True, exist_ok=True)
+        dst.write_bytes(open(os.path.join(ROOT, f), "rb").read())
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_bytes(open(os.path.join(ROOT, "profiles", "traffic.json"), "rb").read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.ncu_traffic("fwd_tc2_kernel", "mixtral_bf16", srcs) == got
+    with open(tmp_path / srcs[0], "a") as fh:
+        fh.write("\n// edited\n")
+    assert bench.ncu_traffic("fwd_tc2_kernel", "mixtral_bf16", srcs) is None
