@@ -48,3 +48,29 @@ def test_traffic_figure_only_for_the_sources_it_was_taken_on(tmp_path, monkeypat
     with open(tmp_path / srcs[0], "a") as fh:
         fh.write("\n// edited\n")
     assert bench.ncu_traffic("fwd_tc2_kernel", "mixtral_bf16", srcs) is None
+
+
+def test_clock_samples_give_the_median_clock_and_the_active_reasons():
+    """The clocks object of the JSON line from nvidia-smi samples taken during the timed region:
+    median SM clock, highest max clock, every throttle reason seen active; malformed lines skipped."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+    cs = bench.ClockSampler(0)
+    cs.proc = FakeProc()
+    cs.lines = ["1560, 2070, 1390.1, 0x4, Not Active, Not Active, Not Active, Active",
+                "1575, 2070, 1395.0, 0x4, Not Active, Not Active, Not Active, Active",
+                "1590, 2070, 1380.2, 0x0, Not Active, Not Active, Not Active, Not Active",
+                "[N/A], 2070, 10.0, 0x0, Not Active, Not Active, Not Active, Not Active",   # no clock: skipped
+                "garbage"]
+    got = cs.stop()
+    assert got == {"sm_mhz": 1575.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    cs.lines = ["1200, 2070, 700.0, 0x60, Active, Active, Not Active, Not Active"]
+    assert cs.stop()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
+    assert bench.ClockSampler(0).stop()["reasons"] == ["nvidia-smi unavailable"]   # never started
