@@ -45,6 +45,17 @@ def useful_flops(gs, k, n) -> float:
     return 2.0 * float(np.sum(np.maximum(gs, 0))) * k * n
 
 
+def issued_rows(gs, tile_m: int, half_tiles: bool) -> int:
+    """Rows the MMAs of a forward cover: the padded-work model of "How to Scale Your Model on AMD",
+    chapter 6 ("Grouped GEMM kernels for MoE"): each group's rows rounded up to whole row tiles of
+    tile_m rows, with 128-row tiles at group ends where the CTA-pair kernel has them."""
+    gs = np.maximum(np.asarray(gs, np.int64), 0)
+    if half_tiles and tile_m == 256:
+        r = gs % 256
+        return int(((gs // 256) * 256 + np.where(r == 0, 0, np.where(r <= 128, 128, 256))).sum())
+    return int((-(-gs // tile_m) * tile_m).sum())
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -332,6 +343,8 @@ def bench_ours(args, rank, world, barrier):
         peak, peak_kind = peaks["bf16_tflops_sustained"], f"{peaks['source']} bf16 sustained (timed region {per_step * args.steps:.2f} s)"
     else:
         peak, peak_kind = peaks["bf16_tflops"], f"{peaks['source']} bf16 burst (timed region {per_step * args.steps:.3f} s)"
+    tile_m, tile_n = int(plan.info["tile_m"]), int(plan.info["tile_n"])
+    w_pad = issued_rows(gs, tile_m, tile_m == 256 and tile_n != 512) / max(1.0, float(np.maximum(gs, 0).sum())) - 1.0
     result = {
         "metric": "ragged-dot useful TFLOP/s (fraction of GB300 dense bf16 peak; speedup vs padded in per_config)",
         "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -349,7 +362,9 @@ def bench_ours(args, rank, world, barrier):
                      "traffic": ncu_traffic(kernel, name, KERNEL_SOURCES[kernel]),
                      "kernel": kernel, "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}",
                      "peak_kind": peak_kind,
-                     "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4)},
+                     "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                     # tile tails: issued rows / useful rows - 1, and the issued MMA work against the peak
+                     "w_pad": round(w_pad, 4), "issued_frac": round(achieved * (1.0 + w_pad) / peak, 4)},
         "e2e": e2e,
         "gpu_launches": args.steps,   # one librdot launch per timed step
         "clocks": clk,

@@ -74,3 +74,28 @@ def test_clock_samples_give_the_median_clock_and_the_active_reasons():
     cs.lines = ["1200, 2070, 700.0, 0x60, Active, Active, Not Active, Not Active"]
     assert cs.stop()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
     assert bench.ClockSampler(0).stop()["reasons"] == ["nvidia-smi unavailable"]   # never started
+
+
+def test_issued_rows_follow_the_padded_work_model():
+    """W_pad of the pages' padded-work model (rows rounded up to whole T_M-row tiles), and the
+    pair kernel's rule: 256-row tiles with a 128-row tile at a group end that needs no more."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import rdot_inputs as ri
+    rng = np.random.default_rng(5)
+    gs = rng.integers(0, 700, size=40)
+    gs[[3, 9]] = 0
+    for tm in (128, 256):
+        assert bench.issued_rows(gs, tm, False) == sum(-(-int(x) // tm) * tm for x in gs)
+    want = 0
+    for x in map(int, gs):
+        tiles, left = 0, x
+        while left > 0:                       # whole 256-row tiles, then the end tile
+            tiles += 128 if left <= 128 else 256
+            left -= 256
+        want += tiles
+    assert bench.issued_rows(gs, 256, True) == want
+    mix = ri.config_group_sizes("mixtral_bf16")
+    assert abs(bench.issued_rows(mix, 256, True) / mix.sum() - 1.0391) < 1e-4      # 3.9 % tile tails
+    assert abs(bench.issued_rows(mix, 256, False) / mix.sum() - 1.0781) < 1e-4
