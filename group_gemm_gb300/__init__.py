@@ -22,8 +22,8 @@ __all__ = [
     "rdot_grad_weight", "rdot_padded_workspace_size", "rdot_padded_forward", "rdot_read_status",
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
-    "rdot_forward_no_alloc", "rdot_grad_input", "rdot_moe_route_workspace_size", "rdot_moe_permute",
-    "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
+    "rdot_forward_no_alloc", "rdot_no_alloc_read_status", "rdot_grad_input", "rdot_moe_route_workspace_size",
+    "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
     "grad_input", "ragged_dot_gated",
     "ragged_dot_mxfp8", "padded_ragged_dot", "EXPORTED_SYMBOLS",
 ]
@@ -44,8 +44,8 @@ EXPORTED_SYMBOLS = (
     "rdot_grad_weight", "rdot_padded_workspace_size", "rdot_padded_forward", "rdot_read_status",
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
-    "rdot_forward_no_alloc", "rdot_grad_input", "rdot_moe_route_workspace_size", "rdot_moe_permute",
-    "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8",
+    "rdot_forward_no_alloc", "rdot_no_alloc_read_status", "rdot_grad_input", "rdot_moe_route_workspace_size",
+    "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8",
 )
 
 _DTYPE_CODES = {"f32": RDOT_F32, "bf16": RDOT_BF16, "e4m3": RDOT_E4M3}
@@ -115,6 +115,7 @@ def load():
             "rdot_last_cuda_error": ([], ctypes.c_char_p),
             "rdot_version": ([], ctypes.c_int),
             "rdot_forward_no_alloc": ([vp, vp, vp, vp, vp, vp], st),
+            "rdot_no_alloc_read_status": ([vp, i32p, vp], st),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -262,6 +263,16 @@ def rdot_forward_no_alloc(plan, lhs, rhs, group_sizes, out, stream=None) -> None
     """Forward with the library's static device scratch instead of a caller workspace."""
     _check(load().rdot_forward_no_alloc(plan, _ptr(lhs), _ptr(rhs), _ptr(group_sizes), _ptr(out),
                                         _stream(stream, out.device)), "rdot_forward_no_alloc")
+
+
+def rdot_no_alloc_read_status(plan, stream=None, device=None):
+    """Returns ``(status, flags)``: the status word the last rdot_forward_no_alloc call on the
+    plan's device left in the library's static scratch (synchronises the stream)."""
+    v = ctypes.c_int32()
+    st = load().rdot_no_alloc_read_status(plan, ctypes.byref(v), _stream(stream, device))
+    if st not in (RDOT_OK, RDOT_WARN_GROUP_SIZES, RDOT_ERR_DEVICE_TIMEOUT):
+        raise RdotError(st, "rdot_no_alloc_read_status")
+    return st, v.value
 
 
 def rdot_status_string(status: int) -> str:

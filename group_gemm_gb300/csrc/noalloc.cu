@@ -6,7 +6,8 @@
 // weights and KV cache up front), code on a latency-critical path where cudaMalloc's implicit
 // device synchronisation would stall other streams, and systems certified to allocate nothing
 // after initialisation. rdot_forward_no_alloc serves them: it runs the same forward kernels with
-// the workspace placed in a fixed-size array in the library's own device memory.
+// the workspace placed in a fixed-size array in the library's own device memory, and
+// rdot_no_alloc_read_status reads back the status word the kernels left there.
 //
 // The array below is a file-scope __device__ object: every GPU on which the library is loaded
 // holds these RDOT_NO_ALLOC_SCRATCH_BYTES bytes until the process exits. Host code must not
@@ -49,6 +50,38 @@ void* scratch_address(int device) {
     return g_scratch_ptr[device];
 }
 
+// Makes `device` current for the lifetime of the object and puts the caller's device back
+// afterwards. Failures are recorded for rdot_last_cuda_error.
+struct CurrentDevice {
+    int prev = -1;
+    bool ok = false;
+    explicit CurrentDevice(int device) {
+        cudaError_t e = cudaGetDevice(&prev);
+        if (e == cudaSuccess && prev != device) e = cudaSetDevice(device);
+        if (e != cudaSuccess) {
+            rdot::set_last_error(std::string("rdot no-alloc path: selecting the plan's device: ") +
+                                 cudaGetErrorString(e));
+            return;
+        }
+        ok = true;
+    }
+    // Restores the caller's device; false (with the error recorded) if that failed.
+    bool restore() {
+        if (prev < 0) return true;
+        int cur = -1;
+        cudaError_t e = cudaGetDevice(&cur);
+        if (e == cudaSuccess && cur != prev) e = cudaSetDevice(prev);
+        prev = -1;
+        if (e != cudaSuccess) {
+            rdot::set_last_error(std::string("rdot no-alloc path: restoring the caller's device: ") +
+                                 cudaGetErrorString(e));
+            return false;
+        }
+        return true;
+    }
+    ~CurrentDevice() { (void)restore(); }
+};
+
 }  // namespace
 
 extern "C" RDOT_API rdot_status rdot_forward_no_alloc(rdot_plan_t plan, const void* lhs, const void* rhs,
@@ -66,11 +99,9 @@ extern "C" RDOT_API rdot_status rdot_forward_no_alloc(rdot_plan_t plan, const vo
         rdot::set_last_error(buf);
         return RDOT_ERR_UNSUPPORTED;
     }
-    const int device = rdot::plan_device(plan);
-    int prev = -1;
-    if (cudaGetDevice(&prev) != cudaSuccess) return RDOT_ERR_CUDA;
-    if (prev != device && cudaSetDevice(device) != cudaSuccess) return RDOT_ERR_CUDA;
-    void* scratch = scratch_address(device);
+    CurrentDevice cd(rdot::plan_device(plan));
+    if (!cd.ok) return RDOT_ERR_CUDA;
+    void* scratch = scratch_address(rdot::plan_device(plan));
     rdot_status result = RDOT_ERR_CUDA;
     if (scratch) {
         // the previous call's status bits are cleared: this call starts from a zero status word
@@ -81,6 +112,19 @@ extern "C" RDOT_API rdot_status rdot_forward_no_alloc(rdot_plan_t plan, const vo
             result = rdot_forward(plan, lhs, rhs, group_sizes, out, scratch, stream);
         }
     }
-    if (prev != device) cudaSetDevice(prev);
+    if (!cd.restore() && result == RDOT_OK) result = RDOT_ERR_CUDA;
     return result;
+}
+
+extern "C" RDOT_API rdot_status rdot_no_alloc_read_status(rdot_plan_t plan, int32_t* flags, void* stream) {
+    if (!plan || !flags) return RDOT_ERR_INVALID_ARG;
+    CurrentDevice cd(rdot::plan_device(plan));
+    if (!cd.ok) return RDOT_ERR_CUDA;
+    void* scratch = scratch_address(rdot::plan_device(plan));
+    if (!scratch) return RDOT_ERR_CUDA;
+    // the status word sits where rdot_read_status expects it in a workspace: read it the same way
+    rdot_status st = rdot_read_status(plan, scratch, flags, stream);
+    if (!cd.restore() && (st == RDOT_OK || st == RDOT_WARN_GROUP_SIZES || st == RDOT_ERR_DEVICE_TIMEOUT))
+        st = RDOT_ERR_CUDA;
+    return st;
 }

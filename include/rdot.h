@@ -116,9 +116,10 @@ RDOT_API rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_pla
 RDOT_API rdot_status rdot_plan_destroy(rdot_plan_t plan);
 
 /* Bytes of device workspace the plan's calls need (at least 256, 256-byte aligned by the
- * caller). The workspace holds the status word followed by the group table exported by
- * rdot_debug_offsets_tilemap; an MXFP8 plan adds the reordered scale blocks, a grad-weight plan
- * two 128-byte tensor maps per group (rewritten on the device by every call). It must be zeroed
+ * caller). The first 256 bytes hold the status word (an int32 at offset 0; the rest is
+ * reserved); that is the whole workspace of the bf16 and fp32 forwards, the data gradient and the
+ * gated projection. An MXFP8 plan adds the scale blocks the call reorders, a grad-weight plan two
+ * 128-byte tensor maps per group (both rewritten on the device by every call). It must be zeroed
  * once before first use. Calls that share a workspace must not overlap on the GPU. */
 RDOT_API rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes);
 
@@ -295,6 +296,14 @@ RDOT_API rdot_status rdot_set_wait_timeout(rdot_plan_t plan, uint64_t timeout_ns
  *     streams, or different host threads) race on the array. */
 RDOT_API rdot_status rdot_forward_no_alloc(rdot_plan_t plan, const void* lhs, const void* rhs,
                                            const int32_t* group_sizes, void* out, void* stream);
+
+/* Reads the status word that the last rdot_forward_no_alloc call on the plan's device left in the
+ * static array (RDOT_STATUS_BIT_*), the counterpart of rdot_read_status for that entry point; no
+ * counterpart on the pages either. Synchronises `stream`, which should be the stream of that call.
+ * Returns RDOT_ERR_DEVICE_TIMEOUT if the timeout bit is set, RDOT_WARN_GROUP_SIZES if only the
+ * group-size bit is set, RDOT_OK otherwise. The next rdot_forward_no_alloc call clears the word,
+ * so read it in between. Allocates nothing. */
+RDOT_API rdot_status rdot_no_alloc_read_status(rdot_plan_t plan, int32_t* flags, void* stream);
 
 /* Human-readable status name. */
 RDOT_API const char* rdot_status_string(rdot_status status);

@@ -88,15 +88,18 @@ def test_full_size_bf16_forward_sampled_rows(name, flags):
     assert cosine_to_rounded(got, ref) >= COSINE_MIN
 
 
-@pytest.mark.parametrize("flags", [0, 4])
+@pytest.mark.parametrize("flags", [0, gg.RDOT_FLAG_NO_CTA_PAIR])
 def test_full_size_grad_weight_sampled_rows(flags):
-    """flags 0 = the plan's own choice (single-CTA tiles); 4 forces CTA pairs."""
+    """flags 0 = the plan's own choice (CTA pairs here: the groups average 1024 rows, above the
+    512-row threshold); RDOT_FLAG_NO_CTA_PAIR forces the single-CTA kernel, the default for
+    smaller groups, so both kernels run at full size."""
     cfg = ri.CONFIGS["wgrad_bf16"]
     m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
     gs = ri.config_group_sizes("wgrad_bf16")
     lhs = ri.device_normal((m, k), 1000, 1.0, DEV, torch.bfloat16)
     dy = ri.device_normal((m, n), 2000, 1.0, DEV, torch.bfloat16)
     plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", flags=flags)
+    assert plan.info["tile_m"] == (128 if flags else 256)
     dw = torch.full((g, k, n), float("nan"), dtype=torch.float32, device=DEV)
     gg.rdot_grad_weight(plan.handle, lhs, dy, torch.from_numpy(gs).to(DEV), dw, plan.workspace)
     assert plan.status() == 0
@@ -136,6 +139,40 @@ def test_full_size_mxfp8_sampled_rows(flags):
     gidx = torch.from_numpy(ug).to(DEV)
     ref = oracle.forward_mxfp8(aq[ridx].cpu(), as_[ridx].cpu(), bq[gidx].cpu(), bs[gidx].cpu(),
                                counts.astype(np.int32))
+    got = out[ridx].double().cpu().numpy()
+    assert rel_err(got, ref) <= TOL
+    assert cosine_to_rounded(got, ref) >= COSINE_MIN
+
+
+def test_full_size_mxfp8_grad_input_sampled_rows():
+    """The MXFP8 data gradient at the MXFP8 workload's shapes: dy [65536, 1536] and the weights
+    [128, 4096, 1536] quantised along the contracted N (one E8M0 scale per 32 of N), output
+    [65536, 4096]; the default plan, as bench.py times it."""
+    cfg = ri.CONFIGS["mxfp8"]
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    gs = ri.config_group_sizes("mxfp8")
+    dy = ri.device_normal((m, n), 1100, 1.0, DEV, torch.float32)
+    dq, ds = ri.quantize_mx_e4m3(dy, axis=1)
+    del dy
+    w = ri.device_normal((g, k, n), 2100, 0.02, DEV, torch.float32)
+    wq, ws = ri.quantize_mx_e4m3(w, axis=2)
+    del w
+    torch.cuda.empty_cache()
+    plan = gg.Plan(m, k, n, g, "grad_input_mxfp8", "e4m3", "bf16")
+    out = torch.full((m, k), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gg.rdot_grad_input_mxfp8(plan.handle, dq, ds, wq, ws, torch.from_numpy(gs).to(DEV), out, plan.workspace)
+    assert plan.status() == 0
+    assert torch.isfinite(out).all()
+    rng = np.random.default_rng(8)
+    nz = np.nonzero(gs)[0]
+    groups = sorted({int(nz[0]), int(nz[-1]), int(np.argmax(gs)), int(nz[np.argmin(gs[nz])])})
+    rows = sample_rows(gs, groups, rng)
+    gor = np.array([oracle.group_of_row(gs, m, int(r)) for r in rows])
+    ug, counts = np.unique(gor, return_counts=True)
+    ridx = torch.from_numpy(rows).to(DEV)
+    gidx = torch.from_numpy(ug).to(DEV)
+    ref = oracle.grad_input_mxfp8(dq[ridx].cpu(), ds[ridx].cpu(), wq[gidx].cpu(), ws[gidx].cpu(),
+                                  counts.astype(np.int32))
     got = out[ridx].double().cpu().numpy()
     assert rel_err(got, ref) <= TOL
     assert cosine_to_rounded(got, ref) >= COSINE_MIN

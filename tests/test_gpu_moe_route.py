@@ -138,18 +138,14 @@ def _layer(x, ids, w_route, w0, w1, wo, e, stream=None):
 
 
 def _layer_ref(x, ids, w_route, w0, w1, wo, e):
-    xd, w0d, w1d, wod = (t.double().cpu().numpy() for t in (x, w0, w1, wo))
-    t, k = ids.shape
-    out = np.zeros((t, wod.shape[2]))
-    for tt in range(t):
-        for j in range(k):
-            g = ids[tt, j]
-            if 0 <= g < e:
-                z0, z1 = xd[tt] @ w0d[g], xd[tt] @ w1d[g]
-                h = torch.from_numpy(z0 / (1.0 + np.exp(-z0)) * z1).to(torch.bfloat16).double().numpy()
-                y = torch.from_numpy(h @ wod[g]).to(torch.bfloat16).double().numpy()
-                out[tt] += w_route[tt, j] * y
-    return out
+    """The layer composed from the oracle's steps: permute (stable sort by expert, bincount,
+    gather), the gated up projection, the down projection, the weighted un-permute. The library
+    keeps the activated hidden rows and the down projection's rows in bf16, so each is rounded to
+    bf16 (round to nearest even) before the next step consumes it."""
+    gs, _order, inv, x_sorted = oracle.moe_permute(ids, x.double().cpu().numpy(), e)
+    h = torch.from_numpy(oracle.gated_forward(x_sorted, w0.cpu(), w1.cpu(), gs)).to(torch.bfloat16)
+    y = torch.from_numpy(oracle.forward(h, wo.cpu(), gs)).to(torch.bfloat16)
+    return oracle.moe_unpermute(y, inv, np.asarray(w_route, dtype=np.float64))
 
 
 def test_moe_layer_with_gated_up_and_down_projection():
