@@ -21,6 +21,10 @@ Functions and the passages they follow (page titles and sections):
 * :func:`gated_forward` -- "Group-GEMM in XLA", Part 4 "The Three MoE Compute Paths in MaxText":
   the up projection's two ragged dots feed ``activation(layer_w0) * layer_w1``; the activation is
   read as SiLU, z * sigmoid(z), the gated unit of the evaluated MoE models.
+* :func:`router_topk` -- the front end the three MoE paths share ("Group-GEMM in XLA", Part 4
+  "The Three MoE Compute Paths in MaxText": ``jax.lax.top_k(gate_logits, k)`` gives every token its
+  top-k experts and a weight per selected expert; "How to Scale Your Model on AMD", ch. 6, "Router
+  to expert and back", step 1). Ranking by value, ties to the lower expert index.
 * :func:`moe_permute` / :func:`moe_unpermute` -- "Group-GEMM in XLA", Part 4 "The Three MoE
   Compute Paths in MaxText", Path 1 (sparse / ragged-dot): the pre-processing sorts the token
   copies by destination expert (a stable argsort of the flattened top-k indices), gathers the
@@ -296,6 +300,54 @@ def tile_map(group_sizes, m: int, n: int, bm: int, bn: int, m_inner: bool, big_m
                      int(bool(m_inner)), int(big_mt), _ptr(pref, ctypes.c_int32), _ptr(tiles, ctypes.c_int32),
                      total)
     return pref, tiles[:total]
+
+
+# ------------------------------------------------------------------------------- router top-k
+ROUTER_WEIGHTS = ("values", "softmax", "softmax_topk")
+
+
+def router_topk(logits, k: int, weights: str = "values"):
+    """The router front end: each token's k highest-scoring experts and a weight for each.
+
+    logits [T, E]: fp32 or bf16 (a torch bf16 tensor or raw uint16 patterns), decoded exactly.
+    Experts are ranked by their logit, highest first; equal logits (+0 and -0 are equal) rank the
+    lower expert index first; NaN ranks below every number, -inf included. Returns
+    ``(ids int64 [T, k], w float64 [T, k])`` in rank order, with ``w`` read three ways:
+
+    * ``"values"`` -- the selected logits themselves, as ``jax.lax.top_k`` returns them;
+    * ``"softmax"`` -- the selected entries of softmax over all E logits of the token;
+    * ``"softmax_topk"`` -- softmax over the k selected logits only (the weights sum to one).
+
+    The softmax is exp(x - m) / sum exp(x - m) with m the token's top-ranked logit, in float64.
+    Selection never looks at the softmax: it is monotone, so its top-k are the logits' top-k."""
+    if weights not in ROUTER_WEIGHTS:
+        raise ValueError(f"weights must be one of {ROUTER_WEIGHTS}")
+    a, dt = _as_np(logits)
+    if dt == BF16:
+        x = (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    elif dt in (F32, F64):
+        x = a.astype(np.float64)
+    else:
+        raise TypeError("logits must be f32 or bf16")
+    if x.ndim != 2:
+        raise ValueError("logits must be [T, E]")
+    t, e = x.shape
+    if not 1 <= k <= e:
+        raise ValueError("need 1 <= k <= E")
+    # ascending sort of -x: the largest logit first, NaN (unordered) last, a stable sort keeps the
+    # lower index first among equal keys (-0 and +0 compare equal)
+    order = np.argsort(-x, axis=1, kind="stable")
+    ids = order[:, :k].astype(np.int64)
+    v = np.take_along_axis(x, ids, axis=1)
+    if weights == "values":
+        return ids, v
+    m = v[:, :1]
+    with np.errstate(invalid="ignore", over="ignore"):
+        if weights == "softmax":
+            z = np.exp(x - m)
+            return ids, np.exp(v - m) / z.sum(axis=1, keepdims=True)
+        z = np.exp(v - m)
+        return ids, z / z.sum(axis=1, keepdims=True)
 
 
 # ------------------------------------------------------------------------ MoE permute / combine

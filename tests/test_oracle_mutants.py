@@ -391,3 +391,81 @@ def test_tile_map_pins_pass_on_the_oracle():
 @pytest.mark.parametrize("name", list(TILE_MAP_MUTANTS))
 def test_tile_map_pins_catch_a_planted_mistake(name):
     assert tile_map_pin_failures(TILE_MAP_MUTANTS[name]) != [], name
+
+
+# ------------------------------------------------------------------------------ router top-k
+def router_pin_failures(fn):
+    from tests.test_oracle_pins import topk_ranking_ok
+    fails = []
+    d = _golden.read("router_topk_example.txt")
+    x = d["logits"].astype(np.float32)
+    for mode in ("values", "softmax", "softmax_topk"):
+        _check(f"worked example ({mode})",
+               lambda: np.array_equal(fn(x, 2, mode)[0], d["ids"]) and
+               np.allclose(fn(x, 2, mode)[1], d[mode], rtol=1e-15, atol=0, equal_nan=True), fails)
+    rng = np.random.default_rng(67)
+    xr = rng.integers(-3, 4, size=(40, 12)).astype(np.float32)
+    xr[rng.random(xr.shape) < 0.1] = np.nan
+    _check("ranking invariants", lambda: all(topk_ranking_ok(xr, k, fn(xr, k, "values")[0]) for k in (1, 3, 12)), fails)
+    xs = (rng.standard_normal((20, 10)) * 2).astype(np.float32)
+    x64 = xs.astype(np.float64)
+    ref = np.exp(x64 - x64.max(axis=1, keepdims=True))
+    ref /= ref.sum(axis=1, keepdims=True)
+    _check("softmax over all experts", lambda: _rel(fn(xs, 10, "softmax")[1],
+                                                    np.take_along_axis(ref, fn(xs, 10, "softmax")[0], axis=1)) < TOL,
+           fails)
+    _check("softmax over the selected sums to one",
+           lambda: np.allclose(fn(xs, 3, "softmax_topk")[1].sum(axis=1), 1.0, rtol=1e-14, atol=0), fails)
+    return fails
+
+
+def _topk_ties_high_index(x, k, mode):
+    # equal logits ranked by the higher expert index
+    x = np.asarray(x, np.float64)
+    e = x.shape[1]
+    ids, _ = oracle.router_topk(x[:, ::-1].copy(), k, "values")
+    ids = e - 1 - ids
+    return _topk_weights(x, ids, mode)
+
+
+def _topk_nan_first(x, k, mode):
+    # NaN ranked above every number (argsort of -x with NaN mapped to -inf)
+    x = np.asarray(x, np.float64)
+    key = np.where(np.isnan(x), -np.inf, -x)
+    ids = np.argsort(key, axis=1, kind="stable")[:, :k]
+    return _topk_weights(x, ids, mode)
+
+
+def _topk_weights(x, ids, mode):
+    v = np.take_along_axis(x, ids, axis=1)
+    if mode == "values":
+        return ids, v
+    m = v[:, :1]
+    with np.errstate(invalid="ignore", over="ignore"):
+        if mode == "softmax":
+            return ids, np.exp(v - m) / np.exp(x - m).sum(axis=1, keepdims=True)
+        z = np.exp(v - m)
+        return ids, z / z.sum(axis=1, keepdims=True)
+
+
+ROUTER_MUTANTS = {
+    "ties to the higher expert index": _topk_ties_high_index,
+    "NaN ranked first": _topk_nan_first,
+    "softmax over the selected in place of all experts":
+        lambda x, k, m: oracle.router_topk(x, k, "softmax_topk" if m == "softmax" else m),
+    "softmax over all in place of the selected":
+        lambda x, k, m: oracle.router_topk(x, k, "softmax" if m == "softmax_topk" else m),
+    "the (k+1)-th expert in place of the k-th":
+        lambda x, k, m: (lambda r: (np.concatenate([r[0][:, :k - 1], r[0][:, k:k + 1]], axis=1)
+                                    if r[0].shape[1] > k else r[0], r[1][:, :k]))(
+            oracle.router_topk(x, min(k + 1, np.asarray(x).shape[1]), m)),
+}
+
+
+def test_router_pins_pass_on_the_oracle():
+    assert router_pin_failures(oracle.router_topk) == []
+
+
+@pytest.mark.parametrize("name", sorted(ROUTER_MUTANTS))
+def test_router_pins_catch_a_planted_mistake(name):
+    assert router_pin_failures(ROUTER_MUTANTS[name]), f"no pin caught: {name}"

@@ -8,7 +8,10 @@
 * MXFP8: the E4M3 decoder against torch's float8_e4m3fn on all 256 codes, E8M0 special
   values, the scale-hoist identity, all-unit scales, power-of-two scale shifts;
 * tile map: closed form of the prefix, brute-force decode, the static tile-count bound.
+* router top-k: a hand-worked example, the ranking invariants that define the selection uniquely,
+  brute force over every ordered choice on tiny inputs, the softmax against scipy's.
 """
+import itertools
 import math
 
 import numpy as np
@@ -332,6 +335,105 @@ def test_gated_forward_brute_force_and_silu_identity():
     diff = got - oracle.gated_forward(x, -w0, w1, gs)
     assert _rel(diff, _np_forward(x, w0, gs) * _np_forward(x, w1, gs)) < 1e-12
     assert np.all(oracle.gated_forward(x, np.zeros_like(w0), w1, gs) == 0.0)     # silu(0) = 0
+
+
+# ------------------------------------------------------------------------------ router top-k
+def _rank_key(v):
+    """Sort key of one logit: larger numbers first, NaN after every number."""
+    return (1, 0.0) if math.isnan(v) else (0, -v)
+
+
+def topk_ranking_ok(x, k, ids):
+    """The selection is the unique one these invariants allow: k distinct experts; none left out
+    ranks above one taken; taken experts in rank order, equal logits by ascending index; a left-out
+    expert tying the last taken one has a higher index than every taken expert of that logit."""
+    x = np.asarray(x, np.float64)
+    ids = np.asarray(ids)
+    if ids.shape != (x.shape[0], k):
+        return False
+    for row, sel in zip(x, ids):
+        if len(set(sel.tolist())) != k or sel.min() < 0 or sel.max() >= row.size:
+            return False
+        keys = [(_rank_key(row[e]), e) for e in sel]
+        if keys != sorted(keys):
+            return False
+        worst = max(keys)
+        rest = [(_rank_key(row[e]), e) for e in range(row.size) if e not in set(sel.tolist())]
+        if rest and min(rest) < worst:
+            return False
+    return True
+
+
+def test_router_topk_worked_example():
+    d = _golden.read("router_topk_example.txt")
+    x = d["logits"].astype(np.float32)
+    k = int(d["k"][0])
+    for mode, key in (("values", "values"), ("softmax", "softmax"), ("softmax_topk", "softmax_topk")):
+        ids, w = oracle.router_topk(x, k, mode)
+        assert np.array_equal(ids, d["ids"].astype(np.int64))
+        assert np.allclose(w, d[key], rtol=1e-15, atol=0.0, equal_nan=True)
+    _, v = oracle.router_topk(x, k)
+    assert np.signbit(v[2, 0]) and not np.signbit(v[2, 1])      # -0 at expert 0, then +0 at expert 1
+
+
+@pytest.mark.parametrize("seed", [61, 62, 63])
+def test_router_topk_ranking_invariants(seed):
+    rng = np.random.default_rng(seed)
+    t, e = 50, 24
+    x = rng.integers(-3, 4, size=(t, e)).astype(np.float32)   # few distinct values: many ties
+    x[rng.random((t, e)) < 0.1] = -np.inf
+    x[rng.random((t, e)) < 0.05] = np.nan
+    x[0] = np.nan                                              # a token of NaN logits only
+    x[1] = -np.inf
+    for k in (1, 2, 7, e):
+        ids, v = oracle.router_topk(x, k)
+        assert topk_ranking_ok(x, k, ids)
+        assert np.array_equal(v, np.take_along_axis(x.astype(np.float64), ids, axis=1), equal_nan=True)
+
+
+def test_router_topk_brute_force_over_ordered_choices():
+    """Every ordered choice of k experts, compared by its sequence of rank keys: the oracle's
+    selection is the best one (tiny E, so the enumeration is complete)."""
+    rng = np.random.default_rng(64)
+    for _ in range(40):
+        e = int(rng.integers(1, 7))
+        k = int(rng.integers(1, e + 1))
+        row = rng.integers(-2, 3, size=e).astype(np.float64)
+        row[rng.random(e) < 0.2] = np.nan
+        best = min(itertools.permutations(range(e), k), key=lambda p: [(_rank_key(row[i]), i) for i in p])
+        ids, _ = oracle.router_topk(row[None, :].astype(np.float32), k)
+        assert tuple(ids[0].tolist()) == best
+
+
+def test_router_topk_softmax_weights_against_scipy():
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(65)
+    x = (rng.standard_normal((40, 16)) * 3).astype(np.float32)
+    x[2, 5] = -np.inf
+    ids, w_all = oracle.router_topk(x, 16, "softmax")                 # k = E: every probability
+    ref = special.softmax(x.astype(np.float64), axis=1)
+    assert _rel(w_all, np.take_along_axis(ref, ids, axis=1)) < 1e-15
+    assert np.allclose(w_all.sum(axis=1), 1.0, rtol=1e-14, atol=0)
+    ids4, w4 = oracle.router_topk(x, 4, "softmax")
+    assert _rel(w4, np.take_along_axis(ref, ids4, axis=1)) < 1e-15
+    _, v4 = oracle.router_topk(x, 4, "values")
+    _, w4k = oracle.router_topk(x, 4, "softmax_topk")
+    assert _rel(w4k, special.softmax(v4, axis=1)) < 1e-15
+    # shifting every logit of a token leaves the selection and both softmax weights unchanged
+    ids_s, w_s = oracle.router_topk(x.astype(np.float64) + 7.25, 4, "softmax")     # exact in fp64
+    assert np.array_equal(ids_s, ids4) and _rel(w_s, w4) < 1e-12
+    _, w1 = oracle.router_topk(x, 1, "softmax_topk")
+    assert np.all(w1 == 1.0)
+
+
+def test_router_topk_bf16_logits_are_decoded_exactly():
+    rng = np.random.default_rng(66)
+    xb = torch.from_numpy(rng.standard_normal((30, 64)).astype(np.float32)).to(torch.bfloat16)
+    ids_b, w_b = oracle.router_topk(xb, 6, "softmax")
+    ids_f, w_f = oracle.router_topk(xb.float().numpy(), 6, "softmax")
+    assert np.array_equal(ids_b, ids_f) and np.array_equal(w_b, w_f)
+    raw = xb.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.router_topk(raw, 6)[0], ids_f)
 
 
 # --------------------------------------------------------------------- MoE permute / combine
