@@ -706,6 +706,20 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                         "unpermute_ms_python_loop": round(tc_loop * 1e3, 4)}
     del x, xs, outc, ws
     torch.cuda.empty_cache()
+    # router top-k (the front end): Mixtral-like 8192 tokens x 8 experts top-2, DeepSeek-like 4096
+    # tokens x 256 experts top-8, fp32 logits N(0, 1), softmax weights; a few MB per call, so the
+    # launch's latency rather than HBM bandwidth bounds it
+    res["router_topk"] = {}
+    for tt, ee, kk in ((8192, 8, 2), (4096, 256, 8)):
+        lg = ri.device_normal((tt, ee), 4100 + ee, 1.0, dev, torch.float32)
+        ids_t = torch.empty((tt, kk), dtype=torch.int32, device=dev)
+        w_t = torch.empty((tt, kk), dtype=torch.float32, device=dev)
+        tr = _time_graph(lambda st: gg.rdot_router_topk(lg, kk, gg.RDOT_ROUTER_SOFTMAX, ids_t, w_t, st), dev)
+        rb = tt * ee * 4 + tt * kk * 8
+        res["router_topk"][f"T{tt}_E{ee}_k{kk}"] = {"us": round(tr * 1e6, 2), "bytes": rb,
+                                                    "hbm_gbs_algorithmic": round(rb / tr / 1e9, 1),
+                                                    "frac_of_hbm": round(rb / tr / 1e9 / peaks["hbm_gbs"], 4)}
+        del lg, ids_t, w_t
     # weight gradient
     cfg = ri.CONFIGS["wgrad_bf16"]
     m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]

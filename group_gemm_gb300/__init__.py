@@ -23,7 +23,8 @@ __all__ = [
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_no_alloc_read_status", "rdot_grad_input", "rdot_moe_route_workspace_size",
-    "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
+    "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "rdot_router_topk",
+    "router_topk", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
     "grad_input", "ragged_dot_gated",
     "ragged_dot_mxfp8", "padded_ragged_dot", "EXPORTED_SYMBOLS",
 ]
@@ -37,6 +38,8 @@ RDOT_STATUS_BIT_GROUP_SIZES, RDOT_STATUS_BIT_TIMEOUT = 0x1, 0x2
 RDOT_FLAG_ROW_TILES_INNER, RDOT_FLAG_COL_TILES_INNER = 0x1, 0x2
 RDOT_FLAG_CTA_PAIR, RDOT_FLAG_NO_CTA_PAIR, RDOT_FLAG_NATURAL_ORDER = 0x4, 0x8, 0x10
 RDOT_MAX_GROUPS = 1024
+RDOT_ROUTER_VALUES, RDOT_ROUTER_SOFTMAX, RDOT_ROUTER_SOFTMAX_TOPK, RDOT_ROUTER_MAX_TOPK = 0, 1, 2, 32
+_ROUTER_MODES = {"values": RDOT_ROUTER_VALUES, "softmax": RDOT_ROUTER_SOFTMAX, "softmax_topk": RDOT_ROUTER_SOFTMAX_TOPK}
 
 # every function include/rdot.h declares
 EXPORTED_SYMBOLS = (
@@ -45,7 +48,7 @@ EXPORTED_SYMBOLS = (
     "rdot_clear_status", "rdot_debug_offsets_tilemap", "rdot_plan_info", "rdot_debug_wait_timeout",
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_no_alloc_read_status", "rdot_grad_input", "rdot_moe_route_workspace_size",
-    "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8",
+    "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "rdot_router_topk",
 )
 
 _DTYPE_CODES = {"f32": RDOT_F32, "bf16": RDOT_BF16, "e4m3": RDOT_E4M3}
@@ -116,6 +119,8 @@ def load():
             "rdot_version": ([], ctypes.c_int),
             "rdot_forward_no_alloc": ([vp, vp, vp, vp, vp, vp], st),
             "rdot_no_alloc_read_status": ([vp, i32p, vp], st),
+            "rdot_router_topk": ([vp, ctypes.c_int32, i64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp],
+                                 st),
         }
         for name, (args, res) in sig.items():
             f = getattr(lib, name)
@@ -209,6 +214,17 @@ def rdot_moe_unpermute(y_sorted, inv, topk_weights, out, stream=None) -> None:
     _check(load().rdot_moe_unpermute(_ptr(y_sorted), _ptr(inv), _ptr(topk_weights), int(t), int(k),
                                      int(y_sorted.shape[1]), _ptr(out), _stream(stream, out.device)),
            "rdot_moe_unpermute")
+
+
+def rdot_router_topk(logits, topk: int, weights_mode: int, topk_ids, topk_weights, stream=None) -> None:
+    """logits [T, E] fp32 or bf16 -> topk_ids int32 [T, k], topk_weights fp32 [T, k]."""
+    import torch
+    t, e = logits.shape
+    dt = {torch.float32: RDOT_F32, torch.bfloat16: RDOT_BF16}.get(logits.dtype)
+    if dt is None:
+        raise TypeError("logits must be float32 or bfloat16")
+    _check(load().rdot_router_topk(_ptr(logits), dt, int(t), int(e), int(topk), int(weights_mode), _ptr(topk_ids),
+                                   _ptr(topk_weights), _stream(stream, logits.device)), "rdot_router_topk")
 
 
 def rdot_padded_workspace_size(plan, capacity: int) -> int:
@@ -403,6 +419,18 @@ def ragged_dot_gated(lhs, w0, w1, group_sizes, out_dtype=None, out=None, stream=
     rdot_forward_gated(plan.handle, lhs.contiguous(), w0.contiguous(), w1.contiguous(),
                        group_sizes.to(torch.int32).contiguous(), out, plan.workspace, stream)
     return out
+
+
+def router_topk(logits, k, weights="softmax_topk", stream=None):
+    """Each token's top-k experts and their weights: returns ``(ids int32 [T, k], w fp32 [T, k])``.
+    ``weights``: "values" (the logits), "softmax" (over all experts) or "softmax_topk" (over the k)."""
+    import torch
+    logits = logits.contiguous()
+    t = logits.shape[0]
+    ids = torch.empty((t, k), dtype=torch.int32, device=logits.device)
+    w = torch.empty((t, k), dtype=torch.float32, device=logits.device)
+    rdot_router_topk(logits, k, _ROUTER_MODES[weights], ids, w, stream)
+    return ids, w
 
 
 def moe_permute(topk_ids, x, n_experts, stream=None):

@@ -1049,6 +1049,27 @@ rdot_status rdot_moe_unpermute(const void* y_sorted, const int32_t* inv, const f
     return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "moe un-permute launch");
 }
 
+rdot_status rdot_router_topk(const void* logits, int32_t dtype, int64_t tokens, int32_t n_experts, int32_t topk,
+                             int32_t weights, int32_t* topk_ids, float* topk_weights, void* stream) {
+    if (tokens < 0 || n_experts < 1 || topk < 1 || (dtype != RDOT_F32 && dtype != RDOT_BF16) ||
+        (weights != RDOT_ROUTER_VALUES && weights != RDOT_ROUTER_SOFTMAX && weights != RDOT_ROUTER_SOFTMAX_TOPK))
+        return RDOT_ERR_INVALID_ARG;
+    if (topk > n_experts) return RDOT_ERR_INVALID_ARG;
+    if (n_experts > RDOT_MAX_GROUPS || topk > RDOT_ROUTER_MAX_TOPK ||
+        tokens * static_cast<int64_t>(n_experts) > 0x7fffffffffffLL || tokens * static_cast<int64_t>(topk) > 0x7fffffffLL)
+        return RDOT_ERR_UNSUPPORTED;
+    if (tokens == 0) return RDOT_OK;
+    if (!logits || !topk_ids || !topk_weights) return RDOT_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(logits) & (dtype == RDOT_F32 ? 3u : 1u)) || !aligned4(topk_ids) ||
+        !aligned4(topk_weights))
+        return RDOT_ERR_INVALID_ARG;
+    const int sms = current_sm_count();
+    if (sms <= 0) return cuda_fail(cudaGetLastError(), "cudaDeviceGetAttribute");
+    cudaError_t e = launch_router_topk(logits, dtype == RDOT_BF16, tokens, n_experts, topk, weights, topk_ids,
+                                       topk_weights, sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "router top-k launch");
+}
+
 const char* rdot_status_string(rdot_status status) {
     switch (status) {
         case RDOT_OK: return "RDOT_OK";

@@ -149,6 +149,11 @@ cudaError_t launch_moe_permute(const int32_t* ids, long long tokens, int k, int 
 cudaError_t launch_moe_combine(const void* y_sorted, const int32_t* inv, const float* weights, long long tokens, int k,
                                long long n, void* out, int sm_count, cudaStream_t stream);
 
+// Router top-k (route.cu): logits [tokens, E] (fp32, or bf16 when bf16) -> ids / weights
+// [tokens, k]; E <= 1024, k <= min(32, E); mode 0 values, 1 softmax over all E, 2 softmax over k.
+cudaError_t launch_router_topk(const void* logits, bool bf16, long long tokens, int E, int k, int mode, int32_t* ids,
+                               float* weights, int sm_count, cudaStream_t stream);
+
 // Padded-dense baseline data movement (padded.cu).
 cudaError_t launch_pad_scatter(const void* lhs, const int32_t* gs, void* lhs_pad, int32_t* uniform_gs, int M, int G,
                                int C, long long row_bytes, int grid, int32_t* status, cudaStream_t stream);

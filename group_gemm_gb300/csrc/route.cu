@@ -224,7 +224,108 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restric
     }
 }
 
+// ------------------------------------------------------------------------------- router top-k
+// The router front end shared by the MoE paths ("Group-GEMM in XLA", Part 4 "The Three MoE Compute
+// Paths in MaxText": jax.lax.top_k over the gate logits): each token's k highest logits, ranked by
+// value with equal values to the lower expert index, and a weight per selected expert.
+//
+// One warp per token; lane l holds experts l, l + 32, ... as 64-bit keys whose high word orders
+// the logits (sign-magnitude bits mapped to an unsigned order, -0 folded onto +0, NaN below
+// every number) and whose low word is ~expert, so the largest key is the highest logit with the
+// lowest index among equals. k rounds of a warp-wide max pick the winners in rank order.
+__device__ __forceinline__ uint32_t logit_order(float f) {
+    if (f != f) return 0u;                                       // NaN: below -inf
+    const uint32_t b = __float_as_uint(f == 0.0f ? 0.0f : f);   // -0 and +0 rank equal
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load_logit(const void* p, long long i) {
+    if (BF16) return __uint_as_float(static_cast<uint32_t>(__ldg(static_cast<const unsigned short*>(p) + i)) << 16);
+    return __ldg(static_cast<const float*>(p) + i);
+}
+
+template <int IPL, bool BF16>
+__global__ void __launch_bounds__(256) router_topk_kernel(const void* __restrict__ logits, long long tokens, int E,
+                                                          int k, int mode, int32_t* __restrict__ ids,
+                                                          float* __restrict__ weights) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    for (long long t = warp; t < tokens; t += nwarps) {
+        const long long row = t * E;
+        float v[IPL];
+        unsigned long long key[IPL];
+#pragma unroll
+        for (int i = 0; i < IPL; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = e < E ? load_logit<BF16>(logits, row + e) : 0.0f;
+            key[i] = e < E ? (static_cast<unsigned long long>(logit_order(v[i])) << 32) | (0xFFFFFFFFu - e) : 0ull;
+        }
+        unsigned long long mine = 0ull;   // lane r < k: the key of the r-th winner
+        for (int r = 0; r < k; ++r) {
+            unsigned long long best = key[0];
+#pragma unroll
+            for (int i = 1; i < IPL; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, d);
+                best = o > best ? o : best;
+            }
+            if (lane == r) mine = best;
+#pragma unroll
+            for (int i = 0; i < IPL; ++i)
+                if (key[i] == best) key[i] = 0ull;   // keys are unique: exactly one item leaves
+        }
+        const int my_e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine));
+        // the winner's logit as stored (a -0 stays -0); lanes past k read nothing
+        const float my_v = lane < k ? load_logit<BF16>(logits, row + my_e) : 0.0f;
+        float w = my_v;
+        if (mode != 0) {
+            const float m = __shfl_sync(0xffffffffu, my_v, 0);   // the top-ranked logit
+            float s = 0.0f;
+            if (mode == 1) {
+#pragma unroll
+                for (int i = 0; i < IPL; ++i)
+                    if (lane + 32 * i < E) s += expf(v[i] - m);
+            } else if (lane < k) {
+                s = expf(my_v - m);
+            }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) s += __shfl_xor_sync(0xffffffffu, s, d);
+            w = expf(my_v - m) / s;
+        }
+        if (lane < k) {
+            ids[t * k + lane] = my_e;
+            weights[t * k + lane] = w;
+        }
+    }
+}
+
+template <int IPL>
+cudaError_t launch_topk_ipl(const void* logits, bool bf16, long long tokens, int E, int k, int mode, int32_t* ids,
+                            float* weights, int grid, cudaStream_t stream) {
+    if (bf16)
+        router_topk_kernel<IPL, true><<<grid, 256, 0, stream>>>(logits, tokens, E, k, mode, ids, weights);
+    else
+        router_topk_kernel<IPL, false><<<grid, 256, 0, stream>>>(logits, tokens, E, k, mode, ids, weights);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_router_topk(const void* logits, bool bf16, long long tokens, int E, int k, int mode, int32_t* ids,
+                               float* weights, int sm_count, cudaStream_t stream) {
+    const long long want = (tokens + 7) / 8;
+    const int grid = static_cast<int>(want < 16LL * sm_count ? want : 16LL * sm_count);
+    if (E <= 32) return launch_topk_ipl<1>(logits, bf16, tokens, E, k, mode, ids, weights, grid, stream);
+    if (E <= 64) return launch_topk_ipl<2>(logits, bf16, tokens, E, k, mode, ids, weights, grid, stream);
+    if (E <= 128) return launch_topk_ipl<4>(logits, bf16, tokens, E, k, mode, ids, weights, grid, stream);
+    if (E <= 256) return launch_topk_ipl<8>(logits, bf16, tokens, E, k, mode, ids, weights, grid, stream);
+    if (E <= 512) return launch_topk_ipl<16>(logits, bf16, tokens, E, k, mode, ids, weights, grid, stream);
+    if (E <= 1024) return launch_topk_ipl<32>(logits, bf16, tokens, E, k, mode, ids, weights, grid, stream);
+    return cudaErrorInvalidValue;
+}
 
 size_t moe_route_workspace_bytes(long long total, int E) {
     const long long nchunks = (total + CHUNK - 1) / CHUNK;

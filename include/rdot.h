@@ -221,6 +221,31 @@ RDOT_API rdot_status rdot_moe_permute(const int32_t* topk_ids, int64_t tokens, i
                              const void* x, int64_t row_bytes, int32_t* group_sizes, int32_t* order,
                              int32_t* inv, void* x_sorted, void* workspace, void* stream);
 
+/* Router top-k, the front end the MoE paths share ("Group-GEMM in XLA", Part 4 "The Three MoE
+ * Compute Paths in MaxText": top_k_weights, top_k_indices = jax.lax.top_k(gate_logits, k); "How to
+ * Scale Your Model on AMD", ch. 6 "Router to expert and back", step 1). Its ids feed
+ * rdot_moe_permute, its weights rdot_moe_unpermute.
+ *   logits        device [T, E], dtype RDOT_F32 or RDOT_BF16 (4- or 2-byte aligned)
+ *   topk_ids      device int32 [T, k] out: each token's k experts, highest logit first; equal
+ *                 logits (+0 and -0 are equal) put the lower expert index first; NaN ranks below
+ *                 every number, -inf included
+ *   topk_weights  device fp32 [T, k] out, by `weights`:
+ *                   RDOT_ROUTER_VALUES        the selected logits as stored (what jax.lax.top_k returns)
+ *                   RDOT_ROUTER_SOFTMAX       softmax over all E logits of the token, at the selected
+ *                   RDOT_ROUTER_SOFTMAX_TOPK  softmax over the k selected logits (sums to one)
+ *                 softmax(x)_e = exp(x_e - m) / sum_j exp(x_j - m), m the top-ranked logit, in fp32;
+ *                 a NaN logit in the sum makes the token's weights NaN
+ * 1 <= k <= min(E, RDOT_ROUTER_MAX_TOPK), E <= RDOT_MAX_GROUPS, T*k < 2^31, else
+ * RDOT_ERR_UNSUPPORTED / RDOT_ERR_INVALID_ARG. The selection compares the logits themselves, so
+ * the ids are exact; runs on the calling thread's current device; T = 0 launches nothing. */
+#define RDOT_ROUTER_VALUES 0
+#define RDOT_ROUTER_SOFTMAX 1
+#define RDOT_ROUTER_SOFTMAX_TOPK 2
+#define RDOT_ROUTER_MAX_TOPK 32
+RDOT_API rdot_status rdot_router_topk(const void* logits, int32_t dtype, int64_t tokens, int32_t n_experts,
+                                      int32_t topk, int32_t weights, int32_t* topk_ids, float* topk_weights,
+                                      void* stream);
+
 /* rdot_moe_unpermute combines each token's k expert outputs, weighted by the router:
  *   out[t, :] = sum_j topk_weights[t, j] * y_sorted[inv[t*k + j], :] over the copies kept,
  * accumulated in fp32 and stored as bf16 (round to nearest even).

@@ -90,3 +90,19 @@ def test_moe_route_argument_checks_without_gpu(lib):
     assert lib.rdot_moe_unpermute(gs, gs, gs, 10, 2, 12, gs, None) == gg.RDOT_ERR_UNSUPPORTED                 # n % 8
     assert lib.rdot_moe_unpermute(gs, gs, gs, 10, 2, 1 << 40, gs, None) == gg.RDOT_ERR_UNSUPPORTED            # n / 8 >= 2^31
     assert lib.rdot_moe_unpermute(gs, gs, gs, -1, 2, 16, gs, None) == gg.RDOT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args, status", [
+    ((gg.RDOT_F32, 4, 40, 33, 0), gg.RDOT_ERR_UNSUPPORTED),                 # k above the 32 a warp holds
+    ((gg.RDOT_F32, 4, 8, 9, 0), gg.RDOT_ERR_INVALID_ARG),                   # k above E
+    ((gg.RDOT_F32, 4, gg.RDOT_MAX_GROUPS + 1, 2, 0), gg.RDOT_ERR_UNSUPPORTED),
+    ((gg.RDOT_E4M3, 4, 8, 2, 0), gg.RDOT_ERR_INVALID_ARG),                  # logits are fp32 or bf16
+    ((gg.RDOT_F32, 4, 8, 2, 3), gg.RDOT_ERR_INVALID_ARG),                   # unknown weight mode
+    ((gg.RDOT_F32, -1, 8, 2, 0), gg.RDOT_ERR_INVALID_ARG),
+    ((gg.RDOT_F32, 4, 8, 0, 0), gg.RDOT_ERR_INVALID_ARG),
+    ((gg.RDOT_F32, 4, 8, 2, 0), gg.RDOT_ERR_INVALID_ARG),                   # null pointers
+    ((gg.RDOT_BF16, 0, 8, 2, 1), gg.RDOT_OK),                               # no tokens: nothing to do
+])
+def test_router_topk_argument_checks(lib, args, status):
+    dt, t, e, k, mode = args
+    assert lib.rdot_router_topk(None, dt, t, e, k, mode, None, None, None) == status
