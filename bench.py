@@ -674,6 +674,31 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                                     "un-permute", "ms": round(tl * 1e3, 4), "tflops": round(fl_l / tl / 1e12, 3),
                         "frac_of_bf16_peak": round(fl_l / tl / 1e12 / peaks["bf16_tflops"], 4),
                         "launches_per_layer": 4 + 1 + 1 + 1}
+
+    # the same layer with the weighted un-permute fused into the down projection's epilogue
+    # (fp32 [T, N] out, cleared by a memset, each copy's row added with fp32 reductions)
+    def layer_fused():
+        xs_l, gs_l, order_l, _ = gg.moe_permute(ids_l, x_l, g, stream)
+        h_l = gg.ragged_dot_gated(xs_l, w0_l, w1_l, gs_l, stream=stream)
+        return gg.ragged_dot_combine(h_l, wo_l, gs_l, order_l, wr_l, stream=stream)
+    tlf = _time_steps(layer_fused, max(5, steps // 3), stream)
+    # the down projection step alone, both ways: ragged dot + un-permute vs the fused call
+    xs_l, gs_l, order_l, inv_l = gg.moe_permute(ids_l, x_l, g, stream)
+    h_l = gg.ragged_dot_gated(xs_l, w0_l, w1_l, gs_l, stream=stream)
+    y_l = torch.empty((t_l * k_l, k), dtype=torch.bfloat16, device=dev)
+    o_l = torch.empty((t_l, k), dtype=torch.bfloat16, device=dev)
+    of_l = torch.empty((t_l, k), dtype=torch.float32, device=dev)
+    t_down = _time_steps(lambda: (gg.ragged_dot(h_l, wo_l, gs_l, out=y_l, stream=stream),
+                                  gg.moe_unpermute(y_l, inv_l, wr_l, out=o_l, stream=stream)), steps, stream)
+    t_down_fused = _time_steps(lambda: gg.ragged_dot_combine(h_l, wo_l, gs_l, order_l, wr_l, out=of_l, stream=stream),
+                               steps, stream)
+    res["moe_layer_fused_combine"] = {
+        "workload": res["moe_layer"]["workload"] + "; un-permute fused into the down projection (fp32 out)",
+        "ms": round(tlf * 1e3, 4), "tflops": round(fl_l / tlf / 1e12, 3),
+        "frac_of_bf16_peak": round(fl_l / tlf / 1e12 / peaks["bf16_tflops"], 4),
+        "launches_per_layer": 4 + 1 + 1 + 1, "speedup_vs_unfused_layer": round(tl / tlf, 4),
+        "down_plus_unpermute_ms": round(t_down * 1e3, 4), "down_fused_combine_ms": round(t_down_fused * 1e3, 4)}
+    del xs_l, h_l, y_l, o_l, of_l
     del x_l, w0_l, w1_l, wo_l
     torch.cuda.empty_cache()
     # MoE permute / un-permute around the Mixtral-like layer: 8192 tokens, top-2 of 8, width 4096

@@ -24,7 +24,7 @@ __all__ = [
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_no_alloc_read_status", "rdot_grad_input", "rdot_moe_route_workspace_size",
     "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "rdot_router_topk",
-    "router_topk", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
+    "rdot_forward_combine", "router_topk", "ragged_dot_combine", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
     "grad_input", "ragged_dot_gated",
     "ragged_dot_mxfp8", "padded_ragged_dot", "EXPORTED_SYMBOLS",
 ]
@@ -49,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_no_alloc_read_status", "rdot_grad_input", "rdot_moe_route_workspace_size",
     "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "rdot_router_topk",
+    "rdot_forward_combine",
 )
 
 _DTYPE_CODES = {"f32": RDOT_F32, "bf16": RDOT_BF16, "e4m3": RDOT_E4M3}
@@ -119,6 +120,7 @@ def load():
             "rdot_version": ([], ctypes.c_int),
             "rdot_forward_no_alloc": ([vp, vp, vp, vp, vp, vp], st),
             "rdot_no_alloc_read_status": ([vp, i32p, vp], st),
+            "rdot_forward_combine": ([vp, vp, vp, vp, vp, vp, i64, ctypes.c_int32, vp, vp, vp], st),
             "rdot_router_topk": ([vp, ctypes.c_int32, i64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp],
                                  st),
         }
@@ -214,6 +216,14 @@ def rdot_moe_unpermute(y_sorted, inv, topk_weights, out, stream=None) -> None:
     _check(load().rdot_moe_unpermute(_ptr(y_sorted), _ptr(inv), _ptr(topk_weights), int(t), int(k),
                                      int(y_sorted.shape[1]), _ptr(out), _stream(stream, out.device)),
            "rdot_moe_unpermute")
+
+
+def rdot_forward_combine(plan, lhs, rhs, group_sizes, order, topk_weights, out, workspace, stream=None) -> None:
+    """Down projection with the router-weighted un-permute fused: out fp32 [T, N]."""
+    t, k = topk_weights.shape
+    _check(load().rdot_forward_combine(plan, _ptr(lhs), _ptr(rhs), _ptr(group_sizes), _ptr(order),
+                                       _ptr(topk_weights), int(t), int(k), _ptr(out), _ptr(workspace),
+                                       _stream(stream, out.device)), "rdot_forward_combine")
 
 
 def rdot_router_topk(logits, topk: int, weights_mode: int, topk_ids, topk_weights, stream=None) -> None:
@@ -418,6 +428,24 @@ def ragged_dot_gated(lhs, w0, w1, group_sizes, out_dtype=None, out=None, stream=
         out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
     rdot_forward_gated(plan.handle, lhs.contiguous(), w0.contiguous(), w1.contiguous(),
                        group_sizes.to(torch.int32).contiguous(), out, plan.workspace, stream)
+    return out
+
+
+def ragged_dot_combine(lhs, rhs, group_sizes, order, topk_weights, out=None, stream=None):
+    """``out[t] = sum_j w[t, j] * (lhs @ rhs[g])[inv[t*k + j]]`` in one pass (fp32 [T, N]): the down
+    projection over the permuted rows with the weighted un-permute fused into its epilogue."""
+    import torch
+    m, kdim = lhs.shape
+    g, _, n = rhs.shape
+    t, k = topk_weights.shape
+    if out is None:
+        out = torch.empty((t, n), dtype=torch.float32, device=lhs.device)
+    key = ("fwd", m, kdim, n, g, "bf16", torch.float32, lhs.device)     # the fp32-out forward's plan
+    plan = _cached_plan(key, m=m, k=kdim, n=n, groups=g, mode="forward", in_dtype="bf16", out_dtype="f32",
+                        device=lhs.device)
+    rdot_forward_combine(plan.handle, lhs.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(),
+                         order.to(torch.int32).contiguous(),
+                         topk_weights.to(torch.float32).contiguous(), out, plan.workspace, stream)
     return out
 
 

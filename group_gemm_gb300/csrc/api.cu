@@ -507,20 +507,25 @@ rdot_status rdot_set_wait_timeout(rdot_plan_t plan, uint64_t timeout_ns) {
     return RDOT_OK;
 }
 
-rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, const int32_t* group_sizes, void* out,
-                         void* workspace, void* stream) {
-    if (!plan || !group_sizes || !workspace) return RDOT_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Combine operands of the fused un-permute (all null for a plain forward).
+struct CombineArgs {
+    const int32_t* order = nullptr;
+    const float* weights = nullptr;
+    int k = 0;
+};
+
+// The forward launch shared by rdot_forward and rdot_forward_combine; arguments already checked.
+rdot_status forward_launch(rdot_plan_t plan, const void* lhs, const void* rhs, const int32_t* group_sizes, void* out,
+                           void* workspace, cudaStream_t s, const CombineArgs& comb) {
     const rdot_problem& p = plan->p;
-    if (p.mode != RDOT_MODE_FORWARD) return RDOT_ERR_INVALID_ARG;
-    if (p.m == 0) return RDOT_OK;
-    if (!lhs || !rhs || !out) return RDOT_ERR_INVALID_ARG;
-    if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || !aligned16(workspace) ||
-        (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
-        return RDOT_ERR_INVALID_ARG;
-    DeviceGuard dg(plan->device);
-    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     FwdArgs a{};
+    a.comb_order = comb.order;
+    a.comb_weights = comb.weights;
+    a.comb_k = comb.k;
     a.group_sizes = group_sizes;
     a.out = out;
     a.M = static_cast<int>(p.m);
@@ -564,6 +569,53 @@ rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, con
     }
     if (e != cudaSuccess) return cuda_fail(e, "fwd_tc launch");
     return RDOT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs, const int32_t* group_sizes, void* out,
+                         void* workspace, void* stream) {
+    if (!plan || !group_sizes || !workspace) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.mode != RDOT_MODE_FORWARD) return RDOT_ERR_INVALID_ARG;
+    if (p.m == 0) return RDOT_OK;
+    if (!lhs || !rhs || !out) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    return forward_launch(plan, lhs, rhs, group_sizes, out, workspace, static_cast<cudaStream_t>(stream),
+                          CombineArgs{});
+}
+
+rdot_status rdot_forward_combine(rdot_plan_t plan, const void* lhs, const void* rhs, const int32_t* group_sizes,
+                                 const int32_t* order, const float* topk_weights, int64_t tokens, int32_t topk,
+                                 float* out, void* workspace, void* stream) {
+    if (!plan || !group_sizes || !workspace || tokens < 0 || topk < 1) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.mode != RDOT_MODE_FORWARD || plan->kind != 1) return RDOT_ERR_INVALID_ARG;
+    if (p.out_dtype != RDOT_F32 || plan->wide) return RDOT_ERR_UNSUPPORTED;
+    if (tokens * static_cast<int64_t>(topk) != p.m) return RDOT_ERR_INVALID_ARG;
+    if (p.m == 0) return RDOT_OK;
+    if (!lhs || !rhs || !out || !order || !topk_weights) return RDOT_ERR_INVALID_ARG;
+    if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(group_sizes) & 3u) || (reinterpret_cast<uintptr_t>(order) & 3u) ||
+        (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // every token row starts from zero: the kernels add each copy's weighted row into it
+    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * static_cast<size_t>(tokens) * static_cast<size_t>(p.n), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    CombineArgs comb;
+    comb.order = order;
+    comb.weights = topk_weights;
+    comb.k = topk;
+    return forward_launch(plan, lhs, rhs, group_sizes, out, workspace, s, comb);
 }
 
 rdot_status rdot_grad_input_mxfp8(rdot_plan_t plan, const void* dy_q, const uint8_t* dy_scale, const void* w_q,

@@ -66,6 +66,56 @@ __device__ __forceinline__ void store_block_32x32(const uint32_t (&v)[32], uint3
     __syncwarp();
 }
 
+// out[0..3] += (a, b, c, d): one 16-byte fp32 reduction in L2 (no return value).
+__device__ __forceinline__ void red_add_f32x4(float* out, float a, float b, float c, float d) {
+    asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// The router-weighted un-permute fused into a forward's epilogue ("Group-GEMM in XLA", Part 4,
+// Path 1 post-processing: scatter back to token order, then the einsum "BKE,BK -> BE" with the
+// router weights). Row `lane` of the 32 x 32 fp32 block (v[j] = column j) belongs to token `tok`
+// with router weight `wt` (tok < 0: the row is not stored); each row is scaled and added into
+// row tok of `out` (pitch ld floats; out points at the block's first column). Lanes run along
+// the rows after the shared-memory transpose, so each reduction covers 16 contiguous bytes.
+// Must be called by all 32 lanes; cols_valid is a multiple of 4.
+__device__ __forceinline__ void combine_block_32x32(const uint32_t (&v)[32], uint32_t* stage, float* out, long long ld,
+                                                    int tok, float wt, int cols_valid) {
+    using S = EpiStage<true>;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stage[lane * S::ROW_WORDS + j] = v[j];
+    __syncwarp();
+    const int rr = lane >> 3, c4 = (lane & 7) * 4;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int row = it * 4 + rr;
+        const int tr = __shfl_sync(0xffffffffu, tok, row);
+        const float wr = __shfl_sync(0xffffffffu, wt, row);
+        if (tr >= 0 && c4 < cols_valid) {
+            const uint32_t* s = stage + row * S::ROW_WORDS + c4;
+            red_add_f32x4(out + static_cast<long long>(tr) * ld + c4, wr * __uint_as_float(s[0]),
+                          wr * __uint_as_float(s[1]), wr * __uint_as_float(s[2]), wr * __uint_as_float(s[3]));
+        }
+    }
+    __syncwarp();
+}
+
+// Destination token and router weight of sorted row p (the caller's lane) for the fused combine:
+// order[p] is the flat copy index t*k + j of the row (-1: no copy), weights the router's [T, k].
+__device__ __forceinline__ void combine_row_target(const int32_t* order, const float* weights, int k, long long p,
+                                                   bool valid, int& tok, float& wt) {
+    tok = -1;
+    wt = 0.0f;
+    if (valid) {
+        const int f = __ldg(order + p);
+        if (f >= 0) {
+            tok = f / k;
+            wt = __ldg(weights + f);
+        }
+    }
+}
+
 // Reads a warp's 32 rows x 128 columns of fp32 accumulator (TMEM columns taddr .. taddr+127 of
 // its lane quarter) as packed bf16: pk[c][j] holds columns 32c + 2j, 32c + 2j + 1 of row `lane`.
 // Two 32-column loads are in flight per wait, which halves the serialised load latency of an

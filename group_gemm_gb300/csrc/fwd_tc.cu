@@ -54,8 +54,9 @@ struct TcLayout {
 };
 
 // KMAJ: the data gradient's K-major B operand, a compile-time choice (a runtime branch costs
-// the forward a few per cent).
-template <int BN, int STAGES, bool OUT_F32, bool KMAJ>
+// the forward a few per cent). COMB: the router-weighted un-permute fused into the epilogue
+// (fp32 out [T, N], rows added into their tokens' rows; see combine_block_32x32).
+template <int BN, int STAGES, bool OUT_F32, bool KMAJ, bool COMB = false>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                   FwdArgs a) {
@@ -230,15 +231,33 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint8_t* out_rows = static_cast<uint8_t*>(a.out) +
                                 (static_cast<long long>(t.row0) + q * 32) * a.N * (OUT_F32 ? 4 : 2);
             uint32_t* stage = epi_stage + (warp - 2) * EpiStage<OUT_F32>::WORDS;
+            if constexpr (COMB) {
+                static_assert(OUT_F32 && !KMAJ, "the fused combine accumulates fp32 rows of the forward");
+                int tok;
+                float wt;
+                combine_row_target(a.comb_order, a.comb_weights, a.comb_k,
+                                   static_cast<long long>(t.row0) + q * 32 + lane, lane < rows_valid, tok, wt);
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, v);
-                tmem_ld_wait();
-                const int col = n0 + c * 32;
-                if (rows_valid > 0 && col < a.N)
-                    store_block_32x32<OUT_F32>(v, stage, out_rows + static_cast<long long>(col) * (OUT_F32 ? 4 : 2),
-                                               a.N, rows_valid, a.N - col);
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    const int col = n0 + c * 32;
+                    if (rows_valid > 0 && col < a.N)
+                        combine_block_32x32(v, stage, static_cast<float*>(a.out) + col, a.N, tok, wt, a.N - col);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    const int col = n0 + c * 32;
+                    if (rows_valid > 0 && col < a.N)
+                        store_block_32x32<OUT_F32>(v, stage,
+                                                   out_rows + static_cast<long long>(col) * (OUT_F32 ? 4 : 2), a.N,
+                                                   rows_valid, a.N - col);
+                }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -246,7 +265,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (acc == 0) acc_phase ^= 1;
         }
         // zero rows [off[G], M): one contiguous range, split over CTAs and the 128 epilogue threads
-        {
+        // (the fused combine's output is indexed by token and cleared by the caller instead)
+        if (!COMB) {
             const int esz = OUT_F32 ? 4 : 2;
             const long long b0 = static_cast<long long>(off[a.G]) * a.N * esz;
             const long long b1 = static_cast<long long>(a.M) * a.N * esz;   // both multiples of 16
@@ -276,6 +296,14 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const FwdAr
     using L = TcLayout<BN, STAGES, OUT_F32>;
     const size_t shm = L::smem_bytes(a.G);
     auto kern = a.b_kmajor ? fwd_tc_kernel<BN, STAGES, OUT_F32, true> : fwd_tc_kernel<BN, STAGES, OUT_F32, false>;
+    if constexpr (OUT_F32) {
+        if (a.comb_order) {
+            if (a.b_kmajor) return cudaErrorInvalidValue;
+            kern = fwd_tc_kernel<BN, STAGES, true, false, true>;
+        }
+    } else {
+        if (a.comb_order) return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
     kern<<<grid, THREADS, shm, stream>>>(ta, tb, a);

@@ -54,7 +54,9 @@ size_t smem_bytes(int G) {
 }
 
 // VAR: 0 = the forward (MN-major B), 1 = the data gradient (K-major B), 2 = the gated up
-// projection. A compile-time choice: runtime branches cost the forward 2.5 %.
+// projection, 3 = the forward with the router-weighted un-permute fused into the epilogue (fp32
+// rows added into their tokens' rows of out [T, N]). A compile-time choice: runtime branches
+// cost the forward 2.5 %.
 template <bool OUT_F32, int VAR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fwd_tc2_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -277,16 +279,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const int hcol0 = n0 + 128 * (q >> 1);
                 uint8_t* hout = static_cast<uint8_t*>(a.out) +
                                 (static_cast<long long>(t.row0) + hfirst) * a.N * (OUT_F32 ? 4 : 2);
+                int tok = -1;
+                float wt = 0.0f;
+                if constexpr (VAR == 3)
+                    combine_row_target(a.comb_order, a.comb_weights, a.comb_k,
+                                       static_cast<long long>(t.row0) + hfirst + lane, lane < hrows, tok, wt);
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; ++c) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tbase + c * 32, v);
                     tmem_ld_wait();
                     const int col = hcol0 + c * 32;
-                    if (hrows > 0 && col < a.N)
-                        store_block_32x32<OUT_F32>(v, stage_buf,
-                                                   hout + static_cast<long long>(col) * (OUT_F32 ? 4 : 2), a.N,
-                                                   hrows, a.N - col);
+                    if (hrows > 0 && col < a.N) {
+                        if constexpr (VAR == 3)
+                            combine_block_32x32(v, stage_buf, static_cast<float*>(a.out) + col, a.N, tok, wt,
+                                                a.N - col);
+                        else
+                            store_block_32x32<OUT_F32>(v, stage_buf,
+                                                       hout + static_cast<long long>(col) * (OUT_F32 ? 4 : 2), a.N,
+                                                       hrows, a.N - col);
+                    }
+                }
+            } else if (VAR == 3) {
+                int tok;
+                float wt;
+                combine_row_target(a.comb_order, a.comb_weights, a.comb_k,
+                                   static_cast<long long>(t.row0) + first + lane, lane < rows_valid, tok, wt);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    const int col = n0 + c * 32;
+                    if (rows_valid > 0 && col < a.N)
+                        combine_block_32x32(v, stage_buf, static_cast<float*>(a.out) + col, a.N, tok, wt, a.N - col);
                 }
             } else {
 #pragma unroll 1
@@ -307,7 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
-        {
+        if (VAR != 3) {   // the fused combine's output is indexed by token and cleared by the caller
             const int esz = OUT_F32 ? 4 : 2;
             const long long b0 = static_cast<long long>(off[a.G]) * a.N * esz;
             const long long b1 = static_cast<long long>(a.M) * a.N * esz;
@@ -347,11 +373,13 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
 cudaError_t launch_fwd_tc2(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const FwdArgs& a, bool out_f32,
                            int grid, cudaStream_t stream, const CUtensorMap* tmap_b1, const CUtensorMap* tmap_a64) {
     if (grid % 2 || (a.gated && (!tmap_b1 || a.b_kmajor)) || (a.a64 && !tmap_a64)) return cudaErrorInvalidValue;
+    if (a.comb_order && (!out_f32 || a.gated || a.b_kmajor)) return cudaErrorInvalidValue;
     const CUtensorMap& tb1 = tmap_b1 ? *tmap_b1 : tmap_b;
     const CUtensorMap& ta64 = tmap_a64 ? *tmap_a64 : tmap_a;
     if (a.gated)
         return out_f32 ? launch_one<true, 2>(tmap_a, tmap_b, tb1, ta64, a, grid, stream)
                        : launch_one<false, 2>(tmap_a, tmap_b, tb1, ta64, a, grid, stream);
+    if (a.comb_order) return launch_one<true, 3>(tmap_a, tmap_b, tb1, ta64, a, grid, stream);
     if (a.b_kmajor)
         return out_f32 ? launch_one<true, 1>(tmap_a, tmap_b, tb1, ta64, a, grid, stream)
                        : launch_one<false, 1>(tmap_a, tmap_b, tb1, ta64, a, grid, stream);

@@ -32,6 +32,12 @@ struct FwdArgs {
                                  // per tile (N = the width of w0, w1 and out)
     int32_t* status;             // device status word (may be null)
     uint64_t timeout_ns;         // bounded-wait limit
+    // fused router-weighted un-permute (fp32 out [T, N], MN-major B only): when comb_order is set,
+    // sorted row p is scaled by comb_weights[comb_order[p]] and added into out row
+    // comb_order[p] / comb_k instead of being stored at row p
+    const int32_t* comb_order;
+    const float* comb_weights;
+    int comb_k;
 };
 
 // Static upper bound on the work items of a forward: sum_g ceil(m_g/BM) <= ceil(M/BM) + G.

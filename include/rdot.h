@@ -135,6 +135,30 @@ RDOT_API rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes);
 RDOT_API rdot_status rdot_forward(rdot_plan_t plan, const void* lhs, const void* rhs,
                          const int32_t* group_sizes, void* out, void* workspace, void* stream);
 
+/* Forward with the router-weighted un-permute fused into its epilogue: the down projection of an
+ * MoE expert layer followed by the scatter back to token order and the weighted sum over each
+ * token's k copies ("Group-GEMM in XLA", Part 4 "The Three MoE Compute Paths in MaxText", Path 1
+ * post-processing: unsorted = the rows back in token order, output = einsum("BKE,BK -> BE",
+ * unsorted, top_k_weights); Part 5 "Next steps"), without the [T*k, N] intermediate:
+ *   out[t, :] = sum over sorted rows p with order[p] / topk == t of
+ *               topk_weights[order[p]] * (lhs[p, :] @ rhs[g(p)])
+ *   lhs           device bf16 [T*topk, K]: rows in rdot_moe_permute's sorted order
+ *   rhs           device bf16 [G, K, N]
+ *   group_sizes   device int32 [G] (from rdot_moe_permute)
+ *   order         device int32 [T*topk] (from rdot_moe_permute): flat copy index t*topk + j of each
+ *                 sorted row, -1 for none (those rows contribute nothing)
+ *   topk_weights  device fp32 [T, topk]
+ *   out           device fp32 [T, N]; cleared on the stream first, then every copy's weighted row
+ *                 is added with fp32 reductions (the sum of a token's copies is exact for topk <= 2;
+ *                 for more copies the order of the additions, and so the last bit, may vary)
+ * The plan is an ordinary forward plan with m = T*topk, in_dtype RDOT_BF16 and out_dtype RDOT_F32
+ * (RDOT_ERR_UNSUPPORTED otherwise, and for tile_n = 512); same workspace and stream rules as
+ * rdot_forward. */
+RDOT_API rdot_status rdot_forward_combine(rdot_plan_t plan, const void* lhs, const void* rhs,
+                                          const int32_t* group_sizes, const int32_t* order,
+                                          const float* topk_weights, int64_t tokens, int32_t topk, float* out,
+                                          void* workspace, void* stream);
+
 /* MXFP8 forward (AITER PR #5658 "Merge MoE MXFP8 GEMM into _moe_gemm_a8w8": OCP E4M3 operands,
  * one E8M0 scale per 32 consecutive K elements, quant_block_size == 32, K % 32 == 0).
  *   lhs        device uint8 [M, K]   E4M3 codes

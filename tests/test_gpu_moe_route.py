@@ -190,3 +190,117 @@ def test_moe_layer_cuda_graph_replay_with_new_routing():
         graph.replay()
         torch.cuda.synchronize()
         assert rel_err(out, _layer_ref(x.cpu(), ids, w_route, w0.cpu(), w1.cpu(), wo.cpu(), e)) <= TOL
+
+
+# ------------------------------------------------------------- fused down projection + combine
+def _combine_case(t, k, e, d, n, seed, drop=0.0):
+    ids = routed_ids(t, k, e, seed, drop)
+    w = np.random.default_rng(seed + 1).random((t, k)).astype(np.float32)
+    x = torch.from_numpy(ri.host_normal((t, d), seed + 2)).to(torch.bfloat16)
+    wo = torch.from_numpy(ri.host_normal((e, d, n), seed + 3, 0.05)).to(torch.bfloat16)
+    gs, order, inv, xs = oracle.moe_permute(ids, x.double().numpy(), e)
+    order_full = np.full(t * k, -1, np.int32)
+    order_full[:order.size] = order
+    xs_b = torch.from_numpy(xs).to(torch.bfloat16)                  # exact: rows of bf16 x
+    ref = oracle.moe_unpermute(oracle.forward(xs_b, wo, gs), inv, w.astype(np.float64))
+    return xs_b, wo, gs, order_full, w, ref
+
+
+@pytest.mark.parametrize("flags", [0, gg.RDOT_FLAG_NO_CTA_PAIR, gg.RDOT_FLAG_CTA_PAIR])
+@pytest.mark.parametrize("t,k,e,d,n,drop", [
+    (700, 2, 4, 256, 384, 0.0),        # groups of ~350 rows: 256-row pair tiles and 128-row half tiles
+    (300, 1, 3, 128, 136, 0.0),        # k = 1, a ragged last column tile
+    (257, 4, 8, 192, 256, 0.05),       # dropped copies (ids outside [0, E)) contribute nothing
+    (96, 8, 16, 64, 128, 0.1),         # k = 8, small groups, some empty
+])
+def test_forward_combine_matches_oracle(t, k, e, d, n, drop, flags):
+    """out[t] = sum_j w[t, j] * (x_sorted @ wo[g])[inv[t*k + j]], fp32, the rows never rounded to
+    bf16 in between; the oracle composes its forward and its un-permute in fp64."""
+    xs, wo, gs, order, w, ref = _combine_case(t, k, e, d, n, 500 + t + k, drop)
+    plan = gg.Plan(t * k, d, n, e, "forward", "bf16", "f32", flags=flags)
+    out = torch.full((t, n), float("nan"), dtype=torch.float32, device=DEV)
+    gg.rdot_forward_combine(plan.handle, xs.to(DEV), wo.to(DEV), torch.from_numpy(gs).to(DEV),
+                            torch.from_numpy(order).to(DEV), torch.from_numpy(w).to(DEV), out, plan.workspace)
+    assert plan.status() == 0
+    assert rel_err(out, ref) <= TOL
+    assert rel_err(out, ref) <= 1e-4          # fp32 accumulation of bf16 products: far inside the bar
+    if k <= 2:                                # two fp32 additions into zero commute: bit-reproducible
+        out2 = torch.empty_like(out)
+        gg.rdot_forward_combine(plan.handle, xs.to(DEV), wo.to(DEV), torch.from_numpy(gs).to(DEV),
+                                torch.from_numpy(order).to(DEV), torch.from_numpy(w).to(DEV), out2, plan.workspace)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2)
+
+
+def test_forward_combine_argument_checks():
+    plan = gg.Plan(200, 64, 64, 4, "forward", "bf16", "bf16")
+    x = torch.zeros((200, 64), dtype=torch.bfloat16, device=DEV)
+    wo = torch.zeros((4, 64, 64), dtype=torch.bfloat16, device=DEV)
+    gs = torch.zeros(4, dtype=torch.int32, device=DEV)
+    order = torch.zeros(200, dtype=torch.int32, device=DEV)
+    w = torch.zeros((100, 2), device=DEV)
+    out = torch.zeros((100, 64), device=DEV)
+    with pytest.raises(gg.RdotError) as ei:
+        gg.rdot_forward_combine(plan.handle, x, wo, gs, order, w, out, plan.workspace)   # bf16-out plan
+    assert ei.value.status == gg.RDOT_ERR_UNSUPPORTED
+    plan32 = gg.Plan(200, 64, 64, 4, "forward", "bf16", "f32")
+    with pytest.raises(gg.RdotError) as ei:
+        gg.rdot_forward_combine(plan32.handle, x, wo, gs, order, torch.zeros((100, 3), device=DEV), out,
+                                plan32.workspace)                                        # T*k != M
+    assert ei.value.status == gg.RDOT_ERR_INVALID_ARG
+
+
+def _layer_fused(x, ids, w_route, w0, w1, wo, e, stream=None):
+    """The expert layer with the un-permute fused into the down projection: permute -> gated up
+    projection -> down projection + weighted combine (fp32 out)."""
+    xs, gs, order, inv = gg.moe_permute(ids, x, e, stream)
+    h = gg.ragged_dot_gated(xs, w0, w1, gs, stream=stream)
+    return gg.ragged_dot_combine(h, wo, gs, order, w_route, stream=stream)
+
+
+def _layer_fused_ref(x, ids, w_route, w0, w1, wo, e):
+    """The oracle's steps: permute, the gated up projection rounded to bf16 (the library keeps the
+    hidden rows in bf16), the down projection in fp64 without rounding, the weighted un-permute."""
+    gs, _order, inv, x_sorted = oracle.moe_permute(ids, x.double().cpu().numpy(), e)
+    h = torch.from_numpy(oracle.gated_forward(x_sorted, w0.cpu(), w1.cpu(), gs)).to(torch.bfloat16)
+    return oracle.moe_unpermute(oracle.forward(h, wo.cpu(), gs), inv, np.asarray(w_route, dtype=np.float64))
+
+
+def test_moe_layer_with_fused_combine():
+    t, k, e, d, f = 300, 2, 4, 128, 256
+    ids = routed_ids(t, k, e, 72, 0.02)
+    w_route = np.random.default_rng(73).random((t, k)).astype(np.float32)
+    x = torch.from_numpy(ri.host_normal((t, d), 74)).to(torch.bfloat16)
+    w0 = torch.from_numpy(ri.host_normal((e, d, f), 75, 0.1)).to(torch.bfloat16)
+    w1 = torch.from_numpy(ri.host_normal((e, d, f), 76, 0.1)).to(torch.bfloat16)
+    wo = torch.from_numpy(ri.host_normal((e, f, d), 77, 0.1)).to(torch.bfloat16)
+    out = _layer_fused(x.to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(w_route).to(DEV), w0.to(DEV),
+                       w1.to(DEV), wo.to(DEV), e)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.float32
+    assert rel_err(out, _layer_fused_ref(x, ids, w_route, w0, w1, wo, e)) <= TOL
+
+
+def test_moe_layer_fused_cuda_graph_replay_with_new_routing():
+    t, k, e, d, f = 256, 2, 4, 128, 128
+    w0 = torch.from_numpy(ri.host_normal((e, d, f), 78, 0.1)).to(torch.bfloat16).to(DEV)
+    w1 = torch.from_numpy(ri.host_normal((e, d, f), 79, 0.1)).to(torch.bfloat16).to(DEV)
+    wo = torch.from_numpy(ri.host_normal((e, f, d), 80, 0.1)).to(torch.bfloat16).to(DEV)
+    x = torch.from_numpy(ri.host_normal((t, d), 81)).to(torch.bfloat16).to(DEV)
+    ids_d = torch.from_numpy(routed_ids(t, k, e, 82)).to(DEV)
+    wr_d = torch.rand((t, k), device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        _layer_fused(x, ids_d, wr_d, w0, w1, wo, e, s)       # plans and tensor maps made outside capture
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        out = _layer_fused(x, ids_d, wr_d, w0, w1, wo, e, s)
+    for seed in (83, 84):
+        ids = routed_ids(t, k, e, seed, 0.05)
+        w_route = np.random.default_rng(seed).random((t, k)).astype(np.float32)
+        ids_d.copy_(torch.from_numpy(ids))
+        wr_d.copy_(torch.from_numpy(w_route))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert rel_err(out, _layer_fused_ref(x.cpu(), ids, w_route, w0.cpu(), w1.cpu(), wo.cpu(), e)) <= TOL
