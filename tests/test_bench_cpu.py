@@ -35,7 +35,7 @@ def test_traffic_figure_only_for_the_sources_it_was_taken_on(tmp_path, monkeypat
     srcs = bench.KERNEL_SOURCES["fwd_tc2_kernel"]
     got = bench.ncu_traffic("fwd_tc2_kernel", "mixtral_bf16", srcs)
     assert got is not None and got > 0                      # the committed capture is of these sources
-    assert bench.ncu_traffic("fwd_tc2_kernel", "deepseek_bf16", srcs) is None   # no capture of that workload
+    assert bench.ncu_traffic("fwd_tc2_kernel", "deepseek_bf16", srcs) is None   # no capture of that pairing
     # a changed source file: copy the sources into a scratch root, edit one, hash again
     for f in srcs:
         dst = tmp_path / f
