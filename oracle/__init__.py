@@ -18,6 +18,10 @@ Functions and the passages they follow (page titles and sections):
 * :func:`grad_input_mxfp8` -- the data gradient (Part 4 Table 7, dgrad_wi) on MXFP8 operands
   (AITER PR #5658 number format): dy and the weights carry one E8M0 scale per 32 elements of the
   contracted axis N; the elements are dequantised one by one and the fp64 data gradient applies.
+* :func:`grad_weight_mxfp8` -- the weight gradient (Part 4 Table 7, wgrad_wi) on MXFP8 operands
+  (AITER PR #5658 number format) with the scales along the contracted rows, in blocks of 32 rows
+  that start at each group's first row (the reading this library takes; the pages give no rule
+  for blocks at group boundaries).
 * :func:`gated_forward` -- "Group-GEMM in XLA", Part 4 "The Three MoE Compute Paths in MaxText":
   the up projection's two ragged dots feed ``activation(layer_w0) * layer_w1``; the activation is
   read as SiLU, z * sigmoid(z), the gated unit of the evaluated MoE models.
@@ -412,6 +416,48 @@ def mx_dequant(codes, scales, axis: int):
     lut_c = np.array([e4m3_decode(i) for i in range(256)])
     lut_s = np.array([e8m0_decode(i) for i in range(256)])
     return lut_c[c] * np.repeat(lut_s[sc], 32, axis=axis)
+
+
+def mx_group_scale_rows(group_sizes, m: int, block: int = 32):
+    """Scale row of each of the m rows under per-group row blocking: row i of group g (after the
+    clamping reading of :func:`offsets`) uses scale row bp[g] + (i - off[g]) // block, where
+    bp[g] = sum over the groups before g of ceil(size / block); rows past the last group get -1."""
+    off, _ = offsets(group_sizes, m)
+    sizes = off[1:] - off[:-1]
+    bp = np.concatenate([[0], np.cumsum((sizes + block - 1) // block)])
+    srow = np.full(m, -1, dtype=np.int64)
+    for g in range(sizes.size):
+        i = np.arange(off[g], off[g + 1])
+        srow[i] = bp[g] + (i - off[g]) // block
+    return srow
+
+
+def grad_weight_mxfp8(lhs_q, lhs_s, dy_q, dy_s, group_sizes):
+    """Weight gradient on MXFP8 operands, float64 ``[G, K, N]``.
+
+    lhs_q [M, K] and dy_q [M, N] hold E4M3 codes; lhs_s [SB, K] and dy_s [SB, N] hold E8M0 scales
+    for blocks of 32 rows that start at each group's first row (:func:`mx_group_scale_rows`; SB is
+    at least the number of blocks, M // 32 + G covers any sizes). Each element of a group's rows
+    is dequantised by this file's decoders, decode(code) * 2^(scale - 127); rows past the last
+    group are never read; then the fp64 weight gradient applies."""
+    aq = np.ascontiguousarray(_as_np(lhs_q)[0]).view(np.uint8)
+    as_ = np.ascontiguousarray(_as_np(lhs_s)[0]).view(np.uint8)
+    dq = np.ascontiguousarray(_as_np(dy_q)[0]).view(np.uint8)
+    ds = np.ascontiguousarray(_as_np(dy_s)[0]).view(np.uint8)
+    m = aq.shape[0]
+    if dq.shape[0] != m or as_.shape[1] != aq.shape[1] or ds.shape[1] != dq.shape[1]:
+        raise ValueError("bad MXFP8 grad-weight shapes")
+    srow = mx_group_scale_rows(group_sizes, m)
+    if srow.max(initial=-1) >= min(as_.shape[0], ds.shape[0]):
+        raise ValueError("scale tensors have fewer rows than the groups' blocks")
+    lut_c = np.array([e4m3_decode(i) for i in range(256)])
+    lut_s = np.array([e8m0_decode(i) for i in range(256)])
+    keep = srow >= 0
+    a = np.zeros(aq.shape)
+    d = np.zeros(dq.shape)
+    a[keep] = lut_c[aq[keep]] * lut_s[as_[srow[keep]]]
+    d[keep] = lut_c[dq[keep]] * lut_s[ds[srow[keep]]]
+    return grad_weight(a, d, group_sizes)
 
 
 def grad_input_mxfp8(dy_q, dy_s, w_q, w_s, group_sizes):

@@ -1,8 +1,9 @@
 """Seeded synthetic inputs for ragged-dot (shared by the oracle tests, the GPU tests and bench.py).
 
-This module draws random numbers and routing decisions only. It contains none of the
-ragged-dot arithmetic (no prefix sums, no products, no decoding of FP8 codes), so the oracle
-and the CUDA path stay independent: both consume the bytes produced here.
+This module draws random numbers and routing decisions and lays quantised inputs out in the
+formats the library takes. It contains none of the ragged-dot arithmetic (no products, no group
+lookup, no decoding of FP8 codes), so the oracle and the CUDA path stay independent: both
+consume the bytes produced here.
 
 Workload recipes (the pages' MoE workloads, "Group-GEMM in XLA", Part 1 and Part 4; "How to
 Scale Your Model on AMD", ch. 6 "Grouped GEMM kernels for MoE"):
@@ -27,6 +28,7 @@ __all__ = [
     "device_normal",
     "device_uniform",
     "quantize_mx_e4m3",
+    "quantize_mx_e4m3_group_rows",
     "CONFIGS",
     "config_group_sizes",
 ]
@@ -187,6 +189,44 @@ def quantize_mx_e4m3(x, axis: int, block: int = 32):
     q = (xb / scale.unsqueeze(-1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
     codes = q.view(torch.uint8).reshape(shp).movedim(-1, axis).contiguous()
     scales = (exp + 127).to(torch.uint8).movedim(-1, axis).contiguous()
+    return codes, scales
+
+
+def quantize_mx_e4m3_group_rows(x, group_sizes, block: int = 32):
+    """OCP-MX quantisation along the ROW axis in blocks that start at each group's first row: the
+    input format of the MXFP8 weight gradient, whose contraction runs over the rows of each group.
+
+    x: torch fp32 [M, C] (rows stacked in group order); group_sizes: the per-group row counts
+    (non-negative, summing to at most M). Group g's rows are quantised in blocks of ``block``
+    consecutive rows from its first row (its last block may be shorter), each column of a block
+    sharing one E8M0 scale chosen as in :func:`quantize_mx_e4m3`. The scales of the groups' blocks
+    are stacked in group order: block b of group g is scale row ``(blocks of the groups before g)
+    + b``; the tensor has the static height ``M // block + G`` (enough for any sizes summing to at
+    most M) and unused rows hold 127 (2^0). Rows past the last group are quantised with unit
+    scale (the operation never reads them).
+
+    Returns ``(codes uint8 [M, C], scales uint8 [M // block + G, C])``."""
+    import torch
+
+    m, c = x.shape
+    sizes = [int(v) for v in np.asarray(group_sizes).reshape(-1)]
+    if min(sizes, default=0) < 0 or sum(sizes) > m:
+        raise ValueError("group sizes must be non-negative and sum to at most M")
+    codes = torch.empty((m, c), dtype=torch.uint8, device=x.device)
+    scales = torch.full((m // block + len(sizes), c), 127, dtype=torch.uint8, device=x.device)
+    row, srow = 0, 0
+    for n in sizes:
+        if n:
+            nb = -(-n // block)
+            pad = torch.zeros((nb * block, c), dtype=torch.float32, device=x.device)
+            pad[:n] = x[row:row + n].float()
+            q, s = quantize_mx_e4m3(pad.reshape(nb, block, c).transpose(0, 1).reshape(block, nb * c), axis=0,
+                                    block=block)
+            codes[row:row + n] = q.reshape(block, nb, c).transpose(0, 1).reshape(nb * block, c)[:n]
+            scales[srow:srow + nb] = s.reshape(nb, c)
+            row, srow = row + n, srow + nb
+    if row < m:
+        codes[row:] = x[row:].float().clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
     return codes, scales
 
 

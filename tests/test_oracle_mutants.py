@@ -469,3 +469,64 @@ def test_router_pins_pass_on_the_oracle():
 @pytest.mark.parametrize("name", sorted(ROUTER_MUTANTS))
 def test_router_pins_catch_a_planted_mistake(name):
     assert router_pin_failures(ROUTER_MUTANTS[name]), f"no pin caught: {name}"
+
+
+# ---------------------------------------------------------------------- MXFP8 grad-weight
+def mxw_pin_failures(fn):
+    from tests.test_oracle_pins import _mxw_case, _mxw_example, _torch_e4m3
+    fails = []
+    aq, a_s, dq, d_s, gs, dw = _mxw_example()
+    _check("worked example", lambda: np.array_equal(fn(aq, a_s, dq, d_s, gs)[:, :, 0], dw), fails)
+    aq, a_s, dq, d_s, gs = _mxw_case(84, [40, 0, 77, 1, 33], 160)
+    _check("unit scales", lambda: _rel(fn(aq, np.full_like(a_s, 127), dq, np.full_like(d_s, 127), gs),
+                                       oracle.grad_weight(_torch_e4m3(aq), _torch_e4m3(dq), gs)) == 0.0, fails)
+    base = oracle.grad_weight_mxfp8(aq, a_s, dq, d_s, gs)
+    _check("random scales", lambda: _rel(fn(aq, a_s, dq, d_s, gs), base) < TOL, fails)
+    return fails
+
+
+def _mxw_global_blocks(aq, a_s, dq, d_s, gs):
+    # blocks of 32 rows counted from row 0 of the stacked rows, ignoring group starts
+    m = aq.shape[0]
+    srow = np.arange(m) // 32
+    lut = np.array([oracle.e4m3_decode(i) for i in range(256)])
+    off = _offsets(gs)
+    a = lut[aq] * 2.0 ** (a_s[srow].astype(np.int64) - 127)
+    d = lut[dq] * 2.0 ** (d_s[srow].astype(np.int64) - 127)
+    a[off[-1]:] = 0.0
+    d[off[-1]:] = 0.0
+    return oracle.grad_weight(a, d, gs)
+
+
+def _mxw_prefix(aq, a_s, dq, d_s, gs, count_empty=False, floor=False):
+    m = aq.shape[0]
+    off = _offsets(gs)
+    nb = [(s // 32 if floor else -(-s // 32)) + (1 if count_empty and s == 0 else 0) for s in gs]
+    bp = np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
+    srow = np.zeros(m, np.int64)
+    for g in range(len(gs)):
+        i = np.arange(off[g], off[g + 1])
+        srow[i] = bp[g] + (i - off[g]) // 32
+    lut = np.array([oracle.e4m3_decode(i) for i in range(256)])
+    keep = np.arange(m) < off[-1]
+    srow = np.minimum(srow, a_s.shape[0] - 1)
+    a = np.where(keep[:, None], lut[aq] * 2.0 ** (a_s[srow].astype(np.int64) - 127), 0.0)
+    d = np.where(keep[:, None], lut[dq] * 2.0 ** (d_s[srow].astype(np.int64) - 127), 0.0)
+    return oracle.grad_weight(a, d, gs)
+
+
+MXW_MUTANTS = {
+    "blocks counted from the first stacked row": _mxw_global_blocks,
+    "empty groups given a block": lambda *a: _mxw_prefix(*a, count_empty=True),
+    "a group's short last block not counted": lambda *a: _mxw_prefix(*a, floor=True),
+    "dy's scales applied to lhs": lambda aq, a_s, dq, d_s, gs: oracle.grad_weight_mxfp8(aq, d_s[:, :1].repeat(a_s.shape[1], 1), dq, d_s, gs),
+}
+
+
+def test_mxw_pins_pass_on_the_oracle():
+    assert mxw_pin_failures(oracle.grad_weight_mxfp8) == []
+
+
+@pytest.mark.parametrize("name", sorted(MXW_MUTANTS))
+def test_mxw_pins_catch_a_planted_mistake(name):
+    assert mxw_pin_failures(MXW_MUTANTS[name]), f"no pin caught: {name}"

@@ -337,6 +337,89 @@ def test_gated_forward_brute_force_and_silu_identity():
     assert np.all(oracle.gated_forward(x, np.zeros_like(w0), w1, gs) == 0.0)     # silu(0) = 0
 
 
+# ---------------------------------------------------------------------- MXFP8 grad-weight
+def _mxw_example():
+    d = _golden.read("mxfp8_grad_weight_example.txt")
+    aq = np.zeros((40, 2), np.uint8)
+    aq[:, 0], aq[:, 1] = 0x38, 0x40
+    aq[36:] = 0x7F                                         # NaN codes past the sum: never read
+    dq = np.full((40, 1), 0x38, np.uint8)
+    dq[36:] = 0x7F
+    return aq, d["lhs_s"].astype(np.uint8), dq, d["dy_s"].astype(np.uint8), d["group_sizes"].astype(np.int32), d["dw"]
+
+
+def _mxw_case(seed, sizes, m, k=6, n=5):
+    rng = np.random.default_rng(seed)
+    gs = np.asarray(sizes, np.int32)
+    sb = m // 32 + gs.size
+    aq = rng.integers(0, 256, size=(m, k)).astype(np.uint8)
+    dq = rng.integers(0, 256, size=(m, n)).astype(np.uint8)
+    for c in (aq, dq):                                    # no E4M3 NaN codes (S.1111.111)
+        c[(c & 0x7F) == 0x7F] = 0x3C
+    a_s = rng.integers(120, 135, size=(sb, k)).astype(np.uint8)
+    d_s = rng.integers(120, 135, size=(sb, n)).astype(np.uint8)
+    return aq, a_s, dq, d_s, gs
+
+
+def _torch_e4m3(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def test_mxfp8_grad_weight_worked_example():
+    aq, a_s, dq, d_s, gs, dw = _mxw_example()
+    assert np.array_equal(oracle.grad_weight_mxfp8(aq, a_s, dq, d_s, gs)[:, :, 0], dw)
+
+
+def test_mxfp8_grad_weight_unit_scales_and_shifts():
+    """All scales 127: the grad-weight of the E4M3 values decoded by torch's float8 cast. Adding 3
+    to every lhs scale and 2 to every dy scale multiplies the result by 2^5 exactly."""
+    aq, a_s, dq, d_s, gs = _mxw_case(81, [40, 0, 77, 1, 33], 160)
+    one_a, one_d = np.full_like(a_s, 127), np.full_like(d_s, 127)
+    got = oracle.grad_weight_mxfp8(aq, one_a, dq, one_d, gs)
+    ref = oracle.grad_weight(_torch_e4m3(aq), _torch_e4m3(dq), gs)
+    assert _rel(got, ref) == 0.0
+    base = oracle.grad_weight_mxfp8(aq, a_s, dq, d_s, gs)
+    assert np.array_equal(oracle.grad_weight_mxfp8(aq, a_s + 3, dq, d_s + 2, gs), base * 32.0)
+
+
+def test_mxfp8_grad_weight_block_locality_by_brute_force():
+    """Raising the scale of one (group, block, lhs column) by one doubles exactly that block's
+    rows' contribution to that row of dW[g] and changes nothing else; each block's 32 (or fewer)
+    rows, summed by hand with torch's decoding, are that contribution."""
+    sizes = [40, 0, 77, 1, 33]
+    aq, a_s, dq, d_s, gs = _mxw_case(82, sizes, 160)
+    base = oracle.grad_weight_mxfp8(aq, a_s, dq, d_s, gs)
+    start, brow = 0, 0
+    fa, fd = _torch_e4m3(aq), _torch_e4m3(dq)
+    for g, size in enumerate(sizes):
+        for b in range(-(-size // 32)):
+            rows = np.arange(start + 32 * b, min(start + size, start + 32 * b + 32))
+            col = (g + b) % aq.shape[1]
+            bumped = a_s.copy()
+            bumped[brow, col] += 1
+            diff = oracle.grad_weight_mxfp8(aq, bumped, dq, d_s, gs) - base
+            contrib = np.zeros(dq.shape[1])
+            for i in rows:
+                sd = np.array([2.0 ** (int(d_s[brow, j]) - 127) for j in range(dq.shape[1])])
+                contrib += fa[i, col] * 2.0 ** (int(a_s[brow, col]) - 127) * fd[i] * sd
+            assert _rel(diff[g, col], contrib) < 1e-12
+            mask = np.ones(diff.shape, bool)
+            mask[g, col] = False
+            assert np.all(diff[mask] == 0.0)
+            brow += 1
+        start += size
+
+
+def test_mxfp8_grad_weight_ignores_rows_past_the_sum_and_empty_groups():
+    aq, a_s, dq, d_s, gs = _mxw_case(83, [0, 50, 0, 20], 96)
+    aq[70:] = 0x7F                                         # NaN codes past the sum
+    dq[70:] = 0x7F
+    got = oracle.grad_weight_mxfp8(aq, a_s, dq, d_s, gs)
+    assert np.isfinite(got).all() and np.all(got[0] == 0.0) and np.all(got[2] == 0.0)
+    # the empty groups take no scale rows: group 1 starts at scale row 0, group 3 at row 2
+    assert list(oracle.mx_group_scale_rows(gs, 96)[[0, 49, 50, 69, 70]]) == [0, 1, 2, 2, -1]
+
+
 # ------------------------------------------------------------------------------ router top-k
 def _rank_key(v):
     """Sort key of one logit: larger numbers first, NaN after every number."""
