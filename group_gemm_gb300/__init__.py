@@ -24,7 +24,8 @@ __all__ = [
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_no_alloc_read_status", "rdot_grad_input", "rdot_moe_route_workspace_size",
     "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "rdot_router_topk",
-    "rdot_forward_combine", "router_topk", "ragged_dot_combine", "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
+    "rdot_forward_combine", "rdot_grad_weight_mxfp8", "router_topk", "ragged_dot_combine", "grad_weight_mxfp8",
+    "moe_permute", "moe_unpermute", "ragged_dot", "grad_weight",
     "grad_input", "ragged_dot_gated",
     "ragged_dot_mxfp8", "padded_ragged_dot", "EXPORTED_SYMBOLS",
 ]
@@ -33,7 +34,7 @@ RDOT_OK, RDOT_ERR_INVALID_ARG, RDOT_ERR_UNSUPPORTED, RDOT_ERR_CUDA = 0, 1, 2, 3
 RDOT_ERR_DEVICE_TIMEOUT, RDOT_WARN_GROUP_SIZES = 4, 5
 RDOT_F32, RDOT_BF16, RDOT_E4M3 = 0, 1, 2
 RDOT_MODE_FORWARD, RDOT_MODE_GRAD_WEIGHT, RDOT_MODE_FORWARD_MXFP8, RDOT_MODE_GRAD_INPUT = 0, 1, 2, 3
-RDOT_MODE_FORWARD_GATED, RDOT_MODE_GRAD_INPUT_MXFP8 = 4, 5
+RDOT_MODE_FORWARD_GATED, RDOT_MODE_GRAD_INPUT_MXFP8, RDOT_MODE_GRAD_WEIGHT_MXFP8 = 4, 5, 6
 RDOT_STATUS_BIT_GROUP_SIZES, RDOT_STATUS_BIT_TIMEOUT = 0x1, 0x2
 RDOT_FLAG_ROW_TILES_INNER, RDOT_FLAG_COL_TILES_INNER = 0x1, 0x2
 RDOT_FLAG_CTA_PAIR, RDOT_FLAG_NO_CTA_PAIR, RDOT_FLAG_NATURAL_ORDER = 0x4, 0x8, 0x10
@@ -49,13 +50,14 @@ EXPORTED_SYMBOLS = (
     "rdot_set_wait_timeout", "rdot_status_string", "rdot_last_cuda_error", "rdot_version",
     "rdot_forward_no_alloc", "rdot_no_alloc_read_status", "rdot_grad_input", "rdot_moe_route_workspace_size",
     "rdot_moe_permute", "rdot_moe_unpermute", "rdot_forward_gated", "rdot_grad_input_mxfp8", "rdot_router_topk",
-    "rdot_forward_combine",
+    "rdot_forward_combine", "rdot_grad_weight_mxfp8",
 )
 
 _DTYPE_CODES = {"f32": RDOT_F32, "bf16": RDOT_BF16, "e4m3": RDOT_E4M3}
 _MODE_CODES = {"forward": RDOT_MODE_FORWARD, "grad_weight": RDOT_MODE_GRAD_WEIGHT,
                "forward_mxfp8": RDOT_MODE_FORWARD_MXFP8, "grad_input": RDOT_MODE_GRAD_INPUT,
-               "forward_gated": RDOT_MODE_FORWARD_GATED, "grad_input_mxfp8": RDOT_MODE_GRAD_INPUT_MXFP8}
+               "forward_gated": RDOT_MODE_FORWARD_GATED, "grad_input_mxfp8": RDOT_MODE_GRAD_INPUT_MXFP8,
+               "grad_weight_mxfp8": RDOT_MODE_GRAD_WEIGHT_MXFP8}
 
 
 class RdotError(RuntimeError):
@@ -120,6 +122,7 @@ def load():
             "rdot_version": ([], ctypes.c_int),
             "rdot_forward_no_alloc": ([vp, vp, vp, vp, vp, vp], st),
             "rdot_no_alloc_read_status": ([vp, i32p, vp], st),
+            "rdot_grad_weight_mxfp8": ([vp, vp, vp, vp, vp, vp, vp, vp, vp], st),
             "rdot_forward_combine": ([vp, vp, vp, vp, vp, vp, i64, ctypes.c_int32, vp, vp, vp], st),
             "rdot_router_topk": ([vp, ctypes.c_int32, i64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, vp, vp, vp],
                                  st),
@@ -216,6 +219,12 @@ def rdot_moe_unpermute(y_sorted, inv, topk_weights, out, stream=None) -> None:
     _check(load().rdot_moe_unpermute(_ptr(y_sorted), _ptr(inv), _ptr(topk_weights), int(t), int(k),
                                      int(y_sorted.shape[1]), _ptr(out), _stream(stream, out.device)),
            "rdot_moe_unpermute")
+
+
+def rdot_grad_weight_mxfp8(plan, lhs_q, lhs_s, dy_q, dy_s, group_sizes, dw, workspace, stream=None) -> None:
+    _check(load().rdot_grad_weight_mxfp8(plan, _ptr(lhs_q), _ptr(lhs_s), _ptr(dy_q), _ptr(dy_s), _ptr(group_sizes),
+                                         _ptr(dw), _ptr(workspace), _stream(stream, dw.device)),
+           "rdot_grad_weight_mxfp8")
 
 
 def rdot_forward_combine(plan, lhs, rhs, group_sizes, order, topk_weights, out, workspace, stream=None) -> None:
@@ -428,6 +437,23 @@ def ragged_dot_gated(lhs, w0, w1, group_sizes, out_dtype=None, out=None, stream=
         out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
     rdot_forward_gated(plan.handle, lhs.contiguous(), w0.contiguous(), w1.contiguous(),
                        group_sizes.to(torch.int32).contiguous(), out, plan.workspace, stream)
+    return out
+
+
+def grad_weight_mxfp8(lhs_q, lhs_s, dy_q, dy_s, group_sizes, out=None, stream=None):
+    """MXFP8 weight gradient: ``dw [G, K, N]`` fp32 from E4M3 codes with E8M0 scales along the rows
+    in blocks of 32 that start at each group's first row (scale tensors ``[M // 32 + G, K | N]``)."""
+    import torch
+    m, k = lhs_q.shape
+    n = dy_q.shape[1]
+    g = group_sizes.shape[0]
+    key = ("wgrad_mxfp8", m, k, n, g, lhs_q.device)
+    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="grad_weight_mxfp8", in_dtype="e4m3", out_dtype="f32",
+                        device=lhs_q.device)
+    if out is None:
+        out = torch.empty((g, k, n), dtype=torch.float32, device=lhs_q.device)
+    rdot_grad_weight_mxfp8(plan.handle, lhs_q.contiguous(), lhs_s.contiguous(), dy_q.contiguous(), dy_s.contiguous(),
+                           group_sizes.to(torch.int32).contiguous(), out, plan.workspace, stream)
     return out
 
 

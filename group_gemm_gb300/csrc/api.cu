@@ -184,6 +184,10 @@ rdot_status check_problem(const rdot_problem* p) {
             if (p->in_dtype != RDOT_BF16 || p->out_dtype != RDOT_F32) return RDOT_ERR_UNSUPPORTED;
             if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;
             return RDOT_OK;
+        case RDOT_MODE_GRAD_WEIGHT_MXFP8:
+            if (p->in_dtype != RDOT_E4M3 || p->out_dtype != RDOT_F32) return RDOT_ERR_UNSUPPORTED;
+            if (p->k % 16 || p->n % 16 || p->tile_n != 0 || (p->flags & RDOT_FLAG_CTA_PAIR)) return RDOT_ERR_UNSUPPORTED;
+            return RDOT_OK;
         case RDOT_MODE_GRAD_INPUT_MXFP8:
             if (p->in_dtype != RDOT_E4M3 || p->out_dtype != RDOT_BF16) return RDOT_ERR_UNSUPPORTED;
             if (p->n % 32 || p->k % 8 || (p->flags & RDOT_FLAG_CTA_PAIR) || p->tile_n == 512)
@@ -286,6 +290,20 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         // small average groups: interleave the tiles of groups with 2+ row tiles with the
         // others so every wave mixes tensor-core-bound and weight-streaming work
         pl->big_mt = (!want_pair && !(p.flags & RDOT_FLAG_NATURAL_ORDER)) ? 2 : 0;
+    } else if (p.mode == RDOT_MODE_GRAD_WEIGHT_MXFP8) {
+        if (prop.major != 10) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->kind = 7;
+        pl->tile_m = 128;   // dw rows (lhs columns) per tile
+        pl->tile_n = 128;
+        const long long work = ((p.k + 127) / 128) * ((p.n + 127) / 128) * static_cast<long long>(p.groups);
+        if (work > 0x7fffffffLL) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(work, pl->sm_count)));
     } else if (p.mode == RDOT_MODE_GRAD_INPUT_MXFP8) {
         if (prop.major != 10) {
             delete pl;
@@ -486,6 +504,9 @@ rdot_status rdot_workspace_size(rdot_plan_t plan, size_t* bytes) {
         *bytes = mx_layout(swapped_kn(plan->p), plan->tile_m, plan->tile_n).total;
     else if (plan->kind == 2)
         *bytes = kWorkspaceBytes + static_cast<size_t>(2 * WG_MAP_BYTES) * plan->p.groups;   // group tensor maps
+    else if (plan->kind == 7)
+        *bytes = kWorkspaceBytes + static_cast<size_t>(2 * WG_MAP_BYTES) * plan->p.groups +
+                 mxw_scale_block_bytes(plan->p.m, plan->p.groups, plan->p.k, plan->p.n);
     else
         *bytes = kWorkspaceBytes;
     return RDOT_OK;
@@ -898,6 +919,68 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
                                : launch_wgrad_tc(plan->map_a, plan->map_b, plan->map_out, a, plan->tile_n,
                                                  plan->grid, s);
     if (e != cudaSuccess) return cuda_fail(e, "wgrad_tc launch");
+    return RDOT_OK;
+}
+
+rdot_status rdot_grad_weight_mxfp8(rdot_plan_t plan, const void* lhs_q, const uint8_t* lhs_s, const void* dy_q,
+                                   const uint8_t* dy_s, const int32_t* group_sizes, float* dw, void* workspace,
+                                   void* stream) {
+    if (!plan || !group_sizes || !workspace || !dw) return RDOT_ERR_INVALID_ARG;
+    const rdot_problem& p = plan->p;
+    if (p.mode != RDOT_MODE_GRAD_WEIGHT_MXFP8 || plan->kind != 7) return RDOT_ERR_INVALID_ARG;
+    if (p.m > 0 && (!lhs_q || !dy_q || !lhs_s || !dy_s)) return RDOT_ERR_INVALID_ARG;
+    if ((lhs_q && !aligned16(lhs_q)) || (dy_q && !aligned16(dy_q)) || !aligned16(dw) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) || (reinterpret_cast<uintptr_t>(group_sizes) & 3u))
+        return RDOT_ERR_INVALID_ARG;
+    DeviceGuard dg(plan->device);
+    if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p.m == 0) {
+        cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * p.groups * p.k * p.n, s);
+        return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    // codes: rows of K (or N) bytes, boxes of 128 columns x 128 rows
+    if (plan->map_lhs_ptr != lhs_q) {
+        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, lhs_q, p.k, p.m, p.k, 128, 128);
+        if (st != RDOT_OK) return st;
+        plan->map_lhs_ptr = lhs_q;
+    }
+    if (plan->map_rhs_ptr != dy_q) {
+        rdot_status st = encode_2d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, dy_q, p.n, p.m, p.n, 128, 128);
+        if (st != RDOT_OK) return st;
+        plan->map_rhs_ptr = dy_q;
+    }
+    if (plan->map_out_ptr != dw) {
+        rdot_status st = encode_3d(&plan->map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dw, p.n, p.k, p.groups, p.n * 4,
+                                   p.k * p.n * 4, 32, 32, 1);
+        if (st != RDOT_OK) return st;
+        plan->map_out_ptr = dw;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    MxwArgs a{};
+    a.group_sizes = group_sizes;
+    a.maps = ws + kWorkspaceBytes;
+    a.M = static_cast<int>(p.m);
+    a.K = static_cast<int>(p.k);
+    a.N = static_cast<int>(p.n);
+    a.G = p.groups;
+    a.KT = static_cast<int>((p.k + 127) / 128);
+    a.NT = static_cast<int>((p.n + 127) / 128);
+    const long long chunks = (p.m + 127) / 128 + p.groups;
+    a.sfa = a.maps + static_cast<size_t>(2 * WG_MAP_BYTES) * p.groups;
+    a.sfb = a.sfa + static_cast<size_t>(chunks) * a.KT * MX_SFA_BLOCK_BYTES;
+    a.status = static_cast<int32_t*>(workspace);
+    a.timeout_ns = plan->timeout_ns;
+    // the per-group copies of the code maps, cut at each group's end (the grad-weight's kernel)
+    WgradArgs wa{};
+    wa.group_sizes = group_sizes;
+    wa.maps = a.maps;
+    wa.M = a.M;
+    wa.G = a.G;
+    cudaError_t e = launch_wg_maps(plan->map_a, plan->map_b, wa, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mxfp8 wgrad group maps launch");
+    e = launch_mxw(plan->map_a, plan->map_b, plan->map_out, lhs_s, dy_s, a, plan->grid, 4 * plan->sm_count, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mxfp8 wgrad launch");
     return RDOT_OK;
 }
 

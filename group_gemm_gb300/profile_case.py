@@ -26,7 +26,7 @@ def main():
     import rdot_inputs as ri
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwd", "dgrad", "wgrad", "padded", "mxfp8"], default="fwd")
+    ap.add_argument("--kernel", choices=["fwd", "dgrad", "wgrad", "padded", "mxfp8", "mxwgrad"], default="fwd")
     ap.add_argument("--workload", default="mixtral_bf16")
     ap.add_argument("--tokens", type=int, default=2048)
     ap.add_argument("--iters", type=int, default=3)
@@ -83,6 +83,18 @@ def main():
 
         def run():
             gg.rdot_grad_weight(plan.handle, lhs, dy, gs_d, dw, plan.workspace, stream)
+        flops = 2.0 * m * k * n
+    elif args.kernel == "mxwgrad":
+        x = ri.device_normal((m, k), 1, 1.0, dev, torch.float32)
+        aq, as_ = ri.quantize_mx_e4m3_group_rows(x, gs)
+        dy = ri.device_normal((m, n), 2, 1.0, dev, torch.float32)
+        dq, ds = ri.quantize_mx_e4m3_group_rows(dy, gs)
+        del x, dy
+        dw = torch.empty((g, k, n), dtype=torch.float32, device=dev)
+        plan = gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", "f32", flags=args.flags)
+
+        def run():
+            gg.rdot_grad_weight_mxfp8(plan.handle, aq, as_, dq, ds, gs_d, dw, plan.workspace, stream)
         flops = 2.0 * m * k * n
     else:
         x = ri.device_normal((m, k), 1, 1.0, dev, torch.float32)

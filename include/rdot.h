@@ -59,7 +59,8 @@ typedef enum {
     RDOT_MODE_FORWARD_MXFP8 = 2, /* forward with E4M3 operands and E8M0 scales per 32 K elements */
     RDOT_MODE_GRAD_INPUT = 3,    /* dlhs[M,K] = dy[M,N] @ rhs[g(i),K,N]^T (contracts rhs's N axis) */
     RDOT_MODE_FORWARD_GATED = 4, /* out[M,N] = silu(lhs @ w0[g(i)]) * (lhs @ w1[g(i)]) (gated up projection) */
-    RDOT_MODE_GRAD_INPUT_MXFP8 = 5  /* the data gradient on MXFP8 operands (scales along N) */
+    RDOT_MODE_GRAD_INPUT_MXFP8 = 5, /* the data gradient on MXFP8 operands (scales along N) */
+    RDOT_MODE_GRAD_WEIGHT_MXFP8 = 6 /* the weight gradient on MXFP8 operands (scales along the rows) */
 } rdot_mode;
 
 /* Bits of the device status word (int32 at offset 0 of the workspace). */
@@ -182,6 +183,26 @@ RDOT_API rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const
 RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy,
                              const int32_t* group_sizes, float* dw, void* workspace,
                              void* stream);
+
+/* Weight gradient on MXFP8 operands (Part 4 Table 7, wgrad_wi, in the number format of AITER PR
+ * #5658: OCP E4M3 codes, E8M0 scales, one scale per 32 elements of the contracted axis):
+ *   dw[g] = A_g^T D_g,  A = dequant(lhs_q, lhs_s), D = dequant(dy_q, dy_s), fp32 accumulation
+ *   lhs_q  device uint8 [M, K]   E4M3 codes;  lhs_s  device uint8 [M/32 + G, K]  E8M0 scales
+ *   dy_q   device uint8 [M, N]   E4M3 codes;  dy_s   device uint8 [M/32 + G, N]  E8M0 scales
+ *   dw     device fp32 [G, K, N]; every slab written (zeros for an empty group)
+ * The contraction runs over each group's rows, so its scale blocks run along the rows. The pages
+ * give no rule for a 32-row block at a group boundary; the reading taken: blocks start at each
+ * group's first row (its last block may be shorter) and never mix two groups. Block b of group g
+ * holds scale row bp[g] + b, bp[g] = sum over the groups before g of ceil(size / 32) (after the
+ * clamping reading of group_sizes); element (i, c) of a row i of group g is
+ * decode(code[i, c]) * 2^(scale[bp[g] + (i - start[g]) / 32, c] - 127). M/32 + G rows (M/32
+ * rounded down) hold the blocks of any sizes summing to at most M; rows past the used ones are
+ * never read, nor are code rows past the last group. Plan: mode RDOT_MODE_GRAD_WEIGHT_MXFP8,
+ * in_dtype RDOT_E4M3, out_dtype RDOT_F32, K % 16 == 0, N % 16 == 0 (16-byte code rows); workspace
+ * rdot_workspace_size bytes, 256-byte aligned (the group maps and the reordered scale blocks). */
+RDOT_API rdot_status rdot_grad_weight_mxfp8(rdot_plan_t plan, const void* lhs_q, const uint8_t* lhs_s,
+                                           const void* dy_q, const uint8_t* dy_s, const int32_t* group_sizes,
+                                           float* dw, void* workspace, void* stream);
 
 /* Data gradient of the forward ("Group-GEMM in XLA", Part 4 Table 7, class dgrad_wi: lhs [M,N],
  * rhs [E,K,N], out [M,K], contracting lhs dimension 1 with rhs dimension 2).
