@@ -843,6 +843,32 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                                      "status": pair.status()}
     del aq, as_, bq, bs, out
     torch.cuda.empty_cache()
+    # MXFP8 weight gradient at the grad-weight workload's shape: E4M3 lhs and dy with E8M0 scales
+    # along the rows, in blocks of 32 from each group's start; fp32 dw
+    cfg = ri.CONFIGS["wgrad_bf16"]
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    gs = ri.config_group_sizes("wgrad_bf16")
+    x = ri.device_normal((m, k), 1000, 1.0, dev, torch.float32)
+    aq, as_ = ri.quantize_mx_e4m3_group_rows(x, gs)
+    del x
+    dy = ri.device_normal((m, n), 2000, 1.0, dev, torch.float32)
+    dq, dsc = ri.quantize_mx_e4m3_group_rows(dy, gs)
+    del dy
+    dw = torch.empty((g, k, n), dtype=torch.float32, device=dev)
+    wplan = gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", "f32", device=dev.index)
+    gs_d = torch.from_numpy(gs).to(dev)
+    t5 = _time_steps(lambda: gg.rdot_grad_weight_mxfp8(wplan.handle, aq, as_, dq, dsc, gs_d, dw, wplan.workspace,
+                                                       stream), steps, stream)
+    fl = useful_flops(gs, k, n)
+    min_bytes = m * (k + n) + (m // 32 + g) * (k + n) + 4 * g * k * n       # codes, scales, fp32 dw
+    res["mxfp8_wgrad"] = {"workload": f"dw [{g}, {k}, {n}] from E4M3 lhs [{m}, {k}] and dy [{m}, {n}], scales "
+                                      "along the rows per group", "tflops": round(fl / t5 / 1e12, 3),
+                          "ms": round(t5 * 1e3, 4), "frac_of_fp8_peak": round(fl / t5 / 1e12 / fp8_peak, 4),
+                          "hbm_gbs_algorithmic": round(min_bytes / t5 / 1e9, 1),
+                          "frac_of_hbm": round(min_bytes / t5 / 1e9 / peaks["hbm_gbs"], 4),
+                          "status": wplan.status(), "tile": f"{wplan.info['tile_m']}x{wplan.info['tile_n']}"}
+    del aq, as_, dq, dsc, dw
+    torch.cuda.empty_cache()
     return res
 
 
