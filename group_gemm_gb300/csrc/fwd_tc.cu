@@ -157,11 +157,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) {
                 // stopping early: let every load still in flight land before the CTA exits
-                WaitGuard drain_guard{guard.abort, nullptr, guard.timeout_ns};
-                int dummy = 0;
-                drain_guard.abort = &dummy;
+                int dummy;
+                const WaitGuard dguard = drain_guard(guard, &dummy);
                 for (int s = 0; s < STAGES; ++s)
-                    if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
+                    if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, dguard);
             }
         }
         __syncwarp();
@@ -208,10 +207,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // all MMAs issued by this thread complete before teardown frees TMEM
             mma_commit(drain);
-            WaitGuard drain_guard = guard;
-            int dummy = 0;
-            drain_guard.abort = &dummy;
-            (void)mbar_wait(drain, 0, drain_guard);
+            int dummy;
+            const WaitGuard dguard = drain_guard(guard, &dummy);
+            (void)mbar_wait(drain, 0, dguard);
         }
         __syncwarp();
     } else {

@@ -27,6 +27,7 @@
 
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "pairdrain.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -45,12 +46,14 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;
 constexpr int MISC_BYTES = 16;
+constexpr int XCH_BYTES = (sizeof(PairExchange<STAGES>) + 15) / 16 * 16;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr uint32_t EMPTY_ARRIVALS = 8;       // 4 epilogue warps x 2 CTAs
 
 template <bool OUT_F32>
 size_t smem_bytes(int G) {
-    return 1024 + RING_BYTES + 4 * EpiStage<OUT_F32>::BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+    return 1024 + RING_BYTES + 4 * EpiStage<OUT_F32>::BYTES + BAR_BYTES + MISC_BYTES + XCH_BYTES +
+           sizeof(int32_t) * 2 * (G + 1);
 }
 
 // VAR: 0 = the forward (MN-major B), 1 = the data gradient (K-major B), 2 = the gated up
@@ -73,7 +76,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    auto* xch = reinterpret_cast<PairExchange<STAGES>*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + XCH_BYTES);
     int32_t* tprefix = off + a.G + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -93,6 +97,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             mbar_init(&tempty[i], EMPTY_ARRIVALS);
         }
         mbar_init(drain, 1);
+        mbar_init(&xch->bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmap_a);
@@ -120,7 +125,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+            uint32_t stage = 0, phase = 0;
+            int pos = 0;   // load iterations issued (see pairdrain.cuh)
             bool ok = true;
             for (int w = cluster; w < W && ok; w += nclusters) {
                 const Tile t = decode_tile(w, tprefix, off, a.G, BM, a.NT, m_inner);
@@ -160,31 +166,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                         for (int j = 0; j < my_c; ++j)
                             tma_load_3d_pair(sb + j * B_CHUNK_BYTES, map_b, fb, b_col + 64 * j, kb * TC_BK, t.g);
                     }
-                    issued_mask |= 1u << stage;
-                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    xch->share[stage] = a1 + c1 * B_CHUNK_BYTES;   // the odd CTA's bytes of this iteration
+                    ++pos;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
-            if (!ok) {
-                // stopping early: let the loads in flight land before the CTA can exit. The even
-                // CTA sees both CTAs' bytes on its barriers; the odd CTA cannot, so it waits a
-                // fixed 100 us, far longer than a TMA transfer.
-                WaitGuard drain_guard = guard;
-                int dummy = 0;
-                drain_guard.abort = &dummy;
-                drain_guard.status = nullptr;
-                if (leader) {
-                    for (int s = 0; s < STAGES; ++s)
-                        if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
-                } else {
-                    const uint64_t t0 = global_timer_ns();
-                    while (global_timer_ns() - t0 < 100000ull) {
-                    }
-                }
-            }
+            // every load either CTA issued lands before either CTA can leave (pairdrain.cuh)
+            pair_drain(xch, full, pos, leader, guard);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -228,10 +219,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (acc == 0) acc_phase ^= 1;
             }
             mma_commit_pair(drain);
-            WaitGuard drain_guard = guard;
-            int dummy = 0;
-            drain_guard.abort = &dummy;
-            (void)mbar_wait(drain, 0, drain_guard);
+            int dummy;
+            (void)mbar_wait(drain, 0, drain_guard(guard, &dummy));
         }
         __syncwarp();
     } else {

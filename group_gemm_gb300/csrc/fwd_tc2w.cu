@@ -18,6 +18,7 @@
 
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "pairdrain.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -39,11 +40,12 @@ constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int EPI_BYTES = EPI_WARPS * EpiStage<false>::BYTES;
 constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;   // full, empty, tfull[2], tempty[2], drain
 constexpr int MISC_BYTES = 16;
+constexpr int XCH_BYTES = (sizeof(PairExchange<STAGES>) + 15) / 16 * 16;
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t EMPTY_ARRIVALS = 2 * EPI_WARPS;   // one per epilogue warp of both CTAs
 
 size_t smem_bytes(int G) {
-    return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+    return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + XCH_BYTES + sizeof(int32_t) * 2 * (G + 1);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
@@ -59,7 +61,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    auto* xch = reinterpret_cast<PairExchange<STAGES>*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + XCH_BYTES);
     int32_t* tprefix = off + a.G + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -79,6 +82,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             mbar_init(&tempty[h], EMPTY_ARRIVALS);
         }
         mbar_init(drain, 1);
+        mbar_init(&xch->bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmap_a);
@@ -105,7 +109,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+            uint32_t stage = 0, phase = 0;
+            int pos = 0;   // load iterations issued (see pairdrain.cuh)
             bool ok = true;
             const int r = static_cast<int>(rank);
             for (int w = cluster; w < W && ok; w += nclusters) {
@@ -113,10 +118,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 const int n0 = t.nt * BN;
                 // each CTA's A half unless wholly past M; the 64-column chunks of B not wholly past N
                 const int a1 = (t.row0 + 128 < a.M) ? A_BYTES : 0;
-                int chunks_all = 0;
+                int chunks_all = 0, odd_chunks = 0;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)   // j = (h, rank, c): columns n0 + 256 h + 128 rank + 64 c
-                    chunks_all += (n0 + 256 * (j >> 2) + 128 * ((j >> 1) & 1) + 64 * (j & 1) < a.N) ? 1 : 0;
+                for (int j = 0; j < 8; ++j) {   // j = (h, rank, c): columns n0 + 256 h + 128 rank + 64 c
+                    const int in = (n0 + 256 * (j >> 2) + 128 * ((j >> 1) & 1) + 64 * (j & 1) < a.N) ? 1 : 0;
+                    chunks_all += in;
+                    if ((j >> 1) & 1) odd_chunks += in;
+                }
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
                         ok = false;
@@ -136,30 +144,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                                 tma_load_3d_pair(sb + h * B_HALF_BYTES + c * B_CHUNK_BYTES, &tmap_b, fb, col, kb * TC_BK,
                                                  t.g);
                         }
-                    issued_mask |= 1u << stage;
-                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    xch->share[stage] = a1 + odd_chunks * B_CHUNK_BYTES;   // the odd CTA's bytes of this iteration
+                    ++pos;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
-            if (!ok) {
-                // stopping early: let the loads in flight land before the CTA can exit (the odd
-                // CTA cannot see its own loads land, so it waits a fixed 100 us)
-                WaitGuard drain_guard = guard;
-                int dummy = 0;
-                drain_guard.abort = &dummy;
-                drain_guard.status = nullptr;
-                if (leader) {
-                    for (int s = 0; s < STAGES; ++s)
-                        if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
-                } else {
-                    const uint64_t t0 = global_timer_ns();
-                    while (global_timer_ns() - t0 < 100000ull) {
-                    }
-                }
-            }
+            // every load either CTA issued lands before either CTA can leave (pairdrain.cuh)
+            pair_drain(xch, full, pos, leader, guard);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -208,10 +202,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 acc_phase ^= 1;
             }
             mma_commit_pair(drain);
-            WaitGuard drain_guard = guard;
-            int dummy = 0;
-            drain_guard.abort = &dummy;
-            (void)mbar_wait(drain, 0, drain_guard);
+            int dummy;
+            (void)mbar_wait(drain, 0, drain_guard(guard, &dummy));
         }
         __syncwarp();
     } else {

@@ -293,12 +293,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (!ok) {
-                WaitGuard drain_guard = guard;
-                int dummy = 0;
-                drain_guard.abort = &dummy;
-                drain_guard.status = nullptr;
+                int dummy;
+                const WaitGuard dguard = drain_guard(guard, &dummy);
                 for (int s = 0; s < STAGES; ++s)
-                    if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
+                    if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, dguard);
             }
         }
         __syncwarp();
@@ -350,10 +348,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             mma_commit(drain);
-            WaitGuard drain_guard = guard;
-            int dummy = 0;
-            drain_guard.abort = &dummy;
-            (void)mbar_wait(drain, 0, drain_guard);
+            int dummy;
+            const WaitGuard dguard = drain_guard(guard, &dummy);
+            (void)mbar_wait(drain, 0, dguard);
         }
         __syncwarp();
     } else {

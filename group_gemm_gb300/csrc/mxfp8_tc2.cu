@@ -18,6 +18,7 @@
 
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "pairdrain.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -40,6 +41,7 @@ constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int EPI_BYTES = EPI_WARPS * EpiStage<false>::BYTES;
 constexpr int BAR_BYTES = (2 * STAGES + 3) * 8;      // full, empty, tfull, tempty, drain
 constexpr int MISC_BYTES = 16;
+constexpr int XCH_BYTES = (sizeof(PairExchange<STAGES>) + 15) / 16 * 16;
 constexpr int TMEM_COLS = 512;
 constexpr int TMEM_SF_BASE = BN;                     // after the accumulator
 constexpr int SF_COLS = 4 + 8;                       // per stage: A scales, B scales (256 columns)
@@ -47,7 +49,7 @@ static_assert(TMEM_SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budge
 constexpr uint32_t EMPTY_ARRIVALS = 2 * EPI_WARPS;
 
 size_t smem_bytes(int G) {
-    return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+    return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + XCH_BYTES + sizeof(int32_t) * 2 * (G + 1);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
@@ -64,7 +66,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint64_t* drain = tempty + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    auto* xch = reinterpret_cast<PairExchange<STAGES>*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + XCH_BYTES);
     int32_t* tprefix = off + a.G + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -82,6 +85,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         mbar_init(tfull, 1);
         mbar_init(tempty, EMPTY_ARRIVALS);
         mbar_init(drain, 1);
+        mbar_init(&xch->bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmap_a);
@@ -109,7 +113,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+            uint32_t stage = 0, phase = 0;
+            int pos = 0;   // load iterations issued (see pairdrain.cuh)
             bool ok = true;
             const int r = static_cast<int>(rank);
             for (int w = cluster; w < W && ok; w += nclusters) {
@@ -135,28 +140,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     if (my_b) tma_load_3d_pair(st + A_BYTES, &tmap_b, fb, n0 + 128 * r, ks * BKB, t.g);
                     tma_load_2d_pair(st + A_BYTES + B_BYTES, &tmap_sfa, fb, 0, sfa_row + 2 * ks);
                     tma_load_2d_pair(st + A_BYTES + B_BYTES + SFA_BYTES, &tmap_sfb, fb, 0, sfb_row + ks);
-                    issued_mask |= 1u << stage;
-                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    xch->share[stage] = a1 + b1 + SFA_BYTES + SFB_BYTES;   // the odd CTA's bytes of this iteration
+                    ++pos;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
-            if (!ok) {
-                WaitGuard drain_guard = guard;
-                int dummy = 0;
-                drain_guard.abort = &dummy;
-                drain_guard.status = nullptr;
-                if (leader) {
-                    for (int s = 0; s < STAGES; ++s)
-                        if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
-                } else {
-                    const uint64_t t0 = global_timer_ns();   // the odd CTA cannot see its own loads land
-                    while (global_timer_ns() - t0 < 100000ull) {
-                    }
-                }
-            }
+            // every load either CTA issued lands before either CTA can leave (pairdrain.cuh)
+            pair_drain(xch, full, pos, leader, guard);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -209,10 +202,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 acc_phase ^= 1;
             }
             mma_commit_pair(drain);
-            WaitGuard drain_guard = guard;
-            int dummy = 0;
-            drain_guard.abort = &dummy;
-            (void)mbar_wait(drain, 0, drain_guard);
+            int dummy;
+            (void)mbar_wait(drain, 0, drain_guard(guard, &dummy));
         }
         __syncwarp();
     } else {

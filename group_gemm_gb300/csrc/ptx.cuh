@@ -90,6 +90,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// Limit of the waits that drain work already issued when a kernel stops early (TMA loads in
+// flight, MMAs not yet complete): such work finishes within microseconds, so the limit only has to
+// be bounded, never short. It does not follow the caller's wait limit, which may be set arbitrarily
+// small to provoke a stop.
+constexpr uint64_t kDrainTimeoutNs = 50000000ull;   // 50 ms
+
+// The guard of a drain: it ignores the CTA's abort flag, reports nothing, and waits at least
+// kDrainTimeoutNs. `dummy` must outlive the guard.
+__device__ __forceinline__ WaitGuard drain_guard(const WaitGuard& g, int* dummy) {
+    *dummy = 0;
+    return WaitGuard{dummy, nullptr, g.timeout_ns > kDrainTimeoutNs ? g.timeout_ns : kDrainTimeoutNs};
+}
+
 // Warp-wide wait: lane 0 alone waits on the barrier and the result is broadcast. A wait by all
 // 32 lanes costs the wake-up of the slowest suspended lane on every call; a shuffle only costs a
 // warp synchronisation. The lanes leave converged, as .sync.aligned tcgen05 instructions need.
@@ -356,6 +369,30 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
     __syncwarp();   // the barrier is .aligned: every warp arrives converged
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Counts `bytes` as arrived on the barrier's current phase, as if a copy had delivered them.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// try_wait with cluster-scope acquire: data another CTA of the cluster stored before its
+// release-arrive on this barrier is visible once the phase is seen complete.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

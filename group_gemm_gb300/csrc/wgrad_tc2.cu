@@ -18,6 +18,7 @@
 //     suite ends in such a tile). Accumulator column c is dw column n0 + c in both widths.
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "pairdrain.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -40,10 +41,11 @@ constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int EPI_BYTES = 4 * EPI_TMA_F32_BYTES;   // one staging tile per epilogue warp
 constexpr int BAR_BYTES = (2 * STAGES + 5) * 8;   // full, empty, tfull[2], tempty[2], drain
 constexpr int MISC_BYTES = 16;
+constexpr int XCH_BYTES = (sizeof(PairExchange<STAGES>) + 15) / 16 * 16;
 constexpr int TMEM_COLS = 2 * BN;
 
 size_t smem_bytes(int G) {
-    return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+    return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + XCH_BYTES + sizeof(int32_t) * 2 * (G + 1);
 }
 
 struct PairTile {
@@ -75,7 +77,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    auto* xch = reinterpret_cast<PairExchange<STAGES>*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + XCH_BYTES);
     int32_t* unused = off + a.G + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -95,6 +98,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             mbar_init(&tempty[i], 8);
         }
         mbar_init(drain, 1);
+        mbar_init(&xch->bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmap_x);
@@ -120,7 +124,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+            uint32_t stage = 0, phase = 0;
+            int pos = 0;   // load iterations issued (see pairdrain.cuh)
             bool ok = true;
             for (int w = cluster; w < W && ok; w += nclusters) {
                 const PairTile t = decode(w, a.KT, a.NT, off);
@@ -160,28 +165,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     const CUtensorMap* mdy = tail ? gmap_dy : &tmap_dy;
                     for (int j = 0; j < ac; ++j) tma_load_2d_pair(sa + j * CHUNK_BYTES, mx, fb, k0 + 64 * j, r0);
                     for (int j = 0; j < bc; ++j) tma_load_2d_pair(sb + j * CHUNK_BYTES, mdy, fb, n0 + 64 * j, r0);
-                    issued_mask |= 1u << stage;
-                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    xch->share[stage] = (ac1 + bc1) * CHUNK_BYTES;   // the odd CTA's bytes of this iteration
+                    ++pos;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1;
                     }
                 }
             }
-            if (!ok) {
-                WaitGuard drain_guard = guard;
-                int dummy = 0;
-                drain_guard.abort = &dummy;
-                drain_guard.status = nullptr;
-                if (leader) {
-                    for (int s = 0; s < STAGES; ++s)
-                        if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, drain_guard);
-                } else {
-                    const uint64_t t0 = global_timer_ns();   // the odd CTA cannot see its own loads land
-                    while (global_timer_ns() - t0 < 100000ull) {
-                    }
-                }
-            }
+            // every load either CTA issued lands before either CTA can leave (pairdrain.cuh)
+            pair_drain(xch, full, pos, leader, guard);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -239,10 +232,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
             if (lane == 0) {
                 mma_commit_pair(drain);
-                WaitGuard drain_guard = guard;
-                int dummy = 0;
-                drain_guard.abort = &dummy;
-                (void)mbar_wait(drain, 0, drain_guard);
+                int dummy;
+                (void)mbar_wait(drain, 0, drain_guard(guard, &dummy));
             }
         }
         __syncwarp();
