@@ -94,3 +94,62 @@ def test_whole_output_mxfp8_forward():
     ref = oracle.forward(oracle.mx_dequant(aq.cpu(), as_.cpu(), 1), oracle.mx_dequant(bq.cpu(), bs.cpu(), 1), gs)
     assert rel_err_chunked(got, ref) <= TOL
     assert cosine_to_rounded(got, ref) >= COSINE_MIN
+
+
+def test_whole_output_grad_input():
+    """The data gradient of the Mixtral-like forward: dy [16384, 14336] x rhs [8, 4096, 14336]^T."""
+    cfg = ri.CONFIGS["mixtral_bf16"]
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    gs = ri.config_group_sizes("mixtral_bf16")
+    dy = ri.device_normal((m, n), 3000, 1.0, DEV, torch.bfloat16)
+    rhs = ri.device_normal((g, k, n), 2000, 0.02, DEV, torch.bfloat16)
+    plan = gg.Plan(m, k, n, g, "grad_input", "bf16", "bf16")
+    out = torch.full((m, k), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gg.rdot_grad_input(plan.handle, dy, rhs, torch.from_numpy(gs).to(DEV), out, plan.workspace)
+    assert plan.status() == 0
+    got = out.cpu()
+    ref = oracle.grad_input(dy.cpu(), rhs.cpu(), gs)
+    assert rel_err_chunked(got, ref) <= TOL
+    assert cosine_to_rounded(got, ref) >= COSINE_MIN
+
+
+def test_whole_output_mxfp8_grad_input():
+    """The MXFP8 data gradient at the MXFP8 workload's shapes (scales along the contracted N)."""
+    cfg = ri.CONFIGS["mxfp8"]
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    gs = ri.config_group_sizes("mxfp8")
+    dy = ri.device_normal((m, n), 1100, 1.0, DEV, torch.float32)
+    dq, ds = ri.quantize_mx_e4m3(dy, axis=1)
+    del dy
+    w = ri.device_normal((g, k, n), 2100, 0.02, DEV, torch.float32)
+    wq, ws = ri.quantize_mx_e4m3(w, axis=2)
+    del w
+    torch.cuda.empty_cache()
+    plan = gg.Plan(m, k, n, g, "grad_input_mxfp8", "e4m3", "bf16")
+    out = torch.full((m, k), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gg.rdot_grad_input_mxfp8(plan.handle, dq, ds, wq, ws, torch.from_numpy(gs).to(DEV), out, plan.workspace)
+    assert plan.status() == 0
+    got = out.cpu()
+    ref = oracle.grad_input(oracle.mx_dequant(dq.cpu(), ds.cpu(), 1), oracle.mx_dequant(wq.cpu(), ws.cpu(), 2), gs)
+    assert rel_err_chunked(got, ref) <= TOL
+    assert cosine_to_rounded(got, ref) >= COSINE_MIN
+
+
+def test_whole_output_fused_down_projection_combine():
+    """The down projection of the Mixtral-like expert layer with the weighted un-permute fused:
+    8192 tokens top-2 of 8, sorted hidden rows [16384, 14336] x wo [8, 14336, 4096] -> fp32
+    [8192, 4096]; the oracle's forward then its un-permute, fp64, on the oracle's own permute."""
+    t, k, e, f, d = 8192, 2, 8, 14336, 4096
+    rng = np.random.default_rng(11)
+    ids = np.argsort(-rng.standard_normal((t, e)), axis=1)[:, :k].astype(np.int32)
+    w_route = rng.random((t, k)).astype(np.float32)
+    gs, order, inv, _ = oracle.moe_permute(ids, np.zeros((t, 1)), e)
+    order_full = np.full(t * k, -1, np.int32)
+    order_full[:order.size] = order
+    h = ri.device_normal((t * k, f), 5100, 1.0, DEV, torch.bfloat16)
+    wo = ri.device_normal((e, f, d), 5103, 0.02, DEV, torch.bfloat16)
+    out = gg.ragged_dot_combine(h, wo, torch.from_numpy(gs).to(DEV), torch.from_numpy(order_full).to(DEV),
+                                torch.from_numpy(w_route).to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.moe_unpermute(oracle.forward(h.cpu(), wo.cpu(), gs), inv, w_route.astype(np.float64))
+    assert rel_err_chunked(out.cpu(), ref) <= TOL
