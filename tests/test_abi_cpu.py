@@ -63,6 +63,15 @@ def test_status_strings_and_version(lib):
     (dict(m=16, k=8, n=8, groups=1, mode=3, in_dtype=gg.RDOT_F32, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=12, n=8, groups=1, mode=3), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=8, n=12, groups=1, mode=3), gg.RDOT_ERR_UNSUPPORTED),
+    # the MXFP8 grad-weight: E4M3 in, fp32 out, 16-byte code rows, single-CTA tiles of its own
+    (dict(m=64, k=32, n=32, groups=2, mode=6, in_dtype=gg.RDOT_BF16, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=64, k=32, n=32, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_BF16), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=64, k=24, n=32, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=64, k=32, n=40, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=64, k=32, n=32, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_F32, tile_n=128),
+     gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=64, k=32, n=32, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_F32,
+          flags=gg.RDOT_FLAG_CTA_PAIR), gg.RDOT_ERR_UNSUPPORTED),
 ])
 def test_plan_argument_checks_without_gpu(lib, kw, status):
     base = dict(m=16, k=8, n=8, groups=1, mode=0, in_dtype=gg.RDOT_BF16, out_dtype=gg.RDOT_BF16, tile_n=0, flags=0)
@@ -77,6 +86,11 @@ def test_null_arguments_are_rejected(lib):
     assert lib.rdot_forward(None, None, None, None, None, None, None) == gg.RDOT_ERR_INVALID_ARG
     assert lib.rdot_workspace_size(None, None) == gg.RDOT_ERR_INVALID_ARG
     assert lib.rdot_plan_destroy(None) == gg.RDOT_OK
+    assert lib.rdot_forward_combine(None, None, None, None, None, None, 1, 2, None, None, None) == gg.RDOT_ERR_INVALID_ARG
+    assert lib.rdot_grad_weight_mxfp8(None, None, None, None, None, None, None, None, None) == gg.RDOT_ERR_INVALID_ARG
+    assert lib.rdot_forward_no_alloc(None, None, None, None, None, None) == gg.RDOT_ERR_INVALID_ARG
+    flags = ctypes.c_int32()
+    assert lib.rdot_no_alloc_read_status(None, ctypes.byref(flags), None) == gg.RDOT_ERR_INVALID_ARG
 
 
 def test_moe_route_argument_checks_without_gpu(lib):
