@@ -26,7 +26,8 @@ def main():
     import rdot_inputs as ri
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwd", "dgrad", "wgrad", "padded", "mxfp8", "mxwgrad"], default="fwd")
+    ap.add_argument("--kernel", choices=["fwd", "dgrad", "wgrad", "padded", "mxfp8", "mxwgrad", "gated", "permute",
+                                         "unpermute", "topk"], default="fwd")
     ap.add_argument("--workload", default="mixtral_bf16")
     ap.add_argument("--tokens", type=int, default=2048)
     ap.add_argument("--iters", type=int, default=3)
@@ -84,6 +85,39 @@ def main():
         def run():
             gg.rdot_grad_weight(plan.handle, lhs, dy, gs_d, dw, plan.workspace, stream)
         flops = 2.0 * m * k * n
+    elif args.kernel == "gated":
+        lhs = ri.device_normal((m, k), 1, 1.0, dev, torch.bfloat16)
+        w0 = ri.device_normal((g, k, n), 2, 0.02, dev, torch.bfloat16)
+        w1 = ri.device_normal((g, k, n), 3, 0.02, dev, torch.bfloat16)
+        out = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+        plan = gg.Plan(m, k, n, g, "forward_gated", "bf16", "bf16", flags=args.flags)
+
+        def run():
+            gg.rdot_forward_gated(plan.handle, lhs, w0, w1, gs_d, out, plan.workspace, stream)
+        flops = 4.0 * m * k * n
+    elif args.kernel in ("permute", "unpermute", "topk"):
+        # the routing kernels on `tokens` tokens routed top-k over the workload's experts: the
+        # permute of rows of width K, the weighted un-permute of rows of width K, the router top-k
+        t = args.tokens
+        logits = ri.device_normal((t, g), 4, 1.0, dev, torch.float32)
+        ids, wts = gg.router_topk(logits, topk, "softmax_topk")
+        x = ri.device_normal((t, k), 5, 1.0, dev, torch.bfloat16)
+        xs, gsz, order, inv = gg.moe_permute(ids, x, g)
+        plan = None
+        if args.kernel == "permute":
+            ws = torch.empty(gg.rdot_moe_route_workspace_size(t, topk, g), dtype=torch.uint8, device=dev)
+
+            def run():
+                gg.rdot_moe_permute(ids, x, g, gsz, order, inv, xs, ws, stream)
+        elif args.kernel == "unpermute":
+            outc = torch.empty((t, k), dtype=torch.bfloat16, device=dev)
+
+            def run():
+                gg.rdot_moe_unpermute(xs, inv, wts, outc, stream)
+        else:
+            def run():
+                gg.rdot_router_topk(logits, topk, gg.RDOT_ROUTER_SOFTMAX_TOPK, ids, wts, stream)
+        flops = 0.0
     elif args.kernel == "mxwgrad":
         x = ri.device_normal((m, k), 1, 1.0, dev, torch.float32)
         aq, as_ = ri.quantize_mx_e4m3_group_rows(x, gs)
@@ -117,7 +151,7 @@ def main():
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / args.iters
-    st = plan.status()
+    st = plan.status() if plan is not None else 0
     print(f"{args.kernel} {args.workload} tokens={args.tokens} M={m} K={k} N={n} G={g}: {ms:.4f} ms/launch, "
           f"{flops / ms / 1e9:.1f} TFLOP/s, status={st}")
     if st:
