@@ -229,10 +229,12 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restric
 // Paths in MaxText": jax.lax.top_k over the gate logits): each token's k highest logits, ranked by
 // value with equal values to the lower expert index, and a weight per selected expert.
 //
-// One warp per token; lane l holds experts l, l + 32, ... as 64-bit keys whose high word orders
-// the logits (sign-magnitude bits mapped to an unsigned order, -0 folded onto +0, NaN below
-// every number) and whose low word is ~expert, so the largest key is the highest logit with the
-// lowest index among equals. k rounds of a warp-wide max pick the winners in rank order.
+// One warp per token; lane l holds experts l, l + 32, ... as 32-bit ranks of their logits
+// (sign-magnitude bits mapped to an unsigned order, -0 folded onto +0, NaN below every number,
+// plus one so that 0 marks an expert already taken or past E). Each of the k rounds takes the
+// warp-wide maximum rank (redux.sync), then the lowest expert index holding it (a second
+// redux.sync over each lane's lowest candidate), so equal logits go to the lower index and the
+// winners come out in rank order; the winner's slot is then cleared.
 __device__ __forceinline__ uint32_t logit_order(float f) {
     if (f != f) return 0u;                                       // NaN: below -inf
     const uint32_t b = __float_as_uint(f == 0.0f ? 0.0f : f);   // -0 and +0 rank equal
@@ -255,31 +257,37 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const void* __restrict
     for (long long t = warp; t < tokens; t += nwarps) {
         const long long row = t * E;
         float v[IPL];
-        unsigned long long key[IPL];
+        uint32_t rank[IPL];
 #pragma unroll
         for (int i = 0; i < IPL; ++i) {
             const int e = lane + 32 * i;
             v[i] = e < E ? load_logit<BF16>(logits, row + e) : 0.0f;
-            key[i] = e < E ? (static_cast<unsigned long long>(logit_order(v[i])) << 32) | (0xFFFFFFFFu - e) : 0ull;
+            rank[i] = e < E ? logit_order(v[i]) + 1u : 0u;   // at most 0xFF800001 (+inf)
         }
-        unsigned long long mine = 0ull;   // lane r < k: the key of the r-th winner
+        int my_e = 0;        // lane r < k: the expert ranked r-th
+        float my_v = 0.0f;   // and its logit as stored (a -0 stays -0)
         for (int r = 0; r < k; ++r) {
-            unsigned long long best = key[0];
+            uint32_t best = rank[0];
 #pragma unroll
-            for (int i = 1; i < IPL; ++i) best = key[i] > best ? key[i] : best;
+            for (int i = 1; i < IPL; ++i) best = max(best, rank[i]);
+            const uint32_t top = __reduce_max_sync(0xffffffffu, best);   // >= 1: k <= E items remain
+            uint32_t cand = 0xffffffffu;                                 // this lane's lowest expert at top
 #pragma unroll
-            for (int d = 16; d > 0; d >>= 1) {
-                const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, d);
-                best = o > best ? o : best;
-            }
-            if (lane == r) mine = best;
+            for (int i = IPL - 1; i >= 0; --i) cand = rank[i] == top ? static_cast<uint32_t>(lane + 32 * i) : cand;
+            const int win = static_cast<int>(__reduce_min_sync(0xffffffffu, cand));
+            float wv = 0.0f;
 #pragma unroll
             for (int i = 0; i < IPL; ++i)
-                if (key[i] == best) key[i] = 0ull;   // keys are unique: exactly one item leaves
+                if (lane + 32 * i == win) {
+                    wv = v[i];
+                    rank[i] = 0u;
+                }
+            wv = __shfl_sync(0xffffffffu, wv, win & 31);
+            if (lane == r) {
+                my_e = win;
+                my_v = wv;
+            }
         }
-        const int my_e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine));
-        // the winner's logit as stored (a -0 stays -0); lanes past k read nothing
-        const float my_v = lane < k ? load_logit<BF16>(logits, row + my_e) : 0.0f;
         float w = my_v;
         if (mode != 0) {
             const float m = __shfl_sync(0xffffffffu, my_v, 0);   // the top-ranked logit

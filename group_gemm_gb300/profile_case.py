@@ -26,7 +26,8 @@ def main():
     import rdot_inputs as ri
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["fwd", "dgrad", "wgrad", "padded", "mxfp8", "mxwgrad", "gated", "permute",
+    ap.add_argument("--kernel", choices=["fwd", "dgrad", "wgrad", "padded", "mxfp8", "mxdgrad", "mxwgrad", "gated",
+                                         "permute",
                                          "unpermute", "topk"], default="fwd")
     ap.add_argument("--workload", default="mixtral_bf16")
     ap.add_argument("--tokens", type=int, default=2048)
@@ -129,6 +130,18 @@ def main():
 
         def run():
             gg.rdot_grad_weight_mxfp8(plan.handle, aq, as_, dq, ds, gs_d, dw, plan.workspace, stream)
+        flops = 2.0 * m * k * n
+    elif args.kernel == "mxdgrad":
+        dy = ri.device_normal((m, n), 1, 1.0, dev, torch.float32)
+        w = ri.device_normal((g, k, n), 2, 0.02, dev, torch.float32)
+        dq, ds = ri.quantize_mx_e4m3(dy, axis=1)
+        wq, ws = ri.quantize_mx_e4m3(w, axis=2)
+        del dy, w
+        out = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
+        plan = gg.Plan(m, k, n, g, "grad_input_mxfp8", "e4m3", "bf16", flags=args.flags)
+
+        def run():
+            gg.rdot_grad_input_mxfp8(plan.handle, dq, ds, wq, ws, gs_d, out, plan.workspace, stream)
         flops = 2.0 * m * k * n
     else:
         x = ri.device_normal((m, k), 1, 1.0, dev, torch.float32)
