@@ -335,7 +335,20 @@ class Plan:
         self.device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
         self.handle = rdot_plan(self.problem, self.device.index or 0)
         self.workspace = torch.zeros(rdot_workspace_size(self.handle) // 4, dtype=torch.int32, device=self.device)
+        self._workspaces = {torch.cuda.current_stream(self.device).cuda_stream: self.workspace}
         self.info = rdot_plan_info(self.handle)
+
+    def workspace_on(self, stream):
+        """A zeroed workspace for calls on ``stream`` (a torch stream), allocated on that stream
+        the first time: calls rewrite their workspace (status word, MXFP8 scale blocks,
+        grad-weight maps), so calls that may run concurrently on different streams get their own."""
+        import torch
+        ws = self._workspaces.get(stream.cuda_stream)
+        if ws is None:
+            with torch.cuda.stream(stream):
+                ws = torch.zeros_like(self.workspace)
+            self._workspaces[stream.cuda_stream] = ws
+        return ws
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -353,18 +366,36 @@ class Plan:
 _plan_cache = {}
 
 
-def _cached_plan(key, **kw):
+def _run_stream(stream, device):
+    """The torch stream a high-level call runs on: ``stream`` (a torch stream, or a raw
+    cudaStream_t as an int, 0 meaning the legacy default stream) or the device's current stream."""
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    if int(stream) == 0:
+        return torch.cuda.default_stream(device)
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
+def _cached_plan(key, stream, **kw):
+    """The plan for a shape (host state, shared by all streams) and its workspace on ``stream``."""
     p = _plan_cache.get(key)
     if p is None:
         p = Plan(**kw)
         _plan_cache[key] = p
-    return p
+    return p, p.workspace_on(stream)
 
 
 def _torch_dtype_name(dt):
     import torch
     return {torch.float32: "f32", torch.bfloat16: "bf16"}[dt]
 
+
+# The high-level calls below allocate what they return (and any scratch) on the stream their
+# kernels run on, so PyTorch's caching allocator never hands that memory to other work while
+# those kernels may still use it.
 
 def ragged_dot(lhs, rhs, group_sizes, out_dtype=None, out=None, stream=None):
     """``out[i, :] = lhs[i, :] @ rhs[g(i)]`` with rows past ``sum(group_sizes)`` zero.
@@ -378,13 +409,15 @@ def ragged_dot(lhs, rhs, group_sizes, out_dtype=None, out=None, stream=None):
         raise ValueError("shape mismatch between lhs, rhs and group_sizes")
     in_dt = _torch_dtype_name(lhs.dtype)
     out_dtype = out_dtype or lhs.dtype
+    s = _run_stream(stream, lhs.device)
     key = ("fwd", m, k, n, g, in_dt, out_dtype, lhs.device)
-    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="forward", in_dtype=in_dt,
-                        out_dtype=_torch_dtype_name(out_dtype), device=lhs.device)
-    if out is None:
-        out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
-    rdot_forward(plan.handle, lhs.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(), out,
-                 plan.workspace, stream)
+    plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="forward", in_dtype=in_dt,
+                            out_dtype=_torch_dtype_name(out_dtype), device=lhs.device)
+    with torch.cuda.stream(s):
+        if out is None:
+            out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
+        rdot_forward(plan.handle, lhs.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(), out,
+                     ws, s)
     return out
 
 
@@ -394,13 +427,15 @@ def grad_weight(lhs, dy, group_sizes, dw=None, stream=None):
     m, k = lhs.shape
     _, n = dy.shape
     g = group_sizes.shape[0]
+    s = _run_stream(stream, lhs.device)
     key = ("wgrad", m, k, n, g, lhs.device)
-    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="grad_weight", in_dtype="bf16", out_dtype="f32",
-                        device=lhs.device)
-    if dw is None:
-        dw = torch.empty((g, k, n), dtype=torch.float32, device=lhs.device)
-    rdot_grad_weight(plan.handle, lhs.contiguous(), dy.contiguous(), group_sizes.to(torch.int32).contiguous(), dw,
-                     plan.workspace, stream)
+    plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="grad_weight", in_dtype="bf16", out_dtype="f32",
+                            device=lhs.device)
+    with torch.cuda.stream(s):
+        if dw is None:
+            dw = torch.empty((g, k, n), dtype=torch.float32, device=lhs.device)
+        rdot_grad_weight(plan.handle, lhs.contiguous(), dy.contiguous(), group_sizes.to(torch.int32).contiguous(),
+                         dw, ws, s)
     return dw
 
 
@@ -412,13 +447,15 @@ def grad_input(dy, rhs, group_sizes, out_dtype=None, dlhs=None, stream=None):
     g, k, _ = rhs.shape
     out_dtype = out_dtype or dy.dtype
     names = {torch.bfloat16: "bf16", torch.float32: "f32"}
+    s = _run_stream(stream, dy.device)
     key = ("dgrad", m, k, n, g, out_dtype, dy.device)
-    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="grad_input", in_dtype="bf16",
-                        out_dtype=names[out_dtype], device=dy.device)
-    if dlhs is None:
-        dlhs = torch.empty((m, k), dtype=out_dtype, device=dy.device)
-    rdot_grad_input(plan.handle, dy.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(), dlhs,
-                    plan.workspace, stream)
+    plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="grad_input", in_dtype="bf16",
+                            out_dtype=names[out_dtype], device=dy.device)
+    with torch.cuda.stream(s):
+        if dlhs is None:
+            dlhs = torch.empty((m, k), dtype=out_dtype, device=dy.device)
+        rdot_grad_input(plan.handle, dy.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(),
+                        dlhs, ws, s)
     return dlhs
 
 
@@ -430,13 +467,15 @@ def ragged_dot_gated(lhs, w0, w1, group_sizes, out_dtype=None, out=None, stream=
     g, _, n = w0.shape
     out_dtype = out_dtype or lhs.dtype
     names = {torch.bfloat16: "bf16", torch.float32: "f32"}
+    s = _run_stream(stream, lhs.device)
     key = ("gated", m, k, n, g, out_dtype, lhs.device)
-    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="forward_gated", in_dtype="bf16",
-                        out_dtype=names[out_dtype], device=lhs.device)
-    if out is None:
-        out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
-    rdot_forward_gated(plan.handle, lhs.contiguous(), w0.contiguous(), w1.contiguous(),
-                       group_sizes.to(torch.int32).contiguous(), out, plan.workspace, stream)
+    plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="forward_gated", in_dtype="bf16",
+                            out_dtype=names[out_dtype], device=lhs.device)
+    with torch.cuda.stream(s):
+        if out is None:
+            out = torch.empty((m, n), dtype=out_dtype, device=lhs.device)
+        rdot_forward_gated(plan.handle, lhs.contiguous(), w0.contiguous(), w1.contiguous(),
+                           group_sizes.to(torch.int32).contiguous(), out, ws, s)
     return out
 
 
@@ -447,13 +486,15 @@ def grad_weight_mxfp8(lhs_q, lhs_s, dy_q, dy_s, group_sizes, out=None, stream=No
     m, k = lhs_q.shape
     n = dy_q.shape[1]
     g = group_sizes.shape[0]
+    s = _run_stream(stream, lhs_q.device)
     key = ("wgrad_mxfp8", m, k, n, g, lhs_q.device)
-    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="grad_weight_mxfp8", in_dtype="e4m3", out_dtype="f32",
-                        device=lhs_q.device)
-    if out is None:
-        out = torch.empty((g, k, n), dtype=torch.float32, device=lhs_q.device)
-    rdot_grad_weight_mxfp8(plan.handle, lhs_q.contiguous(), lhs_s.contiguous(), dy_q.contiguous(), dy_s.contiguous(),
-                           group_sizes.to(torch.int32).contiguous(), out, plan.workspace, stream)
+    plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="grad_weight_mxfp8", in_dtype="e4m3",
+                            out_dtype="f32", device=lhs_q.device)
+    with torch.cuda.stream(s):
+        if out is None:
+            out = torch.empty((g, k, n), dtype=torch.float32, device=lhs_q.device)
+        rdot_grad_weight_mxfp8(plan.handle, lhs_q.contiguous(), lhs_s.contiguous(), dy_q.contiguous(),
+                               dy_s.contiguous(), group_sizes.to(torch.int32).contiguous(), out, ws, s)
     return out
 
 
@@ -464,14 +505,16 @@ def ragged_dot_combine(lhs, rhs, group_sizes, order, topk_weights, out=None, str
     m, kdim = lhs.shape
     g, _, n = rhs.shape
     t, k = topk_weights.shape
-    if out is None:
-        out = torch.empty((t, n), dtype=torch.float32, device=lhs.device)
+    s = _run_stream(stream, lhs.device)
     key = ("fwd", m, kdim, n, g, "bf16", torch.float32, lhs.device)     # the fp32-out forward's plan
-    plan = _cached_plan(key, m=m, k=kdim, n=n, groups=g, mode="forward", in_dtype="bf16", out_dtype="f32",
-                        device=lhs.device)
-    rdot_forward_combine(plan.handle, lhs.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(),
-                         order.to(torch.int32).contiguous(),
-                         topk_weights.to(torch.float32).contiguous(), out, plan.workspace, stream)
+    plan, ws = _cached_plan(key, s, m=m, k=kdim, n=n, groups=g, mode="forward", in_dtype="bf16", out_dtype="f32",
+                            device=lhs.device)
+    with torch.cuda.stream(s):
+        if out is None:
+            out = torch.empty((t, n), dtype=torch.float32, device=lhs.device)
+        rdot_forward_combine(plan.handle, lhs.contiguous(), rhs.contiguous(), group_sizes.to(torch.int32).contiguous(),
+                             order.to(torch.int32).contiguous(), topk_weights.to(torch.float32).contiguous(), out,
+                             ws, s)
     return out
 
 
@@ -479,11 +522,13 @@ def router_topk(logits, k, weights="softmax_topk", stream=None):
     """Each token's top-k experts and their weights: returns ``(ids int32 [T, k], w fp32 [T, k])``.
     ``weights``: "values" (the logits), "softmax" (over all experts) or "softmax_topk" (over the k)."""
     import torch
-    logits = logits.contiguous()
-    t = logits.shape[0]
-    ids = torch.empty((t, k), dtype=torch.int32, device=logits.device)
-    w = torch.empty((t, k), dtype=torch.float32, device=logits.device)
-    rdot_router_topk(logits, k, _ROUTER_MODES[weights], ids, w, stream)
+    s = _run_stream(stream, logits.device)
+    with torch.cuda.stream(s):
+        logits = logits.contiguous()
+        t = logits.shape[0]
+        ids = torch.empty((t, k), dtype=torch.int32, device=logits.device)
+        w = torch.empty((t, k), dtype=torch.float32, device=logits.device)
+        rdot_router_topk(logits, k, _ROUTER_MODES[weights], ids, w, s)
     return ids, w
 
 
@@ -493,13 +538,15 @@ def moe_permute(topk_ids, x, n_experts, stream=None):
     import torch
     t, k = topk_ids.shape
     dev = x.device
-    ids = topk_ids.to(device=dev, dtype=torch.int32).contiguous()
-    gs = torch.empty(n_experts, dtype=torch.int32, device=dev)
-    order = torch.empty(t * k, dtype=torch.int32, device=dev)
-    inv = torch.empty(t * k, dtype=torch.int32, device=dev)
-    xs = torch.empty((t * k, x.shape[1]), dtype=x.dtype, device=dev)
-    ws = torch.empty(rdot_moe_route_workspace_size(t, k, n_experts), dtype=torch.uint8, device=dev)
-    rdot_moe_permute(ids, x.contiguous(), n_experts, gs, order, inv, xs, ws, stream)
+    s = _run_stream(stream, dev)
+    with torch.cuda.stream(s):
+        ids = topk_ids.to(device=dev, dtype=torch.int32).contiguous()
+        gs = torch.empty(n_experts, dtype=torch.int32, device=dev)
+        order = torch.empty(t * k, dtype=torch.int32, device=dev)
+        inv = torch.empty(t * k, dtype=torch.int32, device=dev)
+        xs = torch.empty((t * k, x.shape[1]), dtype=x.dtype, device=dev)
+        ws = torch.empty(rdot_moe_route_workspace_size(t, k, n_experts), dtype=torch.uint8, device=dev)
+        rdot_moe_permute(ids, x.contiguous(), n_experts, gs, order, inv, xs, ws, s)
     return xs, gs, order, inv
 
 
@@ -507,9 +554,11 @@ def moe_unpermute(y_sorted, inv, topk_weights, out=None, stream=None):
     """``out[t] = sum_j w[t, j] * y_sorted[inv[t*k + j]]`` (bf16 [T, N])."""
     import torch
     t, _ = topk_weights.shape
-    if out is None:
-        out = torch.empty((t, y_sorted.shape[1]), dtype=torch.bfloat16, device=y_sorted.device)
-    rdot_moe_unpermute(y_sorted.contiguous(), inv, topk_weights.to(torch.float32).contiguous(), out, stream)
+    s = _run_stream(stream, y_sorted.device)
+    with torch.cuda.stream(s):
+        if out is None:
+            out = torch.empty((t, y_sorted.shape[1]), dtype=torch.bfloat16, device=y_sorted.device)
+        rdot_moe_unpermute(y_sorted.contiguous(), inv, topk_weights.to(torch.float32).contiguous(), out, s)
     return out
 
 
@@ -518,13 +567,15 @@ def ragged_dot_mxfp8(lhs_q, lhs_scale, rhs_q, rhs_scale, group_sizes, out=None, 
     import torch
     m, k = lhs_q.shape
     g, _, n = rhs_q.shape
+    s = _run_stream(stream, lhs_q.device)
     key = ("mxfp8", m, k, n, g, lhs_q.device)
-    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="forward_mxfp8", in_dtype="e4m3", out_dtype="bf16",
-                        device=lhs_q.device)
-    if out is None:
-        out = torch.empty((m, n), dtype=torch.bfloat16, device=lhs_q.device)
-    rdot_forward_mxfp8(plan.handle, lhs_q, lhs_scale, rhs_q, rhs_scale, group_sizes.to(torch.int32).contiguous(),
-                       out, plan.workspace, stream)
+    plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="forward_mxfp8", in_dtype="e4m3", out_dtype="bf16",
+                            device=lhs_q.device)
+    with torch.cuda.stream(s):
+        if out is None:
+            out = torch.empty((m, n), dtype=torch.bfloat16, device=lhs_q.device)
+        rdot_forward_mxfp8(plan.handle, lhs_q, lhs_scale, rhs_q, rhs_scale, group_sizes.to(torch.int32).contiguous(),
+                           out, ws, s)
     return out
 
 
@@ -534,14 +585,16 @@ def padded_ragged_dot(lhs, rhs, group_sizes, capacity, out=None, pad_workspace=N
     import torch
     m, k = lhs.shape
     g, _, n = rhs.shape
+    s = _run_stream(stream, lhs.device)
     key = ("fwd", m, k, n, g, "bf16", torch.bfloat16, lhs.device)
-    plan = _cached_plan(key, m=m, k=k, n=n, groups=g, mode="forward", in_dtype="bf16", out_dtype="bf16",
-                        device=lhs.device)
+    plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="forward", in_dtype="bf16", out_dtype="bf16",
+                            device=lhs.device)
     need = rdot_padded_workspace_size(plan.handle, capacity)
-    if pad_workspace is None or pad_workspace.numel() < need:
-        pad_workspace = torch.empty(need, dtype=torch.uint8, device=lhs.device)
-    if out is None:
-        out = torch.empty((m, n), dtype=torch.bfloat16, device=lhs.device)
-    rdot_padded_forward(plan.handle, lhs, rhs, group_sizes.to(torch.int32).contiguous(), out, capacity,
-                        pad_workspace, plan.workspace, stream)
+    with torch.cuda.stream(s):
+        if pad_workspace is None or pad_workspace.numel() < need:
+            pad_workspace = torch.empty(need, dtype=torch.uint8, device=lhs.device)
+        if out is None:
+            out = torch.empty((m, n), dtype=torch.bfloat16, device=lhs.device)
+        rdot_padded_forward(plan.handle, lhs, rhs, group_sizes.to(torch.int32).contiguous(), out, capacity,
+                            pad_workspace, ws, s)
     return out, pad_workspace
