@@ -96,6 +96,25 @@ def test_whole_output_mxfp8_forward():
     assert cosine_to_rounded(got, ref) >= COSINE_MIN
 
 
+def test_whole_output_gated_up_projection():
+    """The fused gated up projection at the Mixtral-like size: silu(x . w0[g]) * (x . w1[g]) with
+    x [16384, 4096] and w0, w1 [8, 4096, 14336] (two oracle forwards, then the SiLU product)."""
+    cfg = ri.CONFIGS["mixtral_bf16"]
+    m, k, n, g = cfg["m"], cfg["k"], cfg["n"], cfg["g"]
+    gs = ri.config_group_sizes("mixtral_bf16")
+    x = ri.device_normal((m, k), 1000, 1.0, DEV, torch.bfloat16)
+    w0 = ri.device_normal((g, k, n), 2000, 0.02, DEV, torch.bfloat16)
+    w1 = ri.device_normal((g, k, n), 2001, 0.02, DEV, torch.bfloat16)
+    plan = gg.Plan(m, k, n, g, "forward_gated", "bf16", "bf16")
+    out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gg.rdot_forward_gated(plan.handle, x, w0, w1, torch.from_numpy(gs).to(DEV), out, plan.workspace)
+    assert plan.status() == 0
+    got = out.cpu()
+    ref = oracle.gated_forward(x.cpu(), w0.cpu(), w1.cpu(), gs)
+    assert rel_err_chunked(got, ref) <= TOL
+    assert cosine_to_rounded(got, ref) >= COSINE_MIN
+
+
 def test_whole_output_grad_input():
     """The data gradient of the Mixtral-like forward: dy [16384, 14336] x rhs [8, 4096, 14336]^T."""
     cfg = ri.CONFIGS["mixtral_bf16"]
