@@ -155,6 +155,16 @@ rdot_status encode_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, 
     return RDOT_OK;
 }
 
+// The MXFP8 scale-reorder pass numbers its 512-byte blocks in 32 bits: a row tile of `bm` rows
+// holds bm / 128 blocks per 128-wide K stage, the weights one per (group, 128 columns, K stage).
+// `kc` is the contracted width, `nout` the output width.
+bool mx_blocks_fit(long long m, long long kc, long long nout, int groups, int bm) {
+    const long long ks = (kc + 127) / 128;
+    const long long a_blocks = ((m + bm - 1) / bm + groups) * ks * (bm / TC_BM);
+    const long long b_blocks = static_cast<long long>(groups) * ((nout + 127) / 128) * ks;
+    return a_blocks + b_blocks <= 0x7fffffffLL;
+}
+
 rdot_status check_problem(const rdot_problem* p) {
     if (!p) return RDOT_ERR_INVALID_ARG;
     if (p->m < 0 || p->k < 1 || p->n < 1 || p->groups < 1 || p->groups > RDOT_MAX_GROUPS)
@@ -299,7 +309,9 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         pl->tile_m = 128;   // dw rows (lhs columns) per tile
         pl->tile_n = 128;
         const long long work = ((p.k + 127) / 128) * ((p.n + 127) / 128) * static_cast<long long>(p.groups);
-        if (work > 0x7fffffffLL) {
+        // the scale-reorder pass numbers its 512-byte blocks (128-row chunk x 128 columns) in 32 bits
+        const long long chunk_bound = (p.m + 127) / 128 + p.groups;
+        if (work > 0x7fffffffLL || chunk_bound * ((p.k + 127) / 128 + (p.n + 127) / 128) > 0x7fffffffLL) {
             delete pl;
             return RDOT_ERR_UNSUPPORTED;
         }
@@ -317,7 +329,7 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         pl->tile_n = p.tile_n ? p.tile_n : (p.k >= 256 ? 256 : 128);
         const int nt = static_cast<int>((p.k + pl->tile_n - 1) / pl->tile_n);
         const long long bound = forward_tile_bound(p.m, p.groups, TC_BM, nt);
-        if (bound > 0x7fffffffLL) {
+        if (bound > 0x7fffffffLL || !mx_blocks_fit(p.m, p.n, p.k, p.groups, TC_BM)) {
             delete pl;
             return RDOT_ERR_UNSUPPORTED;
         }
@@ -409,7 +421,7 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         pl->tile_n = want_pair ? 256 : (p.tile_n ? p.tile_n : (p.n >= 256 ? 256 : 128));
         const int nt = static_cast<int>((p.n + pl->tile_n - 1) / pl->tile_n);
         const long long bound = forward_tile_bound(p.m, p.groups, pl->tile_m, nt);
-        if (bound > 0x7fffffffLL) {
+        if (bound > 0x7fffffffLL || !mx_blocks_fit(p.m, p.k, p.n, p.groups, pl->tile_m)) {
             delete pl;
             return RDOT_ERR_UNSUPPORTED;
         }
@@ -689,7 +701,7 @@ rdot_status rdot_grad_input_mxfp8(rdot_plan_t plan, const void* dy_q, const uint
     a.status = static_cast<int32_t*>(workspace);
     a.timeout_ns = plan->timeout_ns;
     cudaError_t e = launch_mxfp8(plan->map_a, plan->map_b, dy_scale, w_scale, group_sizes, a, plan->grid,
-                                 4 * plan->sm_count, s);
+                                 kMxPrepBlocksPerSm * plan->sm_count, s);
     if (e != cudaSuccess) return cuda_fail(e, "mxfp8 grad_input launch");
     return RDOT_OK;
 }
@@ -855,10 +867,10 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
             plan->map_ws_ptr = workspace;
         }
         e = launch_mxfp8_pair(plan->map_a, plan->map_b, plan->map_sfa, plan->map_sfb, lhs_scale, rhs_scale,
-                              group_sizes, a, plan->grid, 4 * plan->sm_count, s);
+                              group_sizes, a, plan->grid, kMxPrepBlocksPerSm * plan->sm_count, s);
     } else {
         e = launch_mxfp8(plan->map_a, plan->map_b, lhs_scale, rhs_scale, group_sizes, a, plan->grid,
-                         4 * plan->sm_count, s);
+                         kMxPrepBlocksPerSm * plan->sm_count, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "mxfp8 launch");
     return RDOT_OK;

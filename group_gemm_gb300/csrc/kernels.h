@@ -125,6 +125,8 @@ struct MxArgs {
 
 // tmap_a: lhs codes [M, K] uint8, box (128, 128); tmap_b: rhs codes [G, K, N] uint8 as (N, K, G),
 // box (128, 128, 1); both 128-byte swizzled. Launches the scale reorder, then the GEMM.
+// Blocks per SM of the scale reorder (mx_prep_kernel): its launch bounds let three stay resident.
+constexpr int kMxPrepBlocksPerSm = 3;
 cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const uint8_t* lhs_scale,
                          const uint8_t* rhs_scale, const int32_t* group_sizes, const MxArgs& a, int grid,
                          int prep_grid, cudaStream_t stream);

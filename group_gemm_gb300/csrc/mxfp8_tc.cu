@@ -75,9 +75,9 @@ __device__ __forceinline__ uint32_t scale_word(const uint8_t* p, int avail) {
     return w;
 }
 
-__global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict__ lhs_scale,
-                                                      const uint8_t* __restrict__ rhs_scale,
-                                                      const int32_t* __restrict__ gs, MxArgs a) {
+__global__ void __launch_bounds__(256, kMxPrepBlocksPerSm)
+    mx_prep_kernel(const uint8_t* __restrict__ lhs_scale, const uint8_t* __restrict__ rhs_scale,
+                   const int32_t* __restrict__ gs, MxArgs a) {
     extern __shared__ int32_t table[];
     int32_t* off = table;
     int32_t* mt_prefix = table + a.G + 1;
@@ -87,19 +87,32 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
     if (threadIdx.x < 32) (void)group_scan_warp(gs, a.G, a.M, SBM, 1, off, mt_prefix);
     __syncthreads();
     const int KB32 = a.K / 32;
-    const long long Tm = mt_prefix[a.G];
-    const long long sfa_blocks = Tm * a.KS * halves;
-    const long long sfb_blocks = static_cast<long long>(a.G) * a.NT128 * a.KS;
+    // Work is split into units so that each warp keeps 16 loads in flight and does its index
+    // arithmetic once per unit (the pass is bound by latency, not bandwidth): an lhs unit is one
+    // 128-row block of a row tile over 4 consecutive K stages, a weight unit one (group, K stage)
+    // over all 128-column atoms, 4 atoms at a time. Indices fit 32 bits: the plan rejects
+    // problems with 2^31 blocks of 512 bytes.
+    const int Tm = mt_prefix[a.G];
+    const int KSG = (a.KS + 3) / 4;
+    // 16-byte loads of 4 stages' lhs scales need 16-byte aligned rows
+    const bool sfa_vec16 = a.sfa_vec && (KB32 % 16) == 0 && (reinterpret_cast<uintptr_t>(lhs_scale) & 15u) == 0;
+    const int units_a = Tm * halves * KSG;
+    // weight units: (group, K stage) over all atoms, or for K-major weight scales (group, atom,
+    // 4 K stages) like the lhs units
+    const int units_b = a.b_kmajor ? a.G * a.NT128 * KSG : a.G * a.KS;
+    const bool sfb_vec16 = a.b_kmajor && a.sfb_vec && (KB32 % 16) == 0 &&
+                           (reinterpret_cast<uintptr_t>(rhs_scale) & 15u) == 0;
+    const int atoms = a.BN / 128;   // atoms per tile; a tile's block holds its atoms in order
     const int lane = threadIdx.x & 31;
-    const long long warp0 = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
-    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-    for (long long b = warp0; b < sfa_blocks + sfb_blocks; b += nwarps) {
-        if (b < sfa_blocks) {
-            // block (row tile T, K stage ks, half hh): rows [row0 + 128 hh, +128) of the tile
-            const int T = static_cast<int>(b / (a.KS * halves));
-            const int rem = static_cast<int>(b - static_cast<long long>(T) * a.KS * halves);
-            const int ks = rem / halves;
-            const int hh = rem - ks * halves;
+    const int warp0 = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int nwarps = gridDim.x * (blockDim.x / 32);
+    for (int u = warp0; u < units_a + units_b; u += nwarps) {
+        uint32_t w[4][4];
+        if (u < units_a) {
+            const int T = u / (halves * KSG);
+            const int r = u - T * halves * KSG;
+            const int hh = r / KSG;
+            const int ks0 = 4 * (r - hh * KSG);
             int lo = 0, hi = a.G - 1;   // group of m-tile T: largest g with mt_prefix[g] <= T
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -108,82 +121,155 @@ __global__ void __launch_bounds__(256) mx_prep_kernel(const uint8_t* __restrict_
             }
             const int row0 = off[lo] + (T - mt_prefix[lo]) * SBM + 128 * hh;
             const int rows = min(BM, off[lo + 1] - row0);   // <= 0 for an empty half
-            const int avail = min(4, KB32 - 4 * ks);
-            // lane l gathers rows l, l+32, l+64, l+96: bytes 16*l .. 16*l+15 of the block
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = lane + 32 * i;
-                const uint8_t* src = lhs_scale + static_cast<long long>(row0 + r) * KB32 + 4 * ks;
-                w[i] = 0x7f7f7f7fu;
-                if (r < rows) w[i] = (a.sfa_vec && avail == 4) ? __ldg(reinterpret_cast<const uint32_t*>(src))
-                                                               : scale_word(src, avail);
-            }
-            reinterpret_cast<uint4*>(a.sfa + b * SFA_BYTES)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-            // one 128-column atom: (group g, 128-column block nt, K stage ks)
-            const long long bb = b - sfa_blocks;
-            const int ks = static_cast<int>(bb % a.KS);
-            const long long gn = bb / a.KS;
-            const int nt = static_cast<int>(gn % a.NT128);
-            const int g = static_cast<int>(gn / a.NT128);
-            const int avail = min(4, KB32 - 4 * ks);
-            const int atoms = a.BN / 128;   // atoms per tile; a tile's block holds its atoms in order
-            const long long blk = (static_cast<long long>(g) * a.NT + nt / atoms) * a.KS + ks;
-            uint32_t* dst = reinterpret_cast<uint32_t*>(a.sfb + blk * (atoms * SF_ATOM_BYTES) +
-                                                        (nt % atoms) * SF_ATOM_BYTES);
-            if (a.b_kmajor) {
-                // scales along K: rhs_scale [G, N, K/32]; the atom's 128 B rows are read like the
-                // lhs rows (lane l gathers rows l, l+32, l+64, l+96)
-                uint32_t w[4];
+            // lane l gathers rows l, l+32, l+64, l+96 of each stage: bytes 16*l .. 16*l+15 of its block
+            if (sfa_vec16 && ks0 + 4 <= a.KS) {
+                // the 4 stages' scales of a row are 16 contiguous, 16-byte aligned bytes: one load
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int r = lane + 32 * i;
-                    const int nrow = nt * 128 + r;
-                    w[i] = 0x7f7f7f7fu;
-                    if (nrow < a.N) {
-                        const uint8_t* src = rhs_scale + (static_cast<long long>(g) * a.N + nrow) * KB32 + 4 * ks;
-                        w[i] = (a.sfb_vec && avail == 4) ? __ldg(reinterpret_cast<const uint32_t*>(src))
-                                                         : scale_word(src, avail);
-                    }
-                }
-                reinterpret_cast<uint4*>(dst)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
-                continue;
-            }
-            const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + nt * 128;
-            const int n4 = nt * 128 + 4 * lane;         // this lane's 4 consecutive columns
-            if (a.sfb_vec && n4 + 3 < a.N) {
-                // rows kb 0..3 of the block: one coalesced 128-byte load each, then a 4 x 4 byte
-                // transpose so that word i holds the 4 scales of column n4 + i
-                uint32_t r[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    r[q] = q < avail ? __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<long long>(q) * a.N) +
-                                             lane)
-                                     : 0x7f7f7f7fu;
-                const uint32_t lo01 = __byte_perm(r[0], r[1], 0x5140), hi01 = __byte_perm(r[0], r[1], 0x7362);
-                const uint32_t lo23 = __byte_perm(r[2], r[3], 0x5140), hi23 = __byte_perm(r[2], r[3], 0x7362);
-                const uint32_t w[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
-                                       __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int nl = 4 * lane + i;      // byte 16*(nl%32) + 4*(nl/32) + kblock
-                    dst[4 * (nl & 31) + (nl >> 5)] = w[i];
+                    const int rr = lane + 32 * i;
+                    uint4 v = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+                    if (rr < rows)
+                        v = __ldg(reinterpret_cast<const uint4*>(lhs_scale + static_cast<long long>(row0 + rr) * KB32 +
+                                                                 4 * ks0));
+                    w[0][i] = v.x;
+                    w[1][i] = v.y;
+                    w[2][i] = v.z;
+                    w[3][i] = v.w;
                 }
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int nl = 4 * lane + i;
-                    uint32_t w = 0x7f7f7f7fu;
-                    if (nt * 128 + nl < a.N) {
-                        w = 0;
+                for (int j = 0; j < 4; ++j) {
+                    const int ks = ks0 + j;
+                    const int avail = min(4, KB32 - 4 * ks);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            w |= static_cast<uint32_t>(q < avail ? __ldg(src + static_cast<long long>(q) * a.N + nl)
-                                                                 : 127u)
-                                 << (8 * q);
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = lane + 32 * i;
+                        const uint8_t* src = lhs_scale + static_cast<long long>(row0 + rr) * KB32 + 4 * ks;
+                        w[j][i] = 0x7f7f7f7fu;
+                        if (ks < a.KS && rr < rows)
+                            w[j][i] = (a.sfa_vec && avail == 4) ? __ldg(reinterpret_cast<const uint32_t*>(src))
+                                                                : scale_word(src, avail);
                     }
-                    dst[4 * (nl & 31) + (nl >> 5)] = w;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int ks = ks0 + j;
+                if (ks >= a.KS) break;
+                const long long b = (static_cast<long long>(T) * a.KS + ks) * halves + hh;
+                reinterpret_cast<uint4*>(a.sfa + b * SFA_BYTES)[lane] = make_uint4(w[j][0], w[j][1], w[j][2], w[j][3]);
+            }
+            continue;
+        }
+        const int ub = u - units_a;
+        if (a.b_kmajor) {
+            // weight unit (group g, atom nt, stages ks0 .. ks0+3), scales along K: rhs_scale
+            // [G, N, K/32]; the atom's rows are read like the lhs rows (lane l gathers rows l,
+            // l+32, l+64, l+96), 4 stages at a time
+            const int g = ub / (a.NT128 * KSG);
+            const int r = ub - g * a.NT128 * KSG;
+            const int nt = r / KSG;
+            const int ks0 = 4 * (r - nt * KSG);
+            if (sfb_vec16 && ks0 + 4 <= a.KS) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int nrow = nt * 128 + lane + 32 * i;
+                    uint4 v = make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu);
+                    if (nrow < a.N)
+                        v = __ldg(reinterpret_cast<const uint4*>(rhs_scale + (static_cast<long long>(g) * a.N + nrow) *
+                                                                             KB32 + 4 * ks0));
+                    w[0][i] = v.x;
+                    w[1][i] = v.y;
+                    w[2][i] = v.z;
+                    w[3][i] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int ks = ks0 + j;
+                    const int avail = min(4, KB32 - 4 * ks);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int nrow = nt * 128 + lane + 32 * i;
+                        w[j][i] = 0x7f7f7f7fu;
+                        if (ks < a.KS && nrow < a.N) {
+                            const uint8_t* src = rhs_scale + (static_cast<long long>(g) * a.N + nrow) * KB32 + 4 * ks;
+                            w[j][i] = (a.sfb_vec && avail == 4) ? __ldg(reinterpret_cast<const uint32_t*>(src))
+                                                                : scale_word(src, avail);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int ks = ks0 + j;
+                if (ks >= a.KS) break;
+                const long long blk = (static_cast<long long>(g) * a.NT + nt / atoms) * a.KS + ks;
+                reinterpret_cast<uint4*>(a.sfb + blk * (atoms * SF_ATOM_BYTES) + (nt % atoms) * SF_ATOM_BYTES)[lane] =
+                    make_uint4(w[j][0], w[j][1], w[j][2], w[j][3]);
+            }
+            continue;
+        }
+        // weight unit (group g, K stage ks), scales along K in rows of N: the atoms nt of 128
+        // columns, 4 at a time
+        const int g = ub / a.KS;
+        const int ks = ub - g * a.KS;
+        const int avail = min(4, KB32 - 4 * ks);
+        for (int nt0 = 0; nt0 < a.NT128; nt0 += 4) {
+            bool raw[4];   // per atom: this lane's words are rows kb 0..3 still to be transposed
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int nt = nt0 + j;
+                raw[j] = false;
+                if (nt >= a.NT128) continue;
+                const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + nt * 128;
+                const int n4 = nt * 128 + 4 * lane;   // this lane's 4 consecutive columns
+                if (a.sfb_vec && n4 + 3 < a.N) {
+                    // rows kb 0..3 of the atom: one coalesced 128-byte load each
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        w[j][q] = q < avail ? __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<long long>(q) * a.N) +
+                                                    lane)
+                                            : 0x7f7f7f7fu;
+                    raw[j] = true;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int nl = 4 * lane + i;
+                        uint32_t v = 0x7f7f7f7fu;
+                        if (nt * 128 + nl < a.N) {
+                            v = 0;
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                v |= static_cast<uint32_t>(q < avail ? __ldg(src + static_cast<long long>(q) * a.N + nl)
+                                                                     : 127u)
+                                     << (8 * q);
+                        }
+                        w[j][i] = v;
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int nt = nt0 + j;
+                if (nt >= a.NT128) break;
+                const long long blk = (static_cast<long long>(g) * a.NT + nt / atoms) * a.KS + ks;
+                uint32_t* dst = reinterpret_cast<uint32_t*>(a.sfb + blk * (atoms * SF_ATOM_BYTES) +
+                                                            (nt % atoms) * SF_ATOM_BYTES);
+                uint32_t c[4] = {w[j][0], w[j][1], w[j][2], w[j][3]};
+                if (raw[j]) {
+                    // a 4 x 4 byte transpose: word i then holds the 4 scales of column n4 + i
+                    const uint32_t lo01 = __byte_perm(c[0], c[1], 0x5140), hi01 = __byte_perm(c[0], c[1], 0x7362);
+                    const uint32_t lo23 = __byte_perm(c[2], c[3], 0x5140), hi23 = __byte_perm(c[2], c[3], 0x7362);
+                    c[0] = __byte_perm(lo01, lo23, 0x5410);
+                    c[1] = __byte_perm(lo01, lo23, 0x7632);
+                    c[2] = __byte_perm(hi01, hi23, 0x5410);
+                    c[3] = __byte_perm(hi01, hi23, 0x7632);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int nl = 4 * lane + i;   // byte 16*(nl%32) + 4*(nl/32) + kblock
+                    dst[4 * (nl & 31) + (nl >> 5)] = c[i];
                 }
             }
         }

@@ -83,6 +83,8 @@ def test_mxfp8_scale_axes(vary, variant):
     (420, 96, 144, [130, 0, 77, 200, 5]),         # K = 96 (3 of 4 scale blocks), N = 144, empty group
     (512, 32, 256, [0, 256, 256, 0]),             # K = 32 (one scale block)
     (1000, 512, 384, [0, 313, 1, 0, 257, 300, 129]),   # N = 384: 1.5 tiles of 256
+    (600, 2560, 256, [100, 0, 300, 200]),          # K = 2560: 20 stages, 16-byte scale loads
+    (600, 640, 128, [100, 0, 300, 200]),           # K = 640: 20-byte scale rows, 5 stages (1 + 4)
 ])
 def test_mxfp8_ragged_parity(m, k, n, gs, variant):
     aq, as_, bq, bs, gs = make_case(m, k, n, gs, 17)
@@ -157,6 +159,8 @@ def test_mxfp8_dgrad_scale_axes(vary, tile_n):
     (420, 144, 96, [130, 0, 77, 200, 5]),          # contraction 96 (3 scale blocks), output 144
     (512, 256, 32, [0, 256, 256, 0]),              # contraction 32
     (1000, 384, 512, [0, 313, 1, 0, 257, 300, 129]),
+    (600, 256, 2560, [100, 0, 300, 200]),          # contraction 2560: 16-byte scale loads on both sides
+    (600, 384, 640, [100, 0, 300, 200]),           # contraction 640: 20-byte scale rows, 5 stages
 ])
 def test_mxfp8_dgrad_ragged_parity(m, k, n, gs, tile_n):
     dq, ds, wq, ws, gs = make_dgrad_case(m, k, n, gs, 19)
