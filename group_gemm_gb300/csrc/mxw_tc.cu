@@ -63,18 +63,9 @@ size_t smem_bytes(int G) {
     return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
 }
 
-// Byte j (j < avail) of a 32-bit word gathered from four consecutive scale rows of one column;
-// blocks past the group's rows read 127.
-__device__ __forceinline__ uint32_t gather_scale_col(const uint8_t* p, long long pitch, int avail) {
-    uint32_t w = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) w |= static_cast<uint32_t>(j < avail ? __ldg(p + j * pitch) : 127u) << (8 * j);
-    return w;
-}
-
-// One warp per 512-byte block. Blocks [0, chunks * KT) are lhs blocks (chunk-major, then the
-// 128-column tile of K), the rest dy blocks (chunk-major, then the tile of N); chunk index
-// = cp[g] + c for chunk c of group g.
+// 512-byte blocks: [0, chunks * KT) are lhs blocks (chunk-major, then the 128-column tile of K),
+// the rest dy blocks (chunk-major, then the tile of N); chunk index = cp[g] + c for chunk c of
+// group g. A warp reorders 4 blocks at a time.
 __global__ void __launch_bounds__(256) mxw_prep_kernel(const uint8_t* __restrict__ lhs_s,
                                                        const uint8_t* __restrict__ dy_s, MxwArgs a) {
     extern __shared__ int32_t table[];
@@ -92,33 +83,70 @@ __global__ void __launch_bounds__(256) mxw_prep_kernel(const uint8_t* __restrict
     const int lane = threadIdx.x & 31;
     const long long warp0 = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
     const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
-    for (long long b = warp0; b < nall; b += nwarps) {
-        const bool is_a = b < na;
-        const long long bb = is_a ? b : b - na;
-        const int tiles = is_a ? a.KT : a.NT;
-        const int cg = static_cast<int>(bb / tiles);
-        const int ct = static_cast<int>(bb - static_cast<long long>(cg) * tiles);
-        int lo = 0, hi = a.G - 1;   // group of chunk cg: the largest g with cp[g] <= cg
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (cp[mid] <= cg) lo = mid;
-            else hi = mid - 1;
-        }
-        const int c = cg - cp[lo];
-        const int rows_left = off[lo + 1] - off[lo] - c * ROWS;
-        const int avail = min(4, (rows_left + 31) / 32);     // scale blocks of this chunk
-        const int width = is_a ? a.K : a.N;
-        const uint8_t* s = is_a ? lhs_s : dy_s;
-        const long long srow0 = static_cast<long long>(bp[lo]) + 4LL * c;
-        uint32_t* dst = reinterpret_cast<uint32_t*>((is_a ? a.sfa : a.sfb) + bb * SF_BYTES);
-        // lane l takes columns 4l .. 4l+3 of the tile: word (column) = its 4 blocks, one byte each,
-        // at byte 16 (col % 32) + 4 (col / 32) of the block
+    // Each warp takes 4 blocks at a time and issues all their loads before any store: one
+    // coalesced 32-bit load per scale row (4 columns of one 32-row block) and lane, then a 4 x 4
+    // byte transpose, so that a warp keeps 16 loads in flight (the pass is latency-bound).
+    // rows of scales can be read as 32-bit words when both tensors are 4-byte aligned (their
+    // widths are multiples of 16)
+    const bool words = ((reinterpret_cast<uintptr_t>(lhs_s) | reinterpret_cast<uintptr_t>(dy_s)) & 3u) == 0;
+    for (long long b0 = warp0 * 4; b0 < nall; b0 += nwarps * 4) {
+        uint32_t w[4][4];
+        uint32_t* dst[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int cl = 4 * lane + i;
-            const int col = ct * 128 + cl;
-            const uint32_t w = col < width ? gather_scale_col(s + srow0 * width + col, width, avail) : 0x7f7f7f7fu;
-            dst[4 * (cl & 31) + (cl >> 5)] = w;
+        for (int u = 0; u < 4; ++u) {
+            const long long b = b0 + u;
+            dst[u] = nullptr;
+            if (b >= nall) continue;
+            const bool is_a = b < na;
+            const long long bb = is_a ? b : b - na;
+            const int tiles = is_a ? a.KT : a.NT;
+            const int cg = static_cast<int>(bb / tiles);
+            const int ct = static_cast<int>(bb - static_cast<long long>(cg) * tiles);
+            int lo = 0, hi = a.G - 1;   // group of chunk cg: the largest g with cp[g] <= cg
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (cp[mid] <= cg) lo = mid;
+                else hi = mid - 1;
+            }
+            const int c = cg - cp[lo];
+            const int rows_left = off[lo + 1] - off[lo] - c * ROWS;
+            const int avail = min(4, (rows_left + 31) / 32);     // scale blocks of this chunk
+            const int width = is_a ? a.K : a.N;
+            const long long srow0 = static_cast<long long>(bp[lo]) + 4LL * c;
+            // lane l takes columns 4l .. 4l+3 of the tile (all inside or all past the width,
+            // which is a multiple of 16)
+            const int col0 = ct * 128 + 4 * lane;
+            const uint8_t* src = (is_a ? lhs_s : dy_s) + srow0 * width + col0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                w[u][j] = 0x7f7f7f7fu;
+                if (col0 >= width || j >= avail) continue;
+                const uint8_t* p = src + static_cast<long long>(j) * width;
+                if (words) {
+                    w[u][j] = __ldg(reinterpret_cast<const uint32_t*>(p));
+                } else {
+                    uint32_t v = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v |= static_cast<uint32_t>(__ldg(p + q)) << (8 * q);
+                    w[u][j] = v;
+                }
+            }
+            dst[u] = reinterpret_cast<uint32_t*>((is_a ? a.sfa : a.sfb) + bb * SF_BYTES);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (!dst[u]) continue;
+            // word i = the 4 blocks' scales (one byte each) of column 4l + i, stored at byte
+            // 16 (col % 32) + 4 (col / 32) of the block
+            const uint32_t lo01 = __byte_perm(w[u][0], w[u][1], 0x5140), hi01 = __byte_perm(w[u][0], w[u][1], 0x7362);
+            const uint32_t lo23 = __byte_perm(w[u][2], w[u][3], 0x5140), hi23 = __byte_perm(w[u][2], w[u][3], 0x7362);
+            const uint32_t cw[4] = {__byte_perm(lo01, lo23, 0x5410), __byte_perm(lo01, lo23, 0x7632),
+                                    __byte_perm(hi01, hi23, 0x5410), __byte_perm(hi01, hi23, 0x7632)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int cl = 4 * lane + i;
+                dst[u][4 * (cl & 31) + (cl >> 5)] = cw[i];
+            }
         }
     }
 }

@@ -70,6 +70,28 @@ def test_mxfp8_grad_weight_matches_oracle(m, k, n, gs):
     assert rel_err(dw, ref) <= 1e-4                   # exact products, fp32 sums
 
 
+def test_mxfp8_grad_weight_scale_tensors_off_word_alignment():
+    """Scale tensors that start one byte past a word boundary are read byte by byte by the
+    scale reorder: the result is bit for bit the one from word-aligned copies."""
+    aq, as_, dq, ds, gs = make_case(700, 208, 384, [0, 127, 128, 129, 0, 300], 57)
+    m, k = aq.shape
+    n = dq.shape[1]
+    plan = gg.Plan(m, k, n, gs.size, "grad_weight_mxfp8", "e4m3", "f32")
+    ref, status = run(aq, as_, dq, ds, gs, plan)
+    assert status == 0
+    buf_a = torch.empty(as_.numel() + 16, dtype=torch.uint8, device=DEV)
+    buf_d = torch.empty(ds.numel() + 16, dtype=torch.uint8, device=DEV)
+    as_1 = buf_a[1:1 + as_.numel()].view(as_.shape)                 # one byte past a 16-byte boundary
+    ds_1 = buf_d[1:1 + ds.numel()].view(ds.shape)
+    as_1.copy_(as_.to(DEV))
+    ds_1.copy_(ds.to(DEV))
+    dw = torch.full_like(ref, float("nan"))
+    gg.rdot_grad_weight_mxfp8(plan.handle, aq.to(DEV), as_1, dq.to(DEV), ds_1, torch.from_numpy(gs).to(DEV), dw,
+                              plan.workspace)
+    assert plan.status() == 0
+    assert torch.equal(dw, ref)
+
+
 def test_mxfp8_grad_weight_next_group_nan_does_not_leak():
     """The rows of the next group that a group's last chunk reaches are loaded through the
     group's cut maps and arrive as zeros: NaN codes there stay out of this group's slab."""
