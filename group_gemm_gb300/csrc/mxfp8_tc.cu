@@ -97,9 +97,10 @@ __global__ void __launch_bounds__(256, kMxPrepBlocksPerSm)
     // 16-byte loads of 4 stages' lhs scales need 16-byte aligned rows
     const bool sfa_vec16 = a.sfa_vec && (KB32 % 16) == 0 && (reinterpret_cast<uintptr_t>(lhs_scale) & 15u) == 0;
     const int units_a = Tm * halves * KSG;
-    // weight units: (group, K stage) over all atoms, or for K-major weight scales (group, atom,
-    // 4 K stages) like the lhs units
-    const int units_b = a.b_kmajor ? a.G * a.NT128 * KSG : a.G * a.KS;
+    // weight units: (group, K stage, 4 atoms), or for K-major weight scales (group, atom, 4 K
+    // stages) like the lhs units; units of equal size keep the warps' shares even
+    const int NTG = (a.NT128 + 3) / 4;
+    const int units_b = a.b_kmajor ? a.G * a.NT128 * KSG : a.G * a.KS * NTG;
     const bool sfb_vec16 = a.b_kmajor && a.sfb_vec && (KB32 % 16) == 0 &&
                            (reinterpret_cast<uintptr_t>(rhs_scale) & 15u) == 0;
     const int atoms = a.BN / 128;   // atoms per tile; a tile's block holds its atoms in order
@@ -210,67 +211,66 @@ __global__ void __launch_bounds__(256, kMxPrepBlocksPerSm)
             }
             continue;
         }
-        // weight unit (group g, K stage ks), scales along K in rows of N: the atoms nt of 128
-        // columns, 4 at a time
-        const int g = ub / a.KS;
-        const int ks = ub - g * a.KS;
+        // weight unit (group g, K stage ks, atoms nt0 .. nt0+3), scales along K in rows of N
+        const int gk = ub / NTG;
+        const int nt0 = 4 * (ub - gk * NTG);
+        const int g = gk / a.KS;
+        const int ks = gk - g * a.KS;
         const int avail = min(4, KB32 - 4 * ks);
-        for (int nt0 = 0; nt0 < a.NT128; nt0 += 4) {
-            bool raw[4];   // per atom: this lane's words are rows kb 0..3 still to be transposed
+        bool raw[4];   // per atom: this lane's words are rows kb 0..3 still to be transposed
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int nt = nt0 + j;
-                raw[j] = false;
-                if (nt >= a.NT128) continue;
-                const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + nt * 128;
-                const int n4 = nt * 128 + 4 * lane;   // this lane's 4 consecutive columns
-                if (a.sfb_vec && n4 + 3 < a.N) {
-                    // rows kb 0..3 of the atom: one coalesced 128-byte load each
+        for (int j = 0; j < 4; ++j) {
+            const int nt = nt0 + j;
+            raw[j] = false;
+            if (nt >= a.NT128) continue;
+            const uint8_t* src = rhs_scale + (static_cast<long long>(g) * KB32 + 4 * ks) * a.N + nt * 128;
+            const int n4 = nt * 128 + 4 * lane;   // this lane's 4 consecutive columns
+            if (a.sfb_vec && n4 + 3 < a.N) {
+                // rows kb 0..3 of the atom: one coalesced 128-byte load each
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        w[j][q] = q < avail ? __ldg(reinterpret_cast<const uint32_t*>(src + static_cast<long long>(q) * a.N) +
-                                                    lane)
-                                            : 0x7f7f7f7fu;
-                    raw[j] = true;
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int nl = 4 * lane + i;
-                        uint32_t v = 0x7f7f7f7fu;
-                        if (nt * 128 + nl < a.N) {
-                            v = 0;
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                v |= static_cast<uint32_t>(q < avail ? __ldg(src + static_cast<long long>(q) * a.N + nl)
-                                                                     : 127u)
-                                     << (8 * q);
-                        }
-                        w[j][i] = v;
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t* row = reinterpret_cast<const uint32_t*>(src + static_cast<long long>(q) * a.N);
+                    w[j][q] = q < avail ? __ldg(row + lane) : 0x7f7f7f7fu;
                 }
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int nt = nt0 + j;
-                if (nt >= a.NT128) break;
-                const long long blk = (static_cast<long long>(g) * a.NT + nt / atoms) * a.KS + ks;
-                uint32_t* dst = reinterpret_cast<uint32_t*>(a.sfb + blk * (atoms * SF_ATOM_BYTES) +
-                                                            (nt % atoms) * SF_ATOM_BYTES);
-                uint32_t c[4] = {w[j][0], w[j][1], w[j][2], w[j][3]};
-                if (raw[j]) {
-                    // a 4 x 4 byte transpose: word i then holds the 4 scales of column n4 + i
-                    const uint32_t lo01 = __byte_perm(c[0], c[1], 0x5140), hi01 = __byte_perm(c[0], c[1], 0x7362);
-                    const uint32_t lo23 = __byte_perm(c[2], c[3], 0x5140), hi23 = __byte_perm(c[2], c[3], 0x7362);
-                    c[0] = __byte_perm(lo01, lo23, 0x5410);
-                    c[1] = __byte_perm(lo01, lo23, 0x7632);
-                    c[2] = __byte_perm(hi01, hi23, 0x5410);
-                    c[3] = __byte_perm(hi01, hi23, 0x7632);
-                }
+                raw[j] = true;
+            } else {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const int nl = 4 * lane + i;   // byte 16*(nl%32) + 4*(nl/32) + kblock
-                    dst[4 * (nl & 31) + (nl >> 5)] = c[i];
+                    const int nl = 4 * lane + i;
+                    uint32_t v = 0x7f7f7f7fu;
+                    if (nt * 128 + nl < a.N) {
+                        v = 0;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            v |= static_cast<uint32_t>(q < avail ? __ldg(src + static_cast<long long>(q) * a.N + nl)
+                                                                 : 127u)
+                                 << (8 * q);
+                    }
+                    w[j][i] = v;
                 }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int nt = nt0 + j;
+            if (nt >= a.NT128) break;
+            const long long blk = (static_cast<long long>(g) * a.NT + nt / atoms) * a.KS + ks;
+            uint32_t* dst = reinterpret_cast<uint32_t*>(a.sfb + blk * (atoms * SF_ATOM_BYTES) +
+                                                        (nt % atoms) * SF_ATOM_BYTES);
+            uint32_t c[4] = {w[j][0], w[j][1], w[j][2], w[j][3]};
+            if (raw[j]) {
+                // a 4 x 4 byte transpose: word i then holds the 4 scales of column n4 + i
+                const uint32_t lo01 = __byte_perm(c[0], c[1], 0x5140), hi01 = __byte_perm(c[0], c[1], 0x7362);
+                const uint32_t lo23 = __byte_perm(c[2], c[3], 0x5140), hi23 = __byte_perm(c[2], c[3], 0x7362);
+                c[0] = __byte_perm(lo01, lo23, 0x5410);
+                c[1] = __byte_perm(lo01, lo23, 0x7632);
+                c[2] = __byte_perm(hi01, hi23, 0x5410);
+                c[3] = __byte_perm(hi01, hi23, 0x7632);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int nl = 4 * lane + i;   // byte 16*(nl%32) + 4*(nl/32) + kblock
+                dst[4 * (nl & 31) + (nl >> 5)] = c[i];
             }
         }
     }
