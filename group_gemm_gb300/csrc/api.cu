@@ -309,7 +309,7 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         pl->tile_m = 128;   // dw rows (lhs columns) per tile
         pl->tile_n = 128;
         const long long work = ((p.k + 127) / 128) * ((p.n + 127) / 128) * static_cast<long long>(p.groups);
-        // the scale-reorder pass numbers its 512-byte blocks (128-row chunk x 128 columns) in 32 bits
+        // the scale reorder indexes 128-row chunks and their 512-byte blocks with 32-bit integers
         const long long chunk_bound = (p.m + 127) / 128 + p.groups;
         if (work > 0x7fffffffLL || chunk_bound * ((p.k + 127) / 128 + (p.n + 127) / 128) > 0x7fffffffLL) {
             delete pl;
