@@ -104,6 +104,20 @@ def test_mxfp8_workspace_is_reported():
     assert ws > 256   # scale blocks live in the workspace
 
 
+def test_mxfp8_plans_reject_scale_block_counts_past_32_bits():
+    """The scale reorder numbers its 512-byte blocks in 32 bits: a problem whose blocks would
+    not fit is refused at plan time (K = 2^25 over 2^20 rows: 8193 row tiles x 262144 K stages),
+    while its tile count alone would fit."""
+    with pytest.raises(RuntimeError):
+        gg.Plan(1 << 20, 1 << 25, 128, 1, "forward_mxfp8", "e4m3", "bf16")
+    with pytest.raises(RuntimeError):
+        gg.Plan(1 << 20, 128, 1 << 25, 1, "grad_input_mxfp8", "e4m3", "bf16")
+    # 8193 x 131072 blocks fit: the plan is made (its 550 GB workspace is not allocated here)
+    prob = gg.Problem(m=1 << 20, k=1 << 24, n=128, groups=1, mode=gg.RDOT_MODE_FORWARD_MXFP8, in_dtype=gg.RDOT_E4M3,
+                      out_dtype=gg.RDOT_BF16, tile_n=0, flags=0)
+    gg.rdot_plan_destroy(gg.rdot_plan(prob))
+
+
 @pytest.mark.parametrize("variant", ["t256", "pair"])
 def test_mxfp8_max_groups(variant):
     rng = np.random.default_rng(93)
