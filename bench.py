@@ -597,9 +597,14 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
         res[name] = entry
         del lhs, rhs, out, pad
         torch.cuda.empty_cache()
-    # decode-sized forwards: a few dozen tokens, so every routed expert's weights stream once
-    # (HBM-bound whatever the tile shape); reported against the HBM copy peak
-    for name, tokens, topk, sigma in (("mixtral_bf16", 64, 2, None), ("deepseek_bf16", 64, 8, 1.1)):
+    # decode-sized forwards: a few dozen tokens, or a single one, so every routed expert's weights
+    # stream once (HBM-bound whatever the tile shape: a tile's MMAs on its few valid rows take less
+    # time than its weight slab takes to arrive); reported against the HBM copy peak
+    for name, tokens, topk, sigma, key in (("mixtral_bf16", 64, 2, None, "decode_mixtral_bf16"),
+                                           ("deepseek_bf16", 64, 8, 1.1, "decode_deepseek_bf16"),
+                                           ("mixtral_bf16", 1, 2, None, "decode_mixtral_bf16_t1"),
+                                           ("deepseek_bf16", 1, 8, 1.1, "decode_deepseek_bf16_t1"),
+                                           ("deepseek_bf16", 8, 8, 1.1, "decode_deepseek_bf16_t8")):
         cfg = ri.CONFIGS[name]
         k, n, g = cfg["k"], cfg["n"], cfg["g"]
         gs = (ri.routed_group_sizes(tokens, g, topk, 1.0, seed=0) if sigma is None else
@@ -612,11 +617,18 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
         plan = gg.Plan(m, k, n, g, "forward", "bf16", "bf16", device=dev.index)
         t = _time_steps(lambda: gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace, stream), 20, stream)
         wbytes = int(np.count_nonzero(gs)) * k * n * 2 + m * (k + n) * 2
-        res[f"decode_{name}"] = {"workload": f"{tokens} tokens top-{topk}: M={m}, {int(np.count_nonzero(gs))} of {g} "
-                                             f"experts routed", "ms": round(t * 1e3, 4),
-                                 "hbm_gbs_algorithmic": round(wbytes / t / 1e9, 1),
-                                 "frac_of_hbm": round(wbytes / t / 1e9 / peaks["hbm_gbs"], 4), "status": plan.status(),
-                                 "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}"}
+        res[key] = {"workload": f"{tokens} tokens top-{topk}: M={m}, {int(np.count_nonzero(gs))} of {g} "
+                                f"experts routed", "ms": round(t * 1e3, 4),
+                    "hbm_gbs_algorithmic": round(wbytes / t / 1e9, 1),
+                    "frac_of_hbm": round(wbytes / t / 1e9 / peaks["hbm_gbs"], 4), "status": plan.status(),
+                    "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}"}
+        if plan.info["tile_m"] < 128:
+            # the plan took the swapped small-row kernel; the row-tile kernels on the same call
+            rp = gg.Plan(m, k, n, g, "forward", "bf16", "bf16", flags=gg.RDOT_FLAG_NO_SKINNY, device=dev.index)
+            tr = _time_steps(lambda: gg.rdot_forward(rp.handle, lhs, rhs, gs_d, out, rp.workspace, stream), 20,
+                             stream)
+            res[key]["ms_row_tiles"] = round(tr * 1e3, 4)
+            res[key]["tile_row_tiles"] = f"{rp.info['tile_m']}x{rp.info['tile_n']}"
         del lhs, rhs, out
         torch.cuda.empty_cache()
     # data gradient of the Mixtral-like forward: dlhs [M, K] = dy [M, N] . rhs[g]^T

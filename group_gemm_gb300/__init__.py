@@ -38,6 +38,7 @@ RDOT_MODE_FORWARD_GATED, RDOT_MODE_GRAD_INPUT_MXFP8, RDOT_MODE_GRAD_WEIGHT_MXFP8
 RDOT_STATUS_BIT_GROUP_SIZES, RDOT_STATUS_BIT_TIMEOUT = 0x1, 0x2
 RDOT_FLAG_ROW_TILES_INNER, RDOT_FLAG_COL_TILES_INNER = 0x1, 0x2
 RDOT_FLAG_CTA_PAIR, RDOT_FLAG_NO_CTA_PAIR, RDOT_FLAG_NATURAL_ORDER = 0x4, 0x8, 0x10
+RDOT_FLAG_SKINNY, RDOT_FLAG_NO_SKINNY = 0x20, 0x40
 RDOT_MAX_GROUPS = 1024
 RDOT_ROUTER_VALUES, RDOT_ROUTER_SOFTMAX, RDOT_ROUTER_SOFTMAX_TOPK, RDOT_ROUTER_MAX_TOPK = 0, 1, 2, 32
 _ROUTER_MODES = {"values": RDOT_ROUTER_VALUES, "softmax": RDOT_ROUTER_SOFTMAX, "softmax_topk": RDOT_ROUTER_SOFTMAX_TOPK}

@@ -88,6 +88,7 @@ struct rdot_plan_s {
     int grid = 1;
     bool pair = false;     // CTA pairs (256-row tiles)
     bool wide = false;     // bf16 forward on CTA pairs with 256 x 512 tiles
+    bool skinny = false;   // bf16 forward, few rows per group: the swapped product (fwd_skinny.cu)
     int big_mt = 0;        // > 0: interleaved work order (groups with >= big_mt row tiles vs the rest)
     uint64_t timeout_ns = kDefaultTimeoutNs;
     // tensor maps cached by operand pointers (re-encoded when a pointer changes)
@@ -101,6 +102,8 @@ struct rdot_plan_s {
     // gated up projection: the second weight tensor's map, cached by pointer
     const void* map_b1_ptr = nullptr;
     CUtensorMap map_b1{};
+    const void* map_bs_ptr = nullptr;   // the swapped small-row kernel's rhs map (its own box depth)
+    CUtensorMap map_bs{};
     // MXFP8 on CTA pairs: the scale blocks in the workspace, cached by workspace pointer
     const void* map_ws_ptr = nullptr;
     CUtensorMap map_sfa{}, map_sfb{};
@@ -165,13 +168,41 @@ bool mx_blocks_fit(long long m, long long kc, long long nout, int groups, int bm
     return a_blocks + b_blocks <= 0x7fffffffLL;
 }
 
+// The swapped small-row kernel (fwd_skinny.cu) takes the bf16-out forward by default for at
+// most kSkinnyMaxRows rows: there its 128-column items split the routed weights into twice as
+// many work items as 256-column row tiles, and each SM keeps more weight bytes in flight.
+constexpr long long kSkinnyMaxRows = 64;
+
+bool want_skinny(const rdot_problem& p) {
+    if (p.mode != RDOT_MODE_FORWARD || p.in_dtype != RDOT_BF16) return false;
+    if (p.flags & RDOT_FLAG_SKINNY) return true;
+    if (p.flags & (RDOT_FLAG_NO_SKINNY | RDOT_FLAG_CTA_PAIR)) return false;
+    return p.tile_n == 0 && p.out_dtype == RDOT_BF16 && p.m <= kSkinnyMaxRows;
+}
+
+// Token rows per tile of that kernel: 16 (a sixth stage of weights in flight) when, with the
+// rows spread evenly over min(M, G) groups, 16-row tiles still leave at most two work items per
+// SM; else 32 (half the token tiles re-reading each weight slab).
+int skinny_token_rows(const rdot_problem& p, int sm_count) {
+    const long long routed = std::max<long long>(1, std::min<long long>(p.m, p.groups));
+    const long long rows = (p.m + routed - 1) / routed;
+    const long long items = routed * ((rows + 15) / 16) * ((p.n + SKINNY_BN - 1) / SKINNY_BN);
+    return items <= 2LL * sm_count ? 16 : 32;
+}
+
 rdot_status check_problem(const rdot_problem* p) {
     if (!p) return RDOT_ERR_INVALID_ARG;
     if (p->m < 0 || p->k < 1 || p->n < 1 || p->groups < 1 || p->groups > RDOT_MAX_GROUPS)
         return RDOT_ERR_INVALID_ARG;
     if (p->m > 0x7fffffffLL || p->k > 0x7fffffffLL || p->n > 0x7fffffffLL) return RDOT_ERR_UNSUPPORTED;
-    if (p->flags & ~0x1F) return RDOT_ERR_INVALID_ARG;
+    if (p->flags & ~0x7F) return RDOT_ERR_INVALID_ARG;
     if ((p->flags & RDOT_FLAG_CTA_PAIR) && (p->flags & RDOT_FLAG_NO_CTA_PAIR)) return RDOT_ERR_INVALID_ARG;
+    if ((p->flags & RDOT_FLAG_SKINNY) && (p->flags & RDOT_FLAG_NO_SKINNY)) return RDOT_ERR_INVALID_ARG;
+    // the swapped small-row kernel: the bf16 forward with the plan's own tile shape only
+    if ((p->flags & RDOT_FLAG_SKINNY) &&
+        (p->mode != RDOT_MODE_FORWARD || p->in_dtype != RDOT_BF16 || (p->flags & RDOT_FLAG_CTA_PAIR) ||
+         (p->tile_n != 0 && p->tile_n != SKINNY_BN)))
+        return RDOT_ERR_UNSUPPORTED;
     if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256 && p->tile_n != 512) return RDOT_ERR_UNSUPPORTED;
     // 512-column tiles: the bf16-out forward on CTA pairs only
     if (p->tile_n == 512 && (p->mode != RDOT_MODE_FORWARD || p->in_dtype != RDOT_BF16 || p->out_dtype != RDOT_BF16 ||
@@ -262,6 +293,23 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         const int nt = static_cast<int>((p.n + SIMT_BN - 1) / SIMT_BN);
         const long long bound = forward_tile_bound(p.m, p.groups, SIMT_BM, nt);
         pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, 4LL * pl->sm_count)));
+    } else if (want_skinny(p)) {
+        if (prop.major != 10) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->kind = 1;
+        pl->skinny = true;
+        pl->tile_m = skinny_token_rows(p, pl->sm_count);   // token rows per tile (the MMA's N)
+        pl->tile_n = SKINNY_BN;   // output columns per tile (the MMA's M)
+        pl->m_inner = 1;          // the token tiles of a group read one weight slab together
+        const int nt = static_cast<int>((p.n + pl->tile_n - 1) / pl->tile_n);
+        const long long bound = forward_tile_bound(p.m, p.groups, pl->tile_m, nt);
+        if (bound > 0x7fffffffLL) {
+            delete pl;
+            return RDOT_ERR_UNSUPPORTED;
+        }
+        pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
     } else if (p.mode == RDOT_MODE_FORWARD && p.in_dtype == RDOT_BF16) {
         if (prop.major != 10) {
             delete pl;
@@ -579,11 +627,22 @@ rdot_status forward_launch(rdot_plan_t plan, const void* lhs, const void* rhs, c
     }
     if (plan->map_lhs_ptr != lhs) {
         rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs, p.k, p.m, p.k * 2, TC_BK,
-                                   TC_BM);
+                                   plan->skinny ? plan->tile_m : TC_BM);
         if (st == RDOT_OK && plan->pair)
             st = encode_2d(&plan->map_a64, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lhs, p.k, p.m, p.k * 2, TC_BK, 64);
         if (st != RDOT_OK) return st;
         plan->map_lhs_ptr = lhs;
+    }
+    if (plan->skinny) {
+        if (plan->map_bs_ptr != rhs) {
+            rdot_status st = encode_3d(&plan->map_bs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rhs, p.n, p.k, p.groups,
+                                       p.n * 2, p.k * p.n * 2, 64, SKINNY_KD, 1);
+            if (st != RDOT_OK) return st;
+            plan->map_bs_ptr = rhs;
+        }
+        e = launch_fwd_skinny(plan->map_a, plan->map_bs, a, plan->tile_m, p.out_dtype == RDOT_F32, plan->grid, s);
+        if (e != cudaSuccess) return cuda_fail(e, "fwd_skinny launch");
+        return RDOT_OK;
     }
     if (plan->map_rhs_ptr != rhs) {
         rdot_status st = encode_3d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rhs, p.n, p.k, p.groups, p.n * 2,
@@ -630,7 +689,7 @@ rdot_status rdot_forward_combine(rdot_plan_t plan, const void* lhs, const void* 
     if (!plan || !group_sizes || !workspace || tokens < 0 || topk < 1) return RDOT_ERR_INVALID_ARG;
     const rdot_problem& p = plan->p;
     if (p.mode != RDOT_MODE_FORWARD || plan->kind != 1) return RDOT_ERR_INVALID_ARG;
-    if (p.out_dtype != RDOT_F32 || plan->wide) return RDOT_ERR_UNSUPPORTED;
+    if (p.out_dtype != RDOT_F32 || plan->wide || plan->skinny) return RDOT_ERR_UNSUPPORTED;
     if (tokens * static_cast<int64_t>(topk) != p.m) return RDOT_ERR_INVALID_ARG;
     if (p.m == 0) return RDOT_OK;
     if (!lhs || !rhs || !out || !order || !topk_weights) return RDOT_ERR_INVALID_ARG;

@@ -47,7 +47,17 @@ def test_status_strings_and_version(lib):
     (dict(m=16, k=8, n=8, groups=gg.RDOT_MAX_GROUPS + 1), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=-1, k=8, n=8, groups=1), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=16, k=12, n=8, groups=1, in_dtype=gg.RDOT_BF16), gg.RDOT_ERR_UNSUPPORTED),
-    (dict(m=16, k=8, n=8, groups=1, flags=0x20), gg.RDOT_ERR_INVALID_ARG),
+    (dict(m=16, k=8, n=8, groups=1, flags=0x80), gg.RDOT_ERR_INVALID_ARG),
+    # the swapped small-row forward: bf16 in, forward mode, 64- or 128-column tiles, no CTA pairs
+    (dict(m=16, k=8, n=8, groups=1, in_dtype=gg.RDOT_BF16, flags=gg.RDOT_FLAG_SKINNY | gg.RDOT_FLAG_NO_SKINNY),
+     gg.RDOT_ERR_INVALID_ARG),
+    (dict(m=16, k=8, n=8, groups=1, in_dtype=gg.RDOT_F32, out_dtype=gg.RDOT_F32, flags=gg.RDOT_FLAG_SKINNY),
+     gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=8, n=8, groups=1, in_dtype=gg.RDOT_BF16, flags=gg.RDOT_FLAG_SKINNY | gg.RDOT_FLAG_CTA_PAIR),
+     gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=8, n=8, groups=1, in_dtype=gg.RDOT_BF16, tile_n=256, flags=gg.RDOT_FLAG_SKINNY),
+     gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=8, n=8, groups=1, mode=3, flags=gg.RDOT_FLAG_SKINNY), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=8, n=8, groups=1, flags=gg.RDOT_FLAG_CTA_PAIR | gg.RDOT_FLAG_NO_CTA_PAIR), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=16, k=8, n=8, groups=1, tile_n=96), gg.RDOT_ERR_UNSUPPORTED),
     # 512-column tiles exist for the bf16-out forward on CTA pairs only
