@@ -76,9 +76,11 @@ def kernel_source_hash(files):
 
 KERNEL_SOURCES = {
     "fwd_tc_kernel": ["group_gemm_gb300/csrc/fwd_tc.cu", "group_gemm_gb300/csrc/ptx.cuh",
-                      "group_gemm_gb300/csrc/sched.cuh", "group_gemm_gb300/csrc/epilogue.cuh"],
+                      "group_gemm_gb300/csrc/sched.cuh", "group_gemm_gb300/csrc/epilogue.cuh",
+                      "group_gemm_gb300/csrc/pdl.cuh"],
     "fwd_tc2_kernel": ["group_gemm_gb300/csrc/fwd_tc2.cu", "group_gemm_gb300/csrc/ptx.cuh",
-                       "group_gemm_gb300/csrc/sched.cuh", "group_gemm_gb300/csrc/epilogue.cuh"],
+                       "group_gemm_gb300/csrc/sched.cuh", "group_gemm_gb300/csrc/epilogue.cuh",
+                       "group_gemm_gb300/csrc/pdl.cuh"],
 }
 
 

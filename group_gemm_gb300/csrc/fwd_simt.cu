@@ -9,6 +9,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -49,6 +50,7 @@ __device__ __forceinline__ void zero_tail_rows(void* out, long long first_row, l
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(THREADS) fwd_simt_kernel(const float* __restrict__ lhs,
                                                            const float* __restrict__ rhs, FwdArgs a) {
+    grid_dependency_enter();
     extern __shared__ int32_t table[];   // off[G+1], tile_prefix[G+1]
     __shared__ float As[BK][SIMT_BM + 4];
     __shared__ float Bs[BK][SIMT_BN];
@@ -177,10 +179,9 @@ cudaError_t launch_fwd_simt(const float* lhs, const float* rhs, const FwdArgs& a
                             cudaStream_t stream) {
     const size_t shm = sizeof(int32_t) * 2 * (a.G + 1);
     if (out_bf16)
-        fwd_simt_kernel<true><<<grid, THREADS, shm, stream>>>(lhs, rhs, a);
+        return launch_pdl(fwd_simt_kernel<true>, dim3(grid), dim3(THREADS), shm, stream, lhs, rhs, a);
     else
-        fwd_simt_kernel<false><<<grid, THREADS, shm, stream>>>(lhs, rhs, a);
-    return cudaGetLastError();
+        return launch_pdl(fwd_simt_kernel<false>, dim3(grid), dim3(THREADS), shm, stream, lhs, rhs, a);
 }
 
 cudaError_t launch_scan_export(const int32_t* group_sizes, int G, int M, int BM, int NT, int m_inner, int big_mt,

@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_alloc(tmem_holder, TMEM_COLS);
         tmem_relinquish();
     }
+    grid_dependency_enter();   // group sizes and operands may come from the previous kernel
     if (warp == 2) {
         // work items: per group, ceil(rows / TT) token tiles times NT column tiles of BN
         const int bad = group_scan_warp(a.group_sizes, a.G, a.M, TT, a.NT, off, tprefix);
@@ -282,8 +284,7 @@ cudaError_t launch_tt(const CUtensorMap& tmap_x, const CUtensorMap& tmap_w, cons
     auto kern = out_f32 ? fwd_skinny_kernel<TT, true> : fwd_skinny_kernel<TT, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, shm, stream>>>(tmap_x, tmap_w, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(THREADS), shm, stream, tmap_x, tmap_w, a);
 }
 }  // namespace
 

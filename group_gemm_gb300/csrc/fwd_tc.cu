@@ -28,6 +28,7 @@
 
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -97,6 +98,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_alloc(tmem_holder, L::TMEM_COLS);
         tmem_relinquish();
     }
+    grid_dependency_enter();   // group sizes and operands may come from the previous kernel
     if (warp == 2) {
         const int bad = group_scan_warp(a.group_sizes, a.G, a.M, TC_BM, a.NT, off, tprefix);
         if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
@@ -304,8 +306,7 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const FwdAr
     }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, shm, stream>>>(ta, tb, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(THREADS), shm, stream, ta, tb, a);
 }
 
 }  // namespace

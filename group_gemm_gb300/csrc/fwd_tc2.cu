@@ -28,6 +28,7 @@
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "pairdrain.cuh"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -108,6 +109,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tmem_alloc_pair(tmem_holder, TMEM_COLS);   // collectively, one warp in each CTA of the pair
         tmem_relinquish_pair();
     }
+    grid_dependency_enter();   // group sizes and operands may come from the previous kernel
     if (warp == 2) {
         const int bad = group_scan_warp(a.group_sizes, a.G, a.M, BM, a.NT, off, tprefix);
         if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
@@ -353,8 +355,7 @@ cudaError_t launch_one(const CUtensorMap& ta, const CUtensorMap& tb, const CUten
     auto kern = fwd_tc2_kernel<OUT_F32, VAR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, shm, stream>>>(ta, tb, tb1, ta64, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(THREADS), shm, stream, ta, tb, tb1, ta64, a);
 }
 
 }  // namespace

@@ -19,6 +19,7 @@
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "pairdrain.cuh"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -92,6 +93,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tmem_alloc_pair(tmem_holder, TMEM_COLS);
         tmem_relinquish_pair();
     }
+    grid_dependency_enter();   // group sizes and operands may come from the previous kernel
     if (warp == 2) {
         const int bad = group_scan_warp(a.group_sizes, a.G, a.M, BM, a.NT, off, tprefix);
         if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
@@ -277,8 +279,7 @@ cudaError_t launch_fwd_tc2w(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b
     cudaError_t e =
         cudaFuncSetAttribute(fwd_tc2w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    fwd_tc2w_kernel<<<grid, THREADS, shm, stream>>>(tmap_a, tmap_b, a);
-    return cudaGetLastError();
+    return launch_pdl(fwd_tc2w_kernel, dim3(grid), dim3(THREADS), shm, stream, tmap_a, tmap_b, a);
 }
 
 int fwd_tc2w_max_clusters(int G) {

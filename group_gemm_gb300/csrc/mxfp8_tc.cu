@@ -28,6 +28,7 @@
 
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -78,6 +79,7 @@ __device__ __forceinline__ uint32_t scale_word(const uint8_t* p, int avail) {
 __global__ void __launch_bounds__(256, kMxPrepBlocksPerSm)
     mx_prep_kernel(const uint8_t* __restrict__ lhs_scale, const uint8_t* __restrict__ rhs_scale,
                    const int32_t* __restrict__ gs, MxArgs a) {
+    grid_dependency_enter();
     extern __shared__ int32_t table[];
     int32_t* off = table;
     int32_t* mt_prefix = table + a.G + 1;
@@ -325,6 +327,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_alloc(tmem_holder, L::TMEM_COLS);
         tmem_relinquish();
     }
+    grid_dependency_enter();   // group sizes and operands may come from the previous kernel
     if (warp == 2) {
         const int bad = group_scan_warp(group_sizes, a.G, a.M, BM, a.NT, off, tprefix);
         if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
@@ -518,8 +521,7 @@ cudaError_t launch_main(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, co
     auto kern = a.b_kmajor ? mxfp8_tc_kernel<BN, true> : mxfp8_tc_kernel<BN, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, shm, stream>>>(tmap_a, tmap_b, group_sizes, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(THREADS), shm, stream, tmap_a, tmap_b, group_sizes, a);
 }
 
 }  // namespace
@@ -527,8 +529,8 @@ cudaError_t launch_main(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, co
 cudaError_t launch_mx_prep(const uint8_t* lhs_scale, const uint8_t* rhs_scale, const int32_t* group_sizes,
                            const MxArgs& a, int prep_grid, cudaStream_t stream) {
     const size_t prep_shm = sizeof(int32_t) * 2 * (a.G + 1);
-    mx_prep_kernel<<<prep_grid, 256, prep_shm, stream>>>(lhs_scale, rhs_scale, group_sizes, a);
-    return cudaGetLastError();
+    return launch_pdl(mx_prep_kernel, dim3(prep_grid), dim3(256), prep_shm, stream, lhs_scale, rhs_scale, group_sizes,
+                      a);
 }
 
 cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const uint8_t* lhs_scale,

@@ -19,6 +19,7 @@
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "pairdrain.cuh"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -97,6 +98,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tmem_alloc_pair(tmem_holder, TMEM_COLS);
         tmem_relinquish_pair();
     }
+    grid_dependency_enter();   // group sizes and operands may come from the previous kernel
     if (warp == 2) {
         const int bad = group_scan_warp(group_sizes, a.G, a.M, BM, a.NT, off, tprefix);
         if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
@@ -272,8 +274,8 @@ cudaError_t launch_mxfp8_pair(const CUtensorMap& tmap_a, const CUtensorMap& tmap
     const size_t shm = smem_bytes(a.G);
     e = cudaFuncSetAttribute(mxfp8_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    mxfp8_tc2_kernel<<<grid, THREADS, shm, stream>>>(tmap_a, tmap_b, tmap_sfa, tmap_sfb, group_sizes, a);
-    return cudaGetLastError();
+    return launch_pdl(mxfp8_tc2_kernel, dim3(grid), dim3(THREADS), shm, stream, tmap_a, tmap_b, tmap_sfa, tmap_sfb,
+                      group_sizes, a);
 }
 
 int mxfp8_pair_max_clusters(int G) {

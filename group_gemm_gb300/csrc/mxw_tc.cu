@@ -34,6 +34,7 @@
 //                    group's slab is written as zeros.
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -68,6 +69,7 @@ size_t smem_bytes(int G) {
 // group g. A warp reorders 4 blocks at a time.
 __global__ void __launch_bounds__(256) mxw_prep_kernel(const uint8_t* __restrict__ lhs_s,
                                                        const uint8_t* __restrict__ dy_s, MxwArgs a) {
+    grid_dependency_enter();
     extern __shared__ int32_t table[];
     int32_t* off = table;
     int32_t* cp = table + a.G + 1;             // 128-row chunks before each group
@@ -190,6 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_alloc(tmem_holder, TMEM_COLS);
         tmem_relinquish();
     }
+    grid_dependency_enter();   // group sizes and operands may come from the previous kernel
     if (warp == 2) {
         const int bad = group_scan_warp(a.group_sizes, a.G, a.M, ROWS, 1, off, cp);
         if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
@@ -385,14 +388,12 @@ cudaError_t launch_mxw(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, co
                        const uint8_t* lhs_s, const uint8_t* dy_s, const MxwArgs& a, int grid, int prep_grid,
                        cudaStream_t stream) {
     const size_t prep_shm = sizeof(int32_t) * 3 * (a.G + 1);
-    mxw_prep_kernel<<<prep_grid, 256, prep_shm, stream>>>(lhs_s, dy_s, a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(mxw_prep_kernel, dim3(prep_grid), dim3(256), prep_shm, stream, lhs_s, dy_s, a);
     if (e != cudaSuccess) return e;
     const size_t shm = smem_bytes(a.G);
     e = cudaFuncSetAttribute(mxw_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    mxw_tc_kernel<<<grid, THREADS, shm, stream>>>(tmap_x, tmap_dy, tmap_dw, a);
-    return cudaGetLastError();
+    return launch_pdl(mxw_tc_kernel, dim3(grid), dim3(THREADS), shm, stream, tmap_x, tmap_dy, tmap_dw, a);
 }
 
 }  // namespace rdot

@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -21,6 +22,7 @@ __global__ void __launch_bounds__(THREADS) pad_scatter_kernel(const uint8_t* __r
                                                               const int32_t* __restrict__ gs, uint8_t* lhs_pad,
                                                               int32_t* uniform_gs, int M, int G, int C,
                                                               long long row_bytes, int32_t* status) {
+    grid_dependency_enter();
     extern __shared__ int32_t table[];
     int32_t* off = table;
     int32_t* unused = table + G + 1;
@@ -55,6 +57,7 @@ __global__ void __launch_bounds__(THREADS) pad_scatter_kernel(const uint8_t* __r
 __global__ void __launch_bounds__(THREADS) pad_gather_kernel(const uint8_t* __restrict__ out_pad,
                                                              const int32_t* __restrict__ gs, uint8_t* out, int M,
                                                              int G, int C, long long row_bytes) {
+    grid_dependency_enter();
     extern __shared__ int32_t table[];
     int32_t* off = table;
     int32_t* unused = table + G + 1;
@@ -88,18 +91,15 @@ __global__ void __launch_bounds__(THREADS) pad_gather_kernel(const uint8_t* __re
 cudaError_t launch_pad_scatter(const void* lhs, const int32_t* gs, void* lhs_pad, int32_t* uniform_gs, int M, int G,
                                int C, long long row_bytes, int grid, int32_t* status, cudaStream_t stream) {
     const size_t shm = sizeof(int32_t) * 2 * (G + 1);
-    pad_scatter_kernel<<<grid, THREADS, shm, stream>>>(static_cast<const uint8_t*>(lhs), gs,
-                                                       static_cast<uint8_t*>(lhs_pad), uniform_gs, M, G, C, row_bytes,
-                                                       status);
-    return cudaGetLastError();
+    return launch_pdl(pad_scatter_kernel, dim3(grid), dim3(THREADS), shm, stream, static_cast<const uint8_t*>(lhs), gs,
+                      static_cast<uint8_t*>(lhs_pad), uniform_gs, M, G, C, row_bytes, status);
 }
 
 cudaError_t launch_pad_gather(const void* out_pad, const int32_t* gs, void* out, int M, int G, int C,
                               long long row_bytes, int grid, cudaStream_t stream) {
     const size_t shm = sizeof(int32_t) * 2 * (G + 1);
-    pad_gather_kernel<<<grid, THREADS, shm, stream>>>(static_cast<const uint8_t*>(out_pad), gs,
-                                                      static_cast<uint8_t*>(out), M, G, C, row_bytes);
-    return cudaGetLastError();
+    return launch_pdl(pad_gather_kernel, dim3(grid), dim3(THREADS), shm, stream, static_cast<const uint8_t*>(out_pad),
+                      gs, static_cast<uint8_t*>(out), M, G, C, row_bytes);
 }
 
 }  // namespace rdot

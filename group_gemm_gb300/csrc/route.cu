@@ -21,6 +21,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 
 namespace rdot {
@@ -32,6 +33,7 @@ constexpr int VEC_UNROLL = 4;   // 16-byte loads in flight per lane (gather, com
 
 __global__ void __launch_bounds__(32) moe_count_kernel(const int32_t* __restrict__ ids, long long total, int E,
                                                        int32_t* __restrict__ chunk_hist) {
+    grid_dependency_enter();
     extern __shared__ int32_t cnt[];
     const int lane = threadIdx.x;
     for (int e = lane; e < E; e += 32) cnt[e] = 0;
@@ -53,6 +55,7 @@ __global__ void __launch_bounds__(32) moe_count_kernel(const int32_t* __restrict
 __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E,
                                                         int32_t* __restrict__ group_sizes,
                                                         int32_t* __restrict__ expert_base, int32_t* __restrict__ valid) {
+    grid_dependency_enter();
     __shared__ int32_t tot[1024];
     __shared__ int32_t warp_sum[32];
     const int e = threadIdx.x;
@@ -103,6 +106,7 @@ __global__ void __launch_bounds__(32) moe_place_kernel(const int32_t* __restrict
                                                        const int32_t* __restrict__ chunk_base,
                                                        const int32_t* __restrict__ expert_base,
                                                        int32_t* __restrict__ order, int32_t* __restrict__ inv) {
+    grid_dependency_enter();
     extern __shared__ int32_t pos[];
     const int lane = threadIdx.x;
     for (int e = lane; e < E; e += 32)
@@ -145,6 +149,7 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict
                                                          int32_t* __restrict__ order, const int32_t* __restrict__ valid,
                                                          long long tokens, int k, int vec_per_row,
                                                          uint4* __restrict__ x_sorted) {
+    grid_dependency_enter();
     const int lane = threadIdx.x & 31;
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -187,6 +192,7 @@ __device__ __forceinline__ void acc_bf16x8(float (&a)[8], uint4 u, float w) {
 __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ inv,
                                                           const float* __restrict__ w, long long tokens, int k,
                                                           int vec_per_row, uint4* __restrict__ out) {
+    grid_dependency_enter();
     const int lane = threadIdx.x & 31;
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -251,6 +257,7 @@ template <int IPL, bool BF16>
 __global__ void __launch_bounds__(256) router_topk_kernel(const void* __restrict__ logits, long long tokens, int E,
                                                           int k, int mode, int32_t* __restrict__ ids,
                                                           float* __restrict__ weights) {
+    grid_dependency_enter();
     const int lane = threadIdx.x & 31;
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
@@ -314,10 +321,11 @@ template <int IPL>
 cudaError_t launch_topk_ipl(const void* logits, bool bf16, long long tokens, int E, int k, int mode, int32_t* ids,
                             float* weights, int grid, cudaStream_t stream) {
     if (bf16)
-        router_topk_kernel<IPL, true><<<grid, 256, 0, stream>>>(logits, tokens, E, k, mode, ids, weights);
+        return launch_pdl(router_topk_kernel<IPL, true>, dim3(grid), dim3(256), 0, stream, logits, tokens, E, k, mode, ids,
+                          weights);
     else
-        router_topk_kernel<IPL, false><<<grid, 256, 0, stream>>>(logits, tokens, E, k, mode, ids, weights);
-    return cudaGetLastError();
+        return launch_pdl(router_topk_kernel<IPL, false>, dim3(grid), dim3(256), 0, stream, logits, tokens, E, k, mode, ids,
+                          weights);
 }
 
 }  // namespace
@@ -352,16 +360,19 @@ cudaError_t launch_moe_permute(const int32_t* ids, long long tokens, int k, int 
     int32_t* valid = reinterpret_cast<int32_t*>(ws + hist_bytes);
     int32_t* expert_base = reinterpret_cast<int32_t*>(ws + hist_bytes + 256);
     const size_t cnt_shm = sizeof(int32_t) * E;
-    moe_count_kernel<<<static_cast<unsigned>(nchunks), 32, cnt_shm, stream>>>(ids, total, E, chunk_hist);
-    moe_scan_kernel<<<1, 1024, 0, stream>>>(chunk_hist, static_cast<int>(nchunks), E, group_sizes, expert_base, valid);
-    moe_place_kernel<<<static_cast<unsigned>(nchunks), 32, cnt_shm, stream>>>(ids, total, E, chunk_hist, expert_base,
-                                                                             order, inv);
+    const dim3 chunks(static_cast<unsigned>(nchunks));
+    cudaError_t e = launch_pdl(moe_count_kernel, chunks, dim3(32), cnt_shm, stream, ids, total, E, chunk_hist);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(moe_scan_kernel, dim3(1), dim3(1024), 0, stream, chunk_hist, static_cast<int>(nchunks), E, group_sizes,
+                   expert_base, valid);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(moe_place_kernel, chunks, dim3(32), cnt_shm, stream, ids, total, E, chunk_hist, expert_base, order, inv);
+    if (e != cudaSuccess) return e;
     const int vec = static_cast<int>(row_bytes / 16);
     const long long want = (tokens + 7) / 8;
     const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
-    moe_gather_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), inv, order, valid, tokens, k, vec,
-                                                static_cast<uint4*>(x_sorted));
-    return cudaGetLastError();
+    return launch_pdl(moe_gather_kernel, dim3(grid), dim3(256), 0, stream, static_cast<const uint4*>(x), inv, order, valid,
+                      tokens, k, vec, static_cast<uint4*>(x_sorted));
 }
 
 cudaError_t launch_moe_combine(const void* y_sorted, const int32_t* inv, const float* weights, long long tokens, int k,
@@ -369,9 +380,8 @@ cudaError_t launch_moe_combine(const void* y_sorted, const int32_t* inv, const f
     const int vec = static_cast<int>(n / 8);
     const long long want = (tokens + 7) / 8;
     const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
-    moe_combine_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(y_sorted), inv, weights, tokens, k, vec,
-                                                 static_cast<uint4*>(out));
-    return cudaGetLastError();
+    return launch_pdl(moe_combine_kernel, dim3(grid), dim3(256), 0, stream, static_cast<const uint4*>(y_sorted), inv,
+                      weights, tokens, k, vec, static_cast<uint4*>(out));
 }
 
 }  // namespace rdot

@@ -17,6 +17,7 @@
 // the epilogue of one tile overlap the next tile's mainloop.
 #include "epilogue.cuh"
 #include "kernels.h"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -63,6 +64,7 @@ __device__ __forceinline__ WgTile wg_decode(int w, int KT, int NT, const int32_t
 // One block: offsets by a warp scan, then per group g two map copies with rows = off[g+1].
 __global__ void __launch_bounds__(1024) wg_maps_kernel(const __grid_constant__ CUtensorMap tmap_x,
                                                        const __grid_constant__ CUtensorMap tmap_dy, WgradArgs a) {
+    grid_dependency_enter();
     extern __shared__ int32_t wg_table[];
     int32_t* off = wg_table;
     if (threadIdx.x < 32) (void)group_scan_warp(a.group_sizes, a.G, a.M, 1, 1, off, wg_table + a.G + 1);
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_alloc(tmem_holder, L::TMEM_COLS);
         tmem_relinquish();
     }
+    grid_dependency_enter();   // group sizes and operands may come from the previous kernel
     if (warp == 2) {
         const int bad = group_scan_warp(a.group_sizes, a.G, a.M, 1, 1, off, unused);
         if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
@@ -318,8 +321,7 @@ cudaError_t launch_wg(const CUtensorMap& tx, const CUtensorMap& tdy, const CUten
     auto kern = wgrad_tc_kernel<BN, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, shm, stream>>>(tx, tdy, tdw, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(THREADS), shm, stream, tx, tdy, tdw, a);
 }
 
 }  // namespace
@@ -327,8 +329,7 @@ cudaError_t launch_wg(const CUtensorMap& tx, const CUtensorMap& tdy, const CUten
 cudaError_t launch_wg_maps(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const WgradArgs& a,
                            cudaStream_t stream) {
     const size_t shm = sizeof(int32_t) * 2 * (a.G + 1);
-    wg_maps_kernel<<<1, 1024, shm, stream>>>(tmap_x, tmap_dy, a);
-    return cudaGetLastError();
+    return launch_pdl(wg_maps_kernel, dim3(1), dim3(1024), shm, stream, tmap_x, tmap_dy, a);
 }
 
 cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,

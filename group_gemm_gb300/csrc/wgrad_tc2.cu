@@ -19,6 +19,7 @@
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "pairdrain.cuh"
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -109,6 +110,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tmem_alloc_pair(tmem_holder, TMEM_COLS);
         tmem_relinquish_pair();
     }
+    grid_dependency_enter();   // group sizes and operands may come from the previous kernel
     if (warp == 2) {
         const int bad = group_scan_warp(a.group_sizes, a.G, a.M, 1, 1, off, unused);
         if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
@@ -301,8 +303,7 @@ cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_
     cudaError_t e =
         cudaFuncSetAttribute(wgrad_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    wgrad_tc2_kernel<<<grid, THREADS, shm, stream>>>(tmap_x, tmap_dy, tmap_dw, a);
-    return cudaGetLastError();
+    return launch_pdl(wgrad_tc2_kernel, dim3(grid), dim3(THREADS), shm, stream, tmap_x, tmap_dy, tmap_dw, a);
 }
 
 int wgrad_tc2_max_clusters(int G) {

@@ -222,3 +222,51 @@ def test_skinny_plan_serves_the_padded_baseline_on_the_same_weights():
         gg.rdot_padded_forward(plan.handle, lhs, rhs, gs_d, out, 128, pad, plan.workspace)
         assert rel_err(out, ref) <= TOL_BF16
     assert plan.status() == 0
+
+
+# ------------------------------------------------------------- long contractions
+LONG_K_CASES = [
+    # m, k, n, group sizes
+    (8, 512, 3584, [1] * 8),            # one row per group, 224 work items on 152 SMs
+    (8, 768, 2560, [1] * 8),            # six 128-deep stages per item
+    (9, 1024, 520, [2, 0, 0, 4, 3]),    # eight stages, an 8-column last tile
+    (60, 1024, 384, [0, 40, 1, 19]),    # 40 rows: three token tiles, the last with the next group's row
+]
+
+
+@pytest.mark.parametrize("m,k,n,gs", LONG_K_CASES)
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_skinny_long_contraction_parity(m, k, n, gs, out_dtype):
+    gs = np.asarray(gs, np.int32)
+    lhs = torch.from_numpy(ri.host_normal((m, k), 96)).to(torch.bfloat16)
+    rhs = torch.from_numpy(ri.host_normal((gs.size, k, n), 97, 0.05)).to(torch.bfloat16)
+    total = int(gs.sum())
+    lhs[total:] = float("nan")
+    out, status, _ = run(lhs, rhs, gs, out_dtype=out_dtype)
+    ref = oracle.forward(lhs, rhs, gs)
+    assert status == 0
+    assert rel_err(out, ref) <= TOL_BF16
+    assert cosine_to_rounded(out, ref, out_dtype) >= COSINE_MIN
+    assert torch.all(out[total:] == 0)
+
+
+def test_skinny_repeatable_and_same_through_the_no_alloc_entry():
+    """Each output is one accumulator's fixed sequence of MMAs, so repeated calls, and the
+    no-allocation entry point on the same plan, agree bit for bit."""
+    m, k, n, gs = 8, 512, 3584, np.ones(8, np.int32)
+    lhs = torch.from_numpy(ri.host_normal((m, k), 98)).to(torch.bfloat16).to(DEV)
+    rhs = torch.from_numpy(ri.host_normal((gs.size, k, n), 99, 0.05)).to(torch.bfloat16).to(DEV)
+    plan = gg.Plan(m, k, n, gs.size, "forward", "bf16", "f32", flags=SKINNY)
+    gs_d = torch.from_numpy(gs).to(DEV)
+    outs = []
+    for _ in range(3):
+        out = torch.full((m, n), float("nan"), dtype=torch.float32, device=DEV)
+        gg.rdot_forward(plan.handle, lhs, rhs, gs_d, out, plan.workspace)
+        outs.append(out)
+    assert plan.status() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    na = torch.full((m, n), float("nan"), dtype=torch.float32, device=DEV)
+    gg.rdot_forward_no_alloc(plan.handle, lhs, rhs, gs_d, na)
+    torch.cuda.synchronize()
+    assert torch.equal(na, outs[0])
+    assert rel_err(outs[0], oracle.forward(lhs.cpu(), rhs.cpu(), gs)) <= 1e-5
