@@ -183,6 +183,22 @@ bool want_skinny(const rdot_problem& p) {
 // Token rows per tile of that kernel: 16 (a sixth stage of weights in flight) when, with the
 // rows spread evenly over min(M, G) groups, 16-row tiles still leave at most two work items per
 // SM; else 32 (half the token tiles re-reading each weight slab).
+// Output columns per work item of that kernel: 64 (twice the items, one 256-deep box a stage)
+// with 16-row token tiles when, with rows spread as above, the weight bytes of the busiest SM
+// fall by a quarter; else 128. A 64-column item streams more slowly (one 128-byte segment per
+// weight row), so smaller gains in balance do not pay for it.
+int skinny_tile_cols(const rdot_problem& p, int sm_count, int token_rows) {
+    if (p.tile_n != 0) return p.tile_n;
+    if (token_rows != 16) return 128;
+    const long long routed = std::max<long long>(1, std::min<long long>(p.m, p.groups));
+    const long long rows = (p.m + routed - 1) / routed;
+    const long long w128 = routed * ((rows + token_rows - 1) / token_rows) * ((p.n + 127) / 128);
+    const long long w64 = routed * ((rows + token_rows - 1) / token_rows) * ((p.n + 63) / 64);
+    const long long rounds128 = (w128 + sm_count - 1) / sm_count;   // in 128-column items
+    const long long rounds64 = (w64 + sm_count - 1) / sm_count;     // in 64-column items
+    return 4 * rounds64 <= 3 * 2 * rounds128 ? 64 : 128;
+}
+
 int skinny_token_rows(const rdot_problem& p, int sm_count) {
     const long long routed = std::max<long long>(1, std::min<long long>(p.m, p.groups));
     const long long rows = (p.m + routed - 1) / routed;
@@ -201,9 +217,11 @@ rdot_status check_problem(const rdot_problem* p) {
     // the swapped small-row kernel: the bf16 forward with the plan's own tile shape only
     if ((p->flags & RDOT_FLAG_SKINNY) &&
         (p->mode != RDOT_MODE_FORWARD || p->in_dtype != RDOT_BF16 || (p->flags & RDOT_FLAG_CTA_PAIR) ||
-         (p->tile_n != 0 && p->tile_n != SKINNY_BN)))
+         (p->tile_n != 0 && p->tile_n != 64 && p->tile_n != SKINNY_BN)))
         return RDOT_ERR_UNSUPPORTED;
-    if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256 && p->tile_n != 512) return RDOT_ERR_UNSUPPORTED;
+    if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256 && p->tile_n != 512 &&
+        !(p->tile_n == 64 && (p->flags & RDOT_FLAG_SKINNY)))
+        return RDOT_ERR_UNSUPPORTED;
     // 512-column tiles: the bf16-out forward on CTA pairs only
     if (p->tile_n == 512 && (p->mode != RDOT_MODE_FORWARD || p->in_dtype != RDOT_BF16 || p->out_dtype != RDOT_BF16 ||
                              (p->flags & RDOT_FLAG_NO_CTA_PAIR)))
@@ -301,7 +319,7 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         pl->kind = 1;
         pl->skinny = true;
         pl->tile_m = skinny_token_rows(p, pl->sm_count);   // token rows per tile (the MMA's N)
-        pl->tile_n = SKINNY_BN;   // output columns per tile (the MMA's M)
+        pl->tile_n = skinny_tile_cols(p, pl->sm_count, pl->tile_m);   // output columns per tile
         pl->m_inner = 1;          // the token tiles of a group read one weight slab together
         const int nt = static_cast<int>((p.n + pl->tile_n - 1) / pl->tile_n);
         const long long bound = forward_tile_bound(p.m, p.groups, pl->tile_m, nt);
@@ -636,11 +654,12 @@ rdot_status forward_launch(rdot_plan_t plan, const void* lhs, const void* rhs, c
     if (plan->skinny) {
         if (plan->map_bs_ptr != rhs) {
             rdot_status st = encode_3d(&plan->map_bs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rhs, p.n, p.k, p.groups,
-                                       p.n * 2, p.k * p.n * 2, 64, SKINNY_KD, 1);
+                                       p.n * 2, p.k * p.n * 2, 64, skinny_stage_rows(plan->tile_n), 1);
             if (st != RDOT_OK) return st;
             plan->map_bs_ptr = rhs;
         }
-        e = launch_fwd_skinny(plan->map_a, plan->map_bs, a, plan->tile_m, p.out_dtype == RDOT_F32, plan->grid, s);
+        e = launch_fwd_skinny(plan->map_a, plan->map_bs, a, plan->tile_m, plan->tile_n, p.out_dtype == RDOT_F32,
+                              plan->grid, s);
         if (e != cudaSuccess) return cuda_fail(e, "fwd_skinny launch");
         return RDOT_OK;
     }
@@ -1133,18 +1152,20 @@ rdot_status rdot_padded_forward(rdot_plan_t plan, const void* lhs, const void* r
     a.K = static_cast<int>(p.k);
     a.N = static_cast<int>(p.n);
     a.G = p.groups;
-    a.NT = static_cast<int>((p.n + plan->tile_n - 1) / plan->tile_n);
+    // a swapped small-row plan runs the padded GEMM with 128 x 128 row tiles
+    const int bn = plan->skinny ? 128 : plan->tile_n;
+    a.NT = static_cast<int>((p.n + bn - 1) / bn);
     a.m_inner = C <= p.n ? 1 : 0;
     a.status = status;
     a.timeout_ns = plan->timeout_ns;
-    const long long bound = forward_tile_bound(rows_pad, p.groups, plan->tile_m, a.NT);
+    const long long bound = forward_tile_bound(rows_pad, p.groups, plan->skinny ? TC_BM : plan->tile_m, a.NT);
     if (plan->pair) {
         const int grid = 2 * static_cast<int>(std::max<long long>(1, std::min<long long>(bound, plan->grid / 2)));
         e = plan->wide ? launch_fwd_tc2w(plan->pad_map_a, plan->map_b, a, grid, s)
                        : launch_fwd_tc2(plan->pad_map_a, plan->map_b, a, p.out_dtype == RDOT_F32, grid, s);
     } else {
         const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, plan->sm_count)));
-        e = launch_fwd_tc(plan->pad_map_a, plan->map_b, a, plan->tile_n, p.out_dtype == RDOT_F32, grid, s);
+        e = launch_fwd_tc(plan->pad_map_a, plan->map_b, a, bn, p.out_dtype == RDOT_F32, grid, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "padded GEMM launch");
     e = launch_pad_gather(out_pad, group_sizes, out, static_cast<int>(p.m), p.groups, C, p.n * esz_out,

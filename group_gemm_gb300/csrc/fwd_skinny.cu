@@ -11,13 +11,17 @@
 //   - the MMA's M is 128 weight columns (A = rhs[g] read MN-major, the layout it already has),
 //     its N is a tile of TT = 16 or 32 token rows (B = lhs rows, K-major), K = 16 per
 //     instruction;
-//   - a stage is 128 deep in K: 32 KB of weights (two 64-column boxes, 128 rows each) and
-//     TT * 256 bytes of tokens; as many stages as fit next to a 1024-group table keep 192 KB
-//     (TT = 16) or 160 KB (TT = 32) of weights in flight per SM (fwd_tc: 128 KB);
-//   - work items are (group, TT-row token tile, 128 weight columns), token tiles fastest, so
-//     the token tiles of one group read a weight slab at the same time through L2. Past N the
-//     MMA's lanes hold products of a stale box and are never stored (each lane depends on its
-//     own weight column);
+//   - a stage holds 32 KB of weights: two 64-column boxes 128 rows deep in K (CPT = 2), or one
+//     64-column box 256 rows deep (CPT = 1), and the matching TT rows of tokens; as many stages
+//     as fit next to a 1024-group table keep 160-192 KB of weights in flight per SM (fwd_tc:
+//     128 KB);
+//   - work items are (group, TT-row token tile, 64 CPT weight columns), token tiles fastest, so
+//     the token tiles of one group read a weight slab at the same time through L2. Items of 64
+//     columns make twice as many items from the same weights, for when 128-column items would
+//     leave SMs idle in the last round; their MMAs still span 128 lanes, the second 64-column
+//     half reading the first box again (a zero stride between the two halves), and lanes
+//     64..127 are not stored. Past N the MMA's lanes hold products of a stale box and are never
+//     stored either (each lane depends on its own weight column);
 //   - the accumulator is 128 lanes (output columns) x 32 columns (tokens), two of them so the
 //     epilogue of one tile overlaps the next; lane l of quarter q holds output column
 //     n0 + 32 q + l for every token, and a warp writes each token's 32 consecutive outputs.
@@ -47,16 +51,16 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 }
 
 constexpr int THREADS = 192;     // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int BN = SKINNY_BN;    // weight columns per tile (the MMA's M)
-constexpr int KD = SKINNY_KD;    // K rows per stage
+constexpr int BN = SKINNY_BN;    // the MMA's M: weight columns of one accumulator
 constexpr int BAR_EXTRA = 5;     // tfull[2], tempty[2], drain
 constexpr int MISC_BYTES = 16;   // tmem base, abort flag
 constexpr int SMEM_MAX = 227 * 1024;
 
-template <int TT>
+template <int TT, int CPT>
 struct Ring {
+    static constexpr int KD = 2 * SKINNY_KD / CPT;         // K rows per stage
     static constexpr int W_CHUNK_BYTES = 64 * KD * 2;      // 64 columns x KD rows: one box of the rhs map
-    static constexpr int W_BYTES = (BN / 64) * W_CHUNK_BYTES;
+    static constexpr int W_BYTES = CPT * W_CHUNK_BYTES;
     static constexpr int X_BOX_BYTES = TT * 64 * 2;        // TT rows x 64 K: one box of the lhs map
     static constexpr int X_BYTES = (KD / 64) * X_BOX_BYTES;
     static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
@@ -75,11 +79,13 @@ struct Ring {
     }
 };
 
-template <int TT, bool OUT_F32>
+template <int TT, int CPT, bool OUT_F32>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                       FwdArgs a) {
-    using L = Ring<TT>;
+    using L = Ring<TT, CPT>;
+    constexpr int KD = L::KD;
+    constexpr int BNT = 64 * CPT;   // output columns per work item
     constexpr int TMEM_COLS = L::TMEM_COLS;
     constexpr int STAGES = L::STAGES;
     constexpr int STAGE_BYTES = L::STAGE_BYTES;
@@ -142,8 +148,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
                 const Tile t = decode_tile(w, tprefix, off, a.G, TT, a.NT, true);
-                const int n0 = t.nt * BN;
-                const int chunks = min(BN / 64, (a.N - n0 + 63) / 64);   // weight boxes not wholly past N
+                const int n0 = t.nt * BNT;
+                const int chunks = min(CPT, (a.N - n0 + 63) / 64);   // weight boxes not wholly past N
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
                         ok = false;
@@ -196,9 +202,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sx = sw + L::W_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < KD / 16; ++kk) {
-                        // weights: +16 K rows of 128 bytes per K step, the two 64-column boxes
-                        // W_CHUNK_BYTES apart; tokens: +32 bytes per K step inside a 64-wide box
-                        const uint64_t adesc = smem_desc_sw128(sw + kk * 2048, L::W_CHUNK_BYTES, 1024);
+                        // weights: +16 K rows of 128 bytes per K step, the two 64-column halves
+                        // W_CHUNK_BYTES apart (or both from the one box); tokens: +32 bytes per K
+                        // step inside a 64-wide box
+                        const uint64_t adesc = smem_desc_sw128(sw + kk * 2048, CPT == 2 ? L::W_CHUNK_BYTES : 0, 1024);
                         const uint64_t bdesc = smem_desc_sw128(sx + (kk >> 2) * L::X_BOX_BYTES + (kk & 3) * 32, 16,
                                                                1024);
                         mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
@@ -237,8 +244,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
-            const int col = t.nt * BN + q * 32 + lane;
-            if (col < a.N) {
+            const int col = t.nt * BNT + q * 32 + lane;
+            if (q * 32 + lane < BNT && col < a.N) {
 #pragma unroll
                 for (int j = 0; j < TT; ++j) {
                     if (j >= t.rows) break;
@@ -277,11 +284,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace
 
 namespace {
-template <int TT>
+template <int TT, int CPT>
 cudaError_t launch_tt(const CUtensorMap& tmap_x, const CUtensorMap& tmap_w, const FwdArgs& a, bool out_f32, int grid,
                       cudaStream_t stream) {
-    const size_t shm = Ring<TT>::smem_bytes(a.G);
-    auto kern = out_f32 ? fwd_skinny_kernel<TT, true> : fwd_skinny_kernel<TT, false>;
+    const size_t shm = Ring<TT, CPT>::smem_bytes(a.G);
+    auto kern = out_f32 ? fwd_skinny_kernel<TT, CPT, true> : fwd_skinny_kernel<TT, CPT, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(THREADS), shm, stream, tmap_x, tmap_w, a);
@@ -289,10 +296,15 @@ cudaError_t launch_tt(const CUtensorMap& tmap_x, const CUtensorMap& tmap_w, cons
 }  // namespace
 
 cudaError_t launch_fwd_skinny(const CUtensorMap& tmap_x, const CUtensorMap& tmap_w, const FwdArgs& a, int tt,
-                              bool out_f32, int grid, cudaStream_t stream) {
+                              int tile_cols, bool out_f32, int grid, cudaStream_t stream) {
     if (a.G < 1 || a.G > RDOT_MAX_GROUPS) return cudaErrorInvalidValue;
-    if (tt == 16) return launch_tt<16>(tmap_x, tmap_w, a, out_f32, grid, stream);
-    if (tt == 32) return launch_tt<32>(tmap_x, tmap_w, a, out_f32, grid, stream);
+    if (tile_cols == 128) {
+        if (tt == 16) return launch_tt<16, 2>(tmap_x, tmap_w, a, out_f32, grid, stream);
+        if (tt == 32) return launch_tt<32, 2>(tmap_x, tmap_w, a, out_f32, grid, stream);
+    } else if (tile_cols == 64) {
+        if (tt == 16) return launch_tt<16, 1>(tmap_x, tmap_w, a, out_f32, grid, stream);
+        if (tt == 32) return launch_tt<32, 1>(tmap_x, tmap_w, a, out_f32, grid, stream);
+    }
     return cudaErrorInvalidValue;
 }
 

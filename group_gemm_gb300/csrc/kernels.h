@@ -59,12 +59,14 @@ constexpr int TC_BM = 128;
 constexpr int TC_BK = 64;
 
 // bf16 inputs, a few rows per group (fwd_skinny.cu): the swapped product, weight columns on the
-// MMA's M and tokens on its N. tt: token rows per tile, 16 or 32; tmap_x: lhs [M,K] box (64, tt);
-// tmap_w: rhs [G][K][N] box (64, SKINNY_KD, 1).
-constexpr int SKINNY_BN = 128;   // weight (output) columns per tile
-constexpr int SKINNY_KD = 128;   // K rows per pipeline stage
+// MMA's M and tokens on its N. tt: token rows per tile, 16 or 32; tile_cols: output columns per
+// work item, 128 or 64; tmap_x: lhs [M,K] box (64, tt); tmap_w: rhs [G][K][N] box
+// (64, skinny_stage_rows(tile_cols), 1).
+constexpr int SKINNY_BN = 128;   // weight columns of the MMA
+constexpr int SKINNY_KD = 128;   // K rows per pipeline stage with 128-column items
+inline int skinny_stage_rows(int tile_cols) { return tile_cols == 64 ? 2 * SKINNY_KD : SKINNY_KD; }
 cudaError_t launch_fwd_skinny(const CUtensorMap& tmap_x, const CUtensorMap& tmap_w, const FwdArgs& a, int tt,
-                              bool out_f32, int grid, cudaStream_t stream);
+                              int tile_cols, bool out_f32, int grid, cudaStream_t stream);
 
 // bf16 inputs on CTA pairs (fwd_tc2.cu): clusters of 2 CTAs, 256 x 256 tiles, same maps as
 // launch_fwd_tc. grid must be even (2 CTAs per cluster).

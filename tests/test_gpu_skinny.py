@@ -58,7 +58,7 @@ SKINNY_CASES = [
 
 
 @pytest.mark.parametrize("m,k,n,gs", SKINNY_CASES)
-@pytest.mark.parametrize("tile_n", [0, 128])
+@pytest.mark.parametrize("tile_n", [0, 64, 128])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_skinny_forward_parity(m, k, n, gs, tile_n, out_dtype):
     gs = np.asarray(gs, np.int32)
@@ -67,7 +67,8 @@ def test_skinny_forward_parity(m, k, n, gs, tile_n, out_dtype):
     total = int(gs.sum())
     lhs[total:] = float("nan")                   # rows past the sum must never leak
     out, status, plan = run(lhs, rhs, gs, out_dtype=out_dtype, tile_n=tile_n)
-    assert plan.info["tile_m"] in (16, 32) and plan.info["tile_n"] == 128
+    assert plan.info["tile_m"] in (16, 32) and plan.info["tile_n"] == (tile_n or plan.info["tile_n"])
+    assert plan.info["tile_n"] in (64, 128)
     ref = oracle.forward(lhs, rhs, gs)
     assert status == 0
     assert rel_err(out, ref) <= TOL_BF16
@@ -125,14 +126,15 @@ def test_skinny_invalid_sizes_follow_the_clamping_reading():
 
 @pytest.mark.parametrize("gs, m", [([3, 2, 4], 9), ([0, 0, 5, 0, 33, 0], 60), ([40, 1, 1, 64, 32, 33], 171),
                                    ([5, -3, 7, 20], 20)])
-def test_skinny_tile_map_bit_exact(gs, m):
+@pytest.mark.parametrize("tile_n", [64, 128])
+def test_skinny_tile_map_bit_exact(gs, m, tile_n):
     gs = np.asarray(gs, np.int32)
     n = 520
-    plan = gg.Plan(m, 64, n, gs.size, "forward", "bf16", "bf16", flags=SKINNY)
+    plan = gg.Plan(m, 64, n, gs.size, "forward", "bf16", "bf16", tile_n=tile_n, flags=SKINNY)
     info = plan.info
-    assert info["tile_m"] in (16, 32) and (info["tile_n"], info["m_inner"]) == (128, 1)
+    assert info["tile_m"] in (16, 32) and (info["tile_n"], info["m_inner"]) == (tile_n, 1)
     off_ref, _ = oracle.offsets(gs, m)
-    pref_ref, tiles_ref = oracle.tile_map(gs, m, n, info["tile_m"], 128, True, 0)
+    pref_ref, tiles_ref = oracle.tile_map(gs, m, n, info["tile_m"], tile_n, True, 0)
     gs_d = torch.from_numpy(gs).to(DEV)
     off = torch.full((gs.size + 1,), -7, dtype=torch.int32, device=DEV)
     pref = torch.full((gs.size + 1,), -7, dtype=torch.int32, device=DEV)
@@ -170,7 +172,7 @@ def test_skinny_default_choice():
     """Few routed rows and bf16 output take the swapped kernel unless told not to; fp32 output,
     more rows, or RDOT_FLAG_NO_SKINNY keep the row-tile kernels."""
     decode = gg.Plan(2, 4096, 14336, 8, "forward", "bf16", "bf16")
-    assert decode.info["tile_m"] in (16, 32) and decode.info["tile_n"] == 128
+    assert decode.info["tile_m"] in (16, 32) and decode.info["tile_n"] in (64, 128)
     assert gg.Plan(2, 4096, 14336, 8, "forward", "bf16", "bf16",
                    flags=gg.RDOT_FLAG_NO_SKINNY).info["tile_m"] in (128, 256)
     assert gg.Plan(2, 4096, 14336, 8, "forward", "bf16", "f32").info["tile_m"] in (128, 256)
@@ -180,7 +182,6 @@ def test_skinny_default_choice():
 @pytest.mark.parametrize("kw", [dict(flags=SKINNY | gg.RDOT_FLAG_NO_SKINNY),
                                 dict(flags=SKINNY | gg.RDOT_FLAG_CTA_PAIR),
                                 dict(flags=SKINNY, tile_n=256),
-                                dict(flags=SKINNY, tile_n=64),
                                 dict(flags=SKINNY, in_dtype="f32"),
                                 dict(flags=SKINNY, mode="grad_input")])
 def test_skinny_refused_combinations(kw):
@@ -236,13 +237,14 @@ LONG_K_CASES = [
 
 @pytest.mark.parametrize("m,k,n,gs", LONG_K_CASES)
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-def test_skinny_long_contraction_parity(m, k, n, gs, out_dtype):
+@pytest.mark.parametrize("tile_n", [0, 64])
+def test_skinny_long_contraction_parity(m, k, n, gs, out_dtype, tile_n):
     gs = np.asarray(gs, np.int32)
     lhs = torch.from_numpy(ri.host_normal((m, k), 96)).to(torch.bfloat16)
     rhs = torch.from_numpy(ri.host_normal((gs.size, k, n), 97, 0.05)).to(torch.bfloat16)
     total = int(gs.sum())
     lhs[total:] = float("nan")
-    out, status, _ = run(lhs, rhs, gs, out_dtype=out_dtype)
+    out, status, _ = run(lhs, rhs, gs, out_dtype=out_dtype, tile_n=tile_n)
     ref = oracle.forward(lhs, rhs, gs)
     assert status == 0
     assert rel_err(out, ref) <= TOL_BF16
