@@ -794,7 +794,16 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                      stream)
     res["wgrad_bf16"]["other_tile"] = {"tile": f"{other.info['tile_m']}x{other.info['tile_n']}",
                                        "tflops": round(fl / t2 / 1e12, 3), "ms": round(t2 * 1e3, 4)}
-    del lhs, dy, dw
+    # the same weight gradient with a bf16 dw (the output type of the pages' wgrad_wi example)
+    dwh = torch.empty((g, k, n), dtype=torch.bfloat16, device=dev)
+    ph = gg.Plan(m, k, n, g, "grad_weight", "bf16", "bf16", device=dev.index)
+    t3 = _time_steps(lambda: gg.rdot_grad_weight(ph.handle, lhs, dy, gs_d, dwh, ph.workspace, stream), steps, stream)
+    min_bytes_h = 2 * m * (k + n) + 2 * g * k * n
+    res["wgrad_bf16"]["dw_bf16"] = {"tflops": round(fl / t3 / 1e12, 3), "ms": round(t3 * 1e3, 4),
+                                    "frac_of_bf16_peak": round(fl / t3 / 1e12 / peaks["bf16_tflops"], 4),
+                                    "hbm_gbs_algorithmic": round(min_bytes_h / t3 / 1e9, 1), "status": ph.status(),
+                                    "tile": f"{ph.info['tile_m']}x{ph.info['tile_n']}"}
+    del lhs, dy, dw, dwh
     torch.cuda.empty_cache()
     # MXFP8 forward
     cfg = ri.CONFIGS["mxfp8"]

@@ -422,19 +422,22 @@ def ragged_dot(lhs, rhs, group_sizes, out_dtype=None, out=None, stream=None):
     return out
 
 
-def grad_weight(lhs, dy, group_sizes, dw=None, stream=None):
-    """``dw[g] = lhs_g^T dy_g`` (fp32 [G, K, N]) for bf16 lhs [M, K] and dy [M, N]."""
+def grad_weight(lhs, dy, group_sizes, out_dtype=None, dw=None, stream=None):
+    """``dw[g] = lhs_g^T dy_g`` ([G, K, N], fp32 by default or bf16) for bf16 lhs [M, K] and
+    dy [M, N]."""
     import torch
     m, k = lhs.shape
     _, n = dy.shape
     g = group_sizes.shape[0]
+    out_dtype = out_dtype or (dw.dtype if dw is not None else torch.float32)
+    names = {torch.bfloat16: "bf16", torch.float32: "f32"}
     s = _run_stream(stream, lhs.device)
-    key = ("wgrad", m, k, n, g, lhs.device)
-    plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="grad_weight", in_dtype="bf16", out_dtype="f32",
-                            device=lhs.device)
+    key = ("wgrad", m, k, n, g, out_dtype, lhs.device)
+    plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="grad_weight", in_dtype="bf16",
+                            out_dtype=names[out_dtype], device=lhs.device)
     with torch.cuda.stream(s):
         if dw is None:
-            dw = torch.empty((g, k, n), dtype=torch.float32, device=lhs.device)
+            dw = torch.empty((g, k, n), dtype=out_dtype, device=lhs.device)
         rdot_grad_weight(plan.handle, lhs.contiguous(), dy.contiguous(), group_sizes.to(torch.int32).contiguous(),
                          dw, ws, s)
     return dw

@@ -240,7 +240,8 @@ rdot_status check_problem(const rdot_problem* p) {
             }
             return RDOT_ERR_UNSUPPORTED;
         case RDOT_MODE_GRAD_WEIGHT:
-            if (p->in_dtype != RDOT_BF16 || p->out_dtype != RDOT_F32) return RDOT_ERR_UNSUPPORTED;
+            if (p->in_dtype != RDOT_BF16 || (p->out_dtype != RDOT_F32 && p->out_dtype != RDOT_BF16))
+                return RDOT_ERR_UNSUPPORTED;
             if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;
             return RDOT_OK;
         case RDOT_MODE_GRAD_WEIGHT_MXFP8:
@@ -955,7 +956,7 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
 }
 
 rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, const int32_t* group_sizes,
-                             float* dw, void* workspace, void* stream) {
+                             void* dw, void* workspace, void* stream) {
     if (!plan || !group_sizes || !workspace || !dw) return RDOT_ERR_INVALID_ARG;
     const rdot_problem& p = plan->p;
     if (p.mode != RDOT_MODE_GRAD_WEIGHT || plan->kind != 2) return RDOT_ERR_INVALID_ARG;
@@ -969,7 +970,8 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p.m == 0) {
         // no rows at all: every slab is zero
-        cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * p.groups * p.k * p.n, s);
+        const size_t esz = p.out_dtype == RDOT_BF16 ? 2 : 4;
+        cudaError_t e = cudaMemsetAsync(dw, 0, esz * p.groups * p.k * p.n, s);
         return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "cudaMemsetAsync");
     }
     // boxes of 64 columns x the kernel's contraction rows per stage
@@ -985,9 +987,13 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = dy;
     }
+    const bool out_bf16 = p.out_dtype == RDOT_BF16;
     if (plan->map_out_ptr != dw) {
-        rdot_status st = encode_3d(&plan->map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dw, p.n, p.k, p.groups, p.n * 4,
-                                   p.k * p.n * 4, 32, 32, 1);
+        // 128-byte rows of the staging tile: 32 fp32 or 64 bf16 columns by 32 dw rows
+        rdot_status st = out_bf16 ? encode_3d(&plan->map_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dw, p.n, p.k,
+                                              p.groups, p.n * 2, p.k * p.n * 2, 64, 32, 1)
+                                  : encode_3d(&plan->map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dw, p.n, p.k,
+                                              p.groups, p.n * 4, p.k * p.n * 4, 32, 32, 1);
         if (st != RDOT_OK) return st;
         plan->map_out_ptr = dw;
     }
@@ -1005,9 +1011,9 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
     a.timeout_ns = plan->timeout_ns;
     cudaError_t e = launch_wg_maps(plan->map_a, plan->map_b, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "wgrad group maps launch");
-    e = plan->pair ? launch_wgrad_tc2(plan->map_a, plan->map_b, plan->map_out, a, plan->grid, s)
-                               : launch_wgrad_tc(plan->map_a, plan->map_b, plan->map_out, a, plan->tile_n,
-                                                 plan->grid, s);
+    e = plan->pair ? launch_wgrad_tc2(plan->map_a, plan->map_b, plan->map_out, a, out_bf16, plan->grid, s)
+                   : launch_wgrad_tc(plan->map_a, plan->map_b, plan->map_out, a, plan->tile_n, out_bf16, plan->grid,
+                                     s);
     if (e != cudaSuccess) return cuda_fail(e, "wgrad_tc launch");
     return RDOT_OK;
 }

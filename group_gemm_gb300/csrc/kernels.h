@@ -84,7 +84,7 @@ constexpr int TC2_BM = 256;
 // Arguments of the weight-gradient kernel (passed by value).
 struct WgradArgs {
     const int32_t* group_sizes;  // device [G]
-    float* dw;                   // device [G, K, N]
+    void* dw;                    // device [G, K, N], fp32 or bf16
     uint8_t* maps;               // device workspace: per group, the lhs then the dy tensor map
                                  // with the row extent cut at the group's end (128 B each)
     int M, K, N, G;
@@ -93,9 +93,9 @@ struct WgradArgs {
     uint64_t timeout_ns;
 };
 
-// bf16 lhs [M,K] and dy [M,N], fp32 dw [G,K,N], tcgen05 (wgrad_tc.cu). Both operand maps 2-D
-// with a (64, 64) box, 128-byte swizzled; the dw map 3-D (N, K, G) fp32 with a (32, 32, 1) box,
-// 128-byte swizzled (the epilogue stores through it).
+// bf16 lhs [M,K] and dy [M,N], fp32 or bf16 dw [G,K,N], tcgen05 (wgrad_tc.cu). Both operand maps
+// 2-D with a (64, 64) box, 128-byte swizzled; the dw map 3-D (N, K, G), 128-byte swizzled, with a
+// (32, 32, 1) box for fp32 or (64, 32, 1) for bf16 (out_bf16; the epilogue stores through it).
 // Writes a.maps: for each group g, copies of tmap_x and tmap_dy whose row extent is the group's
 // end offset, so that a box reaching past the group reads zeros (wgrad_tc.cu). Runs before either
 // grad-weight kernel on the same stream.
@@ -107,7 +107,7 @@ constexpr int WG_ROWS = 64;        // wgrad_tc.cu
 constexpr int WG2_ROWS = 128;      // wgrad_tc2.cu
 
 cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
-                            const WgradArgs& a, int bn, int grid, cudaStream_t stream);
+                            const WgradArgs& a, int bn, bool out_bf16, int grid, cudaStream_t stream);
 
 // MXFP8 forward (mxfp8_tc.cu): 128 x BN tiles (BN = 128 or 256), K stages of 128 E4M3 bytes
 // (4 scale blocks).
@@ -143,8 +143,7 @@ cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, c
 
 // CTA-pair grad-weight (wgrad_tc2.cu): 256 x 256 tiles of dw[g]; a.KT counts 256-wide K tiles.
 cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
-                             const WgradArgs& a, int grid,
-                             cudaStream_t stream);
+                             const WgradArgs& a, bool out_bf16, int grid, cudaStream_t stream);
 int wgrad_tc2_max_clusters(int G);
 
 // The scale reorder alone (mxfp8_tc.cu), and the CTA-pair MXFP8 GEMM (mxfp8_tc2.cu): 256 x 256

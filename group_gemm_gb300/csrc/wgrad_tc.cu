@@ -18,6 +18,7 @@
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "pdl.cuh"
+#include "wg_store.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(1024) wg_maps_kernel(const __grid_constant__ C
     tensormap_release_gpu();
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool OUT_BF16>
 __global__ void __launch_bounds__(THREADS, 1)
     wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_dy,
                     const __grid_constant__ CUtensorMap tmap_dw, WgradArgs a) {
@@ -277,22 +278,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t z[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) z[j] = 0u;
-                for (int col = n0; col < min(a.N, n0 + BN); col += 32)
-                    tma_store_block_f32(z, tile, &tmap_dw, col, k0, t.g);
+                if constexpr (OUT_BF16) {
+                    for (int col = n0; col < min(a.N, n0 + BN); col += 64)
+                        tma_store_block_bf16(z, z, tile, &tmap_dw, col, k0, t.g);
+                } else {
+                    for (int col = n0; col < min(a.N, n0 + BN); col += 32)
+                        tma_store_block_f32(z, tile, &tmap_dw, col, k0, t.g);
+                }
                 continue;
             }
             const bool ready = mbar_wait_warp(&tfull[acc], acc_phase, guard);
             if (!ready) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            if constexpr (OUT_BF16) {
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int col = n0 + c * 32;
-                if (col >= a.N) break;
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, v);
-                tmem_ld_wait();
-                tma_store_block_f32(v, tile, &tmap_dw, col, k0, t.g);
+                for (int c = 0; c < BN / 64; ++c) {
+                    const int col = n0 + c * 64;
+                    if (col >= a.N) break;
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(tbase + c * 64, v0);
+                    tmem_ld_32x32b_x32(tbase + c * 64 + 32, v1);
+                    tmem_ld_wait();
+                    tma_store_block_bf16(v0, v1, tile, &tmap_dw, col, k0, t.g);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int col = n0 + c * 32;
+                    if (col >= a.N) break;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    tma_store_block_f32(v, tile, &tmap_dw, col, k0, t.g);
+                }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -315,10 +334,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <int BN, int STAGES>
 cudaError_t launch_wg(const CUtensorMap& tx, const CUtensorMap& tdy, const CUtensorMap& tdw, const WgradArgs& a,
-                      int grid, cudaStream_t stream) {
+                      bool out_bf16, int grid, cudaStream_t stream) {
     using L = WgLayout<BN, STAGES>;
     const size_t shm = L::smem_bytes(a.G);
-    auto kern = wgrad_tc_kernel<BN, STAGES>;
+    auto kern = out_bf16 ? wgrad_tc_kernel<BN, STAGES, true> : wgrad_tc_kernel<BN, STAGES, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(THREADS), shm, stream, tx, tdy, tdw, a);
@@ -333,9 +352,9 @@ cudaError_t launch_wg_maps(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy
 }
 
 cudaError_t launch_wgrad_tc(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
-                            const WgradArgs& a, int bn, int grid, cudaStream_t stream) {
-    if (bn == 256) return launch_wg<256, 4>(tmap_x, tmap_dy, tmap_dw, a, grid, stream);
-    if (bn == 128) return launch_wg<128, 6>(tmap_x, tmap_dy, tmap_dw, a, grid, stream);
+                            const WgradArgs& a, int bn, bool out_bf16, int grid, cudaStream_t stream) {
+    if (bn == 256) return launch_wg<256, 4>(tmap_x, tmap_dy, tmap_dw, a, out_bf16, grid, stream);
+    if (bn == 128) return launch_wg<128, 6>(tmap_x, tmap_dy, tmap_dw, a, out_bf16, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -20,6 +20,7 @@
 #include "kernels.h"
 #include "pairdrain.cuh"
 #include "pdl.cuh"
+#include "wg_store.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -64,6 +65,7 @@ __device__ __forceinline__ PairTile decode(int w, int KT, int NT, const int32_t*
     return t;
 }
 
+template <bool OUT_BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     wgrad_tc2_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_dy,
                      const __grid_constant__ CUtensorMap tmap_dw,
@@ -255,8 +257,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     uint32_t z[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) z[j] = 0u;
-                    for (int col = n0; col < min(a.N, n0 + BN); col += 32)
-                        tma_store_block_f32(z, tile, &tmap_dw, col, k0, t.g);
+                    if constexpr (OUT_BF16) {
+                        for (int col = n0; col < min(a.N, n0 + BN); col += 64)
+                            tma_store_block_bf16(z, z, tile, &tmap_dw, col, k0, t.g);
+                    } else {
+                        for (int col = n0; col < min(a.N, n0 + BN); col += 32)
+                            tma_store_block_f32(z, tile, &tmap_dw, col, k0, t.g);
+                    }
                 }
                 continue;
             }
@@ -265,14 +272,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
             if (k0 < a.K) {
+                if constexpr (OUT_BF16) {
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    const int col = n0 + c * 32;
-                    if (col >= a.N) break;
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, v);
-                    tmem_ld_wait();
-                    tma_store_block_f32(v, tile, &tmap_dw, col, k0, t.g);
+                    for (int c = 0; c < BN / 64; ++c) {
+                        const int col = n0 + c * 64;
+                        if (col >= a.N) break;
+                        uint32_t v0[32], v1[32];
+                        tmem_ld_32x32b_x32(tbase + c * 64, v0);
+                        tmem_ld_32x32b_x32(tbase + c * 64 + 32, v1);
+                        tmem_ld_wait();
+                        tma_store_block_bf16(v0, v1, tile, &tmap_dw, col, k0, t.g);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        const int col = n0 + c * 32;
+                        if (col >= a.N) break;
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(tbase + c * 32, v);
+                        tmem_ld_wait();
+                        tma_store_block_f32(v, tile, &tmap_dw, col, k0, t.g);
+                    }
                 }
             }
             tc_fence_before();
@@ -296,14 +316,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }  // namespace
 
 cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
-                             const WgradArgs& a, int grid,
-                             cudaStream_t stream) {
+                             const WgradArgs& a, bool out_bf16, int grid, cudaStream_t stream) {
     if (grid % 2) return cudaErrorInvalidValue;
     const size_t shm = smem_bytes(a.G);
-    cudaError_t e =
-        cudaFuncSetAttribute(wgrad_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
+    auto kern = out_bf16 ? wgrad_tc2_kernel<true> : wgrad_tc2_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    return launch_pdl(wgrad_tc2_kernel, dim3(grid), dim3(THREADS), shm, stream, tmap_x, tmap_dy, tmap_dw, a);
+    return launch_pdl(kern, dim3(grid), dim3(THREADS), shm, stream, tmap_x, tmap_dy, tmap_dw, a);
 }
 
 int wgrad_tc2_max_clusters(int G) {
@@ -319,9 +338,9 @@ int wgrad_tc2_max_clusters(int G) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    cudaError_t e = cudaFuncSetAttribute(wgrad_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(wgrad_tc2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(cfg.dynamicSmemBytes));
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, wgrad_tc2_kernel, &cfg);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, wgrad_tc2_kernel<false>, &cfg);
     return e == cudaSuccess ? n : 0;
 }
 

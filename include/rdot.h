@@ -189,11 +189,13 @@ RDOT_API rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const
  * "Contracting"; Part 4 Table 7, class wgrad_wi).
  *   lhs  device bf16 [M, K]
  *   dy   device bf16 [M, N]
- *   dw   device fp32 [G, K, N]: dw[g] = sum over rows i of group g of lhs[i,:]^T dy[i,:];
- *        every group's slab is written (zeros for an empty group). Rows at or past the last
- *        end offset are never read into the result. */
+ *   dw   device [G, K, N] of the plan's out_dtype: fp32, or bf16 (each fp32 sum rounded to
+ *        nearest even once, the output type of Part 4's wgrad_wi example,
+ *        preferred_element_type=bfloat16): dw[g] = sum over rows i of group g of
+ *        lhs[i,:]^T dy[i,:]; every group's slab is written (zeros for an empty group). Rows at
+ *        or past the last end offset are never read into the result. */
 RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy,
-                             const int32_t* group_sizes, float* dw, void* workspace,
+                             const int32_t* group_sizes, void* dw, void* workspace,
                              void* stream);
 
 /* Weight gradient on MXFP8 operands (Part 4 Table 7, wgrad_wi, in the number format of AITER PR

@@ -7,6 +7,7 @@ import torch
 import group_gemm_gb300 as gg
 import oracle
 import rdot_inputs as ri
+from tests._metrics import COSINE_MIN, cosine_to_rounded
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -91,21 +92,39 @@ WG_CASES = [
 
 @pytest.mark.parametrize("flags", [gg.RDOT_FLAG_NO_CTA_PAIR, gg.RDOT_FLAG_CTA_PAIR])
 @pytest.mark.parametrize("m,k,n,gs", WG_CASES)
-def test_grad_weight_matches_oracle(m, k, n, gs, flags):
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_grad_weight_matches_oracle(m, k, n, gs, flags, out_dtype):
+    """fp32 dw, and bf16 dw (each fp32 sum rounded once; the output type of the wgrad_wi
+    example in "Group-GEMM in XLA", Part 4): 64-column staging rows, column tails at N."""
     gs = np.asarray(gs, np.int32)
     lhs = torch.from_numpy(ri.host_normal((m, k), 81)).to(torch.bfloat16)
     dy = torch.from_numpy(ri.host_normal((m, n), 82)).to(torch.bfloat16)
     total = int(gs.sum())
     lhs[total:] = float("nan")                       # rows past the sum must never be read
     dy[total:] = float("inf")
-    plan = gg.Plan(m, k, n, gs.size, "grad_weight", "bf16", "f32", flags=flags)
-    dw = torch.full((gs.size, k, n), float("nan"), dtype=torch.float32, device=DEV)
+    names = {torch.float32: "f32", torch.bfloat16: "bf16"}
+    plan = gg.Plan(m, k, n, gs.size, "grad_weight", "bf16", names[out_dtype], flags=flags)
+    dw = torch.full((gs.size, k, n), float("nan"), dtype=out_dtype, device=DEV)
     gg.rdot_grad_weight(plan.handle, lhs.to(DEV), dy.to(DEV), torch.from_numpy(gs).to(DEV), dw, plan.workspace)
     assert plan.status() == 0
     ref = oracle.grad_weight(lhs, dy, gs)
     assert rel_err(dw, ref) <= TOL
+    if out_dtype == torch.bfloat16:
+        assert cosine_to_rounded(dw, ref, out_dtype) >= COSINE_MIN
     for g in np.nonzero(gs == 0)[0]:
         assert torch.all(dw[g] == 0)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_grad_weight_without_rows_writes_zero_slabs(out_dtype):
+    names = {torch.float32: "f32", torch.bfloat16: "bf16"}
+    plan = gg.Plan(0, 64, 128, 3, "grad_weight", "bf16", names[out_dtype])
+    dw = torch.full((3, 64, 128), float("nan"), dtype=out_dtype, device=DEV)
+    x = torch.zeros((1, 64), dtype=torch.bfloat16, device=DEV)
+    y = torch.zeros((1, 128), dtype=torch.bfloat16, device=DEV)
+    gg.rdot_grad_weight(plan.handle, x, y, torch.zeros(3, dtype=torch.int32, device=DEV), dw, plan.workspace)
+    torch.cuda.synchronize()
+    assert torch.all(dw == 0)
 
 
 @pytest.mark.parametrize("flags", [gg.RDOT_FLAG_NO_CTA_PAIR, gg.RDOT_FLAG_CTA_PAIR])
@@ -144,15 +163,17 @@ def test_grad_weight_max_groups(flags):
 
 
 @pytest.mark.parametrize("flags", [gg.RDOT_FLAG_NO_CTA_PAIR, gg.RDOT_FLAG_CTA_PAIR])
-def test_grad_weight_cuda_graph_replay_with_new_sizes(flags):
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_grad_weight_cuda_graph_replay_with_new_sizes(flags, out_dtype):
     """A call is two launches (the per-group tensor maps, then the GEMM); both live on the device
     side, so a captured graph replays correctly when only the group sizes change."""
     m, k, n, g = 900, 256, 384, 4
     lhs = torch.from_numpy(ri.host_normal((m, k), 95)).to(torch.bfloat16).to(DEV)
     dy = torch.from_numpy(ri.host_normal((m, n), 96)).to(torch.bfloat16).to(DEV)
-    plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", flags=flags)
+    plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", {torch.float32: "f32", torch.bfloat16: "bf16"}[out_dtype],
+                   flags=flags)
     gs_d = torch.tensor([300, 200, 0, 300], dtype=torch.int32, device=DEV)
-    dw = torch.empty((g, k, n), dtype=torch.float32, device=DEV)
+    dw = torch.empty((g, k, n), dtype=out_dtype, device=DEV)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         gg.rdot_grad_weight(plan.handle, lhs, dy, gs_d, dw, plan.workspace, s)   # encodes tensor maps
