@@ -890,7 +890,13 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                           "hbm_gbs_algorithmic": round(min_bytes / t5 / 1e9, 1),
                           "frac_of_hbm": round(min_bytes / t5 / 1e9 / peaks["hbm_gbs"], 4),
                           "status": wplan.status(), "tile": f"{wplan.info['tile_m']}x{wplan.info['tile_n']}"}
-    del aq, as_, dq, dsc, dw
+    dwh = torch.empty((g, k, n), dtype=torch.bfloat16, device=dev)
+    hplan = gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", "bf16", device=dev.index)
+    t6 = _time_steps(lambda: gg.rdot_grad_weight_mxfp8(hplan.handle, aq, as_, dq, dsc, gs_d, dwh, hplan.workspace,
+                                                       stream), steps, stream)
+    res["mxfp8_wgrad"]["dw_bf16"] = {"tflops": round(fl / t6 / 1e12, 3), "ms": round(t6 * 1e3, 4),
+                                     "frac_of_fp8_peak": round(fl / t6 / 1e12 / fp8_peak, 4), "status": hplan.status()}
+    del aq, as_, dq, dsc, dw, dwh
     torch.cuda.empty_cache()
     return res
 

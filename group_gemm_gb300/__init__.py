@@ -483,20 +483,23 @@ def ragged_dot_gated(lhs, w0, w1, group_sizes, out_dtype=None, out=None, stream=
     return out
 
 
-def grad_weight_mxfp8(lhs_q, lhs_s, dy_q, dy_s, group_sizes, out=None, stream=None):
-    """MXFP8 weight gradient: ``dw [G, K, N]`` fp32 from E4M3 codes with E8M0 scales along the rows
-    in blocks of 32 that start at each group's first row (scale tensors ``[M // 32 + G, K | N]``)."""
+def grad_weight_mxfp8(lhs_q, lhs_s, dy_q, dy_s, group_sizes, out=None, stream=None, out_dtype=None):
+    """MXFP8 weight gradient: ``dw [G, K, N]`` (fp32 by default, or bf16) from E4M3 codes with E8M0
+    scales along the rows in blocks of 32 that start at each group's first row (scale tensors
+    ``[M // 32 + G, K | N]``)."""
     import torch
     m, k = lhs_q.shape
     n = dy_q.shape[1]
     g = group_sizes.shape[0]
+    out_dtype = out_dtype or (out.dtype if out is not None else torch.float32)
+    names = {torch.bfloat16: "bf16", torch.float32: "f32"}
     s = _run_stream(stream, lhs_q.device)
-    key = ("wgrad_mxfp8", m, k, n, g, lhs_q.device)
+    key = ("wgrad_mxfp8", m, k, n, g, out_dtype, lhs_q.device)
     plan, ws = _cached_plan(key, s, m=m, k=k, n=n, groups=g, mode="grad_weight_mxfp8", in_dtype="e4m3",
-                            out_dtype="f32", device=lhs_q.device)
+                            out_dtype=names[out_dtype], device=lhs_q.device)
     with torch.cuda.stream(s):
         if out is None:
-            out = torch.empty((g, k, n), dtype=torch.float32, device=lhs_q.device)
+            out = torch.empty((g, k, n), dtype=out_dtype, device=lhs_q.device)
         rdot_grad_weight_mxfp8(plan.handle, lhs_q.contiguous(), lhs_s.contiguous(), dy_q.contiguous(),
                                dy_s.contiguous(), group_sizes.to(torch.int32).contiguous(), out, ws, s)
     return out

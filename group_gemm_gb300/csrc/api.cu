@@ -245,7 +245,8 @@ rdot_status check_problem(const rdot_problem* p) {
             if (p->k % 8 || p->n % 8) return RDOT_ERR_UNSUPPORTED;
             return RDOT_OK;
         case RDOT_MODE_GRAD_WEIGHT_MXFP8:
-            if (p->in_dtype != RDOT_E4M3 || p->out_dtype != RDOT_F32) return RDOT_ERR_UNSUPPORTED;
+            if (p->in_dtype != RDOT_E4M3 || (p->out_dtype != RDOT_F32 && p->out_dtype != RDOT_BF16))
+                return RDOT_ERR_UNSUPPORTED;
             if (p->k % 16 || p->n % 16 || p->tile_n != 0 || (p->flags & RDOT_FLAG_CTA_PAIR)) return RDOT_ERR_UNSUPPORTED;
             return RDOT_OK;
         case RDOT_MODE_GRAD_INPUT_MXFP8:
@@ -1019,7 +1020,7 @@ rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const void* dy, 
 }
 
 rdot_status rdot_grad_weight_mxfp8(rdot_plan_t plan, const void* lhs_q, const uint8_t* lhs_s, const void* dy_q,
-                                   const uint8_t* dy_s, const int32_t* group_sizes, float* dw, void* workspace,
+                                   const uint8_t* dy_s, const int32_t* group_sizes, void* dw, void* workspace,
                                    void* stream) {
     if (!plan || !group_sizes || !workspace || !dw) return RDOT_ERR_INVALID_ARG;
     const rdot_problem& p = plan->p;
@@ -1032,7 +1033,8 @@ rdot_status rdot_grad_weight_mxfp8(rdot_plan_t plan, const void* lhs_q, const ui
     if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (p.m == 0) {
-        cudaError_t e = cudaMemsetAsync(dw, 0, sizeof(float) * p.groups * p.k * p.n, s);
+        const size_t esz = p.out_dtype == RDOT_BF16 ? 2 : 4;
+        cudaError_t e = cudaMemsetAsync(dw, 0, esz * p.groups * p.k * p.n, s);
         return e == cudaSuccess ? RDOT_OK : cuda_fail(e, "cudaMemsetAsync");
     }
     // codes: rows of K (or N) bytes, boxes of 128 columns x 128 rows
@@ -1046,9 +1048,12 @@ rdot_status rdot_grad_weight_mxfp8(rdot_plan_t plan, const void* lhs_q, const ui
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = dy_q;
     }
+    const bool out_bf16 = p.out_dtype == RDOT_BF16;
     if (plan->map_out_ptr != dw) {
-        rdot_status st = encode_3d(&plan->map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dw, p.n, p.k, p.groups, p.n * 4,
-                                   p.k * p.n * 4, 32, 32, 1);
+        rdot_status st = out_bf16 ? encode_3d(&plan->map_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dw, p.n, p.k,
+                                              p.groups, p.n * 2, p.k * p.n * 2, 64, 32, 1)
+                                  : encode_3d(&plan->map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dw, p.n, p.k,
+                                              p.groups, p.n * 4, p.k * p.n * 4, 32, 32, 1);
         if (st != RDOT_OK) return st;
         plan->map_out_ptr = dw;
     }
@@ -1075,7 +1080,8 @@ rdot_status rdot_grad_weight_mxfp8(rdot_plan_t plan, const void* lhs_q, const ui
     wa.G = a.G;
     cudaError_t e = launch_wg_maps(plan->map_a, plan->map_b, wa, s);
     if (e != cudaSuccess) return cuda_fail(e, "mxfp8 wgrad group maps launch");
-    e = launch_mxw(plan->map_a, plan->map_b, plan->map_out, lhs_s, dy_s, a, plan->grid, 4 * plan->sm_count, s);
+    e = launch_mxw(plan->map_a, plan->map_b, plan->map_out, lhs_s, dy_s, a, out_bf16, plan->grid, 4 * plan->sm_count,
+                   s);
     if (e != cudaSuccess) return cuda_fail(e, "mxfp8 wgrad launch");
     return RDOT_OK;
 }

@@ -168,7 +168,7 @@ cudaError_t launch_moe_combine(const void* y_sorted, const int32_t* inv, const f
 
 // MXFP8 weight gradient (mxw_tc.cu): E4M3 lhs_q [M, K] and dy_q [M, N] with E8M0 scales along the
 // rows, lhs_s [M/32 + G, K] and dy_s [M/32 + G, N], in blocks of 32 rows from each group's start;
-// fp32 dw [G, K, N]; 128 x 128 tiles on single CTAs.
+// fp32 or bf16 dw [G, K, N]; 128 x 128 tiles on single CTAs.
 struct MxwArgs {
     const int32_t* group_sizes;  // device [G]
     uint8_t* maps;               // workspace: the per-group cut maps of lhs_q and dy_q (launch_wg_maps)
@@ -184,8 +184,8 @@ size_t mxw_scale_block_bytes(long long M, int G, long long K, long long N);
 // tmap_x / tmap_dy: the code tensors as 2-D uint8 maps with a (128, 128) box, 128-byte swizzled;
 // tmap_dw as for the bf16 weight gradient. Launches the scale reorder, then the GEMM.
 cudaError_t launch_mxw(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
-                       const uint8_t* lhs_s, const uint8_t* dy_s, const MxwArgs& a, int grid, int prep_grid,
-                       cudaStream_t stream);
+                       const uint8_t* lhs_s, const uint8_t* dy_s, const MxwArgs& a, bool out_bf16, int grid,
+                       int prep_grid, cudaStream_t stream);
 
 // Router top-k (route.cu): logits [tokens, E] (fp32, or bf16 when bf16) -> ids / weights
 // [tokens, k]; E <= 1024, k <= min(32, E); mode 0 values, 1 softmax over all E, 2 softmax over k.

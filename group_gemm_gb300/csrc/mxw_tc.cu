@@ -35,6 +35,7 @@
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "pdl.cuh"
+#include "wg_store.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -153,6 +154,7 @@ __global__ void __launch_bounds__(256) mxw_prep_kernel(const uint8_t* __restrict
     }
 }
 
+template <bool OUT_BF16>
 __global__ void __launch_bounds__(THREADS, 1)
     mxw_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_dy,
                   const __grid_constant__ CUtensorMap tmap_dw, MxwArgs a) {
@@ -344,21 +346,39 @@ __global__ void __launch_bounds__(THREADS, 1)
                 uint32_t z[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) z[j] = 0u;
-                for (int col = n0; col < min(a.N, n0 + BN); col += 32)
-                    tma_store_block_f32(z, tile, &tmap_dw, col, k0, g);
+                if constexpr (OUT_BF16) {
+                    for (int col = n0; col < min(a.N, n0 + BN); col += 64)
+                        tma_store_block_bf16(z, z, tile, &tmap_dw, col, k0, g);
+                } else {
+                    for (int col = n0; col < min(a.N, n0 + BN); col += 32)
+                        tma_store_block_f32(z, tile, &tmap_dw, col, k0, g);
+                }
                 continue;
             }
             if (!mbar_wait_warp(&tfull[acc], acc_phase, guard)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+            if constexpr (OUT_BF16) {
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                const int col = n0 + c * 32;
-                if (col >= a.N) break;
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tbase + c * 32, v);
-                tmem_ld_wait();
-                tma_store_block_f32(v, tile, &tmap_dw, col, k0, g);
+                for (int c = 0; c < BN / 64; ++c) {
+                    const int col = n0 + c * 64;
+                    if (col >= a.N) break;
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(tbase + c * 64, v0);
+                    tmem_ld_32x32b_x32(tbase + c * 64 + 32, v1);
+                    tmem_ld_wait();
+                    tma_store_block_bf16(v0, v1, tile, &tmap_dw, col, k0, g);
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int col = n0 + c * 32;
+                    if (col >= a.N) break;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    tma_store_block_f32(v, tile, &tmap_dw, col, k0, g);
+                }
             }
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
@@ -385,15 +405,16 @@ size_t mxw_scale_block_bytes(long long M, int G, long long K, long long N) {
 }
 
 cudaError_t launch_mxw(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
-                       const uint8_t* lhs_s, const uint8_t* dy_s, const MxwArgs& a, int grid, int prep_grid,
-                       cudaStream_t stream) {
+                       const uint8_t* lhs_s, const uint8_t* dy_s, const MxwArgs& a, bool out_bf16, int grid,
+                       int prep_grid, cudaStream_t stream) {
     const size_t prep_shm = sizeof(int32_t) * 3 * (a.G + 1);
     cudaError_t e = launch_pdl(mxw_prep_kernel, dim3(prep_grid), dim3(256), prep_shm, stream, lhs_s, dy_s, a);
     if (e != cudaSuccess) return e;
     const size_t shm = smem_bytes(a.G);
-    e = cudaFuncSetAttribute(mxw_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
+    auto kern = out_bf16 ? mxw_tc_kernel<true> : mxw_tc_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;
-    return launch_pdl(mxw_tc_kernel, dim3(grid), dim3(THREADS), shm, stream, tmap_x, tmap_dy, tmap_dw, a);
+    return launch_pdl(kern, dim3(grid), dim3(THREADS), shm, stream, tmap_x, tmap_dy, tmap_dw, a);
 }
 
 }  // namespace rdot

@@ -203,7 +203,8 @@ RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const v
  *   dw[g] = A_g^T D_g,  A = dequant(lhs_q, lhs_s), D = dequant(dy_q, dy_s), fp32 accumulation
  *   lhs_q  device uint8 [M, K]   E4M3 codes;  lhs_s  device uint8 [M/32 + G, K]  E8M0 scales
  *   dy_q   device uint8 [M, N]   E4M3 codes;  dy_s   device uint8 [M/32 + G, N]  E8M0 scales
- *   dw     device fp32 [G, K, N]; every slab written (zeros for an empty group)
+ *   dw     device [G, K, N], fp32 or bf16 (the plan's out_dtype; bf16: each fp32 sum rounded to
+ *          nearest even once); every slab written (zeros for an empty group)
  * The contraction runs over each group's rows, so its scale blocks run along the rows. The pages
  * give no rule for a 32-row block at a group boundary; the reading taken: blocks start at each
  * group's first row (its last block may be shorter) and never mix two groups. Block b of group g
@@ -212,11 +213,11 @@ RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const v
  * decode(code[i, c]) * 2^(scale[bp[g] + (i - start[g]) / 32, c] - 127). M/32 + G rows (M/32
  * rounded down) hold the blocks of any sizes summing to at most M; rows past the used ones are
  * never read, nor are code rows past the last group. Plan: mode RDOT_MODE_GRAD_WEIGHT_MXFP8,
- * in_dtype RDOT_E4M3, out_dtype RDOT_F32, K % 16 == 0, N % 16 == 0 (16-byte code rows); workspace
+ * in_dtype RDOT_E4M3, out_dtype RDOT_F32 or RDOT_BF16, K % 16 == 0, N % 16 == 0 (16-byte code rows); workspace
  * rdot_workspace_size bytes, 256-byte aligned (the group maps and the reordered scale blocks). */
 RDOT_API rdot_status rdot_grad_weight_mxfp8(rdot_plan_t plan, const void* lhs_q, const uint8_t* lhs_s,
                                            const void* dy_q, const uint8_t* dy_s, const int32_t* group_sizes,
-                                           float* dw, void* workspace, void* stream);
+                                           void* dw, void* workspace, void* stream);
 
 /* Data gradient of the forward ("Group-GEMM in XLA", Part 4 Table 7, class dgrad_wi: lhs [M,N],
  * rhs [E,K,N], out [M,K], contracting lhs dimension 1 with rhs dimension 2).

@@ -73,9 +73,9 @@ def test_status_strings_and_version(lib):
     (dict(m=16, k=8, n=8, groups=1, mode=3, in_dtype=gg.RDOT_F32, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=12, n=8, groups=1, mode=3), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=8, n=12, groups=1, mode=3), gg.RDOT_ERR_UNSUPPORTED),
-    # the MXFP8 grad-weight: E4M3 in, fp32 out, 16-byte code rows, single-CTA tiles of its own
+    # the MXFP8 grad-weight: E4M3 in, fp32 or bf16 out, 16-byte code rows, single-CTA tiles of its own
     (dict(m=64, k=32, n=32, groups=2, mode=6, in_dtype=gg.RDOT_BF16, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
-    (dict(m=64, k=32, n=32, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_BF16), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=64, k=32, n=32, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_E4M3), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=64, k=24, n=32, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=64, k=32, n=40, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_F32), gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=64, k=32, n=32, groups=2, mode=6, in_dtype=gg.RDOT_E4M3, out_dtype=gg.RDOT_F32, tile_n=128),

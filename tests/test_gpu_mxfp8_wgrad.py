@@ -39,12 +39,13 @@ def make_case(m, k, n, gs, seed, vary=True):
     return aq, as_, dq, ds, gs
 
 
-def run(aq, as_, dq, ds, gs, plan=None):
+def run(aq, as_, dq, ds, gs, plan=None, out_dtype=torch.float32):
     m, k = aq.shape
     n = dq.shape[1]
     g = gs.size
-    plan = plan or gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", "f32")
-    dw = torch.full((g, k, n), float("nan"), dtype=torch.float32, device=DEV)
+    plan = plan or gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3",
+                           {torch.float32: "f32", torch.bfloat16: "bf16"}[out_dtype])
+    dw = torch.full((g, k, n), float("nan"), dtype=out_dtype, device=DEV)
     gg.rdot_grad_weight_mxfp8(plan.handle, aq.to(DEV), as_.to(DEV), dq.to(DEV), ds.to(DEV),
                               torch.from_numpy(gs).to(DEV), dw, plan.workspace)
     return dw, plan.status()
@@ -68,6 +69,23 @@ def test_mxfp8_grad_weight_matches_oracle(m, k, n, gs):
     assert torch.isfinite(dw).all()
     assert rel_err(dw, ref) <= TOL
     assert rel_err(dw, ref) <= 1e-4                   # exact products, fp32 sums
+
+
+@pytest.mark.parametrize("m,k,n,gs", [
+    (300, 256, 256, [1, 31, 32, 33, 100, 103]),
+    (420, 144, 96, [130, 0, 77, 200, 5]),             # 96 columns: a half-empty 64-column store
+])
+def test_mxfp8_grad_weight_bf16_out(m, k, n, gs):
+    """bf16 dw: the fp32 sums rounded once to nearest even (within bf16 rounding of the oracle)."""
+    aq, as_, dq, ds, gs = make_case(m, k, n, gs, 57 + m)
+    dw, status = run(aq, as_, dq, ds, gs, out_dtype=torch.bfloat16)
+    ref = oracle.grad_weight_mxfp8(aq, as_, dq, ds, gs)
+    assert status == 0
+    assert rel_err(dw, ref) <= TOL
+    rounded = torch.from_numpy(ref).to(torch.float32).to(torch.bfloat16)
+    assert rel_err(dw, rounded.to(torch.float64).numpy()) <= 2 ** -7   # one bf16 rounding at most apart
+    for g in np.nonzero(gs == 0)[0]:
+        assert torch.all(dw[g] == 0)
 
 
 def test_mxfp8_grad_weight_scale_tensors_off_word_alignment():
