@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(256, kMxPrepBlocksPerSm)
             // [G, N, K/32]; the atom's rows are read like the lhs rows (lane l gathers rows l,
             // l+32, l+64, l+96), 4 stages at a time
             const int g = ub / (a.NT128 * KSG);
+            if (off[g + 1] == off[g]) continue;   // no tile of an empty group reads its blocks
             const int r = ub - g * a.NT128 * KSG;
             const int nt = r / KSG;
             const int ks0 = 4 * (r - nt * KSG);
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(256, kMxPrepBlocksPerSm)
         const int gk = ub / NTG;
         const int nt0 = 4 * (ub - gk * NTG);
         const int g = gk / a.KS;
+        if (off[g + 1] == off[g]) continue;   // no tile of an empty group reads its blocks
         const int ks = gk - g * a.KS;
         const int avail = min(4, KB32 - 4 * ks);
         bool raw[4];   // per atom: this lane's words are rows kb 0..3 still to be transposed
