@@ -898,6 +898,41 @@ def extra_configs(args, dev, peaks, main_name, main_step_s):
                                      "frac_of_fp8_peak": round(fl / t6 / 1e12 / fp8_peak, 4), "status": hplan.status()}
     del aq, as_, dq, dsc, dw, dwh
     torch.cuda.empty_cache()
+    # MXFP8 forward at the MoE GEMM shape the AITER follow-ups time (E 32, N 2048, K 6144) with
+    # T rows routed top-1 (the pages give neither the top-k nor the rows per call); the weights
+    # of the routed experts stream once, so the figure is the fraction of the HBM copy peak
+    e_, n_, k_ = 32, 2048, 6144
+    wf = ri.device_normal((e_, k_, n_), 2, 0.02, dev, torch.float32)
+    wq, wsc = ri.quantize_mx_e4m3(wf, axis=1)
+    del wf
+    dec = {}
+    for tokens in (8, 64, 512, 2048):
+        gs = ri.routed_group_sizes(tokens, e_, 1, 1.0, seed=0)
+        m = int(gs.sum())
+        xf = ri.device_normal((m, k_), 1, 1.0, dev, torch.float32)
+        xq, xs = ri.quantize_mx_e4m3(xf, axis=1)
+        del xf
+        out = torch.empty((m, n_), dtype=torch.bfloat16, device=dev)
+        gs_d = torch.from_numpy(gs).to(dev)
+        nz = int(np.count_nonzero(gs))
+        wbytes = nz * k_ * n_ + nz * (k_ // 32) * n_ + m * (k_ + k_ // 32) + 2 * m * n_
+        plan = gg.Plan(m, k_, n_, e_, "forward_mxfp8", "e4m3", "bf16", device=dev.index)
+        t = _time_steps(lambda: gg.rdot_forward_mxfp8(plan.handle, xq, xs, wq, wsc, gs_d, out, plan.workspace,
+                                                      stream), 20, stream)
+        entry = {"rows": m, "experts_routed": nz, "ms": round(t * 1e3, 4),
+                 "frac_of_hbm": round(wbytes / t / 1e9 / peaks["hbm_gbs"], 4), "status": plan.status(),
+                 "tile": f"{plan.info['tile_m']}x{plan.info['tile_n']}"}
+        if plan.info["tile_m"] < 128:
+            rp = gg.Plan(m, k_, n_, e_, "forward_mxfp8", "e4m3", "bf16", flags=gg.RDOT_FLAG_NO_SKINNY,
+                         device=dev.index)
+            tr = _time_steps(lambda: gg.rdot_forward_mxfp8(rp.handle, xq, xs, wq, wsc, gs_d, out, rp.workspace,
+                                                           stream), 20, stream)
+            entry["ms_row_tiles"] = round(tr * 1e3, 4)
+        dec[f"T{tokens}"] = entry
+        del xq, xs, out
+    res["mxfp8_decode_e32_n2048_k6144"] = dec
+    del wq, wsc
+    torch.cuda.empty_cache()
     return res
 
 

@@ -180,6 +180,14 @@ bool want_skinny(const rdot_problem& p) {
     return p.tile_n == 0 && p.out_dtype == RDOT_BF16 && p.m <= kSkinnyMaxRows;
 }
 
+// The MXFP8 forward takes its swapped small-row kernel (mxfp8_skinny.cu) on the same rule.
+bool want_mx_skinny(const rdot_problem& p) {
+    if (p.mode != RDOT_MODE_FORWARD_MXFP8) return false;
+    if (p.flags & RDOT_FLAG_SKINNY) return true;
+    if (p.flags & (RDOT_FLAG_NO_SKINNY | RDOT_FLAG_CTA_PAIR)) return false;
+    return p.tile_n == 0 && p.m <= kSkinnyMaxRows;
+}
+
 // Token rows per tile of that kernel: 16 (a sixth stage of weights in flight) when, with the
 // rows spread evenly over min(M, G) groups, 16-row tiles still leave at most two work items per
 // SM; else 32 (half the token tiles re-reading each weight slab).
@@ -214,11 +222,15 @@ rdot_status check_problem(const rdot_problem* p) {
     if (p->flags & ~0x7F) return RDOT_ERR_INVALID_ARG;
     if ((p->flags & RDOT_FLAG_CTA_PAIR) && (p->flags & RDOT_FLAG_NO_CTA_PAIR)) return RDOT_ERR_INVALID_ARG;
     if ((p->flags & RDOT_FLAG_SKINNY) && (p->flags & RDOT_FLAG_NO_SKINNY)) return RDOT_ERR_INVALID_ARG;
-    // the swapped small-row kernel: the bf16 forward with the plan's own tile shape only
-    if ((p->flags & RDOT_FLAG_SKINNY) &&
-        (p->mode != RDOT_MODE_FORWARD || p->in_dtype != RDOT_BF16 || (p->flags & RDOT_FLAG_CTA_PAIR) ||
-         (p->tile_n != 0 && p->tile_n != 64 && p->tile_n != SKINNY_BN)))
-        return RDOT_ERR_UNSUPPORTED;
+    // the swapped small-row kernels: the bf16 forward (64- or 128-column items) and the MXFP8
+    // forward (128-column items), on single CTAs
+    if (p->flags & RDOT_FLAG_SKINNY) {
+        const bool bf16_fwd = p->mode == RDOT_MODE_FORWARD && p->in_dtype == RDOT_BF16;
+        const bool mx_fwd = p->mode == RDOT_MODE_FORWARD_MXFP8;
+        if ((!bf16_fwd && !mx_fwd) || (p->flags & RDOT_FLAG_CTA_PAIR) ||
+            (p->tile_n != 0 && p->tile_n != SKINNY_BN && !(bf16_fwd && p->tile_n == 64)))
+            return RDOT_ERR_UNSUPPORTED;
+    }
     if (p->tile_n != 0 && p->tile_n != 128 && p->tile_n != 256 && p->tile_n != 512 &&
         !(p->tile_n == 64 && (p->flags & RDOT_FLAG_SKINNY)))
         return RDOT_ERR_UNSUPPORTED;
@@ -471,6 +483,21 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
             return RDOT_ERR_UNSUPPORTED;
         }
         pl->kind = 3;
+        if (want_mx_skinny(p)) {
+            pl->skinny = true;
+            pl->tile_m = skinny_token_rows(p, pl->sm_count);   // token rows per tile (the MMA's N)
+            pl->tile_n = SKINNY_BN;                            // weight columns per tile (its M)
+            pl->m_inner = 1;
+            const int nt = static_cast<int>((p.n + SKINNY_BN - 1) / SKINNY_BN);
+            const long long bound = forward_tile_bound(p.m, p.groups, pl->tile_m, nt);
+            if (bound > 0x7fffffffLL || !mx_blocks_fit(p.m, p.k, p.n, p.groups, pl->tile_m)) {
+                delete pl;
+                return RDOT_ERR_UNSUPPORTED;
+            }
+            pl->grid = static_cast<int>(std::max<long long>(1, std::min<long long>(bound, pl->sm_count)));
+            *plan_out = pl;
+            return RDOT_OK;
+        }
         const bool want_pair = (p.flags & RDOT_FLAG_CTA_PAIR) != 0;
         if (want_pair && p.tile_n == 128) {
             delete pl;
@@ -567,7 +594,7 @@ MxLayout mx_layout(const rdot_problem& p, int bm, int bn) {
     l.ks = static_cast<int>((p.k + 127) / 128);
     l.nt = static_cast<int>((p.n + bn - 1) / bn);
     const size_t mtiles = static_cast<size_t>((p.m + bm - 1) / bm) + static_cast<size_t>(p.groups);
-    l.sfa_blocks = mtiles * l.ks * (bm / TC_BM);
+    l.sfa_blocks = mtiles * l.ks * (bm >= TC_BM ? bm / TC_BM : 1);   // token tiles of the swapped kernel: one
     l.sfb_blocks = static_cast<size_t>(p.groups) * l.nt * l.ks;
     l.sfa_off = kWorkspaceBytes;
     l.sfb_off = l.sfa_off + l.sfa_blocks * MX_SFA_BLOCK_BYTES;
@@ -901,13 +928,16 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
     if (!dg.ok) return cuda_fail(cudaGetLastError(), "cudaSetDevice");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (plan->map_lhs_ptr != lhs) {
-        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, lhs, p.k, p.m, p.k, 128, 128);
+        rdot_status st = encode_2d(&plan->map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, lhs, p.k, p.m, p.k, 128,
+                                   plan->skinny ? plan->tile_m : 128);
         if (st != RDOT_OK) return st;
         plan->map_lhs_ptr = lhs;
     }
+    // the swapped kernel takes its weights 256 K rows (two scale stages) a pipeline stage
+    const int mx_kstages = plan->skinny ? 2 : 1;
     if (plan->map_rhs_ptr != rhs) {
         rdot_status st = encode_3d(&plan->map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, rhs, p.n, p.k, p.groups, p.n,
-                                   p.k * p.n, 128, 128, 1);
+                                   p.k * p.n, 128, plan->skinny ? 128 * mx_kstages : 128, 1);
         if (st != RDOT_OK) return st;
         plan->map_rhs_ptr = rhs;
     }
@@ -931,8 +961,12 @@ rdot_status rdot_forward_mxfp8(rdot_plan_t plan, const void* lhs, const uint8_t*
     a.status = static_cast<int32_t*>(workspace);
     a.timeout_ns = plan->timeout_ns;
     a.pair = plan->pair ? 1 : 0;
+    a.sbm = plan->skinny ? plan->tile_m : 0;
     cudaError_t e;
-    if (plan->pair) {
+    if (plan->skinny) {
+        e = launch_mxfp8_skinny(plan->map_a, plan->map_b, lhs_scale, rhs_scale, group_sizes, a, plan->tile_m,
+                                mx_kstages, plan->grid, kMxPrepBlocksPerSm * plan->sm_count, s);
+    } else if (plan->pair) {
         // the pair kernel fetches the scale blocks by TMA (each CTA's copy completes on the even
         // CTA's barrier): 32-bit views of 512-byte (lhs) and 1 KB (rhs) blocks, one block a box
         if (plan->map_ws_ptr != workspace) {

@@ -129,6 +129,8 @@ struct MxArgs {
     int pair;                    // 1: 256-row tiles on CTA pairs (sfa blocks per 128-row half)
     int b_kmajor;                // 1: the data gradient -- B codes [G, N out, K] with K contiguous and
                                  // rhs_scale [G, N, K/32] (scales along K); 0: the forward
+    int sbm;                     // > 0: rows per lhs scale block's tile (the swapped small-row
+                                 // kernel's token tiles); 0: 128, or 256 on CTA pairs
     int32_t* status;
     uint64_t timeout_ns;
 };
@@ -140,6 +142,15 @@ constexpr int kMxPrepBlocksPerSm = 3;
 cudaError_t launch_mxfp8(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b, const uint8_t* lhs_scale,
                          const uint8_t* rhs_scale, const int32_t* group_sizes, const MxArgs& a, int grid,
                          int prep_grid, cudaStream_t stream);
+
+// MXFP8 forward for a few rows per group (mxfp8_skinny.cu): the swapped product, 128 weight
+// columns x tt (16 or 32) token rows per work item; a.BN = 128, a.sbm = tt, a.NT = ceil(N / 128).
+// tmap_x: lhs codes [M, K] uint8, box (128, tt); tmap_w: rhs codes [G, K, N] as (N, K, G), box
+// (128, 128 kstages, 1); kstages: 128-K scale stages per pipeline stage, 1 or 2. Launches the
+// scale reorder (token-tile blocks of tt rows), then the GEMM.
+cudaError_t launch_mxfp8_skinny(const CUtensorMap& tmap_x, const CUtensorMap& tmap_w, const uint8_t* lhs_scale,
+                                const uint8_t* rhs_scale, const int32_t* group_sizes, const MxArgs& a, int tt,
+                                int kstages, int grid, int prep_grid, cudaStream_t stream);
 
 // CTA-pair grad-weight (wgrad_tc2.cu): 256 x 256 tiles of dw[g]; a.KT counts 256-wide K tiles.
 cudaError_t launch_wgrad_tc2(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,

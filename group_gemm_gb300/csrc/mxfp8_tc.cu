@@ -83,8 +83,10 @@ __global__ void __launch_bounds__(256, kMxPrepBlocksPerSm)
     extern __shared__ int32_t table[];
     int32_t* off = table;
     int32_t* mt_prefix = table + a.G + 1;
-    // row tiles of the GEMM: 128 rows, or 256 rows on CTA pairs (two 128-row halves per tile)
-    const int SBM = a.pair ? 256 : BM;
+    // row tiles of the GEMM: 128 rows, or 256 rows on CTA pairs (two 128-row halves per tile), or
+    // the swapped kernel's token tiles (a block then also holds rows of the tiles after it, which
+    // land in tensor-memory columns that kernel's MMAs do not read)
+    const int SBM = a.sbm ? a.sbm : (a.pair ? 256 : BM);
     const int halves = a.pair ? 2 : 1;
     if (threadIdx.x < 32) (void)group_scan_warp(gs, a.G, a.M, SBM, 1, off, mt_prefix);
     __syncthreads();

@@ -86,16 +86,17 @@ typedef enum {
  * tensor-core-bound and weight-streaming tiles; this flag keeps plain group order. The order is
  * visible through rdot_debug_offsets_tilemap. */
 #define RDOT_FLAG_NATURAL_ORDER 0x10
-/* bf16 forward with few rows per group (decode): the swapped product out^T = rhs[g]^T lhs_g^T,
- * output columns on the MMA's M and tiles of 16 or 32 token rows on its N, so that more SMs
- * stream weights and each keeps more of them in flight. Used by default for bf16 output with
- * m <= 64 and tile_n 0 (unless RDOT_FLAG_CTA_PAIR); RDOT_FLAG_SKINNY forces it (bf16 or fp32
- * output, tile_n 0, 64 or 128, no CTA pairs; else RDOT_ERR_UNSUPPORTED) and RDOT_FLAG_NO_SKINNY
- * rules it out. rdot_forward_combine does not take such a plan. The plan then reports tile_m 16
- * or 32 (token rows: 16 when min(m, groups) groups of ceil(m / min(m, groups)) rows give at
- * most two 16-row work items of 128 columns per SM) and tile_n 64 or 128 (64 with 16-row
- * tiles when twice as many 64-column items cut the most weight bytes any SM streams by a
- * quarter), token tiles fastest. */
+/* Forwards with few rows per group (decode): the swapped product out^T = rhs[g]^T lhs_g^T, output
+ * columns on the MMA's M and tiles of 16 or 32 token rows on its N, so that more SMs stream
+ * weights and each keeps more of them in flight (bf16: fwd_skinny.cu; MXFP8: mxfp8_skinny.cu).
+ * Used by default when m <= 64, tile_n is 0 and RDOT_FLAG_CTA_PAIR is not set: for the bf16
+ * forward with bf16 output, and for the MXFP8 forward. RDOT_FLAG_SKINNY forces it (bf16 forward:
+ * bf16 or fp32 output, tile_n 0, 64 or 128; MXFP8 forward: tile_n 0 or 128; never with CTA pairs;
+ * else RDOT_ERR_UNSUPPORTED) and RDOT_FLAG_NO_SKINNY rules it out. rdot_forward_combine does not
+ * take such a plan. The plan then reports tile_m 16 or 32 (token rows: 16 when min(m, groups)
+ * groups of ceil(m / min(m, groups)) rows give at most two 16-row work items of 128 columns per
+ * SM) and tile_n 64 or 128 (64 only for the bf16 forward, with 16-row tiles, when twice as many
+ * 64-column items cut the most weight bytes any SM streams by a quarter), token tiles fastest. */
 #define RDOT_FLAG_SKINNY 0x20
 #define RDOT_FLAG_NO_SKINNY 0x40
 

@@ -58,6 +58,8 @@ def test_status_strings_and_version(lib):
     (dict(m=16, k=8, n=8, groups=1, in_dtype=gg.RDOT_BF16, tile_n=256, flags=gg.RDOT_FLAG_SKINNY),
      gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=8, n=8, groups=1, mode=3, flags=gg.RDOT_FLAG_SKINNY), gg.RDOT_ERR_UNSUPPORTED),
+    (dict(m=16, k=32, n=32, groups=1, mode=2, in_dtype=gg.RDOT_E4M3, tile_n=64, flags=gg.RDOT_FLAG_SKINNY),
+     gg.RDOT_ERR_UNSUPPORTED),
     (dict(m=16, k=8, n=8, groups=1, flags=gg.RDOT_FLAG_CTA_PAIR | gg.RDOT_FLAG_NO_CTA_PAIR), gg.RDOT_ERR_INVALID_ARG),
     (dict(m=16, k=8, n=8, groups=1, tile_n=96), gg.RDOT_ERR_UNSUPPORTED),
     # 512-column tiles exist for the bf16-out forward on CTA pairs only

@@ -46,8 +46,10 @@ def make_case(m, k, n, gs, seed, vary=("a", "b")):
     return aq, as_, bq, bs, np.asarray(gs, np.int32)
 
 
-# kernel variants: single CTA with 128- or 256-column tiles, and 256 x 256 tiles on CTA pairs
-VARIANTS = {"t128": (128, 0), "t256": (256, 0), "pair": (0, gg.RDOT_FLAG_CTA_PAIR)}
+# kernel variants: single CTA with 128- or 256-column tiles, 256 x 256 tiles on CTA pairs, and
+# the swapped small-row kernel (128 weight columns x 16 or 32 token rows)
+VARIANTS = {"t128": (128, 0), "t256": (256, 0), "pair": (0, gg.RDOT_FLAG_CTA_PAIR),
+            "skinny": (0, gg.RDOT_FLAG_SKINNY)}
 
 
 def run(aq, as_, bq, bs, gs, variant="t256"):
@@ -57,8 +59,10 @@ def run(aq, as_, bq, bs, gs, variant="t256"):
     plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16", tile_n=tile_n, flags=flags)
     if tile_n:
         assert plan.info["tile_n"] == tile_n
-    if flags:
+    if flags == gg.RDOT_FLAG_CTA_PAIR:
         assert plan.info["tile_m"] == 256 and plan.info["tile_n"] == 256
+    if flags == gg.RDOT_FLAG_SKINNY:
+        assert plan.info["tile_m"] in (16, 32) and plan.info["tile_n"] == 128
     ws = torch.zeros(gg.rdot_workspace_size(plan.handle), dtype=torch.uint8, device=DEV)
     out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
     gg.rdot_forward_mxfp8(plan.handle, aq.to(DEV), as_.to(DEV), bq.to(DEV), bs.to(DEV),
@@ -197,3 +201,69 @@ def test_mxfp8_dgrad_max_groups():
     out, status = run_dgrad(dq, ds, wq, ws, gs)
     assert status == 0
     assert rel_err(out, oracle.grad_input_mxfp8(dq, ds, wq, ws, gs)) <= TOL
+
+
+# ---------------------------------------------------------------- decode-sized rows (swapped)
+@pytest.mark.parametrize("m,k,n,gs", [
+    (8, 768, 512, [1, 0, 2, 0, 1, 3, 1, 0]),         # one token top-8-like: a few rows per expert
+    (40, 512, 256, [3, 0, 30, 7]),                    # 30 rows: two 16-row token tiles
+    (64, 1024, 400, [0, 58, 6]),                      # 58 rows: four token tiles; N = 400 (16-column tail)
+    (1, 6144, 2048, [0, 0, 1, 0]),                    # one row at the decode shape of AITER #5832
+])
+@pytest.mark.parametrize("vary", [("a", "b"), ()])
+def test_mxfp8_skinny_decode_parity(m, k, n, gs, vary):
+    """The swapped MXFP8 kernel, chosen by default for these row counts: token-tile scale blocks
+    of 16 or 32 rows, weight blocks per 128 columns, rows of the next group in a token tile."""
+    aq, as_, bq, bs, gs = make_case(m, k, n, gs, 23, vary)
+    total = int(gs.sum())
+    aq[total:] = 0x7F
+    g = gs.size
+    plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16")
+    assert plan.info["tile_m"] in (16, 32) and plan.info["tile_n"] == 128
+    ws = torch.zeros(gg.rdot_workspace_size(plan.handle), dtype=torch.uint8, device=DEV)
+    out = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV)
+    gg.rdot_forward_mxfp8(plan.handle, aq.to(DEV), as_.to(DEV), bq.to(DEV), bs.to(DEV),
+                          torch.from_numpy(gs).to(DEV), out, ws)
+    ref = oracle.forward_mxfp8(aq, as_, bq, bs, gs)
+    assert gg.rdot_read_status(plan.handle, ws) == 0
+    assert rel_err(out, ref) <= TOL
+    assert cosine_to_rounded(out, ref) >= COSINE_MIN
+    assert torch.all(out[total:] == 0)
+
+
+def test_mxfp8_skinny_choice_and_refusals():
+    assert gg.Plan(64, 4096, 1536, 128, "forward_mxfp8", "e4m3", "bf16").info["tile_m"] in (16, 32)
+    assert gg.Plan(65, 4096, 1536, 128, "forward_mxfp8", "e4m3", "bf16").info["tile_m"] == 128
+    assert gg.Plan(8, 4096, 1536, 128, "forward_mxfp8", "e4m3", "bf16",
+                   flags=gg.RDOT_FLAG_NO_SKINNY).info["tile_m"] == 128
+    assert gg.Plan(8, 4096, 1536, 128, "forward_mxfp8", "e4m3", "bf16", tile_n=256).info["tile_m"] == 128
+    for kw in (dict(tile_n=256), dict(tile_n=64), dict(flags_extra=gg.RDOT_FLAG_CTA_PAIR)):
+        with pytest.raises(RuntimeError):
+            gg.Plan(8, 4096, 1536, 128, "forward_mxfp8", "e4m3", "bf16", tile_n=kw.get("tile_n", 0),
+                    flags=gg.RDOT_FLAG_SKINNY | kw.get("flags_extra", 0))
+
+
+def test_mxfp8_skinny_cuda_graph_replay_with_new_sizes():
+    m, k, n, g = 24, 512, 384, 4
+    aq, as_, bq, bs, _ = make_case(m, k, n, [6] * g, 29)
+    aq, as_, bq, bs = aq.to(DEV), as_.to(DEV), bq.to(DEV), bs.to(DEV)
+    plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16")
+    assert plan.info["tile_m"] in (16, 32)
+    ws = torch.zeros(gg.rdot_workspace_size(plan.handle), dtype=torch.uint8, device=DEV)
+    gs_d = torch.tensor([6, 6, 6, 6], dtype=torch.int32, device=DEV)
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        gg.rdot_forward_mxfp8(plan.handle, aq, as_, bq, bs, gs_d, out, ws, s)
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        gg.rdot_forward_mxfp8(plan.handle, aq, as_, bq, bs, gs_d, out, ws, s)
+    for sizes in ([24, 0, 0, 0], [1, 2, 3, 4], [0, 17, 0, 7]):
+        gs_d.copy_(torch.tensor(sizes, dtype=torch.int32))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref = oracle.forward_mxfp8(aq.cpu(), as_.cpu(), bq.cpu(), bs.cpu(), np.array(sizes, np.int32))
+        assert rel_err(out, ref) <= TOL
+    assert gg.rdot_read_status(plan.handle, ws) == 0
