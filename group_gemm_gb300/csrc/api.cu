@@ -387,8 +387,9 @@ rdot_status rdot_plan(const rdot_problem* problem, int device, rdot_plan_t* plan
         }
         pl->kind = 7;
         pl->tile_m = 128;   // dw rows (lhs columns) per tile
-        pl->tile_n = 128;
-        const long long work = ((p.k + 127) / 128) * ((p.n + 127) / 128) * static_cast<long long>(p.groups);
+        pl->tile_n = p.out_dtype == RDOT_BF16 ? 256 : 128;   // 256: one accumulator read out as bf16
+        const long long work =
+            ((p.k + 127) / 128) * ((p.n + pl->tile_n - 1) / pl->tile_n) * static_cast<long long>(p.groups);
         // the scale reorder indexes 128-row chunks and their 512-byte blocks with 32-bit integers
         const long long chunk_bound = (p.m + 127) / 128 + p.groups;
         if (work > 0x7fffffffLL || chunk_bound * ((p.k + 127) / 128 + (p.n + 127) / 128) > 0x7fffffffLL) {
@@ -1114,8 +1115,8 @@ rdot_status rdot_grad_weight_mxfp8(rdot_plan_t plan, const void* lhs_q, const ui
     wa.G = a.G;
     cudaError_t e = launch_wg_maps(plan->map_a, plan->map_b, wa, s);
     if (e != cudaSuccess) return cuda_fail(e, "mxfp8 wgrad group maps launch");
-    e = launch_mxw(plan->map_a, plan->map_b, plan->map_out, lhs_s, dy_s, a, out_bf16, plan->grid, 4 * plan->sm_count,
-                   s);
+    e = launch_mxw(plan->map_a, plan->map_b, plan->map_out, lhs_s, dy_s, a, out_bf16, plan->tile_n == 256, plan->grid,
+                   4 * plan->sm_count, s);
     if (e != cudaSuccess) return cuda_fail(e, "mxfp8 wgrad launch");
     return RDOT_OK;
 }

@@ -194,9 +194,10 @@ struct MxwArgs {
 size_t mxw_scale_block_bytes(long long M, int G, long long K, long long N);
 // tmap_x / tmap_dy: the code tensors as 2-D uint8 maps with a (128, 128) box, 128-byte swizzled;
 // tmap_dw as for the bf16 weight gradient. Launches the scale reorder, then the GEMM.
+// wide_tiles: 128 x 256 tiles of dw (bf16 dw only; grid over G * KT * ceil(NT / 2) work items).
 cudaError_t launch_mxw(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
-                       const uint8_t* lhs_s, const uint8_t* dy_s, const MxwArgs& a, bool out_bf16, int grid,
-                       int prep_grid, cudaStream_t stream);
+                       const uint8_t* lhs_s, const uint8_t* dy_s, const MxwArgs& a, bool out_bf16, bool wide_tiles,
+                       int grid, int prep_grid, cudaStream_t stream);
 
 // Router top-k (route.cu): logits [tokens, E] (fp32, or bf16 when bf16) -> ids / weights
 // [tokens, k]; E <= 1024, k <= min(32, E); mode 0 values, 1 softmax over all E, 2 softmax over k.

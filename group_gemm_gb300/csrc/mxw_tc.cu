@@ -397,6 +397,262 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+
+// ---------------------------------------------------------------------- 128 x 256 tiles, bf16 dw
+// The same product on tiles twice as wide, for a bf16 dw: per 128-row stage 16 KB of lhs codes,
+// 32 KB of dy codes (two 128-column boxes) and three scale blocks feed four M = 128, N = 256
+// block-scaled MMAs, a quarter fewer operand bytes per flop than 128 x 128 tiles, whose feed from
+// L2 bounds them. One 256-column accumulator leaves tensor memory for three stages' scales only;
+// eight epilogue warps (two per lane quarter, one per 128-column half) read it out as packed bf16,
+// hand it back to the MMA warp and then store their 32 x 128 blocks with TMA, so the next tile's
+// MMAs overlap the stores.
+namespace wide {
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int BNW = 256;
+constexpr int STAGES = 3;
+constexpr int B_BOX = ROWS * 128;                      // one 128-column box of dy codes
+constexpr int B_BYTES = 2 * B_BOX;
+constexpr int STAGE_BYTES = ((A_BYTES + B_BYTES + 3 * SF_BYTES + 1023) / 1024) * 1024;
+constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+constexpr int EPI_BYTES = EPI_WARPS * 4096;            // one 32 x 64 bf16 staging tile per warp
+constexpr int BAR_BYTES = (2 * STAGES + 3) * 8;        // full, empty, tfull, tempty, drain
+constexpr int SF_COLS = 12;                            // per stage: 4 columns of lhs scales, 8 of dy
+constexpr int TMEM_SF_BASE = BNW;
+static_assert(TMEM_SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "tensor memory budget");
+
+size_t smem_bytes(int G) {
+    return 1024 + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES + sizeof(int32_t) * 2 * (G + 1);
+}
+}  // namespace wide
+
+__global__ void __launch_bounds__(wide::THREADS, 1)
+    mxw_tc_wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_dy,
+                       const __grid_constant__ CUtensorMap tmap_dw, MxwArgs a) {
+    constexpr int EPI_WARPS = wide::EPI_WARPS;
+    constexpr int BNW = wide::BNW;
+    constexpr int STAGES = wide::STAGES;
+    constexpr int B_BOX = wide::B_BOX;
+    constexpr int B_BYTES = wide::B_BYTES;
+    constexpr int STAGE_BYTES = wide::STAGE_BYTES;
+    constexpr int RING_BYTES = wide::RING_BYTES;
+    constexpr int EPI_BYTES = wide::EPI_BYTES;
+    constexpr int BAR_BYTES = wide::BAR_BYTES;
+    constexpr int SF_COLS = wide::SF_COLS;
+    constexpr int TMEM_SF_BASE = wide::TMEM_SF_BASE;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* epi_stage = smem + RING_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + RING_BYTES + EPI_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 1;
+    uint64_t* drain = tempty + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+    int32_t* off = reinterpret_cast<int32_t*>(smem + RING_BYTES + EPI_BYTES + BAR_BYTES + MISC_BYTES);
+    int32_t* cp = off + a.G + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(tempty, 32 * EPI_WARPS);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmap_x);
+        tma_prefetch_desc(&tmap_dy);
+        tma_prefetch_desc(&tmap_dw);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, TMEM_COLS);
+        tmem_relinquish();
+    }
+    grid_dependency_enter();   // group sizes, codes, cut maps and reordered scales come from earlier kernels
+    if (warp == 2) {
+        const int bad = group_scan_warp(a.group_sizes, a.G, a.M, ROWS, 1, off, cp);
+        if (bad && lane == 0 && blockIdx.x == 0 && a.status) atomicOr(a.status, bad);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *tmem_holder;
+    const int NTW = (a.NT + 1) / 2;   // 256-column tiles (a.NT counts 128-column scale tiles)
+    const int W = a.G * a.KT * NTW;
+    const WaitGuard guard{abort_flag, a.status, a.timeout_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
+                const int g = w / (a.KT * NTW);
+                const int rem = w - g * a.KT * NTW;
+                const int kt = rem / NTW, nt = rem - kt * NTW;
+                const int row0 = off[g], rows = off[g + 1] - off[g];
+                const int nchunks = (rows + ROWS - 1) / ROWS;
+                // the tile's second 128-column half lies past N when N has an odd number of them:
+                // its scale block does not exist and its codes arrive as zeros
+                const int halves = min(2, a.NT - 2 * nt);
+                const CUtensorMap* gmap_x = reinterpret_cast<const CUtensorMap*>(a.maps + (2 * g) * WG_MAP_BYTES);
+                const CUtensorMap* gmap_dy = reinterpret_cast<const CUtensorMap*>(a.maps + (2 * g + 1) * WG_MAP_BYTES);
+                const bool ragged = (rows % ROWS) != 0;
+                if (ragged) {
+                    tensormap_acquire_gpu(gmap_x);
+                    tensormap_acquire_gpu(gmap_dy);
+                    tma_prefetch_desc(gmap_x);
+                    tma_prefetch_desc(gmap_dy);
+                }
+                for (int c = 0; c < nchunks; ++c) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, guard)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    uint8_t* ssf = sb + B_BYTES;
+                    const int r0 = row0 + c * ROWS;
+                    const bool tail = ragged && c == nchunks - 1;
+                    const long long cg = cp[g] + c;
+                    const CUtensorMap* mx = tail ? gmap_x : &tmap_x;
+                    const CUtensorMap* mdy = tail ? gmap_dy : &tmap_dy;
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES + (1 + halves) * SF_BYTES);
+                    tma_load_2d(sa, mx, &full[stage], kt * BM, r0);
+                    tma_load_2d(sb, mdy, &full[stage], nt * BNW, r0);
+                    tma_load_2d(sb + B_BOX, mdy, &full[stage], nt * BNW + 128, r0);
+                    bulk_load(ssf, a.sfa + (cg * a.KT + kt) * SF_BYTES, SF_BYTES, &full[stage]);
+                    // the dy blocks of the tile's two halves are adjacent (chunk-major, then tile)
+                    bulk_load(ssf + SF_BYTES, a.sfb + (cg * a.NT + 2 * nt) * SF_BYTES, halves * SF_BYTES, &full[stage]);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                int dummy;
+                const WaitGuard dguard = drain_guard(guard, &dummy);
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s)) (void)mbar_wait(&full[s], (issued_phase >> s) & 1u, dguard);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; w < W && ok; w += gridDim.x) {
+                const int g = w / (a.KT * NTW);
+                const int nt = (w - g * a.KT * NTW) % NTW;
+                const int rows = off[g + 1] - off[g];
+                const int nchunks = (rows + ROWS - 1) / ROWS;
+                if (nchunks == 0) continue;                 // empty group: the epilogue writes zeros
+                const int halves = min(2, a.NT - 2 * nt);
+                if (!mbar_wait(tempty, acc_phase ^ 1, guard)) break;
+                tc_fence_after();
+                for (int c = 0; c < nchunks; ++c) {
+                    if (!mbar_wait(&full[stage], phase, guard)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t ssf = sb + B_BYTES;
+                    const uint32_t sfa_t = tmem_base + TMEM_SF_BASE + SF_COLS * stage;
+                    const uint32_t sfb_t = sfa_t + 4;
+                    tmem_cp_32x128b_warpx4(sfa_t, smem_desc_rows16(ssf));
+                    // a half past N keeps the columns of an older block: they only reach dw
+                    // columns past N, which the stores clip
+                    for (int h = 0; h < halves; ++h)
+                        tmem_cp_32x128b_warpx4(sfb_t + 4 * h, smem_desc_rows16(ssf + (1 + h) * SF_BYTES));
+                    const int valid = min(ROWS, rows - c * ROWS);
+                    const int ksteps = (valid + 31) / 32;
+#pragma unroll
+                    for (int j = 0; j < ROWS / 32; ++j) {
+                        if (j >= ksteps) break;
+                        // both operands MN-major: +32 rows of 128 bytes per K = 32 step; dy's two
+                        // 128-column boxes one box apart
+                        const uint64_t adesc = smem_desc_sw128(sa + j * 4096, A_BYTES, 1024);
+                        const uint64_t bdesc = smem_desc_sw128(sb + j * 4096, B_BOX, 1024);
+                        mma_mxf8(tmem_base, adesc, bdesc, idesc_mxf8(BM, BNW, true, true, j, j), sfa_t, sfb_t,
+                                 (c | j) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull);
+                acc_phase ^= 1;
+            }
+            mma_commit(drain);
+            int dummy;
+            const WaitGuard dguard = drain_guard(guard, &dummy);
+            (void)mbar_wait(drain, 0, dguard);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        // warp w: TMEM lane quarter w % 4 (32 dw rows) and one 128-column half of the tile
+        const int q = warp & 3;
+        const int half = (warp - 2) / 4;
+        uint8_t* tile = epi_stage + (warp - 2) * 4096;
+        uint32_t acc_phase = 0;
+        for (int w = blockIdx.x; w < W; w += gridDim.x) {
+            const int g = w / (a.KT * NTW);
+            const int rem = w - g * a.KT * NTW;
+            const int kt = rem / NTW, nt = rem - kt * NTW;
+            const int rows = off[g + 1] - off[g];
+            const int k0 = kt * BM + q * 32;
+            const int n0 = nt * BNW + half * 128;
+            if (rows <= 0) {
+                // empty group: its slab is zero, the tensor cores never ran for it
+                if (k0 < a.K) {
+                    uint32_t z[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) z[j] = 0u;
+                    for (int col = n0; col < min(a.N, n0 + 128); col += 64)
+                        tma_store_packed_bf16(z, z, tile, &tmap_dw, col, k0, g);
+                }
+                continue;
+            }
+            if (!mbar_wait_warp(tfull, acc_phase, guard)) break;
+            tc_fence_after();
+            uint32_t pk[4][16];
+            tmem_read_bf16_32x128(tmem_base + half * 128 + (static_cast<uint32_t>(q * 32) << 16), pk);
+            tc_fence_before();
+            mbar_arrive(tempty);                      // the MMA warp may start the next tile
+            acc_phase ^= 1;
+            if (k0 < a.K) {
+                if (n0 < a.N) tma_store_packed_bf16(pk[0], pk[1], tile, &tmap_dw, n0, k0, g);
+                if (n0 + 64 < a.N) tma_store_packed_bf16(pk[2], pk[3], tile, &tmap_dw, n0 + 64, k0, g);
+            }
+        }
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
 }  // namespace
 
 size_t mxw_scale_block_bytes(long long M, int G, long long K, long long N) {
@@ -405,12 +661,21 @@ size_t mxw_scale_block_bytes(long long M, int G, long long K, long long N) {
 }
 
 cudaError_t launch_mxw(const CUtensorMap& tmap_x, const CUtensorMap& tmap_dy, const CUtensorMap& tmap_dw,
-                       const uint8_t* lhs_s, const uint8_t* dy_s, const MxwArgs& a, bool out_bf16, int grid,
-                       int prep_grid, cudaStream_t stream) {
+                       const uint8_t* lhs_s, const uint8_t* dy_s, const MxwArgs& a, bool out_bf16, bool wide_tiles,
+                       int grid, int prep_grid, cudaStream_t stream) {
     const size_t prep_shm = sizeof(int32_t) * 3 * (a.G + 1);
     cudaError_t e = launch_pdl(mxw_prep_kernel, dim3(prep_grid), dim3(256), prep_shm, stream, lhs_s, dy_s, a);
     if (e != cudaSuccess) return e;
     const size_t shm = smem_bytes(a.G);
+    if (wide_tiles) {
+        if (!out_bf16) return cudaErrorInvalidValue;
+        const size_t wshm = wide::smem_bytes(a.G);
+        e = cudaFuncSetAttribute(mxw_tc_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(wshm));
+        if (e != cudaSuccess) return e;
+        return launch_pdl(mxw_tc_wide_kernel, dim3(grid), dim3(wide::THREADS), wshm, stream, tmap_x, tmap_dy,
+                          tmap_dw, a);
+    }
     auto kern = out_bf16 ? mxw_tc_kernel<true> : mxw_tc_kernel<false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(shm));
     if (e != cudaSuccess) return e;

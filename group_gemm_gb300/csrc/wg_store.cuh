@@ -51,4 +51,26 @@ __device__ __forceinline__ void tma_store_block_bf16(const uint32_t (&a)[32], co
     }
 }
 
+// As tma_store_block_bf16 for values already packed two bf16 per word: p0 holds columns 0..31
+// of row `lane`, p1 columns 32..63.
+__device__ __forceinline__ void tma_store_packed_bf16(const uint32_t (&p0)[16], const uint32_t (&p1)[16],
+                                                      uint8_t* tile, const CUtensorMap* map, int x, int y, int z) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
+    uint8_t* row = tile + lane * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const uint32_t(&src)[16] = u < 4 ? p0 : p1;
+        const int b = 4 * (u & 3);
+        *reinterpret_cast<uint4*>(row + ((u ^ (lane & 7)) << 4)) = make_uint4(src[b], src[b + 1], src[b + 2], src[b + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(map, tile, x, y, z);
+        bulk_commit_group();
+    }
+}
+
 }  // namespace rdot

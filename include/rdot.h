@@ -214,7 +214,8 @@ RDOT_API rdot_status rdot_grad_weight(rdot_plan_t plan, const void* lhs, const v
  * decode(code[i, c]) * 2^(scale[bp[g] + (i - start[g]) / 32, c] - 127). M/32 + G rows (M/32
  * rounded down) hold the blocks of any sizes summing to at most M; rows past the used ones are
  * never read, nor are code rows past the last group. Plan: mode RDOT_MODE_GRAD_WEIGHT_MXFP8,
- * in_dtype RDOT_E4M3, out_dtype RDOT_F32 or RDOT_BF16, K % 16 == 0, N % 16 == 0 (16-byte code rows); workspace
+ * in_dtype RDOT_E4M3, out_dtype RDOT_F32 (128 x 128 tiles) or RDOT_BF16 (128 x 256 tiles; the plan
+ * reports tile_n 256), K % 16 == 0, N % 16 == 0 (16-byte code rows); workspace
  * rdot_workspace_size bytes, 256-byte aligned (the group maps and the reordered scale blocks). */
 RDOT_API rdot_status rdot_grad_weight_mxfp8(rdot_plan_t plan, const void* lhs_q, const uint8_t* lhs_s,
                                            const void* dy_q, const uint8_t* dy_s, const int32_t* group_sizes,

@@ -73,11 +73,18 @@ def test_mxfp8_grad_weight_matches_oracle(m, k, n, gs):
 
 @pytest.mark.parametrize("m,k,n,gs", [
     (300, 256, 256, [1, 31, 32, 33, 100, 103]),
-    (420, 144, 96, [130, 0, 77, 200, 5]),             # 96 columns: a half-empty 64-column store
+    (420, 144, 96, [130, 0, 77, 200, 5]),             # 96 columns: one 256-wide tile, its second half past N
+    (700, 208, 384, [0, 127, 128, 129, 0, 300]),      # 384 columns: an odd number of 128-column halves
+    (1000, 512, 160, [513, 0, 0, 257, 1]),            # 160 columns: 32 valid columns in the second half
+    (256, 128, 512, [256]),                           # G = 1, whole chunks, two 256-wide tiles
 ])
 def test_mxfp8_grad_weight_bf16_out(m, k, n, gs):
-    """bf16 dw: the fp32 sums rounded once to nearest even (within bf16 rounding of the oracle)."""
+    """bf16 dw on 128 x 256 tiles (one accumulator read out as packed bf16 by eight warps): the
+    fp32 sums rounded once to nearest even (within bf16 rounding of the oracle)."""
     aq, as_, dq, ds, gs = make_case(m, k, n, gs, 57 + m)
+    total = int(gs.sum())
+    aq[total:] = 0x7F                                 # NaN codes past the sum must never leak
+    dq[total:] = 0x7F
     dw, status = run(aq, as_, dq, ds, gs, out_dtype=torch.bfloat16)
     ref = oracle.grad_weight_mxfp8(aq, as_, dq, ds, gs)
     assert status == 0
@@ -141,17 +148,18 @@ def test_mxfp8_grad_weight_max_groups_and_clamped_sizes():
     assert rel_err(dw2, oracle.grad_weight_mxfp8(aq, as_, dq, ds, bad)) <= 1e-4
 
 
-def test_mxfp8_grad_weight_cuda_graph_replay_with_new_sizes():
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_mxfp8_grad_weight_cuda_graph_replay_with_new_sizes(out_dtype):
     m, k, n, g = 512, 128, 128, 4
     x = torch.from_numpy(ri.host_normal((m, k), 45))
     dy = torch.from_numpy(ri.host_normal((m, n), 46))
-    plan = gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", "f32")
+    plan = gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", {torch.float32: "f32", torch.bfloat16: "bf16"}[out_dtype])
     sizes0 = np.array([128, 128, 128, 128], np.int32)
     aq0, as0 = ri.quantize_mx_e4m3_group_rows(x, sizes0)
     dq0, ds0 = ri.quantize_mx_e4m3_group_rows(dy, sizes0)
     bufs = [t.to(DEV) for t in (aq0, as0, dq0, ds0)]
     gs_d = torch.from_numpy(sizes0).to(DEV)
-    dw = torch.empty((g, k, n), dtype=torch.float32, device=DEV)
+    dw = torch.empty((g, k, n), dtype=out_dtype, device=DEV)
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         gg.rdot_grad_weight_mxfp8(plan.handle, *bufs, gs_d, dw, plan.workspace, s)
@@ -168,7 +176,7 @@ def test_mxfp8_grad_weight_cuda_graph_replay_with_new_sizes():
         gs_d.copy_(torch.from_numpy(sz))
         graph.replay()
         torch.cuda.synchronize()
-        assert rel_err(dw, oracle.grad_weight_mxfp8(aq, as_, dq, ds, sz)) <= 1e-4
+        assert rel_err(dw, oracle.grad_weight_mxfp8(aq, as_, dq, ds, sz)) <= (1e-4 if out_dtype == torch.float32 else TOL)
 
 
 def test_mxfp8_grad_weight_full_size_whole_output():

@@ -56,12 +56,28 @@ def _case(kind):
         dy, rhs = _bf16((m, n), 6), _bf16((g, k, n), 7, 0.05)
         out = torch.empty((m, k), dtype=torch.bfloat16, device=DEV)
         return plan, lambda: gg.rdot_grad_input(plan.handle, dy, rhs, gs, out, plan.workspace), out
-    if kind in ("wgrad_pair", "wgrad_single"):
-        flags = gg.RDOT_FLAG_CTA_PAIR if kind == "wgrad_pair" else gg.RDOT_FLAG_NO_CTA_PAIR
-        plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", flags=flags)
+    if kind in ("wgrad_pair", "wgrad_single", "wgrad_pair_bf16"):
+        flags = gg.RDOT_FLAG_NO_CTA_PAIR if kind == "wgrad_single" else gg.RDOT_FLAG_CTA_PAIR
+        odt = torch.bfloat16 if kind.endswith("bf16") else torch.float32
+        plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "bf16" if odt == torch.bfloat16 else "f32", flags=flags)
         lhs, dy = _bf16((m, k), 8), _bf16((m, n), 9)
-        out = torch.empty((g, k, n), dtype=torch.float32, device=DEV)
+        out = torch.empty((g, k, n), dtype=odt, device=DEV)
         return plan, lambda: gg.rdot_grad_weight(plan.handle, lhs, dy, gs, out, plan.workspace), out
+    if kind in ("skinny_bf16", "skinny_mxfp8"):
+        # decode-sized rows: the swapped small-row kernels
+        sgs = torch.tensor([20, 0, 28, 0], dtype=torch.int32, device=DEV)
+        ms = 48
+        out = torch.empty((ms, n), dtype=torch.bfloat16, device=DEV)
+        if kind == "skinny_bf16":
+            plan = gg.Plan(ms, k, n, g, "forward", "bf16", "bf16")
+            lhs, rhs = _bf16((ms, k), 16), _bf16((g, k, n), 17, 0.05)
+            call = lambda: gg.rdot_forward(plan.handle, lhs, rhs, sgs, out, plan.workspace)
+        else:
+            plan = gg.Plan(ms, k, n, g, "forward_mxfp8", "e4m3", "bf16")
+            (aq, as_), (bq, bs) = _mx((ms, k), 18, 1), _mx((g, k, n), 19, 1, 0.05)
+            call = lambda: gg.rdot_forward_mxfp8(plan.handle, aq, as_, bq, bs, sgs, out, plan.workspace)
+        assert plan.info["tile_m"] in (16, 32)
+        return plan, call, out
     if kind in ("mxfp8_single", "mxfp8_pair"):
         flags = gg.RDOT_FLAG_CTA_PAIR if kind == "mxfp8_pair" else 0
         plan = gg.Plan(m, k, n, g, "forward_mxfp8", "e4m3", "bf16", flags=flags)
@@ -73,19 +89,21 @@ def _case(kind):
         (dq, ds), (wq, ws) = _mx((m, n), 12, 1), _mx((g, k, n), 13, 2, 0.05)
         out = torch.empty((m, k), dtype=torch.bfloat16, device=DEV)
         return plan, lambda: gg.rdot_grad_input_mxfp8(plan.handle, dq, ds, wq, ws, gs, out, plan.workspace), out
-    if kind == "mxfp8_wgrad":
-        plan = gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", "f32")
+    if kind in ("mxfp8_wgrad", "mxfp8_wgrad_bf16"):
+        odt = torch.bfloat16 if kind.endswith("bf16") else torch.float32
+        plan = gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", "bf16" if odt == torch.bfloat16 else "f32")
         sizes = np.array(gs_list, np.int32)
         aq, as_ = ri.quantize_mx_e4m3_group_rows(torch.from_numpy(ri.host_normal((m, k), 14)), sizes)
         dq, ds = ri.quantize_mx_e4m3_group_rows(torch.from_numpy(ri.host_normal((m, n), 15)), sizes)
         aq, as_, dq, ds = aq.to(DEV), as_.to(DEV), dq.to(DEV), ds.to(DEV)
-        out = torch.empty((g, k, n), dtype=torch.float32, device=DEV)
+        out = torch.empty((g, k, n), dtype=odt, device=DEV)
         return plan, lambda: gg.rdot_grad_weight_mxfp8(plan.handle, aq, as_, dq, ds, gs, out, plan.workspace), out
     raise KeyError(kind)
 
 
 @pytest.mark.parametrize("kind", ["fwd_pair", "fwd_single", "fwd_wide", "gated", "dgrad_pair", "wgrad_pair",
-                                  "wgrad_single", "mxfp8_single", "mxfp8_pair", "mxfp8_dgrad", "mxfp8_wgrad"])
+                                  "wgrad_single", "wgrad_pair_bf16", "mxfp8_single", "mxfp8_pair", "mxfp8_dgrad",
+                                  "mxfp8_wgrad", "mxfp8_wgrad_bf16", "skinny_bf16", "skinny_mxfp8"])
 def test_stop_early_then_exact_result(kind):
     plan, call, out = _case(kind)
     call()
