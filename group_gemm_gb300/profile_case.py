@@ -35,6 +35,7 @@ def main():
     ap.add_argument("--groups", type=int, default=0, help="override the workload's expert count")
     ap.add_argument("--flags", type=lambda v: int(v, 0), default=0, help="rdot_problem.flags of the plan")
     ap.add_argument("--tile-n", type=int, default=0, help="rdot_problem.tile_n of the plan (0: the plan's choice)")
+    ap.add_argument("--out", choices=["f32", "bf16"], default="f32", help="dw type of the weight gradients")
     args = ap.parse_args()
 
     gg.build()
@@ -80,8 +81,8 @@ def main():
     elif args.kernel == "wgrad":
         lhs = ri.device_normal((m, k), 1, 1.0, dev, torch.bfloat16)
         dy = ri.device_normal((m, n), 2, 1.0, dev, torch.bfloat16)
-        dw = torch.empty((g, k, n), dtype=torch.float32, device=dev)
-        plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", "f32", flags=args.flags)
+        dw = torch.empty((g, k, n), dtype=torch.float32 if args.out == "f32" else torch.bfloat16, device=dev)
+        plan = gg.Plan(m, k, n, g, "grad_weight", "bf16", args.out, flags=args.flags)
 
         def run():
             gg.rdot_grad_weight(plan.handle, lhs, dy, gs_d, dw, plan.workspace, stream)
@@ -125,8 +126,8 @@ def main():
         dy = ri.device_normal((m, n), 2, 1.0, dev, torch.float32)
         dq, ds = ri.quantize_mx_e4m3_group_rows(dy, gs)
         del x, dy
-        dw = torch.empty((g, k, n), dtype=torch.float32, device=dev)
-        plan = gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", "f32", flags=args.flags)
+        dw = torch.empty((g, k, n), dtype=torch.float32 if args.out == "f32" else torch.bfloat16, device=dev)
+        plan = gg.Plan(m, k, n, g, "grad_weight_mxfp8", "e4m3", args.out, flags=args.flags)
 
         def run():
             gg.rdot_grad_weight_mxfp8(plan.handle, aq, as_, dq, ds, gs_d, dw, plan.workspace, stream)
