@@ -19,6 +19,7 @@
 // contiguous axes), which the 8-bit kinds support.
 //
 // Two kernels per call (after wg_maps_kernel has cut a copy of each code map at every group's end):
+// the scale reorder, then one of the two GEMM kernels.
 //   mxw_prep_kernel  reorders the caller's scales into one 512-byte block per (group, 128-row
 //                    chunk, 128 columns): 128 columns x 4 blocks of 32 rows, byte
 //                    16 (c % 32) + 4 (c / 32) + block, the layout tcgen05.cp .32x128b.warpx4 copies
@@ -32,6 +33,8 @@
 //                    hold group rows; warps 2..5 store the fp32 accumulator with TMA (two
 //                    accumulators, so the stores of one tile overlap the next tile's MMAs). An empty
 //                    group's slab is written as zeros.
+//   mxw_tc_wide_kernel  the same on 128 x 256 tiles for a bf16 dw (below).
+// Every 128-row stage and every block above is the same for both tile widths.
 #include "epilogue.cuh"
 #include "kernels.h"
 #include "pdl.cuh"
