@@ -7,17 +7,19 @@
 // order; the un-permute sums each token's k expert outputs, weighted by the router. Copies whose
 // expert id lies outside [0, E) are dropped (no sorted row, inv = -1, no contribution).
 //
-// The sort is a counting sort in three passes over chunks of 512 copies (one warp per chunk):
-//   moe_count_kernel  per-chunk histogram of the expert ids (shared-memory counters)
-//   moe_scan_kernel   per-expert exclusive scan over the chunks (chunk bases), totals ->
-//                     group_sizes, exclusive scan over the experts (expert bases)
-//   moe_place_kernel  each chunk again, 32 copies at a time: __match_any_sync groups the lanes of
-//                     one expert, a lane's rank is the number of lower lanes in its group, and
-//                     the group's last lane advances the expert's running position -- the order
-//                     of equal keys is the flat order, as the stable sort defines it.
-// The gather (one warp per token: its row read once, its k copies written) and the combine (one
-// warp per token: its k copies read, one row written) are HBM-bound, in 16-byte vectors with
-// four loads in flight per lane.
+// The sort is a counting sort over chunks of 512 copies, in three launches:
+//   moe_count_kernel   per-chunk histogram of the expert ids (one warp per chunk, shared-memory
+//                      counters)
+//   moe_scan_kernel    per-expert exclusive scan over the chunks (chunk bases; lanes over 32
+//                      experts, warps over slices of the chunks), totals -> group_sizes,
+//                      exclusive scan over the experts (expert bases)
+//   moe_place_gather_kernel  one warp per token: the sorted position of each of its copies is
+//                      the expert's base + the chunk's base for that expert + the number of
+//                      copies of that expert earlier in the chunk (so equal keys keep their flat
+//                      order, as the stable sort defines it), counted over the chunk's ids held
+//                      in registers; then the token's row is read once and its k copies written.
+// The gather and the combine (one warp per token: its k copies read, one row written) are
+// HBM-bound, in 16-byte vectors with four loads in flight per lane.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -52,33 +54,105 @@ __global__ void __launch_bounds__(32) moe_count_kernel(const int32_t* __restrict
     for (int e = lane; e < E; e += 32) chunk_hist[static_cast<long long>(blockIdx.x) * E + e] = cnt[e];
 }
 
+constexpr int SCAN_UNROLL = 16;   // chunk counts a lane keeps in registers (loads in flight)
+constexpr int SCAN_RELOAD = 8;    // chunk loads in flight per lane past those
+
 __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ chunk_hist, int nchunks, int E,
                                                         int32_t* __restrict__ group_sizes,
                                                         int32_t* __restrict__ expert_base, int32_t* __restrict__ valid) {
     grid_dependency_enter();
     __shared__ int32_t tot[1024];
     __shared__ int32_t warp_sum[32];
-    const int e = threadIdx.x;
-    int32_t run = 0;
-    if (e < E) {
-        // coalesced across the experts for each chunk; eight chunks' loads in flight at a time
-        for (int c0 = 0; c0 < nchunks; c0 += 8) {
-            int32_t v[8];
+    __shared__ int32_t slice_sum[32][32];   // [warp][lane]: a slice's count of one expert
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (E <= 32 && nchunks <= 64) {
+        // few experts and chunks: warp e scans expert e, its lanes 32 chunks at a time (one load
+        // each, all in flight), with shuffles; no block-wide step before the totals
+        if (w < E) {
+            int32_t run = 0;
+            for (int c0 = 0; c0 < nchunks; c0 += 32) {
+                const int c = c0 + lane;
+                const int32_t v = c < nchunks ? chunk_hist[static_cast<long long>(c) * E + w] : 0;
+                int32_t x = v;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                v[j] = c0 + j < nchunks ? chunk_hist[static_cast<long long>(c0 + j) * E + e] : 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (c0 + j < nchunks) chunk_hist[static_cast<long long>(c0 + j) * E + e] = run;
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int32_t y = __shfl_up_sync(0xffffffffu, x, d);
+                    if (lane >= d) x += y;
+                }
+                if (c < nchunks) chunk_hist[static_cast<long long>(c) * E + w] = run + x - v;
+                run += __shfl_sync(0xffffffffu, x, 31);
+            }
+            if (lane == 0) {
+                group_sizes[w] = run;
+                tot[w] = run;
+            }
+        }
+    } else {
+        // per expert, the exclusive scan over the chunks in place. Lanes take 32 consecutive experts
+        // (coalesced rows of the histogram); the 32 warps split into one team per 32 experts, and a
+        // team's warps split the chunks into slices: each sums its slice, takes the sums of the slices
+        // before it as its start, then writes the running counts over its slice
+        const int teams = (E + 31) / 32;   // <= 32 (E <= 1024)
+        const int wpt = 32 / teams;        // warps per team
+        const int team = w / wpt, slice = w % wpt;
+        const int ex = team * 32 + lane;   // this lane's expert
+        const bool mine = team < teams && ex < E;
+        const int per = (nchunks + wpt - 1) / wpt;
+        const int cb = slice * per, ce = min(nchunks, cb + per);
+        // the slice's first SCAN_UNROLL counts stay in registers for the second pass
+        int32_t first[SCAN_UNROLL];
+    #pragma unroll
+        for (int j = 0; j < SCAN_UNROLL; ++j)
+            first[j] = (mine && cb + j < ce) ? chunk_hist[static_cast<long long>(cb + j) * E + ex] : 0;
+        int32_t part = 0;
+    #pragma unroll
+        for (int j = 0; j < SCAN_UNROLL; ++j) part += first[j];
+        for (int c0 = cb + SCAN_UNROLL; c0 < ce; c0 += SCAN_RELOAD) {
+            int32_t v[SCAN_RELOAD];
+    #pragma unroll
+            for (int j = 0; j < SCAN_RELOAD; ++j)
+                v[j] = (mine && c0 + j < ce) ? chunk_hist[static_cast<long long>(c0 + j) * E + ex] : 0;
+    #pragma unroll
+            for (int j = 0; j < SCAN_RELOAD; ++j) part += v[j];
+        }
+        slice_sum[w][lane] = part;
+        __syncthreads();
+        int32_t run = 0, all = 0;
+        if (team < teams) {
+    #pragma unroll
+            for (int sl = 0; sl < 32; ++sl) {
+                if (sl < wpt) {
+                    const int32_t ps = slice_sum[team * wpt + sl][lane];
+                    all += ps;
+                    run += sl < slice ? ps : 0;
+                }
+            }
+        }
+        if (mine && slice == 0) {
+            group_sizes[ex] = all;
+            tot[ex] = all;
+        }
+    #pragma unroll
+        for (int j = 0; j < SCAN_UNROLL; ++j) {
+            if (mine && cb + j < ce) chunk_hist[static_cast<long long>(cb + j) * E + ex] = run;
+            run += first[j];
+        }
+        for (int c0 = cb + SCAN_UNROLL; c0 < ce; c0 += SCAN_RELOAD) {
+            int32_t v[SCAN_RELOAD];
+    #pragma unroll
+            for (int j = 0; j < SCAN_RELOAD; ++j)
+                v[j] = (mine && c0 + j < ce) ? chunk_hist[static_cast<long long>(c0 + j) * E + ex] : 0;
+    #pragma unroll
+            for (int j = 0; j < SCAN_RELOAD; ++j) {
+                if (mine && c0 + j < ce) chunk_hist[static_cast<long long>(c0 + j) * E + ex] = run;
                 run += v[j];
             }
         }
-        group_sizes[e] = run;
     }
-    tot[e] = e < E ? run : 0;
+    for (int e = E + threadIdx.x; e < 1024; e += blockDim.x) tot[e] = 0;
     __syncthreads();
     // exclusive scan of the totals over the experts (warp scans, then over the warps)
-    const int lane = e & 31, w = e >> 5;
+    const int e = threadIdx.x;
     int32_t x = tot[e];
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -102,75 +176,93 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(int32_t* __restrict__ ch
     if (e == 1023) *valid = incl;
 }
 
-__global__ void __launch_bounds__(32) moe_place_kernel(const int32_t* __restrict__ ids, long long total, int E,
-                                                       const int32_t* __restrict__ chunk_base,
-                                                       const int32_t* __restrict__ expert_base,
-                                                       int32_t* __restrict__ order, int32_t* __restrict__ inv) {
-    grid_dependency_enter();
-    extern __shared__ int32_t pos[];
-    const int lane = threadIdx.x;
-    for (int e = lane; e < E; e += 32)
-        pos[e] = expert_base[e] + chunk_base[static_cast<long long>(blockIdx.x) * E + e];
-    __syncwarp();
-    const long long base = static_cast<long long>(blockIdx.x) * CHUNK;
-    const uint32_t lower = (1u << lane) - 1u;
-    int id[CHUNK / 32];   // all loads of the chunk in flight before the ordered placement
+// Sorted rows of the nj (<= 32) consecutive copies fb .. fb+nj-1, lane j receiving copy fb + j's
+// (-1 for a dropped copy, expert outside [0, E)). A kept copy f of expert e goes to row
+// expert_base[e] + chunk_base[c][e] + the number of copies of e in chunk c = f / CHUNK before f.
+// Lane j loads copy j's expert and its two bases, all copies' loads in flight together; the ids
+// of fb's chunk up to the last of these copies are held in registers (16 a lane), so each copy's
+// count is a register compare and one warp reduction. A copy in a later chunk (k not dividing the
+// chunk) counts over that chunk's ids from memory.
+__device__ __forceinline__ int32_t place_copies(const int32_t* __restrict__ ids,
+                                                const int32_t* __restrict__ chunk_base,
+                                                const int32_t* __restrict__ expert_base, int E, long long fb, int nj,
+                                                int lane) {
+    const long long c0 = fb / CHUNK;
+    const long long fend = min(fb + nj, (c0 + 1) * CHUNK);
+    const int e_l = lane < nj ? __ldg(ids + fb + lane) : -1;   // copy `lane`'s expert
+    int idr[CHUNK / 32];   // ids of chunk c0 before fend, -1 past it
 #pragma unroll
     for (int i = 0; i < CHUNK / 32; ++i) {
-        const long long f = base + i * 32 + lane;
-        id[i] = f < total ? __ldg(ids + f) : -1;
+        const long long g = c0 * CHUNK + 32 * i + lane;
+        idr[i] = g < fend ? __ldg(ids + g) : -1;
     }
+    int32_t base_l = 0;
+    if (e_l >= 0 && e_l < E) base_l = __ldg(expert_base + e_l) + __ldg(chunk_base + ((fb + lane) / CHUNK) * E + e_l);
+    int32_t my_p = -1;
+    for (int j = 0; j < nj; ++j) {
+        const int e = __shfl_sync(0xffffffffu, e_l, j);   // the same for every lane
+        if (e < 0 || e >= E) continue;
+        const long long f = fb + j;
+        const long long c = f / CHUNK;
+        int cnt = 0;
+        if (c == c0) {
+            const int before = static_cast<int>(f - c0 * CHUNK);   // chunk positions before f
 #pragma unroll
-    for (int i = 0; i < CHUNK / 32; ++i) {
-        const long long f = base + i * 32 + lane;
-        const bool in = f < total;
-        int e = id[i];
-        const bool valid = in && e >= 0 && e < E;
-        if (!valid) e = -1 - (in ? 0 : 1);   // -1: dropped copy, -2: past the end (both unmatched to experts)
-        const uint32_t same = __match_any_sync(0xffffffffu, e);
-        if (valid) {
-            const int32_t p = pos[e] + __popc(same & lower);
-            order[p] = static_cast<int32_t>(f);
-            inv[f] = p;
-        } else if (in) {
-            inv[f] = -1;
+            for (int i = 0; i < CHUNK / 32; ++i) cnt += (idr[i] == e && 32 * i + lane < before) ? 1 : 0;
+        } else {
+            for (long long g = c * CHUNK + lane; g < f; g += 32) cnt += __ldg(ids + g) == e ? 1 : 0;
         }
-        __syncwarp();
-        // the group's last lane moves the expert's running position past this step's copies
-        if (valid && (same >> lane) == 1u) pos[e] += __popc(same);
-        __syncwarp();
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        if (lane == j) my_p = base_l + cnt;
     }
+    return my_p;
 }
 
-// x_sorted[inv[t*k + j]] = x[t] for every kept copy: one warp per token reads its row once and
-// writes its k copies (a gather by sorted row would read each token row k times). Then the rows
-// past the kept copies (dropped ids) are zeroed and their order entries set to -1.
-__global__ void __launch_bounds__(256) moe_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv,
-                                                         int32_t* __restrict__ order, const int32_t* __restrict__ valid,
-                                                         long long tokens, int k, int vec_per_row,
-                                                         uint4* __restrict__ x_sorted) {
+// One warp per token t: places its copies f = t*k + j (inv[f], order[p]) 32 at a time and writes
+// its row, read once per 32 copies, to each kept copy's sorted row. Then the rows past the kept
+// copies (dropped ids) are zeroed and their order entries set to -1.
+__global__ void __launch_bounds__(256, 4) moe_place_gather_kernel(
+    const int32_t* __restrict__ ids, const uint4* __restrict__ x, const int32_t* __restrict__ chunk_base,
+    const int32_t* __restrict__ expert_base, const int32_t* __restrict__ valid, long long tokens, int k, int E,
+    int vec_per_row, int32_t* __restrict__ order, int32_t* __restrict__ inv, uint4* __restrict__ x_sorted) {
     grid_dependency_enter();
+    __shared__ int32_t copy_rows[256 / 32][32];   // per warp: the sorted rows of its current copies
     const int lane = threadIdx.x & 31;
+    int32_t* rows = copy_rows[threadIdx.x >> 5];
     const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    const long long total = tokens * k;
     for (long long t = warp; t < tokens; t += nwarps) {
-        const uint4* src = x + t * vec_per_row;
-        for (int i0 = lane; i0 < vec_per_row; i0 += 32 * VEC_UNROLL) {
-            uint4 v[VEC_UNROLL];
-#pragma unroll
-            for (int u = 0; u < VEC_UNROLL; ++u)
-                if (i0 + 32 * u < vec_per_row) v[u] = __ldg(src + i0 + 32 * u);
-            for (int j = 0; j < k; ++j) {
-                const int32_t p = __ldg(inv + t * k + j);
-                if (p < 0) continue;
-                uint4* dst = x_sorted + static_cast<long long>(p) * vec_per_row + i0;
+        for (int j0 = 0; j0 < k; j0 += 32) {
+            const int nj = min(32, k - j0);
+            const long long fb = t * k + j0;
+            const int32_t my_p = place_copies(ids, chunk_base, expert_base, E, fb, nj, lane);
+            if (lane < nj) {
+                inv[fb + lane] = my_p;
+                if (my_p >= 0) order[my_p] = static_cast<int32_t>(fb + lane);
+                rows[lane] = my_p;
+            }
+            __syncwarp();
+            // lanes leave this loop at different counts when a row is not a multiple of 32
+            // vectors, so it reads the rows from shared memory (no warp-wide exchange inside)
+            const uint4* src = x + t * vec_per_row;
+            for (int i0 = lane; i0 < vec_per_row; i0 += 32 * VEC_UNROLL) {
+                uint4 v[VEC_UNROLL];
 #pragma unroll
                 for (int u = 0; u < VEC_UNROLL; ++u)
-                    if (i0 + 32 * u < vec_per_row) dst[32 * u] = v[u];
+                    if (i0 + 32 * u < vec_per_row) v[u] = __ldg(src + i0 + 32 * u);
+                for (int j = 0; j < nj; ++j) {
+                    const int32_t p = rows[j];
+                    if (p < 0) continue;
+                    uint4* dst = x_sorted + static_cast<long long>(p) * vec_per_row + i0;
+#pragma unroll
+                    for (int u = 0; u < VEC_UNROLL; ++u)
+                        if (i0 + 32 * u < vec_per_row) dst[32 * u] = v[u];
+                }
             }
+            __syncwarp();   // every lane has read the rows before the next copies overwrite them
         }
     }
-    const long long total = tokens * k;
     const int32_t v = *valid;
     for (long long p = v + warp; p < total; p += nwarps) {
         uint4* dst = x_sorted + p * vec_per_row;
@@ -366,13 +458,13 @@ cudaError_t launch_moe_permute(const int32_t* ids, long long tokens, int k, int 
     e = launch_pdl(moe_scan_kernel, dim3(1), dim3(1024), 0, stream, chunk_hist, static_cast<int>(nchunks), E, group_sizes,
                    expert_base, valid);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(moe_place_kernel, chunks, dim3(32), cnt_shm, stream, ids, total, E, chunk_hist, expert_base, order, inv);
-    if (e != cudaSuccess) return e;
     const int vec = static_cast<int>(row_bytes / 16);
     const long long want = (tokens + 7) / 8;
     const int grid = static_cast<int>(want < 8LL * sm_count ? want : 8LL * sm_count);
-    return launch_pdl(moe_gather_kernel, dim3(grid), dim3(256), 0, stream, static_cast<const uint4*>(x), inv, order, valid,
-                      tokens, k, vec, static_cast<uint4*>(x_sorted));
+    return launch_pdl(moe_place_gather_kernel, dim3(grid), dim3(256), 0, stream, ids, static_cast<const uint4*>(x),
+                      static_cast<const int32_t*>(chunk_hist), static_cast<const int32_t*>(expert_base),
+                      static_cast<const int32_t*>(valid), tokens, k, E, vec, order, inv,
+                      static_cast<uint4*>(x_sorted));
 }
 
 cudaError_t launch_moe_combine(const void* y_sorted, const int32_t* inv, const float* weights, long long tokens, int k,

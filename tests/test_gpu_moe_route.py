@@ -46,6 +46,11 @@ def routed_ids(t, k, e, seed, drop=0.0):
     (301, 2, 8, 1600, 0.0),         # 200 vectors a row: the last of four in-flight loads ragged
     (40000, 4, 64, 16, 0.02),       # 313 chunks of 512 copies, the last one partial
     (33000, 8, 1024, 24, 0.05),     # 516 chunks with the largest expert count
+    (20000, 2, 8, 16, 0.01),        # few experts over 79 chunks: the sliced scan
+    (2000, 3, 8, 64, 0.05),         # k = 3: tokens whose copies straddle two chunks
+    (700, 5, 64, 32, 0.1),          # k = 5, straddling, dropped copies
+    (300, 33, 64, 16, 0.05),        # k > 32: a token's copies placed in two batches
+    (50, 600, 1024, 16, 0.05),      # k > 512: one token's copies span two or three chunks
 ])
 def test_permute_matches_oracle_bit_for_bit(t, k, e, width, drop):
     ids = routed_ids(t, k, e, 61 + t, drop)
@@ -60,6 +65,26 @@ def test_permute_matches_oracle_bit_for_bit(t, k, e, width, drop):
     assert np.array_equal(inv.cpu().numpy().astype(np.int64), inv_ref)
     xs_h = xs.cpu()
     assert torch.equal(xs_h[:v], x[torch.from_numpy(order_ref // k)])           # exact bytes
+    assert torch.all(xs_h[v:] == 0)
+
+
+@pytest.mark.parametrize("t,k,e", [(1000, 3, 4), (200, 40, 5), (20, 700, 3), (4096, 2, 2)])
+def test_permute_arbitrary_ids_with_repeats(t, k, e):
+    """Ids drawn independently, so a token may pick one expert several times (its copies keep their
+    flat order among the expert's rows) and some lie outside [0, E)."""
+    rng = np.random.default_rng(71 + k)
+    ids = rng.integers(-1, e + 1, size=(t, k)).astype(np.int32)
+    x = torch.from_numpy(ri.host_normal((t, 16), 72)).to(torch.bfloat16)
+    xs, gs, order, inv = gg.moe_permute(torch.from_numpy(ids).to(DEV), x.to(DEV), e)
+    torch.cuda.synchronize()
+    gs_ref, order_ref, inv_ref, _ = oracle.moe_permute(ids, x.double().numpy(), e)
+    v = order_ref.size
+    assert np.array_equal(gs.cpu().numpy(), gs_ref)
+    assert np.array_equal(order.cpu().numpy()[:v].astype(np.int64), order_ref)
+    assert np.all(order.cpu().numpy()[v:] == -1)
+    assert np.array_equal(inv.cpu().numpy().astype(np.int64), inv_ref)
+    xs_h = xs.cpu()
+    assert torch.equal(xs_h[:v], x[torch.from_numpy(order_ref // k)])
     assert torch.all(xs_h[v:] == 0)
 
 
