@@ -10,9 +10,10 @@
 // The sort is a counting sort over chunks of 512 copies, in three launches:
 //   moe_count_kernel   per-chunk histogram of the expert ids (one warp per chunk, shared-memory
 //                      counters)
-//   moe_scan_kernel    per-expert exclusive scan over the chunks (chunk bases; lanes over 32
-//                      experts, warps over slices of the chunks), totals -> group_sizes,
-//                      exclusive scan over the experts (expert bases)
+//   moe_scan_kernel    per-expert exclusive scan over the chunks (chunk bases: for at most 32
+//                      experts and 64 chunks warp e scans expert e with its lanes over the
+//                      chunks; else lanes over 32 experts, warps over slices of the chunks),
+//                      totals -> group_sizes, exclusive scan over the experts (expert bases)
 //   moe_place_gather_kernel  one warp per token: the sorted position of each of its copies is
 //                      the expert's base + the chunk's base for that expert + the number of
 //                      copies of that expert earlier in the chunk (so equal keys keep their flat
